@@ -1,0 +1,681 @@
+/*
+ * oracle.c -- fp64 CPU oracle for batched speculative-decoding verification
+ * and Saguaro pre-speculation.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the plain, slow reference that the
+ * CUDA path is checked against.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg load it.  It shares no code, header, table or
+ * helper with the CUDA library, and it includes nothing from it.
+ *
+ * Sources (pages, by title and section):
+ *   [SD]  "投机解码 (Speculative Decoding): 小模型猜、大模型验" -- blog.
+ *         §3 "拒绝采样验证" (rejection-sampling verification): the per-position
+ *         accept test, the residual (q-p)+ / sum (q-p)+, the inverse-CDF
+ *         `choice`, the bonus token; §4: E[N] = (1-a^(g+1))/(1-a).
+ *   [SAG] "Speculative Speculative Decoding (Saguaro)" -- notes.
+ *         §3.1 (bonus prediction by top-k), §3.2 (Saguaro sampling
+ *         p_saguaro ~ sqrt(p_D * p_residual), residual clamped at 1e-8,
+ *         renormalised by its sum).
+ *   [SSD] "Speculative speculative decoding as async inference" -- blog,
+ *         "rollback": everything after the first rejected position is dropped.
+ *
+ * Notation follows [SD]: q = target distribution, p = draft distribution.
+ * All arithmetic is IEEE fp64.  Inputs (bf16 or fp32 logits) are widened
+ * exactly to fp64 before use.
+ *
+ * Readings taken where the pages are silent or garbled (each also listed in
+ * the design notes):
+ *   - bonus row: the target row after the last draft token (row g), not the
+ *     row the [SD] toy driver passes by mistake (row g-1);
+ *   - temperature: softmax(x / T) on both sides; T == 0 means greedy
+ *     (accept iff the draft token is the target argmax, lowest index wins);
+ *   - p(x) == 0 (draft logit -inf): accept (ratio +inf);
+ *   - residual mass S <= 0 on a rejection: sample from q instead;
+ *   - inverse CDF compares u*S < C_k on unnormalised weights; if rounding
+ *     leaves no such k, the last index with positive weight is returned;
+ *   - uniforms: Philox4x32-10 keyed by the seed, counter (request, position,
+ *     draw/4, 0), word draw%4, u = (w >> 8) * 2^-24;
+ *     draw 0 = accept test, 1 = resample / bonus, 2 = Saguaro sample;
+ *   - Saguaro at j == g (no draft row): r = q_g and p_D = q_g.
+ *
+ * Flags: a draw whose uniform lies within 1e-6 of the threshold it is compared
+ * with (accept threshold, or either CDF boundary of the chosen token) is
+ * flagged; comparisons with another implementation stop at the first flagged
+ * draw of a request.
+ *
+ * ORC_MUTANT (compile-time, default 0) plants one known mistake; the test
+ * suite builds each mutant and checks that some pin fails.  It is never set in
+ * the normal build.
+ */
+
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifndef ORC_MUTANT
+#define ORC_MUTANT 0
+#endif
+
+enum { ORC_BF16 = 0, ORC_F32 = 1 };
+
+#define ORC_FLAG_BAND 1e-6     /* uniform-to-boundary distance that flags a draw */
+#define ORC_SAGUARO_CLAMP 1e-8 /* [SAG] §3.2: residual clamped below at 1e-8     */
+#define ORC_TOPK_REL 1e-5      /* top-k slot ambiguity: relative gap              */
+#define ORC_TOPK_ABS 1e-6      /* top-k slot ambiguity: absolute gap              */
+
+#define ORC_NSTAT_VERIFY 8
+#define ORC_NSTAT_SAGUARO 8
+
+/* ------------------------------------------------------------------------- */
+/* Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as    */
+/* easy as 1, 2, 3", SC'11): 10 rounds of                                     */
+/*   (hi0,lo0) = M0*c0, (hi1,lo1) = M1*c2,                                     */
+/*   c' = (hi1^c1^k0, lo1, hi0^c3^k1, lo0),  then k += (W0, W1).              */
+/* ------------------------------------------------------------------------- */
+
+#define PHILOX_M0 0xD2511F53u
+#define PHILOX_M1 0xCD9E8D57u
+#define PHILOX_W0 0x9E3779B9u
+#define PHILOX_W1 0xBB67AE85u
+
+#if ORC_MUTANT == 8
+#define PHILOX_ROUNDS 9
+#else
+#define PHILOX_ROUNDS 10
+#endif
+
+void orc_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+  uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+  uint32_t k0 = key[0], k1 = key[1];
+  for (int round = 0; round < PHILOX_ROUNDS; ++round) {
+    uint64_t prod0 = (uint64_t)PHILOX_M0 * (uint64_t)c0;
+    uint64_t prod1 = (uint64_t)PHILOX_M1 * (uint64_t)c2;
+    uint32_t hi0 = (uint32_t)(prod0 >> 32), lo0 = (uint32_t)prod0;
+    uint32_t hi1 = (uint32_t)(prod1 >> 32), lo1 = (uint32_t)prod1;
+    uint32_t n0 = hi1 ^ c1 ^ k0;
+    uint32_t n2 = hi0 ^ c3 ^ k1;
+    c0 = n0;
+    c1 = lo1;
+    c2 = n2;
+    c3 = lo0;
+    k0 += PHILOX_W0;
+    k1 += PHILOX_W1;
+  }
+  out[0] = c0;
+  out[1] = c1;
+  out[2] = c2;
+  out[3] = c3;
+}
+
+/* The uniform for (request b, position i, draw d): u in [0, 1 - 2^-24], a
+ * multiple of 2^-24, so it is exact in fp32 and fp64. */
+double orc_uniform(uint64_t seed, uint32_t b, uint32_t i, uint32_t d) {
+  uint32_t key[2] = {(uint32_t)(seed & 0xffffffffu), (uint32_t)(seed >> 32)};
+  uint32_t ctr[4] = {b, i, d >> 2, 0u};
+  uint32_t out[4];
+  orc_philox4x32_10(ctr, key, out);
+  uint32_t w = out[d & 3u];
+  return (double)(w >> 8) * (1.0 / 16777216.0);
+}
+
+/* out[b * W + i] = the uniform for (b, i, d), b < B, i < W. */
+void orc_uniform_grid(uint64_t seed, int B, int W, uint32_t d, double* out) {
+  for (int b = 0; b < B; ++b)
+    for (int i = 0; i < W; ++i) out[(size_t)b * W + i] = orc_uniform(seed, (uint32_t)b, (uint32_t)i, d);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Row helpers                                                                */
+/* ------------------------------------------------------------------------- */
+
+static double bf16_bits_to_double(uint16_t h) {
+  uint32_t bits = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &bits, sizeof f);
+  return (double)f;
+}
+
+/* Widen row `row` (V elements) of a bf16 / fp32 logit array to fp64. */
+void orc_row_to_f64(const void* base, int dtype, size_t row, int V, double* x) {
+  if (dtype == ORC_BF16) {
+    const uint16_t* r = (const uint16_t*)base + row * (size_t)V;
+    for (int v = 0; v < V; ++v) x[v] = bf16_bits_to_double(r[v]);
+  } else {
+    const float* r = (const float*)base + row * (size_t)V;
+    for (int v = 0; v < V; ++v) x[v] = (double)r[v];
+  }
+}
+
+/* Softmax at temperature T > 0 ([SD] §3 verifies distributions q and p; the
+ * sampling parameters must match on both sides, [SD] §5):
+ *   prob[v] = exp((x_v - m) / T) / sum_w exp((x_w - m) / T),  m = max x.
+ * Reports m (raw logit scale) and logsum = ln sum_w exp((x_w - m) / T). */
+void orc_softmax(const double* x, int V, double T, double* prob, double* out_max,
+                 double* out_logsum) {
+  double m = -INFINITY;
+  for (int v = 0; v < V; ++v)
+    if (x[v] > m) m = x[v];
+#if ORC_MUTANT == 5
+  T = 1.0; /* mutant: temperature ignored */
+#endif
+  double sum = 0.0;
+  for (int v = 0; v < V; ++v) {
+    prob[v] = exp((x[v] - m) / T);
+    sum += prob[v];
+  }
+  for (int v = 0; v < V; ++v) prob[v] /= sum;
+  if (out_max) *out_max = m;
+  if (out_logsum) *out_logsum = log(sum);
+}
+
+/* Greedy target choice: the largest logit, lowest index among equals. */
+int orc_argmax(const double* x, int V) {
+  int best = 0;
+  for (int v = 1; v < V; ++v) {
+#if ORC_MUTANT == 10
+    if (x[v] >= x[best]) best = v; /* mutant: highest index wins ties */
+#else
+    if (x[v] > x[best]) best = v;
+#endif
+  }
+  return best;
+}
+
+/* Inverse-CDF draw ([SD] §3, `choice`): the smallest k with
+ * u * S < C_k = sum_{v<=k} w_v, where S = sum_v w_v.  If rounding leaves no
+ * such k, the last index with positive weight.  *dist gets the distance from u
+ * to the nearer of the chosen token's normalised CDF boundaries C_{k-1}/S and
+ * C_k/S. */
+int orc_choice(const double* w, int V, double u, double* dist) {
+  double S = 0.0;
+  for (int v = 0; v < V; ++v) S += w[v];
+  double target = u * S;
+  double acc = 0.0;
+  int chosen = -1;
+  double lo = 0.0, hi = 0.0;
+  for (int v = 0; v < V; ++v) {
+    double before = acc;
+    acc += w[v];
+    if (target < acc) {
+      chosen = v;
+      lo = before;
+      hi = acc;
+      break;
+    }
+  }
+  if (chosen < 0) { /* rounding fallback */
+    double before = 0.0, running = 0.0;
+    for (int v = 0; v < V; ++v) {
+      double prev = running;
+      running += w[v];
+      if (w[v] > 0.0) {
+        chosen = v;
+        before = prev;
+        hi = running;
+      }
+    }
+    lo = before;
+    if (chosen < 0) chosen = V - 1;
+  }
+#if ORC_MUTANT == 4
+  if (chosen > 0) chosen -= 1; /* mutant: off by one */
+#endif
+  if (dist) {
+    double a = fabs(u - lo / S), b = fabs(u - hi / S);
+    *dist = a < b ? a : b;
+  }
+  return chosen;
+}
+
+/* Top-k ([SAG] §3.1): the k largest entries, in descending order, lowest index
+ * among equals.  Plain repeated selection.  val[t] = w[idx[t]]. */
+void orc_topk(const double* w, int V, int k, int32_t* idx, double* val) {
+  for (int t = 0; t < k; ++t) {
+    int best = -1;
+    for (int v = 0; v < V; ++v) {
+      int taken = 0;
+      for (int s = 0; s < t; ++s)
+        if (idx[s] == v) taken = 1;
+      if (taken) continue;
+#if ORC_MUTANT == 7
+      if (best < 0 || w[v] >= w[best]) best = v; /* mutant: ties to higher index */
+#else
+      if (best < 0 || w[v] > w[best]) best = v;
+#endif
+    }
+    idx[t] = best;
+    val[t] = best >= 0 ? w[best] : 0.0;
+  }
+}
+
+/* ------------------------------------------------------------------------- */
+/* Verification of one request ([SD] §3 `spec_verify`, with the readings     */
+/* listed at the top of this file).                                           */
+/*                                                                            */
+/*   xt: (g+1) x V target logits, row i = target distribution for position i  */
+/*       (row g is the position after the last draft token);                  */
+/*   xd: g x V draft logits; tok: g draft tokens;                             */
+/*   u_acc[i], u_res[i]: the accept and resample/bonus uniforms of position i.*/
+/*                                                                            */
+/* Output: out[0..g] (accepted draft tokens, then the correction or bonus     */
+/* token at index n, then -1), return value n = number of accepted tokens.   */
+/* flag_pos / flag_kind: position of the first flagged draw (-1 if none),    */
+/* kind 0 = accept draw, 1 = resample/bonus draw.                            */
+/* stats (nullable, (g+1) x 8): t_max, t_logsum, d_max, d_logsum, q(x), p(x),*/
+/* residual mass S, accept probability a; NaN where it does not apply.        */
+/* Returns -1 when a token lies outside [0, V) (outputs all -1).              */
+/* ------------------------------------------------------------------------- */
+
+static void fill_nan(double* s, int n) {
+  for (int t = 0; t < n; ++t) s[t] = NAN;
+}
+
+/* The quantities of draft position i: q = softmax(target row i), p =
+ * softmax(draft row i), the accept probability a = min(1, q(x)/p(x)) of the
+ * draft token x, and the residual r = (q - p)+ with its mass S. */
+typedef struct {
+  double mt, lst, md, lsd; /* row maxima and log-sums of target and draft */
+  double qx, px, a, S;
+} orc_position;
+
+static orc_position position_quantities(int V, const double* ti, const double* di, double T, int x,
+                                        double* q, double* p, double* r) {
+  orc_position P;
+  orc_softmax(ti, V, T, q, &P.mt, &P.lst);
+  orc_softmax(di, V, T, p, &P.md, &P.lsd);
+  P.qx = q[x];
+  P.px = p[x];
+  /* a = min(1, q(x) / p(x)).  The ratio is evaluated as exp(log q(x) -
+   * log p(x)) so that a p(x) too small for fp64 is not mistaken for zero; p(x)
+   * is zero only for a -inf draft logit, and then the token is accepted. */
+  if (di[x] == -INFINITY) {
+    P.a = 1.0;
+  } else {
+    double log_q = (ti[x] - P.mt) / T - P.lst;
+    double log_p = (di[x] - P.md) / T - P.lsd;
+#if ORC_MUTANT == 3
+    double ratio = exp(log_p - log_q); /* mutant: ratio inverted */
+#else
+    double ratio = exp(log_q - log_p);
+#endif
+    P.a = ratio < 1.0 ? ratio : 1.0;
+  }
+  P.S = 0.0;
+  for (int v = 0; v < V; ++v) {
+#if ORC_MUTANT == 2
+    double d = p[v] - q[v]; /* mutant: residual sign flipped */
+#else
+    double d = q[v] - p[v];
+#endif
+    r[v] = d > 0.0 ? d : 0.0;
+    P.S += r[v];
+  }
+  return P;
+}
+
+int orc_verify_request(int g, int V, const double* xt, const double* xd, double T,
+                       const int32_t* tok, const double* u_acc, const double* u_res,
+                       int32_t* out, int32_t* flag_pos, int32_t* flag_kind, double* stats) {
+  for (int i = 0; i <= g; ++i) out[i] = -1;
+  *flag_pos = -1;
+  *flag_kind = -1;
+  if (stats) fill_nan(stats, (g + 1) * ORC_NSTAT_VERIFY);
+  for (int i = 0; i < g; ++i)
+    if (tok[i] < 0 || tok[i] >= V) return -1;
+
+  if (T == 0.0) {
+    /* Greedy: accept while the draft token equals the target argmax; the
+     * correction (or bonus) is the target argmax at the stopping position. */
+    if (stats)
+      for (int i = 0; i <= g; ++i) {
+        const double* ti = xt + (size_t)i * V;
+        stats[i * ORC_NSTAT_VERIFY + 0] = ti[orc_argmax(ti, V)];
+      }
+    int n = g;
+    for (int i = 0; i < g; ++i) {
+      int gi = orc_argmax(xt + (size_t)i * V, V);
+      if (tok[i] == gi) {
+        out[i] = tok[i];
+      } else {
+        out[i] = gi;
+        n = i;
+        break;
+      }
+    }
+    if (n == g) out[g] = orc_argmax(xt + (size_t)g * V, V);
+    return n;
+  }
+
+  double* q = (double*)malloc(sizeof(double) * (size_t)V);
+  double* p = (double*)malloc(sizeof(double) * (size_t)V);
+  double* r = (double*)malloc(sizeof(double) * (size_t)V);
+
+  if (stats) { /* every position's quantities, whether or not it is reached */
+    for (int i = 0; i < g; ++i) {
+      orc_position P = position_quantities(V, xt + (size_t)i * V, xd + (size_t)i * V, T, tok[i], q, p, r);
+      double* s = stats + i * ORC_NSTAT_VERIFY;
+      s[0] = P.mt;
+      s[1] = P.lst;
+      s[2] = P.md;
+      s[3] = P.lsd;
+      s[4] = P.qx;
+      s[5] = P.px;
+      s[6] = P.S;
+      s[7] = P.a;
+    }
+    double mt, lst;
+    orc_softmax(xt + (size_t)g * V, V, T, q, &mt, &lst);
+    stats[g * ORC_NSTAT_VERIFY + 0] = mt;
+    stats[g * ORC_NSTAT_VERIFY + 1] = lst;
+  }
+
+  int n = g;
+  for (int i = 0; i < g; ++i) {
+    orc_position P = position_quantities(V, xt + (size_t)i * V, xd + (size_t)i * V, T, tok[i], q, p, r);
+    double u = u_acc[i];
+    if (*flag_pos < 0 && fabs(u - P.a) < ORC_FLAG_BAND) {
+      *flag_pos = i;
+      *flag_kind = 0;
+    }
+    if (u < P.a) {
+      out[i] = tok[i]; /* accepted */
+      continue;
+    }
+    /* Rejected at i: one token from the residual, then stop ([SSD] rollback). */
+    if (!(P.S > 0.0))
+      for (int v = 0; v < V; ++v) r[v] = q[v];
+    double dist;
+    out[i] = orc_choice(r, V, u_res[i], &dist);
+    if (*flag_pos < 0 && (dist < ORC_FLAG_BAND || P.S < ORC_FLAG_BAND)) {
+      *flag_pos = i;
+      *flag_kind = 1;
+    }
+    n = i;
+    break;
+  }
+  if (n == g) {
+    /* Every draft token accepted: the bonus token from the target row g. */
+#if ORC_MUTANT == 1
+    int row = g > 0 ? g - 1 : 0; /* mutant: the toy driver's off-by-one row */
+#else
+    int row = g;
+#endif
+    orc_softmax(xt + (size_t)row * V, V, T, q, NULL, NULL);
+    double dist;
+    out[g] = orc_choice(q, V, u_res[g], &dist);
+    if (*flag_pos < 0 && dist < ORC_FLAG_BAND) {
+      *flag_pos = g;
+      *flag_kind = 1;
+    }
+  }
+  free(q);
+  free(p);
+  free(r);
+  return n;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Saguaro pre-speculation for one request ([SAG] §3.1, §3.2, with the        */
+/* residual of [SD] §3).  For each acceptance length j = 0..g:                */
+/*   r_j = (q_j - p_j)+ / S_j   (j < g; r_j = q_j when S_j <= 0),              */
+/*   r_g = q_g, p_D = p_j (j < g) or q_g (j == g);                             */
+/*   topk_j = the k largest entries of r_j;                                    */
+/*   s_j(v) = sqrt(p_D(v) * max(r_j(v), 1e-8)),  p_saguaro = s_j / sum s_j;    */
+/*   token_j = inverse-CDF draw from p_saguaro with u_sag[j].                  */
+/* topk_flag[j]: bit t set when slot t is within the top-k ambiguity gap of a */
+/* neighbouring value; tok_flag[j]: 1 when the draw is within 1e-6 of a CDF   */
+/* boundary.  stats ((g+1) x 8): t_logsum, d_logsum, S, Zs = sum s,           */
+/* p_saguaro(token), r(top slot 0), r(top slot k-1), r(first excluded).       */
+/* ------------------------------------------------------------------------- */
+
+static int topk_close(double a, double b) {
+  double d = fabs(a - b);
+  double m = a > b ? a : b;
+  return d <= ORC_TOPK_REL * m || d <= ORC_TOPK_ABS;
+}
+
+int orc_saguaro_request(int g, int V, const double* xt, const double* xd, double T, int k,
+                        const double* u_sag, int32_t* topk, int32_t* tokens,
+                        int32_t* topk_flag, int32_t* tok_flag, double* stats) {
+  if (stats) fill_nan(stats, (g + 1) * ORC_NSTAT_SAGUARO);
+  double* q = (double*)malloc(sizeof(double) * (size_t)V);
+  double* p = (double*)malloc(sizeof(double) * (size_t)V);
+  double* r = (double*)malloc(sizeof(double) * (size_t)V);
+  double* s = (double*)malloc(sizeof(double) * (size_t)V);
+  int32_t* idx = (int32_t*)malloc(sizeof(int32_t) * (size_t)(k + 1));
+  double* val = (double*)malloc(sizeof(double) * (size_t)(k + 1));
+  for (int j = 0; j <= g; ++j) {
+    double mt, lst, md = NAN, lsd = NAN, S = 1.0;
+    orc_softmax(xt + (size_t)j * V, V, T, q, &mt, &lst);
+    const double* pD;
+    if (j < g) {
+      orc_softmax(xd + (size_t)j * V, V, T, p, &md, &lsd);
+      S = 0.0;
+      for (int v = 0; v < V; ++v) {
+        double d = q[v] - p[v];
+        r[v] = d > 0.0 ? d : 0.0;
+        S += r[v];
+      }
+      if (S > 0.0) {
+        for (int v = 0; v < V; ++v) r[v] /= S;
+      } else {
+        for (int v = 0; v < V; ++v) r[v] = q[v];
+      }
+      pD = p;
+    } else {
+      for (int v = 0; v < V; ++v) r[v] = q[v];
+      pD = q;
+    }
+    /* Bonus prediction: top-k of the residual (one more, to judge ambiguity). */
+    int kk = k + 1 <= V ? k + 1 : V;
+    orc_topk(r, V, kk, idx, val);
+    int flags = 0;
+    for (int t = 0; t < k; ++t) {
+      topk[j * k + t] = idx[t];
+      if (t + 1 < kk && topk_close(val[t], val[t + 1])) flags |= 1 << t;
+      if (t > 0 && topk_close(val[t - 1], val[t])) flags |= 1 << t;
+    }
+    topk_flag[j] = flags;
+    /* Saguaro sampling distribution (geometric mean of p_D and residual). */
+    double Zs = 0.0;
+    for (int v = 0; v < V; ++v) {
+#if ORC_MUTANT == 6
+      double pd = pD[v] > ORC_SAGUARO_CLAMP ? pD[v] : ORC_SAGUARO_CLAMP; /* mutant */
+      s[v] = sqrt(pd * r[v]);
+#elif ORC_MUTANT == 9
+      s[v] = pD[v] * (r[v] > ORC_SAGUARO_CLAMP ? r[v] : ORC_SAGUARO_CLAMP); /* mutant */
+#else
+      double rc = r[v] > ORC_SAGUARO_CLAMP ? r[v] : ORC_SAGUARO_CLAMP;
+      s[v] = sqrt(pD[v] * rc);
+#endif
+      Zs += s[v];
+    }
+    double dist;
+    tokens[j] = orc_choice(s, V, u_sag[j], &dist);
+    tok_flag[j] = dist < ORC_FLAG_BAND ? 1 : 0;
+    if (stats) {
+      double* st = stats + j * ORC_NSTAT_SAGUARO;
+      st[0] = lst;
+      st[1] = lsd;
+      st[2] = S;
+      st[3] = Zs;
+      st[4] = s[tokens[j]] / Zs;
+      st[5] = val[0];
+      st[6] = val[k - 1];
+      st[7] = kk > k ? val[k] : NAN;
+    }
+  }
+  free(q);
+  free(p);
+  free(r);
+  free(s);
+  free(idx);
+  free(val);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Batched drivers over typed logits, uniforms from Philox, threads over      */
+/* requests.  Layout: target [B, gmax+1, V], draft [B, gmax, V], row-major;    */
+/* draft_tokens [B, gmax]; out_tokens [B, gmax+1].  gamma (nullable) gives a  */
+/* per-request draft length (< 0: padded request, all outputs -1); temp       */
+/* (nullable) gives a per-request temperature, else temp_scalar.              */
+/* ------------------------------------------------------------------------- */
+
+typedef struct {
+  const void* target;
+  const void* draft;
+  int dtype;
+  const int32_t* draft_tokens;
+  int B, gmax, V;
+  const int32_t* gamma;
+  const float* temp;
+  float temp_scalar;
+  uint64_t seed;
+  int k;
+  int32_t* out_a; /* verify: out_tokens     saguaro: bonus_topk    */
+  int32_t* out_b; /* verify: n_accepted     saguaro: saguaro_tokens */
+  int32_t* flag_a; /* verify: flag_pos      saguaro: topk_flag      */
+  int32_t* flag_b; /* verify: flag_kind     saguaro: tok_flag       */
+  double* stats;
+  int saguaro;
+  int nthreads;
+  int tid;
+} orc_job;
+
+static void run_request(const orc_job* jb, int b, double* xt, double* xd) {
+  const int gmax = jb->gmax, V = jb->V;
+  const int W = gmax + 1;
+  int g = jb->gamma ? jb->gamma[b] : gmax;
+  double T = jb->temp ? (double)jb->temp[b] : (double)jb->temp_scalar;
+  if (jb->saguaro) {
+    int k = jb->k;
+    for (int t = 0; t < W * k; ++t) jb->out_a[(size_t)b * W * k + t] = -1;
+    for (int j = 0; j < W; ++j) {
+      jb->out_b[(size_t)b * W + j] = -1;
+      jb->flag_a[(size_t)b * W + j] = 0;
+      jb->flag_b[(size_t)b * W + j] = 0;
+    }
+    if (g < 0 || g > gmax) return;
+    for (int j = 0; j <= g; ++j) orc_row_to_f64(jb->target, jb->dtype, (size_t)b * W + j, V, xt + (size_t)j * V);
+    for (int j = 0; j < g; ++j) orc_row_to_f64(jb->draft, jb->dtype, (size_t)b * gmax + j, V, xd + (size_t)j * V);
+    double u[64];
+    for (int j = 0; j <= g; ++j) u[j] = orc_uniform(jb->seed, (uint32_t)b, (uint32_t)j, 2u);
+    orc_saguaro_request(g, V, xt, xd, T, k, u, jb->out_a + (size_t)b * W * k, jb->out_b + (size_t)b * W,
+                        jb->flag_a + (size_t)b * W, jb->flag_b + (size_t)b * W,
+                        jb->stats ? jb->stats + (size_t)b * W * ORC_NSTAT_SAGUARO : NULL);
+    return;
+  }
+  int32_t* out = jb->out_a + (size_t)b * W;
+  for (int t = 0; t < W; ++t) out[t] = -1;
+  jb->out_b[b] = -1;
+  jb->flag_a[b] = -1;
+  jb->flag_b[b] = -1;
+  if (jb->stats) fill_nan(jb->stats + (size_t)b * W * ORC_NSTAT_VERIFY, W * ORC_NSTAT_VERIFY);
+  if (g < 0 || g > gmax || !(T >= 0.0)) return;
+  for (int i = 0; i <= g; ++i) orc_row_to_f64(jb->target, jb->dtype, (size_t)b * W + i, V, xt + (size_t)i * V);
+  if (T > 0.0)
+    for (int i = 0; i < g; ++i) orc_row_to_f64(jb->draft, jb->dtype, (size_t)b * gmax + i, V, xd + (size_t)i * V);
+  double ua[64], ur[64];
+  for (int i = 0; i <= g; ++i) {
+    ua[i] = orc_uniform(jb->seed, (uint32_t)b, (uint32_t)i, 0u);
+    ur[i] = orc_uniform(jb->seed, (uint32_t)b, (uint32_t)i, 1u);
+  }
+  int32_t fp, fk;
+  int n = orc_verify_request(g, V, xt, xd, T, jb->draft_tokens + (size_t)b * gmax, ua, ur, out, &fp, &fk,
+                             jb->stats ? jb->stats + (size_t)b * W * ORC_NSTAT_VERIFY : NULL);
+  if (n < 0) {
+    for (int t = 0; t < W; ++t) out[t] = -1;
+  }
+  jb->out_b[b] = n;
+  jb->flag_a[b] = fp;
+  jb->flag_b[b] = fk;
+}
+
+static void* worker(void* arg) {
+  const orc_job* jb = (const orc_job*)arg;
+  size_t rows = (size_t)(jb->gmax + 1) * (size_t)jb->V;
+  double* xt = (double*)malloc(sizeof(double) * rows);
+  double* xd = (double*)malloc(sizeof(double) * rows);
+  for (int b = jb->tid; b < jb->B; b += jb->nthreads) run_request(jb, b, xt, xd);
+  free(xt);
+  free(xd);
+  return NULL;
+}
+
+static int run_batch(orc_job base) {
+  if (base.gmax < 0 || base.gmax > 62 || base.V <= 0 || base.B < 0) return -1;
+  int nth = base.nthreads > 0 ? base.nthreads : 1;
+  if (nth > base.B) nth = base.B > 0 ? base.B : 1;
+  pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)nth);
+  orc_job* jobs = (orc_job*)malloc(sizeof(orc_job) * (size_t)nth);
+  for (int t = 0; t < nth; ++t) {
+    jobs[t] = base;
+    jobs[t].nthreads = nth;
+    jobs[t].tid = t;
+    pthread_create(&th[t], NULL, worker, &jobs[t]);
+  }
+  for (int t = 0; t < nth; ++t) pthread_join(th[t], NULL);
+  free(th);
+  free(jobs);
+  return 0;
+}
+
+/* Batched verification.  stats (nullable): [B, gmax+1, 8]. */
+int orc_verify_batch(const void* target, const void* draft, int dtype, const int32_t* draft_tokens,
+                     int B, int gmax, int V, const int32_t* gamma, const float* temp,
+                     float temp_scalar, uint64_t seed, int32_t* out_tokens, int32_t* n_accepted,
+                     int32_t* flag_pos, int32_t* flag_kind, double* stats, int nthreads) {
+  orc_job jb;
+  memset(&jb, 0, sizeof jb);
+  jb.target = target;
+  jb.draft = draft;
+  jb.dtype = dtype;
+  jb.draft_tokens = draft_tokens;
+  jb.B = B;
+  jb.gmax = gmax;
+  jb.V = V;
+  jb.gamma = gamma;
+  jb.temp = temp;
+  jb.temp_scalar = temp_scalar;
+  jb.seed = seed;
+  jb.out_a = out_tokens;
+  jb.out_b = n_accepted;
+  jb.flag_a = flag_pos;
+  jb.flag_b = flag_kind;
+  jb.stats = stats;
+  jb.saguaro = 0;
+  jb.nthreads = nthreads;
+  return run_batch(jb);
+}
+
+/* Batched Saguaro pre-speculation.  bonus_topk [B, g+1, k], saguaro_tokens
+ * [B, g+1], topk_flag / tok_flag [B, g+1], stats (nullable) [B, g+1, 8]. */
+int orc_saguaro_batch(const void* target, const void* draft, int dtype, int B, int g, int V, int k,
+                      float temperature, uint64_t seed, int32_t* bonus_topk, int32_t* saguaro_tokens,
+                      int32_t* topk_flag, int32_t* tok_flag, double* stats, int nthreads) {
+  if (k < 1 || k > 30 || k > V || !(temperature > 0.0f)) return -1;
+  orc_job jb;
+  memset(&jb, 0, sizeof jb);
+  jb.target = target;
+  jb.draft = draft;
+  jb.dtype = dtype;
+  jb.B = B;
+  jb.gmax = g;
+  jb.V = V;
+  jb.temp_scalar = temperature;
+  jb.seed = seed;
+  jb.k = k;
+  jb.out_a = bonus_topk;
+  jb.out_b = saguaro_tokens;
+  jb.flag_a = topk_flag;
+  jb.flag_b = tok_flag;
+  jb.stats = stats;
+  jb.saguaro = 1;
+  jb.nthreads = nthreads;
+  return run_batch(jb);
+}
+
+int orc_mutant_id(void) { return ORC_MUTANT; }
