@@ -1,0 +1,418 @@
+"""Benchmark: verified rounds/s and achieved HBM GB/s of batched speculative-decoding
+verification on B=64, gamma=4, V=128256 bf16 logits (T = 0.8, Zipf-biased synthetic
+logits), one ssd_verify call per round.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  ``value`` is whole-job rounds/s with inputs already
+resident in HBM; ``e2e`` is the same metric with the logits copied from pinned host
+memory every step and the outputs read back; ``roofline`` relates the verify kernel's
+algorithmic bytes per launch to its CUDA-event duration; ``cpu_baseline`` times the
+fp64 CPU oracle on a bounded sample of the same workload.  ``--impl reference`` times
+only the CPU oracle (the reference arm).  Under torchrun every rank runs its own
+replica of the workload (requests are independent: weak scaling, no collective on
+the data path; one all-reduce of the timings).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import signal
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "verified rounds/sec and achieved HBM GB/s vs peak (B=64, γ=4, V=128256 bf16)"
+B, GAMMA, V, TEMP = 64, 4, 128256, 0.8
+N_SETS = 4  # rotating input sets: 4 x 147.75 MB > 129 MB L2
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            ident = ["--id=" + (uuid if uuid.startswith("GPU-") else "GPU-" + uuid)]
+        except Exception:
+            ident = []
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                                          "-lms", "200"] + ident, stdout=open(self.path, "w"),
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.send_signal(signal.SIGTERM)
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        smax = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def make_sets(device, n_sets):
+    from speculative_decoding_verification_draft_gb300 import workloads
+    sets = []
+    for s in range(n_sets):
+        sets.append(workloads.zipf_batch(B, GAMMA, V, temperature=TEMP, seed=2 + 1000 * s, device=device))
+    return sets
+
+
+def verify_args(lib, batch, out, n, ws, stream_handle, seed):
+    return (batch.target.data_ptr(), batch.draft.data_ptr(), 0, batch.draft_tokens.data_ptr(), B, GAMMA, V,
+            TEMP, seed, out.data_ptr(), n.data_ptr(), ws.data_ptr(), ws.numel(), stream_handle)
+
+
+def time_gpu(args, local_rank, world, rank):
+    import torch.distributed as dist
+    from speculative_decoding_verification_draft_gb300 import build as cuda_build
+    from speculative_decoding_verification_draft_gb300 import ssdv, workloads
+
+    cuda_build.build()
+    lib = ssdv.lib()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    sh = stream.cuda_stream
+    sets = make_sets(dev, N_SETS)
+    alg_bytes = sets[0].algorithmic_bytes()
+    out = [torch.empty(B, GAMMA + 1, dtype=torch.int32, device=dev) for _ in range(N_SETS)]
+    nac = [torch.empty(B, dtype=torch.int32, device=dev) for _ in range(N_SETS)]
+    ws = ssdv.make_workspace(B, GAMMA, dev)
+    torch.cuda.synchronize()
+    calls = [verify_args(lib, sets[s], out[s], nac[s], ws, sh, 12345 + s) for s in range(N_SETS)]
+
+    def step(k):
+        st = lib.ssd_verify(*calls[k % N_SETS])
+        if st != 0:
+            raise RuntimeError(lib.ssd_last_error().decode())
+
+    clocks = ClockSampler(local_rank)
+    with torch.cuda.stream(stream):
+        for k in range(args.warmup):
+            step(k)
+    stream.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for k in range(args.steps):
+            ev[k][0].record(stream)
+            step(k)
+            ev[k][1].record(stream)
+        t1.record(stream)
+    stream.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    total_ms = t0.elapsed_time(t1)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # acceptance diagnostics (the page's estimator: accepted per round / gamma)
+    n_np = nac[0].cpu().numpy()
+    diag = {"mean_accepted": float(n_np.mean()), "tokens_per_round": float(n_np.mean() + 1),
+            "acceptance_estimate": float(n_np.mean() / GAMMA)}
+
+    # end to end: pinned host logits -> device, verify, outputs -> host, every step
+    e2e = time_e2e(lib, sets[0], dev, stream, args)
+    extra = secondary(ssdv, workloads, dev, stream) if args.secondary and rank == 0 else None
+    return dict(total_ms=total_ms, launch_ms=launch_ms, alg_bytes=alg_bytes, clocks=clk, diag=diag, e2e=e2e,
+                secondary=extra, sets=sets)
+
+
+def time_e2e(lib, batch, dev, stream, args):
+    steps = max(3, min(args.e2e_steps, args.steps))
+    host_t = batch.target.cpu().pin_memory()
+    host_d = batch.draft.cpu().pin_memory()
+    host_k = batch.draft_tokens.cpu().pin_memory()
+    dt = torch.empty_like(batch.target)
+    dd = torch.empty_like(batch.draft)
+    dk = torch.empty_like(batch.draft_tokens)
+    out = torch.empty(B, GAMMA + 1, dtype=torch.int32, device=dev)
+    n = torch.empty(B, dtype=torch.int32, device=dev)
+    out_h = torch.empty(B, GAMMA + 1, dtype=torch.int32).pin_memory()
+    n_h = torch.empty(B, dtype=torch.int32).pin_memory()
+    from speculative_decoding_verification_draft_gb300 import ssdv
+    ws = ssdv.make_workspace(B, GAMMA, dev)
+    torch.cuda.synchronize()
+    sh = stream.cuda_stream
+
+    def one(k):
+        dt.copy_(host_t, non_blocking=True)
+        dd.copy_(host_d, non_blocking=True)
+        dk.copy_(host_k, non_blocking=True)
+        st = lib.ssd_verify(dt.data_ptr(), dd.data_ptr(), 0, dk.data_ptr(), B, GAMMA, V, TEMP, 777 + k,
+                            out.data_ptr(), n.data_ptr(), ws.data_ptr(), ws.numel(), sh)
+        if st != 0:
+            raise RuntimeError(lib.ssd_last_error().decode())
+        out_h.copy_(out, non_blocking=True)
+        n_h.copy_(n, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for k in range(3):
+            one(k)
+    stream.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for k in range(steps):
+            one(k)
+        b.record(stream)
+    stream.synchronize()
+    ms = a.elapsed_time(b)
+    h2d = host_t.numel() * host_t.element_size() + host_d.numel() * host_d.element_size() + host_k.numel() * 4
+    d2h = out_h.numel() * 4 + n_h.numel() * 4
+    return {"value": steps / (ms / 1e3), "unit": "rounds/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": steps}
+
+
+def secondary(ssdv, workloads, dev, stream):
+    """The other workloads of the method, timed the same way (kernel-only)."""
+    res = {}
+
+    def timeit(fn, reps):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+        stream.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            for _ in range(reps):
+                fn()
+            b.record(stream)
+        stream.synchronize()
+        return a.elapsed_time(b) / reps
+
+    peak, _ = load_peaks()
+    # Saguaro pre-speculation: B=256, gamma 6, V 152064 fp32, k 3
+    sb = workloads.zipf_batch(256, 6, 152064, dtype=torch.float32, temperature=0.8, seed=3,
+                              sigma_range=(0.6, 0.6), device=dev, sample_tokens=False)
+    topk = torch.empty(256, 7, 3, dtype=torch.int32, device=dev)
+    tok = torch.empty(256, 7, dtype=torch.int32, device=dev)
+    ms = timeit(lambda: ssdv.saguaro_prespec(sb.target, sb.draft, 3, 0.8, 3, topk, tok, stream=stream), 10)
+    by = sb.algorithmic_bytes()
+    res["saguaro_B256_g6_V152064_f32"] = {"ms_per_round": ms, "rounds_per_s": 1e3 / ms, "bytes": by,
+                                          "gbs": by / ms / 1e6, "frac_of_measured_hbm": by / ms / 1e6 / peak}
+    del sb
+    torch.cuda.empty_cache()
+    # ragged mixed batch: B=512, gamma 1..8, V 128256 bf16, half greedy
+    rb = workloads.ragged_batch(512, 8, 128256, seed=4, device=dev)
+    out = torch.empty(512, 9, dtype=torch.int32, device=dev)
+    n = torch.empty(512, dtype=torch.int32, device=dev)
+    ws = ssdv.make_workspace(512, 8, dev)
+    ms = timeit(lambda: ssdv.verify_ragged(rb.target, rb.draft, rb.draft_tokens, rb.gamma, rb.temperature, 4,
+                                           out, n, ws, stream=stream), 20)
+    by = rb.algorithmic_bytes()
+    res["ragged_B512_g1to8_V128256_bf16"] = {"ms_per_round": ms, "rounds_per_s": 1e3 / ms, "bytes": by,
+                                             "gbs": by / ms / 1e6, "frac_of_measured_hbm": by / ms / 1e6 / peak}
+    del rb
+    torch.cuda.empty_cache()
+    # latency: B=1, gamma 5, V 32000 bf16, T 1
+    gb = workloads.gaussian_batch(1, 5, 32000, seed=1, device=dev)
+    out = torch.empty(1, 6, dtype=torch.int32, device=dev)
+    n = torch.empty(1, dtype=torch.int32, device=dev)
+    ws = ssdv.make_workspace(1, 5, dev)
+    ms = timeit(lambda: ssdv.verify(gb.target, gb.draft, gb.draft_tokens, 1.0, 1, out, n, ws, stream=stream), 200)
+    res["latency_B1_g5_V32000_bf16"] = {"us_per_round": ms * 1e3}
+    # toy: 4096 rounds, V 7 fp32
+    import json as _json
+    with open(os.path.join(ROOT, "tests", "golden", "toy_tables.json")) as f:
+        tables = _json.load(f)
+    tb = workloads.toy_batch(tables, 4096, 4, 0, device=dev)
+    out = torch.empty(4096, 5, dtype=torch.int32, device=dev)
+    n = torch.empty(4096, dtype=torch.int32, device=dev)
+    ws = ssdv.make_workspace(4096, 4, dev)
+    ms = timeit(lambda: ssdv.verify(tb.target, tb.draft, tb.draft_tokens, 1.0, 0, out, n, ws, stream=stream), 50)
+    res["toy_B4096_g4_V7_f32"] = {"us_per_call": ms * 1e3}
+    return res
+
+
+def cpu_baseline(batch_cpu, budget_s=12.0, max_s=30.0):
+    """The fp64 oracle on the host cores: whole rounds of the same workload,
+    repeated until about budget_s of wall time (bounded by max_s)."""
+    import oracle
+    orc = oracle.load()
+    tgt, dft = batch_cpu.numpy_logits()
+    tok = batch_cpu.draft_tokens.cpu().numpy()
+    cores = os.cpu_count() or 1
+    rounds, t_start = 0, time.perf_counter()
+    while True:
+        orc.verify_batch(tgt, dft, tok, TEMP, 99 + rounds, nthreads=cores)
+        rounds += 1
+        el = time.perf_counter() - t_start
+        if el >= budget_s or el + el / rounds > max_s:
+            break
+    return {"value": rounds / el, "unit": "rounds/s", "cores": cores, "kind": "oracle",
+            "sample": f"{rounds} whole rounds (B=64, gamma 4, V 128256 bf16), fp64 C oracle, {cores} threads"}
+
+
+def reference_arm(args):
+    """--impl reference: the CPU oracle as the reference implementation."""
+    from speculative_decoding_verification_draft_gb300 import workloads
+    import oracle
+    orc = oracle.load()
+    batch = workloads.zipf_batch(B, GAMMA, V, temperature=TEMP, seed=2)
+    tgt, dft = batch.numpy_logits()
+    tok = batch.draft_tokens.numpy()
+    cores = os.cpu_count() or 1
+    # size each step so the whole run stays within a few minutes
+    t0 = time.perf_counter()
+    orc.verify_batch(tgt[:cores], dft[:cores], tok[:cores], TEMP, 1, nthreads=cores, req_ids=np.arange(cores))
+    per_req = (time.perf_counter() - t0) / cores * 1.0
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    n_req = int(max(1, min(B, budget / max(per_req, 1e-6))))
+    ids = np.arange(n_req)
+    for w in range(args.warmup):
+        orc.verify_batch(tgt[:n_req], dft[:n_req], tok[:n_req], TEMP, w, nthreads=cores, req_ids=ids)
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        orc.verify_batch(tgt[:n_req], dft[:n_req], tok[:n_req], TEMP, 1000 + k, nthreads=cores, req_ids=ids)
+    el = time.perf_counter() - t0
+    value = args.steps * n_req / B / el
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "rounds/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "verify B=64 gamma=4 V=128256 bf16 T=0.8 (Zipf-biased synthetic logits)",
+                       "sample_requests_per_step": n_req},
+            "cpu_baseline": {"value": value, "unit": "rounds/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{n_req} of 64 requests per step, fp64 C oracle, {cores} threads"},
+            "e2e": {"value": value, "unit": "rounds/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=500)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--no-secondary", dest="secondary", action="store_false")
+    ap.add_argument("--no-cpu-baseline", dest="cpu", action="store_false")
+    args = ap.parse_args()
+    world, rank, local = dist_env()
+
+    if args.impl == "reference":
+        if rank == 0:
+            reference_arm(args)
+        return
+
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    r = time_gpu(args, local, world, rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    peak, peak_kind = load_peaks()
+    step_ms = r["total_ms"] / args.steps
+    launch_ms = float(np.mean(r["launch_ms"]))
+    alg = r["alg_bytes"]
+    achieved = alg / (launch_ms * 1e-3) / 1e9
+    value = world * args.steps / (r["total_ms"] * 1e-3)
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "verify_traffic.json")
+    if os.path.exists(tpath):
+        with open(tpath) as f:
+            traffic = json.load(f).get("bytes_per_launch")
+    line = {
+        "metric": METRIC, "value": value, "unit": "rounds/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "verify B=64 gamma=4 V=128256 bf16 T=0.8 (Zipf-biased synthetic logits)",
+                   "B": B, "gamma": GAMMA, "V": V, "temperature": TEMP,
+                   "l2": f"{N_SETS} rotating input sets of {alg / 1e6:.2f} MB (> 129 MB L2)",
+                   "parallelism": f"replicas x{world}"},
+        "hbm_gbs": alg / (step_ms * 1e-3) / 1e9,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "peak_kind": peak_kind, "kernel": "verify_kernel<bf16>",
+                     "algorithmic_bytes_per_launch": alg, "mean_launch_us": launch_ms * 1e3},
+        "gpu_launches": args.steps,
+        "clocks": r["clocks"],
+        "e2e": r["e2e"],
+        "acceptance": r["diag"],
+    }
+    if r["secondary"] is not None:
+        line["secondary"] = r["secondary"]
+    if args.cpu:
+        line["cpu_baseline"] = cpu_baseline(r["sets"][0].to("cpu"))
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

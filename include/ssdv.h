@@ -1,0 +1,181 @@
+/*
+ * ssdv.h -- C ABI of libssdv: batched speculative-decoding verification and
+ * Saguaro pre-speculation on one GPU (sm_103a).
+ *
+ * Notation (speculative-decoding blog "投机解码 (Speculative Decoding):
+ * 小模型猜、大模型验", section 3): q = target distribution, p = draft
+ * distribution, gamma = number of draft tokens per request.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Pointers named *_logits, draft_tokens, out_*, gamma, temperature,
+ *    workspace, bonus_topk, saguaro_tokens, stats are DEVICE pointers owned by
+ *    the caller.  The library allocates no device memory and keeps no pointer
+ *    after a call returns.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
+ *    NULL = the legacy default stream), except where stated otherwise.
+ *  - Logit layout: target [B, gamma_max+1, V] and draft [B, gamma_max, V],
+ *    row-major, contiguous, row stride V elements.  Row i of the target is the
+ *    target distribution for position i (row gamma is the position after the
+ *    last draft token); row i of the draft is the draft distribution that
+ *    proposed draft token i.  dtype is SSD_BF16 or SSD_F32 for both.
+ *  - Rows whose start is 16-byte aligned (base 16-byte aligned and V*size
+ *    a multiple of 16) are staged into shared memory with bulk async copies;
+ *    other rows take a plain-load path.  Both give the same results.
+ *  - Every real row must hold at least one finite logit; NaN and +inf logits
+ *    are not valid input.  -inf logits are allowed (probability 0).
+ *  - Temperature: softmax(x / T) on both target and draft.  T == 0 selects
+ *    greedy verification (accept while the draft token equals the target
+ *    argmax, lowest index among equal logits; the correction / bonus is the
+ *    target argmax).  0 < T < 1e-6, T < 0, NaN and inf are rejected.
+ *  - Uniforms: Philox4x32-10 (Salmon et al., SC'11) with key (seed low 32
+ *    bits, seed high 32 bits) and counter (request b, position i, 0, 0);
+ *    word 0 is the accept draw, word 1 the resample / bonus draw, word 2 the
+ *    Saguaro draw; u = (word >> 8) * 2^-24.  The same inputs and seed always
+ *    give the same outputs.
+ *  - Errors found on the host are returned before anything is launched.
+ *    Errors found on the device (a draft token outside [0, V), a per-request
+ *    gamma above gamma_max, a bad per-request temperature) make that request's
+ *    outputs -1 and set a bit in the workspace status word (see
+ *    ssd_read_status); the other requests are unaffected.
+ */
+#ifndef SSDV_H
+#define SSDV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SSD_OK = 0,
+  SSD_ERR_NULL = 1,        /* a required pointer is NULL                        */
+  SSD_ERR_SHAPE = 2,       /* B, gamma, V or k out of range                      */
+  SSD_ERR_DTYPE = 3,       /* unknown ssd_dtype                                  */
+  SSD_ERR_ALIGN = 4,       /* a pointer is not aligned to its element size       */
+  SSD_ERR_TOKEN_RANGE = 5, /* (device) a draft token outside [0, V)              */
+  SSD_ERR_TEMPERATURE = 6, /* temperature negative, NaN, inf or in (0, 1e-6)     */
+  SSD_ERR_CUDA = 7,        /* a CUDA runtime call failed (see ssd_last_error)     */
+  SSD_ERR_UNSUPPORTED = 8, /* no launch configuration fits this device / shape   */
+  SSD_ERR_WORKSPACE = 9,   /* workspace missing or smaller than required         */
+  SSD_ERR_GAMMA = 10,      /* (device) a per-request gamma above gamma_max       */
+  SSD_ERR_TIMEOUT = 11     /* (device) a bounded wait for a bulk copy ran out    */
+} ssd_status;
+
+typedef enum { SSD_BF16 = 0, SSD_F32 = 1 } ssd_dtype;
+
+#define SSD_MAX_GAMMA 32   /* largest gamma / gamma_max accepted                 */
+#define SSD_MAX_TOPK 8     /* largest k accepted by ssd_saguaro_prespec           */
+#define SSD_MAX_V (1 << 19)  /* fp32 units above ~440k need more than 16 CTAs */
+#define SSD_NSTAT_VERIFY 8
+#define SSD_NSTAT_SAGUARO 8
+
+/* Bytes of device workspace ssd_verify / ssd_verify_ragged need for a batch of
+ * B requests with up to gamma_max draft tokens.  The workspace holds one
+ * arrival counter per request, the per-position results and a status word. */
+size_t ssd_workspace_bytes(int B, int gamma_max);
+
+/* Zero a workspace (asynchronous memset on `stream`).  A workspace must be
+ * zeroed once before its first use; every call leaves it zeroed again, so it
+ * can be reused by later calls on the same stream.  Two calls that may run at
+ * the same time on the GPU need two workspaces. */
+ssd_status ssd_workspace_init(void* workspace, size_t ws_bytes, void* stream);
+
+/* Batched verification, one gamma and one temperature for the whole batch.
+ *
+ * Blog section 3: for each request b and draft position i = 0..gamma-1, draw
+ * u_i and accept draft token x_i iff u_i < min(1, q_i(x_i) / p_i(x_i)); at the
+ * first rejection n, emit one token sampled from (q_n - p_n)+ / sum (q_n - p_n)+
+ * (from q_n if that mass is zero) and stop; if all gamma are accepted, emit a
+ * bonus token sampled from q_gamma.  Greedy (T == 0): accept while x_i equals
+ * argmax of target row i; emit the argmax at the stopping position.
+ *
+ *   target_logits  [B, gamma+1, V], draft_logits [B, gamma, V] (unused and may
+ *                  be NULL when temperature == 0)
+ *   draft_tokens   [B, gamma] int32
+ *   out_tokens     [B, gamma+1] int32: x_0..x_{n-1}, the correction or bonus
+ *                  token at index n, then -1
+ *   n_accepted     [B] int32: n in 0..gamma (-1 for a request with an error)
+ *   workspace      >= ssd_workspace_bytes(B, gamma) bytes, zeroed once
+ *
+ * Constraints: 1 <= B, 0 <= gamma <= SSD_MAX_GAMMA, 1 <= V <= SSD_MAX_V. */
+ssd_status ssd_verify(const void* target_logits, const void* draft_logits, ssd_dtype dtype,
+                      const int32_t* draft_tokens, int B, int gamma, int V, float temperature,
+                      uint64_t seed, int32_t* out_tokens, int32_t* n_accepted, void* workspace,
+                      size_t ws_bytes, void* stream);
+
+/* Ragged verification: request b uses gamma[b] draft tokens (0..gamma_max;
+ * a negative gamma[b] marks a padded request whose outputs are all -1) and
+ * temperature[b] (0 = greedy).  Layouts are padded to gamma_max: target rows
+ * > gamma[b], draft rows >= gamma[b], draft tokens >= gamma[b], and every draft
+ * row of a greedy request are never read.  out_tokens [B, gamma_max+1]. */
+ssd_status ssd_verify_ragged(const void* target_logits, const void* draft_logits, ssd_dtype dtype,
+                             const int32_t* draft_tokens, int B, int gamma_max, int V,
+                             const int32_t* gamma, const float* temperature, uint64_t seed,
+                             int32_t* out_tokens, int32_t* n_accepted, void* workspace,
+                             size_t ws_bytes, void* stream);
+
+/* Saguaro pre-speculation (SSD notes, sections 3.1 and 3.2).  For each request
+ * b and each acceptance length j = 0..gamma:
+ *   r_j = (q_j - p_j)+ / sum (q_j - p_j)+  for j < gamma (q_j if that mass is
+ *         zero), and r_gamma = q_gamma;
+ *   bonus_topk[b, j, 0..k-1] = the k largest entries of r_j, descending, the
+ *         lower index first among equal values;
+ *   saguaro_tokens[b, j] = one sample from p_saguaro proportional to
+ *         sqrt(p_D(v) * max(r_j(v), 1e-8)), p_D = p_j (q_gamma at j = gamma).
+ *   target_logits [B, gamma+1, V], draft_logits [B, gamma, V];
+ *   bonus_topk [B, gamma+1, k] int32, saguaro_tokens [B, gamma+1] int32.
+ * Constraints: temperature > 0, 1 <= k <= SSD_MAX_TOPK, k <= V.  No
+ * workspace is needed. */
+ssd_status ssd_saguaro_prespec(const void* target_logits, const void* draft_logits, ssd_dtype dtype,
+                               int B, int gamma, int V, int k, float temperature, uint64_t seed,
+                               int32_t* bonus_topk, int32_t* saguaro_tokens, void* stream);
+
+/* Debug / parity: ssd_verify (same arguments and outputs) that also returns
+ * the per-position quantities it computes, for every position whether or not
+ * it is reached (the residual pass then runs at every position).
+ * stats [B, gamma+1, 8] float:
+ *   0 target row max (raw logit), 1 ln sum exp((x - max)/T) of the target row,
+ *   2 draft row max, 3 its log-sum, 4 q_i(x_i), 5 p_i(x_i),
+ *   6 residual mass sum (q_i - p_i)+, 7 accept probability min(1, q/p).
+ * Row gamma fills only 0 and 1; entries that do not apply are NaN.  Greedy
+ * (T == 0) fills only entry 0 (the target row max). */
+ssd_status ssd_debug_rowstats(const void* target_logits, const void* draft_logits, ssd_dtype dtype,
+                              const int32_t* draft_tokens, int B, int gamma, int V,
+                              float temperature, uint64_t seed, int32_t* out_tokens,
+                              int32_t* n_accepted, float* stats, void* workspace,
+                              size_t ws_bytes, void* stream);
+
+/* Debug / parity: the per-position quantities ssd_saguaro_prespec computes.
+ * stats [B, gamma+1, 8] float: 0 target log-sum, 1 draft log-sum (NaN at
+ * j = gamma), 2 residual mass S_j (1 at j = gamma), 3 Zs = sum_v sqrt(p_D(v) *
+ * max(r_j(v), 1e-8)), 4 p_saguaro(token), 5 r_j of top slot 0, 6 r_j of top
+ * slot k-1, 7 NaN.  Outputs as ssd_saguaro_prespec. */
+ssd_status ssd_debug_saguaro_stats(const void* target_logits, const void* draft_logits,
+                                   ssd_dtype dtype, int B, int gamma, int V, int k,
+                                   float temperature, uint64_t seed, int32_t* bonus_topk,
+                                   int32_t* saguaro_tokens, float* stats, void* stream);
+
+/* Debug / parity: the uniforms the kernels draw.  out [B, W, 3] float gets,
+ * for request b < B and position i < W, the accept, resample / bonus and
+ * Saguaro uniforms (Philox4x32-10 words 0, 1, 2 of counter (b, i, 0, 0)). */
+ssd_status ssd_debug_uniforms(uint64_t seed, int B, int W, float* out, void* stream);
+
+/* Read and clear the device status word of a workspace.  Synchronises
+ * `stream`.  *status gets SSD_OK or the lowest-numbered device error seen
+ * since the last read. */
+ssd_status ssd_read_status(void* workspace, size_t ws_bytes, int* status, void* stream);
+
+/* Static text for a status code. */
+const char* ssd_status_str(ssd_status status);
+
+/* Detail of the last error returned on the calling thread ("" if none). */
+const char* ssd_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSDV_H */

@@ -65,10 +65,12 @@ def _declare(lib):
     lib.orc_saguaro_request.argtypes = [c_int, c_int, P, P, c_double, c_int, P, P, P, P, P, P]
     lib.orc_saguaro_request.restype = c_int
     lib.orc_verify_batch.argtypes = [P, P, c_int, P, c_int, c_int, c_int, P, P, c_float, c_u64,
-                                     P, P, P, P, P, c_int]
+                                     P, P, P, P, P, P, c_int]
     lib.orc_verify_batch.restype = c_int
     lib.orc_saguaro_batch.argtypes = [P, P, c_int, c_int, c_int, c_int, c_int, c_float, c_u64,
-                                      P, P, P, P, P, c_int]
+                                      P, P, P, P, P, P, c_int]
+    lib.orc_saguaro_position.argtypes = [c_int, P, P, c_double, P, P]
+    lib.orc_saguaro_position.restype = None
     lib.orc_saguaro_batch.restype = c_int
     lib.orc_mutant_id.argtypes = []
     lib.orc_mutant_id.restype = c_int
@@ -151,6 +153,15 @@ class Oracle:
         self.lib.orc_topk(_ptr(w), w.size, k, _ptr(idx), _ptr(val))
         return idx, val
 
+    def saguaro_position(self, xt_row, xd_row, T: float):
+        """(r, p_saguaro) of one position; xd_row None at the bonus position."""
+        xt = np.ascontiguousarray(xt_row, dtype=np.float64).reshape(-1)
+        xd = None if xd_row is None else np.ascontiguousarray(xd_row, dtype=np.float64).reshape(-1)
+        r = np.empty_like(xt)
+        ps = np.empty_like(xt)
+        self.lib.orc_saguaro_position(xt.size, _ptr(xt), _ptr(xd), float(T), _ptr(r), _ptr(ps))
+        return r, ps
+
     # --- one request, explicit uniforms ----------------------------------
     def verify_request(self, xt, xd, T, tok, u_acc, u_res, stats: bool = False):
         """xt: (g+1, V) fp64 target logits; xd: (g, V) draft logits; tok: (g,)."""
@@ -185,11 +196,13 @@ class Oracle:
 
     # --- batches over typed logits, Philox uniforms ----------------------
     def verify_batch(self, target, draft, draft_tokens, temperature, seed: int,
-                     gamma=None, stats: bool = False, nthreads: int = 1):
+                     gamma=None, stats: bool = False, nthreads: int = 1, req_ids=None):
         """target [B, gmax+1, V], draft [B, gmax, V] (uint16 bf16 bits or float32).
 
         ``temperature``: a float, or a float32 array [B] (per request).
         ``gamma``: None (every request uses gmax) or an int32 array [B].
+        ``req_ids``: request index of each row in the Philox counter (default 0..B-1),
+        so that a sample of a larger batch draws the same uniforms.
         """
         target, dt = _logit_array(target)
         draft, dd = _logit_array(draft)
@@ -209,15 +222,16 @@ class Oracle:
         fp = np.empty(B, np.int32)
         fk = np.empty(B, np.int32)
         st = np.empty((B, W, NSTAT_VERIFY), np.float64) if stats else None
+        rid = None if req_ids is None else np.ascontiguousarray(req_ids, dtype=np.int32).reshape(B)
         rc = self.lib.orc_verify_batch(_ptr(target), _ptr(draft), dt, _ptr(tok), B, gmax, V,
                                        _ptr(gam), _ptr(temps), tscalar, seed, _ptr(out), _ptr(n),
-                                       _ptr(fp), _ptr(fk), _ptr(st), nthreads)
+                                       _ptr(fp), _ptr(fk), _ptr(st), _ptr(rid), nthreads)
         if rc != 0:
             raise ValueError("oracle rejected the batch arguments")
         return dict(out_tokens=out, n_accepted=n, flag_pos=fp, flag_kind=fk, stats=st)
 
     def saguaro_batch(self, target, draft, k: int, temperature: float, seed: int,
-                      stats: bool = False, nthreads: int = 1):
+                      stats: bool = False, nthreads: int = 1, req_ids=None):
         target, dt = _logit_array(target)
         draft, dd = _logit_array(draft)
         assert dt == dd
@@ -228,9 +242,10 @@ class Oracle:
         kf = np.empty((B, W), np.int32)
         tf = np.empty((B, W), np.int32)
         st = np.empty((B, W, NSTAT_SAGUARO), np.float64) if stats else None
+        rid = None if req_ids is None else np.ascontiguousarray(req_ids, dtype=np.int32).reshape(B)
         rc = self.lib.orc_saguaro_batch(_ptr(target), _ptr(draft), dt, B, g, V, k,
                                         float(temperature), seed, _ptr(topk), _ptr(tok), _ptr(kf),
-                                        _ptr(tf), _ptr(st), nthreads)
+                                        _ptr(tf), _ptr(st), _ptr(rid), nthreads)
         if rc != 0:
             raise ValueError("oracle rejected the batch arguments")
         return dict(bonus_topk=topk, saguaro_tokens=tok, topk_flag=kf, tok_flag=tf, stats=st)

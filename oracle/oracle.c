@@ -516,6 +516,42 @@ int orc_saguaro_request(int g, int V, const double* xt, const double* xd, double
   return 0;
 }
 
+/* One Saguaro position's distributions (for checking ambiguous top-k slots and
+ * sample laws): r = the normalised residual (or q), psag = p_saguaro.  xd may be
+ * NULL for the bonus position. */
+void orc_saguaro_position(int V, const double* xt, const double* xd, double T, double* r, double* psag) {
+  double* q = (double*)malloc(sizeof(double) * (size_t)V);
+  double* p = (double*)malloc(sizeof(double) * (size_t)V);
+  orc_softmax(xt, V, T, q, NULL, NULL);
+  const double* pD = q;
+  if (xd) {
+    orc_softmax(xd, V, T, p, NULL, NULL);
+    double S = 0.0;
+    for (int v = 0; v < V; ++v) {
+      double d = q[v] - p[v];
+      r[v] = d > 0.0 ? d : 0.0;
+      S += r[v];
+    }
+    if (S > 0.0) {
+      for (int v = 0; v < V; ++v) r[v] /= S;
+    } else {
+      for (int v = 0; v < V; ++v) r[v] = q[v];
+    }
+    pD = p;
+  } else {
+    for (int v = 0; v < V; ++v) r[v] = q[v];
+  }
+  double Zs = 0.0;
+  for (int v = 0; v < V; ++v) {
+    double rc = r[v] > ORC_SAGUARO_CLAMP ? r[v] : ORC_SAGUARO_CLAMP;
+    psag[v] = sqrt(pD[v] * rc);
+    Zs += psag[v];
+  }
+  for (int v = 0; v < V; ++v) psag[v] /= Zs;
+  free(q);
+  free(p);
+}
+
 /* ------------------------------------------------------------------------- */
 /* Batched drivers over typed logits, uniforms from Philox, threads over      */
 /* requests.  Layout: target [B, gmax+1, V], draft [B, gmax, V], row-major;    */
@@ -535,6 +571,7 @@ typedef struct {
   float temp_scalar;
   uint64_t seed;
   int k;
+  const int32_t* req_ids; /* nullable: request index used in the Philox counter */
   int32_t* out_a; /* verify: out_tokens     saguaro: bonus_topk    */
   int32_t* out_b; /* verify: n_accepted     saguaro: saguaro_tokens */
   int32_t* flag_a; /* verify: flag_pos      saguaro: topk_flag      */
@@ -548,6 +585,7 @@ typedef struct {
 static void run_request(const orc_job* jb, int b, double* xt, double* xd) {
   const int gmax = jb->gmax, V = jb->V;
   const int W = gmax + 1;
+  const uint32_t rid = (uint32_t)(jb->req_ids ? jb->req_ids[b] : b);
   int g = jb->gamma ? jb->gamma[b] : gmax;
   double T = jb->temp ? (double)jb->temp[b] : (double)jb->temp_scalar;
   if (jb->saguaro) {
@@ -562,7 +600,7 @@ static void run_request(const orc_job* jb, int b, double* xt, double* xd) {
     for (int j = 0; j <= g; ++j) orc_row_to_f64(jb->target, jb->dtype, (size_t)b * W + j, V, xt + (size_t)j * V);
     for (int j = 0; j < g; ++j) orc_row_to_f64(jb->draft, jb->dtype, (size_t)b * gmax + j, V, xd + (size_t)j * V);
     double u[64];
-    for (int j = 0; j <= g; ++j) u[j] = orc_uniform(jb->seed, (uint32_t)b, (uint32_t)j, 2u);
+    for (int j = 0; j <= g; ++j) u[j] = orc_uniform(jb->seed, rid, (uint32_t)j, 2u);
     orc_saguaro_request(g, V, xt, xd, T, k, u, jb->out_a + (size_t)b * W * k, jb->out_b + (size_t)b * W,
                         jb->flag_a + (size_t)b * W, jb->flag_b + (size_t)b * W,
                         jb->stats ? jb->stats + (size_t)b * W * ORC_NSTAT_SAGUARO : NULL);
@@ -580,8 +618,8 @@ static void run_request(const orc_job* jb, int b, double* xt, double* xd) {
     for (int i = 0; i < g; ++i) orc_row_to_f64(jb->draft, jb->dtype, (size_t)b * gmax + i, V, xd + (size_t)i * V);
   double ua[64], ur[64];
   for (int i = 0; i <= g; ++i) {
-    ua[i] = orc_uniform(jb->seed, (uint32_t)b, (uint32_t)i, 0u);
-    ur[i] = orc_uniform(jb->seed, (uint32_t)b, (uint32_t)i, 1u);
+    ua[i] = orc_uniform(jb->seed, rid, (uint32_t)i, 0u);
+    ur[i] = orc_uniform(jb->seed, rid, (uint32_t)i, 1u);
   }
   int32_t fp, fk;
   int n = orc_verify_request(g, V, xt, xd, T, jb->draft_tokens + (size_t)b * gmax, ua, ur, out, &fp, &fk,
@@ -627,9 +665,11 @@ static int run_batch(orc_job base) {
 int orc_verify_batch(const void* target, const void* draft, int dtype, const int32_t* draft_tokens,
                      int B, int gmax, int V, const int32_t* gamma, const float* temp,
                      float temp_scalar, uint64_t seed, int32_t* out_tokens, int32_t* n_accepted,
-                     int32_t* flag_pos, int32_t* flag_kind, double* stats, int nthreads) {
+                     int32_t* flag_pos, int32_t* flag_kind, double* stats, const int32_t* req_ids,
+                     int nthreads) {
   orc_job jb;
   memset(&jb, 0, sizeof jb);
+  jb.req_ids = req_ids;
   jb.target = target;
   jb.draft = draft;
   jb.dtype = dtype;
@@ -655,10 +695,12 @@ int orc_verify_batch(const void* target, const void* draft, int dtype, const int
  * [B, g+1], topk_flag / tok_flag [B, g+1], stats (nullable) [B, g+1, 8]. */
 int orc_saguaro_batch(const void* target, const void* draft, int dtype, int B, int g, int V, int k,
                       float temperature, uint64_t seed, int32_t* bonus_topk, int32_t* saguaro_tokens,
-                      int32_t* topk_flag, int32_t* tok_flag, double* stats, int nthreads) {
+                      int32_t* topk_flag, int32_t* tok_flag, double* stats, const int32_t* req_ids,
+                      int nthreads) {
   if (k < 1 || k > 30 || k > V || !(temperature > 0.0f)) return -1;
   orc_job jb;
   memset(&jb, 0, sizeof jb);
+  jb.req_ids = req_ids;
   jb.target = target;
   jb.draft = draft;
   jb.dtype = dtype;

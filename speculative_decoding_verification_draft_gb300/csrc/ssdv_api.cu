@@ -1,0 +1,320 @@
+// ssdv_api.cu -- the C ABI of libssdv (declared in include/ssdv.h): argument
+// validation, launch geometry, workspace layout, status reporting.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <string>
+
+#include "ssdv_device.cuh"
+#include "ssdv_internal.h"
+
+namespace ssdv {
+
+namespace {
+
+thread_local std::string g_last_error;
+
+ssd_status fail(ssd_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+ssd_status fail(ssd_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+ssd_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(SSD_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned_to(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int esize_of(ssd_dtype dt) { return dt == SSD_BF16 ? 2 : (dt == SSD_F32 ? 4 : 0); }
+
+bool temperature_valid(float T) { return T == 0.f || (T >= 1e-6f && isfinite(T)); }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int env_int(const char* name, int fallback) {
+  const char* v = getenv(name);
+  if (!v || !*v) return fallback;
+  return atoi(v);
+}
+
+}  // namespace
+
+WorkspaceLayout workspace_layout(int B, int gmax) {
+  WorkspaceLayout L;
+  const size_t units = static_cast<size_t>(B) * static_cast<size_t>(gmax + 1);
+  L.status = 0;
+  L.ticket = 16;
+  L.unit_flag = L.ticket + round_up(4 * static_cast<size_t>(B), 16);
+  L.unit_tok = L.unit_flag + round_up(4 * units, 16);
+  L.total = round_up(L.unit_tok + 4 * units, 256);
+  return L;
+}
+
+int max_dynamic_smem() {
+  int dev = 0, v = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
+  return v - 8 * 1024;  // leave room for the kernels' static shared memory
+}
+
+// Split a row of V elements over the CTAs of a cluster.  The default aims at
+// about 32 KB of each staged row per CTA (so two to three CTAs share an SM and
+// one stages while another computes); SSDV_CLUSTER / SSDV_SLICE_BYTES override.
+ssd_status choose_geometry(int V, int esize, bool aligned, bool two_rows, Geometry* geo, int* smem_bytes) {
+  const int max_smem = max_dynamic_smem();
+  if (max_smem <= 0) return fail(SSD_ERR_CUDA, "cannot query the device's shared-memory limit");
+  const long long row_bytes = static_cast<long long>(V) * esize;
+  const int want = env_int("SSDV_SLICE_BYTES", 32 * 1024);
+  int C = env_int("SSDV_CLUSTER", 0);
+  if (C <= 0) C = static_cast<int>((row_bytes + want - 1) / want);
+  C = C < 1 ? 1 : (C > 16 ? 16 : C);
+  for (;; ++C) {
+    if (C > 16)
+      return fail(SSD_ERR_UNSUPPORTED, "V=%d does not fit the shared memory of a 16-CTA cluster", V);
+    const int slice = static_cast<int>(round_up((static_cast<size_t>(V) + C - 1) / C, 8));
+    const int row_smem = static_cast<int>(round_up(static_cast<size_t>(slice) * esize, 128));
+    const int smem = (two_rows ? 2 : 1) * row_smem;
+    const int stage_elems = kStageBytes / esize;
+    const int nstage = (slice + stage_elems - 1) / stage_elems;
+    if (smem > max_smem || nstage > kMaxStages) continue;
+    geo->V = V;
+    geo->slice = slice;
+    geo->csize = (V + slice - 1) / slice;
+    geo->row_smem = row_smem;
+    geo->stage_elems = stage_elems;
+    geo->bulk = aligned ? 1 : 0;
+    *smem_bytes = smem;
+    return SSD_OK;
+  }
+}
+
+namespace {
+
+ssd_status verify_common(const void* target, const void* draft, ssd_dtype dtype, const int32_t* draft_tokens, int B,
+                         int gmax, int V, const int32_t* gamma, const float* temps, float temp_scalar,
+                         bool all_greedy, uint64_t seed, int32_t* out_tokens, int32_t* n_accepted, void* workspace,
+                         size_t ws_bytes, float* stats, void* stream) {
+  const int es = esize_of(dtype);
+  if (es == 0) return fail(SSD_ERR_DTYPE, "unknown dtype %d", static_cast<int>(dtype));
+  if (!target || !out_tokens || !n_accepted || !workspace) return fail(SSD_ERR_NULL, "a required pointer is NULL");
+  if (!draft && !all_greedy && gmax > 0)
+    return fail(SSD_ERR_NULL, "draft_logits is NULL but some request samples");
+  if (gmax > 0 && !draft_tokens) return fail(SSD_ERR_NULL, "draft_tokens is NULL");
+  if (B < 1 || gmax < 0 || gmax > SSD_MAX_GAMMA || V < 1 || V > SSD_MAX_V)
+    return fail(SSD_ERR_SHAPE, "bad shape B=%d gamma=%d V=%d", B, gmax, V);
+  if (!aligned_to(target, es) || (draft && !aligned_to(draft, es)) || !aligned_to(out_tokens, 4) ||
+      !aligned_to(n_accepted, 4) || (draft_tokens && !aligned_to(draft_tokens, 4)) || !aligned_to(workspace, 16) ||
+      (stats && !aligned_to(stats, 4)) || (gamma && !aligned_to(gamma, 4)) || (temps && !aligned_to(temps, 4)))
+    return fail(SSD_ERR_ALIGN, "a pointer is not aligned to its element size (workspace: 16 bytes)");
+  const WorkspaceLayout L = workspace_layout(B, gmax);
+  if (ws_bytes < L.total)
+    return fail(SSD_ERR_WORKSPACE, "workspace of %zu bytes < %zu required", ws_bytes, L.total);
+  const bool aligned = aligned_to(target, 16) && (!draft || aligned_to(draft, 16)) &&
+                       ((static_cast<size_t>(V) * es) % 16 == 0);
+  Geometry geo;
+  int smem = 0;
+  ssd_status st = choose_geometry(V, es, aligned, !all_greedy, &geo, &smem);
+  if (st != SSD_OK) return st;
+  const long long ctas = static_cast<long long>(B) * (gmax + 1) * geo.csize;
+  if (ctas >= (1LL << 31)) return fail(SSD_ERR_SHAPE, "grid too large");
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  VerifyArgs a;
+  a.target = target;
+  a.draft = draft;
+  a.draft_tokens = draft_tokens;
+  a.B = B;
+  a.gmax = gmax;
+  a.gamma = gamma;
+  a.temps = temps;
+  a.temp_scalar = temp_scalar;
+  a.seed = seed;
+  a.out_tokens = out_tokens;
+  a.n_accepted = n_accepted;
+  a.status = reinterpret_cast<int32_t*>(ws + L.status);
+  a.ticket = reinterpret_cast<int32_t*>(ws + L.ticket);
+  a.unit_flag = reinterpret_cast<int32_t*>(ws + L.unit_flag);
+  a.unit_tok = reinterpret_cast<int32_t*>(ws + L.unit_tok);
+  a.stats = stats;
+  a.force_residual = stats ? 1 : 0;
+  a.geo = geo;
+  const cudaError_t e = launch_verify(a, es, smem, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "verify launch");
+  return SSD_OK;
+}
+
+}  // namespace
+
+}  // namespace ssdv
+
+using namespace ssdv;
+
+extern "C" {
+
+size_t ssd_workspace_bytes(int B, int gamma_max) {
+  if (B < 1 || gamma_max < 0) return 0;
+  return workspace_layout(B, gamma_max).total;
+}
+
+ssd_status ssd_workspace_init(void* workspace, size_t ws_bytes, void* stream) {
+  if (!workspace) return fail(SSD_ERR_NULL, "workspace is NULL");
+  const cudaError_t e = cudaMemsetAsync(workspace, 0, ws_bytes, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "workspace memset");
+  return SSD_OK;
+}
+
+ssd_status ssd_verify(const void* target_logits, const void* draft_logits, ssd_dtype dtype,
+                      const int32_t* draft_tokens, int B, int gamma, int V, float temperature, uint64_t seed,
+                      int32_t* out_tokens, int32_t* n_accepted, void* workspace, size_t ws_bytes, void* stream) {
+  g_last_error.clear();
+  if (!temperature_valid(temperature))
+    return fail(SSD_ERR_TEMPERATURE, "temperature %g is not 0 or in [1e-6, inf)", static_cast<double>(temperature));
+  return verify_common(target_logits, draft_logits, dtype, draft_tokens, B, gamma, V, nullptr, nullptr, temperature,
+                       temperature == 0.f, seed, out_tokens, n_accepted, workspace, ws_bytes, nullptr, stream);
+}
+
+ssd_status ssd_verify_ragged(const void* target_logits, const void* draft_logits, ssd_dtype dtype,
+                             const int32_t* draft_tokens, int B, int gamma_max, int V, const int32_t* gamma,
+                             const float* temperature, uint64_t seed, int32_t* out_tokens, int32_t* n_accepted,
+                             void* workspace, size_t ws_bytes, void* stream) {
+  g_last_error.clear();
+  if (!gamma || !temperature) return fail(SSD_ERR_NULL, "gamma / temperature arrays are NULL");
+  return verify_common(target_logits, draft_logits, dtype, draft_tokens, B, gamma_max, V, gamma, temperature, 0.f,
+                       false, seed, out_tokens, n_accepted, workspace, ws_bytes, nullptr, stream);
+}
+
+ssd_status ssd_debug_rowstats(const void* target_logits, const void* draft_logits, ssd_dtype dtype,
+                              const int32_t* draft_tokens, int B, int gamma, int V, float temperature,
+                              uint64_t seed, int32_t* out_tokens, int32_t* n_accepted, float* stats, void* workspace,
+                              size_t ws_bytes, void* stream) {
+  g_last_error.clear();
+  if (!stats) return fail(SSD_ERR_NULL, "stats is NULL");
+  if (!temperature_valid(temperature))
+    return fail(SSD_ERR_TEMPERATURE, "temperature %g is not 0 or in [1e-6, inf)", static_cast<double>(temperature));
+  if (B < 1 || gamma < 0 || gamma > SSD_MAX_GAMMA) return fail(SSD_ERR_SHAPE, "bad shape");
+  const size_t n_stats = static_cast<size_t>(B) * (gamma + 1) * SSD_NSTAT_VERIFY;
+  cudaError_t e = cudaMemsetAsync(stats, 0xFF, n_stats * sizeof(float), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "stats memset");
+  return verify_common(target_logits, draft_logits, dtype, draft_tokens, B, gamma, V, nullptr, nullptr, temperature,
+                       temperature == 0.f, seed, out_tokens, n_accepted, workspace, ws_bytes, stats, stream);
+}
+
+static ssd_status saguaro_common(const void* target, const void* draft, ssd_dtype dtype, int B, int g, int V, int k,
+                                 float temperature, uint64_t seed, int32_t* bonus_topk, int32_t* tokens, float* stats,
+                                 void* stream) {
+  const int es = esize_of(dtype);
+  if (es == 0) return fail(SSD_ERR_DTYPE, "unknown dtype %d", static_cast<int>(dtype));
+  if (!target || !bonus_topk || !tokens || (g > 0 && !draft)) return fail(SSD_ERR_NULL, "a required pointer is NULL");
+  if (B < 1 || g < 0 || g > SSD_MAX_GAMMA || V < 1 || V > SSD_MAX_V || k < 1 || k > SSD_MAX_TOPK || k > V)
+    return fail(SSD_ERR_SHAPE, "bad shape B=%d gamma=%d V=%d k=%d", B, g, V, k);
+  if (!(temperature >= 1e-6f) || !isfinite(temperature))
+    return fail(SSD_ERR_TEMPERATURE, "Saguaro needs a temperature in [1e-6, inf), got %g",
+                static_cast<double>(temperature));
+  if (!aligned_to(target, es) || (draft && !aligned_to(draft, es)) || !aligned_to(bonus_topk, 4) ||
+      !aligned_to(tokens, 4) || (stats && !aligned_to(stats, 4)))
+    return fail(SSD_ERR_ALIGN, "a pointer is not aligned to its element size");
+  const bool aligned =
+      aligned_to(target, 16) && (!draft || aligned_to(draft, 16)) && ((static_cast<size_t>(V) * es) % 16 == 0);
+  Geometry geo;
+  int smem = 0;
+  ssd_status st = choose_geometry(V, es, aligned, true, &geo, &smem);
+  if (st != SSD_OK) return st;
+  if (static_cast<long long>(B) * (g + 1) * geo.csize >= (1LL << 31)) return fail(SSD_ERR_SHAPE, "grid too large");
+  if (stats) {
+    const size_t n_stats = static_cast<size_t>(B) * (g + 1) * SSD_NSTAT_SAGUARO;
+    cudaError_t e = cudaMemsetAsync(stats, 0xFF, n_stats * sizeof(float), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "stats memset");
+  }
+  SaguaroArgs a;
+  a.target = target;
+  a.draft = draft;
+  a.B = B;
+  a.g = g;
+  a.k = k;
+  a.temperature = temperature;
+  a.seed = seed;
+  a.bonus_topk = bonus_topk;
+  a.saguaro_tokens = tokens;
+  a.stats = stats;
+  a.geo = geo;
+  const cudaError_t e = launch_saguaro(a, es, smem, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "saguaro launch");
+  return SSD_OK;
+}
+
+ssd_status ssd_saguaro_prespec(const void* target_logits, const void* draft_logits, ssd_dtype dtype, int B, int gamma,
+                               int V, int k, float temperature, uint64_t seed, int32_t* bonus_topk,
+                               int32_t* saguaro_tokens, void* stream) {
+  g_last_error.clear();
+  return saguaro_common(target_logits, draft_logits, dtype, B, gamma, V, k, temperature, seed, bonus_topk,
+                        saguaro_tokens, nullptr, stream);
+}
+
+ssd_status ssd_debug_saguaro_stats(const void* target_logits, const void* draft_logits, ssd_dtype dtype, int B,
+                                   int gamma, int V, int k, float temperature, uint64_t seed, int32_t* bonus_topk,
+                                   int32_t* saguaro_tokens, float* stats, void* stream) {
+  g_last_error.clear();
+  if (!stats) return fail(SSD_ERR_NULL, "stats is NULL");
+  return saguaro_common(target_logits, draft_logits, dtype, B, gamma, V, k, temperature, seed, bonus_topk,
+                        saguaro_tokens, stats, stream);
+}
+
+ssd_status ssd_debug_uniforms(uint64_t seed, int B, int W, float* out, void* stream) {
+  g_last_error.clear();
+  if (!out) return fail(SSD_ERR_NULL, "out is NULL");
+  if (B < 1 || W < 1 || static_cast<long long>(B) * W >= (1LL << 31)) return fail(SSD_ERR_SHAPE, "bad shape");
+  const cudaError_t e = launch_uniforms(seed, B, W, out, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "uniforms launch");
+  return SSD_OK;
+}
+
+ssd_status ssd_read_status(void* workspace, size_t ws_bytes, int* status, void* stream) {
+  g_last_error.clear();
+  if (!workspace || !status) return fail(SSD_ERR_NULL, "a required pointer is NULL");
+  if (ws_bytes < 16) return fail(SSD_ERR_WORKSPACE, "workspace too small");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t bits = 0;
+  cudaError_t e = cudaMemcpyAsync(&bits, workspace, sizeof bits, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, sizeof bits, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "status read");
+  *status = SSD_OK;
+  for (int c = 1; c < 32; ++c)
+    if (bits & (1 << c)) {
+      *status = c;
+      break;
+    }
+  return SSD_OK;
+}
+
+const char* ssd_status_str(ssd_status status) {
+  switch (status) {
+    case SSD_OK: return "SSD_OK";
+    case SSD_ERR_NULL: return "SSD_ERR_NULL: a required pointer is NULL";
+    case SSD_ERR_SHAPE: return "SSD_ERR_SHAPE: B, gamma, V or k out of range";
+    case SSD_ERR_DTYPE: return "SSD_ERR_DTYPE: unknown dtype";
+    case SSD_ERR_ALIGN: return "SSD_ERR_ALIGN: misaligned pointer";
+    case SSD_ERR_TOKEN_RANGE: return "SSD_ERR_TOKEN_RANGE: a draft token outside [0, V)";
+    case SSD_ERR_TEMPERATURE: return "SSD_ERR_TEMPERATURE: invalid temperature";
+    case SSD_ERR_CUDA: return "SSD_ERR_CUDA: a CUDA runtime call failed";
+    case SSD_ERR_UNSUPPORTED: return "SSD_ERR_UNSUPPORTED: no launch configuration fits";
+    case SSD_ERR_WORKSPACE: return "SSD_ERR_WORKSPACE: workspace missing or too small";
+    case SSD_ERR_GAMMA: return "SSD_ERR_GAMMA: a per-request gamma above gamma_max";
+    case SSD_ERR_TIMEOUT: return "SSD_ERR_TIMEOUT: a bounded wait for a bulk copy ran out";
+  }
+  return "unknown ssd_status";
+}
+
+const char* ssd_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

@@ -1,0 +1,700 @@
+// ssdv_device.cuh -- device building blocks shared by the verification and
+// Saguaro kernels: inline-PTX wrappers (mbarrier, bulk async copy, cluster
+// barrier, distributed shared memory), the Philox4x32-10 generator, row
+// staging into shared memory, the fused softmax-statistics pass, the weighted
+// pass with per-warp partial sums, and the inverse-CDF search.
+//
+// Work decomposition: one thread-block cluster per (request, position) unit.
+// CTA `rank` of the cluster owns the contiguous vocabulary slice
+// [rank * slice, rank * slice + n) of the unit's rows and keeps it resident in
+// its shared memory, so every logit is read from HBM exactly once; the
+// second and later passes (residual, Saguaro mix, CDF search) run on-chip.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "ssdv_internal.h"
+
+namespace ssdv {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kVecPerThreadStage = 2;
+constexpr int kStageBytes = kThreads * kVecPerThreadStage * 16;  // 8 KB per row per stage
+constexpr int kMaxStages = 32;
+constexpr uint32_t kWaitLimit = 1u << 24;  // bounded polls of an mbarrier
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---------------------------------------------------------------------------
+// Element types: bf16 is handled as its raw 16-bit pattern.
+// ---------------------------------------------------------------------------
+template <typename E>
+struct Elem;
+template <>
+struct Elem<uint16_t> {
+  static constexpr int kVec = 8;  // elements per 16-byte vector
+  static __device__ __forceinline__ float to_float(uint16_t h) {
+    return __uint_as_float(static_cast<uint32_t>(h) << 16);
+  }
+  static __device__ __forceinline__ uint16_t neg_inf() { return 0xFF80u; }
+  static __device__ __forceinline__ void unpack(const uint4& v, float (&f)[8]) {
+    f[0] = __uint_as_float(v.x << 16);
+    f[1] = __uint_as_float(v.x & 0xFFFF0000u);
+    f[2] = __uint_as_float(v.y << 16);
+    f[3] = __uint_as_float(v.y & 0xFFFF0000u);
+    f[4] = __uint_as_float(v.z << 16);
+    f[5] = __uint_as_float(v.z & 0xFFFF0000u);
+    f[6] = __uint_as_float(v.w << 16);
+    f[7] = __uint_as_float(v.w & 0xFFFF0000u);
+  }
+};
+template <>
+struct Elem<float> {
+  static constexpr int kVec = 4;
+  static __device__ __forceinline__ float to_float(float x) { return x; }
+  static __device__ __forceinline__ float neg_inf() { return -INFINITY; }
+  static __device__ __forceinline__ void unpack(const uint4& v, float (&f)[4]) {
+    f[0] = __uint_as_float(v.x);
+    f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z);
+    f[3] = __uint_as_float(v.w);
+  }
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Bounded wait for phase `parity` of an mbarrier; false if the bound ran out.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  for (uint32_t it = 0; it < kWaitLimit; ++it)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// Bulk asynchronous copy global -> this CTA's shared memory, completing on an
+// mbarrier.  dst, src 16-byte aligned; bytes a positive multiple of 16.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                              uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Full cluster barrier with release/acquire semantics (all threads call it).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of the same shared variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t dsmem_addr(const void* local, uint32_t rank) {
+  uint32_t out;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(smem_addr(local)), "r"(rank));
+  return out;
+}
+__device__ __forceinline__ float dsmem_ld_f32(uint32_t a) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ double dsmem_ld_f64(uint32_t a) {
+  double v;
+  asm volatile("ld.shared::cluster.f64 %0, [%1];" : "=d"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ int dsmem_ld_s32(uint32_t a) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ int ld_volatile(const int32_t* p) { return *reinterpret_cast<const volatile int32_t*>(p); }
+
+// ---------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11).  Key = (seed lo, seed hi),
+// counter = (request, position, 0, 0).  Word d is the uniform of draw d.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t a0 = 0xD2511F53u * c.x, h0 = __umulhi(0xD2511F53u, c.x);
+    const uint32_t a1 = 0xCD9E8D57u * c.z, h1 = __umulhi(0xCD9E8D57u, c.z);
+    c = make_uint4(h1 ^ c.y ^ k0, a1, h0 ^ c.w ^ k1, a0);
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return c;
+}
+
+__device__ __forceinline__ float word_to_uniform(uint32_t w) { return static_cast<float>(w >> 8) * 0x1p-24f; }
+
+struct Draws {
+  float accept, resample, saguaro;
+};
+__device__ __forceinline__ Draws unit_draws(uint64_t seed, int b, int i) {
+  const uint4 w = philox4x32_10(make_uint4(static_cast<uint32_t>(b), static_cast<uint32_t>(i), 0u, 0u),
+                                static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
+  return Draws{word_to_uniform(w.x), word_to_uniform(w.y), word_to_uniform(w.z)};
+}
+
+// ---------------------------------------------------------------------------
+// Softmax statistics: (m, s) with s = sum exp2(x*c - fl(m*c)), c = log2(e)/T.
+// Partial pairs combine exactly as the terms were formed, so the combined s
+// equals sum exp2(x*c - fl(M*c)) up to rounding.
+// ---------------------------------------------------------------------------
+struct MaxSum {
+  float m, s;
+};
+// fl(m * c) without contraction into a neighbouring add: every term and every
+// rescale factor of a row uses this same rounded product.
+__device__ __forceinline__ float scaled_max(float m, float c) { return __fmul_rn(m, c); }
+// exp2(fl(m_from*c) - fl(m_to*c)): moves a partial sum from one reference max to another.
+__device__ __forceinline__ float rescale(float m_from, float m_to, float c) {
+  return exp2f(__fsub_rn(scaled_max(m_from, c), scaled_max(m_to, c)));
+}
+__device__ __forceinline__ MaxSum combine_ms(MaxSum a, MaxSum b, float c) {
+  const float M = fmaxf(a.m, b.m);
+  if (M == -INFINITY) return MaxSum{M, 0.f};
+  const float sa = (a.m == -INFINITY) ? 0.f : a.s * rescale(a.m, M, c);
+  const float sb = (b.m == -INFINITY) ? 0.f : b.s * rescale(b.m, M, c);
+  return MaxSum{M, sa + sb};
+}
+
+struct ArgMax {
+  float v;
+  int i;  // -1 = empty
+};
+__device__ __forceinline__ ArgMax better_arg(ArgMax a, ArgMax b) {
+  if (a.i < 0) return b;
+  if (b.i < 0) return a;
+  if (b.v > a.v || (b.v == a.v && b.i < a.i)) return b;
+  return a;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+// Pairwise sum of a small fixed-size array.
+template <int N>
+__device__ __forceinline__ float pair_sum(const float (&a)[N]) {
+  if constexpr (N == 8) {
+    return ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+  } else {
+    return (a[0] + a[1]) + (a[2] + a[3]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Slice staging.  The caller owns `bars` (kMaxStages mbarriers) in shared
+// memory.  Bulk path: thread 0 issues, per stage, one copy per row; every
+// thread later waits on the stage's barrier.  Plain path (rows not 16-byte
+// aligned): all threads copy with ordinary loads, padding the slice to a whole
+// vector with -inf, then the block synchronises.
+// ---------------------------------------------------------------------------
+template <typename E>
+struct Slice {
+  const E* gt;  // global target slice start (row + lo)
+  const E* gd;  // global draft slice start, or nullptr
+  E* st;        // shared target slice
+  E* sd;        // shared draft slice (valid when gd)
+  int n;        // elements in this CTA's slice (may be 0)
+  int nvec;     // ceil(n / kVec)
+  int nstage;   // stages covering nvec
+  bool bulk;
+};
+
+template <typename E>
+__device__ __forceinline__ void stage_issue(const Slice<E>& sl, uint64_t* bars, int stage_elems) {
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < sl.nstage; ++s) mbar_init(&bars[s], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (sl.bulk) {
+    if (threadIdx.x == 0) {
+      const uint64_t pol = l2_policy_evict_first();
+      for (int s = 0; s < sl.nstage; ++s) {
+        const int e0 = s * stage_elems;
+        const int ne = min(stage_elems, sl.n - e0);
+        const uint32_t bytes = static_cast<uint32_t>(ne) * sizeof(E);
+        mbar_arrive_expect_tx(&bars[s], sl.gd ? 2 * bytes : bytes);
+        bulk_copy_g2s(sl.st + e0, sl.gt + e0, bytes, &bars[s], pol);
+        if (sl.gd) bulk_copy_g2s(sl.sd + e0, sl.gd + e0, bytes, &bars[s], pol);
+      }
+    }
+  } else {
+    constexpr int kVec = Elem<E>::kVec;
+    const int padded = sl.nvec * kVec;
+    for (int e = threadIdx.x; e < padded; e += kThreads) {
+      sl.st[e] = e < sl.n ? sl.gt[e] : Elem<E>::neg_inf();
+      if (sl.gd) sl.sd[e] = e < sl.n ? sl.gd[e] : Elem<E>::neg_inf();
+    }
+    __syncthreads();
+  }
+}
+
+// Wait for stage s (bulk path).  Returns false when the bounded wait ran out.
+template <typename E>
+__device__ __forceinline__ bool stage_wait(const Slice<E>& sl, uint64_t* bars, int s) {
+  if (!sl.bulk) return true;
+  return mbar_wait_bounded(&bars[s], 0);
+}
+
+// After a timeout: give the copies still in flight a bounded chance to land
+// before the CTA leaves (its shared memory is their destination).
+template <typename E>
+__device__ __forceinline__ void stage_drain(const Slice<E>& sl, uint64_t* bars) {
+  if (!sl.bulk || threadIdx.x != 0) return;
+  for (int s = 0; s < sl.nstage; ++s) mbar_wait_bounded(&bars[s], 0);
+}
+
+template <typename E>
+__device__ __forceinline__ void load_vec(const E* base, int v, float (&f)[Elem<E>::kVec]) {
+  const uint4 raw = reinterpret_cast<const uint4*>(base)[v];
+  Elem<E>::unpack(raw, f);
+}
+
+// ---------------------------------------------------------------------------
+// Statistics pass over the staged slice, stage by stage as the copies land.
+// Target: (m, s) at scale c (if want_exp) and the argmax (if want_arg);
+// draft: (m, s) when sl.gd.  Results are per thread.
+// ---------------------------------------------------------------------------
+template <typename E>
+struct ThreadStats {
+  MaxSum t, d;
+  ArgMax a;
+  bool timeout;
+};
+
+template <typename E>
+__device__ __forceinline__ ThreadStats<E> stats_pass(const Slice<E>& sl, uint64_t* bars, int stage_vecs, float c,
+                                                     bool want_exp, bool want_arg, int lo) {
+  constexpr int kVec = Elem<E>::kVec;
+  ThreadStats<E> r{{-INFINITY, 0.f}, {-INFINITY, 0.f}, {-INFINITY, -1}, false};
+  for (int s = 0; s < sl.nstage; ++s) {
+    if (!stage_wait(sl, bars, s)) r.timeout = true;
+    const int v_end = min(sl.nvec, (s + 1) * stage_vecs);
+    float ft[kVecPerThreadStage][kVec], fd[kVecPerThreadStage][kVec];
+    bool have[kVecPerThreadStage];
+    float lmt = -INFINITY, lmd = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < kVecPerThreadStage; ++k) {
+      const int v = s * stage_vecs + k * kThreads + threadIdx.x;
+      have[k] = v < v_end;
+      if (have[k]) {
+        load_vec(sl.st, v, ft[k]);
+        if (sl.gd) load_vec(sl.sd, v, fd[k]);
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) {
+          lmt = fmaxf(lmt, ft[k][e]);
+          if (sl.gd) lmd = fmaxf(lmd, fd[k][e]);
+        }
+        if (want_arg) {
+#pragma unroll
+          for (int e = 0; e < kVec; ++e) {
+            if (r.a.i < 0 || ft[k][e] > r.a.v) {
+              r.a.v = ft[k][e];
+              r.a.i = lo + v * kVec + e;
+            }
+          }
+        }
+      }
+    }
+    if (!want_exp) continue;
+    if (lmt > r.t.m) {
+      r.t.s = (r.t.m == -INFINITY) ? 0.f : r.t.s * rescale(r.t.m, lmt, c);
+      r.t.m = lmt;
+    }
+    if (sl.gd && lmd > r.d.m) {
+      r.d.s = (r.d.m == -INFINITY) ? 0.f : r.d.s * rescale(r.d.m, lmd, c);
+      r.d.m = lmd;
+    }
+    const float mct = scaled_max(r.t.m, c), mcd = scaled_max(r.d.m, c);
+#pragma unroll
+    for (int k = 0; k < kVecPerThreadStage; ++k) {
+      if (!have[k]) continue;
+      float et[kVec];
+#pragma unroll
+      for (int e = 0; e < kVec; ++e) et[e] = exp2f(fmaf(ft[k][e], c, -mct));
+      r.t.s += pair_sum(et);
+      if (sl.gd) {
+        float ed[kVec];
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) ed[e] = exp2f(fmaf(fd[k][e], c, -mcd));
+        r.d.s += pair_sum(ed);
+      }
+    }
+  }
+  return r;
+}
+
+// Block reduction of per-thread statistics into thread 0 (fixed order).
+struct BlockStats {
+  MaxSum t, d;
+  ArgMax a;
+  int timeout;
+};
+
+template <typename E>
+__device__ __forceinline__ BlockStats block_reduce_stats(const ThreadStats<E>& ts, float c, float* red_f,
+                                                         int* red_i) {
+  // red_f: 5 * kWarps floats, red_i: 2 * kWarps ints
+  MaxSum t = ts.t, d = ts.d;
+  ArgMax a = ts.a;
+  int to = ts.timeout ? 1 : 0;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    MaxSum ot{__shfl_xor_sync(0xFFFFFFFFu, t.m, o), __shfl_xor_sync(0xFFFFFFFFu, t.s, o)};
+    MaxSum od{__shfl_xor_sync(0xFFFFFFFFu, d.m, o), __shfl_xor_sync(0xFFFFFFFFu, d.s, o)};
+    ArgMax oa{__shfl_xor_sync(0xFFFFFFFFu, a.v, o), __shfl_xor_sync(0xFFFFFFFFu, a.i, o)};
+    t = combine_ms(t, ot, c);
+    d = combine_ms(d, od, c);
+    a = better_arg(a, oa);
+    to |= __shfl_xor_sync(0xFFFFFFFFu, to, o);
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+    red_f[0 * kWarps + warp] = t.m;
+    red_f[1 * kWarps + warp] = t.s;
+    red_f[2 * kWarps + warp] = d.m;
+    red_f[3 * kWarps + warp] = d.s;
+    red_f[4 * kWarps + warp] = a.v;
+    red_i[0 * kWarps + warp] = a.i;
+    red_i[1 * kWarps + warp] = to;
+  }
+  __syncthreads();
+  BlockStats out{{-INFINITY, 0.f}, {-INFINITY, 0.f}, {-INFINITY, -1}, 0};
+  if (threadIdx.x == 0) {
+    for (int w = 0; w < kWarps; ++w) {
+      out.t = combine_ms(out.t, MaxSum{red_f[0 * kWarps + w], red_f[1 * kWarps + w]}, c);
+      out.d = combine_ms(out.d, MaxSum{red_f[2 * kWarps + w], red_f[3 * kWarps + w]}, c);
+      out.a = better_arg(out.a, ArgMax{red_f[4 * kWarps + w], red_i[0 * kWarps + w]});
+      out.timeout |= red_i[1 * kWarps + w];
+    }
+  }
+  return out;
+}
+
+// Shared-memory record each CTA publishes to its cluster.
+struct Part {
+  float tm, ts, dm, ds, av;
+  int ai, timeout, pad;
+  double sum[3];  // per-pass CTA sums of weights
+  float topv[SSD_MAX_TOPK];
+  int topi[SSD_MAX_TOPK];
+};
+
+// Thread 0: combine every CTA's published statistics in rank order.
+__device__ __forceinline__ BlockStats cluster_combine_stats(const Part* part, int csize, float c) {
+  BlockStats out{{-INFINITY, 0.f}, {-INFINITY, 0.f}, {-INFINITY, -1}, 0};
+  for (int r = 0; r < csize; ++r) {
+    MaxSum t{dsmem_ld_f32(dsmem_addr(&part->tm, r)), dsmem_ld_f32(dsmem_addr(&part->ts, r))};
+    MaxSum d{dsmem_ld_f32(dsmem_addr(&part->dm, r)), dsmem_ld_f32(dsmem_addr(&part->ds, r))};
+    ArgMax a{dsmem_ld_f32(dsmem_addr(&part->av, r)), dsmem_ld_s32(dsmem_addr(&part->ai, r))};
+    out.t = combine_ms(out.t, t, c);
+    out.d = combine_ms(out.d, d, c);
+    out.a = better_arg(out.a, a);
+    out.timeout |= dsmem_ld_s32(dsmem_addr(&part->timeout, r));
+  }
+  return out;
+}
+
+// ---------------------------------------------------------------------------
+// Weighted pass: each warp owns a contiguous run of vectors of the slice (its
+// lanes interleave inside the run, so the shared-memory reads are conflict
+// free).  wfun(xt[], xd[], w[]) turns one vector into kVec weights.  Writes the
+// per-warp sums to wsum[] and returns the CTA sum (thread 0, fp64 over warps).
+// If TOPK > 0, each lane also keeps its TOPK largest (weight, token) pairs.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void warp_range(int nvec, int warp, int& v0, int& v1) {
+  const int per = (nvec + kWarps - 1) / kWarps;
+  v0 = min(nvec, warp * per);
+  v1 = min(nvec, v0 + per);
+}
+
+template <int K>
+struct TopK {
+  float v[K > 0 ? K : 1];
+  int i[K > 0 ? K : 1];
+  __device__ __forceinline__ void init() {
+#pragma unroll
+    for (int s = 0; s < (K > 0 ? K : 1); ++s) {
+      v[s] = -1.f;
+      i[s] = 0x7FFFFFFF;
+    }
+  }
+  // Insert (w, idx); indices arrive in increasing order per lane, so an equal
+  // weight never displaces an earlier (lower-index) entry.
+  __device__ __forceinline__ void push(float w, int idx) {
+    if constexpr (K > 0) {
+      if (!(w > v[K - 1])) return;
+#pragma unroll
+      for (int s = K - 1; s >= 0; --s) {
+        const float pv = (s > 0) ? v[s - 1] : INFINITY;
+        const int pi = (s > 0) ? i[s - 1] : 0;
+        if (w > pv) {
+          v[s] = pv;
+          i[s] = pi;
+        } else if (w > v[s]) {
+          v[s] = w;
+          i[s] = idx;
+        }
+      }
+    }
+  }
+  __device__ __forceinline__ void pop() {
+#pragma unroll
+    for (int s = 0; s < (K > 0 ? K : 1) - 1; ++s) {
+      v[s] = v[s + 1];
+      i[s] = i[s + 1];
+    }
+    v[(K > 0 ? K : 1) - 1] = -1.f;
+    i[(K > 0 ? K : 1) - 1] = 0x7FFFFFFF;
+  }
+};
+
+__device__ __forceinline__ bool ranks_before(float v1, int i1, float v2, int i2) {
+  return v1 > v2 || (v1 == v2 && i1 < i2);
+}
+
+template <typename E, int K, typename WFun>
+__device__ __forceinline__ double weighted_pass(const Slice<E>& sl, int lo, const WFun& wfun, float* wsum,
+                                                TopK<K>& tk) {
+  constexpr int kVec = Elem<E>::kVec;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int v0, v1;
+  warp_range(sl.nvec, warp, v0, v1);
+  float acc = 0.f;
+  for (int v = v0 + lane; v < v1; v += 32) {
+    float xt[kVec], xd[kVec], w[kVec];
+    load_vec(sl.st, v, xt);
+    if (sl.gd) load_vec(sl.sd, v, xd);
+    wfun(xt, xd, w);
+    acc += pair_sum(w);
+    if constexpr (K > 0) {
+#pragma unroll
+      for (int e = 0; e < kVec; ++e) tk.push(w[e], lo + v * kVec + e);
+    }
+  }
+  acc = warp_sum(acc);
+  if (lane == 0) wsum[warp] = acc;
+  __syncthreads();
+  double cta = 0.0;
+  if (threadIdx.x == 0)
+    for (int w = 0; w < kWarps; ++w) cta += static_cast<double>(wsum[w]);
+  return cta;
+}
+
+// Merge the lanes' top-K lists of one warp; every lane returns the warp's
+// list in `out` (descending, lower index first among equals).
+template <int K>
+__device__ __forceinline__ void warp_merge_topk(TopK<K>& tk, float (&ov)[K], int (&oi)[K]) {
+#pragma unroll
+  for (int r = 0; r < K; ++r) {
+    float v = tk.v[0];
+    int id = tk.i[0];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float v2 = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+      const int i2 = __shfl_xor_sync(0xFFFFFFFFu, id, o);
+      if (ranks_before(v2, i2, v, id)) {
+        v = v2;
+        id = i2;
+      }
+    }
+    ov[r] = v;
+    oi[r] = id;
+    if (tk.i[0] == id && tk.v[0] == v && id != 0x7FFFFFFF) tk.pop();
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Inverse-CDF search inside this CTA's slice for the local target tl (the
+// global target minus the weight of the CTAs before this one).  Thread 0
+// picks the warp from wsum[]; that warp rescans its run with a warp prefix
+// scan and fp64 carries.  If rounding leaves the target beyond every
+// boundary, the last element with positive weight is taken.  Returns the
+// global token in thread 0 (via *result in shared memory).
+// ---------------------------------------------------------------------------
+template <typename E, typename WFun>
+__device__ __forceinline__ void cdf_search(const Slice<E>& sl, int lo, const WFun& wfun, const float* wsum, double tl,
+                                           int* sh_warp, double* sh_base, int* result) {
+  constexpr int kVec = Elem<E>::kVec;
+  if (threadIdx.x == 0) {
+    double acc = 0.0;
+    int pick = -1, last_pos = -1;
+    double pick_base = 0.0, last_base = 0.0;
+    for (int w = 0; w < kWarps; ++w) {
+      const double ws = static_cast<double>(wsum[w]);
+      if (ws > 0.0) {
+        last_pos = w;
+        last_base = acc;
+      }
+      if (pick < 0 && ws > 0.0 && tl < acc + ws) {
+        pick = w;
+        pick_base = acc;
+      }
+      acc += ws;
+    }
+    if (pick < 0) {
+      pick = last_pos;
+      pick_base = last_base;
+    }
+    *sh_warp = pick;
+    *sh_base = pick_base;
+    *result = -1;
+  }
+  __syncthreads();
+  const int pick = *sh_warp;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (pick >= 0 && warp == pick) {
+    int v0, v1;
+    warp_range(sl.nvec, warp, v0, v1);
+    double carry = *sh_base;
+    int found = -1;
+    int last_vec = -1;  // last vector in the run with positive weight
+    for (int vb = v0; vb < v1 && found < 0; vb += 32) {
+      const int v = vb + lane;
+      float w[kVec];
+      float vs = 0.f;
+      if (v < v1) {
+        float xt[kVec], xd[kVec];
+        load_vec(sl.st, v, xt);
+        if (sl.gd) load_vec(sl.sd, v, xd);
+        wfun(xt, xd, w);
+        vs = pair_sum(w);
+      } else {
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) w[e] = 0.f;
+      }
+      float incl = vs;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const float total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+      const unsigned pos = __ballot_sync(0xFFFFFFFFu, vs > 0.f);
+      if (pos) last_vec = vb + 31 - __clz(pos);
+      const bool hit = (vs > 0.f) && (tl < carry + static_cast<double>(incl));
+      const unsigned hm = __ballot_sync(0xFFFFFFFFu, hit);
+      if (hm) {
+        const int L = __ffs(hm) - 1;
+        int tok = -1;
+        if (lane == L) {
+          double a = carry + static_cast<double>(incl - vs);
+          int last_e = -1;
+#pragma unroll
+          for (int e = 0; e < kVec; ++e) {
+            if (w[e] > 0.f) last_e = e;
+            a += static_cast<double>(w[e]);
+            if (tok < 0 && w[e] > 0.f && tl < a) tok = e;
+          }
+          if (tok < 0) tok = last_e;
+          tok = v * kVec + tok;
+        }
+        found = __shfl_sync(0xFFFFFFFFu, tok, L);
+      }
+      carry += static_cast<double>(total);
+    }
+    if (found < 0 && last_vec >= 0 && lane == 0) {
+      float xt[kVec], xd[kVec], w[kVec];
+      load_vec(sl.st, last_vec, xt);
+      if (sl.gd) load_vec(sl.sd, last_vec, xd);
+      wfun(xt, xd, w);
+      int last_e = kVec - 1;
+#pragma unroll
+      for (int e = 0; e < kVec; ++e)
+        if (w[e] > 0.f) last_e = e;
+      found = last_vec * kVec + last_e;
+    }
+    if (lane == 0) *result = found >= 0 ? lo + found : -1;
+  }
+  __syncthreads();
+}
+
+// Thread 0: cluster totals of pass `p` (CTA sums in rank order), the global
+// target u * total, and which CTA owns it.  Returns the total; *owner gets the
+// rank (-1 if the total is not positive), *local the target minus the weight
+// of the ranks before the owner.
+__device__ __forceinline__ double cluster_locate(const Part* part, int csize, int p, double u, int* owner,
+                                                 double* local) {
+  double tot = 0.0;
+  double sums[16];
+  for (int r = 0; r < csize; ++r) {
+    sums[r] = dsmem_ld_f64(dsmem_addr(&part->sum[p], r));
+    tot += sums[r];
+  }
+  *owner = -1;
+  *local = 0.0;
+  if (!(tot > 0.0)) return tot;
+  const double target = u * tot;
+  double acc = 0.0;
+  int last_pos = -1;
+  double last_acc = 0.0;
+  for (int r = 0; r < csize; ++r) {
+    if (sums[r] > 0.0) {
+      last_pos = r;
+      last_acc = acc;
+      if (*owner < 0 && target < acc + sums[r]) {
+        *owner = r;
+        *local = target - acc;
+      }
+    }
+    acc += sums[r];
+  }
+  if (*owner < 0) {
+    *owner = last_pos;
+    *local = target - last_acc;
+  }
+  return tot;
+}
+
+}  // namespace ssdv

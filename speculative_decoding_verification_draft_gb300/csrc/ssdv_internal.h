@@ -1,0 +1,72 @@
+// ssdv_internal.h -- launch arguments shared by the host launchers and the
+// kernels of libssdv (not part of the public ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "ssdv.h"
+
+namespace ssdv {
+
+// How a unit's rows are split across the CTAs of its cluster.
+struct Geometry {
+  int V;            // vocabulary size
+  int slice;        // elements per CTA slice, a multiple of 8 (16 bytes for bf16 and fp32)
+  int csize;        // CTAs per cluster (1..16)
+  int row_smem;     // shared-memory bytes reserved per staged row slice
+  int stage_elems;  // elements per staged copy (one stage)
+  int bulk;         // 1: rows 16-byte aligned, staged with bulk async copies
+};
+
+struct VerifyArgs {
+  const void* target;          // [B, gmax+1, V]
+  const void* draft;           // [B, gmax, V] (may be null if every request is greedy)
+  const int32_t* draft_tokens; // [B, gmax]
+  int B, gmax;
+  const int32_t* gamma;        // [B] or null (every request uses gmax)
+  const float* temps;          // [B] or null (temp_scalar)
+  float temp_scalar;
+  uint64_t seed;
+  int32_t* out_tokens;         // [B, gmax+1]
+  int32_t* n_accepted;         // [B]
+  int32_t* ticket;             // [B]        workspace: arrivals per request
+  int32_t* unit_flag;          // [B, gmax+1] workspace: 1 accept, 0 reject, -1 error
+  int32_t* unit_tok;           // [B, gmax+1] workspace: correction / bonus / greedy token
+  int32_t* status;             // [1]        workspace: device error bits
+  float* stats;                // [B, gmax+1, SSD_NSTAT_VERIFY] or null (debug)
+  int force_residual;          // debug: residual pass at every position
+  Geometry geo;
+};
+
+struct SaguaroArgs {
+  const void* target;  // [B, g+1, V]
+  const void* draft;   // [B, g, V]
+  int B, g, k;
+  float temperature;
+  uint64_t seed;
+  int32_t* bonus_topk;      // [B, g+1, k]
+  int32_t* saguaro_tokens;  // [B, g+1]
+  float* stats;             // [B, g+1, SSD_NSTAT_SAGUARO] or null
+  Geometry geo;
+};
+
+// Workspace layout (byte offsets), shared by the launchers and the API.
+struct WorkspaceLayout {
+  size_t status, ticket, unit_flag, unit_tok, total;
+};
+WorkspaceLayout workspace_layout(int B, int gmax);
+
+// Launch configuration for one call; returns SSD_OK or an error.
+ssd_status choose_geometry(int V, int esize, bool aligned, bool two_rows, Geometry* geo, int* smem_bytes);
+
+cudaError_t launch_verify(const VerifyArgs& a, int esize, int smem_bytes, cudaStream_t stream);
+cudaError_t launch_saguaro(const SaguaroArgs& a, int esize, int smem_bytes, cudaStream_t stream);
+
+cudaError_t launch_uniforms(uint64_t seed, int B, int W, float* out, cudaStream_t stream);
+
+// Largest dynamic shared memory one CTA may use (bytes).
+int max_dynamic_smem();
+
+}  // namespace ssdv

@@ -1,0 +1,68 @@
+"""The C-ABI library builds, loads and exports every entry point declared in
+include/ssdv.h; host-side validation answers without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ssdv.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ssd_[a-z_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from speculative_decoding_verification_draft_gb300 import build
+    try:
+        build.nvcc()
+    except RuntimeError:
+        pytest.skip("nvcc not available")
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for want in ("ssd_verify", "ssd_verify_ragged", "ssd_saguaro_prespec", "ssd_workspace_bytes",
+                 "ssd_workspace_init", "ssd_debug_rowstats", "ssd_debug_saguaro_stats",
+                 "ssd_debug_uniforms", "ssd_read_status", "ssd_status_str", "ssd_last_error"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"libssdv.so does not export {name}"
+
+
+def test_host_validation_without_gpu(lib):
+    from speculative_decoding_verification_draft_gb300 import ssdv
+    L = ssdv._declare(lib)
+    assert L.ssd_workspace_bytes(64, 4) >= 16 + 4 * 64 + 2 * 4 * 64 * 5
+    assert L.ssd_workspace_bytes(0, 4) == 0
+    # temperature rejected first
+    assert L.ssd_verify(None, None, 0, None, 1, 1, 8, -1.0, 0, None, None, None, 0, None) == 6
+    assert L.ssd_verify(None, None, 0, None, 1, 1, 8, float("nan"), 0, None, None, None, 0, None) == 6
+    assert L.ssd_verify(None, None, 0, None, 1, 1, 8, 1e-9, 0, None, None, None, 0, None) == 6
+    # unknown dtype, NULL pointers
+    assert L.ssd_verify(None, None, 7, None, 1, 1, 8, 1.0, 0, None, None, None, 0, None) == 3
+    assert L.ssd_verify(None, None, 0, None, 1, 1, 8, 1.0, 0, None, None, None, 0, None) == 1
+    assert b"NULL" in L.ssd_last_error()
+    # shape checks run before any device query
+    p = ctypes.c_void_p(16)
+    assert L.ssd_verify(p, p, 0, p, 0, 1, 8, 1.0, 0, p, p, p, 1 << 20, None) == 2
+    assert L.ssd_verify(p, p, 0, p, 1, 33, 8, 1.0, 0, p, p, p, 1 << 20, None) == 2
+    # misaligned bf16 pointer, small workspace
+    odd = ctypes.c_void_p(17)
+    assert L.ssd_verify(odd, p, 0, p, 1, 1, 8, 1.0, 0, p, p, p, 1 << 20, None) == 4
+    assert L.ssd_verify(p, p, 0, p, 4, 2, 8, 1.0, 0, p, p, p, 8, None) == 9
+    # Saguaro: k and temperature
+    assert L.ssd_saguaro_prespec(p, p, 0, 1, 1, 8, 9, 1.0, 0, p, p, None) == 2
+    assert L.ssd_saguaro_prespec(p, p, 0, 1, 1, 8, 3, 0.0, 0, p, p, None) == 6
+    for code in range(12):
+        assert L.ssd_status_str(code).startswith(b"SSD_")

@@ -1,0 +1,134 @@
+"""GPU Saguaro pre-speculation kernel vs the fp64 oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import gpu_common as gc
+import pins
+from speculative_decoding_verification_draft_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+TOPK_REL, TOPK_ABS = 1e-5, 2e-6
+
+
+@pytest.fixture(scope="module")
+def ssdv():
+    return gc.cuda_lib()
+
+
+def widen(arr, dtype):
+    if arr.dtype == np.uint16:
+        return (arr.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return arr.astype(np.float64)
+
+
+def assert_saguaro_parity(batch, k, T, seed, topk_g, tok_g, stats_g=None, subset=None, what=""):
+    """Top-k slots: exact where the oracle does not flag them; where it does,
+    the GPU's token must carry (per the oracle) the slot's value within the
+    top-k tolerance.  Tokens: exact unless the draw is flagged.  Statistics:
+    log-sums 1e-5, residual mass 1e-5 relative (+2e-6), Zs and p_saguaro of
+    the drawn token 1e-5 relative."""
+    o = gc.orc()
+    tgt, dft = batch.numpy_logits()
+    idx = np.arange(batch.B) if subset is None else np.asarray(subset)
+    ref = o.saguaro_batch(tgt[idx], dft[idx], k, T, seed, stats=stats_g is not None, nthreads=16, req_ids=idx)
+    topk_g = topk_g[idx]
+    tok_g = tok_g[idx]
+    flagged_tok = 0
+    g = batch.gmax
+    for r, b in enumerate(idx):
+        for j in range(g + 1):
+            want = ref["bonus_topk"][r, j]
+            got = topk_g[r, j]
+            flags = ref["topk_flag"][r, j]
+            if flags == 0:
+                assert np.array_equal(got, want), f"{what}: topk b={b} j={j} gpu {got} oracle {want}"
+            else:
+                rr, _ = o.saguaro_position(widen(tgt[b, j], tgt.dtype),
+                                           None if j == g else widen(dft[b, j], dft.dtype), T)
+                for s in range(k):
+                    if flags & (1 << s):
+                        a, c = rr[got[s]], rr[want[s]]
+                        assert abs(a - c) <= TOPK_REL * c + TOPK_ABS, f"{what}: flagged slot b={b} j={j} s={s}"
+                    else:
+                        assert got[s] == want[s], f"{what}: topk b={b} j={j} slot {s}"
+            if ref["tok_flag"][r, j]:
+                flagged_tok += 1
+            else:
+                assert tok_g[r, j] == ref["saguaro_tokens"][r, j], (
+                    f"{what}: token b={b} j={j} gpu {tok_g[r, j]} oracle {ref['saguaro_tokens'][r, j]}")
+    assert flagged_tok <= max(1, 1e-4 * len(idx) * (g + 1))
+    if stats_g is not None:
+        sg = stats_g[idx].astype(np.float64)
+        so = ref["stats"]
+        assert np.abs(sg[:, :, 0] - so[:, :, 0]).max() < 1e-5, f"{what}: target log-sum"
+        if g > 0:
+            assert np.abs(sg[:, :g, 1] - so[:, :g, 1]).max() < 1e-5, f"{what}: draft log-sum"
+        dS = np.abs(sg[:, :, 2] - so[:, :, 2])
+        assert (dS <= 1e-5 * so[:, :, 2] + 2e-6).all(), f"{what}: residual mass {dS.max()}"
+        rel = np.abs(sg[:, :, 3] - so[:, :, 3]) / so[:, :, 3]
+        assert rel.max() < 1e-5, f"{what}: Zs rel {rel.max()}"
+        ok = ref["tok_flag"] == 0
+        rel = np.abs(sg[:, :, 4] - so[:, :, 4]) / so[:, :, 4]
+        assert rel[ok].max() < 1e-5, f"{what}: p_saguaro(token) rel {rel[ok].max()}"
+        rel = np.abs(sg[:, :, 5] - so[:, :, 5]) / np.maximum(so[:, :, 5], 1e-30)
+        assert (rel < 1e-5).all() or (np.abs(sg[:, :, 5] - so[:, :, 5]) < TOPK_ABS).all()
+
+
+def run(ssdv, batch, k, T, seed, stats=False):
+    b = batch.to("cuda")
+    if stats:
+        topk, tok, st = ssdv.debug_saguaro_stats(b.target, b.draft, k, T, seed)
+        torch.cuda.synchronize()
+        return topk.cpu().numpy(), tok.cpu().numpy(), st.cpu().numpy()
+    topk, tok = ssdv.saguaro_prespec(b.target, b.draft, k, T, seed)
+    torch.cuda.synchronize()
+    return topk.cpu().numpy(), tok.cpu().numpy(), None
+
+
+def test_toy_tables_topk(ssdv):
+    """The page-4 toy tables' residual top-3: token 1 first, then {2, 3}
+    (prev 0) / {2, 6} (prev != 0) -- closed forms from the printed tables."""
+    t = pins.golden("toy_tables.json")
+    lt = np.log(np.array([t["target"]["prev0"], t["target"]["other"]], np.float64)).astype(np.float32)
+    ld = np.log(np.array([t["draft"]["prev0"], t["draft"]["other"]], np.float64)).astype(np.float32)
+    target = torch.from_numpy(np.stack([np.stack([lt[0], lt[0]]), np.stack([lt[1], lt[1]])]))
+    draft = torch.from_numpy(np.stack([ld[0:1], ld[1:2]]))
+    batch = wl.Batch(target, draft, torch.zeros(2, 1, dtype=torch.int32), 1.0)
+    topk, tok, st = run(ssdv, batch, 3, 1.0, 0, stats=True)
+    assert topk[0, 0, 0] == 1 and set(topk[0, 0, 1:]) == {2, 3}
+    assert topk[1, 0, 0] == 1 and set(topk[1, 0, 1:]) == {2, 6}
+    assert abs(st[0, 0, 2] - 0.05) < 1e-6 and abs(st[1, 0, 2] - 0.04) < 1e-6
+    assert abs(st[0, 0, 5] - 0.6) < 1e-5 and abs(st[1, 0, 5] - 0.5) < 1e-5
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("V,gamma,k", [(7, 2, 3), (1000, 3, 1), (4099, 1, 8), (20000, 4, 3), (1, 1, 1)])
+def test_small_shapes(ssdv, dtype, V, gamma, k):
+    batch = wl.zipf_batch(16, gamma, V, dtype=dtype, temperature=0.8, seed=V, sigma_range=(0.6, 0.6),
+                          sample_tokens=False)
+    topk, tok, st = run(ssdv, batch, k, 0.8, 21, stats=True)
+    assert_saguaro_parity(batch, k, 0.8, 21, topk, tok, st, what=f"V={V} g={gamma} k={k} {dtype}")
+
+
+def test_equal_distributions(ssdv):
+    """q == p at every position: zero residual mass, the residual falls back to q."""
+    batch = wl.zipf_batch(8, 3, 3000, seed=5, sample_tokens=False)
+    batch.draft.copy_(batch.target[:, :3])
+    topk, tok, st = run(ssdv, batch, 3, 0.8, 2, stats=True)
+    assert np.all(st[:, :3, 2] == 0)
+    assert_saguaro_parity(batch, 3, 0.8, 2, topk, tok, st, what="q == p")
+
+
+def test_saguaro_config_full_sampled(ssdv):
+    """B=256, gamma 6, V 152064 fp32, sigma 0.6, T 0.8, k 3 (config 4):
+    GPU over the whole batch, oracle on 12 sampled requests."""
+    batch = wl.zipf_batch(256, 6, 152064, dtype=torch.float32, temperature=0.8, seed=3, sigma_range=(0.6, 0.6),
+                          sample_tokens=False)
+    topk, tok, st = run(ssdv, batch, 3, 0.8, 3, stats=True)
+    subset = np.random.default_rng(1).choice(256, 12, replace=False)
+    assert_saguaro_parity(batch, 3, 0.8, 3, topk, tok, st, subset=subset, what="config 4")
+    # product entry point agrees with the debug entry point
+    topk2, tok2, _ = run(ssdv, batch, 3, 0.8, 3)
+    assert np.array_equal(topk, topk2) and np.array_equal(tok, tok2)

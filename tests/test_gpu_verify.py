@@ -1,0 +1,239 @@
+"""GPU verification kernel vs the fp64 oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import gpu_common as gc
+import pins
+from speculative_decoding_verification_draft_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ssdv():
+    return gc.cuda_lib()
+
+
+def toy_tables():
+    return pins.golden("toy_tables.json")
+
+
+def run_verify(ssdv, batch, seed):
+    b = batch.to("cuda")
+    out, n = ssdv.verify(b.target, b.draft, b.draft_tokens, b.temperature, seed)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), n.cpu().numpy()
+
+
+def test_device_uniforms_match_oracle(ssdv):
+    """The kernels' Philox4x32-10 uniforms equal the oracle's, bit for bit."""
+    o = gc.orc()
+    for seed, B, W in [(0, 4096, 5), (2, 64, 9), ((1 << 64) - 1, 3, 33), (0xDEADBEEF12345678, 1 << 16, 40)]:
+        u = ssdv.debug_uniforms(seed, B, W).cpu().numpy().astype(np.float64)
+        for d in range(3):
+            want = o.uniform_grid(seed, B, W, d)
+            assert np.array_equal(u[:, :, d], want), (seed, d)
+
+
+def test_toy_config(ssdv):
+    """Page-4 Markov toy: 4096 rounds, gamma 4, V 7, fp32 (unaligned rows)."""
+    batch = wl.toy_batch(toy_tables(), 4096, 4, seed=0)
+    out, n = run_verify(ssdv, batch, seed=0)
+    ref = gc.verify_oracle(batch, seed=0)
+    gc.assert_verify_parity(out, n, ref, 7, "toy")
+
+
+def test_toy_unbiasedness_on_gpu(ssdv):
+    """200k GPU rounds of the toy: first-token histogram vs the target, KL < 1e-4."""
+    info = pins.golden("unbiasedness_check.json")
+    t = toy_tables()
+    batch = wl.toy_batch(t, info["draws"], 4, seed=7)
+    out, n = run_verify(ssdv, batch, seed=11)
+    q0 = np.array(t["target"]["prev0"])
+    first = np.bincount(out[:, 0], minlength=7) / len(out)
+    assert pins.kl(first, q0) < info["kl_bound"]
+    ref = gc.verify_oracle(batch, seed=11)
+    gc.assert_verify_parity(out, n, ref, 7, "toy 200k")
+
+
+def test_gaussian_config(ssdv):
+    """B=1, gamma 5, V 32000 bf16, T 1 (config 2), over 24 seeds."""
+    batch = wl.gaussian_batch(1, 5, 32000, seed=1)
+    acc = []
+    for seed in range(24):
+        out, n = run_verify(ssdv, batch, seed)
+        ref = gc.verify_oracle(batch, seed)
+        gc.assert_verify_parity(out, n, ref, 32000, f"gaussian seed {seed}")
+        acc.append(int(n[0]))
+
+
+@pytest.fixture(scope="module")
+def zipf64():
+    return wl.zipf_batch(64, 4, 128256, seed=2)
+
+
+def test_zipf_config_full(ssdv, zipf64):
+    """B=64, gamma 4, V 128256 bf16, T 0.8 (the benchmark workload), all requests."""
+    for seed in (2, 3, 4):
+        out, n = run_verify(ssdv, zipf64, seed)
+        ref = gc.verify_oracle(zipf64, seed)
+        gc.assert_verify_parity(out, n, ref, 128256, f"zipf seed {seed}")
+
+
+def test_zipf_rowstats(ssdv, zipf64):
+    """Softmax log-sums, q(x), p(x), residual mass and accept probability."""
+    b = zipf64.to("cuda")
+    out, n, st = ssdv.debug_rowstats(b.target, b.draft, b.draft_tokens, b.temperature, 2)
+    ref = gc.verify_oracle(zipf64, 2, stats=True)
+    gc.assert_stats_close(st, ref["stats"], what="zipf")
+    gc.assert_verify_parity(out, n, ref, 128256, "zipf (debug entry)")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("V", [1, 8, 1000, 4099, 33001])
+@pytest.mark.parametrize("gamma", [0, 1, 8])
+def test_small_shapes(ssdv, dtype, V, gamma):
+    """Ragged tails (V not a multiple of 8 or of the slice), gamma 0/1/8, both dtypes."""
+    batch = wl.zipf_batch(24, gamma, V, dtype=dtype, temperature=0.9, seed=V + gamma, sigma_range=(0.2, 1.4))
+    out, n = run_verify(ssdv, batch, seed=5)
+    ref = gc.verify_oracle(batch, 5)
+    gc.assert_verify_parity(out, n, ref, V, f"V={V} g={gamma} {dtype}")
+
+
+@pytest.mark.parametrize("T", [0.05, 0.7, 1.0, 2.5])
+def test_temperatures(ssdv, T):
+    batch = wl.zipf_batch(32, 4, 5000, temperature=T, seed=31)
+    b = batch.to("cuda")
+    out, n, st = ssdv.debug_rowstats(b.target, b.draft, b.draft_tokens, T, 9)
+    ref = gc.verify_oracle(batch, 9, stats=True)
+    gc.assert_verify_parity(out, n, ref, 5000, f"T={T}")
+    gc.assert_stats_close(st, ref["stats"], what=f"T={T}")
+
+
+def test_greedy_with_ties(ssdv):
+    """T = 0: integer-valued bf16 logits (many ties; lowest index wins)."""
+    g, V, B = 6, 3000, 64
+    gen = torch.Generator().manual_seed(3)
+    target = torch.randint(-4, 5, (B, g + 1, V), generator=gen).to(torch.bfloat16)
+    am = target.float().argmax(dim=-1)[:, :g]
+    flip = torch.rand(B, g, generator=gen) < 0.25
+    tok = torch.where(flip, torch.randint(0, V, (B, g), generator=gen), am).to(torch.int32)
+    draft = torch.full((B, g, V), float("nan"), dtype=torch.bfloat16)  # never read
+    batch = wl.Batch(target, draft, tok, 0.0)
+    b = batch.to("cuda")
+    out, n = ssdv.verify(b.target, None, b.draft_tokens, 0.0, 1)
+    ref = gc.verify_oracle(batch, 1)
+    gc.assert_verify_parity(out, n, ref, V, "greedy ties")
+    out2, n2, st = ssdv.debug_rowstats(b.target, None, b.draft_tokens, 0.0, 1)
+    ref2 = gc.verify_oracle(batch, 1, stats=True)
+    gc.assert_stats_close(st, ref2["stats"], greedy=True, what="greedy")
+
+
+def test_draft_equals_target(ssdv):
+    """q == p: every draft token is accepted and the bonus is drawn from q_gamma."""
+    batch = wl.zipf_batch(16, 5, 20000, seed=41)
+    batch.draft.copy_(batch.target[:, :5])
+    out, n = run_verify(ssdv, batch, 3)
+    assert np.all(n == 5)
+    ref = gc.verify_oracle(batch, 3)
+    gc.assert_verify_parity(out, n, ref, 20000, "draft == target")
+
+
+def test_minus_inf_logits(ssdv):
+    """p(x) = 0 (draft logit -inf) is accepted; q(x) = 0 (target -inf) is rejected."""
+    batch = wl.zipf_batch(8, 3, 4096, dtype=torch.float32, seed=43)
+    tok = batch.draft_tokens
+    for b in range(8):
+        x = int(tok[b, 0])
+        if b % 2 == 0:
+            batch.draft[b, 0, x] = float("-inf")
+        else:
+            batch.target[b, 0, x] = float("-inf")
+        batch.target[b, 2, :100] = float("-inf")
+    out, n = run_verify(ssdv, batch, 4)
+    assert np.all(n[0::2] >= 1) and np.all(n[1::2] == 0)
+    ref = gc.verify_oracle(batch, 4)
+    gc.assert_verify_parity(out, n, ref, 4096, "-inf logits")
+
+
+def test_ragged_small(ssdv):
+    """Ragged mixed batch: per-request gamma and temperature, NaN padding never read."""
+    batch = wl.ragged_batch(96, 8, 9000, seed=4)
+    b = batch.to("cuda")
+    out, n = ssdv.verify_ragged(b.target, b.draft, b.draft_tokens, b.gamma, b.temperature, 17)
+    ref = gc.verify_oracle(batch, 17)
+    gc.assert_verify_parity(out, n, ref, 9000, "ragged small")
+    assert ssdv.read_status() == 0
+
+
+def test_ragged_full_config_sampled(ssdv):
+    """B=512, gamma 1..8, V 128256 bf16 (config 5); oracle on 48 sampled requests."""
+    batch = wl.ragged_batch(512, 8, 128256, seed=4)
+    b = batch.to("cuda")
+    out, n = ssdv.verify_ragged(b.target, b.draft, b.draft_tokens, b.gamma, b.temperature, 4)
+    out, n = out.cpu().numpy(), n.cpu().numpy()
+    subset = np.random.default_rng(0).choice(512, 48, replace=False)
+    ref = gc.verify_oracle(batch, 4, subset=subset)
+    gc.assert_verify_parity(out[subset], n[subset], ref, 128256, "ragged full (sample)")
+    # every request's shape: n in [0, gamma_b], tokens valid, -1 after n
+    gam = batch.gamma.numpy()
+    assert np.all((n >= 0) & (n <= gam))
+    for r in range(512):
+        assert np.all(out[r, : n[r] + 1] >= 0) and np.all(out[r, n[r] + 1:] == -1)
+
+
+def test_padded_and_bad_requests(ssdv):
+    """Padded (gamma < 0), gamma > gamma_max, bad temperature and out-of-range
+    tokens give -1 outputs for that request only, and set the status word."""
+    batch = wl.ragged_batch(16, 4, 512, dtype=torch.float32, seed=5)
+    gam = batch.gamma.clone()
+    temps = batch.temperature.clone()
+    tok = batch.draft_tokens.clone()
+    gam[1] = -1          # padded
+    gam[3] = 9           # above gamma_max
+    temps[5] = -1.0      # invalid
+    gam[7] = 4
+    temps[7] = 1.0
+    tok[7, 2] = 512      # out of range
+    b = batch.to("cuda")
+    ssdv.read_status()
+    out, n = ssdv.verify_ragged(b.target, b.draft, tok.cuda(), gam.cuda(), temps.cuda(), 3)
+    out, n = out.cpu().numpy(), n.cpu().numpy()
+    for r in (1, 3, 5, 7):
+        assert n[r] == -1 and np.all(out[r] == -1), r
+    st = ssdv.read_status()
+    assert st in (5, 6, 10)  # the lowest error code seen: token range
+    assert st == 5
+    assert ssdv.read_status() == 0
+    good = [r for r in range(16) if r not in (1, 3, 5, 7)]
+    fixed = wl.Batch(batch.target, batch.draft, tok, temps, gam)
+    ref = gc.verify_oracle(fixed, 3, subset=good)
+    gc.assert_verify_parity(out[good], n[good], ref, 512, "good requests of a bad batch")
+
+
+def test_workspace_reuse_and_determinism(ssdv, zipf64):
+    """Calls on one workspace leave it reusable; same seed, same outputs."""
+    b = zipf64.to("cuda")
+    ws = ssdv.make_workspace(64, 4)
+    r1 = [t.clone() for t in ssdv.verify(b.target, b.draft, b.draft_tokens, 0.8, 5, workspace=ws)]
+    for _ in range(3):
+        r2 = ssdv.verify(b.target, b.draft, b.draft_tokens, 0.8, 5, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(r1[0], r2[0]) and torch.equal(r1[1], r2[1])
+    assert int(ws[16:16 + 4 * 64].view(torch.int32).abs().sum()) == 0  # tickets back to zero
+
+
+def test_host_side_errors(ssdv):
+    """Host validation returns distinct errors before any launch."""
+    b = wl.zipf_batch(2, 2, 64, seed=1).to("cuda")
+    with pytest.raises(ssdv.SsdError) as e:
+        ssdv.verify(b.target, b.draft, b.draft_tokens, -0.5, 1)
+    assert e.value.status == 6
+    with pytest.raises(ssdv.SsdError) as e:
+        ssdv.verify(b.target, b.draft, b.draft_tokens, 0.8, 1, workspace=torch.zeros(16, dtype=torch.uint8,
+                                                                                     device="cuda"))
+    assert e.value.status == 9
+    with pytest.raises(ssdv.SsdError) as e:
+        ssdv.verify(b.target, None, b.draft_tokens, 0.8, 1)
+    assert e.value.status == 1
