@@ -69,8 +69,8 @@ typedef enum { SSD_BF16 = 0, SSD_F32 = 1 } ssd_dtype;
 #define SSD_MAX_GAMMA 32   /* largest gamma / gamma_max accepted                 */
 #define SSD_MAX_TOPK 8     /* largest k accepted by ssd_saguaro_prespec           */
 #define SSD_MAX_V (1 << 19)  /* fp32 units above ~440k need more than 16 CTAs */
-#define SSD_NSTAT_VERIFY 8
-#define SSD_NSTAT_SAGUARO 8
+#define SSD_NSTAT_VERIFY 10
+#define SSD_NSTAT_SAGUARO 10
 
 /* Bytes of device workspace ssd_verify / ssd_verify_ragged need for a batch of
  * B requests with up to gamma_max draft tokens.  The workspace holds one
@@ -78,9 +78,10 @@ typedef enum { SSD_BF16 = 0, SSD_F32 = 1 } ssd_dtype;
 size_t ssd_workspace_bytes(int B, int gamma_max);
 
 /* Zero a workspace (asynchronous memset on `stream`).  A workspace must be
- * zeroed once before its first use; every call leaves it zeroed again, so it
- * can be reused by later calls on the same stream.  Two calls that may run at
- * the same time on the GPU need two workspaces. */
+ * zeroed once before its first use; every completed call leaves it zeroed
+ * again (except the sticky status word, see ssd_read_status), so it can be
+ * reused by later calls of any shape that fits it, on the same stream.  Two
+ * calls that may run at the same time on the GPU need two workspaces. */
 ssd_status ssd_workspace_init(void* workspace, size_t ws_bytes, void* stream);
 
 /* Batched verification, one gamma and one temperature for the whole batch.
@@ -136,12 +137,15 @@ ssd_status ssd_saguaro_prespec(const void* target_logits, const void* draft_logi
 /* Debug / parity: ssd_verify (same arguments and outputs) that also returns
  * the per-position quantities it computes, for every position whether or not
  * it is reached (the residual pass then runs at every position).
- * stats [B, gamma+1, 8] float:
+ * stats [B, gamma+1, 10] float:
  *   0 target row max (raw logit), 1 ln sum exp((x - max)/T) of the target row,
  *   2 draft row max, 3 its log-sum, 4 q_i(x_i), 5 p_i(x_i),
- *   6 residual mass sum (q_i - p_i)+, 7 accept probability min(1, q/p).
- * Row gamma fills only 0 and 1; entries that do not apply are NaN.  Greedy
- * (T == 0) fills only entry 0 (the target row max). */
+ *   6 residual mass sum (q_i - p_i)+, 7 accept probability min(1, q/p),
+ *   8, 9 the distances u - C_{k-1}/S and C_k/S - u of the resample / bonus
+ *   uniform u to the normalised CDF boundaries of the token drawn at this
+ *   position (the correction after a rejection, or the bonus).
+ * Row gamma fills only 0, 1, 8 and 9; entries that do not apply are NaN.
+ * Greedy (T == 0) fills only entry 0 (the target row max). */
 ssd_status ssd_debug_rowstats(const void* target_logits, const void* draft_logits, ssd_dtype dtype,
                               const int32_t* draft_tokens, int B, int gamma, int V,
                               float temperature, uint64_t seed, int32_t* out_tokens,
@@ -149,10 +153,12 @@ ssd_status ssd_debug_rowstats(const void* target_logits, const void* draft_logit
                               size_t ws_bytes, void* stream);
 
 /* Debug / parity: the per-position quantities ssd_saguaro_prespec computes.
- * stats [B, gamma+1, 8] float: 0 target log-sum, 1 draft log-sum (NaN at
+ * stats [B, gamma+1, 10] float: 0 target log-sum, 1 draft log-sum (NaN at
  * j = gamma), 2 residual mass S_j (1 at j = gamma), 3 Zs = sum_v sqrt(p_D(v) *
  * max(r_j(v), 1e-8)), 4 p_saguaro(token), 5 r_j of top slot 0, 6 r_j of top
- * slot k-1, 7 NaN.  Outputs as ssd_saguaro_prespec. */
+ * slot k-1, 7 NaN, 8, 9 the distances u - lo, hi - u of the Saguaro uniform to
+ * the normalised CDF boundaries of the drawn token.
+ * Outputs as ssd_saguaro_prespec. */
 ssd_status ssd_debug_saguaro_stats(const void* target_logits, const void* draft_logits,
                                    ssd_dtype dtype, int B, int gamma, int V, int k,
                                    float temperature, uint64_t seed, int32_t* bonus_topk,

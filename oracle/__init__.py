@@ -26,8 +26,8 @@ LIBRARY = os.path.join(HERE, "liboracle.so")
 
 BF16 = 0
 F32 = 1
-NSTAT_VERIFY = 8
-NSTAT_SAGUARO = 8
+NSTAT_VERIFY = 10
+NSTAT_SAGUARO = 10
 FLAG_BAND = 1e-6
 SAGUARO_CLAMP = 1e-8
 
@@ -60,16 +60,16 @@ def _declare(lib):
     lib.orc_choice.restype = c_int
     lib.orc_topk.argtypes = [P, c_int, c_int, P, P]
     lib.orc_topk.restype = None
-    lib.orc_verify_request.argtypes = [c_int, c_int, P, P, c_double, P, P, P, P, P, P, P]
+    lib.orc_verify_request.argtypes = [c_int, c_int, P, P, c_double, P, P, P, c_double, P, P, P, P]
     lib.orc_verify_request.restype = c_int
-    lib.orc_saguaro_request.argtypes = [c_int, c_int, P, P, c_double, c_int, P, P, P, P, P, P]
+    lib.orc_saguaro_request.argtypes = [c_int, c_int, P, P, c_double, c_int, P, c_double, P, P, P, P, P]
     lib.orc_saguaro_request.restype = c_int
     lib.orc_verify_batch.argtypes = [P, P, c_int, P, c_int, c_int, c_int, P, P, c_float, c_u64,
-                                     P, P, P, P, P, P, c_int]
+                                     P, P, P, P, P, P, c_double, c_int]
     lib.orc_verify_batch.restype = c_int
     lib.orc_saguaro_batch.argtypes = [P, P, c_int, c_int, c_int, c_int, c_int, c_float, c_u64,
-                                      P, P, P, P, P, P, c_int]
-    lib.orc_saguaro_position.argtypes = [c_int, P, P, c_double, P, P]
+                                      P, P, P, P, P, P, c_double, c_int]
+    lib.orc_saguaro_position.argtypes = [c_int, P, P, c_double, P, P, P, P, P]
     lib.orc_saguaro_position.restype = None
     lib.orc_saguaro_batch.restype = c_int
     lib.orc_mutant_id.argtypes = []
@@ -153,17 +153,24 @@ class Oracle:
         self.lib.orc_topk(_ptr(w), w.size, k, _ptr(idx), _ptr(val))
         return idx, val
 
-    def saguaro_position(self, xt_row, xd_row, T: float):
-        """(r, p_saguaro) of one position; xd_row None at the bonus position."""
+    def saguaro_position(self, xt_row, xd_row, T: float, full: bool = False):
+        """(r, p_saguaro) of one position; xd_row None at the bonus position.
+        full=True also returns q, p_D and the residual mass S."""
         xt = np.ascontiguousarray(xt_row, dtype=np.float64).reshape(-1)
         xd = None if xd_row is None else np.ascontiguousarray(xd_row, dtype=np.float64).reshape(-1)
         r = np.empty_like(xt)
         ps = np.empty_like(xt)
-        self.lib.orc_saguaro_position(xt.size, _ptr(xt), _ptr(xd), float(T), _ptr(r), _ptr(ps))
+        q = np.empty_like(xt)
+        pd = np.empty_like(xt)
+        S = ctypes.c_double()
+        self.lib.orc_saguaro_position(xt.size, _ptr(xt), _ptr(xd), float(T), _ptr(r), _ptr(ps), _ptr(q),
+                                      _ptr(pd), ctypes.byref(S))
+        if full:
+            return r, ps, q, pd, S.value
         return r, ps
 
     # --- one request, explicit uniforms ----------------------------------
-    def verify_request(self, xt, xd, T, tok, u_acc, u_res, stats: bool = False):
+    def verify_request(self, xt, xd, T, tok, u_acc, u_res, stats: bool = False, band: float = FLAG_BAND):
         """xt: (g+1, V) fp64 target logits; xd: (g, V) draft logits; tok: (g,)."""
         xt = np.ascontiguousarray(xt, dtype=np.float64)
         g, V = xt.shape[0] - 1, xt.shape[1]
@@ -176,11 +183,11 @@ class Oracle:
         fp, fk = ctypes.c_int32(), ctypes.c_int32()
         st = np.empty((g + 1, NSTAT_VERIFY), np.float64) if stats else None
         n = self.lib.orc_verify_request(g, V, _ptr(xt), _ptr(xd), float(T), _ptr(tok), _ptr(ua),
-                                        _ptr(ur), _ptr(out), ctypes.byref(fp), ctypes.byref(fk),
-                                        _ptr(st))
+                                        _ptr(ur), float(band), _ptr(out), ctypes.byref(fp),
+                                        ctypes.byref(fk), _ptr(st))
         return dict(n=n, out=out, flag_pos=fp.value, flag_kind=fk.value, stats=st)
 
-    def saguaro_request(self, xt, xd, T, k, u_sag, stats: bool = False):
+    def saguaro_request(self, xt, xd, T, k, u_sag, stats: bool = False, band: float = FLAG_BAND):
         xt = np.ascontiguousarray(xt, dtype=np.float64)
         g, V = xt.shape[0] - 1, xt.shape[1]
         xd = np.ascontiguousarray(xd, dtype=np.float64).reshape(g, V) if g > 0 else np.zeros((1, V))
@@ -190,19 +197,21 @@ class Oracle:
         kf = np.empty(g + 1, np.int32)
         tf = np.empty(g + 1, np.int32)
         st = np.empty((g + 1, NSTAT_SAGUARO), np.float64) if stats else None
-        self.lib.orc_saguaro_request(g, V, _ptr(xt), _ptr(xd), float(T), k, _ptr(u), _ptr(topk),
-                                     _ptr(tok), _ptr(kf), _ptr(tf), _ptr(st))
+        self.lib.orc_saguaro_request(g, V, _ptr(xt), _ptr(xd), float(T), k, _ptr(u), float(band),
+                                     _ptr(topk), _ptr(tok), _ptr(kf), _ptr(tf), _ptr(st))
         return dict(topk=topk, tokens=tok, topk_flag=kf, tok_flag=tf, stats=st)
 
     # --- batches over typed logits, Philox uniforms ----------------------
     def verify_batch(self, target, draft, draft_tokens, temperature, seed: int,
-                     gamma=None, stats: bool = False, nthreads: int = 1, req_ids=None):
+                     gamma=None, stats: bool = False, nthreads: int = 1, req_ids=None,
+                     band: float = FLAG_BAND):
         """target [B, gmax+1, V], draft [B, gmax, V] (uint16 bf16 bits or float32).
 
         ``temperature``: a float, or a float32 array [B] (per request).
         ``gamma``: None (every request uses gmax) or an int32 array [B].
         ``req_ids``: request index of each row in the Philox counter (default 0..B-1),
         so that a sample of a larger batch draws the same uniforms.
+        ``band``: a draw within ``band`` of its threshold or CDF boundary is flagged.
         """
         target, dt = _logit_array(target)
         draft, dd = _logit_array(draft)
@@ -225,13 +234,13 @@ class Oracle:
         rid = None if req_ids is None else np.ascontiguousarray(req_ids, dtype=np.int32).reshape(B)
         rc = self.lib.orc_verify_batch(_ptr(target), _ptr(draft), dt, _ptr(tok), B, gmax, V,
                                        _ptr(gam), _ptr(temps), tscalar, seed, _ptr(out), _ptr(n),
-                                       _ptr(fp), _ptr(fk), _ptr(st), _ptr(rid), nthreads)
+                                       _ptr(fp), _ptr(fk), _ptr(st), _ptr(rid), float(band), nthreads)
         if rc != 0:
             raise ValueError("oracle rejected the batch arguments")
         return dict(out_tokens=out, n_accepted=n, flag_pos=fp, flag_kind=fk, stats=st)
 
     def saguaro_batch(self, target, draft, k: int, temperature: float, seed: int,
-                      stats: bool = False, nthreads: int = 1, req_ids=None):
+                      stats: bool = False, nthreads: int = 1, req_ids=None, band: float = FLAG_BAND):
         target, dt = _logit_array(target)
         draft, dd = _logit_array(draft)
         assert dt == dd
@@ -245,7 +254,7 @@ class Oracle:
         rid = None if req_ids is None else np.ascontiguousarray(req_ids, dtype=np.int32).reshape(B)
         rc = self.lib.orc_saguaro_batch(_ptr(target), _ptr(draft), dt, B, g, V, k,
                                         float(temperature), seed, _ptr(topk), _ptr(tok), _ptr(kf),
-                                        _ptr(tf), _ptr(st), _ptr(rid), nthreads)
+                                        _ptr(tf), _ptr(st), _ptr(rid), float(band), nthreads)
         if rc != 0:
             raise ValueError("oracle rejected the batch arguments")
         return dict(bonus_topk=topk, saguaro_tokens=tok, topk_flag=kf, tok_flag=tf, stats=st)

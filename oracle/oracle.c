@@ -38,10 +38,10 @@
  *     draw 0 = accept test, 1 = resample / bonus, 2 = Saguaro sample;
  *   - Saguaro at j == g (no draft row): r = q_g and p_D = q_g.
  *
- * Flags: a draw whose uniform lies within 1e-6 of the threshold it is compared
- * with (accept threshold, or either CDF boundary of the chosen token) is
- * flagged; comparisons with another implementation stop at the first flagged
- * draw of a request.
+ * Flags: a draw whose uniform lies within `band` (an argument; 1e-6 by default)
+ * of the threshold it is compared with (accept threshold, or either CDF
+ * boundary of the chosen token) is flagged; comparisons with another
+ * implementation stop at the first flagged draw of a request.
  *
  * ORC_MUTANT (compile-time, default 0) plants one known mistake; the test
  * suite builds each mutant and checks that some pin fails.  It is never set in
@@ -60,13 +60,13 @@
 
 enum { ORC_BF16 = 0, ORC_F32 = 1 };
 
-#define ORC_FLAG_BAND 1e-6     /* uniform-to-boundary distance that flags a draw */
+#define ORC_FLAG_BAND 1e-6     /* default uniform-to-boundary distance that flags a draw */
 #define ORC_SAGUARO_CLAMP 1e-8 /* [SAG] §3.2: residual clamped below at 1e-8     */
 #define ORC_TOPK_REL 1e-5      /* top-k slot ambiguity: relative gap              */
 #define ORC_TOPK_ABS 1e-6      /* top-k slot ambiguity: absolute gap              */
 
-#define ORC_NSTAT_VERIFY 8
-#define ORC_NSTAT_SAGUARO 8
+#define ORC_NSTAT_VERIFY 10
+#define ORC_NSTAT_SAGUARO 10
 
 /* ------------------------------------------------------------------------- */
 /* Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as    */
@@ -187,8 +187,8 @@ int orc_argmax(const double* x, int V) {
  * u * S < C_k = sum_{v<=k} w_v, where S = sum_v w_v.  If rounding leaves no
  * such k, the last index with positive weight.  *dist gets the distance from u
  * to the nearer of the chosen token's normalised CDF boundaries C_{k-1}/S and
- * C_k/S. */
-int orc_choice(const double* w, int V, double u, double* dist) {
+ * C_k/S (reported in *edge_lo, *edge_hi when not NULL). */
+int orc_choice_edges(const double* w, int V, double u, double* dist, double* edge_lo, double* edge_hi) {
   double S = 0.0;
   for (int v = 0; v < V; ++v) S += w[v];
   double target = u * S;
@@ -226,7 +226,13 @@ int orc_choice(const double* w, int V, double u, double* dist) {
     double a = fabs(u - lo / S), b = fabs(u - hi / S);
     *dist = a < b ? a : b;
   }
+  if (edge_lo) *edge_lo = lo / S;
+  if (edge_hi) *edge_hi = hi / S;
   return chosen;
+}
+
+int orc_choice(const double* w, int V, double u, double* dist) {
+  return orc_choice_edges(w, V, u, dist, NULL, NULL);
 }
 
 /* Top-k ([SAG] §3.1): the k largest entries, in descending order, lowest index
@@ -263,8 +269,11 @@ void orc_topk(const double* w, int V, int k, int32_t* idx, double* val) {
 /* token at index n, then -1), return value n = number of accepted tokens.   */
 /* flag_pos / flag_kind: position of the first flagged draw (-1 if none),    */
 /* kind 0 = accept draw, 1 = resample/bonus draw.                            */
-/* stats (nullable, (g+1) x 8): t_max, t_logsum, d_max, d_logsum, q(x), p(x),*/
-/* residual mass S, accept probability a; NaN where it does not apply.        */
+/* stats (nullable, (g+1) x 10): t_max, t_logsum, d_max, d_logsum, q(x),     */
+/* p(x), residual mass S, accept probability a, and the distances u - lo and  */
+/* hi - u of the drawn uniform to the normalised CDF edges of the token drawn */
+/* at this position; NaN where it does not apply.                             */
+/* band: a draw within `band` of its threshold / boundary is flagged.        */
 /* Returns -1 when a token lies outside [0, V) (outputs all -1).              */
 /* ------------------------------------------------------------------------- */
 
@@ -316,7 +325,7 @@ static orc_position position_quantities(int V, const double* ti, const double* d
 }
 
 int orc_verify_request(int g, int V, const double* xt, const double* xd, double T,
-                       const int32_t* tok, const double* u_acc, const double* u_res,
+                       const int32_t* tok, const double* u_acc, const double* u_res, double band,
                        int32_t* out, int32_t* flag_pos, int32_t* flag_kind, double* stats) {
   for (int i = 0; i <= g; ++i) out[i] = -1;
   *flag_pos = -1;
@@ -375,7 +384,7 @@ int orc_verify_request(int g, int V, const double* xt, const double* xd, double 
   for (int i = 0; i < g; ++i) {
     orc_position P = position_quantities(V, xt + (size_t)i * V, xd + (size_t)i * V, T, tok[i], q, p, r);
     double u = u_acc[i];
-    if (*flag_pos < 0 && fabs(u - P.a) < ORC_FLAG_BAND) {
+    if (*flag_pos < 0 && fabs(u - P.a) < band) {
       *flag_pos = i;
       *flag_kind = 0;
     }
@@ -386,9 +395,13 @@ int orc_verify_request(int g, int V, const double* xt, const double* xd, double 
     /* Rejected at i: one token from the residual, then stop ([SSD] rollback). */
     if (!(P.S > 0.0))
       for (int v = 0; v < V; ++v) r[v] = q[v];
-    double dist;
-    out[i] = orc_choice(r, V, u_res[i], &dist);
-    if (*flag_pos < 0 && (dist < ORC_FLAG_BAND || P.S < ORC_FLAG_BAND)) {
+    double dist, e_lo, e_hi;
+    out[i] = orc_choice_edges(r, V, u_res[i], &dist, &e_lo, &e_hi);
+    if (stats) {
+      stats[i * ORC_NSTAT_VERIFY + 8] = u_res[i] - e_lo;
+      stats[i * ORC_NSTAT_VERIFY + 9] = e_hi - u_res[i];
+    }
+    if (*flag_pos < 0 && (dist < band || P.S < band)) {
       *flag_pos = i;
       *flag_kind = 1;
     }
@@ -403,9 +416,13 @@ int orc_verify_request(int g, int V, const double* xt, const double* xd, double 
     int row = g;
 #endif
     orc_softmax(xt + (size_t)row * V, V, T, q, NULL, NULL);
-    double dist;
-    out[g] = orc_choice(q, V, u_res[g], &dist);
-    if (*flag_pos < 0 && dist < ORC_FLAG_BAND) {
+    double dist, e_lo, e_hi;
+    out[g] = orc_choice_edges(q, V, u_res[g], &dist, &e_lo, &e_hi);
+    if (stats) {
+      stats[g * ORC_NSTAT_VERIFY + 8] = u_res[g] - e_lo;
+      stats[g * ORC_NSTAT_VERIFY + 9] = e_hi - u_res[g];
+    }
+    if (*flag_pos < 0 && dist < band) {
       *flag_pos = g;
       *flag_kind = 1;
     }
@@ -426,8 +443,9 @@ int orc_verify_request(int g, int V, const double* xt, const double* xd, double 
 /*   token_j = inverse-CDF draw from p_saguaro with u_sag[j].                  */
 /* topk_flag[j]: bit t set when slot t is within the top-k ambiguity gap of a */
 /* neighbouring value; tok_flag[j]: 1 when the draw is within 1e-6 of a CDF   */
-/* boundary.  stats ((g+1) x 8): t_logsum, d_logsum, S, Zs = sum s,           */
-/* p_saguaro(token), r(top slot 0), r(top slot k-1), r(first excluded).       */
+/* boundary.  stats ((g+1) x 10): t_logsum, d_logsum, S, Zs = sum s,          */
+/* p_saguaro(token), r(top slot 0), r(top slot k-1), r(first excluded), and   */
+/* the distances u - lo, hi - u to the drawn token's normalised CDF edges.    */
 /* ------------------------------------------------------------------------- */
 
 static int topk_close(double a, double b) {
@@ -437,7 +455,7 @@ static int topk_close(double a, double b) {
 }
 
 int orc_saguaro_request(int g, int V, const double* xt, const double* xd, double T, int k,
-                        const double* u_sag, int32_t* topk, int32_t* tokens,
+                        const double* u_sag, double band, int32_t* topk, int32_t* tokens,
                         int32_t* topk_flag, int32_t* tok_flag, double* stats) {
   if (stats) fill_nan(stats, (g + 1) * ORC_NSTAT_SAGUARO);
   double* q = (double*)malloc(sizeof(double) * (size_t)V);
@@ -492,9 +510,9 @@ int orc_saguaro_request(int g, int V, const double* xt, const double* xd, double
 #endif
       Zs += s[v];
     }
-    double dist;
-    tokens[j] = orc_choice(s, V, u_sag[j], &dist);
-    tok_flag[j] = dist < ORC_FLAG_BAND ? 1 : 0;
+    double dist, e_lo, e_hi;
+    tokens[j] = orc_choice_edges(s, V, u_sag[j], &dist, &e_lo, &e_hi);
+    tok_flag[j] = dist < band ? 1 : 0;
     if (stats) {
       double* st = stats + j * ORC_NSTAT_SAGUARO;
       st[0] = lst;
@@ -505,6 +523,8 @@ int orc_saguaro_request(int g, int V, const double* xt, const double* xd, double
       st[5] = val[0];
       st[6] = val[k - 1];
       st[7] = kk > k ? val[k] : NAN;
+      st[8] = u_sag[j] - e_lo;
+      st[9] = e_hi - u_sag[j];
     }
   }
   free(q);
@@ -517,16 +537,19 @@ int orc_saguaro_request(int g, int V, const double* xt, const double* xd, double
 }
 
 /* One Saguaro position's distributions (for checking ambiguous top-k slots and
- * sample laws): r = the normalised residual (or q), psag = p_saguaro.  xd may be
+ * sample laws): r = the normalised residual (or q), psag = p_saguaro, and
+ * (nullable) q_out = q, pd_out = p_D, mass_out = the residual mass S.  xd may be
  * NULL for the bonus position. */
-void orc_saguaro_position(int V, const double* xt, const double* xd, double T, double* r, double* psag) {
+void orc_saguaro_position(int V, const double* xt, const double* xd, double T, double* r, double* psag,
+                          double* q_out, double* pd_out, double* mass_out) {
   double* q = (double*)malloc(sizeof(double) * (size_t)V);
   double* p = (double*)malloc(sizeof(double) * (size_t)V);
   orc_softmax(xt, V, T, q, NULL, NULL);
   const double* pD = q;
+  double S = 1.0;
   if (xd) {
     orc_softmax(xd, V, T, p, NULL, NULL);
-    double S = 0.0;
+    S = 0.0;
     for (int v = 0; v < V; ++v) {
       double d = q[v] - p[v];
       r[v] = d > 0.0 ? d : 0.0;
@@ -548,6 +571,9 @@ void orc_saguaro_position(int V, const double* xt, const double* xd, double T, d
     Zs += psag[v];
   }
   for (int v = 0; v < V; ++v) psag[v] /= Zs;
+  if (q_out) memcpy(q_out, q, sizeof(double) * (size_t)V);
+  if (pd_out) memcpy(pd_out, pD, sizeof(double) * (size_t)V);
+  if (mass_out) *mass_out = S;
   free(q);
   free(p);
 }
@@ -578,6 +604,7 @@ typedef struct {
   int32_t* flag_b; /* verify: flag_kind     saguaro: tok_flag       */
   double* stats;
   int saguaro;
+  double band;
   int nthreads;
   int tid;
 } orc_job;
@@ -601,7 +628,7 @@ static void run_request(const orc_job* jb, int b, double* xt, double* xd) {
     for (int j = 0; j < g; ++j) orc_row_to_f64(jb->draft, jb->dtype, (size_t)b * gmax + j, V, xd + (size_t)j * V);
     double u[64];
     for (int j = 0; j <= g; ++j) u[j] = orc_uniform(jb->seed, rid, (uint32_t)j, 2u);
-    orc_saguaro_request(g, V, xt, xd, T, k, u, jb->out_a + (size_t)b * W * k, jb->out_b + (size_t)b * W,
+    orc_saguaro_request(g, V, xt, xd, T, k, u, jb->band, jb->out_a + (size_t)b * W * k, jb->out_b + (size_t)b * W,
                         jb->flag_a + (size_t)b * W, jb->flag_b + (size_t)b * W,
                         jb->stats ? jb->stats + (size_t)b * W * ORC_NSTAT_SAGUARO : NULL);
     return;
@@ -622,7 +649,7 @@ static void run_request(const orc_job* jb, int b, double* xt, double* xd) {
     ur[i] = orc_uniform(jb->seed, rid, (uint32_t)i, 1u);
   }
   int32_t fp, fk;
-  int n = orc_verify_request(g, V, xt, xd, T, jb->draft_tokens + (size_t)b * gmax, ua, ur, out, &fp, &fk,
+  int n = orc_verify_request(g, V, xt, xd, T, jb->draft_tokens + (size_t)b * gmax, ua, ur, jb->band, out, &fp, &fk,
                              jb->stats ? jb->stats + (size_t)b * W * ORC_NSTAT_VERIFY : NULL);
   if (n < 0) {
     for (int t = 0; t < W; ++t) out[t] = -1;
@@ -661,15 +688,16 @@ static int run_batch(orc_job base) {
   return 0;
 }
 
-/* Batched verification.  stats (nullable): [B, gmax+1, 8]. */
+/* Batched verification.  stats (nullable): [B, gmax+1, 10]. */
 int orc_verify_batch(const void* target, const void* draft, int dtype, const int32_t* draft_tokens,
                      int B, int gmax, int V, const int32_t* gamma, const float* temp,
                      float temp_scalar, uint64_t seed, int32_t* out_tokens, int32_t* n_accepted,
                      int32_t* flag_pos, int32_t* flag_kind, double* stats, const int32_t* req_ids,
-                     int nthreads) {
+                     double band, int nthreads) {
   orc_job jb;
   memset(&jb, 0, sizeof jb);
   jb.req_ids = req_ids;
+  jb.band = band;
   jb.target = target;
   jb.draft = draft;
   jb.dtype = dtype;
@@ -692,15 +720,16 @@ int orc_verify_batch(const void* target, const void* draft, int dtype, const int
 }
 
 /* Batched Saguaro pre-speculation.  bonus_topk [B, g+1, k], saguaro_tokens
- * [B, g+1], topk_flag / tok_flag [B, g+1], stats (nullable) [B, g+1, 8]. */
+ * [B, g+1], topk_flag / tok_flag [B, g+1], stats (nullable) [B, g+1, 10]. */
 int orc_saguaro_batch(const void* target, const void* draft, int dtype, int B, int g, int V, int k,
                       float temperature, uint64_t seed, int32_t* bonus_topk, int32_t* saguaro_tokens,
                       int32_t* topk_flag, int32_t* tok_flag, double* stats, const int32_t* req_ids,
-                      int nthreads) {
+                      double band, int nthreads) {
   if (k < 1 || k > 30 || k > V || !(temperature > 0.0f)) return -1;
   orc_job jb;
   memset(&jb, 0, sizeof jb);
   jb.req_ids = req_ids;
+  jb.band = band;
   jb.target = target;
   jb.draft = draft;
   jb.dtype = dtype;

@@ -560,12 +560,15 @@ __device__ __forceinline__ void warp_merge_topk(TopK<K>& tk, float (&ov)[K], int
 // global target minus the weight of the CTAs before this one).  Thread 0
 // picks the warp from wsum[]; that warp rescans its run with a warp prefix
 // scan and fp64 carries.  If rounding leaves the target beyond every
-// boundary, the last element with positive weight is taken.  Returns the
-// global token in thread 0 (via *result in shared memory).
+// boundary, the last element with positive weight is taken.  Writes the
+// global token to *result, and the drawn element's CDF position (weight
+// before it, relative to this CTA's start; NaN after a rounding fallback)
+// and weight to *edge_lo / *edge_w (all in shared memory).
 // ---------------------------------------------------------------------------
 template <typename E, typename WFun>
 __device__ __forceinline__ void cdf_search(const Slice<E>& sl, int lo, const WFun& wfun, const float* wsum, double tl,
-                                           int* sh_warp, double* sh_base, int* result) {
+                                           int* sh_warp, double* sh_base, int* result, double* edge_lo,
+                                           float* edge_w) {
   constexpr int kVec = Elem<E>::kVec;
   if (threadIdx.x == 0) {
     double acc = 0.0;
@@ -590,6 +593,8 @@ __device__ __forceinline__ void cdf_search(const Slice<E>& sl, int lo, const WFu
     *sh_warp = pick;
     *sh_base = pick_base;
     *result = -1;
+    *edge_lo = NAN;
+    *edge_w = 0.f;
   }
   __syncthreads();
   const int pick = *sh_warp;
@@ -599,6 +604,8 @@ __device__ __forceinline__ void cdf_search(const Slice<E>& sl, int lo, const WFu
     warp_range(sl.nvec, warp, v0, v1);
     double carry = *sh_base;
     int found = -1;
+    double found_edge = NAN;
+    float found_w = 0.f;
     int last_vec = -1;  // last vector in the run with positive weight
     for (int vb = v0; vb < v1 && found < 0; vb += 32) {
       const int v = vb + lane;
@@ -628,19 +635,37 @@ __device__ __forceinline__ void cdf_search(const Slice<E>& sl, int lo, const WFu
       if (hm) {
         const int L = __ffs(hm) - 1;
         int tok = -1;
+        double edge = 0.0;
+        float wt = 0.f;
         if (lane == L) {
           double a = carry + static_cast<double>(incl - vs);
           int last_e = -1;
+          double a_last = a;
 #pragma unroll
           for (int e = 0; e < kVec; ++e) {
-            if (w[e] > 0.f) last_e = e;
+            const double before = a;
+            if (w[e] > 0.f) {
+              last_e = e;
+              a_last = before;
+            }
             a += static_cast<double>(w[e]);
-            if (tok < 0 && w[e] > 0.f && tl < a) tok = e;
+            if (tok < 0 && w[e] > 0.f && tl < a) {
+              tok = e;
+              edge = before;
+            }
           }
-          if (tok < 0) tok = last_e;
+          if (tok < 0) {
+            tok = last_e;
+            edge = a_last;
+          }
+#pragma unroll
+          for (int e = 0; e < kVec; ++e)
+            if (e == tok) wt = w[e];
           tok = v * kVec + tok;
         }
         found = __shfl_sync(0xFFFFFFFFu, tok, L);
+        found_edge = __shfl_sync(0xFFFFFFFFu, edge, L);
+        found_w = __shfl_sync(0xFFFFFFFFu, wt, L);
       }
       carry += static_cast<double>(total);
     }
@@ -655,7 +680,11 @@ __device__ __forceinline__ void cdf_search(const Slice<E>& sl, int lo, const WFu
         if (w[e] > 0.f) last_e = e;
       found = last_vec * kVec + last_e;
     }
-    if (lane == 0) *result = found >= 0 ? lo + found : -1;
+    if (lane == 0) {
+      *result = found >= 0 ? lo + found : -1;
+      *edge_lo = found_edge;
+      *edge_w = found_w;
+    }
   }
   __syncthreads();
 }
@@ -663,9 +692,9 @@ __device__ __forceinline__ void cdf_search(const Slice<E>& sl, int lo, const WFu
 // Thread 0: cluster totals of pass `p` (CTA sums in rank order), the global
 // target u * total, and which CTA owns it.  Returns the total; *owner gets the
 // rank (-1 if the total is not positive), *local the target minus the weight
-// of the ranks before the owner.
+// of the ranks before the owner, *prefix that weight.
 __device__ __forceinline__ double cluster_locate(const Part* part, int csize, int p, double u, int* owner,
-                                                 double* local) {
+                                                 double* local, double* prefix) {
   double tot = 0.0;
   double sums[16];
   for (int r = 0; r < csize; ++r) {
@@ -674,6 +703,7 @@ __device__ __forceinline__ double cluster_locate(const Part* part, int csize, in
   }
   *owner = -1;
   *local = 0.0;
+  *prefix = 0.0;
   if (!(tot > 0.0)) return tot;
   const double target = u * tot;
   double acc = 0.0;
@@ -686,6 +716,7 @@ __device__ __forceinline__ double cluster_locate(const Part* part, int csize, in
       if (*owner < 0 && target < acc + sums[r]) {
         *owner = r;
         *local = target - acc;
+        *prefix = acc;
       }
     }
     acc += sums[r];
@@ -693,6 +724,7 @@ __device__ __forceinline__ double cluster_locate(const Part* part, int csize, in
   if (*owner < 0) {
     *owner = last_pos;
     *local = target - last_acc;
+    *prefix = last_acc;
   }
   return tot;
 }

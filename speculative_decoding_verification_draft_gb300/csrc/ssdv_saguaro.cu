@@ -76,7 +76,8 @@ __global__ void __launch_bounds__(kThreads) saguaro_kernel(const SaguaroArgs a) 
   __shared__ float wtop_v[kWarps][kTopK];
   __shared__ int wtop_i[kWarps][kTopK];
   __shared__ int sh_warp, sh_result, sh_owner, sh_err;
-  __shared__ double sh_base, sh_local, sh_total;
+  __shared__ double sh_base, sh_local, sh_total, sh_prefix, sh_edge;
+  __shared__ float sh_edge_w;
   __shared__ float sh_mt, sh_zt, sh_md, sh_zd;
 
   const Geometry& geo = a.geo;
@@ -180,8 +181,8 @@ __global__ void __launch_bounds__(kThreads) saguaro_kernel(const SaguaroArgs a) 
     cluster_sync();  // (2) pass-A sums and top-8 lists published
     if (tid == 0) {
       int owner;
-      double local;
-      sh_total = cluster_locate(&part, C, p, 0.5, &owner, &local);
+      double local, prefix;
+      sh_total = cluster_locate(&part, C, p, 0.5, &owner, &local, &prefix);
     }
     __syncthreads();
     if (p == 0 && !bonus) resid_mass = sh_total / static_cast<double>(sh_zt);
@@ -236,14 +237,15 @@ __global__ void __launch_bounds__(kThreads) saguaro_kernel(const SaguaroArgs a) 
   cluster_sync();  // (3) mix sums published
   if (tid == 0) {
     int owner;
-    double local;
-    sh_total = cluster_locate(&part, C, 2, static_cast<double>(u_sag), &owner, &local);
+    double local, prefix;
+    sh_total = cluster_locate(&part, C, 2, static_cast<double>(u_sag), &owner, &local, &prefix);
     sh_owner = owner;
     sh_local = local;
+    sh_prefix = prefix;
   }
   __syncthreads();
   if (sh_owner == rank) {
-    cdf_search(sl, lo, mw, wsum, sh_local, &sh_warp, &sh_base, &sh_result);
+    cdf_search(sl, lo, mw, wsum, sh_local, &sh_warp, &sh_base, &sh_result, &sh_edge, &sh_edge_w);
     if (tid == 0) a.saguaro_tokens[out_idx] = sh_err ? -1 : sh_result;
     if (a.stats && tid == 0 && sh_result >= lo) {
       // p_saguaro of the drawn token (debug statistics only)
@@ -255,6 +257,9 @@ __global__ void __launch_bounds__(kThreads) saguaro_kernel(const SaguaroArgs a) 
       float* st0 = a.stats + out_idx * SSD_NSTAT_SAGUARO;
       st0[3] = static_cast<float>(sh_total);
       st0[4] = static_cast<float>(w[e] / sh_total);
+      st0[8] = static_cast<float>(static_cast<double>(u_sag) - (sh_prefix + sh_edge) / sh_total);
+      st0[9] = static_cast<float>((sh_prefix + sh_edge + static_cast<double>(sh_edge_w)) / sh_total -
+                                  static_cast<double>(u_sag));
     }
   } else if (sh_owner < 0 && rank == 0 && tid == 0) {
     a.saguaro_tokens[out_idx] = -1;

@@ -76,7 +76,15 @@ __device__ void finish_request(const VerifyArgs& a, int b, int g) {
     for (int k = n + 1; k < W; ++k) out[k] = -1;
     a.n_accepted[b] = n;
   }
-  a.ticket[b] = 0;  // leave the workspace zeroed for the next call
+  // Leave the whole workspace zeroed (its layout depends on B and gamma, so a
+  // later call with another shape may read these words as arrival counters).
+  int32_t* wflag = a.unit_flag + static_cast<size_t>(b) * W;
+  int32_t* wtok = a.unit_tok + static_cast<size_t>(b) * W;
+  for (int k = 0; k < W; ++k) {
+    wflag[k] = 0;
+    wtok[k] = 0;
+  }
+  a.ticket[b] = 0;
 }
 
 }  // namespace
@@ -91,7 +99,8 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const VerifyArgs a) {
   __shared__ int red_i[2 * kWarps];
   __shared__ float wsum[kWarps];
   __shared__ int sh_warp, sh_result, sh_owner, sh_accept, sh_pass, sh_err;
-  __shared__ double sh_base, sh_local;
+  __shared__ double sh_base, sh_local, sh_prefix, sh_total, sh_edge;
+  __shared__ float sh_edge_w;
   __shared__ float sh_mt, sh_zt, sh_md, sh_zd;
 
   const Geometry& geo = a.geo;
@@ -253,10 +262,12 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const VerifyArgs a) {
       cluster_sync();  // (2) pass sums published
       if (tid == 0) {
         int owner;
-        double local;
-        total = cluster_locate(&part, C, p, static_cast<double>(u.resample), &owner, &local);
+        double local, prefix;
+        total = cluster_locate(&part, C, p, static_cast<double>(u.resample), &owner, &local, &prefix);
         sh_owner = owner;
         sh_local = local;
+        sh_prefix = prefix;
+        sh_total = total;
       }
       __syncthreads();
       if (!use_target && p == 0 && tid == 0) resid_mass = total;
@@ -275,13 +286,19 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const VerifyArgs a) {
     if (sh_owner == rank && (!sh_accept || bonus)) {
       if (use_target) {
         const TargetW<E> wf{c, mct};
-        cdf_search(sl, lo, wf, wsum, sh_local, &sh_warp, &sh_base, &sh_result);
+        cdf_search(sl, lo, wf, wsum, sh_local, &sh_warp, &sh_base, &sh_result, &sh_edge, &sh_edge_w);
       } else {
         const ResidualW<E> wf{c, mct, scaled_max(sh_md, c), sh_zt / sh_zd};
-        cdf_search(sl, lo, wf, wsum, sh_local, &sh_warp, &sh_base, &sh_result);
+        cdf_search(sl, lo, wf, wsum, sh_local, &sh_warp, &sh_base, &sh_result, &sh_edge, &sh_edge_w);
       }
       if (tid == 0) {
         a.unit_tok[out_idx] = sh_result;
+        if (a.stats) {  // distances of u to the drawn token's CDF edges (debug statistics)
+          float* st = a.stats + static_cast<size_t>(out_idx) * SSD_NSTAT_VERIFY;
+          const double ur = static_cast<double>(u.resample);
+          st[8] = static_cast<float>(ur - (sh_prefix + sh_edge) / sh_total);
+          st[9] = static_cast<float>((sh_prefix + sh_edge + static_cast<double>(sh_edge_w)) / sh_total - ur);
+        }
         __threadfence();
       }
     }

@@ -20,8 +20,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIBRARY = os.path.join(PKG, "libssdv.so")
 
 SSD_BF16, SSD_F32 = 0, 1
-NSTAT_VERIFY = 8
-NSTAT_SAGUARO = 8
+NSTAT_VERIFY = 10
+NSTAT_SAGUARO = 10
 MAX_TOPK = 8
 
 STATUS_NAMES = {
@@ -122,10 +122,16 @@ def make_workspace(B: int, gamma_max: int, device=None) -> torch.Tensor:
     return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
 
 
+def _ws_key(device):
+    device = torch.device(device if device is not None else "cuda")
+    index = device.index if device.index is not None else torch.cuda.current_device()
+    return (index, torch.cuda.current_stream(index).cuda_stream)
+
+
 def _workspace(B: int, gmax: int, device, given: Optional[torch.Tensor]):
     if given is not None:
         return given
-    key = (str(device), torch.cuda.current_stream(device).cuda_stream)
+    key = _ws_key(device)
     need = workspace_bytes(B, gmax)
     ws = _ws_cache.get(key)
     if ws is None or ws.numel() < need:
@@ -205,7 +211,7 @@ def saguaro_prespec(target: torch.Tensor, draft: torch.Tensor, k: int, temperatu
 
 
 def debug_rowstats(target, draft, draft_tokens, temperature, seed, workspace=None, stream=None):
-    """ssd_debug_rowstats: (out_tokens, n_accepted, stats [B, g+1, 8] float32)."""
+    """ssd_debug_rowstats: (out_tokens, n_accepted, stats [B, g+1, 10] float32)."""
     B, W, V = target.shape
     g = W - 1
     dev = target.device
@@ -223,7 +229,7 @@ def debug_rowstats(target, draft, draft_tokens, temperature, seed, workspace=Non
 
 
 def debug_saguaro_stats(target, draft, k, temperature, seed, stream=None):
-    """ssd_debug_saguaro_stats: (bonus_topk, saguaro_tokens, stats [B, g+1, 8])."""
+    """ssd_debug_saguaro_stats: (bonus_topk, saguaro_tokens, stats [B, g+1, 10])."""
     B, W, V = target.shape
     g = W - 1
     dev = target.device
@@ -248,8 +254,7 @@ def debug_uniforms(seed: int, B: int, W: int, device=None, stream=None) -> torch
 def read_status(workspace: Optional[torch.Tensor] = None, device=None, stream=None) -> int:
     """Read and clear the device status word (synchronises the stream)."""
     if workspace is None:
-        device = torch.device(device or "cuda")
-        workspace = _ws_cache.get((str(device), torch.cuda.current_stream(device).cuda_stream))
+        workspace = _ws_cache.get(_ws_key(device))
         if workspace is None:
             return 0
     st = ctypes.c_int(0)

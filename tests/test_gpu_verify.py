@@ -90,6 +90,21 @@ def test_zipf_rowstats(ssdv, zipf64):
     gc.assert_verify_parity(out, n, ref, 128256, "zipf (debug entry)")
 
 
+def test_cdf_edge_accuracy(ssdv, zipf64):
+    """The GPU's inverse-CDF boundaries of each drawn token, against the
+    oracle's: the measured error sets how wide the flag band must be."""
+    b = zipf64.to("cuda")
+    errs = []
+    for seed in range(10, 26):
+        out, n, st = ssdv.debug_rowstats(b.target, b.draft, b.draft_tokens, 0.8, seed)
+        ref = gc.verify_oracle(zipf64, seed, stats=True)
+        errs.append(gc.edge_errors(st, ref, out))
+    e = np.concatenate(errs)
+    print(f"\nCDF edge error over {e.size} edges: max {e.max():.3g}, p99 {np.quantile(e, 0.99):.3g}, "
+          f"median {np.median(e):.3g}")
+    assert e.size > 500 and e.max() < 1e-6
+
+
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("V", [1, 8, 1000, 4099, 33001])
 @pytest.mark.parametrize("gamma", [0, 1, 8])
@@ -222,6 +237,20 @@ def test_workspace_reuse_and_determinism(ssdv, zipf64):
     torch.cuda.synchronize()
     assert torch.equal(r1[0], r2[0]) and torch.equal(r1[1], r2[1])
     assert int(ws[16:16 + 4 * 64].view(torch.int32).abs().sum()) == 0  # tickets back to zero
+
+
+def test_workspace_shared_across_shapes(ssdv):
+    """One workspace serves calls of different (B, gamma) in any order."""
+    ws = ssdv.make_workspace(64, 8)
+    shapes = [(1, 5, 32000), (24, 0, 1000), (64, 4, 5000), (3, 8, 700), (64, 1, 64), (24, 0, 1000)]
+    for B, g, V in shapes * 2:
+        batch = wl.zipf_batch(B, g, V, seed=B * 100 + g, temperature=0.9)
+        b = batch.to("cuda")
+        out, n = ssdv.verify(b.target, b.draft, b.draft_tokens, 0.9, 6, workspace=ws)
+        ref = gc.verify_oracle(batch, 6)
+        gc.assert_verify_parity(out, n, ref, V, f"shared workspace B={B} g={g}")
+    torch.cuda.synchronize()
+    assert int(ws[16:].to(torch.int32).abs().sum()) == 0
 
 
 def test_host_side_errors(ssdv):
