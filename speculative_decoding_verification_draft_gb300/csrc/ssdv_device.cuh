@@ -125,9 +125,42 @@ __device__ __forceinline__ uint32_t cluster_rank() {
   return r;
 }
 
-// Full cluster barrier with release/acquire semantics (all threads call it).
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+// Split cluster barrier (all threads of every CTA execute both halves).
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Asynchronous stores into another CTA's shared memory that complete on that
+// CTA's mbarrier (remote addresses from mapa).
+__device__ __forceinline__ void st_async_v4(uint32_t remote, float4 v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   remote),
+               "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(remote_bar)
+               : "memory");
+}
+__device__ __forceinline__ void st_async_b64(uint32_t remote, unsigned long long v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b64 [%0], %1, [%2];" ::"r"(remote), "l"(v),
+               "r"(remote_bar)
+               : "memory");
+}
+
+// Wait (bounded) for phase 0 of a barrier completed by other CTAs' st.async.
+__device__ __forceinline__ bool xbar_wait_bounded(uint64_t* bar) {
+  for (uint32_t it = 0; it < kWaitLimit; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], 0;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar))
+        : "memory");
+    if (done) return true;
+  }
+  return false;
 }
 
 // Address of the same shared variable in CTA `rank` of the cluster.
@@ -375,20 +408,15 @@ __device__ __forceinline__ ThreadStats<E> stats_pass(const Slice<E>& sl, uint64_
   return r;
 }
 
-// Block reduction of per-thread statistics into thread 0 (fixed order).
+// Block reduction of per-thread statistics; the result is valid in every lane
+// of warp 0 (a fixed butterfly over the warps' partials).
 struct BlockStats {
   MaxSum t, d;
   ArgMax a;
   int timeout;
 };
 
-template <typename E>
-__device__ __forceinline__ BlockStats block_reduce_stats(const ThreadStats<E>& ts, float c, float* red_f,
-                                                         int* red_i) {
-  // red_f: 5 * kWarps floats, red_i: 2 * kWarps ints
-  MaxSum t = ts.t, d = ts.d;
-  ArgMax a = ts.a;
-  int to = ts.timeout ? 1 : 0;
+__device__ __forceinline__ void butterfly_stats(MaxSum& t, MaxSum& d, ArgMax& a, int& to, float c) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     MaxSum ot{__shfl_xor_sync(0xFFFFFFFFu, t.m, o), __shfl_xor_sync(0xFFFFFFFFu, t.s, o)};
@@ -399,6 +427,16 @@ __device__ __forceinline__ BlockStats block_reduce_stats(const ThreadStats<E>& t
     a = better_arg(a, oa);
     to |= __shfl_xor_sync(0xFFFFFFFFu, to, o);
   }
+}
+
+template <typename E>
+__device__ __forceinline__ BlockStats block_reduce_stats(const ThreadStats<E>& ts, float c, float* red_f,
+                                                         int* red_i) {
+  // red_f: 5 * kWarps floats, red_i: 2 * kWarps ints
+  MaxSum t = ts.t, d = ts.d;
+  ArgMax a = ts.a;
+  int to = ts.timeout ? 1 : 0;
+  butterfly_stats(t, d, a, to, c);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (lane == 0) {
     red_f[0 * kWarps + warp] = t.m;
@@ -411,39 +449,122 @@ __device__ __forceinline__ BlockStats block_reduce_stats(const ThreadStats<E>& t
   }
   __syncthreads();
   BlockStats out{{-INFINITY, 0.f}, {-INFINITY, 0.f}, {-INFINITY, -1}, 0};
-  if (threadIdx.x == 0) {
-    for (int w = 0; w < kWarps; ++w) {
-      out.t = combine_ms(out.t, MaxSum{red_f[0 * kWarps + w], red_f[1 * kWarps + w]}, c);
-      out.d = combine_ms(out.d, MaxSum{red_f[2 * kWarps + w], red_f[3 * kWarps + w]}, c);
-      out.a = better_arg(out.a, ArgMax{red_f[4 * kWarps + w], red_i[0 * kWarps + w]});
-      out.timeout |= red_i[1 * kWarps + w];
+  if (warp == 0) {
+    if (lane < kWarps) {
+      out.t = MaxSum{red_f[0 * kWarps + lane], red_f[1 * kWarps + lane]};
+      out.d = MaxSum{red_f[2 * kWarps + lane], red_f[3 * kWarps + lane]};
+      out.a = ArgMax{red_f[4 * kWarps + lane], red_i[0 * kWarps + lane]};
+      out.timeout = red_i[1 * kWarps + lane];
     }
+    butterfly_stats(out.t, out.d, out.a, out.timeout, c);
   }
   return out;
 }
 
-// Shared-memory record each CTA publishes to its cluster.
-struct Part {
-  float tm, ts, dm, ds, av;
-  int ai, timeout, pad;
-  double sum[3];  // per-pass CTA sums of weights
-  float topv[SSD_MAX_TOPK];
-  int topi[SSD_MAX_TOPK];
+// ---------------------------------------------------------------------------
+// Push-based cluster exchange.  Every CTA owns an Inbox; for exchange e it
+// expects one record from each CTA of the cluster, delivered by st.async and
+// counted on its barrier xbar[e].  No CTA ever reads another CTA's shared
+// memory, so no CTA has to wait for its peers before it exits.
+// ---------------------------------------------------------------------------
+constexpr int kMaxCluster = 16;
+enum { kXStats = 0, kXSum0 = 1, kXSum1 = 2, kXSum2 = 3, kXTop = 4, kNumX = 5 };
+
+struct Inbox {
+  float4 stats[kMaxCluster][2];       // {t.m, t.s, d.m, d.s}, {argmax v, argmax i, timeout, 0}
+  double sums[3][kMaxCluster];        // per-pass CTA sums of weights
+  float4 top[kMaxCluster][4];         // top-8: 8 values, 8 indices (Saguaro, rank 0 only)
 };
 
-// Thread 0: combine every CTA's published statistics in rank order.
-__device__ __forceinline__ BlockStats cluster_combine_stats(const Part* part, int csize, float c) {
-  BlockStats out{{-INFINITY, 0.f}, {-INFINITY, 0.f}, {-INFINITY, -1}, 0};
-  for (int r = 0; r < csize; ++r) {
-    MaxSum t{dsmem_ld_f32(dsmem_addr(&part->tm, r)), dsmem_ld_f32(dsmem_addr(&part->ts, r))};
-    MaxSum d{dsmem_ld_f32(dsmem_addr(&part->dm, r)), dsmem_ld_f32(dsmem_addr(&part->ds, r))};
-    ArgMax a{dsmem_ld_f32(dsmem_addr(&part->av, r)), dsmem_ld_s32(dsmem_addr(&part->ai, r))};
-    out.t = combine_ms(out.t, t, c);
-    out.d = combine_ms(out.d, d, c);
-    out.a = better_arg(out.a, a);
-    out.timeout |= dsmem_ld_s32(dsmem_addr(&part->timeout, r));
+// Thread 0 at start-up: the exchange barriers and their expected bytes.
+__device__ __forceinline__ void inbox_init(uint64_t* xbar, int csize, bool want_top) {
+  for (int e = 0; e < kNumX; ++e) mbar_init(&xbar[e], 1);
+  fence_mbar_init();
+  mbar_arrive_expect_tx(&xbar[kXStats], static_cast<uint32_t>(csize) * 32u);
+  mbar_arrive_expect_tx(&xbar[kXSum0], static_cast<uint32_t>(csize) * 8u);
+  mbar_arrive_expect_tx(&xbar[kXSum1], static_cast<uint32_t>(csize) * 8u);
+  mbar_arrive_expect_tx(&xbar[kXSum2], static_cast<uint32_t>(csize) * 8u);
+  if (want_top) mbar_arrive_expect_tx(&xbar[kXTop], static_cast<uint32_t>(csize) * 64u);
+}
+
+// Warp 0: send this CTA's statistics (held by lane 0) to every CTA.
+__device__ __forceinline__ void push_stats(Inbox* inbox, uint64_t* xbar, int csize, int my_rank,
+                                           const BlockStats& bs) {
+  const int lane = threadIdx.x & 31;
+  float4 a = make_float4(bs.t.m, bs.t.s, bs.d.m, bs.d.s);
+  float4 b = make_float4(bs.a.v, __int_as_float(bs.a.i), __int_as_float(bs.timeout), 0.f);
+  a.x = __shfl_sync(0xFFFFFFFFu, a.x, 0);
+  a.y = __shfl_sync(0xFFFFFFFFu, a.y, 0);
+  a.z = __shfl_sync(0xFFFFFFFFu, a.z, 0);
+  a.w = __shfl_sync(0xFFFFFFFFu, a.w, 0);
+  b.x = __shfl_sync(0xFFFFFFFFu, b.x, 0);
+  b.y = __shfl_sync(0xFFFFFFFFu, b.y, 0);
+  b.z = __shfl_sync(0xFFFFFFFFu, b.z, 0);
+  if (lane < csize) {
+    const uint32_t bar = dsmem_addr(&xbar[kXStats], lane);
+    st_async_v4(dsmem_addr(&inbox->stats[my_rank][0], lane), a, bar);
+    st_async_v4(dsmem_addr(&inbox->stats[my_rank][1], lane), b, bar);
   }
+}
+
+// Warp 0: wait for every CTA's statistics and combine them.  The xor
+// butterfly applies the same (commutative) combine tree in every lane and in
+// every CTA, so all of them obtain bit-identical row statistics.
+__device__ __forceinline__ BlockStats gather_stats(Inbox* inbox, uint64_t* xbar, int csize, float c) {
+  const int lane = threadIdx.x & 31;
+  const bool ok = xbar_wait_bounded(&xbar[kXStats]);
+  BlockStats out{{-INFINITY, 0.f}, {-INFINITY, 0.f}, {-INFINITY, -1}, ok ? 0 : 1};
+  if (lane < csize) {
+    const float4 a = inbox->stats[lane][0], b = inbox->stats[lane][1];
+    out.t = MaxSum{a.x, a.y};
+    out.d = MaxSum{a.z, a.w};
+    out.a = ArgMax{b.x, __float_as_int(b.y)};
+    out.timeout |= __float_as_int(b.z);
+  }
+  butterfly_stats(out.t, out.d, out.a, out.timeout, c);
   return out;
+}
+
+// Warp 0: send this CTA's pass-p weight sum (held by lane 0) to every CTA.
+__device__ __forceinline__ void push_sum(Inbox* inbox, uint64_t* xbar, int csize, int my_rank, int p, double v) {
+  const int lane = threadIdx.x & 31;
+  v = __shfl_sync(0xFFFFFFFFu, v, 0);
+  if (lane < csize)
+    st_async_b64(dsmem_addr(&inbox->sums[p][my_rank], lane), static_cast<unsigned long long>(__double_as_longlong(v)),
+                 dsmem_addr(&xbar[kXSum0 + p], lane));
+}
+
+// Warp 0: wait for every CTA's pass-p sum; returns the cluster total and, for
+// the target u * total, the owning rank (-1 if the total is not positive), the
+// target minus the weight of the ranks before the owner (*local), and that
+// weight (*prefix).  A target beyond every boundary (rounding) goes to the
+// last rank with positive weight.  Identical in every lane and CTA.
+__device__ __forceinline__ double gather_sums(Inbox* inbox, uint64_t* xbar, int csize, int p, double u, int* owner,
+                                              double* local, double* prefix, int* timeout) {
+  const int lane = threadIdx.x & 31;
+  if (!xbar_wait_bounded(&xbar[kXSum0 + p])) *timeout = 1;
+  const double mine = lane < csize ? inbox->sums[p][lane] : 0.0;
+  double incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  const double tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+  *owner = -1;
+  *local = 0.0;
+  *prefix = 0.0;
+  if (!(tot > 0.0)) return tot;
+  const double target = u * tot;
+  const double excl = incl - mine;
+  const unsigned hit = __ballot_sync(0xFFFFFFFFu, lane < csize && mine > 0.0 && target < incl);
+  const unsigned pos = __ballot_sync(0xFFFFFFFFu, lane < csize && mine > 0.0);
+  const int r = hit ? __ffs(hit) - 1 : 31 - __clz(pos);
+  const double pre = __shfl_sync(0xFFFFFFFFu, excl, r);
+  *owner = r;
+  *prefix = pre;
+  *local = target - pre;
+  return tot;
 }
 
 // ---------------------------------------------------------------------------
@@ -687,46 +808,6 @@ __device__ __forceinline__ void cdf_search(const Slice<E>& sl, int lo, const WFu
     }
   }
   __syncthreads();
-}
-
-// Thread 0: cluster totals of pass `p` (CTA sums in rank order), the global
-// target u * total, and which CTA owns it.  Returns the total; *owner gets the
-// rank (-1 if the total is not positive), *local the target minus the weight
-// of the ranks before the owner, *prefix that weight.
-__device__ __forceinline__ double cluster_locate(const Part* part, int csize, int p, double u, int* owner,
-                                                 double* local, double* prefix) {
-  double tot = 0.0;
-  double sums[16];
-  for (int r = 0; r < csize; ++r) {
-    sums[r] = dsmem_ld_f64(dsmem_addr(&part->sum[p], r));
-    tot += sums[r];
-  }
-  *owner = -1;
-  *local = 0.0;
-  *prefix = 0.0;
-  if (!(tot > 0.0)) return tot;
-  const double target = u * tot;
-  double acc = 0.0;
-  int last_pos = -1;
-  double last_acc = 0.0;
-  for (int r = 0; r < csize; ++r) {
-    if (sums[r] > 0.0) {
-      last_pos = r;
-      last_acc = acc;
-      if (*owner < 0 && target < acc + sums[r]) {
-        *owner = r;
-        *local = target - acc;
-        *prefix = acc;
-      }
-    }
-    acc += sums[r];
-  }
-  if (*owner < 0) {
-    *owner = last_pos;
-    *local = target - last_acc;
-    *prefix = last_acc;
-  }
-  return tot;
 }
 
 }  // namespace ssdv

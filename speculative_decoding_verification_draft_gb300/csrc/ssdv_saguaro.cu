@@ -69,7 +69,10 @@ __global__ void __launch_bounds__(kThreads) saguaro_kernel(const SaguaroArgs a) 
   constexpr int kVec = Elem<E>::kVec;
   extern __shared__ __align__(128) uint8_t dyn_smem[];
   __shared__ __align__(8) uint64_t bars[kMaxStages];
-  __shared__ __align__(16) Part part;
+  __shared__ __align__(8) uint64_t xbar[kNumX];
+  __shared__ __align__(16) Inbox inbox;
+  __shared__ __align__(16) float cta_top_v[kTopK];
+  __shared__ __align__(16) int cta_top_i[kTopK];
   __shared__ float red_f[5 * kWarps];
   __shared__ int red_i[2 * kWarps];
   __shared__ float wsum[kWarps];
@@ -107,32 +110,30 @@ __global__ void __launch_bounds__(kThreads) saguaro_kernel(const SaguaroArgs a) 
   sl.nstage = (n + geo.stage_elems - 1) / geo.stage_elems;
   sl.bulk = geo.bulk != 0;
 
+  if (tid == 0) inbox_init(xbar, C, rank == 0);
   const float c = kLog2e / a.temperature;
   stage_issue(sl, bars, geo.stage_elems);
+  cluster_arrive_release();
   const ThreadStats<E> ts = stats_pass(sl, bars, geo.stage_elems / kVec, c, true, false, lo);
   const BlockStats bs = block_reduce_stats(ts, c, red_f, red_i);
-  if (tid == 0) {
-    part.tm = bs.t.m;
-    part.ts = bs.t.s;
-    part.dm = bs.d.m;
-    part.ds = bs.d.s;
-    part.timeout = bs.timeout;
-  }
-  cluster_sync();  // (1) statistics published
+  cluster_wait_acquire();
   const float u_sag = unit_draws(a.seed, b, j).saguaro;
   const size_t out_idx = static_cast<size_t>(b) * W + j;
   float* st = (a.stats && rank == 0) ? a.stats + out_idx * SSD_NSTAT_SAGUARO : nullptr;
-  if (tid == 0) {
-    const BlockStats all = cluster_combine_stats(&part, C, c);
-    sh_mt = all.t.m;
-    sh_zt = all.t.s;
-    sh_md = all.d.m;
-    sh_zd = all.d.s;
-    sh_err = all.timeout;
-    if (st) {
-      st[0] = logf(all.t.s) - fmaf(all.t.m, c, -scaled_max(all.t.m, c)) * 0.6931471805599453f;
-      st[1] = bonus ? NAN : logf(all.d.s) - fmaf(all.d.m, c, -scaled_max(all.d.m, c)) * 0.6931471805599453f;
-      st[7] = NAN;
+  if (warp == 0) {
+    push_stats(&inbox, xbar, C, rank, bs);
+    const BlockStats all = gather_stats(&inbox, xbar, C, c);
+    if (tid == 0) {
+      sh_mt = all.t.m;
+      sh_zt = all.t.s;
+      sh_md = all.d.m;
+      sh_zd = all.d.s;
+      sh_err = all.timeout;
+      if (st) {
+        st[0] = logf(all.t.s) - fmaf(all.t.m, c, -scaled_max(all.t.m, c)) * 0.6931471805599453f;
+        st[1] = bonus ? NAN : logf(all.d.s) - fmaf(all.d.m, c, -scaled_max(all.d.m, c)) * 0.6931471805599453f;
+        st[7] = NAN;
+      }
     }
   }
   __syncthreads();
@@ -142,7 +143,7 @@ __global__ void __launch_bounds__(kThreads) saguaro_kernel(const SaguaroArgs a) 
   const float kr = bonus ? 0.f : sh_zt / sh_zd;
 
   // Pass A: residual weights (or q at the bonus position / on zero residual
-  // mass), their sum, and each lane's top-8.
+  // mass), their cluster sum, and this CTA's top-8.
   int target_only = bonus ? 1 : 0;
   int p = 0;
   double sum_a = 0.0, resid_mass = 1.0;
@@ -162,66 +163,75 @@ __global__ void __launch_bounds__(kThreads) saguaro_kernel(const SaguaroArgs a) 
       }
     }
     __syncthreads();
-    if (tid == 0) {
-      int head[kWarps] = {0};
-      for (int r = 0; r < kTopK; ++r) {
-        int best = -1;
-        for (int w = 0; w < kWarps; ++w) {
-          if (head[w] >= kTopK) continue;
-          if (best < 0 || ranks_before(wtop_v[w][head[w]], wtop_i[w][head[w]], wtop_v[best][head[best]],
-                                       wtop_i[best][head[best]]))
-            best = w;
+    if (warp == 0) {
+      if (tid == 0) {
+        int head[kWarps] = {0};
+        for (int r = 0; r < kTopK; ++r) {
+          int best = -1;
+          for (int w = 0; w < kWarps; ++w) {
+            if (head[w] >= kTopK) continue;
+            if (best < 0 || ranks_before(wtop_v[w][head[w]], wtop_i[w][head[w]], wtop_v[best][head[best]],
+                                         wtop_i[best][head[best]]))
+              best = w;
+          }
+          cta_top_v[r] = wtop_v[best][head[best]];
+          cta_top_i[r] = wtop_i[best][head[best]];
+          ++head[best];
         }
-        part.topv[r] = wtop_v[best][head[best]];
-        part.topi[r] = wtop_i[best][head[best]];
-        ++head[best];
       }
-      part.sum[p] = cta;
-    }
-    cluster_sync();  // (2) pass-A sums and top-8 lists published
-    if (tid == 0) {
-      int owner;
+      push_sum(&inbox, xbar, C, rank, p, cta);
+      int owner, to = 0;
       double local, prefix;
-      sh_total = cluster_locate(&part, C, p, 0.5, &owner, &local, &prefix);
+      const double total = gather_sums(&inbox, xbar, C, p, 0.5, &owner, &local, &prefix, &to);
+      if (tid == 0) {
+        sh_total = total;
+        sh_err |= to;
+      }
     }
     __syncthreads();
     if (p == 0 && !bonus) resid_mass = sh_total / static_cast<double>(sh_zt);
     if (!(sh_total > 0.0) && !target_only) {
       target_only = 1;
       ++p;
-      __syncthreads();
       continue;
     }
     sum_a = sh_total;
     break;
   }
 
-  // Bonus prediction: merge the clusters' top-8 lists (rank 0 writes).
+  // Bonus prediction: every CTA sends its top-8 to rank 0, which merges them.
+  if (tid == 0) {
+    const uint32_t bar = dsmem_addr(&xbar[kXTop], 0);
+    const float4* v4 = reinterpret_cast<const float4*>(cta_top_v);
+    const float4* i4 = reinterpret_cast<const float4*>(cta_top_i);
+    st_async_v4(dsmem_addr(&inbox.top[rank][0], 0), v4[0], bar);
+    st_async_v4(dsmem_addr(&inbox.top[rank][1], 0), v4[1], bar);
+    st_async_v4(dsmem_addr(&inbox.top[rank][2], 0), i4[0], bar);
+    st_async_v4(dsmem_addr(&inbox.top[rank][3], 0), i4[1], bar);
+  }
   if (rank == 0 && tid == 0) {
-    float hv[16][kTopK];
-    int hi[16][kTopK];
-    int head[16];
-    for (int r = 0; r < C; ++r) {
-      head[r] = 0;
-      for (int s = 0; s < a.k; ++s) {
-        hv[r][s] = dsmem_ld_f32(dsmem_addr(&part.topv[s], r));
-        hi[r][s] = dsmem_ld_s32(dsmem_addr(&part.topi[s], r));
-      }
-    }
+    if (!xbar_wait_bounded(&xbar[kXTop])) sh_err = 1;
+    int head[kMaxCluster];
+    for (int r = 0; r < C; ++r) head[r] = 0;
     int32_t* out = a.bonus_topk + out_idx * a.k;
     for (int s = 0; s < a.k; ++s) {
       int best = -1;
+      float bv = 0.f;
+      int bi = 0;
       for (int r = 0; r < C; ++r) {
         if (head[r] >= a.k) continue;
-        if (best < 0 || ranks_before(hv[r][head[r]], hi[r][head[r]], hv[best][head[best]], hi[best][head[best]]))
+        const float* tv = reinterpret_cast<const float*>(&inbox.top[r][0]);
+        const int* ti = reinterpret_cast<const int*>(&inbox.top[r][2]);
+        if (best < 0 || ranks_before(tv[head[r]], ti[head[r]], bv, bi)) {
           best = r;
+          bv = tv[head[r]];
+          bi = ti[head[r]];
+        }
       }
-      const float v = hv[best][head[best]];
-      int id = hi[best][head[best]];
       ++head[best];
-      out[s] = (id >= 0 && id < V) ? id : -1;
-      if (st && s == 0) st[5] = static_cast<float>(v / sum_a);
-      if (st && s == a.k - 1) st[6] = static_cast<float>(v / sum_a);
+      out[s] = (bi >= 0 && bi < V && !sh_err) ? bi : -1;
+      if (st && s == 0) st[5] = static_cast<float>(bv / sum_a);
+      if (st && s == a.k - 1) st[6] = static_cast<float>(bv / sum_a);
     }
     if (st) st[2] = static_cast<float>(resid_mass);
   }
@@ -232,18 +242,21 @@ __global__ void __launch_bounds__(kThreads) saguaro_kernel(const SaguaroArgs a) 
   {
     TopK<0> none;
     const double cta = weighted_pass<E, 0>(sl, lo, mw, wsum, none);
-    if (tid == 0) part.sum[2] = cta;
+    if (warp == 0) {
+      push_sum(&inbox, xbar, C, rank, 2, cta);
+      int owner, to = 0;
+      double local, prefix;
+      const double total = gather_sums(&inbox, xbar, C, 2, static_cast<double>(u_sag), &owner, &local, &prefix, &to);
+      if (tid == 0) {
+        sh_total = total;
+        sh_owner = owner;
+        sh_local = local;
+        sh_prefix = prefix;
+        sh_err |= to;
+      }
+    }
+    __syncthreads();
   }
-  cluster_sync();  // (3) mix sums published
-  if (tid == 0) {
-    int owner;
-    double local, prefix;
-    sh_total = cluster_locate(&part, C, 2, static_cast<double>(u_sag), &owner, &local, &prefix);
-    sh_owner = owner;
-    sh_local = local;
-    sh_prefix = prefix;
-  }
-  __syncthreads();
   if (sh_owner == rank) {
     cdf_search(sl, lo, mw, wsum, sh_local, &sh_warp, &sh_base, &sh_result, &sh_edge, &sh_edge_w);
     if (tid == 0) a.saguaro_tokens[out_idx] = sh_err ? -1 : sh_result;
@@ -265,7 +278,6 @@ __global__ void __launch_bounds__(kThreads) saguaro_kernel(const SaguaroArgs a) 
     a.saguaro_tokens[out_idx] = -1;
   }
   if (sh_err) stage_drain(sl, bars);
-  cluster_sync();  // (4) every remote read done
 }
 
 template __global__ void saguaro_kernel<uint16_t>(const SaguaroArgs);

@@ -56,35 +56,49 @@ __device__ __forceinline__ bool temperature_ok(float T) {
 // Last unit of request b: scan the per-position decisions and write outputs.
 __device__ void finish_request(const VerifyArgs& a, int b, int g) {
   const int W = a.gmax + 1;
-  const int32_t* flag = a.unit_flag + static_cast<size_t>(b) * W;
-  const int32_t* tok = a.unit_tok + static_cast<size_t>(b) * W;
+  int32_t* wflag = a.unit_flag + static_cast<size_t>(b) * W;
+  int32_t* wtok = a.unit_tok + static_cast<size_t>(b) * W;
   int32_t* out = a.out_tokens + static_cast<size_t>(b) * W;
+  int32_t flags[SSD_MAX_GAMMA + 1];
+#pragma unroll 4
+  for (int k = 0; k <= g; ++k) flags[k] = ld_volatile(wflag + k);
   bool err = false;
-  for (int k = 0; k <= g; ++k) err |= ld_volatile(flag + k) < 0;
   int n = g;
-  for (int k = 0; k < g; ++k)
-    if (ld_volatile(flag + k) == 0) {
-      n = k;
-      break;
-    }
+  for (int k = g; k >= 0; --k) {
+    err |= flags[k] < 0;
+    if (k < g && flags[k] == 0) n = k;
+  }
   if (err) {
     for (int k = 0; k < W; ++k) out[k] = -1;
     a.n_accepted[b] = -1;
   } else {
+    const int32_t last = ld_volatile(wtok + n);
     for (int k = 0; k < n; ++k) out[k] = a.draft_tokens[static_cast<size_t>(b) * a.gmax + k];
-    out[n] = ld_volatile(tok + n);
+    out[n] = last;
     for (int k = n + 1; k < W; ++k) out[k] = -1;
     a.n_accepted[b] = n;
   }
   // Leave the whole workspace zeroed (its layout depends on B and gamma, so a
   // later call with another shape may read these words as arrival counters).
-  int32_t* wflag = a.unit_flag + static_cast<size_t>(b) * W;
-  int32_t* wtok = a.unit_tok + static_cast<size_t>(b) * W;
   for (int k = 0; k < W; ++k) {
     wflag[k] = 0;
     wtok[k] = 0;
   }
   a.ticket[b] = 0;
+}
+
+// Record unit (b, i)'s decision and count it; the last unit of the request
+// writes the outputs.  Called by one thread per unit.
+__device__ __forceinline__ void arrive_unit(const VerifyArgs& a, int b, int i, int g, int flag, int tok,
+                                            bool write_tok) {
+  const int out_idx = b * (a.gmax + 1) + i;
+  if (write_tok) a.unit_tok[out_idx] = tok;
+  a.unit_flag[out_idx] = flag;
+  __threadfence();
+  if (atomicAdd(a.ticket + b, 1) == g) {
+    __threadfence();
+    finish_request(a, b, g);
+  }
 }
 
 }  // namespace
@@ -94,7 +108,8 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const VerifyArgs a) {
   constexpr int kVec = Elem<E>::kVec;
   extern __shared__ __align__(128) uint8_t dyn_smem[];
   __shared__ __align__(8) uint64_t bars[kMaxStages];
-  __shared__ __align__(16) Part part;
+  __shared__ __align__(8) uint64_t xbar[kNumX];
+  __shared__ __align__(16) Inbox inbox;
   __shared__ float red_f[5 * kWarps];
   __shared__ int red_i[2 * kWarps];
   __shared__ float wsum[kWarps];
@@ -112,6 +127,7 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const VerifyArgs a) {
   const int b = unit / W;
   const int i = unit % W;
   const int tid = threadIdx.x;
+  const int warp = tid >> 5;
 
   const int g = a.gamma ? a.gamma[b] : a.gmax;
   const float T = a.temps ? a.temps[b] : a.temp_scalar;
@@ -138,6 +154,14 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const VerifyArgs a) {
     x = a.draft_tokens[static_cast<size_t>(b) * a.gmax + i];
     tok_err = (x < 0 || x >= V);
   }
+  const int out_idx = b * W + i;
+  if (tok_err) {  // the whole cluster agrees: no staging, no exchange
+    if (rank == 0 && tid == 0) {
+      atomicOr(a.status, 1 << SSD_ERR_TOKEN_RANGE);
+      arrive_unit(a, b, i, g, -1, 0, false);
+    }
+    return;
+  }
 
   const size_t trow = (static_cast<size_t>(b) * W + i) * V;
   const size_t drow = (static_cast<size_t>(b) * a.gmax + i) * V;
@@ -156,20 +180,6 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const VerifyArgs a) {
   sl.nstage = (n + geo.stage_elems - 1) / geo.stage_elems;
   sl.bulk = geo.bulk != 0;
 
-  const int out_idx = b * W + i;
-  if (tok_err) {  // the whole cluster agrees: no staging, no cluster barriers
-    if (rank == 0 && tid == 0) {
-      a.unit_flag[out_idx] = -1;
-      atomicOr(a.status, 1 << SSD_ERR_TOKEN_RANGE);
-      __threadfence();
-      if (atomicAdd(a.ticket + b, 1) == g) {
-        __threadfence();
-        finish_request(a, b, g);
-      }
-    }
-    return;
-  }
-
   // The two token logits of the accept test (sampled draft positions).
   float xt_tok = 0.f, xd_tok = 0.f;
   if (has_draft && tid == 0) {
@@ -177,150 +187,150 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const VerifyArgs a) {
     xd_tok = Elem<E>::to_float(dbase[drow + x]);
   }
 
+  if (tid == 0) inbox_init(xbar, C, false);
   const float c = greedy ? 1.f : kLog2e / T;
-  stage_issue(sl, bars, geo.stage_elems);
+  stage_issue(sl, bars, geo.stage_elems);  // (its __syncthreads also publishes the inbox barriers)
+  cluster_arrive_release();                // this CTA's inbox is ready
   const ThreadStats<E> ts =
       stats_pass(sl, bars, geo.stage_elems / kVec, c, /*want_exp=*/!greedy, /*want_arg=*/greedy, lo);
   const BlockStats bs = block_reduce_stats(ts, c, red_f, red_i);
-  if (tid == 0) {
-    part.tm = bs.t.m;
-    part.ts = bs.t.s;
-    part.dm = bs.d.m;
-    part.ds = bs.d.s;
-    part.av = bs.a.v;
-    part.ai = bs.a.i;
-    part.timeout = bs.timeout;
-  }
-  cluster_sync();  // (1) statistics published
-
+  cluster_wait_acquire();  // every inbox of the cluster is ready
   const Draws u = unit_draws(a.seed, b, i);
-  if (tid == 0) {
-    const BlockStats all = cluster_combine_stats(&part, C, c);
-    int accept = 0, need_pass = 0, err = all.timeout;
-    if (greedy) {
-      accept = (!bonus && x == all.a.i) ? 1 : 0;
-      sh_result = all.a.i;
-    } else if (bonus) {
-      need_pass = 1;
-    } else {
-      // a = min(1, q(x)/p(x)) with q(x) = e_t(x)/Z_t, p(x) = e_d(x)/Z_d, the
-      // ratio taken as one exp2 of the exponent difference.
-      const float mct = scaled_max(all.t.m, c), mcd = scaled_max(all.d.m, c);
-      float ratio_acc;
-      if (xd_tok == -INFINITY) {
-        ratio_acc = 1.f;
+  if (warp == 0) {
+    push_stats(&inbox, xbar, C, rank, bs);
+    const BlockStats all = gather_stats(&inbox, xbar, C, c);
+    if (tid == 0) {
+      int accept = 0, need_pass = 0, err = all.timeout;
+      if (greedy) {
+        accept = (!bonus && x == all.a.i) ? 1 : 0;
+        sh_result = all.a.i;
+      } else if (bonus) {
+        need_pass = 1;
       } else {
-        const float lt = fmaf(xt_tok, c, -mct), ld = fmaf(xd_tok, c, -mcd);
-        const float ratio = exp2f(lt - ld) * (all.d.s / all.t.s);
-        ratio_acc = fminf(1.f, ratio);
+        // a = min(1, q(x)/p(x)) with q(x) = e_t(x)/Z_t, p(x) = e_d(x)/Z_d, the
+        // ratio taken as one exp2 of the exponent difference.
+        const float mct = scaled_max(all.t.m, c), mcd = scaled_max(all.d.m, c);
+        float ratio_acc;
+        if (xd_tok == -INFINITY) {
+          ratio_acc = 1.f;
+        } else {
+          const float lt = fmaf(xt_tok, c, -mct), ld = fmaf(xd_tok, c, -mcd);
+          const float ratio = exp2f(lt - ld) * (all.d.s / all.t.s);
+          ratio_acc = fminf(1.f, ratio);
+        }
+        accept = u.accept < ratio_acc ? 1 : 0;
+        need_pass = (!accept || a.force_residual) ? 1 : 0;
+        if (a.stats && rank == 0) {
+          float* st = a.stats + static_cast<size_t>(out_idx) * SSD_NSTAT_VERIFY;
+          st[2] = all.d.m;
+          st[3] = logf(all.d.s) - fmaf(all.d.m, c, -mcd) * 0.6931471805599453f;
+          st[4] = exp2f(fmaf(xt_tok, c, -mct)) / all.t.s;
+          st[5] = exp2f(fmaf(xd_tok, c, -mcd)) / all.d.s;
+          st[7] = ratio_acc;
+        }
       }
-      accept = u.accept < ratio_acc ? 1 : 0;
-      need_pass = (!accept || a.force_residual) ? 1 : 0;
+      if (err) need_pass = 0;
       if (a.stats && rank == 0) {
         float* st = a.stats + static_cast<size_t>(out_idx) * SSD_NSTAT_VERIFY;
-        st[2] = all.d.m;
-        st[3] = logf(all.d.s) - fmaf(all.d.m, c, -mcd) * 0.6931471805599453f;
-        st[4] = exp2f(fmaf(xt_tok, c, -mct)) / all.t.s;
-        st[5] = exp2f(fmaf(xd_tok, c, -mcd)) / all.d.s;
-        st[7] = ratio_acc;
+        st[0] = greedy ? all.a.v : all.t.m;
+        // ln sum exp((x - m)/T): the sums carry the factor exp2(m*c - fl(m*c)).
+        if (!greedy) st[1] = logf(all.t.s) - fmaf(all.t.m, c, -scaled_max(all.t.m, c)) * 0.6931471805599453f;
       }
+      sh_accept = accept;
+      sh_pass = need_pass;
+      sh_err = err;
+      sh_mt = all.t.m;
+      sh_zt = all.t.s;
+      sh_md = all.d.m;
+      sh_zd = all.d.s;
     }
-    if (err) need_pass = 0;
-    if (a.stats && rank == 0) {
-      float* st = a.stats + static_cast<size_t>(out_idx) * SSD_NSTAT_VERIFY;
-      st[0] = greedy ? all.a.v : all.t.m;
-      // ln sum exp((x - m)/T): the sums carry the factor exp2(m*c - fl(m*c)).
-      if (!greedy) st[1] = logf(all.t.s) - fmaf(all.t.m, c, -scaled_max(all.t.m, c)) * 0.6931471805599453f;
-    }
-    sh_accept = accept;
-    sh_pass = need_pass;
-    sh_err = err;
-    sh_mt = all.t.m;
-    sh_zt = all.t.s;
-    sh_md = all.d.m;
-    sh_zd = all.d.s;
   }
   __syncthreads();
 
-  if (sh_pass) {
-    const float mct = scaled_max(sh_mt, c);
-    TopK<0> none;
-    int p = 0;
-    int use_target = bonus ? 1 : 0;
-    double total = 0.0;
-    double resid_mass = 0.0;
-    for (;;) {
-      double cta;
-      if (use_target) {
-        const TargetW<E> wf{c, mct};
-        cta = weighted_pass<E, 0>(sl, lo, wf, wsum, none);
-      } else {
-        const ResidualW<E> wf{c, mct, scaled_max(sh_md, c), sh_zt / sh_zd};
-        cta = weighted_pass<E, 0>(sl, lo, wf, wsum, none);
-      }
-      if (tid == 0) part.sum[p] = cta;
-      cluster_sync();  // (2) pass sums published
+  if (!sh_pass) {
+    // Decided without a draw (accepted, greedy, or an error): rank 0 reports.
+    if (rank == 0 && tid == 0)
+      arrive_unit(a, b, i, g, sh_err ? -1 : sh_accept, sh_result, greedy && !sh_err);
+    if (sh_err) stage_drain(sl, bars);
+    return;
+  }
+
+  // Residual (or bonus) pass over the resident slice, the cluster-wide sums,
+  // and the inverse-CDF draw in the CTA that owns the target.
+  const float mct = scaled_max(sh_mt, c);
+  TopK<0> none;
+  int p = 0;
+  int use_target = bonus ? 1 : 0;
+  double resid_mass = 0.0;
+  for (;;) {
+    double cta;
+    if (use_target) {
+      const TargetW<E> wf{c, mct};
+      cta = weighted_pass<E, 0>(sl, lo, wf, wsum, none);
+    } else {
+      const ResidualW<E> wf{c, mct, scaled_max(sh_md, c), sh_zt / sh_zd};
+      cta = weighted_pass<E, 0>(sl, lo, wf, wsum, none);
+    }
+    if (warp == 0) {
+      push_sum(&inbox, xbar, C, rank, p, cta);
+      int owner, to = 0;
+      double local, prefix;
+      const double total =
+          gather_sums(&inbox, xbar, C, p, static_cast<double>(u.resample), &owner, &local, &prefix, &to);
       if (tid == 0) {
-        int owner;
-        double local, prefix;
-        total = cluster_locate(&part, C, p, static_cast<double>(u.resample), &owner, &local, &prefix);
         sh_owner = owner;
         sh_local = local;
         sh_prefix = prefix;
         sh_total = total;
-      }
-      __syncthreads();
-      if (!use_target && p == 0 && tid == 0) resid_mass = total;
-      // Rejected with no residual mass: sample from q instead (same cluster-wide
-      // decision in every CTA: all of them read the same sums).
-      if (sh_owner < 0 && !use_target) {
-        use_target = 1;
-        ++p;
-        __syncthreads();
-        continue;
-      }
-      break;
-    }
-    if (a.stats && rank == 0 && tid == 0 && !bonus)
-      a.stats[static_cast<size_t>(out_idx) * SSD_NSTAT_VERIFY + 6] = static_cast<float>(resid_mass / sh_zt);
-    if (sh_owner == rank && (!sh_accept || bonus)) {
-      if (use_target) {
-        const TargetW<E> wf{c, mct};
-        cdf_search(sl, lo, wf, wsum, sh_local, &sh_warp, &sh_base, &sh_result, &sh_edge, &sh_edge_w);
-      } else {
-        const ResidualW<E> wf{c, mct, scaled_max(sh_md, c), sh_zt / sh_zd};
-        cdf_search(sl, lo, wf, wsum, sh_local, &sh_warp, &sh_base, &sh_result, &sh_edge, &sh_edge_w);
-      }
-      if (tid == 0) {
-        a.unit_tok[out_idx] = sh_result;
-        if (a.stats) {  // distances of u to the drawn token's CDF edges (debug statistics)
-          float* st = a.stats + static_cast<size_t>(out_idx) * SSD_NSTAT_VERIFY;
-          const double ur = static_cast<double>(u.resample);
-          st[8] = static_cast<float>(ur - (sh_prefix + sh_edge) / sh_total);
-          st[9] = static_cast<float>((sh_prefix + sh_edge + static_cast<double>(sh_edge_w)) / sh_total - ur);
-        }
-        __threadfence();
+        sh_err |= to;
+        if (!use_target && p == 0) resid_mass = total;
       }
     }
-  } else if (greedy && rank == 0 && tid == 0) {
-    a.unit_tok[out_idx] = sh_result;
+    __syncthreads();
+    // Rejected with no residual mass: sample from q instead (the same decision
+    // in every CTA: all of them received the same sums).
+    if (sh_owner < 0 && !use_target) {
+      use_target = 1;
+      ++p;
+      continue;
+    }
+    break;
   }
+  if (a.stats && rank == 0 && tid == 0 && !bonus)
+    a.stats[static_cast<size_t>(out_idx) * SSD_NSTAT_VERIFY + 6] = static_cast<float>(resid_mass / sh_zt);
 
-  if (sh_err) stage_drain(sl, bars);
-  cluster_sync();  // (3) every remote read done; the token is in global memory
-
-  if (rank == 0 && tid == 0) {
-    // A token was needed (rejection or bonus) but no positive weight exists:
-    // only possible for invalid input (e.g. NaN logits); report an error.
-    const bool no_token = sh_pass && (!sh_accept || bonus) && sh_owner < 0;
-    a.unit_flag[out_idx] = (sh_err || no_token) ? -1 : (bonus ? 1 : sh_accept);
+  const bool draws = !sh_accept || bonus;  // debug runs may pass accepted positions here
+  if (!draws) {
+    if (rank == 0 && tid == 0) arrive_unit(a, b, i, g, sh_err ? -1 : 1, 0, false);
+    if (sh_err) stage_drain(sl, bars);
+    return;
+  }
+  if (sh_owner < 0) {  // no positive weight at all: only possible for invalid input
+    if (rank == 0 && tid == 0) arrive_unit(a, b, i, g, -1, 0, false);
+    return;
+  }
+  if (sh_owner != rank) {
+    if (sh_err) stage_drain(sl, bars);
+    return;
+  }
+  if (use_target) {
+    const TargetW<E> wf{c, mct};
+    cdf_search(sl, lo, wf, wsum, sh_local, &sh_warp, &sh_base, &sh_result, &sh_edge, &sh_edge_w);
+  } else {
+    const ResidualW<E> wf{c, mct, scaled_max(sh_md, c), sh_zt / sh_zd};
+    cdf_search(sl, lo, wf, wsum, sh_local, &sh_warp, &sh_base, &sh_result, &sh_edge, &sh_edge_w);
+  }
+  if (tid == 0) {
+    if (a.stats) {  // distances of u to the drawn token's CDF edges (debug statistics)
+      float* st = a.stats + static_cast<size_t>(out_idx) * SSD_NSTAT_VERIFY;
+      const double ur = static_cast<double>(u.resample);
+      st[8] = static_cast<float>(ur - (sh_prefix + sh_edge) / sh_total);
+      st[9] = static_cast<float>((sh_prefix + sh_edge + static_cast<double>(sh_edge_w)) / sh_total - ur);
+    }
     if (sh_err) atomicOr(a.status, 1 << SSD_ERR_TIMEOUT);
-    __threadfence();
-    if (atomicAdd(a.ticket + b, 1) == g) {
-      __threadfence();
-      finish_request(a, b, g);
-    }
+    arrive_unit(a, b, i, g, sh_err ? -1 : (bonus ? 1 : 0), sh_result, true);
   }
+  if (sh_err) stage_drain(sl, bars);
 }
 
 template __global__ void verify_kernel<uint16_t>(const VerifyArgs);
