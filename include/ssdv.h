@@ -66,21 +66,21 @@ typedef enum {
 
 typedef enum { SSD_BF16 = 0, SSD_F32 = 1 } ssd_dtype;
 
-#define SSD_MAX_GAMMA 32   /* largest gamma / gamma_max accepted                 */
+#define SSD_MAX_GAMMA 31   /* largest gamma / gamma_max accepted                 */
 #define SSD_MAX_TOPK 8     /* largest k accepted by ssd_saguaro_prespec           */
 #define SSD_MAX_V (1 << 19)  /* fp32 units above ~440k need more than 16 CTAs */
 #define SSD_NSTAT_VERIFY 10
 #define SSD_NSTAT_SAGUARO 10
 
-/* Bytes of device workspace ssd_verify / ssd_verify_ragged need for a batch of
- * B requests with up to gamma_max draft tokens.  The workspace holds one
- * arrival counter per request, the per-position results and a status word. */
+/* Bytes of device workspace ssd_verify / ssd_verify_ragged / ssd_debug_rowstats
+ * need for a batch of B requests with up to gamma_max draft tokens.  The
+ * workspace holds a status word, per-chunk row statistics, per-chunk residual
+ * sums and arrival counters (the counters are cleared by every call). */
 size_t ssd_workspace_bytes(int B, int gamma_max);
 
-/* Zero a workspace (asynchronous memset on `stream`).  A workspace must be
- * zeroed once before its first use; every completed call leaves it zeroed
- * again (except the sticky status word, see ssd_read_status), so it can be
- * reused by later calls of any shape that fits it, on the same stream.  Two
+/* Zero a workspace (asynchronous memset on `stream`).  Zero a workspace once
+ * before its first use so that its status word starts clear; after that it can
+ * be reused by later calls of any shape that fits it, on the same stream.  Two
  * calls that may run at the same time on the GPU need two workspaces. */
 ssd_status ssd_workspace_init(void* workspace, size_t ws_bytes, void* stream);
 

@@ -54,9 +54,9 @@ WorkspaceLayout workspace_layout(int B, int gmax) {
   const size_t units = static_cast<size_t>(B) * static_cast<size_t>(gmax + 1);
   L.status = 0;
   L.ticket = 16;
-  L.unit_flag = L.ticket + round_up(4 * static_cast<size_t>(B), 16);
-  L.unit_tok = L.unit_flag + round_up(4 * units, 16);
-  L.total = round_up(L.unit_tok + 4 * units, 256);
+  L.part = round_up(L.ticket + 4 * units, 256);
+  L.csum = L.part + units * kMaxChunks * 2 * sizeof(float4);
+  L.total = round_up(L.csum + units * kMaxChunks * sizeof(double), 256);
   return L;
 }
 
@@ -98,6 +98,30 @@ ssd_status choose_geometry(int V, int esize, bool aligned, bool two_rows, Geomet
   }
 }
 
+// Split a row of V elements into chunks for verification: about 16 KB of each
+// row per CTA (SSDV_CHUNK_BYTES overrides), at most kMaxChunks chunks, each a
+// multiple of 8 elements.
+ssd_status choose_chunks(int V, int esize, bool aligned, ChunkGeometry* geo, int* smem_bytes) {
+  const int max_smem = max_dynamic_smem();
+  if (max_smem <= 0) return fail(SSD_ERR_CUDA, "cannot query the device's shared-memory limit");
+  const long long row_bytes = static_cast<long long>(V) * esize;
+  const int want = env_int("SSDV_CHUNK_BYTES", 16 * 1024);
+  long long nc = (row_bytes + want - 1) / want;
+  if (nc < 1) nc = 1;
+  if (nc > kMaxChunks) nc = kMaxChunks;
+  const int chunk = static_cast<int>(round_up((static_cast<size_t>(V) + nc - 1) / nc, 8));
+  const int row_smem = static_cast<int>(round_up(static_cast<size_t>(chunk) * esize, 128));
+  if (2 * row_smem > max_smem)
+    return fail(SSD_ERR_UNSUPPORTED, "V=%d: a chunk of %d elements does not fit in shared memory", V, chunk);
+  geo->V = V;
+  geo->chunk = chunk;
+  geo->nchunk = (V + chunk - 1) / chunk;
+  geo->row_smem = row_smem;
+  geo->bulk = aligned ? 1 : 0;
+  *smem_bytes = 2 * row_smem;
+  return SSD_OK;
+}
+
 namespace {
 
 ssd_status verify_common(const void* target, const void* draft, ssd_dtype dtype, const int32_t* draft_tokens, int B,
@@ -121,11 +145,11 @@ ssd_status verify_common(const void* target, const void* draft, ssd_dtype dtype,
     return fail(SSD_ERR_WORKSPACE, "workspace of %zu bytes < %zu required", ws_bytes, L.total);
   const bool aligned = aligned_to(target, 16) && (!draft || aligned_to(draft, 16)) &&
                        ((static_cast<size_t>(V) * es) % 16 == 0);
-  Geometry geo;
+  ChunkGeometry geo;
   int smem = 0;
-  ssd_status st = choose_geometry(V, es, aligned, !all_greedy, &geo, &smem);
+  ssd_status st = choose_chunks(V, es, aligned, &geo, &smem);
   if (st != SSD_OK) return st;
-  const long long ctas = static_cast<long long>(B) * (gmax + 1) * geo.csize;
+  const long long ctas = static_cast<long long>(B) * (gmax + 1) * geo.nchunk;
   if (ctas >= (1LL << 31)) return fail(SSD_ERR_SHAPE, "grid too large");
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   VerifyArgs a;
@@ -142,10 +166,10 @@ ssd_status verify_common(const void* target, const void* draft, ssd_dtype dtype,
   a.n_accepted = n_accepted;
   a.status = reinterpret_cast<int32_t*>(ws + L.status);
   a.ticket = reinterpret_cast<int32_t*>(ws + L.ticket);
-  a.unit_flag = reinterpret_cast<int32_t*>(ws + L.unit_flag);
-  a.unit_tok = reinterpret_cast<int32_t*>(ws + L.unit_tok);
+  a.part = reinterpret_cast<float4*>(ws + L.part);
+  a.csum = reinterpret_cast<double*>(ws + L.csum);
   a.stats = stats;
-  a.force_residual = stats ? 1 : 0;
+  a.debug = stats ? 1 : 0;
   a.geo = geo;
   const cudaError_t e = launch_verify(a, es, smem, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "verify launch");

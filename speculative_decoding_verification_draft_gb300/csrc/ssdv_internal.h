@@ -20,6 +20,18 @@ struct Geometry {
   int bulk;         // 1: rows 16-byte aligned, staged with bulk async copies
 };
 
+// How verification splits each row into chunks: the streaming kernel runs one
+// CTA per (request, position, chunk), the sampling kernel one CTA per
+// (request, chunk) (per (request, position, chunk) in the debug mode).
+struct ChunkGeometry {
+  int V;         // vocabulary size
+  int chunk;     // elements per chunk, a multiple of 8
+  int nchunk;    // chunks per row, 1..kMaxChunks
+  int row_smem;  // shared-memory bytes per staged row chunk (a multiple of 128)
+  int bulk;      // 1: rows 16-byte aligned, staged with bulk async copies
+};
+constexpr int kMaxChunks = 32;
+
 struct VerifyArgs {
   const void* target;          // [B, gmax+1, V]
   const void* draft;           // [B, gmax, V] (may be null if every request is greedy)
@@ -31,13 +43,13 @@ struct VerifyArgs {
   uint64_t seed;
   int32_t* out_tokens;         // [B, gmax+1]
   int32_t* n_accepted;         // [B]
-  int32_t* ticket;             // [B]        workspace: arrivals per request
-  int32_t* unit_flag;          // [B, gmax+1] workspace: 1 accept, 0 reject, -1 error
-  int32_t* unit_tok;           // [B, gmax+1] workspace: correction / bonus / greedy token
-  int32_t* status;             // [1]        workspace: device error bits
+  float4* part;                // workspace [B, gmax+1, nchunk, 2]: per-chunk row statistics
+  double* csum;                // workspace [B, gmax+1, nchunk]: per-chunk residual weight sums
+  int32_t* ticket;             // workspace [B, gmax+1]: residual chunks arrived
+  int32_t* status;             // workspace [1]: device error bits
   float* stats;                // [B, gmax+1, SSD_NSTAT_VERIFY] or null (debug)
-  int force_residual;          // debug: residual pass at every position
-  Geometry geo;
+  int debug;                   // 1: decide and report every position (statistics)
+  ChunkGeometry geo;
 };
 
 struct SaguaroArgs {
@@ -54,13 +66,17 @@ struct SaguaroArgs {
 
 // Workspace layout (byte offsets), shared by the launchers and the API.
 struct WorkspaceLayout {
-  size_t status, ticket, unit_flag, unit_tok, total;
+  size_t status, ticket, part, csum, total;
 };
 WorkspaceLayout workspace_layout(int B, int gmax);
+
+ssd_status choose_chunks(int V, int esize, bool aligned, ChunkGeometry* geo, int* smem_bytes);
 
 // Launch configuration for one call; returns SSD_OK or an error.
 ssd_status choose_geometry(int V, int esize, bool aligned, bool two_rows, Geometry* geo, int* smem_bytes);
 
+// Streaming statistics kernel followed (programmatic dependent launch) by the
+// decision / sampling kernel.
 cudaError_t launch_verify(const VerifyArgs& a, int esize, int smem_bytes, cudaStream_t stream);
 cudaError_t launch_saguaro(const SaguaroArgs& a, int esize, int smem_bytes, cudaStream_t stream);
 

@@ -8,19 +8,30 @@
 // token drawn from q_gamma.  Greedy requests (T = 0) accept while x_i equals
 // the target argmax.
 //
-// One cluster handles one (request b, position i) unit: it stages target row i
-// (and draft row i for a sampled draft position) into shared memory, reduces
-// the softmax statistics of both rows in the same pass, takes the accept
-// decision, and -- only if position i rejects, or i is the bonus position --
-// runs the on-chip residual pass and inverse-CDF search.  Every position is
-// decided independently; the last unit of a request to finish (arrival
-// ticket in the workspace, no spinning) scans the decisions to the first
-// rejection and writes the request's outputs.
+// Two kernels on the caller's stream:
+//  1. stream_kernel: one CTA per (request, position, vocabulary chunk) stages
+//     the target chunk (and the draft chunk of a sampled draft position) into
+//     shared memory with bulk async copies and reduces both in one pass to a
+//     32-byte record (max and sum of exponentials of each row, target argmax).
+//     Every logit is read from HBM exactly once, by short-lived CTAs.
+//  2. sample_kernel (programmatic dependent launch): the CTAs of a request
+//     combine the records, take every accept decision and find the first
+//     rejection n.  Only position n needs a draw: the bonus draw locates its
+//     chunk from the records and rescans one chunk; a residual draw runs one
+//     chunk-parallel pass over rows n (mostly L2-resident), the last CTA to
+//     arrive locates the chunk holding the target and rescans it.
 #include "ssdv_device.cuh"
 
 namespace ssdv {
 
 namespace {
+
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ bool temperature_ok(float T) { return T == 0.f || (T >= 1e-6f && T <= 3.0e38f); }
 
 // Residual weights scaled by Z_t: w = max(e_t - (Z_t/Z_d) e_d, 0) with
 // e = exp2(x*c - fl(m*c)).  Its sum is Z_t * sum (q - p)+.
@@ -49,292 +60,507 @@ struct TargetW {
   }
 };
 
-__device__ __forceinline__ bool temperature_ok(float T) {
-  return T == 0.f || (T >= 1e-6f && T <= 3.0e38f);
+// Stage one chunk (target and optionally draft) into shared memory: bulk
+// copies completing on `bar` (fresh phase 0), or plain loads padded with -inf
+// to a whole vector when the rows are not 16-byte aligned.  Returns false when
+// the bounded wait ran out.
+template <typename E>
+__device__ __forceinline__ bool stage_chunk(const Slice<E>& sl, uint64_t* bar) {
+  if (sl.bulk) {
+    if (threadIdx.x == 0) {
+      mbar_init(bar, 1);
+      fence_mbar_init();
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      const uint32_t bytes = static_cast<uint32_t>(sl.n) * sizeof(E);
+      mbar_arrive_expect_tx(bar, sl.gd ? 2 * bytes : bytes);
+      const uint64_t pol = l2_policy_evict_normal();
+      bulk_copy_g2s(sl.st, sl.gt, bytes, bar, pol);
+      if (sl.gd) bulk_copy_g2s(sl.sd, sl.gd, bytes, bar, pol);
+    }
+    __syncthreads();
+    return mbar_wait_bounded(bar, 0);
+  }
+  constexpr int kVec = Elem<E>::kVec;
+  const int padded = sl.nvec * kVec;
+  for (int e = threadIdx.x; e < padded; e += kThreads) {
+    sl.st[e] = e < sl.n ? sl.gt[e] : Elem<E>::neg_inf();
+    if (sl.gd) sl.sd[e] = e < sl.n ? sl.gd[e] : Elem<E>::neg_inf();
+  }
+  __syncthreads();
+  return true;
 }
 
-// Last unit of request b: scan the per-position decisions and write outputs.
-__device__ void finish_request(const VerifyArgs& a, int b, int g) {
+// One unit's combined row statistics (sampling kernel).
+struct UnitStat {
+  float tm, ts, dm, ds, av;
+  int ai, err;
+};
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Kernel 1: per-chunk row statistics.
+// ---------------------------------------------------------------------------
+template <typename E>
+__global__ void __launch_bounds__(kThreads) stream_kernel(const VerifyArgs a) {
+  constexpr int kVec = Elem<E>::kVec;
+  extern __shared__ __align__(128) uint8_t dyn_smem[];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ float red[4][kWarps];
+  __shared__ int red_i[kWarps];
+  __shared__ float sh_mt, sh_md;
+  griddep_launch_dependents();
+
+  const ChunkGeometry& geo = a.geo;
+  const int V = geo.V, NC = geo.nchunk, W = a.gmax + 1;
+  const int c = blockIdx.x % NC;
+  const int unit = blockIdx.x / NC;
+  const int b = unit / W, i = unit % W;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // The first CTA of each request clears the request's arrival counters for
+  // the sampling kernel (which only reads them after this grid completes).
+  if (i == 0 && c == 0 && tid < W) a.ticket[b * W + tid] = 0;
+
+  const int g = a.gamma ? a.gamma[b] : a.gmax;
+  const float T = a.temps ? a.temps[b] : a.temp_scalar;
+  if (g < 0 || g > a.gmax || !temperature_ok(T) || i > g) return;  // padded rows are never read
+  const bool greedy = (T == 0.f);
+  const bool has_draft = !greedy && i < g;
+
+  const int lo = c * geo.chunk;
+  Slice<E> sl;
+  sl.n = min(geo.chunk, V - lo);
+  sl.nvec = (sl.n + kVec - 1) / kVec;
+  sl.nstage = 1;
+  sl.bulk = geo.bulk != 0;
+  sl.gt = static_cast<const E*>(a.target) + (static_cast<size_t>(b) * W + i) * V + lo;
+  sl.gd = has_draft ? static_cast<const E*>(a.draft) + (static_cast<size_t>(b) * a.gmax + i) * V + lo : nullptr;
+  sl.st = reinterpret_cast<E*>(dyn_smem);
+  sl.sd = reinterpret_cast<E*>(dyn_smem + geo.row_smem);
+  const bool ok = stage_chunk(sl, &bar);
+
+  // pass 1: maxima (and the target argmax: each thread scans its vectors in
+  // index order, so the first of equal values is kept)
+  float mt = -INFINITY, md = -INFINITY;
+  ArgMax am{-INFINITY, -1};
+  for (int v = tid; v < sl.nvec; v += kThreads) {
+    float xt[kVec];
+    load_vec(sl.st, v, xt);
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) {
+      mt = fmaxf(mt, xt[e]);
+      if (greedy && (am.i < 0 || xt[e] > am.v)) {
+        am.v = xt[e];
+        am.i = lo + v * kVec + e;
+      }
+    }
+    if (has_draft) {
+      float xd[kVec];
+      load_vec(sl.sd, v, xd);
+#pragma unroll
+      for (int e = 0; e < kVec; ++e) md = fmaxf(md, xd[e]);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, o));
+    md = fmaxf(md, __shfl_xor_sync(0xFFFFFFFFu, md, o));
+    const ArgMax oa{__shfl_xor_sync(0xFFFFFFFFu, am.v, o), __shfl_xor_sync(0xFFFFFFFFu, am.i, o)};
+    am = better_arg(am, oa);
+  }
+  if (lane == 0) {
+    red[0][warp] = mt;
+    red[1][warp] = md;
+    red[2][warp] = am.v;
+    red_i[warp] = am.i;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float m0 = -INFINITY, m1 = -INFINITY;
+    ArgMax a0{-INFINITY, -1};
+    for (int w = 0; w < kWarps; ++w) {
+      m0 = fmaxf(m0, red[0][w]);
+      m1 = fmaxf(m1, red[1][w]);
+      a0 = better_arg(a0, ArgMax{red[2][w], red_i[w]});
+    }
+    sh_mt = m0;
+    sh_md = m1;
+    if (greedy) {
+      float4* rec = a.part + (static_cast<size_t>(unit) * NC + c) * 2;
+      rec[0] = make_float4(m0, 0.f, -INFINITY, 0.f);
+      rec[1] = make_float4(a0.v, __int_as_float(a0.i), __int_as_float(ok ? 0 : 1), 0.f);
+    }
+  }
+  __syncthreads();
+  if (greedy) return;
+
+  // pass 2: sums of exp2(x*c - fl(m*c)) against the chunk maxima
+  const float cc = kLog2e / T;
+  const float mct = scaled_max(sh_mt, cc), mcd = scaled_max(sh_md, cc);
+  float st = 0.f, sd = 0.f;
+  for (int v = tid; v < sl.nvec; v += kThreads) {
+    float xt[kVec], et[kVec];
+    load_vec(sl.st, v, xt);
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) et[e] = exp2f(fmaf(xt[e], cc, -mct));
+    st += pair_sum(et);
+    if (has_draft) {
+      float xd[kVec], ed[kVec];
+      load_vec(sl.sd, v, xd);
+#pragma unroll
+      for (int e = 0; e < kVec; ++e) ed[e] = exp2f(fmaf(xd[e], cc, -mcd));
+      sd += pair_sum(ed);
+    }
+  }
+  st = warp_sum(st);
+  sd = warp_sum(sd);
+  if (lane == 0) {
+    red[0][warp] = st;
+    red[1][warp] = sd;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float s0 = 0.f, s1 = 0.f;
+    for (int w = 0; w < kWarps; ++w) {
+      s0 += red[0][w];
+      s1 += red[1][w];
+    }
+    float4* rec = a.part + (static_cast<size_t>(unit) * NC + c) * 2;
+    rec[0] = make_float4(sh_mt, s0, has_draft ? sh_md : -INFINITY, s1);
+    rec[1] = make_float4(-INFINITY, __int_as_float(-1), __int_as_float(ok ? 0 : 1), 0.f);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Kernel 2: decisions and the draw.
+// ---------------------------------------------------------------------------
+namespace {
+
+__device__ void write_outputs(const VerifyArgs& a, int b, int n, int last, const int* tok_x) {
   const int W = a.gmax + 1;
-  int32_t* wflag = a.unit_flag + static_cast<size_t>(b) * W;
-  int32_t* wtok = a.unit_tok + static_cast<size_t>(b) * W;
   int32_t* out = a.out_tokens + static_cast<size_t>(b) * W;
-  int32_t flags[SSD_MAX_GAMMA + 1];
-#pragma unroll 4
-  for (int k = 0; k <= g; ++k) flags[k] = ld_volatile(wflag + k);
-  bool err = false;
-  int n = g;
-  for (int k = g; k >= 0; --k) {
-    err |= flags[k] < 0;
-    if (k < g && flags[k] == 0) n = k;
-  }
-  if (err) {
-    for (int k = 0; k < W; ++k) out[k] = -1;
-    a.n_accepted[b] = -1;
-  } else {
-    const int32_t last = ld_volatile(wtok + n);
-    for (int k = 0; k < n; ++k) out[k] = a.draft_tokens[static_cast<size_t>(b) * a.gmax + k];
-    out[n] = last;
-    for (int k = n + 1; k < W; ++k) out[k] = -1;
-    a.n_accepted[b] = n;
-  }
-  // Leave the whole workspace zeroed (its layout depends on B and gamma, so a
-  // later call with another shape may read these words as arrival counters).
-  for (int k = 0; k < W; ++k) {
-    wflag[k] = 0;
-    wtok[k] = 0;
-  }
-  a.ticket[b] = 0;
+  for (int k = 0; k < n; ++k) out[k] = tok_x[k];
+  out[n] = last;
+  for (int k = n + 1; k < W; ++k) out[k] = -1;
+  a.n_accepted[b] = n;
 }
 
-// Record unit (b, i)'s decision and count it; the last unit of the request
-// writes the outputs.  Called by one thread per unit.
-__device__ __forceinline__ void arrive_unit(const VerifyArgs& a, int b, int i, int g, int flag, int tok,
-                                            bool write_tok) {
-  const int out_idx = b * (a.gmax + 1) + i;
-  if (write_tok) a.unit_tok[out_idx] = tok;
-  a.unit_flag[out_idx] = flag;
-  __threadfence();
-  if (atomicAdd(a.ticket + b, 1) == g) {
-    __threadfence();
-    finish_request(a, b, g);
+__device__ void write_error(const VerifyArgs& a, int b) {
+  const int W = a.gmax + 1;
+  int32_t* out = a.out_tokens + static_cast<size_t>(b) * W;
+  for (int k = 0; k < W; ++k) out[k] = -1;
+  a.n_accepted[b] = -1;
+}
+
+// Warp 0: the chunk weights of q at unit u (the records' sums moved to the
+// row maximum), their fp64 inclusive scan, and the chunk holding u*total.
+__device__ __forceinline__ void locate_target_chunk(const VerifyArgs& a, int unit, float M, float cc, double u,
+                                                    int* owner, double* local, double* prefix, double* total) {
+  const int lane = threadIdx.x & 31, NC = a.geo.nchunk;
+  double w = 0.0;
+  if (lane < NC) {
+    const float4 r = a.part[(static_cast<size_t>(unit) * NC + lane) * 2];
+    w = (r.x == -INFINITY) ? 0.0 : static_cast<double>(r.y * rescale(r.x, M, cc));
   }
+  double incl = w;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  const double tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+  const double target = u * tot;
+  const unsigned hit = __ballot_sync(0xFFFFFFFFu, lane < NC && w > 0.0 && target < incl);
+  const unsigned pos = __ballot_sync(0xFFFFFFFFu, lane < NC && w > 0.0);
+  const int r = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : -1);
+  const double pre = __shfl_sync(0xFFFFFFFFu, incl - w, r >= 0 ? r : 0);
+  *owner = r;
+  *prefix = r >= 0 ? pre : 0.0;
+  *local = target - *prefix;
+  *total = tot;
 }
 
 }  // namespace
 
 template <typename E>
-__global__ void __launch_bounds__(kThreads) verify_kernel(const VerifyArgs a) {
-  constexpr int kVec = Elem<E>::kVec;
+__global__ void __launch_bounds__(kThreads) sample_kernel(const VerifyArgs a) {
   extern __shared__ __align__(128) uint8_t dyn_smem[];
-  __shared__ __align__(8) uint64_t bars[kMaxStages];
-  __shared__ __align__(8) uint64_t xbar[kNumX];
-  __shared__ __align__(16) Inbox inbox;
-  __shared__ float red_f[5 * kWarps];
-  __shared__ int red_i[2 * kWarps];
+  __shared__ __align__(8) uint64_t bar[2];
+  __shared__ UnitStat ust[SSD_MAX_GAMMA + 1];
+  __shared__ int tok_x[SSD_MAX_GAMMA];
+  __shared__ float tok_t[SSD_MAX_GAMMA], tok_d[SSD_MAX_GAMMA];
   __shared__ float wsum[kWarps];
-  __shared__ int sh_warp, sh_result, sh_owner, sh_accept, sh_pass, sh_err;
+  __shared__ int sh_n, sh_bad, sh_last, sh_owner, sh_warp, sh_result, sh_target_w;
+  __shared__ float sh_edge_w, sh_ures;
   __shared__ double sh_base, sh_local, sh_prefix, sh_total, sh_edge;
-  __shared__ float sh_edge_w;
-  __shared__ float sh_mt, sh_zt, sh_md, sh_zd;
+  constexpr int kVec = Elem<E>::kVec;
 
-  const Geometry& geo = a.geo;
-  const int V = geo.V;
-  const int C = geo.csize;
-  const int rank = static_cast<int>(cluster_rank());
-  const int unit = blockIdx.x / C;
-  const int W = a.gmax + 1;
-  const int b = unit / W;
-  const int i = unit % W;
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
+  const ChunkGeometry& geo = a.geo;
+  const int V = geo.V, NC = geo.nchunk, W = a.gmax + 1;
+  const int P = a.debug ? W : 1;
+  const int c = blockIdx.x % NC;
+  const int rest = blockIdx.x / NC;
+  const int pi = rest % P;
+  const int b = rest / P;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   const int g = a.gamma ? a.gamma[b] : a.gmax;
   const float T = a.temps ? a.temps[b] : a.temp_scalar;
-  const bool bad_gamma = g > a.gmax;
-  const bool bad_temp = !temperature_ok(T);
-  if (g < 0 || bad_gamma || bad_temp) {  // padded or invalid request: position 0 writes -1s
-    if (i == 0 && rank == 0 && tid == 0) {
-      int32_t* out = a.out_tokens + static_cast<size_t>(b) * W;
-      for (int k = 0; k < W; ++k) out[k] = -1;
-      a.n_accepted[b] = -1;
+  const bool bad_gamma = g > a.gmax, bad_temp = !temperature_ok(T);
+  if (g < 0 || bad_gamma || bad_temp) {  // padded or invalid request
+    if (pi == 0 && c == 0 && tid == 0) {
+      write_error(a, b);
       if (bad_gamma) atomicOr(a.status, 1 << SSD_ERR_GAMMA);
       if (bad_temp && g >= 0) atomicOr(a.status, 1 << SSD_ERR_TEMPERATURE);
     }
     return;
   }
-  if (i > g) return;
-
+  if (pi > g) return;
   const bool greedy = (T == 0.f);
-  const bool bonus = (i == g);
-  const bool has_draft = !greedy && !bonus;
-  int x = -1;
-  bool tok_err = false;
-  if (!bonus) {
-    x = a.draft_tokens[static_cast<size_t>(b) * a.gmax + i];
-    tok_err = (x < 0 || x >= V);
+  const E* tb = static_cast<const E*>(a.target);
+  const E* db = static_cast<const E*>(a.draft);
+
+  // Inputs only (overlaps the streaming kernel's tail): draft tokens and the
+  // two logits of each accept test.
+  if (warp == 0) {
+    bool bad = false;
+    if (lane < g) {
+      const int x = a.draft_tokens[static_cast<size_t>(b) * a.gmax + lane];
+      bad = x < 0 || x >= V;
+      tok_x[lane] = x;
+      if (!bad && !greedy) {
+        tok_t[lane] = Elem<E>::to_float(tb[(static_cast<size_t>(b) * W + lane) * V + x]);
+        tok_d[lane] = Elem<E>::to_float(db[(static_cast<size_t>(b) * a.gmax + lane) * V + x]);
+      }
+    }
+    const unsigned anybad = __ballot_sync(0xFFFFFFFFu, bad);
+    if (lane == 0) sh_bad = anybad != 0;
   }
-  const int out_idx = b * W + i;
-  if (tok_err) {  // the whole cluster agrees: no staging, no exchange
-    if (rank == 0 && tid == 0) {
+  __syncthreads();
+  if (sh_bad) {
+    if (pi == 0 && c == 0 && tid == 0) {
+      write_error(a, b);
       atomicOr(a.status, 1 << SSD_ERR_TOKEN_RANGE);
-      arrive_unit(a, b, i, g, -1, 0, false);
     }
     return;
   }
+  griddep_wait();  // the streaming kernel's records are complete and visible
 
-  const size_t trow = (static_cast<size_t>(b) * W + i) * V;
-  const size_t drow = (static_cast<size_t>(b) * a.gmax + i) * V;
-  const E* tbase = static_cast<const E*>(a.target);
-  const E* dbase = has_draft ? static_cast<const E*>(a.draft) : nullptr;
-  const int lo = rank * geo.slice;
-  const int n = max(0, min(geo.slice, V - lo));
-
-  Slice<E> sl;
-  sl.gt = tbase + trow + lo;
-  sl.gd = has_draft ? dbase + drow + lo : nullptr;
-  sl.st = reinterpret_cast<E*>(dyn_smem);
-  sl.sd = reinterpret_cast<E*>(dyn_smem + geo.row_smem);
-  sl.n = n;
-  sl.nvec = (n + kVec - 1) / kVec;
-  sl.nstage = (n + geo.stage_elems - 1) / geo.stage_elems;
-  sl.bulk = geo.bulk != 0;
-
-  // The two token logits of the accept test (sampled draft positions).
-  float xt_tok = 0.f, xd_tok = 0.f;
-  if (has_draft && tid == 0) {
-    xt_tok = Elem<E>::to_float(tbase[trow + x]);
-    xd_tok = Elem<E>::to_float(dbase[drow + x]);
-  }
-
-  if (tid == 0) inbox_init(xbar, C, false);
-  const float c = greedy ? 1.f : kLog2e / T;
-  stage_issue(sl, bars, geo.stage_elems);  // (its __syncthreads also publishes the inbox barriers)
-  cluster_arrive_release();                // this CTA's inbox is ready
-  const ThreadStats<E> ts =
-      stats_pass(sl, bars, geo.stage_elems / kVec, c, /*want_exp=*/!greedy, /*want_arg=*/greedy, lo);
-  const BlockStats bs = block_reduce_stats(ts, c, red_f, red_i);
-  cluster_wait_acquire();  // every inbox of the cluster is ready
-  const Draws u = unit_draws(a.seed, b, i);
-  if (warp == 0) {
-    push_stats(&inbox, xbar, C, rank, bs);
-    const BlockStats all = gather_stats(&inbox, xbar, C, c);
-    if (tid == 0) {
-      int accept = 0, need_pass = 0, err = all.timeout;
-      if (greedy) {
-        accept = (!bonus && x == all.a.i) ? 1 : 0;
-        sh_result = all.a.i;
-      } else if (bonus) {
-        need_pass = 1;
-      } else {
-        // a = min(1, q(x)/p(x)) with q(x) = e_t(x)/Z_t, p(x) = e_d(x)/Z_d, the
-        // ratio taken as one exp2 of the exponent difference.
-        const float mct = scaled_max(all.t.m, c), mcd = scaled_max(all.d.m, c);
-        float ratio_acc;
-        if (xd_tok == -INFINITY) {
-          ratio_acc = 1.f;
-        } else {
-          const float lt = fmaf(xt_tok, c, -mct), ld = fmaf(xd_tok, c, -mcd);
-          const float ratio = exp2f(lt - ld) * (all.d.s / all.t.s);
-          ratio_acc = fminf(1.f, ratio);
-        }
-        accept = u.accept < ratio_acc ? 1 : 0;
-        need_pass = (!accept || a.force_residual) ? 1 : 0;
-        if (a.stats && rank == 0) {
-          float* st = a.stats + static_cast<size_t>(out_idx) * SSD_NSTAT_VERIFY;
-          st[2] = all.d.m;
-          st[3] = logf(all.d.s) - fmaf(all.d.m, c, -mcd) * 0.6931471805599453f;
-          st[4] = exp2f(fmaf(xt_tok, c, -mct)) / all.t.s;
-          st[5] = exp2f(fmaf(xd_tok, c, -mcd)) / all.d.s;
-          st[7] = ratio_acc;
-        }
-      }
-      if (err) need_pass = 0;
-      if (a.stats && rank == 0) {
-        float* st = a.stats + static_cast<size_t>(out_idx) * SSD_NSTAT_VERIFY;
-        st[0] = greedy ? all.a.v : all.t.m;
-        // ln sum exp((x - m)/T): the sums carry the factor exp2(m*c - fl(m*c)).
-        if (!greedy) st[1] = logf(all.t.s) - fmaf(all.t.m, c, -scaled_max(all.t.m, c)) * 0.6931471805599453f;
-      }
-      sh_accept = accept;
-      sh_pass = need_pass;
-      sh_err = err;
-      sh_mt = all.t.m;
-      sh_zt = all.t.s;
-      sh_md = all.d.m;
-      sh_zd = all.d.s;
+  // Row statistics of every position of the request, combined from the chunk
+  // records (the same butterfly in every CTA: identical results).
+  const float cc = greedy ? 1.f : kLog2e / T;
+  for (int u = warp; u <= g; u += kWarps) {
+    MaxSum t{-INFINITY, 0.f}, d{-INFINITY, 0.f};
+    ArgMax am{-INFINITY, -1};
+    int err = 0;
+    if (lane < NC) {
+      const float4* rec = a.part + ((static_cast<size_t>(b) * W + u) * NC + lane) * 2;
+      const float4 r0 = rec[0], r1 = rec[1];
+      t = MaxSum{r0.x, r0.y};
+      d = MaxSum{r0.z, r0.w};
+      am = ArgMax{r1.x, __float_as_int(r1.y)};
+      err = __float_as_int(r1.z);
     }
+    butterfly_stats(t, d, am, err, cc);
+    if (lane == 0) ust[u] = UnitStat{t.m, t.s, d.m, d.s, am.v, am.i, err};
   }
   __syncthreads();
 
-  if (!sh_pass) {
-    // Decided without a draw (accepted, greedy, or an error): rank 0 reports.
-    if (rank == 0 && tid == 0)
-      arrive_unit(a, b, i, g, sh_err ? -1 : sh_accept, sh_result, greedy && !sh_err);
-    if (sh_err) stage_drain(sl, bars);
+  // Decisions: accept tests of positions 0..g-1 and the first rejection.
+  if (warp == 0) {
+    const Draws dr = unit_draws(a.seed, b, min(lane, g));
+    bool acc = true;
+    float ratio_acc = 1.f;
+    if (lane < g) {
+      const UnitStat s = ust[lane];
+      if (greedy) {
+        acc = tok_x[lane] == s.ai;
+      } else {
+        // a = min(1, q(x)/p(x)), the ratio as one exp2 of the exponent difference
+        if (tok_d[lane] != -INFINITY) {
+          const float lt = fmaf(tok_t[lane], cc, -scaled_max(s.tm, cc));
+          const float ld = fmaf(tok_d[lane], cc, -scaled_max(s.dm, cc));
+          ratio_acc = fminf(1.f, exp2f(lt - ld) * (s.ds / s.ts));
+        }
+        acc = dr.accept < ratio_acc;
+      }
+    }
+    const unsigned rej = __ballot_sync(0xFFFFFFFFu, lane < g && !acc);
+    const int n = rej ? __ffs(rej) - 1 : g;
+    if (lane == 0) {
+      sh_n = n;
+      sh_ures = unit_draws(a.seed, b, a.debug ? pi : n).resample;
+    }
+    if (a.stats && c == 0 && lane == pi) {
+      float* st = a.stats + (static_cast<size_t>(b) * W + pi) * SSD_NSTAT_VERIFY;
+      const UnitStat s = ust[pi];
+      if (greedy) {
+        st[0] = s.av;
+      } else {
+        st[0] = s.tm;
+        st[1] = logf(s.ts) - fmaf(s.tm, cc, -scaled_max(s.tm, cc)) * 0.6931471805599453f;
+        if (pi < g) {
+          const float mct = scaled_max(s.tm, cc), mcd = scaled_max(s.dm, cc);
+          st[2] = s.dm;
+          st[3] = logf(s.ds) - fmaf(s.dm, cc, -mcd) * 0.6931471805599453f;
+          st[4] = exp2f(fmaf(tok_t[pi], cc, -mct)) / s.ts;
+          st[5] = exp2f(fmaf(tok_d[pi], cc, -mcd)) / s.ds;
+          st[7] = ratio_acc;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  const int n = sh_n;
+  int err_any = 0;
+  for (int u = 0; u <= g; ++u) err_any |= ust[u].err;
+
+  if (greedy || err_any) {
+    if (pi == 0 && c == 0 && tid == 0) {
+      if (err_any) {
+        write_error(a, b);
+        atomicOr(a.status, 1 << SSD_ERR_TIMEOUT);
+      } else {
+        write_outputs(a, b, n, ust[n].ai, tok_x);
+      }
+    }
     return;
   }
+  const int pos = a.debug ? pi : n;
+  const UnitStat s = ust[pos];
+  const float mct = scaled_max(s.tm, cc);
+  const double ures = static_cast<double>(sh_ures);
+  const size_t trow = (static_cast<size_t>(b) * W + pos) * V;
+  const size_t drow = (static_cast<size_t>(b) * a.gmax + pos) * V;
 
-  // Residual (or bonus) pass over the resident slice, the cluster-wide sums,
-  // and the inverse-CDF draw in the CTA that owns the target.
-  const float mct = scaled_max(sh_mt, c);
-  TopK<0> none;
-  int p = 0;
-  int use_target = bonus ? 1 : 0;
-  double resid_mass = 0.0;
-  for (;;) {
-    double cta;
-    if (use_target) {
-      const TargetW<E> wf{c, mct};
-      cta = weighted_pass<E, 0>(sl, lo, wf, wsum, none);
-    } else {
-      const ResidualW<E> wf{c, mct, scaled_max(sh_md, c), sh_zt / sh_zd};
-      cta = weighted_pass<E, 0>(sl, lo, wf, wsum, none);
-    }
+  Slice<E> sl;
+  sl.nstage = 1;
+  sl.bulk = geo.bulk != 0;
+  sl.st = reinterpret_cast<E*>(dyn_smem);
+  sl.sd = reinterpret_cast<E*>(dyn_smem + geo.row_smem);
+
+  int owner = -1;
+  bool target_w = (pos == g);
+  if (pos == g) {
+    // Bonus draw from q_gamma: its chunk weights are the records' sums.
+    if (pos != n) return;
     if (warp == 0) {
-      push_sum(&inbox, xbar, C, rank, p, cta);
-      int owner, to = 0;
-      double local, prefix;
-      const double total =
-          gather_sums(&inbox, xbar, C, p, static_cast<double>(u.resample), &owner, &local, &prefix, &to);
-      if (tid == 0) {
+      double local, prefix, total;
+      locate_target_chunk(a, b * W + pos, s.tm, cc, ures, &owner, &local, &prefix, &total);
+      if (lane == 0) {
         sh_owner = owner;
         sh_local = local;
         sh_prefix = prefix;
         sh_total = total;
-        sh_err |= to;
-        if (!use_target && p == 0) resid_mass = total;
       }
     }
     __syncthreads();
-    // Rejected with no residual mass: sample from q instead (the same decision
-    // in every CTA: all of them received the same sums).
-    if (sh_owner < 0 && !use_target) {
-      use_target = 1;
-      ++p;
-      continue;
+    owner = sh_owner;
+    if (owner != c) return;
+  } else {
+    // Residual pass over chunk c of rows pos; the last chunk to arrive draws.
+    const int lo = c * geo.chunk;
+    sl.n = min(geo.chunk, V - lo);
+    sl.nvec = (sl.n + kVec - 1) / kVec;
+    sl.gt = tb + trow + lo;
+    sl.gd = db + drow + lo;
+    const bool ok = stage_chunk(sl, &bar[0]);
+    const ResidualW<E> wf{cc, mct, scaled_max(s.dm, cc), s.ts / s.ds};
+    TopK<0> none;
+    const double cta = weighted_pass<E, 0>(sl, lo, wf, wsum, none);
+    if (tid == 0) {
+      a.csum[(static_cast<size_t>(b) * W + pi) * NC + c] = ok ? cta : NAN;
+      __threadfence();
+      sh_last = atomicAdd(a.ticket + b * W + pi, 1) == NC - 1;
     }
-    break;
+    __syncthreads();
+    if (!sh_last) return;
+    __threadfence();
+    if (warp == 0) {
+      double w = 0.0;
+      if (lane < NC) w = *reinterpret_cast<volatile double*>(a.csum + (static_cast<size_t>(b) * W + pi) * NC + lane);
+      double incl = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const double t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const double tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+      double local = 0.0, prefix = 0.0, total = tot;
+      int tw = 0;
+      if (tot > 0.0) {
+        const double target = ures * tot;
+        const unsigned hit = __ballot_sync(0xFFFFFFFFu, lane < NC && w > 0.0 && target < incl);
+        const unsigned posm = __ballot_sync(0xFFFFFFFFu, lane < NC && w > 0.0);
+        owner = hit ? __ffs(hit) - 1 : 31 - __clz(posm);
+        prefix = __shfl_sync(0xFFFFFFFFu, incl - w, owner);
+        local = target - prefix;
+      } else {
+        // No residual mass (or an invalid sum): draw from q_pos instead.
+        locate_target_chunk(a, b * W + pos, s.tm, cc, ures, &owner, &local, &prefix, &total);
+        tw = 1;
+      }
+      if (lane == 0) {
+        if (a.stats)
+          a.stats[(static_cast<size_t>(b) * W + pi) * SSD_NSTAT_VERIFY + 6] = static_cast<float>(tot / s.ts);
+        a.ticket[b * W + pi] = 0;
+        sh_owner = owner;
+        sh_local = local;
+        sh_prefix = prefix;
+        sh_total = total;
+        sh_target_w = tw;
+      }
+    }
+    __syncthreads();
+    if (pos != n) return;
+    owner = sh_owner;
+    target_w = sh_target_w != 0;
+    if (owner < 0 || !(sh_total > 0.0)) {
+      if (tid == 0) {
+        write_error(a, b);
+        atomicOr(a.status, 1 << SSD_ERR_TIMEOUT);
+      }
+      return;
+    }
   }
-  if (a.stats && rank == 0 && tid == 0 && !bonus)
-    a.stats[static_cast<size_t>(out_idx) * SSD_NSTAT_VERIFY + 6] = static_cast<float>(resid_mass / sh_zt);
 
-  const bool draws = !sh_accept || bonus;  // debug runs may pass accepted positions here
-  if (!draws) {
-    if (rank == 0 && tid == 0) arrive_unit(a, b, i, g, sh_err ? -1 : 1, 0, false);
-    if (sh_err) stage_drain(sl, bars);
-    return;
-  }
-  if (sh_owner < 0) {  // no positive weight at all: only possible for invalid input
-    if (rank == 0 && tid == 0) arrive_unit(a, b, i, g, -1, 0, false);
-    return;
-  }
-  if (sh_owner != rank) {
-    if (sh_err) stage_drain(sl, bars);
-    return;
-  }
-  if (use_target) {
-    const TargetW<E> wf{c, mct};
+  // Draw: (re)stage the owning chunk and search it.
+  const int lo = owner * geo.chunk;
+  sl.n = min(geo.chunk, V - lo);
+  sl.nvec = (sl.n + kVec - 1) / kVec;
+  sl.gt = tb + trow + lo;
+  sl.gd = target_w ? nullptr : db + drow + lo;
+  __syncthreads();  // every read of the previous chunk is done before it is overwritten
+  const bool ok = stage_chunk(sl, &bar[1]);
+  TopK<0> none;
+  if (target_w) {
+    const TargetW<E> wf{cc, mct};
+    weighted_pass<E, 0>(sl, lo, wf, wsum, none);
     cdf_search(sl, lo, wf, wsum, sh_local, &sh_warp, &sh_base, &sh_result, &sh_edge, &sh_edge_w);
   } else {
-    const ResidualW<E> wf{c, mct, scaled_max(sh_md, c), sh_zt / sh_zd};
+    const ResidualW<E> wf{cc, mct, scaled_max(s.dm, cc), s.ts / s.ds};
+    weighted_pass<E, 0>(sl, lo, wf, wsum, none);
     cdf_search(sl, lo, wf, wsum, sh_local, &sh_warp, &sh_base, &sh_result, &sh_edge, &sh_edge_w);
   }
   if (tid == 0) {
-    if (a.stats) {  // distances of u to the drawn token's CDF edges (debug statistics)
-      float* st = a.stats + static_cast<size_t>(out_idx) * SSD_NSTAT_VERIFY;
-      const double ur = static_cast<double>(u.resample);
-      st[8] = static_cast<float>(ur - (sh_prefix + sh_edge) / sh_total);
-      st[9] = static_cast<float>((sh_prefix + sh_edge + static_cast<double>(sh_edge_w)) / sh_total - ur);
+    if (!ok || sh_result < 0) {
+      write_error(a, b);
+      atomicOr(a.status, 1 << SSD_ERR_TIMEOUT);
+      return;
     }
-    if (sh_err) atomicOr(a.status, 1 << SSD_ERR_TIMEOUT);
-    arrive_unit(a, b, i, g, sh_err ? -1 : (bonus ? 1 : 0), sh_result, true);
+    if (a.stats) {  // distances of u to the drawn token's CDF edges (debug statistics)
+      float* st = a.stats + (static_cast<size_t>(b) * W + pos) * SSD_NSTAT_VERIFY;
+      st[8] = static_cast<float>(ures - (sh_prefix + sh_edge) / sh_total);
+      st[9] = static_cast<float>((sh_prefix + sh_edge + static_cast<double>(sh_edge_w)) / sh_total - ures);
+    }
+    write_outputs(a, b, n, sh_result, tok_x);
   }
-  if (sh_err) stage_drain(sl, bars);
 }
 
-template __global__ void verify_kernel<uint16_t>(const VerifyArgs);
-template __global__ void verify_kernel<float>(const VerifyArgs);
+template __global__ void stream_kernel<uint16_t>(const VerifyArgs);
+template __global__ void stream_kernel<float>(const VerifyArgs);
+template __global__ void sample_kernel<uint16_t>(const VerifyArgs);
+template __global__ void sample_kernel<float>(const VerifyArgs);
 
 __global__ void uniforms_kernel(uint64_t seed, int B, int W, float* out) {
   const long long n = static_cast<long long>(B) * W;
@@ -354,30 +580,52 @@ cudaError_t launch_uniforms(uint64_t seed, int B, int W, float* out, cudaStream_
   return cudaGetLastError();
 }
 
-cudaError_t launch_verify(const VerifyArgs& a, int esize, int smem_bytes, cudaStream_t stream) {
-  const void* fn = esize == 2 ? reinterpret_cast<const void*>(&verify_kernel<uint16_t>)
-                              : reinterpret_cast<const void*>(&verify_kernel<float>);
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+namespace {
+
+// cudaFuncSetAttribute once per (kernel, size) on the current device.
+cudaError_t ensure_smem(const void* fn, int smem_bytes, int* cached) {
+  if (*cached == smem_bytes) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  if (e == cudaSuccess) *cached = smem_bytes;
+  return e;
+}
+
+template <typename E>
+cudaError_t launch_verify_t(const VerifyArgs& a, int smem_bytes, cudaStream_t stream) {
+  static thread_local int dev_cached = -1, smem1 = -1, smem2 = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (a.geo.csize > 8) {
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
+  if (dev != dev_cached) {
+    smem1 = smem2 = -1;
+    dev_cached = dev;
   }
+  e = ensure_smem(reinterpret_cast<const void*>(&stream_kernel<E>), smem_bytes, &smem1);
+  if (e != cudaSuccess) return e;
+  e = ensure_smem(reinterpret_cast<const void*>(&sample_kernel<E>), smem_bytes, &smem2);
+  if (e != cudaSuccess) return e;
   const long long units = static_cast<long long>(a.B) * (a.gmax + 1);
+  stream_kernel<E><<<static_cast<unsigned>(units * a.geo.nchunk), kThreads, smem_bytes, stream>>>(a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int P = a.debug ? a.gmax + 1 : 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(units * a.geo.csize), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(static_cast<long long>(a.B) * P * a.geo.nchunk), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = a.geo.csize;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (esize == 2) return cudaLaunchKernelEx(&cfg, verify_kernel<uint16_t>, a);
-  return cudaLaunchKernelEx(&cfg, verify_kernel<float>, a);
+  return cudaLaunchKernelEx(&cfg, sample_kernel<E>, a);
+}
+
+}  // namespace
+
+cudaError_t launch_verify(const VerifyArgs& a, int esize, int smem_bytes, cudaStream_t stream) {
+  return esize == 2 ? launch_verify_t<uint16_t>(a, smem_bytes, stream) : launch_verify_t<float>(a, smem_bytes, stream);
 }
 
 }  // namespace ssdv
