@@ -56,7 +56,8 @@ WorkspaceLayout workspace_layout(int B, int gmax) {
   L.ticket = 16;
   L.part = round_up(L.ticket + 4 * units, 256);
   L.csum = L.part + units * kMaxChunks * 2 * sizeof(float4);
-  L.total = round_up(L.csum + units * kMaxChunks * sizeof(double), 256);
+  L.wsums = L.csum + units * kMaxChunks * sizeof(double);
+  L.total = round_up(L.wsums + units * kMaxChunks * kWarps * sizeof(float), 256);
   return L;
 }
 
@@ -168,6 +169,7 @@ ssd_status verify_common(const void* target, const void* draft, ssd_dtype dtype,
   a.ticket = reinterpret_cast<int32_t*>(ws + L.ticket);
   a.part = reinterpret_cast<float4*>(ws + L.part);
   a.csum = reinterpret_cast<double*>(ws + L.csum);
+  a.wsums = reinterpret_cast<float*>(ws + L.wsums);
   a.stats = stats;
   a.debug = stats ? 1 : 0;
   a.geo = geo;

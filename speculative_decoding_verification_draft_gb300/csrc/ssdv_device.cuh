@@ -35,6 +35,21 @@ struct Elem;
 template <>
 struct Elem<uint16_t> {
   static constexpr int kVec = 8;  // elements per 16-byte vector
+  // running maximum of raw vectors, two bf16 lanes per word (max.bf16x2 is
+  // exact: it only selects one of its inputs)
+  static __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+  }
+  static __device__ __forceinline__ uint4 max_init() { return make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u); }
+  static __device__ __forceinline__ uint4 max_acc(uint4 acc, const uint4& v) {
+    return make_uint4(bmax2(acc.x, v.x), bmax2(acc.y, v.y), bmax2(acc.z, v.z), bmax2(acc.w, v.w));
+  }
+  static __device__ __forceinline__ float max_final(const uint4& acc) {
+    const uint32_t m = bmax2(bmax2(acc.x, acc.y), bmax2(acc.z, acc.w));
+    return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u));
+  }
   static __device__ __forceinline__ float to_float(uint16_t h) {
     return __uint_as_float(static_cast<uint32_t>(h) << 16);
   }
@@ -53,6 +68,21 @@ struct Elem<uint16_t> {
 template <>
 struct Elem<float> {
   static constexpr int kVec = 4;
+  // running maximum of raw vectors (kept as four floats)
+  static __device__ __forceinline__ uint4 max_init() {
+    const uint32_t n = __float_as_uint(-INFINITY);
+    return make_uint4(n, n, n, n);
+  }
+  static __device__ __forceinline__ uint4 max_acc(uint4 acc, const uint4& v) {
+    return make_uint4(__float_as_uint(fmaxf(__uint_as_float(acc.x), __uint_as_float(v.x))),
+                      __float_as_uint(fmaxf(__uint_as_float(acc.y), __uint_as_float(v.y))),
+                      __float_as_uint(fmaxf(__uint_as_float(acc.z), __uint_as_float(v.z))),
+                      __float_as_uint(fmaxf(__uint_as_float(acc.w), __uint_as_float(v.w))));
+  }
+  static __device__ __forceinline__ float max_final(const uint4& acc) {
+    return fmaxf(fmaxf(__uint_as_float(acc.x), __uint_as_float(acc.y)),
+                 fmaxf(__uint_as_float(acc.z), __uint_as_float(acc.w)));
+  }
   static __device__ __forceinline__ float to_float(float x) { return x; }
   static __device__ __forceinline__ float neg_inf() { return -INFINITY; }
   static __device__ __forceinline__ void unpack(const uint4& v, float (&f)[4]) {
@@ -62,6 +92,17 @@ struct Elem<float> {
     f[3] = __uint_as_float(v.w);
   }
 };
+
+// ---------------------------------------------------------------------------
+// 2^x as one ex2.approx.ftz.f32 instruction (relative error about 2 ulp;
+// results below 2^-126 flush to zero, which no sum here can notice).  Every
+// weight and every partial sum of a row uses this same function.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 // ---------------------------------------------------------------------------
 // PTX wrappers
@@ -233,7 +274,7 @@ struct MaxSum {
 __device__ __forceinline__ float scaled_max(float m, float c) { return __fmul_rn(m, c); }
 // exp2(fl(m_from*c) - fl(m_to*c)): moves a partial sum from one reference max to another.
 __device__ __forceinline__ float rescale(float m_from, float m_to, float c) {
-  return exp2f(__fsub_rn(scaled_max(m_from, c), scaled_max(m_to, c)));
+  return fast_exp2(__fsub_rn(scaled_max(m_from, c), scaled_max(m_to, c)));
 }
 __device__ __forceinline__ MaxSum combine_ms(MaxSum a, MaxSum b, float c) {
   const float M = fmaxf(a.m, b.m);
@@ -401,12 +442,12 @@ __device__ __forceinline__ ThreadStats<E> stats_pass(const Slice<E>& sl, uint64_
       if (!have[k]) continue;
       float et[kVec];
 #pragma unroll
-      for (int e = 0; e < kVec; ++e) et[e] = exp2f(fmaf(ft[k][e], c, -mct));
+      for (int e = 0; e < kVec; ++e) et[e] = fast_exp2(fmaf(ft[k][e], c, -mct));
       r.t.s += pair_sum(et);
       if (sl.gd) {
         float ed[kVec];
 #pragma unroll
-        for (int e = 0; e < kVec; ++e) ed[e] = exp2f(fmaf(fd[k][e], c, -mcd));
+        for (int e = 0; e < kVec; ++e) ed[e] = fast_exp2(fmaf(fd[k][e], c, -mcd));
         r.d.s += pair_sum(ed);
       }
     }
@@ -683,42 +724,150 @@ __device__ __forceinline__ void warp_merge_topk(TopK<K>& tk, float (&ov)[K], int
 }
 
 // ---------------------------------------------------------------------------
-// Inverse-CDF search inside this CTA's slice for the local target tl (the
-// global target minus the weight of the CTAs before this one).  Thread 0
-// picks the warp from wsum[]; that warp rescans its run with a warp prefix
-// scan and fp64 carries.  If rounding leaves the target beyond every
-// boundary, the last element with positive weight is taken.  Writes the
-// global token to *result, and the drawn element's CDF position (weight
-// before it, relative to this CTA's start; NaN after a rounding fallback)
-// and weight to *edge_lo / *edge_w (all in shared memory).
+// Inverse-CDF search.
+//
+// pick_warp (thread 0): given per-warp sums of a chunk and a target tl
+// relative to the chunk start, the warp whose run holds tl and the weight
+// before that run (a target beyond every boundary through rounding goes to
+// the last warp with positive weight; -1 if none).
+//
+// warp_scan (one warp): scans vectors [v0, v1) with a warp prefix scan and
+// fp64 carries for the smallest element whose running sum exceeds tl (tl
+// relative to v0; again falling back to the last positive element).  `load`
+// fills the target / draft values of vector v and `wfun` turns them into
+// weights.  Returns in every lane the element index relative to the chunk
+// start (-1 if no positive weight), its CDF position relative to v0 and its
+// weight.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ int pick_warp(const float* wsum, int nwarps, double tl, double* base) {
+  double acc = 0.0;
+  int pick = -1, last_pos = -1;
+  double pick_base = 0.0, last_base = 0.0;
+  for (int w = 0; w < nwarps; ++w) {
+    const double ws = static_cast<double>(wsum[w]);
+    if (ws > 0.0) {
+      last_pos = w;
+      last_base = acc;
+    }
+    if (pick < 0 && ws > 0.0 && tl < acc + ws) {
+      pick = w;
+      pick_base = acc;
+    }
+    acc += ws;
+  }
+  if (pick < 0) {
+    pick = last_pos;
+    pick_base = last_base;
+  }
+  *base = pick_base;
+  return pick;
+}
+
+struct ScanHit {
+  int elem;     // element index relative to the chunk start, -1 if none
+  double edge;  // weight before the element, relative to the scan start
+  float w;      // the element's weight
+};
+
+template <int kVec, typename Load, typename WFun>
+__device__ __forceinline__ ScanHit warp_scan(int v0, int v1, double tl, const Load& load, const WFun& wfun) {
+  const int lane = threadIdx.x & 31;
+  double carry = 0.0;
+  ScanHit hit{-1, NAN, 0.f};
+  int last_vec = -1;  // last vector with positive weight
+  for (int vb = v0; vb < v1 && hit.elem < 0; vb += 32) {
+    const int v = vb + lane;
+    float w[kVec];
+    float vs = 0.f;
+    if (v < v1) {
+      float xt[kVec], xd[kVec];
+      load(v, xt, xd);
+      wfun(xt, xd, w);
+      vs = pair_sum(w);
+    } else {
+#pragma unroll
+      for (int e = 0; e < kVec; ++e) w[e] = 0.f;
+    }
+    float incl = vs;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const float total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    const unsigned pos = __ballot_sync(0xFFFFFFFFu, vs > 0.f);
+    if (pos) last_vec = vb + 31 - __clz(pos);
+    const unsigned hm = __ballot_sync(0xFFFFFFFFu, (vs > 0.f) && (tl < carry + static_cast<double>(incl)));
+    if (hm) {
+      const int L = __ffs(hm) - 1;
+      int tok = -1;
+      double edge = 0.0;
+      float wt = 0.f;
+      if (lane == L) {
+        double a = carry + static_cast<double>(incl - vs);
+        int last_e = -1;
+        double a_last = a;
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) {
+          const double before = a;
+          if (w[e] > 0.f) {
+            last_e = e;
+            a_last = before;
+          }
+          a += static_cast<double>(w[e]);
+          if (tok < 0 && w[e] > 0.f && tl < a) {
+            tok = e;
+            edge = before;
+          }
+        }
+        if (tok < 0) {
+          tok = last_e;
+          edge = a_last;
+        }
+#pragma unroll
+        for (int e = 0; e < kVec; ++e)
+          if (e == tok) wt = w[e];
+        tok = v * kVec + tok;
+      }
+      hit.elem = __shfl_sync(0xFFFFFFFFu, tok, L);
+      hit.edge = __shfl_sync(0xFFFFFFFFu, edge, L);
+      hit.w = __shfl_sync(0xFFFFFFFFu, wt, L);
+    }
+    carry += static_cast<double>(total);
+  }
+  if (hit.elem < 0 && last_vec >= 0) {
+    // rounding left the target past the run: take its last positive element
+    int e_last = kVec - 1;
+    float wl = 0.f;
+    if (lane == 0) {
+      float xt[kVec], xd[kVec], w[kVec];
+      load(last_vec, xt, xd);
+      wfun(xt, xd, w);
+#pragma unroll
+      for (int e = 0; e < kVec; ++e)
+        if (w[e] > 0.f) {
+          e_last = e;
+          wl = w[e];
+        }
+    }
+    hit.elem = __shfl_sync(0xFFFFFFFFu, last_vec * kVec + e_last, 0);
+    hit.w = __shfl_sync(0xFFFFFFFFu, wl, 0);
+    hit.edge = NAN;
+  }
+  return hit;
+}
+
+// The search inside a slice resident in shared memory whose per-warp sums
+// (from weighted_pass) are in wsum[].  Writes the global token to *result,
+// the drawn element's CDF position relative to this CTA's start (NaN after a
+// rounding fallback) to *edge_lo and its weight to *edge_w (shared memory).
 template <typename E, typename WFun>
 __device__ __forceinline__ void cdf_search(const Slice<E>& sl, int lo, const WFun& wfun, const float* wsum, double tl,
                                            int* sh_warp, double* sh_base, int* result, double* edge_lo,
                                            float* edge_w) {
   constexpr int kVec = Elem<E>::kVec;
   if (threadIdx.x == 0) {
-    double acc = 0.0;
-    int pick = -1, last_pos = -1;
-    double pick_base = 0.0, last_base = 0.0;
-    for (int w = 0; w < kWarps; ++w) {
-      const double ws = static_cast<double>(wsum[w]);
-      if (ws > 0.0) {
-        last_pos = w;
-        last_base = acc;
-      }
-      if (pick < 0 && ws > 0.0 && tl < acc + ws) {
-        pick = w;
-        pick_base = acc;
-      }
-      acc += ws;
-    }
-    if (pick < 0) {
-      pick = last_pos;
-      pick_base = last_base;
-    }
-    *sh_warp = pick;
-    *sh_base = pick_base;
+    *sh_warp = pick_warp(wsum, kWarps, tl, sh_base);
     *result = -1;
     *edge_lo = NAN;
     *edge_w = 0.f;
@@ -729,88 +878,16 @@ __device__ __forceinline__ void cdf_search(const Slice<E>& sl, int lo, const WFu
   if (pick >= 0 && warp == pick) {
     int v0, v1;
     warp_range(sl.nvec, warp, v0, v1);
-    double carry = *sh_base;
-    int found = -1;
-    double found_edge = NAN;
-    float found_w = 0.f;
-    int last_vec = -1;  // last vector in the run with positive weight
-    for (int vb = v0; vb < v1 && found < 0; vb += 32) {
-      const int v = vb + lane;
-      float w[kVec];
-      float vs = 0.f;
-      if (v < v1) {
-        float xt[kVec], xd[kVec];
-        load_vec(sl.st, v, xt);
-        if (sl.gd) load_vec(sl.sd, v, xd);
-        wfun(xt, xd, w);
-        vs = pair_sum(w);
-      } else {
-#pragma unroll
-        for (int e = 0; e < kVec; ++e) w[e] = 0.f;
-      }
-      float incl = vs;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += t;
-      }
-      const float total = __shfl_sync(0xFFFFFFFFu, incl, 31);
-      const unsigned pos = __ballot_sync(0xFFFFFFFFu, vs > 0.f);
-      if (pos) last_vec = vb + 31 - __clz(pos);
-      const bool hit = (vs > 0.f) && (tl < carry + static_cast<double>(incl));
-      const unsigned hm = __ballot_sync(0xFFFFFFFFu, hit);
-      if (hm) {
-        const int L = __ffs(hm) - 1;
-        int tok = -1;
-        double edge = 0.0;
-        float wt = 0.f;
-        if (lane == L) {
-          double a = carry + static_cast<double>(incl - vs);
-          int last_e = -1;
-          double a_last = a;
-#pragma unroll
-          for (int e = 0; e < kVec; ++e) {
-            const double before = a;
-            if (w[e] > 0.f) {
-              last_e = e;
-              a_last = before;
-            }
-            a += static_cast<double>(w[e]);
-            if (tok < 0 && w[e] > 0.f && tl < a) {
-              tok = e;
-              edge = before;
-            }
-          }
-          if (tok < 0) {
-            tok = last_e;
-            edge = a_last;
-          }
-#pragma unroll
-          for (int e = 0; e < kVec; ++e)
-            if (e == tok) wt = w[e];
-          tok = v * kVec + tok;
-        }
-        found = __shfl_sync(0xFFFFFFFFu, tok, L);
-        found_edge = __shfl_sync(0xFFFFFFFFu, edge, L);
-        found_w = __shfl_sync(0xFFFFFFFFu, wt, L);
-      }
-      carry += static_cast<double>(total);
-    }
-    if (found < 0 && last_vec >= 0 && lane == 0) {
-      float xt[kVec], xd[kVec], w[kVec];
-      load_vec(sl.st, last_vec, xt);
-      if (sl.gd) load_vec(sl.sd, last_vec, xd);
-      wfun(xt, xd, w);
-      int last_e = kVec - 1;
-#pragma unroll
-      for (int e = 0; e < kVec; ++e)
-        if (w[e] > 0.f) last_e = e;
-      found = last_vec * kVec + last_e;
-    }
+    const double base = *sh_base;
+    auto load = [&](int v, float(&xt)[kVec], float(&xd)[kVec]) {
+      load_vec(sl.st, v, xt);
+      if (sl.gd) load_vec(sl.sd, v, xd);
+    };
+    const ScanHit h = warp_scan<kVec>(v0, v1, tl - base, load, wfun);
     if (lane == 0) {
-      *result = found >= 0 ? lo + found : -1;
-      *edge_lo = found_edge;
-      *edge_w = found_w;
+      *result = h.elem >= 0 ? lo + h.elem : -1;
+      *edge_lo = base + h.edge;
+      *edge_w = h.w;
     }
   }
   __syncthreads();

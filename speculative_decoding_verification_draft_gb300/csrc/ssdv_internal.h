@@ -45,6 +45,7 @@ struct VerifyArgs {
   int32_t* n_accepted;         // [B]
   float4* part;                // workspace [B, gmax+1, nchunk, 2]: per-chunk row statistics
   double* csum;                // workspace [B, gmax+1, nchunk]: per-chunk residual weight sums
+  float* wsums;                // workspace [B, gmax+1, nchunk, 8]: their per-warp parts
   int32_t* ticket;             // workspace [B, gmax+1]: residual chunks arrived
   int32_t* status;             // workspace [1]: device error bits
   float* stats;                // [B, gmax+1, SSD_NSTAT_VERIFY] or null (debug)
@@ -66,7 +67,7 @@ struct SaguaroArgs {
 
 // Workspace layout (byte offsets), shared by the launchers and the API.
 struct WorkspaceLayout {
-  size_t status, ticket, part, csum, total;
+  size_t status, ticket, part, csum, wsums, total;
 };
 WorkspaceLayout workspace_layout(int B, int gmax);
 

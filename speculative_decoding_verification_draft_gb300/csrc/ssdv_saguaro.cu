@@ -28,11 +28,11 @@ struct PassAW {  // residual (scaled by Z_t) or target weights
                                              float (&w)[Elem<E>::kVec]) const {
 #pragma unroll
     for (int e = 0; e < Elem<E>::kVec; ++e) {
-      const float et = exp2f(fmaf(xt[e], c, -mct));
+      const float et = fast_exp2(fmaf(xt[e], c, -mct));
       if (target_only) {
         w[e] = et;
       } else {
-        const float ed = exp2f(fmaf(xd[e], c, -mcd));
+        const float ed = fast_exp2(fmaf(xd[e], c, -mcd));
         w[e] = fmaxf(fmaf(-kr, ed, et), 0.f);
       }
     }
@@ -51,9 +51,9 @@ struct MixW {
                                              float (&w)[Elem<E>::kVec]) const {
 #pragma unroll
     for (int e = 0; e < Elem<E>::kVec; ++e) {
-      const float et = exp2f(fmaf(xt[e], c, -mct));
+      const float et = fast_exp2(fmaf(xt[e], c, -mct));
       float ed = 0.f;
-      if (!pd_target) ed = exp2f(fmaf(xd[e], c, -mcd));
+      if (!pd_target) ed = fast_exp2(fmaf(xd[e], c, -mcd));
       const float wa = target_only ? et : fmaxf(fmaf(-kr, ed, et), 0.f);
       const float r = wa * inv_s;
       const float pd = (pd_target ? et : ed) * inv_zp;

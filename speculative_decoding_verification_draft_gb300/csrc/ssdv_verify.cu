@@ -12,7 +12,9 @@
 //  1. stream_kernel: one CTA per (request, position, vocabulary chunk) stages
 //     the target chunk (and the draft chunk of a sampled draft position) into
 //     shared memory with bulk async copies and reduces both in one pass to a
-//     32-byte record (max and sum of exponentials of each row, target argmax).
+//     32-byte record (max and sum of exponentials of each row, the target
+//     argmax of a greedy row, and the draft token's two logits when the token
+//     falls in the chunk).
 //     Every logit is read from HBM exactly once, by short-lived CTAs.
 //  2. sample_kernel (programmatic dependent launch): the CTAs of a request
 //     combine the records, take every accept decision and find the first
@@ -42,8 +44,8 @@ struct ResidualW {
                                              float (&w)[Elem<E>::kVec]) const {
 #pragma unroll
     for (int e = 0; e < Elem<E>::kVec; ++e) {
-      const float et = exp2f(fmaf(xt[e], c, -mct));
-      const float ed = exp2f(fmaf(xd[e], c, -mcd));
+      const float et = fast_exp2(fmaf(xt[e], c, -mct));
+      const float ed = fast_exp2(fmaf(xd[e], c, -mcd));
       w[e] = fmaxf(fmaf(-kr, ed, et), 0.f);
     }
   }
@@ -56,7 +58,7 @@ struct TargetW {
   __device__ __forceinline__ void operator()(const float (&xt)[Elem<E>::kVec], const float (&)[Elem<E>::kVec],
                                              float (&w)[Elem<E>::kVec]) const {
 #pragma unroll
-    for (int e = 0; e < Elem<E>::kVec; ++e) w[e] = exp2f(fmaf(xt[e], c, -mct));
+    for (int e = 0; e < Elem<E>::kVec; ++e) w[e] = fast_exp2(fmaf(xt[e], c, -mct));
   }
 };
 
@@ -137,29 +139,38 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const VerifyArgs a) {
   sl.gd = has_draft ? static_cast<const E*>(a.draft) + (static_cast<size_t>(b) * a.gmax + i) * V + lo : nullptr;
   sl.st = reinterpret_cast<E*>(dyn_smem);
   sl.sd = reinterpret_cast<E*>(dyn_smem + geo.row_smem);
+  // the draft token of this position: if it falls in this chunk, the record
+  // carries its two logits for the accept test
+  const int x = (has_draft && tid == 0) ? a.draft_tokens[static_cast<size_t>(b) * a.gmax + i] : -1;
   const bool ok = stage_chunk(sl, &bar);
 
   // pass 1: maxima (and the target argmax: each thread scans its vectors in
   // index order, so the first of equal values is kept)
   float mt = -INFINITY, md = -INFINITY;
   ArgMax am{-INFINITY, -1};
-  for (int v = tid; v < sl.nvec; v += kThreads) {
-    float xt[kVec];
-    load_vec(sl.st, v, xt);
+  if (greedy) {
+    for (int v = tid; v < sl.nvec; v += kThreads) {
+      float xt[kVec];
+      load_vec(sl.st, v, xt);
 #pragma unroll
-    for (int e = 0; e < kVec; ++e) {
-      mt = fmaxf(mt, xt[e]);
-      if (greedy && (am.i < 0 || xt[e] > am.v)) {
-        am.v = xt[e];
-        am.i = lo + v * kVec + e;
+      for (int e = 0; e < kVec; ++e) {
+        mt = fmaxf(mt, xt[e]);
+        if (am.i < 0 || xt[e] > am.v) {
+          am.v = xt[e];
+          am.i = lo + v * kVec + e;
+        }
       }
     }
-    if (has_draft) {
-      float xd[kVec];
-      load_vec(sl.sd, v, xd);
-#pragma unroll
-      for (int e = 0; e < kVec; ++e) md = fmaxf(md, xd[e]);
+  } else {
+    uint4 pt = Elem<E>::max_init(), pd = Elem<E>::max_init();
+    const uint4* vt = reinterpret_cast<const uint4*>(sl.st);
+    const uint4* vd = reinterpret_cast<const uint4*>(sl.sd);
+    for (int v = tid; v < sl.nvec; v += kThreads) {
+      pt = Elem<E>::max_acc(pt, vt[v]);
+      if (has_draft) pd = Elem<E>::max_acc(pd, vd[v]);
     }
+    mt = Elem<E>::max_final(pt);
+    md = Elem<E>::max_final(pd);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -202,13 +213,13 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const VerifyArgs a) {
     float xt[kVec], et[kVec];
     load_vec(sl.st, v, xt);
 #pragma unroll
-    for (int e = 0; e < kVec; ++e) et[e] = exp2f(fmaf(xt[e], cc, -mct));
+    for (int e = 0; e < kVec; ++e) et[e] = fast_exp2(fmaf(xt[e], cc, -mct));
     st += pair_sum(et);
     if (has_draft) {
       float xd[kVec], ed[kVec];
       load_vec(sl.sd, v, xd);
 #pragma unroll
-      for (int e = 0; e < kVec; ++e) ed[e] = exp2f(fmaf(xd[e], cc, -mcd));
+      for (int e = 0; e < kVec; ++e) ed[e] = fast_exp2(fmaf(xd[e], cc, -mcd));
       sd += pair_sum(ed);
     }
   }
@@ -227,7 +238,12 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const VerifyArgs a) {
     }
     float4* rec = a.part + (static_cast<size_t>(unit) * NC + c) * 2;
     rec[0] = make_float4(sh_mt, s0, has_draft ? sh_md : -INFINITY, s1);
-    rec[1] = make_float4(-INFINITY, __int_as_float(-1), __int_as_float(ok ? 0 : 1), 0.f);
+    float xt_tok = 0.f, xd_tok = 0.f;
+    if (x >= lo && x < lo + sl.n) {
+      xt_tok = Elem<E>::to_float(sl.st[x - lo]);
+      xd_tok = Elem<E>::to_float(sl.sd[x - lo]);
+    }
+    rec[1] = make_float4(xd_tok, 0.f, __int_as_float(ok ? 0 : 1), xt_tok);
   }
 }
 
@@ -320,18 +336,13 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const VerifyArgs a) {
   const E* tb = static_cast<const E*>(a.target);
   const E* db = static_cast<const E*>(a.draft);
 
-  // Inputs only (overlaps the streaming kernel's tail): draft tokens and the
-  // two logits of each accept test.
+  // Inputs only (overlaps the streaming kernel's tail): the draft tokens.
   if (warp == 0) {
     bool bad = false;
     if (lane < g) {
       const int x = a.draft_tokens[static_cast<size_t>(b) * a.gmax + lane];
       bad = x < 0 || x >= V;
       tok_x[lane] = x;
-      if (!bad && !greedy) {
-        tok_t[lane] = Elem<E>::to_float(tb[(static_cast<size_t>(b) * W + lane) * V + x]);
-        tok_d[lane] = Elem<E>::to_float(db[(static_cast<size_t>(b) * a.gmax + lane) * V + x]);
-      }
     }
     const unsigned anybad = __ballot_sync(0xFFFFFFFFu, bad);
     if (lane == 0) sh_bad = anybad != 0;
@@ -364,6 +375,13 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const VerifyArgs a) {
     butterfly_stats(t, d, am, err, cc);
     if (lane == 0) ust[u] = UnitStat{t.m, t.s, d.m, d.s, am.v, am.i, err};
   }
+  // the two logits of each accept test, from the record of the token's chunk
+  if (!greedy && warp == 0 && lane < g) {
+    const int cx = tok_x[lane] / geo.chunk;
+    const float4 r1 = a.part[((static_cast<size_t>(b) * W + lane) * NC + cx) * 2 + 1];
+    tok_d[lane] = r1.x;
+    tok_t[lane] = r1.w;
+  }
   __syncthreads();
 
   // Decisions: accept tests of positions 0..g-1 and the first rejection.
@@ -380,7 +398,7 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const VerifyArgs a) {
         if (tok_d[lane] != -INFINITY) {
           const float lt = fmaf(tok_t[lane], cc, -scaled_max(s.tm, cc));
           const float ld = fmaf(tok_d[lane], cc, -scaled_max(s.dm, cc));
-          ratio_acc = fminf(1.f, exp2f(lt - ld) * (s.ds / s.ts));
+          ratio_acc = fminf(1.f, fast_exp2(lt - ld) * (s.ds / s.ts));
         }
         acc = dr.accept < ratio_acc;
       }
@@ -403,8 +421,8 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const VerifyArgs a) {
           const float mct = scaled_max(s.tm, cc), mcd = scaled_max(s.dm, cc);
           st[2] = s.dm;
           st[3] = logf(s.ds) - fmaf(s.dm, cc, -mcd) * 0.6931471805599453f;
-          st[4] = exp2f(fmaf(tok_t[pi], cc, -mct)) / s.ts;
-          st[5] = exp2f(fmaf(tok_d[pi], cc, -mcd)) / s.ds;
+          st[4] = fast_exp2(fmaf(tok_t[pi], cc, -mct)) / s.ts;
+          st[5] = fast_exp2(fmaf(tok_d[pi], cc, -mcd)) / s.ds;
           st[7] = ratio_acc;
         }
       }
@@ -468,8 +486,10 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const VerifyArgs a) {
     const ResidualW<E> wf{cc, mct, scaled_max(s.dm, cc), s.ts / s.ds};
     TopK<0> none;
     const double cta = weighted_pass<E, 0>(sl, lo, wf, wsum, none);
+    const size_t ci = (static_cast<size_t>(b) * W + pi) * NC + c;
     if (tid == 0) {
-      a.csum[(static_cast<size_t>(b) * W + pi) * NC + c] = ok ? cta : NAN;
+      for (int w = 0; w < kWarps; ++w) a.wsums[ci * kWarps + w] = wsum[w];
+      a.csum[ci] = ok ? cta : NAN;
       __threadfence();
       sh_last = atomicAdd(a.ticket + b * W + pi, 1) == NC - 1;
     }
@@ -524,7 +544,51 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const VerifyArgs a) {
     }
   }
 
-  // Draw: (re)stage the owning chunk and search it.
+  // Draw from the owning chunk.  A residual draw on 16-byte aligned rows scans
+  // only the warp run that holds the target, straight from global memory
+  // (the chunk's per-warp sums were published by the CTA that summed it).
+  if (!target_w && geo.bulk) {
+    if (warp == 0) {
+      const size_t ci = (static_cast<size_t>(b) * W + pi) * NC + owner;
+      float ws8[kWarps];
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) ws8[w] = *reinterpret_cast<volatile float*>(a.wsums + ci * kWarps + w);
+      double wbase = 0.0;
+      const int wpick = pick_warp(ws8, kWarps, sh_local, &wbase);
+      const int lo = owner * geo.chunk;
+      const int nvec = (min(geo.chunk, V - lo) + kVec - 1) / kVec;
+      const uint4* gt = reinterpret_cast<const uint4*>(tb + trow + lo);
+      const uint4* gd = reinterpret_cast<const uint4*>(db + drow + lo);
+      auto load = [&](int v, float(&xt)[kVec], float(&xd)[kVec]) {
+        Elem<E>::unpack(gt[v], xt);
+        Elem<E>::unpack(gd[v], xd);
+      };
+      const ResidualW<E> wf{cc, mct, scaled_max(s.dm, cc), s.ts / s.ds};
+      ScanHit h{-1, NAN, 0.f};
+      if (wpick >= 0) {
+        int v0, v1;
+        warp_range(nvec, wpick, v0, v1);
+        h = warp_scan<kVec>(v0, v1, sh_local - wbase, load, wf);
+      }
+      if (lane == 0) {
+        if (h.elem < 0) {
+          write_error(a, b);
+          atomicOr(a.status, 1 << SSD_ERR_TIMEOUT);
+        } else {
+          if (a.stats) {
+            float* st = a.stats + (static_cast<size_t>(b) * W + pos) * SSD_NSTAT_VERIFY;
+            const double e0 = sh_prefix + wbase + h.edge;
+            st[8] = static_cast<float>(ures - e0 / sh_total);
+            st[9] = static_cast<float>((e0 + static_cast<double>(h.w)) / sh_total - ures);
+          }
+          write_outputs(a, b, n, lo + h.elem, tok_x);
+        }
+      }
+    }
+    return;
+  }
+
+  // Otherwise (re)stage the owning chunk and search it.
   const int lo = owner * geo.chunk;
   sl.n = min(geo.chunk, V - lo);
   sl.nvec = (sl.n + kVec - 1) / kVec;
