@@ -119,6 +119,8 @@ ssd_status choose_chunks(int V, int esize, bool aligned, ChunkGeometry* geo, int
   geo->nchunk = (V + chunk - 1) / chunk;
   geo->row_smem = row_smem;
   geo->bulk = aligned ? 1 : 0;
+  geo->span = env_int("SSDV_SPAN", 4);
+  if (geo->span < 1) geo->span = 1;
   *smem_bytes = 2 * row_smem;
   return SSD_OK;
 }

@@ -29,6 +29,7 @@ struct ChunkGeometry {
   int nchunk;    // chunks per row, 1..kMaxChunks
   int row_smem;  // shared-memory bytes per staged row chunk (a multiple of 128)
   int bulk;      // 1: rows 16-byte aligned, staged with bulk async copies
+  int span;      // streaming chunks per range of the sampling kernel
 };
 constexpr int kMaxChunks = 32;
 

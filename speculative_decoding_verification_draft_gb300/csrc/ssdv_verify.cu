@@ -19,9 +19,10 @@
 //  2. sample_kernel (programmatic dependent launch): the CTAs of a request
 //     combine the records, take every accept decision and find the first
 //     rejection n.  Only position n needs a draw: the bonus draw locates its
-//     chunk from the records and rescans one chunk; a residual draw runs one
-//     chunk-parallel pass over rows n (mostly L2-resident), the last CTA to
-//     arrive locates the chunk holding the target and rescans it.
+//     chunk from the records and scans that chunk; a residual draw runs one
+//     range-parallel pass over rows n (mostly L2-resident, read straight from
+//     global memory), and the last range to arrive scans the one warp run
+//     that holds the target.
 #include "ssdv_device.cuh"
 
 namespace ssdv {
@@ -66,8 +67,11 @@ struct TargetW {
 // copies completing on `bar` (fresh phase 0), or plain loads padded with -inf
 // to a whole vector when the rows are not 16-byte aligned.  Returns false when
 // the bounded wait ran out.
+// One thread issues the copies and waits on the barrier while the others
+// park at __syncthreads (which costs no issue slots); the copies' data is
+// visible to every thread after the barrier.
 template <typename E>
-__device__ __forceinline__ bool stage_chunk(const Slice<E>& sl, uint64_t* bar) {
+__device__ __forceinline__ bool stage_chunk(const Slice<E>& sl, uint64_t* bar, int* sh_ok) {
   if (sl.bulk) {
     if (threadIdx.x == 0) {
       mbar_init(bar, 1);
@@ -78,9 +82,10 @@ __device__ __forceinline__ bool stage_chunk(const Slice<E>& sl, uint64_t* bar) {
       const uint64_t pol = l2_policy_evict_normal();
       bulk_copy_g2s(sl.st, sl.gt, bytes, bar, pol);
       if (sl.gd) bulk_copy_g2s(sl.sd, sl.gd, bytes, bar, pol);
+      *sh_ok = mbar_wait_bounded(bar, 0) ? 1 : 0;
     }
     __syncthreads();
-    return mbar_wait_bounded(bar, 0);
+    return *sh_ok != 0;
   }
   constexpr int kVec = Elem<E>::kVec;
   const int padded = sl.nvec * kVec;
@@ -111,6 +116,7 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const VerifyArgs a) {
   __shared__ float red[4][kWarps];
   __shared__ int red_i[kWarps];
   __shared__ float sh_mt, sh_md;
+  __shared__ int sh_ok;
   griddep_launch_dependents();
 
   const ChunkGeometry& geo = a.geo;
@@ -142,7 +148,7 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const VerifyArgs a) {
   // the draft token of this position: if it falls in this chunk, the record
   // carries its two logits for the accept test
   const int x = (has_draft && tid == 0) ? a.draft_tokens[static_cast<size_t>(b) * a.gmax + i] : -1;
-  const bool ok = stage_chunk(sl, &bar);
+  const bool ok = stage_chunk(sl, &bar, &sh_ok);
 
   // pass 1: maxima (and the target argmax: each thread scans its vectors in
   // index order, so the first of equal values is kept)
@@ -298,24 +304,92 @@ __device__ __forceinline__ void locate_target_chunk(const VerifyArgs& a, int uni
 
 }  // namespace
 
+// Vector v of a row range straight from global memory (L2-resident rows in
+// practice): 16-byte loads when the rows are aligned, else element loads with
+// -inf beyond the range.  gd may be null (target weights).
+template <typename E>
+struct GlobalRange {
+  const E* gt;
+  const E* gd;
+  int n;
+  bool aligned;
+  __device__ __forceinline__ void operator()(int v, float (&xt)[Elem<E>::kVec], float (&xd)[Elem<E>::kVec]) const {
+    constexpr int kVec = Elem<E>::kVec;
+    if (aligned) {
+      Elem<E>::unpack(__ldg(reinterpret_cast<const uint4*>(gt) + v), xt);
+      if (gd) Elem<E>::unpack(__ldg(reinterpret_cast<const uint4*>(gd) + v), xd);
+    } else {
+#pragma unroll
+      for (int e = 0; e < kVec; ++e) {
+        const int k = v * kVec + e;
+        xt[e] = k < n ? Elem<E>::to_float(gt[k]) : -INFINITY;
+        if (gd) xd[e] = k < n ? Elem<E>::to_float(gd[k]) : -INFINITY;
+      }
+    }
+  }
+};
+
+// Weighted pass over a global row range: each warp owns a contiguous run of
+// vectors (lanes interleaved: coalesced).  Per-warp sums to wsum[] (shared),
+// returns the CTA sum (fp64 over warps) in thread 0.
+template <typename E, typename WFun>
+__device__ __forceinline__ double global_weighted_pass(const GlobalRange<E>& rg, const WFun& wfun, float* wsum) {
+  constexpr int kVec = Elem<E>::kVec;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nvec = (rg.n + kVec - 1) / kVec;
+  int v0, v1;
+  warp_range(nvec, warp, v0, v1);
+  float acc = 0.f;
+  for (int v = v0 + lane; v < v1; v += 32) {
+    float xt[kVec], xd[kVec], w[kVec];
+    rg(v, xt, xd);
+    wfun(xt, xd, w);
+    acc += pair_sum(w);
+  }
+  acc = warp_sum(acc);
+  if (lane == 0) wsum[warp] = acc;
+  __syncthreads();
+  double cta = 0.0;
+  if (threadIdx.x == 0)
+    for (int w = 0; w < kWarps; ++w) cta += static_cast<double>(wsum[w]);
+  return cta;
+}
+
+// The draw inside one global row range whose per-warp sums are ws8[]: warp 0
+// picks the warp run holding tl (relative to the range start) and scans it.
+template <typename E, typename WFun>
+__device__ __forceinline__ ScanHit draw_in_range(const GlobalRange<E>& rg, const WFun& wfun, const float* ws8,
+                                                 double tl, double* run_base) {
+  constexpr int kVec = Elem<E>::kVec;
+  double wbase = 0.0;
+  const int wpick = pick_warp(ws8, kWarps, tl, &wbase);
+  ScanHit h{-1, NAN, 0.f};
+  if (wpick >= 0) {
+    int v0, v1;
+    warp_range((rg.n + kVec - 1) / kVec, wpick, v0, v1);
+    h = warp_scan<kVec>(v0, v1, tl - wbase, rg, wfun);
+  }
+  *run_base = wbase;
+  return h;
+}
+
 template <typename E>
 __global__ void __launch_bounds__(kThreads) sample_kernel(const VerifyArgs a) {
-  extern __shared__ __align__(128) uint8_t dyn_smem[];
-  __shared__ __align__(8) uint64_t bar[2];
   __shared__ UnitStat ust[SSD_MAX_GAMMA + 1];
   __shared__ int tok_x[SSD_MAX_GAMMA];
   __shared__ float tok_t[SSD_MAX_GAMMA], tok_d[SSD_MAX_GAMMA];
   __shared__ float wsum[kWarps];
-  __shared__ int sh_n, sh_bad, sh_last, sh_owner, sh_warp, sh_result, sh_target_w;
-  __shared__ float sh_edge_w, sh_ures;
-  __shared__ double sh_base, sh_local, sh_prefix, sh_total, sh_edge;
-  constexpr int kVec = Elem<E>::kVec;
+  __shared__ int sh_n, sh_bad, sh_last, sh_owner, sh_target_w;
+  __shared__ float sh_ures;
+  __shared__ double sh_local, sh_prefix, sh_total;
 
   const ChunkGeometry& geo = a.geo;
   const int V = geo.V, NC = geo.nchunk, W = a.gmax + 1;
+  const int span = geo.span * geo.chunk;  // elements per sampling range
+  const int NR = (V + span - 1) / span;   // sampling ranges per row
   const int P = a.debug ? W : 1;
-  const int c = blockIdx.x % NC;
-  const int rest = blockIdx.x / NC;
+  const int c = blockIdx.x % NR;
+  const int rest = blockIdx.x / NR;
   const int pi = rest % P;
   const int b = rest / P;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -358,8 +432,15 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const VerifyArgs a) {
   griddep_wait();  // the streaming kernel's records are complete and visible
 
   // Row statistics of every position of the request, combined from the chunk
-  // records (the same butterfly in every CTA: identical results).
+  // records (the same butterfly in every CTA: identical results), and the two
+  // logits of each accept test from the record of the token's chunk.
   const float cc = greedy ? 1.f : kLog2e / T;
+  if (!greedy && warp == 0 && lane < g) {
+    const int cx = tok_x[lane] / geo.chunk;
+    const float4 r1 = a.part[((static_cast<size_t>(b) * W + lane) * NC + cx) * 2 + 1];
+    tok_d[lane] = r1.x;
+    tok_t[lane] = r1.w;
+  }
   for (int u = warp; u <= g; u += kWarps) {
     MaxSum t{-INFINITY, 0.f}, d{-INFINITY, 0.f};
     ArgMax am{-INFINITY, -1};
@@ -369,18 +450,11 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const VerifyArgs a) {
       const float4 r0 = rec[0], r1 = rec[1];
       t = MaxSum{r0.x, r0.y};
       d = MaxSum{r0.z, r0.w};
-      am = ArgMax{r1.x, __float_as_int(r1.y)};
+      if (greedy) am = ArgMax{r1.x, __float_as_int(r1.y)};
       err = __float_as_int(r1.z);
     }
     butterfly_stats(t, d, am, err, cc);
     if (lane == 0) ust[u] = UnitStat{t.m, t.s, d.m, d.s, am.v, am.i, err};
-  }
-  // the two logits of each accept test, from the record of the token's chunk
-  if (!greedy && warp == 0 && lane < g) {
-    const int cx = tok_x[lane] / geo.chunk;
-    const float4 r1 = a.part[((static_cast<size_t>(b) * W + lane) * NC + cx) * 2 + 1];
-    tok_d[lane] = r1.x;
-    tok_t[lane] = r1.w;
   }
   __syncthreads();
 
@@ -432,7 +506,6 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const VerifyArgs a) {
   const int n = sh_n;
   int err_any = 0;
   for (int u = 0; u <= g; ++u) err_any |= ust[u].err;
-
   if (greedy || err_any) {
     if (pi == 0 && c == 0 && tid == 0) {
       if (err_any) {
@@ -444,25 +517,117 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const VerifyArgs a) {
     }
     return;
   }
+
   const int pos = a.debug ? pi : n;
   const UnitStat s = ust[pos];
   const float mct = scaled_max(s.tm, cc);
   const double ures = static_cast<double>(sh_ures);
-  const size_t trow = (static_cast<size_t>(b) * W + pos) * V;
-  const size_t drow = (static_cast<size_t>(b) * a.gmax + pos) * V;
+  const E* trow = tb + (static_cast<size_t>(b) * W + pos) * V;
+  const E* drow = db + (static_cast<size_t>(b) * a.gmax + pos) * V;
+  const bool aligned = geo.bulk != 0;
+  const ResidualW<E> rw{cc, mct, pos < g ? scaled_max(s.dm, cc) : 0.f, pos < g ? s.ts / s.ds : 0.f};
+  const TargetW<E> tw{cc, mct};
 
-  Slice<E> sl;
-  sl.nstage = 1;
-  sl.bulk = geo.bulk != 0;
-  sl.st = reinterpret_cast<E*>(dyn_smem);
-  sl.sd = reinterpret_cast<E*>(dyn_smem + geo.row_smem);
-
-  int owner = -1;
-  bool target_w = (pos == g);
-  if (pos == g) {
-    // Bonus draw from q_gamma: its chunk weights are the records' sums.
+  int draw_lo = 0, draw_n = 0;  // the range searched for the draw
+  bool target_w = false;
+  if (pos < g) {
+    // Residual pass over this CTA's range of rows pos; the last range to
+    // arrive draws.
+    const int lo = c * span;
+    const GlobalRange<E> rg{trow + lo, drow + lo, min(span, V - lo), aligned};
+    const double cta = global_weighted_pass(rg, rw, wsum);
+    const size_t ci = (static_cast<size_t>(b) * W + pi) * NR + c;
+    if (tid == 0) {
+      for (int w = 0; w < kWarps; ++w) a.wsums[ci * kWarps + w] = wsum[w];
+      a.csum[ci] = cta;
+      __threadfence();
+      sh_last = atomicAdd(a.ticket + b * W + pi, 1) == NR - 1;
+    }
+    __syncthreads();
+    if (!sh_last) return;
+    __threadfence();
+    if (warp == 0) {
+      double w = 0.0;
+      if (lane < NR) w = *reinterpret_cast<volatile double*>(a.csum + (static_cast<size_t>(b) * W + pi) * NR + lane);
+      double incl = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const double t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const double tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+      int owner = -1, tgt = 0;
+      double local = 0.0, prefix = 0.0, total = tot;
+      if (tot > 0.0) {
+        const double target = ures * tot;
+        const unsigned hit = __ballot_sync(0xFFFFFFFFu, lane < NR && w > 0.0 && target < incl);
+        const unsigned posm = __ballot_sync(0xFFFFFFFFu, lane < NR && w > 0.0);
+        owner = hit ? __ffs(hit) - 1 : 31 - __clz(posm);
+        prefix = __shfl_sync(0xFFFFFFFFu, incl - w, owner);
+        local = target - prefix;
+      } else {
+        // No residual mass: draw from q_pos instead, located by chunk record.
+        locate_target_chunk(a, b * W + pos, s.tm, cc, ures, &owner, &local, &prefix, &total);
+        tgt = 1;
+      }
+      if (lane == 0) {
+        if (a.stats)
+          a.stats[(static_cast<size_t>(b) * W + pi) * SSD_NSTAT_VERIFY + 6] = static_cast<float>(tot / s.ts);
+        a.ticket[b * W + pi] = 0;
+        sh_owner = owner;
+        sh_local = local;
+        sh_prefix = prefix;
+        sh_total = total;
+        sh_target_w = tgt;
+      }
+    }
+    __syncthreads();
+    if (pos != n) return;
+    if (sh_owner < 0 || !(sh_total > 0.0)) {
+      if (tid == 0) {
+        write_error(a, b);
+        atomicOr(a.status, 1 << SSD_ERR_TIMEOUT);
+      }
+      return;
+    }
+    target_w = sh_target_w != 0;
+    if (!target_w) {
+      // The owning range's per-warp sums were published by the CTA that
+      // summed it: scan only the warp run holding the target.
+      if (warp == 0) {
+        const int owner = sh_owner;
+        const size_t oi = (static_cast<size_t>(b) * W + pi) * NR + owner;
+        float ws8[kWarps];
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) ws8[w] = *reinterpret_cast<volatile float*>(a.wsums + oi * kWarps + w);
+        const int lo = owner * span;
+        const GlobalRange<E> rg{trow + lo, drow + lo, min(span, V - lo), aligned};
+        double run_base;
+        const ScanHit h = draw_in_range(rg, rw, ws8, sh_local, &run_base);
+        if (lane == 0) {
+          if (h.elem < 0) {
+            write_error(a, b);
+            atomicOr(a.status, 1 << SSD_ERR_TIMEOUT);
+          } else {
+            if (a.stats) {
+              float* st = a.stats + (static_cast<size_t>(b) * W + pos) * SSD_NSTAT_VERIFY;
+              const double e0 = sh_prefix + run_base + h.edge;
+              st[8] = static_cast<float>(ures - e0 / sh_total);
+              st[9] = static_cast<float>((e0 + static_cast<double>(h.w)) / sh_total - ures);
+            }
+            write_outputs(a, b, n, lo + h.elem, tok_x);
+          }
+        }
+      }
+      return;
+    }
+    draw_lo = sh_owner * geo.chunk;  // q fallback: the owner is a streaming chunk
+  } else {
+    // Bonus draw from q_gamma: the streaming chunk holding the target comes
+    // from the records; the CTA whose range covers it draws.
     if (pos != n) return;
     if (warp == 0) {
+      int owner;
       double local, prefix, total;
       locate_target_chunk(a, b * W + pos, s.tm, cc, ures, &owner, &local, &prefix, &total);
       if (lane == 0) {
@@ -473,151 +638,33 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const VerifyArgs a) {
       }
     }
     __syncthreads();
-    owner = sh_owner;
-    if (owner != c) return;
-  } else {
-    // Residual pass over chunk c of rows pos; the last chunk to arrive draws.
-    const int lo = c * geo.chunk;
-    sl.n = min(geo.chunk, V - lo);
-    sl.nvec = (sl.n + kVec - 1) / kVec;
-    sl.gt = tb + trow + lo;
-    sl.gd = db + drow + lo;
-    const bool ok = stage_chunk(sl, &bar[0]);
-    const ResidualW<E> wf{cc, mct, scaled_max(s.dm, cc), s.ts / s.ds};
-    TopK<0> none;
-    const double cta = weighted_pass<E, 0>(sl, lo, wf, wsum, none);
-    const size_t ci = (static_cast<size_t>(b) * W + pi) * NC + c;
-    if (tid == 0) {
-      for (int w = 0; w < kWarps; ++w) a.wsums[ci * kWarps + w] = wsum[w];
-      a.csum[ci] = ok ? cta : NAN;
-      __threadfence();
-      sh_last = atomicAdd(a.ticket + b * W + pi, 1) == NC - 1;
-    }
-    __syncthreads();
-    if (!sh_last) return;
-    __threadfence();
-    if (warp == 0) {
-      double w = 0.0;
-      if (lane < NC) w = *reinterpret_cast<volatile double*>(a.csum + (static_cast<size_t>(b) * W + pi) * NC + lane);
-      double incl = w;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const double t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += t;
-      }
-      const double tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
-      double local = 0.0, prefix = 0.0, total = tot;
-      int tw = 0;
-      if (tot > 0.0) {
-        const double target = ures * tot;
-        const unsigned hit = __ballot_sync(0xFFFFFFFFu, lane < NC && w > 0.0 && target < incl);
-        const unsigned posm = __ballot_sync(0xFFFFFFFFu, lane < NC && w > 0.0);
-        owner = hit ? __ffs(hit) - 1 : 31 - __clz(posm);
-        prefix = __shfl_sync(0xFFFFFFFFu, incl - w, owner);
-        local = target - prefix;
-      } else {
-        // No residual mass (or an invalid sum): draw from q_pos instead.
-        locate_target_chunk(a, b * W + pos, s.tm, cc, ures, &owner, &local, &prefix, &total);
-        tw = 1;
-      }
-      if (lane == 0) {
-        if (a.stats)
-          a.stats[(static_cast<size_t>(b) * W + pi) * SSD_NSTAT_VERIFY + 6] = static_cast<float>(tot / s.ts);
-        a.ticket[b * W + pi] = 0;
-        sh_owner = owner;
-        sh_local = local;
-        sh_prefix = prefix;
-        sh_total = total;
-        sh_target_w = tw;
-      }
-    }
-    __syncthreads();
-    if (pos != n) return;
-    owner = sh_owner;
-    target_w = sh_target_w != 0;
-    if (owner < 0 || !(sh_total > 0.0)) {
-      if (tid == 0) {
+    if (sh_owner < 0 || (sh_owner * geo.chunk) / span != c) return;
+    target_w = true;
+    draw_lo = sh_owner * geo.chunk;
+  }
+
+  // Target-weight draw inside one streaming chunk: a whole-CTA pass for the
+  // per-warp sums, then warp 0 scans the run holding the target.
+  draw_n = min(geo.chunk, V - draw_lo);
+  const GlobalRange<E> rg{trow + draw_lo, nullptr, draw_n, aligned};
+  global_weighted_pass(rg, tw, wsum);
+  if (warp == 0) {
+    double run_base;
+    const ScanHit h = draw_in_range(rg, tw, wsum, sh_local, &run_base);
+    if (lane == 0) {
+      if (h.elem < 0) {
         write_error(a, b);
         atomicOr(a.status, 1 << SSD_ERR_TIMEOUT);
-      }
-      return;
-    }
-  }
-
-  // Draw from the owning chunk.  A residual draw on 16-byte aligned rows scans
-  // only the warp run that holds the target, straight from global memory
-  // (the chunk's per-warp sums were published by the CTA that summed it).
-  if (!target_w && geo.bulk) {
-    if (warp == 0) {
-      const size_t ci = (static_cast<size_t>(b) * W + pi) * NC + owner;
-      float ws8[kWarps];
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) ws8[w] = *reinterpret_cast<volatile float*>(a.wsums + ci * kWarps + w);
-      double wbase = 0.0;
-      const int wpick = pick_warp(ws8, kWarps, sh_local, &wbase);
-      const int lo = owner * geo.chunk;
-      const int nvec = (min(geo.chunk, V - lo) + kVec - 1) / kVec;
-      const uint4* gt = reinterpret_cast<const uint4*>(tb + trow + lo);
-      const uint4* gd = reinterpret_cast<const uint4*>(db + drow + lo);
-      auto load = [&](int v, float(&xt)[kVec], float(&xd)[kVec]) {
-        Elem<E>::unpack(gt[v], xt);
-        Elem<E>::unpack(gd[v], xd);
-      };
-      const ResidualW<E> wf{cc, mct, scaled_max(s.dm, cc), s.ts / s.ds};
-      ScanHit h{-1, NAN, 0.f};
-      if (wpick >= 0) {
-        int v0, v1;
-        warp_range(nvec, wpick, v0, v1);
-        h = warp_scan<kVec>(v0, v1, sh_local - wbase, load, wf);
-      }
-      if (lane == 0) {
-        if (h.elem < 0) {
-          write_error(a, b);
-          atomicOr(a.status, 1 << SSD_ERR_TIMEOUT);
-        } else {
-          if (a.stats) {
-            float* st = a.stats + (static_cast<size_t>(b) * W + pos) * SSD_NSTAT_VERIFY;
-            const double e0 = sh_prefix + wbase + h.edge;
-            st[8] = static_cast<float>(ures - e0 / sh_total);
-            st[9] = static_cast<float>((e0 + static_cast<double>(h.w)) / sh_total - ures);
-          }
-          write_outputs(a, b, n, lo + h.elem, tok_x);
+      } else {
+        if (a.stats) {
+          float* st = a.stats + (static_cast<size_t>(b) * W + pos) * SSD_NSTAT_VERIFY;
+          const double e0 = sh_prefix + run_base + h.edge;
+          st[8] = static_cast<float>(ures - e0 / sh_total);
+          st[9] = static_cast<float>((e0 + static_cast<double>(h.w)) / sh_total - ures);
         }
+        write_outputs(a, b, n, draw_lo + h.elem, tok_x);
       }
     }
-    return;
-  }
-
-  // Otherwise (re)stage the owning chunk and search it.
-  const int lo = owner * geo.chunk;
-  sl.n = min(geo.chunk, V - lo);
-  sl.nvec = (sl.n + kVec - 1) / kVec;
-  sl.gt = tb + trow + lo;
-  sl.gd = target_w ? nullptr : db + drow + lo;
-  __syncthreads();  // every read of the previous chunk is done before it is overwritten
-  const bool ok = stage_chunk(sl, &bar[1]);
-  TopK<0> none;
-  if (target_w) {
-    const TargetW<E> wf{cc, mct};
-    weighted_pass<E, 0>(sl, lo, wf, wsum, none);
-    cdf_search(sl, lo, wf, wsum, sh_local, &sh_warp, &sh_base, &sh_result, &sh_edge, &sh_edge_w);
-  } else {
-    const ResidualW<E> wf{cc, mct, scaled_max(s.dm, cc), s.ts / s.ds};
-    weighted_pass<E, 0>(sl, lo, wf, wsum, none);
-    cdf_search(sl, lo, wf, wsum, sh_local, &sh_warp, &sh_base, &sh_result, &sh_edge, &sh_edge_w);
-  }
-  if (tid == 0) {
-    if (!ok || sh_result < 0) {
-      write_error(a, b);
-      atomicOr(a.status, 1 << SSD_ERR_TIMEOUT);
-      return;
-    }
-    if (a.stats) {  // distances of u to the drawn token's CDF edges (debug statistics)
-      float* st = a.stats + (static_cast<size_t>(b) * W + pos) * SSD_NSTAT_VERIFY;
-      st[8] = static_cast<float>(ures - (sh_prefix + sh_edge) / sh_total);
-      st[9] = static_cast<float>((sh_prefix + sh_edge + static_cast<double>(sh_edge_w)) / sh_total - ures);
-    }
-    write_outputs(a, b, n, sh_result, tok_x);
   }
 }
 
@@ -656,27 +703,28 @@ cudaError_t ensure_smem(const void* fn, int smem_bytes, int* cached) {
 
 template <typename E>
 cudaError_t launch_verify_t(const VerifyArgs& a, int smem_bytes, cudaStream_t stream) {
-  static thread_local int dev_cached = -1, smem1 = -1, smem2 = -1;
+  static thread_local int dev_cached = -1, smem1 = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev != dev_cached) {
-    smem1 = smem2 = -1;
+    smem1 = -1;
     dev_cached = dev;
   }
   e = ensure_smem(reinterpret_cast<const void*>(&stream_kernel<E>), smem_bytes, &smem1);
   if (e != cudaSuccess) return e;
-  e = ensure_smem(reinterpret_cast<const void*>(&sample_kernel<E>), smem_bytes, &smem2);
-  if (e != cudaSuccess) return e;
+
   const long long units = static_cast<long long>(a.B) * (a.gmax + 1);
   stream_kernel<E><<<static_cast<unsigned>(units * a.geo.nchunk), kThreads, smem_bytes, stream>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int P = a.debug ? a.gmax + 1 : 1;
+  const int span = a.geo.span * a.geo.chunk;
+  const int nr = (a.geo.V + span - 1) / span;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(static_cast<long long>(a.B) * P * a.geo.nchunk), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(static_cast<long long>(a.B) * P * nr), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
+  cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
