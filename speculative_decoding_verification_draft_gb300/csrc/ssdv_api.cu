@@ -119,8 +119,13 @@ ssd_status choose_chunks(int V, int esize, bool aligned, ChunkGeometry* geo, int
   geo->nchunk = (V + chunk - 1) / chunk;
   geo->row_smem = row_smem;
   geo->bulk = aligned ? 1 : 0;
-  geo->span = env_int("SSDV_SPAN", 4);
-  if (geo->span < 1) geo->span = 1;
+  // the sampling kernel's ranges: at most 64 KB of a row (so a warp's run of a
+  // range fits its staging buffer), SSDV_SPAN chunks when set
+  int span = (64 * 1024) / (chunk * esize);
+  span = env_int("SSDV_SPAN", span);
+  if (span < 1) span = 1;
+  while (span > 1 && static_cast<long long>(span) * chunk * esize > 64 * 1024) --span;
+  geo->span = span;
   *smem_bytes = 2 * row_smem;
   return SSD_OK;
 }
@@ -137,7 +142,7 @@ ssd_status verify_common(const void* target, const void* draft, ssd_dtype dtype,
   if (!draft && !all_greedy && gmax > 0)
     return fail(SSD_ERR_NULL, "draft_logits is NULL but some request samples");
   if (gmax > 0 && !draft_tokens) return fail(SSD_ERR_NULL, "draft_tokens is NULL");
-  if (B < 1 || gmax < 0 || gmax > SSD_MAX_GAMMA || V < 1 || V > SSD_MAX_V)
+  if (B < 1 || B > 65535 || gmax < 0 || gmax > SSD_MAX_GAMMA || V < 1 || V > SSD_MAX_V)
     return fail(SSD_ERR_SHAPE, "bad shape B=%d gamma=%d V=%d", B, gmax, V);
   if (!aligned_to(target, es) || (draft && !aligned_to(draft, es)) || !aligned_to(out_tokens, 4) ||
       !aligned_to(n_accepted, 4) || (draft_tokens && !aligned_to(draft_tokens, 4)) || !aligned_to(workspace, 16) ||

@@ -28,6 +28,42 @@ constexpr uint32_t kWaitLimit = 1u << 24;  // bounded polls of an mbarrier
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------------------
+// 2^x as one ex2.approx.ftz.f32 instruction (relative error about 2 ulp;
+// results below 2^-126 flush to zero, which no sum here can notice).  Every
+// weight and every partial sum of a row uses this same function.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ---------------------------------------------------------------------------
+// Packed pairs of fp32 (one FMA / ADD instruction for two lanes of data).
+// ---------------------------------------------------------------------------
+struct F2 {
+  unsigned long long v;
+};
+__device__ __forceinline__ F2 f2_make(float lo, float hi) {
+  F2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r.v) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_split(F2 a, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a.v));
+}
+__device__ __forceinline__ F2 f2_fma(F2 a, F2 b, F2 c) {
+  F2 r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r.v) : "l"(a.v), "l"(b.v), "l"(c.v));
+  return r;
+}
+__device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
+  F2 r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+  return r;
+}
+
+// ---------------------------------------------------------------------------
 // Element types: bf16 is handled as its raw 16-bit pattern.
 // ---------------------------------------------------------------------------
 template <typename E>
@@ -35,6 +71,8 @@ struct Elem;
 template <>
 struct Elem<uint16_t> {
   static constexpr int kVec = 8;  // elements per 16-byte vector
+  // exp2(x * c - mc) summed over a raw vector, as a packed pair of partial sums
+  static __device__ __forceinline__ F2 exp_sum(const uint4& v, F2 c2, F2 nmc2);
   // running maximum of raw vectors, two bf16 lanes per word (max.bf16x2 is
   // exact: it only selects one of its inputs)
   static __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
@@ -68,6 +106,8 @@ struct Elem<uint16_t> {
 template <>
 struct Elem<float> {
   static constexpr int kVec = 4;
+  // exp2(x * c - mc) summed over a raw vector, as a packed pair of partial sums
+  static __device__ __forceinline__ F2 exp_sum(const uint4& v, F2 c2, F2 nmc2);
   // running maximum of raw vectors (kept as four floats)
   static __device__ __forceinline__ uint4 max_init() {
     const uint32_t n = __float_as_uint(-INFINITY);
@@ -93,15 +133,22 @@ struct Elem<float> {
   }
 };
 
-// ---------------------------------------------------------------------------
-// 2^x as one ex2.approx.ftz.f32 instruction (relative error about 2 ulp;
-// results below 2^-126 flush to zero, which no sum here can notice).  Every
-// weight and every partial sum of a row uses this same function.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
+__device__ __forceinline__ F2 f2_exp2(F2 a) {
+  float lo, hi;
+  f2_split(a, lo, hi);
+  return f2_make(fast_exp2(lo), fast_exp2(hi));
+}
+__device__ __forceinline__ F2 Elem<uint16_t>::exp_sum(const uint4& v, F2 c2, F2 nmc2) {
+  const F2 a = f2_exp2(f2_fma(f2_make(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u)), c2, nmc2));
+  const F2 b = f2_exp2(f2_fma(f2_make(__uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u)), c2, nmc2));
+  const F2 d = f2_exp2(f2_fma(f2_make(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xFFFF0000u)), c2, nmc2));
+  const F2 e = f2_exp2(f2_fma(f2_make(__uint_as_float(v.w << 16), __uint_as_float(v.w & 0xFFFF0000u)), c2, nmc2));
+  return f2_add(f2_add(a, b), f2_add(d, e));
+}
+__device__ __forceinline__ F2 Elem<float>::exp_sum(const uint4& v, F2 c2, F2 nmc2) {
+  const F2 a = f2_exp2(f2_fma(f2_make(__uint_as_float(v.x), __uint_as_float(v.y)), c2, nmc2));
+  const F2 b = f2_exp2(f2_fma(f2_make(__uint_as_float(v.z), __uint_as_float(v.w)), c2, nmc2));
+  return f2_add(a, b);
 }
 
 // ---------------------------------------------------------------------------

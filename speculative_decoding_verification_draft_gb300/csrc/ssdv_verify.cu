@@ -113,18 +113,15 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const VerifyArgs a) {
   constexpr int kVec = Elem<E>::kVec;
   extern __shared__ __align__(128) uint8_t dyn_smem[];
   __shared__ __align__(8) uint64_t bar;
-  __shared__ float red[4][kWarps];
-  __shared__ int red_i[kWarps];
-  __shared__ float sh_mt, sh_md;
+  __shared__ float red_f[5 * kWarps];
+  __shared__ int red_i[2 * kWarps];
   __shared__ int sh_ok;
   griddep_launch_dependents();
 
   const ChunkGeometry& geo = a.geo;
   const int V = geo.V, NC = geo.nchunk, W = a.gmax + 1;
-  const int c = blockIdx.x % NC;
-  const int unit = blockIdx.x / NC;
-  const int b = unit / W, i = unit % W;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int c = blockIdx.x, i = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x;
   // The first CTA of each request clears the request's arrival counters for
   // the sampling kernel (which only reads them after this grid completes).
   if (i == 0 && c == 0 && tid < W) a.ticket[b * W + tid] = 0;
@@ -149,10 +146,14 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const VerifyArgs a) {
   // carries its two logits for the accept test
   const int x = (has_draft && tid == 0) ? a.draft_tokens[static_cast<size_t>(b) * a.gmax + i] : -1;
   const bool ok = stage_chunk(sl, &bar, &sh_ok);
+  const uint4* vt = reinterpret_cast<const uint4*>(sl.st);
+  const uint4* vd = reinterpret_cast<const uint4*>(sl.sd);
 
-  // pass 1: maxima (and the target argmax: each thread scans its vectors in
-  // index order, so the first of equal values is kept)
-  float mt = -INFINITY, md = -INFINITY;
+  // Each thread reduces its own vectors (index order, so the first of equal
+  // values wins the argmax): pass 1 the maxima, pass 2 the sums of
+  // exp2(x*c - fl(m*c)) against the thread's own maxima; one block reduction
+  // of the (max, sum) pairs follows.
+  MaxSum t{-INFINITY, 0.f}, d{-INFINITY, 0.f};
   ArgMax am{-INFINITY, -1};
   if (greedy) {
     for (int v = tid; v < sl.nvec; v += kThreads) {
@@ -160,96 +161,58 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const VerifyArgs a) {
       load_vec(sl.st, v, xt);
 #pragma unroll
       for (int e = 0; e < kVec; ++e) {
-        mt = fmaxf(mt, xt[e]);
         if (am.i < 0 || xt[e] > am.v) {
           am.v = xt[e];
           am.i = lo + v * kVec + e;
         }
       }
     }
+    t.m = am.v;
   } else {
     uint4 pt = Elem<E>::max_init(), pd = Elem<E>::max_init();
-    const uint4* vt = reinterpret_cast<const uint4*>(sl.st);
-    const uint4* vd = reinterpret_cast<const uint4*>(sl.sd);
     for (int v = tid; v < sl.nvec; v += kThreads) {
       pt = Elem<E>::max_acc(pt, vt[v]);
       if (has_draft) pd = Elem<E>::max_acc(pd, vd[v]);
     }
-    mt = Elem<E>::max_final(pt);
-    md = Elem<E>::max_final(pd);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, o));
-    md = fmaxf(md, __shfl_xor_sync(0xFFFFFFFFu, md, o));
-    const ArgMax oa{__shfl_xor_sync(0xFFFFFFFFu, am.v, o), __shfl_xor_sync(0xFFFFFFFFu, am.i, o)};
-    am = better_arg(am, oa);
-  }
-  if (lane == 0) {
-    red[0][warp] = mt;
-    red[1][warp] = md;
-    red[2][warp] = am.v;
-    red_i[warp] = am.i;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    float m0 = -INFINITY, m1 = -INFINITY;
-    ArgMax a0{-INFINITY, -1};
-    for (int w = 0; w < kWarps; ++w) {
-      m0 = fmaxf(m0, red[0][w]);
-      m1 = fmaxf(m1, red[1][w]);
-      a0 = better_arg(a0, ArgMax{red[2][w], red_i[w]});
+    t.m = Elem<E>::max_final(pt);
+    d.m = Elem<E>::max_final(pd);
+    const float cc = kLog2e / T;
+    const F2 c2 = f2_make(cc, cc);
+    if (t.m != -INFINITY) {
+      const float nm = -scaled_max(t.m, cc);
+      const F2 nm2 = f2_make(nm, nm);
+      F2 acc = f2_make(0.f, 0.f);
+      for (int v = tid; v < sl.nvec; v += kThreads) acc = f2_add(acc, Elem<E>::exp_sum(vt[v], c2, nm2));
+      float lo_s, hi_s;
+      f2_split(acc, lo_s, hi_s);
+      t.s = lo_s + hi_s;
     }
-    sh_mt = m0;
-    sh_md = m1;
+    if (has_draft && d.m != -INFINITY) {
+      const float nm = -scaled_max(d.m, cc);
+      const F2 nm2 = f2_make(nm, nm);
+      F2 acc = f2_make(0.f, 0.f);
+      for (int v = tid; v < sl.nvec; v += kThreads) acc = f2_add(acc, Elem<E>::exp_sum(vd[v], c2, nm2));
+      float lo_s, hi_s;
+      f2_split(acc, lo_s, hi_s);
+      d.s = lo_s + hi_s;
+    }
+  }
+  ThreadStats<E> ts{t, d, am, !ok};
+  const BlockStats bs = block_reduce_stats(ts, greedy ? 1.f : kLog2e / T, red_f, red_i);
+  if (tid == 0) {
+    float4* rec = a.part + ((static_cast<size_t>(b) * W + i) * NC + c) * 2;
     if (greedy) {
-      float4* rec = a.part + (static_cast<size_t>(unit) * NC + c) * 2;
-      rec[0] = make_float4(m0, 0.f, -INFINITY, 0.f);
-      rec[1] = make_float4(a0.v, __int_as_float(a0.i), __int_as_float(ok ? 0 : 1), 0.f);
+      rec[0] = make_float4(bs.a.v, 0.f, -INFINITY, 0.f);
+      rec[1] = make_float4(bs.a.v, __int_as_float(bs.a.i), __int_as_float(bs.timeout), 0.f);
+    } else {
+      rec[0] = make_float4(bs.t.m, bs.t.s, has_draft ? bs.d.m : -INFINITY, bs.d.s);
+      float xt_tok = 0.f, xd_tok = 0.f;
+      if (x >= lo && x < lo + sl.n) {
+        xt_tok = Elem<E>::to_float(sl.st[x - lo]);
+        xd_tok = Elem<E>::to_float(sl.sd[x - lo]);
+      }
+      rec[1] = make_float4(xd_tok, 0.f, __int_as_float(bs.timeout), xt_tok);
     }
-  }
-  __syncthreads();
-  if (greedy) return;
-
-  // pass 2: sums of exp2(x*c - fl(m*c)) against the chunk maxima
-  const float cc = kLog2e / T;
-  const float mct = scaled_max(sh_mt, cc), mcd = scaled_max(sh_md, cc);
-  float st = 0.f, sd = 0.f;
-  for (int v = tid; v < sl.nvec; v += kThreads) {
-    float xt[kVec], et[kVec];
-    load_vec(sl.st, v, xt);
-#pragma unroll
-    for (int e = 0; e < kVec; ++e) et[e] = fast_exp2(fmaf(xt[e], cc, -mct));
-    st += pair_sum(et);
-    if (has_draft) {
-      float xd[kVec], ed[kVec];
-      load_vec(sl.sd, v, xd);
-#pragma unroll
-      for (int e = 0; e < kVec; ++e) ed[e] = fast_exp2(fmaf(xd[e], cc, -mcd));
-      sd += pair_sum(ed);
-    }
-  }
-  st = warp_sum(st);
-  sd = warp_sum(sd);
-  if (lane == 0) {
-    red[0][warp] = st;
-    red[1][warp] = sd;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    float s0 = 0.f, s1 = 0.f;
-    for (int w = 0; w < kWarps; ++w) {
-      s0 += red[0][w];
-      s1 += red[1][w];
-    }
-    float4* rec = a.part + (static_cast<size_t>(unit) * NC + c) * 2;
-    rec[0] = make_float4(sh_mt, s0, has_draft ? sh_md : -INFINITY, s1);
-    float xt_tok = 0.f, xd_tok = 0.f;
-    if (x >= lo && x < lo + sl.n) {
-      xt_tok = Elem<E>::to_float(sl.st[x - lo]);
-      xd_tok = Elem<E>::to_float(sl.sd[x - lo]);
-    }
-    rec[1] = make_float4(xd_tok, 0.f, __int_as_float(ok ? 0 : 1), xt_tok);
   }
 }
 
@@ -330,21 +293,49 @@ struct GlobalRange {
 };
 
 // Weighted pass over a global row range: each warp owns a contiguous run of
-// vectors (lanes interleaved: coalesced).  Per-warp sums to wsum[] (shared),
-// returns the CTA sum (fp64 over warps) in thread 0.
+// vectors (lanes interleaved: coalesced); loads are issued four vectors at a
+// time before any is used.  Per-warp sums to wsum[] (shared), returns the CTA
+// sum (fp64 over warps) in thread 0.
 template <typename E, typename WFun>
 __device__ __forceinline__ double global_weighted_pass(const GlobalRange<E>& rg, const WFun& wfun, float* wsum) {
   constexpr int kVec = Elem<E>::kVec;
+  constexpr int kBatch = 4;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nvec = (rg.n + kVec - 1) / kVec;
   int v0, v1;
   warp_range(nvec, warp, v0, v1);
   float acc = 0.f;
-  for (int v = v0 + lane; v < v1; v += 32) {
-    float xt[kVec], xd[kVec], w[kVec];
-    rg(v, xt, xd);
-    wfun(xt, xd, w);
-    acc += pair_sum(w);
+  if (rg.aligned) {
+    const uint4* gt = reinterpret_cast<const uint4*>(rg.gt);
+    const uint4* gd = reinterpret_cast<const uint4*>(rg.gd);
+    for (int vb = v0 + lane; vb < v1; vb += 32 * kBatch) {
+      uint4 rt[kBatch], rd[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const int v = vb + 32 * k;
+        if (v < v1) {
+          rt[k] = __ldg(gt + v);
+          if (rg.gd) rd[k] = __ldg(gd + v);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        if (vb + 32 * k < v1) {
+          float xt[kVec], xd[kVec], w[kVec];
+          Elem<E>::unpack(rt[k], xt);
+          if (rg.gd) Elem<E>::unpack(rd[k], xd);
+          wfun(xt, xd, w);
+          acc += pair_sum(w);
+        }
+      }
+    }
+  } else {
+    for (int v = v0 + lane; v < v1; v += 32) {
+      float xt[kVec], xd[kVec], w[kVec];
+      rg(v, xt, xd);
+      wfun(xt, xd, w);
+      acc += pair_sum(w);
+    }
   }
   acc = warp_sum(acc);
   if (lane == 0) wsum[warp] = acc;
@@ -356,26 +347,46 @@ __device__ __forceinline__ double global_weighted_pass(const GlobalRange<E>& rg,
 }
 
 // The draw inside one global row range whose per-warp sums are ws8[]: warp 0
-// picks the warp run holding tl (relative to the range start) and scans it.
+// picks the warp run holding tl (relative to the range start), stages that
+// run into shared memory (all loads in flight at once) and scans it.
+constexpr int kMaxRun = 512;  // vectors per warp run of a sampling range
+
 template <typename E, typename WFun>
 __device__ __forceinline__ ScanHit draw_in_range(const GlobalRange<E>& rg, const WFun& wfun, const float* ws8,
-                                                 double tl, double* run_base) {
+                                                 double tl, double* run_base, uint4* run_t, uint4* run_d) {
   constexpr int kVec = Elem<E>::kVec;
+  const int lane = threadIdx.x & 31;
   double wbase = 0.0;
   const int wpick = pick_warp(ws8, kWarps, tl, &wbase);
   ScanHit h{-1, NAN, 0.f};
-  if (wpick >= 0) {
-    int v0, v1;
-    warp_range((rg.n + kVec - 1) / kVec, wpick, v0, v1);
+  *run_base = wbase;
+  if (wpick < 0) return h;
+  int v0, v1;
+  warp_range((rg.n + kVec - 1) / kVec, wpick, v0, v1);
+  if (rg.aligned && v1 - v0 <= kMaxRun) {
+    const uint4* gt = reinterpret_cast<const uint4*>(rg.gt);
+    const uint4* gd = reinterpret_cast<const uint4*>(rg.gd);
+#pragma unroll 8
+    for (int v = v0 + lane; v < v1; v += 32) {
+      run_t[v - v0] = __ldg(gt + v);
+      if (rg.gd) run_d[v - v0] = __ldg(gd + v);
+    }
+    __syncwarp();
+    auto load = [&](int v, float(&xt)[kVec], float(&xd)[kVec]) {
+      Elem<E>::unpack(run_t[v - v0], xt);
+      if (rg.gd) Elem<E>::unpack(run_d[v - v0], xd);
+    };
+    h = warp_scan<kVec>(v0, v1, tl - wbase, load, wfun);
+  } else {
     h = warp_scan<kVec>(v0, v1, tl - wbase, rg, wfun);
   }
-  *run_base = wbase;
   return h;
 }
 
 template <typename E>
 __global__ void __launch_bounds__(kThreads) sample_kernel(const VerifyArgs a) {
   __shared__ UnitStat ust[SSD_MAX_GAMMA + 1];
+  __shared__ uint4 run_t[kMaxRun], run_d[kMaxRun];
   __shared__ int tok_x[SSD_MAX_GAMMA];
   __shared__ float tok_t[SSD_MAX_GAMMA], tok_d[SSD_MAX_GAMMA];
   __shared__ float wsum[kWarps];
@@ -387,11 +398,7 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const VerifyArgs a) {
   const int V = geo.V, NC = geo.nchunk, W = a.gmax + 1;
   const int span = geo.span * geo.chunk;  // elements per sampling range
   const int NR = (V + span - 1) / span;   // sampling ranges per row
-  const int P = a.debug ? W : 1;
-  const int c = blockIdx.x % NR;
-  const int rest = blockIdx.x / NR;
-  const int pi = rest % P;
-  const int b = rest / P;
+  const int c = blockIdx.x, pi = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   const int g = a.gamma ? a.gamma[b] : a.gmax;
@@ -603,7 +610,7 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const VerifyArgs a) {
         const int lo = owner * span;
         const GlobalRange<E> rg{trow + lo, drow + lo, min(span, V - lo), aligned};
         double run_base;
-        const ScanHit h = draw_in_range(rg, rw, ws8, sh_local, &run_base);
+        const ScanHit h = draw_in_range(rg, rw, ws8, sh_local, &run_base, run_t, run_d);
         if (lane == 0) {
           if (h.elem < 0) {
             write_error(a, b);
@@ -650,7 +657,7 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const VerifyArgs a) {
   global_weighted_pass(rg, tw, wsum);
   if (warp == 0) {
     double run_base;
-    const ScanHit h = draw_in_range(rg, tw, wsum, sh_local, &run_base);
+    const ScanHit h = draw_in_range(rg, tw, wsum, sh_local, &run_base, run_t, run_d);
     if (lane == 0) {
       if (h.elem < 0) {
         write_error(a, b);
@@ -714,15 +721,14 @@ cudaError_t launch_verify_t(const VerifyArgs& a, int smem_bytes, cudaStream_t st
   e = ensure_smem(reinterpret_cast<const void*>(&stream_kernel<E>), smem_bytes, &smem1);
   if (e != cudaSuccess) return e;
 
-  const long long units = static_cast<long long>(a.B) * (a.gmax + 1);
-  stream_kernel<E><<<static_cast<unsigned>(units * a.geo.nchunk), kThreads, smem_bytes, stream>>>(a);
+  stream_kernel<E><<<dim3(a.geo.nchunk, a.gmax + 1, a.B), kThreads, smem_bytes, stream>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int P = a.debug ? a.gmax + 1 : 1;
   const int span = a.geo.span * a.geo.chunk;
   const int nr = (a.geo.V + span - 1) / span;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(static_cast<long long>(a.B) * P * nr), 1, 1);
+  cfg.gridDim = dim3(nr, P, a.B);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
