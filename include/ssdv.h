@@ -101,7 +101,7 @@ ssd_status ssd_workspace_init(void* workspace, size_t ws_bytes, void* stream);
  *   n_accepted     [B] int32: n in 0..gamma (-1 for a request with an error)
  *   workspace      >= ssd_workspace_bytes(B, gamma) bytes, zeroed once
  *
- * Constraints: 1 <= B <= 65535, 0 <= gamma <= SSD_MAX_GAMMA, 1 <= V <= SSD_MAX_V. */
+ * Constraints: 1 <= B, 0 <= gamma <= SSD_MAX_GAMMA, 1 <= V <= SSD_MAX_V. */
 ssd_status ssd_verify(const void* target_logits, const void* draft_logits, ssd_dtype dtype,
                       const int32_t* draft_tokens, int B, int gamma, int V, float temperature,
                       uint64_t seed, int32_t* out_tokens, int32_t* n_accepted, void* workspace,

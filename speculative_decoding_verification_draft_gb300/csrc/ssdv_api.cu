@@ -56,8 +56,8 @@ WorkspaceLayout workspace_layout(int B, int gmax) {
   L.ticket = 16;
   L.part = round_up(L.ticket + 4 * units, 256);
   L.csum = L.part + units * kMaxChunks * 2 * sizeof(float4);
-  L.wsums = L.csum + units * kMaxChunks * sizeof(double);
-  L.total = round_up(L.wsums + units * kMaxChunks * kWarps * sizeof(float), 256);
+  L.blocks = L.csum + units * kMaxChunks * sizeof(double);
+  L.total = round_up(L.blocks + units * kMaxChunks * 128 * sizeof(float), 256);
   return L;
 }
 
@@ -99,14 +99,14 @@ ssd_status choose_geometry(int V, int esize, bool aligned, bool two_rows, Geomet
   }
 }
 
-// Split a row of V elements into chunks for verification: about 16 KB of each
+// Split a row of V elements into chunks for verification: about 24 KB of each
 // row per CTA (SSDV_CHUNK_BYTES overrides), at most kMaxChunks chunks, each a
 // multiple of 8 elements.
 ssd_status choose_chunks(int V, int esize, bool aligned, ChunkGeometry* geo, int* smem_bytes) {
   const int max_smem = max_dynamic_smem();
   if (max_smem <= 0) return fail(SSD_ERR_CUDA, "cannot query the device's shared-memory limit");
   const long long row_bytes = static_cast<long long>(V) * esize;
-  const int want = env_int("SSDV_CHUNK_BYTES", 16 * 1024);
+  const int want = env_int("SSDV_CHUNK_BYTES", 24 * 1024);
   long long nc = (row_bytes + want - 1) / want;
   if (nc < 1) nc = 1;
   if (nc > kMaxChunks) nc = kMaxChunks;
@@ -142,7 +142,7 @@ ssd_status verify_common(const void* target, const void* draft, ssd_dtype dtype,
   if (!draft && !all_greedy && gmax > 0)
     return fail(SSD_ERR_NULL, "draft_logits is NULL but some request samples");
   if (gmax > 0 && !draft_tokens) return fail(SSD_ERR_NULL, "draft_tokens is NULL");
-  if (B < 1 || B > 65535 || gmax < 0 || gmax > SSD_MAX_GAMMA || V < 1 || V > SSD_MAX_V)
+  if (B < 1 || gmax < 0 || gmax > SSD_MAX_GAMMA || V < 1 || V > SSD_MAX_V)
     return fail(SSD_ERR_SHAPE, "bad shape B=%d gamma=%d V=%d", B, gmax, V);
   if (!aligned_to(target, es) || (draft && !aligned_to(draft, es)) || !aligned_to(out_tokens, 4) ||
       !aligned_to(n_accepted, 4) || (draft_tokens && !aligned_to(draft_tokens, 4)) || !aligned_to(workspace, 16) ||
@@ -166,6 +166,7 @@ ssd_status verify_common(const void* target, const void* draft, ssd_dtype dtype,
   a.draft_tokens = draft_tokens;
   a.B = B;
   a.gmax = gmax;
+  a.req_base = 0;
   a.gamma = gamma;
   a.temps = temps;
   a.temp_scalar = temp_scalar;
@@ -176,12 +177,28 @@ ssd_status verify_common(const void* target, const void* draft, ssd_dtype dtype,
   a.ticket = reinterpret_cast<int32_t*>(ws + L.ticket);
   a.part = reinterpret_cast<float4*>(ws + L.part);
   a.csum = reinterpret_cast<double*>(ws + L.csum);
-  a.wsums = reinterpret_cast<float*>(ws + L.wsums);
+  a.blocks = reinterpret_cast<float*>(ws + L.blocks);
   a.stats = stats;
   a.debug = stats ? 1 : 0;
   a.geo = geo;
-  const cudaError_t e = launch_verify(a, es, smem, static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(e, "verify launch");
+  // Launch in slices of at most 65535 requests (the grid's third dimension);
+  // each slice keeps its requests' global indices for the Philox counters.
+  const int W = gmax + 1;
+  for (int b0 = 0; b0 < B; b0 += 65535) {
+    VerifyArgs s = a;
+    s.B = B - b0 < 65535 ? B - b0 : 65535;
+    s.req_base = b0;
+    s.target = static_cast<const uint8_t*>(target) + static_cast<size_t>(b0) * W * V * es;
+    if (draft) s.draft = static_cast<const uint8_t*>(draft) + static_cast<size_t>(b0) * gmax * V * es;
+    if (draft_tokens) s.draft_tokens = draft_tokens + static_cast<size_t>(b0) * gmax;
+    if (gamma) s.gamma = gamma + b0;
+    if (temps) s.temps = temps + b0;
+    s.out_tokens = out_tokens + static_cast<size_t>(b0) * W;
+    s.n_accepted = n_accepted + b0;
+    if (stats) s.stats = stats + static_cast<size_t>(b0) * W * SSD_NSTAT_VERIFY;
+    const cudaError_t e = launch_verify(s, es, smem, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "verify launch");
+  }
   return SSD_OK;
 }
 

@@ -38,6 +38,7 @@ struct VerifyArgs {
   const void* draft;           // [B, gmax, V] (may be null if every request is greedy)
   const int32_t* draft_tokens; // [B, gmax]
   int B, gmax;
+  int req_base;                // request index of row 0 in the Philox counters
   const int32_t* gamma;        // [B] or null (every request uses gmax)
   const float* temps;          // [B] or null (temp_scalar)
   float temp_scalar;
@@ -46,7 +47,7 @@ struct VerifyArgs {
   int32_t* n_accepted;         // [B]
   float4* part;                // workspace [B, gmax+1, nchunk, 2]: per-chunk row statistics
   double* csum;                // workspace [B, gmax+1, nchunk]: per-chunk residual weight sums
-  float* wsums;                // workspace [B, gmax+1, nchunk, 8]: their per-warp parts
+  float* blocks;               // workspace [B, gmax+1, nchunk, 128]: their 32-vector block sums
   int32_t* ticket;             // workspace [B, gmax+1]: residual chunks arrived
   int32_t* status;             // workspace [1]: device error bits
   float* stats;                // [B, gmax+1, SSD_NSTAT_VERIFY] or null (debug)
@@ -68,7 +69,7 @@ struct SaguaroArgs {
 
 // Workspace layout (byte offsets), shared by the launchers and the API.
 struct WorkspaceLayout {
-  size_t status, ticket, part, csum, wsums, total;
+  size_t status, ticket, part, csum, blocks, total;
 };
 WorkspaceLayout workspace_layout(int B, int gmax);
 

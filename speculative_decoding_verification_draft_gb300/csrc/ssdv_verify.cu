@@ -149,13 +149,12 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const VerifyArgs a) {
   const uint4* vt = reinterpret_cast<const uint4*>(sl.st);
   const uint4* vd = reinterpret_cast<const uint4*>(sl.sd);
 
-  // Each thread reduces its own vectors (index order, so the first of equal
-  // values wins the argmax): pass 1 the maxima, pass 2 the sums of
-  // exp2(x*c - fl(m*c)) against the thread's own maxima; one block reduction
-  // of the (max, sum) pairs follows.
-  MaxSum t{-INFINITY, 0.f}, d{-INFINITY, 0.f};
-  ArgMax am{-INFINITY, -1};
+  const int warp = tid >> 5, lane = tid & 31;
+  float4* rec = a.part + ((static_cast<size_t>(b) * W + i) * NC + c) * 2;
   if (greedy) {
+    // Target argmax: each thread scans its vectors in index order (the first
+    // of equal values wins), then a warp butterfly and thread 0 over warps.
+    ArgMax am{-INFINITY, -1};
     for (int v = tid; v < sl.nvec; v += kThreads) {
       float xt[kVec];
       load_vec(sl.st, v, xt);
@@ -167,52 +166,93 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const VerifyArgs a) {
         }
       }
     }
-    t.m = am.v;
-  } else {
-    uint4 pt = Elem<E>::max_init(), pd = Elem<E>::max_init();
-    for (int v = tid; v < sl.nvec; v += kThreads) {
-      pt = Elem<E>::max_acc(pt, vt[v]);
-      if (has_draft) pd = Elem<E>::max_acc(pd, vd[v]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const ArgMax oa{__shfl_xor_sync(0xFFFFFFFFu, am.v, o), __shfl_xor_sync(0xFFFFFFFFu, am.i, o)};
+      am = better_arg(am, oa);
     }
-    t.m = Elem<E>::max_final(pt);
-    d.m = Elem<E>::max_final(pd);
-    const float cc = kLog2e / T;
-    const F2 c2 = f2_make(cc, cc);
-    if (t.m != -INFINITY) {
-      const float nm = -scaled_max(t.m, cc);
-      const F2 nm2 = f2_make(nm, nm);
-      F2 acc = f2_make(0.f, 0.f);
-      for (int v = tid; v < sl.nvec; v += kThreads) acc = f2_add(acc, Elem<E>::exp_sum(vt[v], c2, nm2));
-      float lo_s, hi_s;
-      f2_split(acc, lo_s, hi_s);
-      t.s = lo_s + hi_s;
+    if (lane == 0) {
+      red_f[warp] = am.v;
+      red_i[warp] = am.i;
     }
-    if (has_draft && d.m != -INFINITY) {
-      const float nm = -scaled_max(d.m, cc);
-      const F2 nm2 = f2_make(nm, nm);
-      F2 acc = f2_make(0.f, 0.f);
-      for (int v = tid; v < sl.nvec; v += kThreads) acc = f2_add(acc, Elem<E>::exp_sum(vd[v], c2, nm2));
-      float lo_s, hi_s;
-      f2_split(acc, lo_s, hi_s);
-      d.s = lo_s + hi_s;
+    __syncthreads();
+    if (tid == 0) {
+      ArgMax best{-INFINITY, -1};
+      for (int w = 0; w < kWarps; ++w) best = better_arg(best, ArgMax{red_f[w], red_i[w]});
+      rec[0] = make_float4(best.v, 0.f, -INFINITY, 0.f);
+      rec[1] = make_float4(best.v, __int_as_float(best.i), __int_as_float(ok ? 0 : 1), 0.f);
     }
+    return;
   }
-  ThreadStats<E> ts{t, d, am, !ok};
-  const BlockStats bs = block_reduce_stats(ts, greedy ? 1.f : kLog2e / T, red_f, red_i);
+
+  // pass 1: the chunk maxima (packed max per thread, warp butterfly, and every
+  // thread folds the eight warp maxima itself)
+  uint4 pt = Elem<E>::max_init(), pd = Elem<E>::max_init();
+  for (int v = tid; v < sl.nvec; v += kThreads) {
+    pt = Elem<E>::max_acc(pt, vt[v]);
+    if (has_draft) pd = Elem<E>::max_acc(pd, vd[v]);
+  }
+  float mt = Elem<E>::max_final(pt), md = Elem<E>::max_final(pd);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, o));
+    md = fmaxf(md, __shfl_xor_sync(0xFFFFFFFFu, md, o));
+  }
+  if (lane == 0) {
+    red_f[warp] = mt;
+    red_f[kWarps + warp] = md;
+  }
+  __syncthreads();
+  mt = red_f[0];
+  md = red_f[kWarps];
+#pragma unroll
+  for (int w = 1; w < kWarps; ++w) {
+    mt = fmaxf(mt, red_f[w]);
+    md = fmaxf(md, red_f[kWarps + w]);
+  }
+
+  // pass 2: sums of exp2(x*c - fl(m*c)) against the chunk maxima
+  const float cc = kLog2e / T;
+  const F2 c2 = f2_make(cc, cc);
+  float st = 0.f, sd = 0.f;
+  if (mt != -INFINITY) {
+    const float nm = -scaled_max(mt, cc);
+    const F2 nm2 = f2_make(nm, nm);
+    F2 acc = f2_make(0.f, 0.f);
+    for (int v = tid; v < sl.nvec; v += kThreads) acc = f2_add(acc, Elem<E>::exp_sum(vt[v], c2, nm2));
+    float a0, a1;
+    f2_split(acc, a0, a1);
+    st = a0 + a1;
+  }
+  if (has_draft && md != -INFINITY) {
+    const float nm = -scaled_max(md, cc);
+    const F2 nm2 = f2_make(nm, nm);
+    F2 acc = f2_make(0.f, 0.f);
+    for (int v = tid; v < sl.nvec; v += kThreads) acc = f2_add(acc, Elem<E>::exp_sum(vd[v], c2, nm2));
+    float a0, a1;
+    f2_split(acc, a0, a1);
+    sd = a0 + a1;
+  }
+  st = warp_sum(st);
+  sd = warp_sum(sd);
+  if (lane == 0) {
+    red_f[2 * kWarps + warp] = st;
+    red_f[3 * kWarps + warp] = sd;
+  }
+  __syncthreads();
   if (tid == 0) {
-    float4* rec = a.part + ((static_cast<size_t>(b) * W + i) * NC + c) * 2;
-    if (greedy) {
-      rec[0] = make_float4(bs.a.v, 0.f, -INFINITY, 0.f);
-      rec[1] = make_float4(bs.a.v, __int_as_float(bs.a.i), __int_as_float(bs.timeout), 0.f);
-    } else {
-      rec[0] = make_float4(bs.t.m, bs.t.s, has_draft ? bs.d.m : -INFINITY, bs.d.s);
-      float xt_tok = 0.f, xd_tok = 0.f;
-      if (x >= lo && x < lo + sl.n) {
-        xt_tok = Elem<E>::to_float(sl.st[x - lo]);
-        xd_tok = Elem<E>::to_float(sl.sd[x - lo]);
-      }
-      rec[1] = make_float4(xd_tok, 0.f, __int_as_float(bs.timeout), xt_tok);
+    float s0 = 0.f, s1 = 0.f;
+    for (int w = 0; w < kWarps; ++w) {
+      s0 += red_f[2 * kWarps + w];
+      s1 += red_f[3 * kWarps + w];
     }
+    rec[0] = make_float4(mt, s0, has_draft ? md : -INFINITY, s1);
+    float xt_tok = 0.f, xd_tok = 0.f;
+    if (x >= lo && x < lo + sl.n) {
+      xt_tok = Elem<E>::to_float(sl.st[x - lo]);
+      xd_tok = Elem<E>::to_float(sl.sd[x - lo]);
+    }
+    rec[1] = make_float4(xd_tok, 0.f, __int_as_float(ok ? 0 : 1), xt_tok);
   }
 }
 
@@ -294,10 +334,13 @@ struct GlobalRange {
 
 // Weighted pass over a global row range: each warp owns a contiguous run of
 // vectors (lanes interleaved: coalesced); loads are issued four vectors at a
-// time before any is used.  Per-warp sums to wsum[] (shared), returns the CTA
+// time before any is used.  Per-warp sums go to wsum[] (shared) and, when
+// `blocks` is given, the sum of every 32-vector block of each warp's run to
+// blocks[warp * bpw + j] (global; blocks in index order).  Returns the CTA
 // sum (fp64 over warps) in thread 0.
 template <typename E, typename WFun>
-__device__ __forceinline__ double global_weighted_pass(const GlobalRange<E>& rg, const WFun& wfun, float* wsum) {
+__device__ __forceinline__ double global_weighted_pass(const GlobalRange<E>& rg, const WFun& wfun, float* wsum,
+                                                       float* blocks, int bpw) {
   constexpr int kVec = Elem<E>::kVec;
   constexpr int kBatch = 4;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -305,10 +348,11 @@ __device__ __forceinline__ double global_weighted_pass(const GlobalRange<E>& rg,
   int v0, v1;
   warp_range(nvec, warp, v0, v1);
   float acc = 0.f;
+  int j = 0;
   if (rg.aligned) {
     const uint4* gt = reinterpret_cast<const uint4*>(rg.gt);
     const uint4* gd = reinterpret_cast<const uint4*>(rg.gd);
-    for (int vb = v0 + lane; vb < v1; vb += 32 * kBatch) {
+    for (int vb = v0 + lane; vb - lane < v1; vb += 32 * kBatch) {
       uint4 rt[kBatch], rd[kBatch];
 #pragma unroll
       for (int k = 0; k < kBatch; ++k) {
@@ -320,23 +364,43 @@ __device__ __forceinline__ double global_weighted_pass(const GlobalRange<E>& rg,
       }
 #pragma unroll
       for (int k = 0; k < kBatch; ++k) {
+        if (vb - lane + 32 * k >= v1) break;  // warp-uniform
+        float vs = 0.f;
         if (vb + 32 * k < v1) {
           float xt[kVec], xd[kVec], w[kVec];
           Elem<E>::unpack(rt[k], xt);
           if (rg.gd) Elem<E>::unpack(rd[k], xd);
           wfun(xt, xd, w);
-          acc += pair_sum(w);
+          vs = pair_sum(w);
         }
+        acc += vs;
+        if (blocks) {
+          const float bsum = warp_sum(vs);
+          if (lane == 0) blocks[warp * bpw + j] = bsum;
+        }
+        ++j;
       }
     }
   } else {
-    for (int v = v0 + lane; v < v1; v += 32) {
-      float xt[kVec], xd[kVec], w[kVec];
-      rg(v, xt, xd);
-      wfun(xt, xd, w);
-      acc += pair_sum(w);
+    for (int vb = v0; vb < v1; vb += 32) {
+      const int v = vb + lane;
+      float vs = 0.f;
+      if (v < v1) {
+        float xt[kVec], xd[kVec], w[kVec];
+        rg(v, xt, xd);
+        wfun(xt, xd, w);
+        vs = pair_sum(w);
+      }
+      acc += vs;
+      if (blocks) {
+        const float bsum = warp_sum(vs);
+        if (lane == 0) blocks[warp * bpw + j] = bsum;
+      }
+      ++j;
     }
   }
+  if (blocks && lane == 0)
+    for (; j < bpw; ++j) blocks[warp * bpw + j] = 0.f;
   acc = warp_sum(acc);
   if (lane == 0) wsum[warp] = acc;
   __syncthreads();
@@ -346,47 +410,61 @@ __device__ __forceinline__ double global_weighted_pass(const GlobalRange<E>& rg,
   return cta;
 }
 
-// The draw inside one global row range whose per-warp sums are ws8[]: warp 0
-// picks the warp run holding tl (relative to the range start), stages that
-// run into shared memory (all loads in flight at once) and scans it.
-constexpr int kMaxRun = 512;  // vectors per warp run of a sampling range
-
-template <typename E, typename WFun>
-__device__ __forceinline__ ScanHit draw_in_range(const GlobalRange<E>& rg, const WFun& wfun, const float* ws8,
-                                                 double tl, double* run_base, uint4* run_t, uint4* run_d) {
-  constexpr int kVec = Elem<E>::kVec;
+// Warp-wide: the 32-vector block of a range that holds target tl (relative
+// to the range start), from the range's block sums (nb of them, in index
+// order); returns the block (-1 if no positive weight) and the weight before
+// it.  A target past every boundary goes to the last positive block.
+__device__ __forceinline__ int locate_block(const float* blocks, int nb, double tl, double* before) {
   const int lane = threadIdx.x & 31;
-  double wbase = 0.0;
-  const int wpick = pick_warp(ws8, kWarps, tl, &wbase);
-  ScanHit h{-1, NAN, 0.f};
-  *run_base = wbase;
-  if (wpick < 0) return h;
-  int v0, v1;
-  warp_range((rg.n + kVec - 1) / kVec, wpick, v0, v1);
-  if (rg.aligned && v1 - v0 <= kMaxRun) {
-    const uint4* gt = reinterpret_cast<const uint4*>(rg.gt);
-    const uint4* gd = reinterpret_cast<const uint4*>(rg.gd);
-#pragma unroll 8
-    for (int v = v0 + lane; v < v1; v += 32) {
-      run_t[v - v0] = __ldg(gt + v);
-      if (rg.gd) run_d[v - v0] = __ldg(gd + v);
-    }
-    __syncwarp();
-    auto load = [&](int v, float(&xt)[kVec], float(&xd)[kVec]) {
-      Elem<E>::unpack(run_t[v - v0], xt);
-      if (rg.gd) Elem<E>::unpack(run_d[v - v0], xd);
-    };
-    h = warp_scan<kVec>(v0, v1, tl - wbase, load, wfun);
-  } else {
-    h = warp_scan<kVec>(v0, v1, tl - wbase, rg, wfun);
+  const int per = (nb + 31) / 32;  // consecutive blocks per lane
+  double mine = 0.0;
+  for (int k = 0; k < per; ++k) {
+    const int q = lane * per + k;
+    if (q < nb) mine += static_cast<double>(*reinterpret_cast<const volatile float*>(blocks + q));
   }
-  return h;
+  double incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  const unsigned hit = __ballot_sync(0xFFFFFFFFu, mine > 0.0 && tl < incl);
+  const unsigned pos = __ballot_sync(0xFFFFFFFFu, mine > 0.0);
+  if (!pos) return -1;
+  const int L = hit ? __ffs(hit) - 1 : 31 - __clz(pos);
+  double acc = __shfl_sync(0xFFFFFFFFu, incl - mine, L);
+  int found = -1, last = -1;
+  double found_before = 0.0, last_before = 0.0;
+  for (int k = 0; k < per; ++k) {  // every lane walks lane L's blocks
+    const int q = L * per + k;
+    if (q >= nb) break;
+    const double w = static_cast<double>(*reinterpret_cast<const volatile float*>(blocks + q));
+    if (w > 0.0) {
+      last = q;
+      last_before = acc;
+      if (found < 0 && tl < acc + w) {
+        found = q;
+        found_before = acc;
+      }
+    }
+    acc += w;
+  }
+  if (found < 0) {
+    found = last;
+    found_before = last_before;
+  }
+  *before = found_before;
+  return found;
 }
 
+// Block sums kept per sampling range: 32-vector blocks of at most 64 KB of
+// a row (4096 bf16 vectors / 8 warps / 32 = 16 per warp).
+constexpr int kBlocksPerRange = 128;
+
 template <typename E>
-__global__ void __launch_bounds__(kThreads) sample_kernel(const VerifyArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) sample_kernel(const VerifyArgs a) {
   __shared__ UnitStat ust[SSD_MAX_GAMMA + 1];
-  __shared__ uint4 run_t[kMaxRun], run_d[kMaxRun];
+  __shared__ float sh_blocks[kBlocksPerRange];
   __shared__ int tok_x[SSD_MAX_GAMMA];
   __shared__ float tok_t[SSD_MAX_GAMMA], tok_d[SSD_MAX_GAMMA];
   __shared__ float wsum[kWarps];
@@ -398,6 +476,8 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const VerifyArgs a) {
   const int V = geo.V, NC = geo.nchunk, W = a.gmax + 1;
   const int span = geo.span * geo.chunk;  // elements per sampling range
   const int NR = (V + span - 1) / span;   // sampling ranges per row
+  constexpr int kVec = Elem<E>::kVec;
+  const int bpw = ((span + kVec - 1) / kVec + kWarps * 32 - 1) / (kWarps * 32);  // blocks per warp run
   const int c = blockIdx.x, pi = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -467,7 +547,7 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const VerifyArgs a) {
 
   // Decisions: accept tests of positions 0..g-1 and the first rejection.
   if (warp == 0) {
-    const Draws dr = unit_draws(a.seed, b, min(lane, g));
+    const Draws dr = unit_draws(a.seed, a.req_base + b, min(lane, g));
     bool acc = true;
     float ratio_acc = 1.f;
     if (lane < g) {
@@ -488,7 +568,7 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const VerifyArgs a) {
     const int n = rej ? __ffs(rej) - 1 : g;
     if (lane == 0) {
       sh_n = n;
-      sh_ures = unit_draws(a.seed, b, a.debug ? pi : n).resample;
+      sh_ures = unit_draws(a.seed, a.req_base + b, a.debug ? pi : n).resample;
     }
     if (a.stats && c == 0 && lane == pi) {
       float* st = a.stats + (static_cast<size_t>(b) * W + pi) * SSD_NSTAT_VERIFY;
@@ -542,10 +622,10 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const VerifyArgs a) {
     // arrive draws.
     const int lo = c * span;
     const GlobalRange<E> rg{trow + lo, drow + lo, min(span, V - lo), aligned};
-    const double cta = global_weighted_pass(rg, rw, wsum);
     const size_t ci = (static_cast<size_t>(b) * W + pi) * NR + c;
+    const double cta = global_weighted_pass(rg, rw, wsum, a.blocks + ci * kBlocksPerRange, bpw);
+    __syncthreads();  // every warp's block sums are written before the fence below
     if (tid == 0) {
-      for (int w = 0; w < kWarps; ++w) a.wsums[ci * kWarps + w] = wsum[w];
       a.csum[ci] = cta;
       __threadfence();
       sh_last = atomicAdd(a.ticket + b * W + pi, 1) == NR - 1;
@@ -599,18 +679,23 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const VerifyArgs a) {
     }
     target_w = sh_target_w != 0;
     if (!target_w) {
-      // The owning range's per-warp sums were published by the CTA that
-      // summed it: scan only the warp run holding the target.
+      // The owning range's block sums were published by the CTA that summed
+      // it: locate the 32-vector block holding the target and scan just it.
       if (warp == 0) {
         const int owner = sh_owner;
         const size_t oi = (static_cast<size_t>(b) * W + pi) * NR + owner;
-        float ws8[kWarps];
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) ws8[w] = *reinterpret_cast<volatile float*>(a.wsums + oi * kWarps + w);
         const int lo = owner * span;
-        const GlobalRange<E> rg{trow + lo, drow + lo, min(span, V - lo), aligned};
-        double run_base;
-        const ScanHit h = draw_in_range(rg, rw, ws8, sh_local, &run_base, run_t, run_d);
+        const int rn = min(span, V - lo);
+        const GlobalRange<E> rg{trow + lo, drow + lo, rn, aligned};
+        double before = 0.0;
+        const int blk = locate_block(a.blocks + oi * kBlocksPerRange, kWarps * bpw, sh_local, &before);
+        ScanHit h{-1, NAN, 0.f};
+        if (blk >= 0) {
+          int w0, w1;
+          warp_range((rn + kVec - 1) / kVec, blk / bpw, w0, w1);
+          const int b0 = w0 + 32 * (blk % bpw);
+          h = warp_scan<kVec>(b0, min(b0 + 32, w1), sh_local - before, rg, rw);
+        }
         if (lane == 0) {
           if (h.elem < 0) {
             write_error(a, b);
@@ -618,7 +703,7 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const VerifyArgs a) {
           } else {
             if (a.stats) {
               float* st = a.stats + (static_cast<size_t>(b) * W + pos) * SSD_NSTAT_VERIFY;
-              const double e0 = sh_prefix + run_base + h.edge;
+              const double e0 = sh_prefix + before + h.edge;
               st[8] = static_cast<float>(ures - e0 / sh_total);
               st[9] = static_cast<float>((e0 + static_cast<double>(h.w)) / sh_total - ures);
             }
@@ -654,10 +739,19 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const VerifyArgs a) {
   // per-warp sums, then warp 0 scans the run holding the target.
   draw_n = min(geo.chunk, V - draw_lo);
   const GlobalRange<E> rg{trow + draw_lo, nullptr, draw_n, aligned};
-  global_weighted_pass(rg, tw, wsum);
+  const int bpw1 = ((draw_n + kVec - 1) / kVec + kWarps * 32 - 1) / (kWarps * 32);
+  global_weighted_pass(rg, tw, wsum, sh_blocks, bpw1);
   if (warp == 0) {
-    double run_base;
-    const ScanHit h = draw_in_range(rg, tw, wsum, sh_local, &run_base, run_t, run_d);
+    double before = 0.0;
+    const int blk = locate_block(sh_blocks, kWarps * bpw1, sh_local, &before);
+    ScanHit h{-1, NAN, 0.f};
+    if (blk >= 0) {
+      int w0, w1;
+      warp_range((draw_n + kVec - 1) / kVec, blk / bpw1, w0, w1);
+      const int b0 = w0 + 32 * (blk % bpw1);
+      h = warp_scan<kVec>(b0, min(b0 + 32, w1), sh_local - before, rg, tw);
+    }
+    const double run_base = before;
     if (lane == 0) {
       if (h.elem < 0) {
         write_error(a, b);
