@@ -120,11 +120,21 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const VerifyArgs a) {
 
   const ChunkGeometry& geo = a.geo;
   const int V = geo.V, NC = geo.nchunk, W = a.gmax + 1;
-  const int c = blockIdx.x, i = blockIdx.y, b = blockIdx.z;
+  // Dispatch order: chunk, then request, then position from the last to the
+  // first, so the rows of the low positions -- where the first rejection, and
+  // with it the sampling kernel's residual pass, usually falls -- are read
+  // last and are still in L2 when the sampling kernel needs them.
+  const int c = blockIdx.x, b = blockIdx.y, i = W - 1 - static_cast<int>(blockIdx.z);
   const int tid = threadIdx.x;
   // The first CTA of each request clears the request's arrival counters for
   // the sampling kernel (which only reads them after this grid completes).
-  if (i == 0 && c == 0 && tid < W) a.ticket[b * W + tid] = 0;
+  // Workspace writes wait for the previous kernel on the stream (the
+  // previous call's sampling kernel may still be reading the workspace:
+  // this grid may start early under programmatic dependent launch).
+  if (i == 0 && c == 0) {
+    griddep_wait();
+    if (tid < W) a.ticket[b * W + tid] = 0;
+  }
 
   const int g = a.gamma ? a.gamma[b] : a.gmax;
   const float T = a.temps ? a.temps[b] : a.temp_scalar;
@@ -179,6 +189,7 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const VerifyArgs a) {
     if (tid == 0) {
       ArgMax best{-INFINITY, -1};
       for (int w = 0; w < kWarps; ++w) best = better_arg(best, ArgMax{red_f[w], red_i[w]});
+      griddep_wait();
       rec[0] = make_float4(best.v, 0.f, -INFINITY, 0.f);
       rec[1] = make_float4(best.v, __int_as_float(best.i), __int_as_float(ok ? 0 : 1), 0.f);
     }
@@ -246,6 +257,7 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const VerifyArgs a) {
       s0 += red_f[2 * kWarps + w];
       s1 += red_f[3 * kWarps + w];
     }
+    griddep_wait();
     rec[0] = make_float4(mt, s0, has_draft ? md : -INFINITY, s1);
     float xt_tok = 0.f, xd_tok = 0.f;
     if (x >= lo && x < lo + sl.n) {
@@ -480,6 +492,7 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const VerifyArgs a)
   const int bpw = ((span + kVec - 1) / kVec + kWarps * 32 - 1) / (kWarps * 32);  // blocks per warp run
   const int c = blockIdx.x, pi = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  griddep_launch_dependents();  // the next call's streaming kernel may start
 
   const int g = a.gamma ? a.gamma[b] : a.gmax;
   const float T = a.temps ? a.temps[b] : a.temp_scalar;
@@ -547,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const VerifyArgs a)
 
   // Decisions: accept tests of positions 0..g-1 and the first rejection.
   if (warp == 0) {
-    const Draws dr = unit_draws(a.seed, a.req_base + b, min(lane, g));
+    const Draws dr = unit_draws(a.seed, a.req_base + b, min(lane, g));  // lane g: the bonus position
     bool acc = true;
     float ratio_acc = 1.f;
     if (lane < g) {
@@ -566,9 +579,11 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const VerifyArgs a)
     }
     const unsigned rej = __ballot_sync(0xFFFFFFFFu, lane < g && !acc);
     const int n = rej ? __ffs(rej) - 1 : g;
+    const int dp = a.debug ? pi : n;
+    const float ures_dp = __shfl_sync(0xFFFFFFFFu, dr.resample, min(dp, 31));
     if (lane == 0) {
       sh_n = n;
-      sh_ures = unit_draws(a.seed, a.req_base + b, a.debug ? pi : n).resample;
+      sh_ures = ures_dp;
     }
     if (a.stats && c == 0 && lane == pi) {
       float* st = a.stats + (static_cast<size_t>(b) * W + pi) * SSD_NSTAT_VERIFY;
@@ -815,8 +830,17 @@ cudaError_t launch_verify_t(const VerifyArgs& a, int smem_bytes, cudaStream_t st
   e = ensure_smem(reinterpret_cast<const void*>(&stream_kernel<E>), smem_bytes, &smem1);
   if (e != cudaSuccess) return e;
 
-  stream_kernel<E><<<dim3(a.geo.nchunk, a.gmax + 1, a.B), kThreads, smem_bytes, stream>>>(a);
-  e = cudaGetLastError();
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t c1 = {};
+  c1.gridDim = dim3(a.geo.nchunk, a.B, a.gmax + 1);
+  c1.blockDim = dim3(kThreads, 1, 1);
+  c1.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
+  c1.stream = stream;
+  c1.attrs = pdl;
+  c1.numAttrs = 1;
+  e = cudaLaunchKernelEx(&c1, stream_kernel<E>, a);
   if (e != cudaSuccess) return e;
   const int P = a.debug ? a.gmax + 1 : 1;
   const int span = a.geo.span * a.geo.chunk;
