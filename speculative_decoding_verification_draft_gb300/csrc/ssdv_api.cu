@@ -7,7 +7,9 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <mutex>
 #include <string>
+#include <unordered_map>
 
 #include "ssdv_device.cuh"
 #include "ssdv_internal.h"
@@ -53,13 +55,30 @@ WorkspaceLayout workspace_layout(int B, int gmax) {
   WorkspaceLayout L;
   const size_t units = static_cast<size_t>(B) * static_cast<size_t>(gmax + 1);
   L.status = 0;
-  L.ticket = 16;
+  L.half0 = 256;
+  L.ticket = 0;
   L.part = round_up(L.ticket + 4 * units, 256);
   L.csum = L.part + units * kMaxChunks * 2 * sizeof(float4);
   L.blocks = L.csum + units * kMaxChunks * sizeof(double);
-  L.total = round_up(L.blocks + units * kMaxChunks * 128 * sizeof(float), 256);
+  L.half_bytes = round_up(L.blocks + units * kMaxChunks * 128 * sizeof(float), 256);
+  L.total = L.half0 + 2 * L.half_bytes;
   return L;
 }
+
+namespace {
+
+// Consecutive calls on one workspace use alternate halves, so a call's
+// streaming kernel can overlap the previous call's sampling kernel without
+// touching its data.  The parity is kept per workspace address on the host.
+std::mutex g_parity_mutex;
+std::unordered_map<const void*, unsigned long long> g_parity;
+
+int next_half(const void* workspace) {
+  std::lock_guard<std::mutex> lock(g_parity_mutex);
+  return static_cast<int>(g_parity[workspace]++ & 1ull);
+}
+
+}  // namespace
 
 int max_dynamic_smem() {
   int dev = 0, v = 0;
@@ -174,10 +193,11 @@ ssd_status verify_common(const void* target, const void* draft, ssd_dtype dtype,
   a.out_tokens = out_tokens;
   a.n_accepted = n_accepted;
   a.status = reinterpret_cast<int32_t*>(ws + L.status);
-  a.ticket = reinterpret_cast<int32_t*>(ws + L.ticket);
-  a.part = reinterpret_cast<float4*>(ws + L.part);
-  a.csum = reinterpret_cast<double*>(ws + L.csum);
-  a.blocks = reinterpret_cast<float*>(ws + L.blocks);
+  uint8_t* half = ws + L.half0 + static_cast<size_t>(next_half(workspace)) * L.half_bytes;
+  a.ticket = reinterpret_cast<int32_t*>(half + L.ticket);
+  a.part = reinterpret_cast<float4*>(half + L.part);
+  a.csum = reinterpret_cast<double*>(half + L.csum);
+  a.blocks = reinterpret_cast<float*>(half + L.blocks);
   a.stats = stats;
   a.debug = stats ? 1 : 0;
   a.geo = geo;

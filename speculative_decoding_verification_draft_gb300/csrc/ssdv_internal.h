@@ -68,8 +68,11 @@ struct SaguaroArgs {
 };
 
 // Workspace layout (byte offsets), shared by the launchers and the API.
+// The status word sits at offset 0; two halves follow, used by alternate
+// calls on the same workspace (offsets of ticket .. blocks are relative to
+// the start of a half).
 struct WorkspaceLayout {
-  size_t status, ticket, part, csum, blocks, total;
+  size_t status, half0, half_bytes, ticket, part, csum, blocks, total;
 };
 WorkspaceLayout workspace_layout(int B, int gmax);
 

@@ -128,13 +128,13 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const VerifyArgs a) {
   const int tid = threadIdx.x;
   // The first CTA of each request clears the request's arrival counters for
   // the sampling kernel (which only reads them after this grid completes).
-  // Workspace writes wait for the previous kernel on the stream (the
-  // previous call's sampling kernel may still be reading the workspace:
-  // this grid may start early under programmatic dependent launch).
-  if (i == 0 && c == 0) {
-    griddep_wait();
-    if (tid < W) a.ticket[b * W + tid] = 0;
-  }
+  // This grid may start while the previous call's sampling kernel still runs
+  // (programmatic dependent launch); it writes the other half of the
+  // workspace, and one CTA waits for that kernel before it exits, so this
+  // call's sampling kernel -- which waits for this grid -- writes its outputs
+  // after the previous call's.
+  if (i == 0 && c == 0 && tid < W) a.ticket[b * W + tid] = 0;
+  if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) griddep_wait();
 
   const int g = a.gamma ? a.gamma[b] : a.gmax;
   const float T = a.temps ? a.temps[b] : a.temp_scalar;
@@ -189,7 +189,6 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const VerifyArgs a) {
     if (tid == 0) {
       ArgMax best{-INFINITY, -1};
       for (int w = 0; w < kWarps; ++w) best = better_arg(best, ArgMax{red_f[w], red_i[w]});
-      griddep_wait();
       rec[0] = make_float4(best.v, 0.f, -INFINITY, 0.f);
       rec[1] = make_float4(best.v, __int_as_float(best.i), __int_as_float(ok ? 0 : 1), 0.f);
     }
@@ -257,7 +256,6 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const VerifyArgs a) {
       s0 += red_f[2 * kWarps + w];
       s1 += red_f[3 * kWarps + w];
     }
-    griddep_wait();
     rec[0] = make_float4(mt, s0, has_draft ? md : -INFINITY, s1);
     float xt_tok = 0.f, xd_tok = 0.f;
     if (x >= lo && x < lo + sl.n) {
@@ -423,16 +421,19 @@ __device__ __forceinline__ double global_weighted_pass(const GlobalRange<E>& rg,
 }
 
 // Warp-wide: the 32-vector block of a range that holds target tl (relative
-// to the range start), from the range's block sums (nb of them, in index
-// order); returns the block (-1 if no positive weight) and the weight before
-// it.  A target past every boundary goes to the last positive block.
+// to the range start), from the range's block sums (nb <= 128 of them, in
+// index order; each lane reads four consecutive ones once); returns the block
+// (-1 if no positive weight) and the weight before it.  A target past every
+// boundary goes to the last positive block.
 __device__ __forceinline__ int locate_block(const float* blocks, int nb, double tl, double* before) {
   const int lane = threadIdx.x & 31;
-  const int per = (nb + 31) / 32;  // consecutive blocks per lane
+  float v[4];
   double mine = 0.0;
-  for (int k = 0; k < per; ++k) {
-    const int q = lane * per + k;
-    if (q < nb) mine += static_cast<double>(*reinterpret_cast<const volatile float*>(blocks + q));
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int q = lane * 4 + k;
+    v[k] = q < nb ? *reinterpret_cast<const volatile float*>(blocks + q) : 0.f;
+    mine += static_cast<double>(v[k]);
   }
   double incl = mine;
 #pragma unroll
@@ -447,15 +448,14 @@ __device__ __forceinline__ int locate_block(const float* blocks, int nb, double 
   double acc = __shfl_sync(0xFFFFFFFFu, incl - mine, L);
   int found = -1, last = -1;
   double found_before = 0.0, last_before = 0.0;
-  for (int k = 0; k < per; ++k) {  // every lane walks lane L's blocks
-    const int q = L * per + k;
-    if (q >= nb) break;
-    const double w = static_cast<double>(*reinterpret_cast<const volatile float*>(blocks + q));
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {  // lane L's four blocks, broadcast
+    const double w = static_cast<double>(__shfl_sync(0xFFFFFFFFu, v[k], L));
     if (w > 0.0) {
-      last = q;
+      last = L * 4 + k;
       last_before = acc;
       if (found < 0 && tl < acc + w) {
-        found = q;
+        found = L * 4 + k;
         found_before = acc;
       }
     }
@@ -467,6 +467,14 @@ __device__ __forceinline__ int locate_block(const float* blocks, int nb, double 
   }
   *before = found_before;
   return found;
+}
+
+// Arrival counter with acquire-release semantics: the releases of earlier
+// arrivals (their published sums) are visible to the last one.
+__device__ __forceinline__ int ticket_add(int32_t* p) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(p) : "memory");
+  return old;
 }
 
 // Block sums kept per sampling range: 32-vector blocks of at most 64 KB of
@@ -639,15 +647,13 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const VerifyArgs a)
     const GlobalRange<E> rg{trow + lo, drow + lo, min(span, V - lo), aligned};
     const size_t ci = (static_cast<size_t>(b) * W + pi) * NR + c;
     const double cta = global_weighted_pass(rg, rw, wsum, a.blocks + ci * kBlocksPerRange, bpw);
-    __syncthreads();  // every warp's block sums are written before the fence below
+    __syncthreads();  // every warp's block sums are written before the release below
     if (tid == 0) {
       a.csum[ci] = cta;
-      __threadfence();
-      sh_last = atomicAdd(a.ticket + b * W + pi, 1) == NR - 1;
+      sh_last = ticket_add(a.ticket + b * W + pi) == NR - 1;
     }
     __syncthreads();
     if (!sh_last) return;
-    __threadfence();
     if (warp == 0) {
       double w = 0.0;
       if (lane < NR) w = *reinterpret_cast<volatile double*>(a.csum + (static_cast<size_t>(b) * W + pi) * NR + lane);
