@@ -107,6 +107,38 @@ ssd_status ssd_verify(const void* target_logits, const void* draft_logits, ssd_d
                       uint64_t seed, int32_t* out_tokens, int32_t* n_accepted, void* workspace,
                       size_t ws_bytes, void* stream);
 
+/* Verification without a caller workspace.  This entry point has no
+ * counterpart in the method's description: it is a packaging variant of
+ * ssd_verify for callers that cannot hand over device memory -- a plain C
+ * caller with no caching allocator (a cudaMalloc/cudaFree per call would
+ * synchronise the device and cost more than the verification itself), or an
+ * engine that has reserved all free HBM up front for its KV-cache pool, so
+ * that one more allocation would fail.
+ *
+ * Same arguments, outputs, numerics and random draws as ssd_verify (the same
+ * kernels run); the scratch is a fixed file-scope device array of
+ * SSD_NOALLOC_SCRATCH_BYTES bytes inside the library, and the call allocates
+ * no device memory.  The batch must fit it:
+ * ssd_workspace_bytes(B, gamma) <= SSD_NOALLOC_SCRATCH_BYTES, i.e.
+ * B * (gamma + 1) <= 474 (B = 64 at gamma <= 6); a larger batch returns
+ * SSD_ERR_WORKSPACE before anything is launched.
+ *
+ * The first call on each device (with that device current) looks up the
+ * array's address with cudaGetSymbolAddress and zeroes the array with
+ * cudaMemsetAsync on `stream`; make that first call before any stream capture
+ * begins.  The kernels clear their own arrival counters on every call; the
+ * status word is never read back on this path (a request with bad input still
+ * gets n_accepted = -1 and out_tokens = -1).
+ *
+ * One array per device is shared by every caller: calls in sequence on one
+ * stream are safe, but calls that may overlap on the GPU (two streams, or two
+ * host threads with no ordering between their streams) race on the scratch
+ * and give wrong results.  Use ssd_verify with separate workspaces there. */
+#define SSD_NOALLOC_SCRATCH_BYTES (16u << 20)
+ssd_status ssd_verify_noalloc(const void* target_logits, const void* draft_logits, ssd_dtype dtype,
+                              const int32_t* draft_tokens, int B, int gamma, int V, float temperature,
+                              uint64_t seed, int32_t* out_tokens, int32_t* n_accepted, void* stream);
+
 /* Ragged verification: request b uses gamma[b] draft tokens (0..gamma_max;
  * a negative gamma[b] marks a padded request whose outputs are all -1) and
  * temperature[b] (0 = greedy).  Layouts are padded to gamma_max: target rows

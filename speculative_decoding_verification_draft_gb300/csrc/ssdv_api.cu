@@ -226,6 +226,40 @@ ssd_status verify_common(const void* target, const void* draft, ssd_dtype dtype,
 
 }  // namespace ssdv
 
+// Scratch of ssd_verify_noalloc: one fixed array per device, so that entry
+// point never allocates.  Its address is looked up once per device.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SSD_NOALLOC_SCRATCH_BYTES];
+
+namespace ssdv {
+namespace {
+
+constexpr int kNoallocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kNoallocMaxDevices] = {};
+
+// The current device's scratch address; on the first call for a device, look
+// it up (that device is current) and zero the array on `stream`.
+ssd_status noalloc_scratch(cudaStream_t stream, void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kNoallocMaxDevices) return fail(SSD_ERR_UNSUPPORTED, "device ordinal %d >= 64", dev);
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the no-alloc scratch");
+    e = cudaMemsetAsync(p, 0, SSD_NOALLOC_SCRATCH_BYTES, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "no-alloc scratch memset");
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return SSD_OK;
+}
+
+}  // namespace
+}  // namespace ssdv
+
 using namespace ssdv;
 
 extern "C" {
@@ -250,6 +284,28 @@ ssd_status ssd_verify(const void* target_logits, const void* draft_logits, ssd_d
     return fail(SSD_ERR_TEMPERATURE, "temperature %g is not 0 or in [1e-6, inf)", static_cast<double>(temperature));
   return verify_common(target_logits, draft_logits, dtype, draft_tokens, B, gamma, V, nullptr, nullptr, temperature,
                        temperature == 0.f, seed, out_tokens, n_accepted, workspace, ws_bytes, nullptr, stream);
+}
+
+ssd_status ssd_verify_noalloc(const void* target_logits, const void* draft_logits, ssd_dtype dtype,
+                              const int32_t* draft_tokens, int B, int gamma, int V, float temperature, uint64_t seed,
+                              int32_t* out_tokens, int32_t* n_accepted, void* stream) {
+  g_last_error.clear();
+  if (!temperature_valid(temperature))
+    return fail(SSD_ERR_TEMPERATURE, "temperature %g is not 0 or in [1e-6, inf)", static_cast<double>(temperature));
+  if (B < 1 || gamma < 0 || gamma > SSD_MAX_GAMMA)
+    return fail(SSD_ERR_SHAPE, "bad shape B=%d gamma=%d V=%d", B, gamma, V);
+  const size_t need = workspace_layout(B, gamma).total;
+  if (need > SSD_NOALLOC_SCRATCH_BYTES)
+    return fail(SSD_ERR_WORKSPACE,
+                "B=%d gamma=%d needs %zu bytes of scratch, above the fixed %u-byte array of ssd_verify_noalloc "
+                "(B*(gamma+1) <= 474); call ssd_verify with a workspace instead",
+                B, gamma, need, SSD_NOALLOC_SCRATCH_BYTES);
+  void* scratch = nullptr;
+  const ssd_status st = noalloc_scratch(static_cast<cudaStream_t>(stream), &scratch);
+  if (st != SSD_OK) return st;
+  return verify_common(target_logits, draft_logits, dtype, draft_tokens, B, gamma, V, nullptr, nullptr, temperature,
+                       temperature == 0.f, seed, out_tokens, n_accepted, scratch, SSD_NOALLOC_SCRATCH_BYTES, nullptr,
+                       stream);
 }
 
 ssd_status ssd_verify_ragged(const void* target_logits, const void* draft_logits, ssd_dtype dtype,

@@ -48,6 +48,7 @@ def _declare(lib):
     lib.ssd_workspace_init.argtypes = [P, SZ, P]
     lib.ssd_verify.argtypes = [P, P, I, P, I, I, I, F, U64, P, P, P, SZ, P]
     lib.ssd_verify_ragged.argtypes = [P, P, I, P, I, I, I, P, P, U64, P, P, P, SZ, P]
+    lib.ssd_verify_noalloc.argtypes = [P, P, I, P, I, I, I, F, U64, P, P, P]
     lib.ssd_saguaro_prespec.argtypes = [P, P, I, I, I, I, I, F, U64, P, P, P]
     lib.ssd_debug_rowstats.argtypes = [P, P, I, P, I, I, I, F, U64, P, P, P, P, SZ, P]
     lib.ssd_debug_saguaro_stats.argtypes = [P, P, I, I, I, I, I, F, U64, P, P, P, P]
@@ -57,8 +58,8 @@ def _declare(lib):
     lib.ssd_status_str.restype = ctypes.c_char_p
     lib.ssd_last_error.argtypes = []
     lib.ssd_last_error.restype = ctypes.c_char_p
-    for name in ("ssd_workspace_init", "ssd_verify", "ssd_verify_ragged", "ssd_saguaro_prespec",
-                 "ssd_debug_rowstats", "ssd_debug_saguaro_stats", "ssd_read_status",
+    for name in ("ssd_workspace_init", "ssd_verify", "ssd_verify_noalloc", "ssd_verify_ragged",
+                 "ssd_saguaro_prespec", "ssd_debug_rowstats", "ssd_debug_saguaro_stats", "ssd_read_status",
                  "ssd_debug_uniforms"):
         getattr(lib, name).restype = I
     return lib
@@ -165,6 +166,29 @@ def verify(target: torch.Tensor, draft: Optional[torch.Tensor], draft_tokens: to
                             int(seed) & ((1 << 64) - 1), _dev(out_tokens, "out_tokens", torch.int32),
                             _dev(n_accepted, "n_accepted", torch.int32), _dev(ws, "workspace"),
                             ws.numel(), _stream(stream)))
+    return out_tokens, n_accepted
+
+
+def verify_noalloc(target: torch.Tensor, draft: Optional[torch.Tensor], draft_tokens: torch.Tensor,
+                   temperature: float, seed: int, out_tokens: torch.Tensor, n_accepted: torch.Tensor,
+                   stream=None):
+    """ssd_verify_noalloc: ssd_verify on the library's fixed device scratch.
+
+    The caller passes the outputs (out_tokens [B, g+1], n_accepted [B] int32),
+    so neither this wrapper nor the library allocates device memory."""
+    B, W, V = target.shape
+    g = W - 1
+    dptr = _dev(draft, "draft_logits", target.dtype) if draft is not None else None
+    if draft is not None and tuple(draft.shape) != (B, g, V):
+        raise ValueError("draft_logits must be [B, gamma, V]")
+    if tuple(draft_tokens.shape) != (B, g):
+        raise ValueError("draft_tokens must be [B, gamma]")
+    if tuple(out_tokens.shape) != (B, W) or tuple(n_accepted.shape) != (B,):
+        raise ValueError("out_tokens must be [B, gamma+1] and n_accepted [B]")
+    _check(lib().ssd_verify_noalloc(_dev(target, "target_logits"), dptr, _dtype_code(target),
+                                    _dev(draft_tokens, "draft_tokens", torch.int32), B, g, V, float(temperature),
+                                    int(seed) & ((1 << 64) - 1), _dev(out_tokens, "out_tokens", torch.int32),
+                                    _dev(n_accepted, "n_accepted", torch.int32), _stream(stream)))
     return out_tokens, n_accepted
 
 
