@@ -107,11 +107,34 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
-def make_sets(device, n_sets):
+def replica_seed(rank: int, s: int) -> int:
+    """Input seed of rotating set s on rank r: every rank verifies its own
+    requests (rank 0 keeps the single-GPU seeds)."""
+    return 2 + 1000 * s + 1_000_003 * rank
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The slowest rank's time: one all-reduce (MAX) of a scalar, the only
+    collective of the benchmark."""
+    if world <= 1:
+        return float(x)
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, steps: int, total_ms: float) -> float:
+    """Rounds per second of the whole job: every rank verifies `steps` batches
+    in the slowest rank's time."""
+    return world * steps / (total_ms * 1e-3)
+
+
+def make_sets(device, n_sets, rank=0):
     from speculative_decoding_verification_draft_gb300 import workloads
     sets = []
     for s in range(n_sets):
-        sets.append(workloads.zipf_batch(B, GAMMA, V, temperature=TEMP, seed=2 + 1000 * s, device=device))
+        sets.append(workloads.zipf_batch(B, GAMMA, V, temperature=TEMP, seed=replica_seed(rank, s), device=device))
     return sets
 
 
@@ -131,7 +154,7 @@ def time_gpu(args, local_rank, world, rank):
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(dev)
     sh = stream.cuda_stream
-    sets = make_sets(dev, N_SETS)
+    sets = make_sets(dev, N_SETS, rank)
     alg_bytes = sets[0].algorithmic_bytes()
     out = [torch.empty(B, GAMMA + 1, dtype=torch.int32, device=dev) for _ in range(N_SETS)]
     nac = [torch.empty(B, dtype=torch.int32, device=dev) for _ in range(N_SETS)]
@@ -179,10 +202,7 @@ def time_gpu(args, local_rank, world, rank):
             lat.append((a, b_))
     stream.synchronize()
     launch_ms = [a.elapsed_time(b_) for a, b_ in lat]
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
 
     # acceptance diagnostics (the page's estimator: accepted per round / gamma)
     n_np = nac[0].cpu().numpy()
@@ -357,6 +377,22 @@ def reference_arm(args):
     print(json.dumps(line), flush=True)
 
 
+def measured_traffic():
+    """DRAM bytes per call from the committed ncu counters, or None once the
+    kernel sources differ from the ones the counters were taken on."""
+    import hashlib
+    tpath = os.path.join(ROOT, "profiles", "verify_traffic.json")
+    if not os.path.exists(tpath):
+        return None
+    with open(tpath) as f:
+        rec = json.load(f)
+    h = hashlib.sha256()
+    for p in rec.get("sources", []):
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return rec.get("bytes_per_launch") if h.hexdigest() == rec.get("sources_sha256") else None
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -392,12 +428,8 @@ def main():
     alg = r["alg_bytes"]
     # the verify pair of kernels per call, back to back: bytes per call / time per call
     achieved = alg / (step_ms * 1e-3) / 1e9
-    value = world * args.steps / (r["total_ms"] * 1e-3)
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "verify_traffic.json")
-    if os.path.exists(tpath):
-        with open(tpath) as f:
-            traffic = json.load(f).get("bytes_per_launch")
+    value = whole_job_rate(world, args.steps, r["total_ms"])
+    traffic = measured_traffic()
     line = {
         "metric": METRIC, "value": value, "unit": "rounds/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
