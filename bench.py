@@ -175,9 +175,10 @@ def time_gpu(args, local_rank, world, rank):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    # Back-to-back calls: each call's streaming kernel may overlap the previous
-    # call's sampling kernel (programmatic dependent launch), so only the two
-    # ends of the timed region carry events.
+    # Back-to-back calls: each kernel becomes resident while its predecessor
+    # finishes (programmatic dependent launch; it waits for that kernel's
+    # completion before touching memory), so only the two ends of the timed
+    # region carry events.
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):

@@ -74,8 +74,8 @@ typedef enum { SSD_BF16 = 0, SSD_F32 = 1 } ssd_dtype;
 
 /* Bytes of device workspace ssd_verify / ssd_verify_ragged / ssd_debug_rowstats
  * need for a batch of B requests with up to gamma_max draft tokens.  The
- * workspace holds a status word, per-chunk row statistics, per-chunk residual
- * sums and arrival counters (the counters are cleared by every call). */
+ * workspace holds a status word, arrival counters (cleared by every call),
+ * per-chunk row statistics and per-range residual sums. */
 size_t ssd_workspace_bytes(int B, int gamma_max);
 
 /* Zero a workspace (asynchronous memset on `stream`).  Zero a workspace once
@@ -120,7 +120,7 @@ ssd_status ssd_verify(const void* target_logits, const void* draft_logits, ssd_d
  * SSD_NOALLOC_SCRATCH_BYTES bytes inside the library, and the call allocates
  * no device memory.  The batch must fit it:
  * ssd_workspace_bytes(B, gamma) <= SSD_NOALLOC_SCRATCH_BYTES, i.e.
- * B * (gamma + 1) <= 474 (B = 64 at gamma <= 6); a larger batch returns
+ * B * (gamma + 1) <= 949 (B = 64 at gamma <= 13); a larger batch returns
  * SSD_ERR_WORKSPACE before anything is launched.
  *
  * The first call on each device (with that device current) looks up the

@@ -55,30 +55,13 @@ WorkspaceLayout workspace_layout(int B, int gmax) {
   WorkspaceLayout L;
   const size_t units = static_cast<size_t>(B) * static_cast<size_t>(gmax + 1);
   L.status = 0;
-  L.half0 = 256;
-  L.ticket = 0;
+  L.ticket = 256;
   L.part = round_up(L.ticket + 4 * units, 256);
   L.csum = L.part + units * kMaxChunks * 2 * sizeof(float4);
   L.blocks = L.csum + units * kMaxChunks * sizeof(double);
-  L.half_bytes = round_up(L.blocks + units * kMaxChunks * 128 * sizeof(float), 256);
-  L.total = L.half0 + 2 * L.half_bytes;
+  L.total = round_up(L.blocks + units * kMaxChunks * 128 * sizeof(float), 256);
   return L;
 }
-
-namespace {
-
-// Consecutive calls on one workspace use alternate halves, so a call's
-// streaming kernel can overlap the previous call's sampling kernel without
-// touching its data.  The parity is kept per workspace address on the host.
-std::mutex g_parity_mutex;
-std::unordered_map<const void*, unsigned long long> g_parity;
-
-int next_half(const void* workspace) {
-  std::lock_guard<std::mutex> lock(g_parity_mutex);
-  return static_cast<int>(g_parity[workspace]++ & 1ull);
-}
-
-}  // namespace
 
 int max_dynamic_smem() {
   int dev = 0, v = 0;
@@ -193,16 +176,16 @@ ssd_status verify_common(const void* target, const void* draft, ssd_dtype dtype,
   a.out_tokens = out_tokens;
   a.n_accepted = n_accepted;
   a.status = reinterpret_cast<int32_t*>(ws + L.status);
-  uint8_t* half = ws + L.half0 + static_cast<size_t>(next_half(workspace)) * L.half_bytes;
-  a.ticket = reinterpret_cast<int32_t*>(half + L.ticket);
-  a.part = reinterpret_cast<float4*>(half + L.part);
-  a.csum = reinterpret_cast<double*>(half + L.csum);
-  a.blocks = reinterpret_cast<float*>(half + L.blocks);
+  a.ticket = reinterpret_cast<int32_t*>(ws + L.ticket);
+  a.part = reinterpret_cast<float4*>(ws + L.part);
+  a.csum = reinterpret_cast<double*>(ws + L.csum);
+  a.blocks = reinterpret_cast<float*>(ws + L.blocks);
   a.stats = stats;
   a.debug = stats ? 1 : 0;
   a.geo = geo;
   // Launch in slices of at most 65535 requests (the grid's third dimension);
   // each slice keeps its requests' global indices for the Philox counters.
+  // Slices run one after another on the stream and share the workspace.
   const int W = gmax + 1;
   for (int b0 = 0; b0 < B; b0 += 65535) {
     VerifyArgs s = a;
@@ -298,7 +281,7 @@ ssd_status ssd_verify_noalloc(const void* target_logits, const void* draft_logit
   if (need > SSD_NOALLOC_SCRATCH_BYTES)
     return fail(SSD_ERR_WORKSPACE,
                 "B=%d gamma=%d needs %zu bytes of scratch, above the fixed %u-byte array of ssd_verify_noalloc "
-                "(B*(gamma+1) <= 474); call ssd_verify with a workspace instead",
+                "(B*(gamma+1) <= 949); call ssd_verify with a workspace instead",
                 B, gamma, need, SSD_NOALLOC_SCRATCH_BYTES);
   void* scratch = nullptr;
   const ssd_status st = noalloc_scratch(static_cast<cudaStream_t>(stream), &scratch);

@@ -67,12 +67,11 @@ struct SaguaroArgs {
   Geometry geo;
 };
 
-// Workspace layout (byte offsets), shared by the launchers and the API.
-// The status word sits at offset 0; two halves follow, used by alternate
-// calls on the same workspace (offsets of ticket .. blocks are relative to
-// the start of a half).
+// Workspace layout (byte offsets), shared by the launchers and the API: the
+// status word, then the arrival counters (cleared by every call), chunk
+// records, range sums and block sums of the call's shape.
 struct WorkspaceLayout {
-  size_t status, half0, half_bytes, ticket, part, csum, blocks, total;
+  size_t status, ticket, part, csum, blocks, total;
 };
 WorkspaceLayout workspace_layout(int B, int gmax);
 
@@ -81,8 +80,8 @@ ssd_status choose_chunks(int V, int esize, bool aligned, ChunkGeometry* geo, int
 // Launch configuration for one call; returns SSD_OK or an error.
 ssd_status choose_geometry(int V, int esize, bool aligned, bool two_rows, Geometry* geo, int* smem_bytes);
 
-// Streaming statistics kernel followed (programmatic dependent launch) by the
-// decision / sampling kernel.
+// Streaming statistics kernel followed by the decision / sampling kernel (both
+// with programmatic dependent launch; each waits for its predecessor).
 cudaError_t launch_verify(const VerifyArgs& a, int esize, int smem_bytes, cudaStream_t stream);
 cudaError_t launch_saguaro(const SaguaroArgs& a, int esize, int smem_bytes, cudaStream_t stream);
 

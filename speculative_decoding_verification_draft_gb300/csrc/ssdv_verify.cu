@@ -16,9 +16,17 @@
 //     argmax of a greedy row, and the draft token's two logits when the token
 //     falls in the chunk).
 //     Every logit is read from HBM exactly once, by short-lived CTAs.
-//  2. sample_kernel (programmatic dependent launch): the CTAs of a request
-//     combine the records, take every accept decision and find the first
-//     rejection n.  Only position n needs a draw: the bonus draw locates its
+//
+// Both kernels are launched with programmatic dependent launch.  Every CTA of
+// either kernel waits (griddepcontrol.wait) for the previous kernel on the
+// stream to complete before it reads data that kernel may have produced or
+// writes the workspace, and only then lets its own dependents launch; so a
+// call never overlaps the work of the previous one, and one workspace region
+// serves every call.
+//  2. sample_kernel (programmatic dependent launch: resident while the
+//     streaming kernel finishes, it reads the records once that kernel has
+//     completed): the CTAs of a request combine the records, take every accept
+//     decision and find the first rejection n.  Only position n needs a draw: the bonus draw locates its
 //     chunk from the records and scans that chunk; a residual draw runs one
 //     range-parallel pass over rows n (mostly L2-resident, read straight from
 //     global memory), and the last range to arrive scans the one warp run
@@ -116,7 +124,8 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const VerifyArgs a) {
   __shared__ float red_f[5 * kWarps];
   __shared__ int red_i[2 * kWarps];
   __shared__ int sh_ok;
-  griddep_launch_dependents();
+  griddep_wait();               // the previous kernel on the stream has completed
+  griddep_launch_dependents();  // the sampling kernel may become resident
 
   const ChunkGeometry& geo = a.geo;
   const int V = geo.V, NC = geo.nchunk, W = a.gmax + 1;
@@ -127,14 +136,8 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const VerifyArgs a) {
   const int c = blockIdx.x, b = blockIdx.y, i = W - 1 - static_cast<int>(blockIdx.z);
   const int tid = threadIdx.x;
   // The first CTA of each request clears the request's arrival counters for
-  // the sampling kernel (which only reads them after this grid completes).
-  // This grid may start while the previous call's sampling kernel still runs
-  // (programmatic dependent launch); it writes the other half of the
-  // workspace, and one CTA waits for that kernel before it exits, so this
-  // call's sampling kernel -- which waits for this grid -- writes its outputs
-  // after the previous call's.
+  // the sampling kernel (which reads them only after this grid completes).
   if (i == 0 && c == 0 && tid < W) a.ticket[b * W + tid] = 0;
-  if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) griddep_wait();
 
   const int g = a.gamma ? a.gamma[b] : a.gmax;
   const float T = a.temps ? a.temps[b] : a.temp_scalar;
@@ -500,7 +503,6 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const VerifyArgs a)
   const int bpw = ((span + kVec - 1) / kVec + kWarps * 32 - 1) / (kWarps * 32);  // blocks per warp run
   const int c = blockIdx.x, pi = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  griddep_launch_dependents();  // the next call's streaming kernel may start
 
   const int g = a.gamma ? a.gamma[b] : a.gmax;
   const float T = a.temps ? a.temps[b] : a.temp_scalar;
@@ -518,7 +520,9 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const VerifyArgs a)
   const E* tb = static_cast<const E*>(a.target);
   const E* db = static_cast<const E*>(a.draft);
 
-  // Inputs only (overlaps the streaming kernel's tail): the draft tokens.
+  // Inputs only (overlaps the streaming kernel's tail; the kernel that wrote
+  // them completed before any streaming CTA let this grid launch): the draft
+  // tokens.
   if (warp == 0) {
     bool bad = false;
     if (lane < g) {
@@ -537,7 +541,8 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const VerifyArgs a)
     }
     return;
   }
-  griddep_wait();  // the streaming kernel's records are complete and visible
+  griddep_wait();               // the streaming kernel's records are complete and visible
+  griddep_launch_dependents();  // the next kernel may become resident (it waits for this grid)
 
   // Row statistics of every position of the request, combined from the chunk
   // records (the same butterfly in every CTA: identical results), and the two
