@@ -7,6 +7,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 #include <string>
 #include <unordered_map>
@@ -121,13 +122,23 @@ ssd_status choose_chunks(int V, int esize, bool aligned, ChunkGeometry* geo, int
   geo->nchunk = (V + chunk - 1) / chunk;
   geo->row_smem = row_smem;
   geo->bulk = aligned ? 1 : 0;
-  // the sampling kernel's ranges: at most 64 KB of a row (so a warp's run of a
-  // range fits its staging buffer), SSDV_SPAN chunks when set
-  int span = (64 * 1024) / (chunk * esize);
-  span = env_int("SSDV_SPAN", span);
-  if (span < 1) span = 1;
-  while (span > 1 && static_cast<long long>(span) * chunk * esize > 64 * 1024) --span;
-  geo->span = span;
+  // residual ranges of the sampling kernel: about 16 KB of a row
+  // (SSDV_RANGE_BYTES overrides), a whole number of 32-vector blocks, at most
+  // kMaxChunks ranges and 128 blocks per range
+  const int kvec = 16 / esize;
+  const int blk = 32 * kvec;
+  int range = static_cast<int>(round_up(static_cast<size_t>(env_int("SSDV_RANGE_BYTES", 16 * 1024) / esize), blk));
+  if (range < blk) range = blk;
+  if ((V + range - 1) / range > kMaxChunks) range = static_cast<int>(round_up((static_cast<size_t>(V) + kMaxChunks - 1) / kMaxChunks, blk));
+  if (range > 128 * blk) return fail(SSD_ERR_UNSUPPORTED, "V=%d: a residual range exceeds 128 blocks", V);
+  geo->range = range;
+  geo->nrange = (V + range - 1) / range;
+  const size_t s2 = round_up(std::max({static_cast<size_t>(2) * range * esize,
+                                       round_up(static_cast<size_t>(chunk), kvec) * esize,
+                                       static_cast<size_t>(geo->nrange) * (range / blk) * sizeof(float)}), 128);
+  if (s2 > static_cast<size_t>(max_smem))
+    return fail(SSD_ERR_UNSUPPORTED, "V=%d: a residual range does not fit in shared memory", V);
+  geo->smem2 = static_cast<int>(s2);
   *smem_bytes = 2 * row_smem;
   return SSD_OK;
 }
@@ -183,14 +194,20 @@ ssd_status verify_common(const void* target, const void* draft, ssd_dtype dtype,
   a.stats = stats;
   a.debug = stats ? 1 : 0;
   a.geo = geo;
-  // Launch in slices of at most 65535 requests (the grid's third dimension);
-  // each slice keeps its requests' global indices for the Philox counters.
-  // Slices run one after another on the stream and share the workspace.
+  // Launch in segments of at most 65535 requests (the grid's third
+  // dimension; SSDV_SEGMENT sets a smaller size).  Each segment keeps its
+  // requests' global indices for the Philox counters and its own rows of the
+  // workspace; a segment's sampling kernel may run while the next segment
+  // streams.
+  int seg = env_int("SSDV_SEGMENT", 65535);
+  seg = std::max(1, std::min(seg, 65535));
+  const int NRg = geo.nrange;
   const int W = gmax + 1;
-  for (int b0 = 0; b0 < B; b0 += 65535) {
+  for (int b0 = 0; b0 < B; b0 += seg) {
     VerifyArgs s = a;
-    s.B = B - b0 < 65535 ? B - b0 : 65535;
+    s.B = B - b0 < seg ? B - b0 : seg;
     s.req_base = b0;
+    s.first = b0 == 0 ? 1 : 0;
     s.target = static_cast<const uint8_t*>(target) + static_cast<size_t>(b0) * W * V * es;
     if (draft) s.draft = static_cast<const uint8_t*>(draft) + static_cast<size_t>(b0) * gmax * V * es;
     if (draft_tokens) s.draft_tokens = draft_tokens + static_cast<size_t>(b0) * gmax;
@@ -199,6 +216,11 @@ ssd_status verify_common(const void* target, const void* draft, ssd_dtype dtype,
     s.out_tokens = out_tokens + static_cast<size_t>(b0) * W;
     s.n_accepted = n_accepted + b0;
     if (stats) s.stats = stats + static_cast<size_t>(b0) * W * SSD_NSTAT_VERIFY;
+    const size_t u0 = static_cast<size_t>(b0) * W;  // the segment's first (request, position) unit
+    s.ticket = a.ticket + u0;
+    s.part = a.part + u0 * geo.nchunk * 2;
+    s.csum = a.csum + u0 * NRg;
+    s.blocks = a.blocks + u0 * NRg * 128;
     const cudaError_t e = launch_verify(s, es, smem, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "verify launch");
   }

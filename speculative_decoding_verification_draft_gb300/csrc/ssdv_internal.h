@@ -20,16 +20,18 @@ struct Geometry {
   int bulk;         // 1: rows 16-byte aligned, staged with bulk async copies
 };
 
-// How verification splits each row into chunks: the streaming kernel runs one
-// CTA per (request, position, chunk), the sampling kernel one CTA per
-// (request, chunk) (per (request, position, chunk) in the debug mode).
+// How verification splits each row: the streaming kernel runs one CTA per
+// (request, position, chunk), the sampling kernel one CTA per (request,
+// residual range) (per (request, position, range) in the debug mode).
 struct ChunkGeometry {
   int V;         // vocabulary size
   int chunk;     // elements per chunk, a multiple of 8
   int nchunk;    // chunks per row, 1..kMaxChunks
   int row_smem;  // shared-memory bytes per staged row chunk (a multiple of 128)
   int bulk;      // 1: rows 16-byte aligned, staged with bulk async copies
-  int span;      // streaming chunks per range of the sampling kernel
+  int range;     // elements per residual range, a whole number of 32-vector blocks
+  int nrange;    // residual ranges per row, 1..kMaxChunks
+  int smem2;     // dynamic shared memory of a sampling CTA (bytes)
 };
 constexpr int kMaxChunks = 32;
 
@@ -46,12 +48,14 @@ struct VerifyArgs {
   int32_t* out_tokens;         // [B, gmax+1]
   int32_t* n_accepted;         // [B]
   float4* part;                // workspace [B, gmax+1, nchunk, 2]: per-chunk row statistics
-  double* csum;                // workspace [B, gmax+1, nchunk]: per-chunk residual weight sums
-  float* blocks;               // workspace [B, gmax+1, nchunk, 128]: their 32-vector block sums
+  double* csum;                // workspace [B, gmax+1, nrange]: per-range residual weight sums
+  float* blocks;               // workspace [B, gmax+1, nrange, 128]: their 32-vector block sums
   int32_t* ticket;             // workspace [B, gmax+1]: residual chunks arrived
   int32_t* status;             // workspace [1]: device error bits
   float* stats;                // [B, gmax+1, SSD_NSTAT_VERIFY] or null (debug)
   int debug;                   // 1: decide and report every position (statistics)
+  int first;                   // 1: the call's first segment (every streaming CTA waits for the
+                               // previous kernel); 0: a later one (only its first CTA waits)
   ChunkGeometry geo;
 };
 

@@ -16,21 +16,25 @@
 //     argmax of a greedy row, and the draft token's two logits when the token
 //     falls in the chunk).
 //     Every logit is read from HBM exactly once, by short-lived CTAs.
+//  2. sample_kernel: one small CTA per (request, residual range).  Each
+//     combines the request's records, takes every accept decision and finds
+//     the first rejection n.  For a residual draw every CTA stages its range
+//     of rows n (L2-resident: the streaming kernel reads the low positions
+//     last) with one bulk copy per row and publishes the range's weight sum
+//     and 32-vector block sums; the last range to arrive loads all of them at
+//     once, locates the block holding u * S and scans just that block.  A
+//     bonus draw (n = gamma) locates its streaming chunk from the records,
+//     stages that chunk and scans it.
 //
-// Both kernels are launched with programmatic dependent launch.  Every CTA of
-// either kernel waits (griddepcontrol.wait) for the previous kernel on the
-// stream to complete before it reads data that kernel may have produced or
-// writes the workspace, and only then lets its own dependents launch; so a
-// call never overlaps the work of the previous one, and one workspace region
-// serves every call.
-//  2. sample_kernel (programmatic dependent launch: resident while the
-//     streaming kernel finishes, it reads the records once that kernel has
-//     completed): the CTAs of a request combine the records, take every accept
-//     decision and find the first rejection n.  Only position n needs a draw: the bonus draw locates its
-//     chunk from the records and scans that chunk; a residual draw runs one
-//     range-parallel pass over rows n (mostly L2-resident, read straight from
-//     global memory), and the last range to arrive scans the one warp run
-//     that holds the target.
+// A call runs as segments of requests, each a streaming + sampling pair, all
+// launched with programmatic dependent launch.  The first streaming kernel's
+// CTAs wait (griddepcontrol.wait) for the previous kernel on the stream before
+// reading anything; every sampling CTA waits for its streaming kernel before
+// reading the records.  Each kernel lets its dependents launch only after its
+// own wait, so a later segment's streaming kernel launches after the first
+// segment's CTAs saw the call's inputs complete, and may stream while the
+// previous segment's sampling kernel runs: the segments use disjoint
+// workspace rows.  A call never overlaps the work of the previous call.
 #include "ssdv_device.cuh"
 
 namespace ssdv {
@@ -51,11 +55,17 @@ struct ResidualW {
   float c, mct, mcd, kr;
   __device__ __forceinline__ void operator()(const float (&xt)[Elem<E>::kVec], const float (&xd)[Elem<E>::kVec],
                                              float (&w)[Elem<E>::kVec]) const {
+    constexpr int kVec = Elem<E>::kVec;
+    const F2 c2 = f2_make(c, c), nt = f2_make(-mct, -mct), nd = f2_make(-mcd, -mcd), nk = f2_make(-kr, -kr);
 #pragma unroll
-    for (int e = 0; e < Elem<E>::kVec; ++e) {
-      const float et = fast_exp2(fmaf(xt[e], c, -mct));
-      const float ed = fast_exp2(fmaf(xd[e], c, -mcd));
-      w[e] = fmaxf(fmaf(-kr, ed, et), 0.f);
+    for (int e = 0; e < kVec; e += 2) {
+      const F2 et = f2_exp2(f2_fma(f2_make(xt[e], xt[e + 1]), c2, nt));
+      const F2 ad = f2_fma(f2_make(xd[e], xd[e + 1]), c2, nd);
+      const F2 ed = f2_exp2(ad);
+      float w0, w1;
+      f2_split(f2_fma(nk, ed, et), w0, w1);
+      w[e] = fmaxf(w0, 0.f);
+      w[e + 1] = fmaxf(w1, 0.f);
     }
   }
 };
@@ -124,7 +134,13 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const VerifyArgs a) {
   __shared__ float red_f[5 * kWarps];
   __shared__ int red_i[2 * kWarps];
   __shared__ int sh_ok;
-  griddep_wait();               // the previous kernel on the stream has completed
+  // The first segment of a call waits for the previous kernel on the stream
+  // before it reads or writes anything.  A later segment reads logits that
+  // were complete before the first segment's CTAs passed that wait (its
+  // launch follows them through the chain of launches) and writes workspace
+  // rows of its own requests, so only its first CTA waits -- for the previous
+  // segment's sampling kernel -- which orders the completions of the chain.
+  if (a.first || (blockIdx.x | blockIdx.y | blockIdx.z) == 0) griddep_wait();
   griddep_launch_dependents();  // the sampling kernel may become resident
 
   const ChunkGeometry& geo = a.geo;
@@ -297,7 +313,7 @@ __device__ __forceinline__ void locate_target_chunk(const VerifyArgs& a, int uni
   const int lane = threadIdx.x & 31, NC = a.geo.nchunk;
   double w = 0.0;
   if (lane < NC) {
-    const float4 r = a.part[(static_cast<size_t>(unit) * NC + lane) * 2];
+    const float4 r = __ldcg(a.part + (static_cast<size_t>(unit) * NC + lane) * 2);
     w = (r.x == -INFINITY) ? 0.0 : static_cast<double>(r.y * rescale(r.x, M, cc));
   }
   double incl = w;
@@ -344,84 +360,6 @@ struct GlobalRange {
     }
   }
 };
-
-// Weighted pass over a global row range: each warp owns a contiguous run of
-// vectors (lanes interleaved: coalesced); loads are issued four vectors at a
-// time before any is used.  Per-warp sums go to wsum[] (shared) and, when
-// `blocks` is given, the sum of every 32-vector block of each warp's run to
-// blocks[warp * bpw + j] (global; blocks in index order).  Returns the CTA
-// sum (fp64 over warps) in thread 0.
-template <typename E, typename WFun>
-__device__ __forceinline__ double global_weighted_pass(const GlobalRange<E>& rg, const WFun& wfun, float* wsum,
-                                                       float* blocks, int bpw) {
-  constexpr int kVec = Elem<E>::kVec;
-  constexpr int kBatch = 4;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nvec = (rg.n + kVec - 1) / kVec;
-  int v0, v1;
-  warp_range(nvec, warp, v0, v1);
-  float acc = 0.f;
-  int j = 0;
-  if (rg.aligned) {
-    const uint4* gt = reinterpret_cast<const uint4*>(rg.gt);
-    const uint4* gd = reinterpret_cast<const uint4*>(rg.gd);
-    for (int vb = v0 + lane; vb - lane < v1; vb += 32 * kBatch) {
-      uint4 rt[kBatch], rd[kBatch];
-#pragma unroll
-      for (int k = 0; k < kBatch; ++k) {
-        const int v = vb + 32 * k;
-        if (v < v1) {
-          rt[k] = __ldg(gt + v);
-          if (rg.gd) rd[k] = __ldg(gd + v);
-        }
-      }
-#pragma unroll
-      for (int k = 0; k < kBatch; ++k) {
-        if (vb - lane + 32 * k >= v1) break;  // warp-uniform
-        float vs = 0.f;
-        if (vb + 32 * k < v1) {
-          float xt[kVec], xd[kVec], w[kVec];
-          Elem<E>::unpack(rt[k], xt);
-          if (rg.gd) Elem<E>::unpack(rd[k], xd);
-          wfun(xt, xd, w);
-          vs = pair_sum(w);
-        }
-        acc += vs;
-        if (blocks) {
-          const float bsum = warp_sum(vs);
-          if (lane == 0) blocks[warp * bpw + j] = bsum;
-        }
-        ++j;
-      }
-    }
-  } else {
-    for (int vb = v0; vb < v1; vb += 32) {
-      const int v = vb + lane;
-      float vs = 0.f;
-      if (v < v1) {
-        float xt[kVec], xd[kVec], w[kVec];
-        rg(v, xt, xd);
-        wfun(xt, xd, w);
-        vs = pair_sum(w);
-      }
-      acc += vs;
-      if (blocks) {
-        const float bsum = warp_sum(vs);
-        if (lane == 0) blocks[warp * bpw + j] = bsum;
-      }
-      ++j;
-    }
-  }
-  if (blocks && lane == 0)
-    for (; j < bpw; ++j) blocks[warp * bpw + j] = 0.f;
-  acc = warp_sum(acc);
-  if (lane == 0) wsum[warp] = acc;
-  __syncthreads();
-  double cta = 0.0;
-  if (threadIdx.x == 0)
-    for (int w = 0; w < kWarps; ++w) cta += static_cast<double>(wsum[w]);
-  return cta;
-}
 
 // Warp-wide: the 32-vector block of a range that holds target tl (relative
 // to the range start), from the range's block sums (nb <= 128 of them, in
@@ -480,27 +418,120 @@ __device__ __forceinline__ int ticket_add(int32_t* p) {
   return old;
 }
 
-// Block sums kept per sampling range: 32-vector blocks of at most 64 KB of
-// a row (4096 bf16 vectors / 8 warps / 32 = 16 per warp).
-constexpr int kBlocksPerRange = 128;
+// ---------------------------------------------------------------------------
+// Kernel 2: decisions and the draw.  One CTA of kT2 threads per (residual
+// range r, position slot, request); a residual range is `range` elements of a
+// row (a whole number of 32-vector blocks).
+// ---------------------------------------------------------------------------
+constexpr int kT2 = 128;  // threads of a sampling CTA
+constexpr int kW2 = kT2 / 32;
+constexpr int kBlocksPerRange = 128;  // 32-vector blocks of a residual range, at most
+
+// Rows [0, n) of gt (and gd) into shared memory: one bulk copy per row
+// completing on `bar` (fresh, phase 0; bounded wait), or plain loads padded
+// with -inf to whole vectors when the rows are not 16-byte aligned.  All
+// threads; returns false when the bounded wait ran out.
+template <typename E>
+__device__ __forceinline__ bool stage_rows(const E* gt, const E* gd, int n, bool bulk, E* st, E* sd, uint64_t* bar,
+                                           int* sh_ok) {
+  constexpr int kVec = Elem<E>::kVec;
+  if (bulk) {
+    if (threadIdx.x == 0) {
+      mbar_init(bar, 1);
+      fence_mbar_init();
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      const uint32_t bytes = static_cast<uint32_t>(n) * sizeof(E);
+      mbar_arrive_expect_tx(bar, gd ? 2 * bytes : bytes);
+      const uint64_t pol = l2_policy_evict_normal();
+      bulk_copy_g2s(st, gt, bytes, bar, pol);
+      if (gd) bulk_copy_g2s(sd, gd, bytes, bar, pol);
+      *sh_ok = mbar_wait_bounded(bar, 0) ? 1 : 0;
+    }
+    __syncthreads();
+    return *sh_ok != 0;
+  }
+  const int padded = (n + kVec - 1) / kVec * kVec;
+  for (int e = threadIdx.x; e < padded; e += kT2) {
+    st[e] = e < n ? gt[e] : Elem<E>::neg_inf();
+    if (gd) sd[e] = e < n ? gd[e] : Elem<E>::neg_inf();
+  }
+  __syncthreads();
+  return true;
+}
+
+// Vector v of rows staged in shared memory (sd may be null: target weights).
+template <typename E>
+struct SmemRows {
+  const E* st;
+  const E* sd;
+  __device__ __forceinline__ void operator()(int v, float (&xt)[Elem<E>::kVec], float (&xd)[Elem<E>::kVec]) const {
+    Elem<E>::unpack(reinterpret_cast<const uint4*>(st)[v], xt);
+    if (sd) Elem<E>::unpack(reinterpret_cast<const uint4*>(sd)[v], xd);
+  }
+};
+
+// The weight sum of every 32-vector block of nvec staged vectors (lanes
+// summed by a fixed butterfly) into blk[] (shared) and, when given, gblk[]
+// (global); returns their sum in block order (fp64) in thread 0.
+template <typename E, typename WFun>
+__device__ double block_sums(const SmemRows<E>& rows, int nvec, const WFun& wfun, float* blk, float* gblk) {
+  constexpr int kVec = Elem<E>::kVec;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nb = (nvec + 31) / 32;
+  for (int j = warp; j < nb; j += kW2) {
+    const int v = j * 32 + lane;
+    float s = 0.f;
+    if (v < nvec) {
+      float xt[kVec], xd[kVec], w[kVec];
+      rows(v, xt, xd);
+      wfun(xt, xd, w);
+      s = pair_sum(w);
+    }
+    s = warp_sum(s);
+    if (lane == 0) {
+      blk[j] = s;
+      if (gblk) gblk[j] = s;
+    }
+  }
+  __syncthreads();
+  double tot = 0.0;
+  if (threadIdx.x == 0)
+    for (int j = 0; j < nb; ++j) tot += static_cast<double>(blk[j]);
+  return tot;
+}
+
+// Warp 0: the token at target tl (relative to the staged or global rows'
+// start) from their block sums blk[0..nb): the 32-vector block, then a scan of
+// just that block.  Returns the hit (element relative to the rows' start, -1
+// if none) and the weight before its block in *before.
+template <typename E, typename Load, typename WFun>
+__device__ __forceinline__ ScanHit locate_in_rows(const float* blk, int nb, int nvec, double tl, const Load& load,
+                                                  const WFun& wfun, double* before) {
+  constexpr int kVec = Elem<E>::kVec;
+  *before = 0.0;
+  const int j = locate_block(blk, nb, tl, before);
+  ScanHit h{-1, NAN, 0.f};
+  if (j >= 0) h = warp_scan<kVec>(j * 32, min(j * 32 + 32, nvec), tl - *before, load, wfun);
+  return h;
+}
 
 template <typename E>
-__global__ void __launch_bounds__(kThreads, 4) sample_kernel(const VerifyArgs a) {
+__global__ void __launch_bounds__(kT2) sample_kernel(const VerifyArgs a) {
+  extern __shared__ __align__(128) uint8_t dyn_smem[];
+  __shared__ __align__(8) uint64_t bars[2];
   __shared__ UnitStat ust[SSD_MAX_GAMMA + 1];
-  __shared__ float sh_blocks[kBlocksPerRange];
+  __shared__ float sh_blk[kBlocksPerRange];
   __shared__ int tok_x[SSD_MAX_GAMMA];
   __shared__ float tok_t[SSD_MAX_GAMMA], tok_d[SSD_MAX_GAMMA];
-  __shared__ float wsum[kWarps];
-  __shared__ int sh_n, sh_bad, sh_last, sh_owner, sh_target_w;
+  __shared__ int sh_n, sh_bad, sh_last, sh_owner, sh_target_w, sh_ok;
   __shared__ float sh_ures;
   __shared__ double sh_local, sh_prefix, sh_total;
 
+  constexpr int kVec = Elem<E>::kVec;
   const ChunkGeometry& geo = a.geo;
   const int V = geo.V, NC = geo.nchunk, W = a.gmax + 1;
-  const int span = geo.span * geo.chunk;  // elements per sampling range
-  const int NR = (V + span - 1) / span;   // sampling ranges per row
-  constexpr int kVec = Elem<E>::kVec;
-  const int bpw = ((span + kVec - 1) / kVec + kWarps * 32 - 1) / (kWarps * 32);  // blocks per warp run
+  const int R = geo.range, NR = geo.nrange;
+  const int nbr = R / (32 * kVec);  // blocks of a full range
   const int c = blockIdx.x, pi = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -550,17 +581,17 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const VerifyArgs a)
   const float cc = greedy ? 1.f : kLog2e / T;
   if (!greedy && warp == 0 && lane < g) {
     const int cx = tok_x[lane] / geo.chunk;
-    const float4 r1 = a.part[((static_cast<size_t>(b) * W + lane) * NC + cx) * 2 + 1];
+    const float4 r1 = __ldcg(a.part + ((static_cast<size_t>(b) * W + lane) * NC + cx) * 2 + 1);
     tok_d[lane] = r1.x;
     tok_t[lane] = r1.w;
   }
-  for (int u = warp; u <= g; u += kWarps) {
+  for (int u = warp; u <= g; u += kW2) {
     MaxSum t{-INFINITY, 0.f}, d{-INFINITY, 0.f};
     ArgMax am{-INFINITY, -1};
     int err = 0;
     if (lane < NC) {
       const float4* rec = a.part + ((static_cast<size_t>(b) * W + u) * NC + lane) * 2;
-      const float4 r0 = rec[0], r1 = rec[1];
+      const float4 r0 = __ldcg(rec), r1 = __ldcg(rec + 1);
       t = MaxSum{r0.x, r0.y};
       d = MaxSum{r0.z, r0.w};
       if (greedy) am = ArgMax{r1.x, __float_as_int(r1.y)};
@@ -639,29 +670,39 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const VerifyArgs a)
   const double ures = static_cast<double>(sh_ures);
   const E* trow = tb + (static_cast<size_t>(b) * W + pos) * V;
   const E* drow = db + (static_cast<size_t>(b) * a.gmax + pos) * V;
-  const bool aligned = geo.bulk != 0;
+  const bool bulk = geo.bulk != 0;
   const ResidualW<E> rw{cc, mct, pos < g ? scaled_max(s.dm, cc) : 0.f, pos < g ? s.ts / s.ds : 0.f};
   const TargetW<E> tw{cc, mct};
+  E* s_t = reinterpret_cast<E*>(dyn_smem);
+  E* s_d = reinterpret_cast<E*>(dyn_smem + static_cast<size_t>(R) * sizeof(E));
 
-  int draw_lo = 0, draw_n = 0;  // the range searched for the draw
-  bool target_w = false;
+  int chunk_draw = -1;  // streaming chunk of row pos to draw from with target weights
   if (pos < g) {
-    // Residual pass over this CTA's range of rows pos; the last range to
-    // arrive draws.
-    const int lo = c * span;
-    const GlobalRange<E> rg{trow + lo, drow + lo, min(span, V - lo), aligned};
-    const size_t ci = (static_cast<size_t>(b) * W + pi) * NR + c;
-    const double cta = global_weighted_pass(rg, rw, wsum, a.blocks + ci * kBlocksPerRange, bpw);
+    // Residual pass over this CTA's range of rows pos, staged by one bulk
+    // copy per row; the last range to arrive locates the draw.
+    const int lo = c * R;
+    const int rn = min(R, V - lo);
+    const int nvec = (rn + kVec - 1) / kVec;
+    const size_t pi_idx = static_cast<size_t>(b) * W + pi;
+    const size_t ci = pi_idx * NR + c;
+    const bool ok = stage_rows(trow + lo, drow + lo, rn, bulk, s_t, s_d, &bars[0], &sh_ok);
+    const double cta = block_sums(SmemRows<E>{s_t, s_d}, nvec, rw, sh_blk, a.blocks + ci * kBlocksPerRange);
     __syncthreads();  // every warp's block sums are written before the release below
     if (tid == 0) {
-      a.csum[ci] = cta;
-      sh_last = ticket_add(a.ticket + b * W + pi) == NR - 1;
+      a.csum[ci] = ok ? cta : NAN;
+      sh_last = ticket_add(a.ticket + pi_idx) == NR - 1;
     }
     __syncthreads();
     if (!sh_last) return;
+    // Every range's sum and block sums, in one round of loads.
+    float* s_blk = reinterpret_cast<float*>(dyn_smem);  // the staged rows are no longer needed
+    for (int k = tid; k < NR * nbr; k += kT2) {
+      const int r = k / nbr, j = k - r * nbr;
+      s_blk[k] = __ldcg(a.blocks + (pi_idx * NR + r) * kBlocksPerRange + j);
+    }
     if (warp == 0) {
       double w = 0.0;
-      if (lane < NR) w = *reinterpret_cast<volatile double*>(a.csum + (static_cast<size_t>(b) * W + pi) * NR + lane);
+      if (lane < NR) w = __ldcg(a.csum + pi_idx * NR + lane);
       double incl = w;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -678,15 +719,15 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const VerifyArgs a)
         owner = hit ? __ffs(hit) - 1 : 31 - __clz(posm);
         prefix = __shfl_sync(0xFFFFFFFFu, incl - w, owner);
         local = target - prefix;
-      } else {
+      } else if (tot == 0.0) {
         // No residual mass: draw from q_pos instead, located by chunk record.
         locate_target_chunk(a, b * W + pos, s.tm, cc, ures, &owner, &local, &prefix, &total);
         tgt = 1;
-      }
+      }  // NaN: a staging wait ran out (owner stays -1)
       if (lane == 0) {
         if (a.stats)
           a.stats[(static_cast<size_t>(b) * W + pi) * SSD_NSTAT_VERIFY + 6] = static_cast<float>(tot / s.ts);
-        a.ticket[b * W + pi] = 0;
+        a.ticket[pi_idx] = 0;
         sh_owner = owner;
         sh_local = local;
         sh_prefix = prefix;
@@ -703,25 +744,17 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const VerifyArgs a)
       }
       return;
     }
-    target_w = sh_target_w != 0;
-    if (!target_w) {
-      // The owning range's block sums were published by the CTA that summed
-      // it: locate the 32-vector block holding the target and scan just it.
+    if (!sh_target_w) {
+      // The owning range's block sums locate the 32-vector block; one scan of
+      // just that block (rows read from L2) finds the token.
       if (warp == 0) {
         const int owner = sh_owner;
-        const size_t oi = (static_cast<size_t>(b) * W + pi) * NR + owner;
-        const int lo = owner * span;
-        const int rn = min(span, V - lo);
-        const GlobalRange<E> rg{trow + lo, drow + lo, rn, aligned};
+        const int olo = owner * R;
+        const int orn = min(R, V - olo);
+        const int onv = (orn + kVec - 1) / kVec;
+        const GlobalRange<E> rg{trow + olo, drow + olo, orn, bulk};
         double before = 0.0;
-        const int blk = locate_block(a.blocks + oi * kBlocksPerRange, kWarps * bpw, sh_local, &before);
-        ScanHit h{-1, NAN, 0.f};
-        if (blk >= 0) {
-          int w0, w1;
-          warp_range((rn + kVec - 1) / kVec, blk / bpw, w0, w1);
-          const int b0 = w0 + 32 * (blk % bpw);
-          h = warp_scan<kVec>(b0, min(b0 + 32, w1), sh_local - before, rg, rw);
-        }
+        const ScanHit h = locate_in_rows<E>(s_blk + owner * nbr, (onv + 31) / 32, onv, sh_local, rg, rw, &before);
         if (lane == 0) {
           if (h.elem < 0) {
             write_error(a, b);
@@ -733,17 +766,17 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const VerifyArgs a)
               st[8] = static_cast<float>(ures - e0 / sh_total);
               st[9] = static_cast<float>((e0 + static_cast<double>(h.w)) / sh_total - ures);
             }
-            write_outputs(a, b, n, lo + h.elem, tok_x);
+            write_outputs(a, b, n, olo + h.elem, tok_x);
           }
         }
       }
       return;
     }
-    draw_lo = sh_owner * geo.chunk;  // q fallback: the owner is a streaming chunk
+    chunk_draw = sh_owner;  // q fallback: the owner is a streaming chunk
   } else {
-    // Bonus draw from q_gamma: the streaming chunk holding the target comes
-    // from the records; the CTA whose range covers it draws.
-    if (pos != n) return;
+    // Bonus draw from q_gamma, by the first range's CTA: the streaming chunk
+    // holding the target comes from the records.
+    if (pos != n || c != 0) return;
     if (warp == 0) {
       int owner;
       double local, prefix, total;
@@ -756,36 +789,35 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const VerifyArgs a)
       }
     }
     __syncthreads();
-    if (sh_owner < 0 || (sh_owner * geo.chunk) / span != c) return;
-    target_w = true;
-    draw_lo = sh_owner * geo.chunk;
+    if (sh_owner < 0 || !(sh_total > 0.0)) {
+      if (tid == 0) {
+        write_error(a, b);
+        atomicOr(a.status, 1 << SSD_ERR_TIMEOUT);
+      }
+      return;
+    }
+    chunk_draw = sh_owner;
   }
 
-  // Target-weight draw inside one streaming chunk: a whole-CTA pass for the
-  // per-warp sums, then warp 0 scans the run holding the target.
-  draw_n = min(geo.chunk, V - draw_lo);
-  const GlobalRange<E> rg{trow + draw_lo, nullptr, draw_n, aligned};
-  const int bpw1 = ((draw_n + kVec - 1) / kVec + kWarps * 32 - 1) / (kWarps * 32);
-  global_weighted_pass(rg, tw, wsum, sh_blocks, bpw1);
+  // Target-weight draw inside one streaming chunk of row pos: the chunk is
+  // staged, its block sums give the 32-vector block, one scan finds the token.
+  const int draw_lo = chunk_draw * geo.chunk;
+  const int draw_n = min(geo.chunk, V - draw_lo);
+  const int dnv = (draw_n + kVec - 1) / kVec;
+  const bool ok = stage_rows<E>(trow + draw_lo, nullptr, draw_n, bulk, s_t, nullptr, &bars[1], &sh_ok);
+  const SmemRows<E> rows{s_t, nullptr};
+  block_sums(rows, dnv, tw, sh_blk, nullptr);
   if (warp == 0) {
     double before = 0.0;
-    const int blk = locate_block(sh_blocks, kWarps * bpw1, sh_local, &before);
-    ScanHit h{-1, NAN, 0.f};
-    if (blk >= 0) {
-      int w0, w1;
-      warp_range((draw_n + kVec - 1) / kVec, blk / bpw1, w0, w1);
-      const int b0 = w0 + 32 * (blk % bpw1);
-      h = warp_scan<kVec>(b0, min(b0 + 32, w1), sh_local - before, rg, tw);
-    }
-    const double run_base = before;
+    const ScanHit h = locate_in_rows<E>(sh_blk, (dnv + 31) / 32, dnv, sh_local, rows, tw, &before);
     if (lane == 0) {
-      if (h.elem < 0) {
+      if (!ok || h.elem < 0) {
         write_error(a, b);
         atomicOr(a.status, 1 << SSD_ERR_TIMEOUT);
       } else {
         if (a.stats) {
           float* st = a.stats + (static_cast<size_t>(b) * W + pos) * SSD_NSTAT_VERIFY;
-          const double e0 = sh_prefix + run_base + h.edge;
+          const double e0 = sh_prefix + before + h.edge;
           st[8] = static_cast<float>(ures - e0 / sh_total);
           st[9] = static_cast<float>((e0 + static_cast<double>(h.w)) / sh_total - ures);
         }
@@ -830,12 +862,13 @@ cudaError_t ensure_smem(const void* fn, int smem_bytes, int* cached) {
 
 template <typename E>
 cudaError_t launch_verify_t(const VerifyArgs& a, int smem_bytes, cudaStream_t stream) {
-  static thread_local int dev_cached = -1, smem1 = -1;
+  static thread_local int dev_cached = -1, smem1 = -1, smem2 = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev != dev_cached) {
     smem1 = -1;
+    smem2 = -1;
     dev_cached = dev;
   }
   e = ensure_smem(reinterpret_cast<const void*>(&stream_kernel<E>), smem_bytes, &smem1);
@@ -853,13 +886,13 @@ cudaError_t launch_verify_t(const VerifyArgs& a, int smem_bytes, cudaStream_t st
   c1.numAttrs = 1;
   e = cudaLaunchKernelEx(&c1, stream_kernel<E>, a);
   if (e != cudaSuccess) return e;
+  e = ensure_smem(reinterpret_cast<const void*>(&sample_kernel<E>), a.geo.smem2, &smem2);
+  if (e != cudaSuccess) return e;
   const int P = a.debug ? a.gmax + 1 : 1;
-  const int span = a.geo.span * a.geo.chunk;
-  const int nr = (a.geo.V + span - 1) / span;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(nr, P, a.B);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.gridDim = dim3(a.geo.nrange, P, a.B);
+  cfg.blockDim = dim3(kT2, 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(a.geo.smem2);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
