@@ -122,23 +122,9 @@ ssd_status choose_chunks(int V, int esize, bool aligned, ChunkGeometry* geo, int
   geo->nchunk = (V + chunk - 1) / chunk;
   geo->row_smem = row_smem;
   geo->bulk = aligned ? 1 : 0;
-  // residual ranges of the sampling kernel: about 16 KB of a row
-  // (SSDV_RANGE_BYTES overrides), a whole number of 32-vector blocks, at most
-  // kMaxChunks ranges and 128 blocks per range
-  const int kvec = 16 / esize;
-  const int blk = 32 * kvec;
-  int range = static_cast<int>(round_up(static_cast<size_t>(env_int("SSDV_RANGE_BYTES", 16 * 1024) / esize), blk));
-  if (range < blk) range = blk;
-  if ((V + range - 1) / range > kMaxChunks) range = static_cast<int>(round_up((static_cast<size_t>(V) + kMaxChunks - 1) / kMaxChunks, blk));
-  if (range > 128 * blk) return fail(SSD_ERR_UNSUPPORTED, "V=%d: a residual range exceeds 128 blocks", V);
-  geo->range = range;
-  geo->nrange = (V + range - 1) / range;
-  const size_t s2 = round_up(std::max({static_cast<size_t>(2) * range * esize,
-                                       round_up(static_cast<size_t>(chunk), kvec) * esize,
-                                       static_cast<size_t>(geo->nrange) * (range / blk) * sizeof(float)}), 128);
-  if (s2 > static_cast<size_t>(max_smem))
-    return fail(SSD_ERR_UNSUPPORTED, "V=%d: a residual range does not fit in shared memory", V);
-  geo->smem2 = static_cast<int>(s2);
+  // pieces of the sampling kernel: 128 vectors of a row each
+  geo->npiece = static_cast<int>((static_cast<long long>(V) + 128 * (16 / esize) - 1) / (128 * (16 / esize)));
+  if (geo->npiece > kMaxPieces) return fail(SSD_ERR_UNSUPPORTED, "V=%d: more than %d pieces per row", V, kMaxPieces);
   *smem_bytes = 2 * row_smem;
   return SSD_OK;
 }
@@ -189,8 +175,7 @@ ssd_status verify_common(const void* target, const void* draft, ssd_dtype dtype,
   a.status = reinterpret_cast<int32_t*>(ws + L.status);
   a.ticket = reinterpret_cast<int32_t*>(ws + L.ticket);
   a.part = reinterpret_cast<float4*>(ws + L.part);
-  a.csum = reinterpret_cast<double*>(ws + L.csum);
-  a.blocks = reinterpret_cast<float*>(ws + L.blocks);
+  a.psum = reinterpret_cast<float*>(ws + L.blocks);
   a.stats = stats;
   a.debug = stats ? 1 : 0;
   a.geo = geo;
@@ -201,7 +186,7 @@ ssd_status verify_common(const void* target, const void* draft, ssd_dtype dtype,
   // streams.
   int seg = env_int("SSDV_SEGMENT", 65535);
   seg = std::max(1, std::min(seg, 65535));
-  const int NRg = geo.nrange;
+  const int NP = geo.npiece;
   const int W = gmax + 1;
   for (int b0 = 0; b0 < B; b0 += seg) {
     VerifyArgs s = a;
@@ -219,8 +204,7 @@ ssd_status verify_common(const void* target, const void* draft, ssd_dtype dtype,
     const size_t u0 = static_cast<size_t>(b0) * W;  // the segment's first (request, position) unit
     s.ticket = a.ticket + u0;
     s.part = a.part + u0 * geo.nchunk * 2;
-    s.csum = a.csum + u0 * NRg;
-    s.blocks = a.blocks + u0 * NRg * 128;
+    s.psum = a.psum + u0 * NP;
     const cudaError_t e = launch_verify(s, es, smem, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "verify launch");
   }

@@ -21,19 +21,18 @@ struct Geometry {
 };
 
 // How verification splits each row: the streaming kernel runs one CTA per
-// (request, position, chunk), the sampling kernel one CTA per (request,
-// residual range) (per (request, position, range) in the debug mode).
+// (request, position, chunk); the sampling kernel one warp per piece (128
+// vectors) of each request's draw row (of every row in the debug mode).
 struct ChunkGeometry {
   int V;         // vocabulary size
   int chunk;     // elements per chunk, a multiple of 8
   int nchunk;    // chunks per row, 1..kMaxChunks
   int row_smem;  // shared-memory bytes per staged row chunk (a multiple of 128)
   int bulk;      // 1: rows 16-byte aligned, staged with bulk async copies
-  int range;     // elements per residual range, a whole number of 32-vector blocks
-  int nrange;    // residual ranges per row, 1..kMaxChunks
-  int smem2;     // dynamic shared memory of a sampling CTA (bytes)
+  int npiece;    // pieces (128 vectors) per row, at most kMaxPieces
 };
 constexpr int kMaxChunks = 32;
+constexpr int kMaxPieces = 1024;  // 2^19 fp32 elements / 512
 
 struct VerifyArgs {
   const void* target;          // [B, gmax+1, V]
@@ -48,9 +47,8 @@ struct VerifyArgs {
   int32_t* out_tokens;         // [B, gmax+1]
   int32_t* n_accepted;         // [B]
   float4* part;                // workspace [B, gmax+1, nchunk, 2]: per-chunk row statistics
-  double* csum;                // workspace [B, gmax+1, nrange]: per-range residual weight sums
-  float* blocks;               // workspace [B, gmax+1, nrange, 128]: their 32-vector block sums
-  int32_t* ticket;             // workspace [B, gmax+1]: residual chunks arrived
+  float* psum;                 // workspace [B, gmax+1, npiece]: per-piece weight sums of the draw rows
+  int32_t* ticket;             // workspace [B, gmax+1]: pieces arrived
   int32_t* status;             // workspace [1]: device error bits
   float* stats;                // [B, gmax+1, SSD_NSTAT_VERIFY] or null (debug)
   int debug;                   // 1: decide and report every position (statistics)

@@ -16,15 +16,14 @@
 //     argmax of a greedy row, and the draft token's two logits when the token
 //     falls in the chunk).
 //     Every logit is read from HBM exactly once, by short-lived CTAs.
-//  2. sample_kernel: one small CTA per (request, residual range).  Each
-//     combines the request's records, takes every accept decision and finds
-//     the first rejection n.  For a residual draw every CTA stages its range
-//     of rows n (L2-resident: the streaming kernel reads the low positions
-//     last) with one bulk copy per row and publishes the range's weight sum
-//     and 32-vector block sums; the last range to arrive loads all of them at
-//     once, locates the block holding u * S and scans just that block.  A
-//     bonus draw (n = gamma) locates its streaming chunk from the records,
-//     stages that chunk and scans it.
+//  2. sample_kernel: small CTAs, each covering four pieces (128 vectors
+//     each) of one request's draw row.  Every CTA combines the request's
+//     records, takes every accept decision and finds the first rejection n;
+//     then each warp loads its piece of row n (L2-resident: the streaming
+//     kernel reads the low positions last) in one round of loads -- target and
+//     draft for a residual draw, target for the bonus draw -- and publishes the
+//     piece's weight sum.  The last warp to arrive sums the pieces in order,
+//     finds the piece holding u * S, reloads that piece and scans it.
 //
 // A call runs as segments of requests, each a streaming + sampling pair, all
 // launched with programmatic dependent launch.  The first streaming kernel's
@@ -336,80 +335,6 @@ __device__ __forceinline__ void locate_target_chunk(const VerifyArgs& a, int uni
 
 }  // namespace
 
-// Vector v of a row range straight from global memory (L2-resident rows in
-// practice): 16-byte loads when the rows are aligned, else element loads with
-// -inf beyond the range.  gd may be null (target weights).
-template <typename E>
-struct GlobalRange {
-  const E* gt;
-  const E* gd;
-  int n;
-  bool aligned;
-  __device__ __forceinline__ void operator()(int v, float (&xt)[Elem<E>::kVec], float (&xd)[Elem<E>::kVec]) const {
-    constexpr int kVec = Elem<E>::kVec;
-    if (aligned) {
-      Elem<E>::unpack(__ldg(reinterpret_cast<const uint4*>(gt) + v), xt);
-      if (gd) Elem<E>::unpack(__ldg(reinterpret_cast<const uint4*>(gd) + v), xd);
-    } else {
-#pragma unroll
-      for (int e = 0; e < kVec; ++e) {
-        const int k = v * kVec + e;
-        xt[e] = k < n ? Elem<E>::to_float(gt[k]) : -INFINITY;
-        if (gd) xd[e] = k < n ? Elem<E>::to_float(gd[k]) : -INFINITY;
-      }
-    }
-  }
-};
-
-// Warp-wide: the 32-vector block of a range that holds target tl (relative
-// to the range start), from the range's block sums (nb <= 128 of them, in
-// index order; each lane reads four consecutive ones once); returns the block
-// (-1 if no positive weight) and the weight before it.  A target past every
-// boundary goes to the last positive block.
-__device__ __forceinline__ int locate_block(const float* blocks, int nb, double tl, double* before) {
-  const int lane = threadIdx.x & 31;
-  float v[4];
-  double mine = 0.0;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int q = lane * 4 + k;
-    v[k] = q < nb ? *reinterpret_cast<const volatile float*>(blocks + q) : 0.f;
-    mine += static_cast<double>(v[k]);
-  }
-  double incl = mine;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const double t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (lane >= o) incl += t;
-  }
-  const unsigned hit = __ballot_sync(0xFFFFFFFFu, mine > 0.0 && tl < incl);
-  const unsigned pos = __ballot_sync(0xFFFFFFFFu, mine > 0.0);
-  if (!pos) return -1;
-  const int L = hit ? __ffs(hit) - 1 : 31 - __clz(pos);
-  double acc = __shfl_sync(0xFFFFFFFFu, incl - mine, L);
-  int found = -1, last = -1;
-  double found_before = 0.0, last_before = 0.0;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {  // lane L's four blocks, broadcast
-    const double w = static_cast<double>(__shfl_sync(0xFFFFFFFFu, v[k], L));
-    if (w > 0.0) {
-      last = L * 4 + k;
-      last_before = acc;
-      if (found < 0 && tl < acc + w) {
-        found = L * 4 + k;
-        found_before = acc;
-      }
-    }
-    acc += w;
-  }
-  if (found < 0) {
-    found = last;
-    found_before = last_before;
-  }
-  *before = found_before;
-  return found;
-}
-
 // Arrival counter with acquire-release semantics: the releases of earlier
 // arrivals (their published sums) are visible to the last one.
 __device__ __forceinline__ int ticket_add(int32_t* p) {
@@ -419,119 +344,242 @@ __device__ __forceinline__ int ticket_add(int32_t* p) {
 }
 
 // ---------------------------------------------------------------------------
-// Kernel 2: decisions and the draw.  One CTA of kT2 threads per (residual
-// range r, position slot, request); a residual range is `range` elements of a
-// row (a whole number of 32-vector blocks).
+// Kernel 2: decisions and the draw, warp by warp.  A piece is 128 vectors
+// (four 32-vector blocks) of a row; a warp takes kPiecesPerWarp consecutive
+// pieces of one draw row and a CTA of kT2 threads kW2 such runs.  Every CTA of
+// a request combines the request's records and takes the decisions (identical
+// results); then each warp loads its pieces of row n -- target and draft for a
+// residual draw, target for the bonus draw -- one round of loads per piece,
+// publishes their weight sums and arrives once on the row's counter.  The last
+// warp to arrive sums the pieces in order, finds the piece holding u * S,
+// reloads that piece and scans it.
 // ---------------------------------------------------------------------------
 constexpr int kT2 = 128;  // threads of a sampling CTA
 constexpr int kW2 = kT2 / 32;
-constexpr int kBlocksPerRange = 128;  // 32-vector blocks of a residual range, at most
+constexpr int kPieceVecs = 128;  // vectors per piece: 4 per lane
+constexpr int kPiecesPerWarp = 2;
 
-// Rows [0, n) of gt (and gd) into shared memory: one bulk copy per row
-// completing on `bar` (fresh, phase 0; bounded wait), or plain loads padded
-// with -inf to whole vectors when the rows are not 16-byte aligned.  All
-// threads; returns false when the bounded wait ran out.
+// A piece's vectors as raw 16-byte words, lane L holding the 4 consecutive
+// vectors 4L .. 4L+3, target and, when gd is given, draft; elements past n
+// read as -inf (weight 0).  One round of loads.
 template <typename E>
-__device__ __forceinline__ bool stage_rows(const E* gt, const E* gd, int n, bool bulk, E* st, E* sd, uint64_t* bar,
-                                           int* sh_ok) {
-  constexpr int kVec = Elem<E>::kVec;
-  if (bulk) {
-    if (threadIdx.x == 0) {
-      mbar_init(bar, 1);
-      fence_mbar_init();
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      const uint32_t bytes = static_cast<uint32_t>(n) * sizeof(E);
-      mbar_arrive_expect_tx(bar, gd ? 2 * bytes : bytes);
-      const uint64_t pol = l2_policy_evict_normal();
-      bulk_copy_g2s(st, gt, bytes, bar, pol);
-      if (gd) bulk_copy_g2s(sd, gd, bytes, bar, pol);
-      *sh_ok = mbar_wait_bounded(bar, 0) ? 1 : 0;
+struct PieceRows {
+  uint4 rt[4], rd[4];
+  __device__ __forceinline__ void load(const E* gt, const E* gd, int n, bool aligned) {
+    constexpr int kVec = Elem<E>::kVec;
+    const int lane = threadIdx.x & 31;
+    const int nv = (n + kVec - 1) / kVec;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int v = 4 * lane + k;
+      rt[k] = rd[k] = Elem<E>::max_init();  // all -inf
+      if (v >= nv) continue;
+      if (aligned) {
+        rt[k] = __ldg(reinterpret_cast<const uint4*>(gt) + v);
+        if (gd) rd[k] = __ldg(reinterpret_cast<const uint4*>(gd) + v);
+      } else {
+        rt[k] = gather_vec(gt, v * kVec, n);
+        if (gd) rd[k] = gather_vec(gd, v * kVec, n);
+      }
     }
-    __syncthreads();
-    return *sh_ok != 0;
   }
-  const int padded = (n + kVec - 1) / kVec * kVec;
-  for (int e = threadIdx.x; e < padded; e += kT2) {
-    st[e] = e < n ? gt[e] : Elem<E>::neg_inf();
-    if (gd) sd[e] = e < n ? gd[e] : Elem<E>::neg_inf();
+  // Elements [i0, i0 + kVec) of a row not aligned to 16 bytes, -inf past n.
+  static __device__ __forceinline__ uint4 gather_vec(const E* g, int i0, int n) {
+    uint32_t w[4];
+    if constexpr (sizeof(E) == 2) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t lo = i0 + 2 * j < n ? static_cast<uint32_t>(g[i0 + 2 * j]) : 0xFF80u;
+        const uint32_t hi = i0 + 2 * j + 1 < n ? static_cast<uint32_t>(g[i0 + 2 * j + 1]) : 0xFF80u;
+        w[j] = lo | (hi << 16);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) w[j] = __float_as_uint(i0 + j < n ? static_cast<float>(g[i0 + j]) : -INFINITY);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
   }
-  __syncthreads();
-  return true;
-}
-
-// Vector v of rows staged in shared memory (sd may be null: target weights).
-template <typename E>
-struct SmemRows {
-  const E* st;
-  const E* sd;
-  __device__ __forceinline__ void operator()(int v, float (&xt)[Elem<E>::kVec], float (&xd)[Elem<E>::kVec]) const {
-    Elem<E>::unpack(reinterpret_cast<const uint4*>(st)[v], xt);
-    if (sd) Elem<E>::unpack(reinterpret_cast<const uint4*>(sd)[v], xd);
+  template <typename WFun>
+  __device__ __forceinline__ void weights(int k, const WFun& wfun, float (&w)[Elem<E>::kVec]) const {
+    float xt[Elem<E>::kVec], xd[Elem<E>::kVec];
+    Elem<E>::unpack(rt[k], xt);
+    Elem<E>::unpack(rd[k], xd);
+    wfun(xt, xd, w);
   }
 };
 
-// The weight sum of every 32-vector block of nvec staged vectors (lanes
-// summed by a fixed butterfly) into blk[] (shared) and, when given, gblk[]
-// (global); returns their sum in block order (fp64) in thread 0.
+// The weight sum of a lane's 4 vectors (in vector order).
 template <typename E, typename WFun>
-__device__ double block_sums(const SmemRows<E>& rows, int nvec, const WFun& wfun, float* blk, float* gblk) {
-  constexpr int kVec = Elem<E>::kVec;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nb = (nvec + 31) / 32;
-  for (int j = warp; j < nb; j += kW2) {
-    const int v = j * 32 + lane;
-    float s = 0.f;
-    if (v < nvec) {
-      float xt[kVec], xd[kVec], w[kVec];
-      rows(v, xt, xd);
-      wfun(xt, xd, w);
-      s = pair_sum(w);
-    }
-    s = warp_sum(s);
-    if (lane == 0) {
-      blk[j] = s;
-      if (gblk) gblk[j] = s;
-    }
+__device__ __forceinline__ float piece_lane_sum(const PieceRows<E>& pr, const WFun& wfun) {
+  float s = 0.f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float w[Elem<E>::kVec];
+    pr.weights(k, wfun, w);
+    s += pair_sum(w);
   }
-  __syncthreads();
-  double tot = 0.0;
-  if (threadIdx.x == 0)
-    for (int j = 0; j < nb; ++j) tot += static_cast<double>(blk[j]);
-  return tot;
+  return s;
 }
 
-// Warp 0: the token at target tl (relative to the staged or global rows'
-// start) from their block sums blk[0..nb): the 32-vector block, then a scan of
-// just that block.  Returns the hit (element relative to the rows' start, -1
-// if none) and the weight before its block in *before.
-template <typename E, typename Load, typename WFun>
-__device__ __forceinline__ ScanHit locate_in_rows(const float* blk, int nb, int nvec, double tl, const Load& load,
-                                                  const WFun& wfun, double* before) {
+// One warp, one value per lane in index order: the exclusive prefix of every
+// lane (fp64) and the first lane whose running sum passes tl, else the last
+// lane with a positive value (-1 if none).
+__device__ __forceinline__ int lane_locate(double v, double tl, double* before) {
+  const int lane = threadIdx.x & 31;
+  double incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  const unsigned hm = __ballot_sync(0xFFFFFFFFu, v > 0.0 && tl < incl);
+  const unsigned pm = __ballot_sync(0xFFFFFFFFu, v > 0.0);
+  const int L = hm ? __ffs(hm) - 1 : (pm ? 31 - __clz(pm) : -1);
+  *before = __shfl_sync(0xFFFFFFFFu, incl - v, L >= 0 ? L : 0);
+  return L;
+}
+
+// One warp: the element of a loaded piece whose running weight first exceeds
+// tl (relative to the piece start), falling back to the last element with
+// positive weight: a lane scan over the lanes' sums, then the found lane's 4
+// vectors element by element (fp32 from the lane's start: the lane's weight is
+// a small share of the row's).  Returns the element index relative to the
+// piece start (-1 if none), the weight before it and its weight.
+template <typename E, typename WFun>
+__device__ __forceinline__ ScanHit scan_piece(const PieceRows<E>& pr, const WFun& wfun, double tl) {
   constexpr int kVec = Elem<E>::kVec;
-  *before = 0.0;
-  const int j = locate_block(blk, nb, tl, before);
+  const int lane = threadIdx.x & 31;
+  float w[4][kVec];
+  float ls = 0.f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    pr.weights(k, wfun, w[k]);
+    ls += pair_sum(w[k]);
+  }
+  double before = 0.0;
+  const int L = lane_locate(static_cast<double>(ls), tl, &before);
+  if (L < 0) return ScanHit{-1, NAN, 0.f};
+  int el = -1;
+  float edge = 0.f, we = 0.f;
+  if (lane == L) {
+    const float t = static_cast<float>(tl - before);
+    float acc = 0.f;
+    bool done = false;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+#pragma unroll
+      for (int e = 0; e < kVec; ++e) {
+        if (!done && w[k][e] > 0.f) {
+          el = k * kVec + e;  // the hit, or the last positive element so far
+          edge = acc;
+          we = w[k][e];
+          done = t < acc + w[k][e];
+        }
+        acc += w[k][e];
+      }
+    }
+  }
+  el = __shfl_sync(0xFFFFFFFFu, el, L);
+  edge = __shfl_sync(0xFFFFFFFFu, edge, L);
+  we = __shfl_sync(0xFFFFFFFFu, we, L);
+  if (el < 0) return ScanHit{-1, NAN, 0.f};
+  return ScanHit{4 * L * kVec + el, before + static_cast<double>(edge), we};
+}
+
+// One warp: a row's piece sums, copied into the warp's shared slice `v` (lane
+// L's consecutive share first summed by lane L), the lane sums and the row
+// total (fp64 over lanes), valid in every lane.
+struct RowPieces {
+  float* v;  // shared, kMaxPieces
+  int per;
+  float lane_sum;
+  double total;
+  __device__ __forceinline__ void load(const float* psum, int np, float* slice) {
+    const int lane = threadIdx.x & 31;
+    v = slice;
+    per = (np + 31) / 32;
+    for (int q = lane; q < np; q += 32) v[q] = __ldcg(psum + q);
+    __syncwarp();
+    lane_sum = 0.f;
+    for (int k = 0; k < per; ++k) {
+      const int q = lane * per + k;
+      if (q < np) lane_sum += v[q];
+    }
+    double t = static_cast<double>(lane_sum);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
+    total = t;
+  }
+};
+
+// One warp: the draw at u * total from a row's piece sums: the lane whose
+// pieces hold it, the piece within that lane's run, then that piece reloaded
+// and scanned; writes request b's outputs (tok_x: its first n draft tokens)
+// and, with statistics, the CDF edges of the drawn token.
+template <typename E, typename WFun>
+__device__ __noinline__ void warp_draw_row(const VerifyArgs& a, int b, int n, size_t pi_idx, const RowPieces& rp,
+                                           double ures, const E* trow, const E* drow, bool aligned, const WFun& wfun,
+                                           const int* tok_x) {
+  constexpr int kVec = Elem<E>::kVec;
+  const int lane = threadIdx.x & 31;
+  const int V = a.geo.V, pelems = kPieceVecs * kVec;
+  const double tot = rp.total;
+  const double target = ures * tot;
+  double before = 0.0;
+  const int L = lane_locate(static_cast<double>(rp.lane_sum), target, &before);
+  int owner = -1;
+  float obefore = 0.f;
+  if (lane == L) {
+    const float t = static_cast<float>(target - before);
+    float acc = 0.f;
+    for (int k = 0; k < rp.per; ++k) {
+      const int q = L * rp.per + k;
+      const float w = q < a.geo.npiece ? rp.v[q] : 0.f;
+      if (w > 0.f) {
+        owner = q;  // the hit, or the last positive piece so far
+        obefore = acc;
+        if (t < acc + w) break;
+      }
+      acc += w;
+    }
+  }
+  owner = __shfl_sync(0xFFFFFFFFu, owner, L >= 0 ? L : 0);
+  const double owner_before = before + static_cast<double>(__shfl_sync(0xFFFFFFFFu, obefore, L >= 0 ? L : 0));
   ScanHit h{-1, NAN, 0.f};
-  if (j >= 0) h = warp_scan<kVec>(j * 32, min(j * 32 + 32, nvec), tl - *before, load, wfun);
-  return h;
+  const int olo = owner * pelems;
+  if (L >= 0 && owner >= 0) {
+    PieceRows<E> pr;
+    pr.load(trow + olo, drow ? drow + olo : nullptr, min(pelems, V - olo), aligned);
+    h = scan_piece(pr, wfun, target - owner_before);
+  }
+  if (lane == 0) {
+    if (h.elem < 0 || !(tot > 0.0)) {
+      write_error(a, b);
+      atomicOr(a.status, 1 << SSD_ERR_TIMEOUT);
+    } else {
+      if (a.stats) {
+        float* st = a.stats + pi_idx * SSD_NSTAT_VERIFY;
+        const double e0 = owner_before + h.edge;
+        st[8] = static_cast<float>(ures - e0 / tot);
+        st[9] = static_cast<float>((e0 + static_cast<double>(h.w)) / tot - ures);
+      }
+      write_outputs(a, b, n, olo + h.elem, tok_x);
+    }
+  }
 }
 
 template <typename E>
-__global__ void __launch_bounds__(kT2) sample_kernel(const VerifyArgs a) {
-  extern __shared__ __align__(128) uint8_t dyn_smem[];
-  __shared__ __align__(8) uint64_t bars[2];
+__global__ void __launch_bounds__(kT2, 8) sample_kernel(const VerifyArgs a) {
   __shared__ UnitStat ust[SSD_MAX_GAMMA + 1];
-  __shared__ float sh_blk[kBlocksPerRange];
   __shared__ int tok_x[SSD_MAX_GAMMA];
   __shared__ float tok_t[SSD_MAX_GAMMA], tok_d[SSD_MAX_GAMMA];
-  __shared__ int sh_n, sh_bad, sh_last, sh_owner, sh_target_w, sh_ok;
-  __shared__ float sh_ures;
-  __shared__ double sh_local, sh_prefix, sh_total;
+  __shared__ int sh_n, sh_bad;
+  __shared__ float s_pieces[kW2][kMaxPieces];  // the last warp's copy of its row's piece sums
 
   constexpr int kVec = Elem<E>::kVec;
   const ChunkGeometry& geo = a.geo;
-  const int V = geo.V, NC = geo.nchunk, W = a.gmax + 1;
-  const int R = geo.range, NR = geo.nrange;
-  const int nbr = R / (32 * kVec);  // blocks of a full range
+  const int V = geo.V, NC = geo.nchunk, W = a.gmax + 1, NP = geo.npiece;
+  const int pelems = kPieceVecs * kVec;
   const int c = blockIdx.x, pi = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -548,8 +596,6 @@ __global__ void __launch_bounds__(kT2) sample_kernel(const VerifyArgs a) {
   }
   if (pi > g) return;
   const bool greedy = (T == 0.f);
-  const E* tb = static_cast<const E*>(a.target);
-  const E* db = static_cast<const E*>(a.draft);
 
   // Inputs only (overlaps the streaming kernel's tail; the kernel that wrote
   // them completed before any streaming CTA let this grid launch): the draft
@@ -585,20 +631,35 @@ __global__ void __launch_bounds__(kT2) sample_kernel(const VerifyArgs a) {
     tok_d[lane] = r1.x;
     tok_t[lane] = r1.w;
   }
-  for (int u = warp; u <= g; u += kW2) {
-    MaxSum t{-INFINITY, 0.f}, d{-INFINITY, 0.f};
-    ArgMax am{-INFINITY, -1};
-    int err = 0;
-    if (lane < NC) {
-      const float4* rec = a.part + ((static_cast<size_t>(b) * W + u) * NC + lane) * 2;
-      const float4 r0 = __ldcg(rec), r1 = __ldcg(rec + 1);
-      t = MaxSum{r0.x, r0.y};
-      d = MaxSum{r0.z, r0.w};
-      if (greedy) am = ArgMax{r1.x, __float_as_int(r1.y)};
-      err = __float_as_int(r1.z);
+  // A warp combines positions warp, warp + kW2, ..., two at a time: both
+  // positions' records are loaded (one round), then combined.
+  for (int u0 = warp; u0 <= g; u0 += 2 * kW2) {
+    float4 r0[2], r1[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int u = u0 + j * kW2;
+      if (u <= g && lane < NC) {
+        const float4* rec = a.part + ((static_cast<size_t>(b) * W + u) * NC + lane) * 2;
+        r0[j] = __ldcg(rec);
+        r1[j] = __ldcg(rec + 1);
+      }
     }
-    butterfly_stats(t, d, am, err, cc);
-    if (lane == 0) ust[u] = UnitStat{t.m, t.s, d.m, d.s, am.v, am.i, err};
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int u = u0 + j * kW2;
+      if (u > g) break;
+      MaxSum t{-INFINITY, 0.f}, d{-INFINITY, 0.f};
+      ArgMax am{-INFINITY, -1};
+      int err = 0;
+      if (lane < NC) {
+        t = MaxSum{r0[j].x, r0[j].y};
+        d = MaxSum{r0[j].z, r0[j].w};
+        if (greedy) am = ArgMax{r1[j].x, __float_as_int(r1[j].y)};
+        err = __float_as_int(r1[j].z);
+      }
+      butterfly_stats(t, d, am, err, cc);
+      if (lane == 0) ust[u] = UnitStat{t.m, t.s, d.m, d.s, am.v, am.i, err};
+    }
   }
   __syncthreads();
 
@@ -623,12 +684,7 @@ __global__ void __launch_bounds__(kT2) sample_kernel(const VerifyArgs a) {
     }
     const unsigned rej = __ballot_sync(0xFFFFFFFFu, lane < g && !acc);
     const int n = rej ? __ffs(rej) - 1 : g;
-    const int dp = a.debug ? pi : n;
-    const float ures_dp = __shfl_sync(0xFFFFFFFFu, dr.resample, min(dp, 31));
-    if (lane == 0) {
-      sh_n = n;
-      sh_ures = ures_dp;
-    }
+    if (lane == 0) sh_n = n;
     if (a.stats && c == 0 && lane == pi) {
       float* st = a.stats + (static_cast<size_t>(b) * W + pi) * SSD_NSTAT_VERIFY;
       const UnitStat s = ust[pi];
@@ -664,166 +720,74 @@ __global__ void __launch_bounds__(kT2) sample_kernel(const VerifyArgs a) {
     return;
   }
 
+  // The draw row: row n (pos = pi for every row below g with statistics; the
+  // bonus row g only when it is drawn from).
   const int pos = a.debug ? pi : n;
+  if (pos == g && n != g) return;
+  const bool residual = pos < g;
   const UnitStat s = ust[pos];
   const float mct = scaled_max(s.tm, cc);
-  const double ures = static_cast<double>(sh_ures);
-  const E* trow = tb + (static_cast<size_t>(b) * W + pos) * V;
-  const E* drow = db + (static_cast<size_t>(b) * a.gmax + pos) * V;
-  const bool bulk = geo.bulk != 0;
-  const ResidualW<E> rw{cc, mct, pos < g ? scaled_max(s.dm, cc) : 0.f, pos < g ? s.ts / s.ds : 0.f};
+  const ResidualW<E> rw{cc, mct, residual ? scaled_max(s.dm, cc) : 0.f, residual ? s.ts / s.ds : 0.f};
   const TargetW<E> tw{cc, mct};
-  E* s_t = reinterpret_cast<E*>(dyn_smem);
-  E* s_d = reinterpret_cast<E*>(dyn_smem + static_cast<size_t>(R) * sizeof(E));
+  const double ures = static_cast<double>(unit_draws(a.seed, a.req_base + b, pos).resample);
+  const E* trow = static_cast<const E*>(a.target) + (static_cast<size_t>(b) * W + pos) * V;
+  const E* drow = residual ? static_cast<const E*>(a.draft) + (static_cast<size_t>(b) * a.gmax + pos) * V : nullptr;
+  const bool aligned = geo.bulk != 0;
+  const size_t pi_idx = static_cast<size_t>(b) * W + pi;
+  float* psum = a.psum + pi_idx * NP;
 
-  int chunk_draw = -1;  // streaming chunk of row pos to draw from with target weights
-  if (pos < g) {
-    // Residual pass over this CTA's range of rows pos, staged by one bulk
-    // copy per row; the last range to arrive locates the draw.
-    const int lo = c * R;
-    const int rn = min(R, V - lo);
-    const int nvec = (rn + kVec - 1) / kVec;
-    const size_t pi_idx = static_cast<size_t>(b) * W + pi;
-    const size_t ci = pi_idx * NR + c;
-    const bool ok = stage_rows(trow + lo, drow + lo, rn, bulk, s_t, s_d, &bars[0], &sh_ok);
-    const double cta = block_sums(SmemRows<E>{s_t, s_d}, nvec, rw, sh_blk, a.blocks + ci * kBlocksPerRange);
-    __syncthreads();  // every warp's block sums are written before the release below
-    if (tid == 0) {
-      a.csum[ci] = ok ? cta : NAN;
-      sh_last = ticket_add(a.ticket + pi_idx) == NR - 1;
-    }
-    __syncthreads();
-    if (!sh_last) return;
-    // Every range's sum and block sums, in one round of loads.
-    float* s_blk = reinterpret_cast<float*>(dyn_smem);  // the staged rows are no longer needed
-    for (int k = tid; k < NR * nbr; k += kT2) {
-      const int r = k / nbr, j = k - r * nbr;
-      s_blk[k] = __ldcg(a.blocks + (pi_idx * NR + r) * kBlocksPerRange + j);
-    }
-    if (warp == 0) {
-      double w = 0.0;
-      if (lane < NR) w = __ldcg(a.csum + pi_idx * NR + lane);
-      double incl = w;
+  // This warp's pieces (kPiecesPerWarp, one after the other): their weight
+  // sums, then one arrival for all of them.
+  const int p0 = (c * kW2 + warp) * kPiecesPerWarp;
+  if (p0 >= NP) return;
+  const int pn = min(kPiecesPerWarp, NP - p0);
+  bool last;
+  {
+    float ps[kPiecesPerWarp];
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const double t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += t;
-      }
-      const double tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
-      int owner = -1, tgt = 0;
-      double local = 0.0, prefix = 0.0, total = tot;
-      if (tot > 0.0) {
-        const double target = ures * tot;
-        const unsigned hit = __ballot_sync(0xFFFFFFFFu, lane < NR && w > 0.0 && target < incl);
-        const unsigned posm = __ballot_sync(0xFFFFFFFFu, lane < NR && w > 0.0);
-        owner = hit ? __ffs(hit) - 1 : 31 - __clz(posm);
-        prefix = __shfl_sync(0xFFFFFFFFu, incl - w, owner);
-        local = target - prefix;
-      } else if (tot == 0.0) {
-        // No residual mass: draw from q_pos instead, located by chunk record.
-        locate_target_chunk(a, b * W + pos, s.tm, cc, ures, &owner, &local, &prefix, &total);
-        tgt = 1;
-      }  // NaN: a staging wait ran out (owner stays -1)
-      if (lane == 0) {
-        if (a.stats)
-          a.stats[(static_cast<size_t>(b) * W + pi) * SSD_NSTAT_VERIFY + 6] = static_cast<float>(tot / s.ts);
-        a.ticket[pi_idx] = 0;
-        sh_owner = owner;
-        sh_local = local;
-        sh_prefix = prefix;
-        sh_total = total;
-        sh_target_w = tgt;
-      }
+    for (int j = 0; j < kPiecesPerWarp; ++j) {
+      ps[j] = 0.f;
+      if (j >= pn) continue;
+      const int lo = (p0 + j) * pelems;
+      PieceRows<E> pr;
+      pr.load(trow + lo, drow ? drow + lo : nullptr, min(pelems, V - lo), aligned);
+      ps[j] = warp_sum(residual ? piece_lane_sum(pr, rw) : piece_lane_sum(pr, tw));
     }
-    __syncthreads();
-    if (pos != n) return;
-    if (sh_owner < 0 || !(sh_total > 0.0)) {
-      if (tid == 0) {
-        write_error(a, b);
-        atomicOr(a.status, 1 << SSD_ERR_TIMEOUT);
-      }
-      return;
-    }
-    if (!sh_target_w) {
-      // The owning range's block sums locate the 32-vector block; one scan of
-      // just that block (rows read from L2) finds the token.
-      if (warp == 0) {
-        const int owner = sh_owner;
-        const int olo = owner * R;
-        const int orn = min(R, V - olo);
-        const int onv = (orn + kVec - 1) / kVec;
-        const GlobalRange<E> rg{trow + olo, drow + olo, orn, bulk};
-        double before = 0.0;
-        const ScanHit h = locate_in_rows<E>(s_blk + owner * nbr, (onv + 31) / 32, onv, sh_local, rg, rw, &before);
-        if (lane == 0) {
-          if (h.elem < 0) {
-            write_error(a, b);
-            atomicOr(a.status, 1 << SSD_ERR_TIMEOUT);
-          } else {
-            if (a.stats) {
-              float* st = a.stats + (static_cast<size_t>(b) * W + pos) * SSD_NSTAT_VERIFY;
-              const double e0 = sh_prefix + before + h.edge;
-              st[8] = static_cast<float>(ures - e0 / sh_total);
-              st[9] = static_cast<float>((e0 + static_cast<double>(h.w)) / sh_total - ures);
-            }
-            write_outputs(a, b, n, olo + h.elem, tok_x);
-          }
-        }
-      }
-      return;
-    }
-    chunk_draw = sh_owner;  // q fallback: the owner is a streaming chunk
-  } else {
-    // Bonus draw from q_gamma, by the first range's CTA: the streaming chunk
-    // holding the target comes from the records.
-    if (pos != n || c != 0) return;
-    if (warp == 0) {
-      int owner;
-      double local, prefix, total;
-      locate_target_chunk(a, b * W + pos, s.tm, cc, ures, &owner, &local, &prefix, &total);
-      if (lane == 0) {
-        sh_owner = owner;
-        sh_local = local;
-        sh_prefix = prefix;
-        sh_total = total;
-      }
-    }
-    __syncthreads();
-    if (sh_owner < 0 || !(sh_total > 0.0)) {
-      if (tid == 0) {
-        write_error(a, b);
-        atomicOr(a.status, 1 << SSD_ERR_TIMEOUT);
-      }
-      return;
-    }
-    chunk_draw = sh_owner;
-  }
-
-  // Target-weight draw inside one streaming chunk of row pos: the chunk is
-  // staged, its block sums give the 32-vector block, one scan finds the token.
-  const int draw_lo = chunk_draw * geo.chunk;
-  const int draw_n = min(geo.chunk, V - draw_lo);
-  const int dnv = (draw_n + kVec - 1) / kVec;
-  const bool ok = stage_rows<E>(trow + draw_lo, nullptr, draw_n, bulk, s_t, nullptr, &bars[1], &sh_ok);
-  const SmemRows<E> rows{s_t, nullptr};
-  block_sums(rows, dnv, tw, sh_blk, nullptr);
-  if (warp == 0) {
-    double before = 0.0;
-    const ScanHit h = locate_in_rows<E>(sh_blk, (dnv + 31) / 32, dnv, sh_local, rows, tw, &before);
+    int is_last = 0;
     if (lane == 0) {
-      if (!ok || h.elem < 0) {
-        write_error(a, b);
-        atomicOr(a.status, 1 << SSD_ERR_TIMEOUT);
-      } else {
-        if (a.stats) {
-          float* st = a.stats + (static_cast<size_t>(b) * W + pos) * SSD_NSTAT_VERIFY;
-          const double e0 = sh_prefix + before + h.edge;
-          st[8] = static_cast<float>(ures - e0 / sh_total);
-          st[9] = static_cast<float>((e0 + static_cast<double>(h.w)) / sh_total - ures);
-        }
-        write_outputs(a, b, n, draw_lo + h.elem, tok_x);
-      }
+      for (int j = 0; j < pn; ++j) psum[p0 + j] = ps[j];
+      is_last = ticket_add(a.ticket + pi_idx) == (NP + kPiecesPerWarp - 1) / kPiecesPerWarp - 1;
     }
+    last = __shfl_sync(0xFFFFFFFFu, is_last, 0) != 0;
+  }
+  if (!last) return;
+  __syncwarp();  // the arrival's acquire (lane 0) orders every lane's loads below
+
+  // The last warp: the piece sums in order, the piece holding u * S, then
+  // that piece reloaded and scanned.
+  if (lane == 0) a.ticket[pi_idx] = 0;  // the last arrival of this call: reset for the next
+  RowPieces rp;
+  rp.load(psum, NP, s_pieces[warp]);
+  if (a.stats && residual && lane == 0)
+    a.stats[pi_idx * SSD_NSTAT_VERIFY + 6] = static_cast<float>(rp.total / static_cast<double>(s.ts));
+  if (pos != n) return;
+  if (residual && rp.total > 0.0) {
+    warp_draw_row<E>(a, b, n, pi_idx, rp, ures, trow, drow, aligned, rw, tok_x);
+  } else {
+    // The bonus draw, or a zero residual mass (a rounding corner case): draw
+    // from q_pos.  For the latter this warp first sums the target pieces.
+    if (residual) {
+      for (int q = 0; q < NP; ++q) {
+        const int lo = q * pelems;
+        PieceRows<E> pr;
+        pr.load(trow + lo, nullptr, min(pelems, V - lo), aligned);
+        const float ps = warp_sum(piece_lane_sum(pr, tw));
+        if (lane == 0) psum[q] = ps;
+      }
+      __syncwarp();
+      rp.load(psum, NP, s_pieces[warp]);
+    }
+    warp_draw_row<E>(a, b, n, pi_idx, rp, ures, trow, nullptr, aligned, tw, tok_x);
   }
 }
 
@@ -862,13 +826,12 @@ cudaError_t ensure_smem(const void* fn, int smem_bytes, int* cached) {
 
 template <typename E>
 cudaError_t launch_verify_t(const VerifyArgs& a, int smem_bytes, cudaStream_t stream) {
-  static thread_local int dev_cached = -1, smem1 = -1, smem2 = -1;
+  static thread_local int dev_cached = -1, smem1 = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev != dev_cached) {
     smem1 = -1;
-    smem2 = -1;
     dev_cached = dev;
   }
   e = ensure_smem(reinterpret_cast<const void*>(&stream_kernel<E>), smem_bytes, &smem1);
@@ -886,13 +849,11 @@ cudaError_t launch_verify_t(const VerifyArgs& a, int smem_bytes, cudaStream_t st
   c1.numAttrs = 1;
   e = cudaLaunchKernelEx(&c1, stream_kernel<E>, a);
   if (e != cudaSuccess) return e;
-  e = ensure_smem(reinterpret_cast<const void*>(&sample_kernel<E>), a.geo.smem2, &smem2);
-  if (e != cudaSuccess) return e;
-  const int P = a.debug ? a.gmax + 1 : 1;
+  const int P = a.debug ? a.gmax + 1 : 1;  // position slots of the sampling grid
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.geo.nrange, P, a.B);
+  cfg.gridDim = dim3((a.geo.npiece + kW2 * kPiecesPerWarp - 1) / (kW2 * kPiecesPerWarp), P, a.B);
   cfg.blockDim = dim3(kT2, 1, 1);
-  cfg.dynamicSmemBytes = static_cast<size_t>(a.geo.smem2);
+  cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
