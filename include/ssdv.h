@@ -72,10 +72,11 @@ typedef enum { SSD_BF16 = 0, SSD_F32 = 1 } ssd_dtype;
 #define SSD_NSTAT_VERIFY 10
 #define SSD_NSTAT_SAGUARO 10
 
-/* Bytes of device workspace ssd_verify / ssd_verify_ragged / ssd_debug_rowstats
- * need for a batch of B requests with up to gamma_max draft tokens.  The
- * workspace holds a status word, arrival counters (cleared by every call),
- * per-chunk row statistics and per-range residual sums. */
+/* Bytes of device workspace ssd_verify / ssd_verify_pipelined /
+ * ssd_verify_ragged / ssd_debug_rowstats need for a batch of B requests with
+ * up to gamma_max draft tokens.  The workspace holds a status word and two
+ * halves, used by alternate calls, of arrival counters (cleared by every call),
+ * per-chunk row statistics and per-piece residual sums. */
 size_t ssd_workspace_bytes(int B, int gamma_max);
 
 /* Zero a workspace (asynchronous memset on `stream`).  Zero a workspace once
@@ -107,6 +108,28 @@ ssd_status ssd_verify(const void* target_logits, const void* draft_logits, ssd_d
                       uint64_t seed, int32_t* out_tokens, int32_t* n_accepted, void* workspace,
                       size_t ws_bytes, void* stream);
 
+/* Pipelined verification: ssd_verify for a chain of calls whose inputs are
+ * already complete.  This entry point has no counterpart in the method's
+ * description; it serves a caller that keeps several independent batches in
+ * flight (a round of batch A verified while batch B's next round drafts).
+ *
+ * Same arguments, outputs, numerics and random draws as ssd_verify.  The
+ * difference is ordering: ssd_verify's kernels wait for the previous kernel on
+ * `stream` to complete before they read anything, so a call never overlaps the
+ * previous one.  Here the streaming kernel may start reading this call's
+ * logits while the previous call's sampling kernel still runs, which hides
+ * that kernel's latency.  The caller guarantees that the inputs (logits, draft
+ * tokens) were complete before the previous verification call on `stream`
+ * completed: produced before it in stream order, or resident all along.
+ * Outputs and the workspace are still ordered: every call's outputs are
+ * written after the previous call's, and alternate calls use alternate halves
+ * of the workspace.  Use ssd_verify when the logits come from the kernel just
+ * before the call. */
+ssd_status ssd_verify_pipelined(const void* target_logits, const void* draft_logits, ssd_dtype dtype,
+                                const int32_t* draft_tokens, int B, int gamma, int V, float temperature,
+                                uint64_t seed, int32_t* out_tokens, int32_t* n_accepted, void* workspace,
+                                size_t ws_bytes, void* stream);
+
 /* Verification without a caller workspace.  This entry point has no
  * counterpart in the method's description: it is a packaging variant of
  * ssd_verify for callers that cannot hand over device memory -- a plain C
@@ -120,7 +143,7 @@ ssd_status ssd_verify(const void* target_logits, const void* draft_logits, ssd_d
  * SSD_NOALLOC_SCRATCH_BYTES bytes inside the library, and the call allocates
  * no device memory.  The batch must fit it:
  * ssd_workspace_bytes(B, gamma) <= SSD_NOALLOC_SCRATCH_BYTES, i.e.
- * B * (gamma + 1) <= 949 (B = 64 at gamma <= 13); a larger batch returns
+ * B * (gamma + 1) <= 474 (B = 64 at gamma <= 6); a larger batch returns
  * SSD_ERR_WORKSPACE before anything is launched.
  *
  * The first call on each device (with that device current) looks up the

@@ -56,13 +56,30 @@ WorkspaceLayout workspace_layout(int B, int gmax) {
   WorkspaceLayout L;
   const size_t units = static_cast<size_t>(B) * static_cast<size_t>(gmax + 1);
   L.status = 0;
-  L.ticket = 256;
+  L.half0 = 256;
+  L.ticket = 0;  // offsets within a half
   L.part = round_up(L.ticket + 4 * units, 256);
   L.csum = L.part + units * kMaxChunks * 2 * sizeof(float4);
   L.blocks = L.csum + units * kMaxChunks * sizeof(double);
-  L.total = round_up(L.blocks + units * kMaxChunks * 128 * sizeof(float), 256);
+  L.half_bytes = round_up(L.blocks + units * kMaxChunks * 128 * sizeof(float), 256);
+  L.total = L.half0 + 2 * L.half_bytes;
   return L;
 }
+
+namespace {
+
+// Consecutive calls on one workspace use alternate halves, so a pipelined
+// call's streaming kernel may run while the previous call's sampling kernel
+// reads the other half.  The parity is kept per workspace address on the host.
+std::mutex g_half_mutex;
+std::unordered_map<const void*, unsigned long long> g_half;
+
+int next_half(const void* workspace) {
+  std::lock_guard<std::mutex> lock(g_half_mutex);
+  return static_cast<int>(g_half[workspace]++ & 1ull);
+}
+
+}  // namespace
 
 int max_dynamic_smem() {
   int dev = 0, v = 0;
@@ -134,7 +151,7 @@ namespace {
 ssd_status verify_common(const void* target, const void* draft, ssd_dtype dtype, const int32_t* draft_tokens, int B,
                          int gmax, int V, const int32_t* gamma, const float* temps, float temp_scalar,
                          bool all_greedy, uint64_t seed, int32_t* out_tokens, int32_t* n_accepted, void* workspace,
-                         size_t ws_bytes, float* stats, void* stream) {
+                         size_t ws_bytes, float* stats, void* stream, bool pipelined = false) {
   const int es = esize_of(dtype);
   if (es == 0) return fail(SSD_ERR_DTYPE, "unknown dtype %d", static_cast<int>(dtype));
   if (!target || !out_tokens || !n_accepted || !workspace) return fail(SSD_ERR_NULL, "a required pointer is NULL");
@@ -158,6 +175,12 @@ ssd_status verify_common(const void* target, const void* draft, ssd_dtype dtype,
   if (st != SSD_OK) return st;
   const long long ctas = static_cast<long long>(B) * (gmax + 1) * geo.nchunk;
   if (ctas >= (1LL << 31)) return fail(SSD_ERR_SHAPE, "grid too large");
+  // Pieces per warp of the sampling kernel: two (one wave of small CTAs, the
+  // shortest chain) for a plain call; for a pipelined call enough that the
+  // sampling grid becomes resident while the streaming kernel still runs, so
+  // the next call's streaming kernel can launch early (SSDV_PPW overrides).
+  geo.ppw = env_int("SSDV_PPW", pipelined ? 4 : 2);
+  if (geo.ppw < 1) geo.ppw = 1;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   VerifyArgs a;
   a.target = target;
@@ -173,9 +196,10 @@ ssd_status verify_common(const void* target, const void* draft, ssd_dtype dtype,
   a.out_tokens = out_tokens;
   a.n_accepted = n_accepted;
   a.status = reinterpret_cast<int32_t*>(ws + L.status);
-  a.ticket = reinterpret_cast<int32_t*>(ws + L.ticket);
-  a.part = reinterpret_cast<float4*>(ws + L.part);
-  a.psum = reinterpret_cast<float*>(ws + L.blocks);
+  uint8_t* half = ws + L.half0 + static_cast<size_t>(next_half(workspace)) * L.half_bytes;
+  a.ticket = reinterpret_cast<int32_t*>(half + L.ticket);
+  a.part = reinterpret_cast<float4*>(half + L.part);
+  a.psum = reinterpret_cast<float*>(half + L.blocks);
   a.stats = stats;
   a.debug = stats ? 1 : 0;
   a.geo = geo;
@@ -192,7 +216,7 @@ ssd_status verify_common(const void* target, const void* draft, ssd_dtype dtype,
     VerifyArgs s = a;
     s.B = B - b0 < seg ? B - b0 : seg;
     s.req_base = b0;
-    s.first = b0 == 0 ? 1 : 0;
+    s.first = (b0 == 0 && !pipelined) ? 1 : 0;
     s.target = static_cast<const uint8_t*>(target) + static_cast<size_t>(b0) * W * V * es;
     if (draft) s.draft = static_cast<const uint8_t*>(draft) + static_cast<size_t>(b0) * gmax * V * es;
     if (draft_tokens) s.draft_tokens = draft_tokens + static_cast<size_t>(b0) * gmax;
@@ -275,6 +299,17 @@ ssd_status ssd_verify(const void* target_logits, const void* draft_logits, ssd_d
                        temperature == 0.f, seed, out_tokens, n_accepted, workspace, ws_bytes, nullptr, stream);
 }
 
+ssd_status ssd_verify_pipelined(const void* target_logits, const void* draft_logits, ssd_dtype dtype,
+                                const int32_t* draft_tokens, int B, int gamma, int V, float temperature,
+                                uint64_t seed, int32_t* out_tokens, int32_t* n_accepted, void* workspace,
+                                size_t ws_bytes, void* stream) {
+  g_last_error.clear();
+  if (!temperature_valid(temperature))
+    return fail(SSD_ERR_TEMPERATURE, "temperature %g is not 0 or in [1e-6, inf)", static_cast<double>(temperature));
+  return verify_common(target_logits, draft_logits, dtype, draft_tokens, B, gamma, V, nullptr, nullptr, temperature,
+                       temperature == 0.f, seed, out_tokens, n_accepted, workspace, ws_bytes, nullptr, stream, true);
+}
+
 ssd_status ssd_verify_noalloc(const void* target_logits, const void* draft_logits, ssd_dtype dtype,
                               const int32_t* draft_tokens, int B, int gamma, int V, float temperature, uint64_t seed,
                               int32_t* out_tokens, int32_t* n_accepted, void* stream) {
@@ -287,7 +322,7 @@ ssd_status ssd_verify_noalloc(const void* target_logits, const void* draft_logit
   if (need > SSD_NOALLOC_SCRATCH_BYTES)
     return fail(SSD_ERR_WORKSPACE,
                 "B=%d gamma=%d needs %zu bytes of scratch, above the fixed %u-byte array of ssd_verify_noalloc "
-                "(B*(gamma+1) <= 949); call ssd_verify with a workspace instead",
+                "(B*(gamma+1) <= 474); call ssd_verify with a workspace instead",
                 B, gamma, need, SSD_NOALLOC_SCRATCH_BYTES);
   void* scratch = nullptr;
   const ssd_status st = noalloc_scratch(static_cast<cudaStream_t>(stream), &scratch);

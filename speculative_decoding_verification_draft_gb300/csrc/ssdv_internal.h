@@ -30,6 +30,7 @@ struct ChunkGeometry {
   int row_smem;  // shared-memory bytes per staged row chunk (a multiple of 128)
   int bulk;      // 1: rows 16-byte aligned, staged with bulk async copies
   int npiece;    // pieces (128 vectors) per row, at most kMaxPieces
+  int ppw;       // pieces per warp of the sampling kernel
 };
 constexpr int kMaxChunks = 32;
 constexpr int kMaxPieces = 1024;  // 2^19 fp32 elements / 512
@@ -52,8 +53,9 @@ struct VerifyArgs {
   int32_t* status;             // workspace [1]: device error bits
   float* stats;                // [B, gmax+1, SSD_NSTAT_VERIFY] or null (debug)
   int debug;                   // 1: decide and report every position (statistics)
-  int first;                   // 1: the call's first segment (every streaming CTA waits for the
-                               // previous kernel); 0: a later one (only its first CTA waits)
+  int first;                   // 1: every streaming CTA waits for the previous kernel (the first
+                               // segment of a call); 0: only the first CTA waits (a later segment, or
+                               // a pipelined call)
   ChunkGeometry geo;
 };
 
@@ -70,10 +72,11 @@ struct SaguaroArgs {
 };
 
 // Workspace layout (byte offsets), shared by the launchers and the API: the
-// status word, then the arrival counters (cleared by every call), chunk
-// records, range sums and block sums of the call's shape.
+// status word, then two halves used by alternate calls, each holding the
+// arrival counters (cleared by every call), chunk records and piece sums of
+// the call's shape (ticket .. blocks are offsets within a half).
 struct WorkspaceLayout {
-  size_t status, ticket, part, csum, blocks, total;
+  size_t status, half0, half_bytes, ticket, part, csum, blocks, total;
 };
 WorkspaceLayout workspace_layout(int B, int gmax);
 

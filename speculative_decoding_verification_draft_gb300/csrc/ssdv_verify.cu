@@ -345,8 +345,8 @@ __device__ __forceinline__ int ticket_add(int32_t* p) {
 
 // ---------------------------------------------------------------------------
 // Kernel 2: decisions and the draw, warp by warp.  A piece is 128 vectors
-// (four 32-vector blocks) of a row; a warp takes kPiecesPerWarp consecutive
-// pieces of one draw row and a CTA of kT2 threads kW2 such runs.  Every CTA of
+// (four 32-vector blocks) of a row; a warp takes geo.ppw consecutive pieces
+// of one draw row and a CTA of kT2 threads kW2 such runs.  Every CTA of
 // a request combines the request's records and takes the decisions (identical
 // results); then each warp loads its pieces of row n -- target and draft for a
 // residual draw, target for the bonus draw -- one round of loads per piece,
@@ -357,7 +357,6 @@ __device__ __forceinline__ int ticket_add(int32_t* p) {
 constexpr int kT2 = 128;  // threads of a sampling CTA
 constexpr int kW2 = kT2 / 32;
 constexpr int kPieceVecs = 128;  // vectors per piece: 4 per lane
-constexpr int kPiecesPerWarp = 2;
 
 // A piece's vectors as raw 16-byte words, lane L holding the 4 consecutive
 // vectors 4L .. 4L+3, target and, when gd is given, draft; elements past n
@@ -490,7 +489,7 @@ __device__ __forceinline__ ScanHit scan_piece(const PieceRows<E>& pr, const WFun
 // L's consecutive share first summed by lane L), the lane sums and the row
 // total (fp64 over lanes), valid in every lane.
 struct RowPieces {
-  float* v;  // shared, kMaxPieces
+  float* v;  // shared, np floats
   int per;
   float lane_sum;
   double total;
@@ -574,7 +573,7 @@ __global__ void __launch_bounds__(kT2, 8) sample_kernel(const VerifyArgs a) {
   __shared__ int tok_x[SSD_MAX_GAMMA];
   __shared__ float tok_t[SSD_MAX_GAMMA], tok_d[SSD_MAX_GAMMA];
   __shared__ int sh_n, sh_bad;
-  __shared__ float s_pieces[kW2][kMaxPieces];  // the last warp's copy of its row's piece sums
+  extern __shared__ float s_pieces[];  // [kW2][NP]: the last warp's copy of its row's piece sums
 
   constexpr int kVec = Elem<E>::kVec;
   const ChunkGeometry& geo = a.geo;
@@ -583,6 +582,12 @@ __global__ void __launch_bounds__(kT2, 8) sample_kernel(const VerifyArgs a) {
   const int c = blockIdx.x, pi = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
+  // The next kernel may launch now.  The first CTA of every streaming kernel
+  // waits for this grid to complete before it lets its own dependents launch,
+  // so the next-but-one sampling kernel still starts after this one ends, and
+  // a streaming kernel launched now writes only the other workspace half
+  // (the previous sampling kernel, which used that half, has completed).
+  griddep_launch_dependents();
   const int g = a.gamma ? a.gamma[b] : a.gmax;
   const float T = a.temps ? a.temps[b] : a.temp_scalar;
   const bool bad_gamma = g > a.gmax, bad_temp = !temperature_ok(T);
@@ -618,8 +623,7 @@ __global__ void __launch_bounds__(kT2, 8) sample_kernel(const VerifyArgs a) {
     }
     return;
   }
-  griddep_wait();               // the streaming kernel's records are complete and visible
-  griddep_launch_dependents();  // the next kernel may become resident (it waits for this grid)
+  griddep_wait();  // the streaming kernel's records are complete and visible
 
   // Row statistics of every position of the request, combined from the chunk
   // records (the same butterfly in every CTA: identical results), and the two
@@ -736,28 +740,23 @@ __global__ void __launch_bounds__(kT2, 8) sample_kernel(const VerifyArgs a) {
   const size_t pi_idx = static_cast<size_t>(b) * W + pi;
   float* psum = a.psum + pi_idx * NP;
 
-  // This warp's pieces (kPiecesPerWarp, one after the other): their weight
+  // This warp's pieces (geo.ppw of them, one after the other): their weight
   // sums, then one arrival for all of them.
-  const int p0 = (c * kW2 + warp) * kPiecesPerWarp;
+  const int ppw = geo.ppw;
+  const int p0 = (c * kW2 + warp) * ppw;
   if (p0 >= NP) return;
-  const int pn = min(kPiecesPerWarp, NP - p0);
+  const int pn = min(ppw, NP - p0);
   bool last;
   {
-    float ps[kPiecesPerWarp];
-#pragma unroll
-    for (int j = 0; j < kPiecesPerWarp; ++j) {
-      ps[j] = 0.f;
-      if (j >= pn) continue;
+    for (int j = 0; j < pn; ++j) {
       const int lo = (p0 + j) * pelems;
       PieceRows<E> pr;
       pr.load(trow + lo, drow ? drow + lo : nullptr, min(pelems, V - lo), aligned);
-      ps[j] = warp_sum(residual ? piece_lane_sum(pr, rw) : piece_lane_sum(pr, tw));
+      const float ps = warp_sum(residual ? piece_lane_sum(pr, rw) : piece_lane_sum(pr, tw));
+      if (lane == 0) psum[p0 + j] = ps;
     }
     int is_last = 0;
-    if (lane == 0) {
-      for (int j = 0; j < pn; ++j) psum[p0 + j] = ps[j];
-      is_last = ticket_add(a.ticket + pi_idx) == (NP + kPiecesPerWarp - 1) / kPiecesPerWarp - 1;
-    }
+    if (lane == 0) is_last = ticket_add(a.ticket + pi_idx) == (NP + ppw - 1) / ppw - 1;
     last = __shfl_sync(0xFFFFFFFFu, is_last, 0) != 0;
   }
   if (!last) return;
@@ -767,7 +766,7 @@ __global__ void __launch_bounds__(kT2, 8) sample_kernel(const VerifyArgs a) {
   // that piece reloaded and scanned.
   if (lane == 0) a.ticket[pi_idx] = 0;  // the last arrival of this call: reset for the next
   RowPieces rp;
-  rp.load(psum, NP, s_pieces[warp]);
+  rp.load(psum, NP, s_pieces + warp * NP);
   if (a.stats && residual && lane == 0)
     a.stats[pi_idx * SSD_NSTAT_VERIFY + 6] = static_cast<float>(rp.total / static_cast<double>(s.ts));
   if (pos != n) return;
@@ -785,7 +784,7 @@ __global__ void __launch_bounds__(kT2, 8) sample_kernel(const VerifyArgs a) {
         if (lane == 0) psum[q] = ps;
       }
       __syncwarp();
-      rp.load(psum, NP, s_pieces[warp]);
+      rp.load(psum, NP, s_pieces + warp * NP);
     }
     warp_draw_row<E>(a, b, n, pi_idx, rp, ures, trow, nullptr, aligned, tw, tok_x);
   }
@@ -851,9 +850,9 @@ cudaError_t launch_verify_t(const VerifyArgs& a, int smem_bytes, cudaStream_t st
   if (e != cudaSuccess) return e;
   const int P = a.debug ? a.gmax + 1 : 1;  // position slots of the sampling grid
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((a.geo.npiece + kW2 * kPiecesPerWarp - 1) / (kW2 * kPiecesPerWarp), P, a.B);
+  cfg.gridDim = dim3((a.geo.npiece + kW2 * a.geo.ppw - 1) / (kW2 * a.geo.ppw), P, a.B);
   cfg.blockDim = dim3(kT2, 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = static_cast<size_t>(kW2) * a.geo.npiece * sizeof(float);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -49,6 +49,7 @@ def _declare(lib):
     lib.ssd_verify.argtypes = [P, P, I, P, I, I, I, F, U64, P, P, P, SZ, P]
     lib.ssd_verify_ragged.argtypes = [P, P, I, P, I, I, I, P, P, U64, P, P, P, SZ, P]
     lib.ssd_verify_noalloc.argtypes = [P, P, I, P, I, I, I, F, U64, P, P, P]
+    lib.ssd_verify_pipelined.argtypes = [P, P, I, P, I, I, I, F, U64, P, P, P, SZ, P]
     lib.ssd_saguaro_prespec.argtypes = [P, P, I, I, I, I, I, F, U64, P, P, P]
     lib.ssd_debug_rowstats.argtypes = [P, P, I, P, I, I, I, F, U64, P, P, P, P, SZ, P]
     lib.ssd_debug_saguaro_stats.argtypes = [P, P, I, I, I, I, I, F, U64, P, P, P, P]
@@ -58,8 +59,8 @@ def _declare(lib):
     lib.ssd_status_str.restype = ctypes.c_char_p
     lib.ssd_last_error.argtypes = []
     lib.ssd_last_error.restype = ctypes.c_char_p
-    for name in ("ssd_workspace_init", "ssd_verify", "ssd_verify_noalloc", "ssd_verify_ragged",
-                 "ssd_saguaro_prespec", "ssd_debug_rowstats", "ssd_debug_saguaro_stats", "ssd_read_status",
+    for name in ("ssd_workspace_init", "ssd_verify", "ssd_verify_noalloc", "ssd_verify_pipelined",
+                 "ssd_verify_ragged", "ssd_saguaro_prespec", "ssd_debug_rowstats", "ssd_debug_saguaro_stats", "ssd_read_status",
                  "ssd_debug_uniforms"):
         getattr(lib, name).restype = I
     return lib
@@ -166,6 +167,33 @@ def verify(target: torch.Tensor, draft: Optional[torch.Tensor], draft_tokens: to
                             int(seed) & ((1 << 64) - 1), _dev(out_tokens, "out_tokens", torch.int32),
                             _dev(n_accepted, "n_accepted", torch.int32), _dev(ws, "workspace"),
                             ws.numel(), _stream(stream)))
+    return out_tokens, n_accepted
+
+
+def verify_pipelined(target: torch.Tensor, draft: Optional[torch.Tensor], draft_tokens: torch.Tensor,
+                     temperature: float, seed: int, out_tokens: Optional[torch.Tensor] = None,
+                     n_accepted: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                     stream=None):
+    """ssd_verify_pipelined: ssd_verify for a chain of calls whose inputs were
+    complete before the previous verification call on the stream completed."""
+    B, W, V = target.shape
+    g = W - 1
+    dev = target.device
+    if out_tokens is None:
+        out_tokens = torch.empty(B, W, dtype=torch.int32, device=dev)
+    if n_accepted is None:
+        n_accepted = torch.empty(B, dtype=torch.int32, device=dev)
+    ws = _workspace(B, g, dev, workspace)
+    dptr = _dev(draft, "draft_logits", target.dtype) if draft is not None else None
+    if draft is not None and tuple(draft.shape) != (B, g, V):
+        raise ValueError("draft_logits must be [B, gamma, V]")
+    if tuple(draft_tokens.shape) != (B, g):
+        raise ValueError("draft_tokens must be [B, gamma]")
+    _check(lib().ssd_verify_pipelined(_dev(target, "target_logits"), dptr, _dtype_code(target),
+                                      _dev(draft_tokens, "draft_tokens", torch.int32), B, g, V, float(temperature),
+                                      int(seed) & ((1 << 64) - 1), _dev(out_tokens, "out_tokens", torch.int32),
+                                      _dev(n_accepted, "n_accepted", torch.int32), _dev(ws, "workspace"),
+                                      ws.numel(), _stream(stream)))
     return out_tokens, n_accepted
 
 

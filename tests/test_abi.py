@@ -29,7 +29,8 @@ def lib():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for want in ("ssd_verify", "ssd_verify_ragged", "ssd_saguaro_prespec", "ssd_workspace_bytes",
+    for want in ("ssd_verify", "ssd_verify_pipelined", "ssd_verify_noalloc", "ssd_verify_ragged",
+                 "ssd_saguaro_prespec", "ssd_workspace_bytes",
                  "ssd_workspace_init", "ssd_debug_rowstats", "ssd_debug_saguaro_stats",
                  "ssd_debug_uniforms", "ssd_read_status", "ssd_status_str", "ssd_last_error"):
         assert want in names

@@ -236,9 +236,40 @@ def test_workspace_reuse_and_determinism(ssdv, zipf64):
         r2 = ssdv.verify(b.target, b.draft, b.draft_tokens, 0.8, 5, workspace=ws)
     torch.cuda.synchronize()
     assert torch.equal(r1[0], r2[0]) and torch.equal(r1[1], r2[1])
-    # the arrival counters (after the status word) are back at zero
-    t = ws[256: 256 + 4 * 64 * 5].view(torch.int32)
-    assert int(t.abs().sum()) == 0
+    half = (ssdv.workspace_bytes(64, 4) - 256) // 2  # two halves after the status word
+    for h in range(2):
+        t = ws[256 + h * half: 256 + h * half + 4 * 64 * 5].view(torch.int32)
+        assert int(t.abs().sum()) == 0  # arrival counters back to zero in both halves
+
+
+def test_pipelined_chain_matches_plain_calls(ssdv):
+    """A chain of pipelined calls (inputs resident before the chain) gives the
+    outputs of the same calls made one at a time, also when plain and
+    pipelined calls are mixed on one workspace."""
+    sets = [wl.zipf_batch(16, 4, 40000, seed=70 + k, temperature=0.9).to("cuda") for k in range(4)]
+    ws = ssdv.make_workspace(16, 4)
+    ref = []
+    for k, b in enumerate(sets):
+        o, n = ssdv.verify(b.target, b.draft, b.draft_tokens, 0.9, 100 + k, workspace=ws)
+        torch.cuda.synchronize()
+        ref.append((o.clone(), n.clone()))
+    outs = [(torch.full((16, 5), -9, dtype=torch.int32, device="cuda"),
+             torch.full((16,), -9, dtype=torch.int32, device="cuda")) for _ in range(12)]
+    for r in range(12):  # no synchronisation inside the chain
+        k = r % 4
+        b = sets[k]
+        fn = ssdv.verify if r in (0, 5) else ssdv.verify_pipelined
+        fn(b.target, b.draft, b.draft_tokens, 0.9, 100 + k, outs[r][0], outs[r][1], workspace=ws)
+    torch.cuda.synchronize()
+    for r in range(12):
+        assert torch.equal(outs[r][0], ref[r % 4][0]) and torch.equal(outs[r][1], ref[r % 4][1]), r
+    # the same tensor rewritten by consecutive pipelined calls ends with the last call's outputs
+    o, n = torch.empty(16, 5, dtype=torch.int32, device="cuda"), torch.empty(16, dtype=torch.int32, device="cuda")
+    for k in (0, 1, 2, 3, 0, 1):
+        b = sets[k]
+        ssdv.verify_pipelined(b.target, b.draft, b.draft_tokens, 0.9, 100 + k, o, n, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(o, ref[1][0]) and torch.equal(n, ref[1][1])
 
 
 def test_workspace_shared_across_shapes(ssdv):
