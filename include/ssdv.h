@@ -183,11 +183,20 @@ ssd_status ssd_verify_ragged(const void* target_logits, const void* draft_logits
  *         sqrt(p_D(v) * max(r_j(v), 1e-8)), p_D = p_j (q_gamma at j = gamma).
  *   target_logits [B, gamma+1, V], draft_logits [B, gamma, V];
  *   bonus_topk [B, gamma+1, k] int32, saguaro_tokens [B, gamma+1] int32.
- * Constraints: temperature > 0, 1 <= k <= SSD_MAX_TOPK, k <= V.  No
- * workspace is needed. */
+ *   workspace >= ssd_saguaro_workspace_bytes(B, gamma, V) bytes, zeroed once
+ *   (ssd_workspace_init), 16-byte aligned; its status word reports device
+ *   errors as for verification (ssd_read_status).
+ * Constraints: temperature > 0, 1 <= k <= SSD_MAX_TOPK, k <= V. */
 ssd_status ssd_saguaro_prespec(const void* target_logits, const void* draft_logits, ssd_dtype dtype,
                                int B, int gamma, int V, int k, float temperature, uint64_t seed,
-                               int32_t* bonus_topk, int32_t* saguaro_tokens, void* stream);
+                               int32_t* bonus_topk, int32_t* saguaro_tokens, void* workspace,
+                               size_t ws_bytes, void* stream);
+
+/* Bytes of device workspace ssd_saguaro_prespec / ssd_debug_saguaro_stats
+ * need for B requests, gamma draft tokens and vocabulary V (either dtype): a
+ * status word, arrival counters, per-chunk row statistics, per-piece weight
+ * sums and every warp's top-8 candidates. */
+size_t ssd_saguaro_workspace_bytes(int B, int gamma, int V);
 
 /* Debug / parity: ssd_verify (same arguments and outputs) that also returns
  * the per-position quantities it computes, for every position whether or not
@@ -213,11 +222,12 @@ ssd_status ssd_debug_rowstats(const void* target_logits, const void* draft_logit
  * max(r_j(v), 1e-8)), 4 p_saguaro(token), 5 r_j of top slot 0, 6 r_j of top
  * slot k-1, 7 NaN, 8, 9 the distances u - lo, hi - u of the Saguaro uniform to
  * the normalised CDF boundaries of the drawn token.
- * Outputs as ssd_saguaro_prespec. */
+ * Outputs and workspace as ssd_saguaro_prespec. */
 ssd_status ssd_debug_saguaro_stats(const void* target_logits, const void* draft_logits,
                                    ssd_dtype dtype, int B, int gamma, int V, int k,
                                    float temperature, uint64_t seed, int32_t* bonus_topk,
-                                   int32_t* saguaro_tokens, float* stats, void* stream);
+                                   int32_t* saguaro_tokens, float* stats, void* workspace,
+                                   size_t ws_bytes, void* stream);
 
 /* Debug / parity: the uniforms the kernels draw.  out [B, W, 3] float gets,
  * for request b < B and position i < W, the accept, resample / bonus and

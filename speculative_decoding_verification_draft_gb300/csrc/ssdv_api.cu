@@ -66,6 +66,25 @@ WorkspaceLayout workspace_layout(int B, int gmax) {
   return L;
 }
 
+SagLayout saguaro_layout(int B, int g, int V) {
+  SagLayout L;
+  const size_t units = static_cast<size_t>(B) * static_cast<size_t>(g + 1);
+  // sized for fp32 rows (the most pieces per row) and the fewest pieces per warp
+  const size_t np = (static_cast<size_t>(V) + 511) / 512;
+  const size_t npw = (np + kSagMinPpw - 1) / kSagMinPpw;
+  L.ticket2 = 256;  // after the status word
+  L.ticket3 = round_up(L.ticket2 + 4 * units, 256);
+  L.rowstat = round_up(L.ticket3 + 4 * units, 256);
+  L.rowsum = L.rowstat + units * sizeof(float4);
+  L.part = round_up(L.rowsum + units * sizeof(double), 256);
+  L.psum2 = L.part + units * kMaxChunks * 2 * sizeof(float4);
+  L.psum3 = round_up(L.psum2 + units * np * sizeof(float), 256);
+  L.cand_v = round_up(L.psum3 + units * np * sizeof(float), 256);
+  L.cand_i = round_up(L.cand_v + units * npw * SSD_MAX_TOPK * sizeof(float), 256);
+  L.total = round_up(L.cand_i + units * npw * SSD_MAX_TOPK * sizeof(int32_t), 256);
+  return L;
+}
+
 namespace {
 
 // Consecutive calls on one workspace use alternate halves, so a pipelined
@@ -86,37 +105,6 @@ int max_dynamic_smem() {
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
   return v - 8 * 1024;  // leave room for the kernels' static shared memory
-}
-
-// Split a row of V elements over the CTAs of a cluster.  The default aims at
-// about 32 KB of each staged row per CTA (so two to three CTAs share an SM and
-// one stages while another computes); SSDV_CLUSTER / SSDV_SLICE_BYTES override.
-ssd_status choose_geometry(int V, int esize, bool aligned, bool two_rows, Geometry* geo, int* smem_bytes) {
-  const int max_smem = max_dynamic_smem();
-  if (max_smem <= 0) return fail(SSD_ERR_CUDA, "cannot query the device's shared-memory limit");
-  const long long row_bytes = static_cast<long long>(V) * esize;
-  const int want = env_int("SSDV_SLICE_BYTES", 32 * 1024);
-  int C = env_int("SSDV_CLUSTER", 0);
-  if (C <= 0) C = static_cast<int>((row_bytes + want - 1) / want);
-  C = C < 1 ? 1 : (C > 16 ? 16 : C);
-  for (;; ++C) {
-    if (C > 16)
-      return fail(SSD_ERR_UNSUPPORTED, "V=%d does not fit the shared memory of a 16-CTA cluster", V);
-    const int slice = static_cast<int>(round_up((static_cast<size_t>(V) + C - 1) / C, 8));
-    const int row_smem = static_cast<int>(round_up(static_cast<size_t>(slice) * esize, 128));
-    const int smem = (two_rows ? 2 : 1) * row_smem;
-    const int stage_elems = kStageBytes / esize;
-    const int nstage = (slice + stage_elems - 1) / stage_elems;
-    if (smem > max_smem || nstage > kMaxStages) continue;
-    geo->V = V;
-    geo->slice = slice;
-    geo->csize = (V + slice - 1) / slice;
-    geo->row_smem = row_smem;
-    geo->stage_elems = stage_elems;
-    geo->bulk = aligned ? 1 : 0;
-    *smem_bytes = smem;
-    return SSD_OK;
-  }
 }
 
 // Split a row of V elements into chunks for verification: about 24 KB of each
@@ -282,6 +270,11 @@ size_t ssd_workspace_bytes(int B, int gamma_max) {
   return workspace_layout(B, gamma_max).total;
 }
 
+size_t ssd_saguaro_workspace_bytes(int B, int gamma, int V) {
+  if (B < 1 || gamma < 0 || V < 1) return 0;
+  return saguaro_layout(B, gamma, V).total;
+}
+
 ssd_status ssd_workspace_init(void* workspace, size_t ws_bytes, void* stream) {
   if (!workspace) return fail(SSD_ERR_NULL, "workspace is NULL");
   const cudaError_t e = cudaMemsetAsync(workspace, 0, ws_bytes, static_cast<cudaStream_t>(stream));
@@ -360,62 +353,116 @@ ssd_status ssd_debug_rowstats(const void* target_logits, const void* draft_logit
 
 static ssd_status saguaro_common(const void* target, const void* draft, ssd_dtype dtype, int B, int g, int V, int k,
                                  float temperature, uint64_t seed, int32_t* bonus_topk, int32_t* tokens, float* stats,
-                                 void* stream) {
+                                 void* workspace, size_t ws_bytes, void* stream) {
   const int es = esize_of(dtype);
   if (es == 0) return fail(SSD_ERR_DTYPE, "unknown dtype %d", static_cast<int>(dtype));
-  if (!target || !bonus_topk || !tokens || (g > 0 && !draft)) return fail(SSD_ERR_NULL, "a required pointer is NULL");
+  if (!target || !bonus_topk || !tokens || !workspace || (g > 0 && !draft))
+    return fail(SSD_ERR_NULL, "a required pointer is NULL");
   if (B < 1 || g < 0 || g > SSD_MAX_GAMMA || V < 1 || V > SSD_MAX_V || k < 1 || k > SSD_MAX_TOPK || k > V)
     return fail(SSD_ERR_SHAPE, "bad shape B=%d gamma=%d V=%d k=%d", B, g, V, k);
   if (!(temperature >= 1e-6f) || !isfinite(temperature))
     return fail(SSD_ERR_TEMPERATURE, "Saguaro needs a temperature in [1e-6, inf), got %g",
                 static_cast<double>(temperature));
   if (!aligned_to(target, es) || (draft && !aligned_to(draft, es)) || !aligned_to(bonus_topk, 4) ||
-      !aligned_to(tokens, 4) || (stats && !aligned_to(stats, 4)))
-    return fail(SSD_ERR_ALIGN, "a pointer is not aligned to its element size");
+      !aligned_to(tokens, 4) || (stats && !aligned_to(stats, 4)) || !aligned_to(workspace, 16))
+    return fail(SSD_ERR_ALIGN, "a pointer is not aligned to its element size (workspace: 16 bytes)");
+  const SagLayout L = saguaro_layout(B, g, V);
+  if (ws_bytes < L.total)
+    return fail(SSD_ERR_WORKSPACE, "workspace of %zu bytes < %zu required", ws_bytes, L.total);
   const bool aligned =
       aligned_to(target, 16) && (!draft || aligned_to(draft, 16)) && ((static_cast<size_t>(V) * es) % 16 == 0);
-  Geometry geo;
+  ChunkGeometry geo;
   int smem = 0;
-  ssd_status st = choose_geometry(V, es, aligned, true, &geo, &smem);
+  ssd_status st = choose_chunks(V, es, aligned, &geo, &smem);
   if (st != SSD_OK) return st;
-  if (static_cast<long long>(B) * (g + 1) * geo.csize >= (1LL << 31)) return fail(SSD_ERR_SHAPE, "grid too large");
+  // Pieces per warp of the residual and mix kernels (SSDV_SAG_PPW overrides).
+  geo.ppw = std::max(kSagMinPpw, env_int("SSDV_SAG_PPW", 8));
+  const int npw = (geo.npiece + geo.ppw - 1) / geo.ppw;
+  const int W = g + 1;
+  if (static_cast<long long>(B) * W * geo.nchunk >= (1LL << 31)) return fail(SSD_ERR_SHAPE, "grid too large");
   if (stats) {
-    const size_t n_stats = static_cast<size_t>(B) * (g + 1) * SSD_NSTAT_SAGUARO;
+    const size_t n_stats = static_cast<size_t>(B) * W * SSD_NSTAT_SAGUARO;
     cudaError_t e = cudaMemsetAsync(stats, 0xFF, n_stats * sizeof(float), static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "stats memset");
   }
-  SaguaroArgs a;
-  a.target = target;
-  a.draft = draft;
-  a.B = B;
-  a.g = g;
-  a.k = k;
-  a.temperature = temperature;
-  a.seed = seed;
-  a.bonus_topk = bonus_topk;
-  a.saguaro_tokens = tokens;
-  a.stats = stats;
-  a.geo = geo;
-  const cudaError_t e = launch_saguaro(a, es, smem, static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(e, "saguaro launch");
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* status = reinterpret_cast<int32_t*>(ws);
+  // Segments of requests (SSDV_SAG_SEGMENT; at most 65535, the grid's third
+  // dimension): each runs the streaming, residual and mix kernels on its own
+  // workspace rows; a later segment streams while the previous one finishes.
+  int seg = env_int("SSDV_SAG_SEGMENT", 65535);
+  seg = std::max(1, std::min(seg, 65535));
+  for (int b0 = 0; b0 < B; b0 += seg) {
+    const int nb = B - b0 < seg ? B - b0 : seg;
+    const size_t u0 = static_cast<size_t>(b0) * W;
+    const void* t = static_cast<const uint8_t*>(target) + u0 * V * es;
+    const void* d = draft ? static_cast<const uint8_t*>(draft) + static_cast<size_t>(b0) * g * V * es : nullptr;
+    VerifyArgs v = {};
+    v.target = t;
+    v.draft = d;
+    v.draft_tokens = nullptr;
+    v.B = nb;
+    v.gmax = g;
+    v.req_base = b0;
+    v.gamma = nullptr;
+    v.temps = nullptr;
+    v.temp_scalar = temperature;
+    v.seed = seed;
+    v.part = reinterpret_cast<float4*>(ws + L.part) + u0 * geo.nchunk * 2;
+    v.ticket = reinterpret_cast<int32_t*>(ws + L.ticket2) + u0;  // cleared by the streaming kernel
+    v.status = status;
+    v.stats = nullptr;
+    v.debug = 0;
+    v.first = b0 == 0 ? 1 : 0;
+    v.geo = geo;
+    cudaError_t e = launch_stream(v, es, smem, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "saguaro streaming launch");
+    SagArgs a;
+    a.target = t;
+    a.draft = d;
+    a.B = nb;
+    a.g = g;
+    a.k = k;
+    a.req_base = b0;
+    a.temperature = temperature;
+    a.seed = seed;
+    a.npw = npw;
+    a.bonus_topk = bonus_topk + u0 * k;
+    a.saguaro_tokens = tokens + u0;
+    a.stats = stats ? stats + u0 * SSD_NSTAT_SAGUARO : nullptr;
+    a.part = v.part;
+    a.psum2 = reinterpret_cast<float*>(ws + L.psum2) + u0 * geo.npiece;
+    a.psum3 = reinterpret_cast<float*>(ws + L.psum3) + u0 * geo.npiece;
+    a.cand_v = reinterpret_cast<float*>(ws + L.cand_v) + u0 * npw * SSD_MAX_TOPK;
+    a.cand_i = reinterpret_cast<int32_t*>(ws + L.cand_i) + u0 * npw * SSD_MAX_TOPK;
+    a.rowstat = reinterpret_cast<float4*>(ws + L.rowstat) + u0;
+    a.rowsum = reinterpret_cast<double*>(ws + L.rowsum) + u0;
+    a.ticket2 = v.ticket;
+    a.ticket3 = reinterpret_cast<int32_t*>(ws + L.ticket3) + u0;
+    a.status = status;
+    a.geo = geo;
+    e = launch_saguaro(a, es, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "saguaro launch");
+  }
   return SSD_OK;
 }
 
 ssd_status ssd_saguaro_prespec(const void* target_logits, const void* draft_logits, ssd_dtype dtype, int B, int gamma,
                                int V, int k, float temperature, uint64_t seed, int32_t* bonus_topk,
-                               int32_t* saguaro_tokens, void* stream) {
+                               int32_t* saguaro_tokens, void* workspace, size_t ws_bytes, void* stream) {
   g_last_error.clear();
   return saguaro_common(target_logits, draft_logits, dtype, B, gamma, V, k, temperature, seed, bonus_topk,
-                        saguaro_tokens, nullptr, stream);
+                        saguaro_tokens, nullptr, workspace, ws_bytes, stream);
 }
 
 ssd_status ssd_debug_saguaro_stats(const void* target_logits, const void* draft_logits, ssd_dtype dtype, int B,
                                    int gamma, int V, int k, float temperature, uint64_t seed, int32_t* bonus_topk,
-                                   int32_t* saguaro_tokens, float* stats, void* stream) {
+                                   int32_t* saguaro_tokens, float* stats, void* workspace, size_t ws_bytes,
+                                   void* stream) {
   g_last_error.clear();
   if (!stats) return fail(SSD_ERR_NULL, "stats is NULL");
   return saguaro_common(target_logits, draft_logits, dtype, B, gamma, V, k, temperature, seed, bonus_topk,
-                        saguaro_tokens, stats, stream);
+                        saguaro_tokens, stats, workspace, ws_bytes, stream);
 }
 
 ssd_status ssd_debug_uniforms(uint64_t seed, int B, int W, float* out, void* stream) {

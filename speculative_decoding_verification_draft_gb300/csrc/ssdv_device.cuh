@@ -940,4 +940,233 @@ __device__ __forceinline__ void cdf_search(const Slice<E>& sl, int lo, const WFu
   __syncthreads();
 }
 
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch and arrival counters.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+
+// Arrival counter with acquire-release semantics: the releases of earlier
+// arrivals (their published sums) are visible to the last one.
+__device__ __forceinline__ int ticket_add(int32_t* p) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(p) : "memory");
+  return old;
+}
+
+
+// ---------------------------------------------------------------------------
+// Pieces: 128 vectors of a row, handled by one warp (lane L holds vectors
+// 4L .. 4L+3).  Piece sums, the lane-scan search of a row's pieces and of one
+// piece, used by the sampling passes of verification and Saguaro.
+// ---------------------------------------------------------------------------
+constexpr int kPieceVecs = 128;  // vectors per piece: 4 per lane
+
+// A piece's vectors as raw 16-byte words, lane L holding the 4 consecutive
+// vectors 4L .. 4L+3, target and, when gd is given, draft; elements past n
+// read as -inf (weight 0).  One round of loads.
+template <typename E>
+struct PieceRows {
+  uint4 rt[4], rd[4];
+  __device__ __forceinline__ void load(const E* gt, const E* gd, int n, bool aligned) {
+    constexpr int kVec = Elem<E>::kVec;
+    const int lane = threadIdx.x & 31;
+    const int nv = (n + kVec - 1) / kVec;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int v = 4 * lane + k;
+      rt[k] = rd[k] = Elem<E>::max_init();  // all -inf
+      if (v >= nv) continue;
+      if (aligned) {
+        rt[k] = __ldg(reinterpret_cast<const uint4*>(gt) + v);
+        if (gd) rd[k] = __ldg(reinterpret_cast<const uint4*>(gd) + v);
+      } else {
+        rt[k] = gather_vec(gt, v * kVec, n);
+        if (gd) rd[k] = gather_vec(gd, v * kVec, n);
+      }
+    }
+  }
+  // Elements [i0, i0 + kVec) of a row not aligned to 16 bytes, -inf past n.
+  static __device__ __forceinline__ uint4 gather_vec(const E* g, int i0, int n) {
+    uint32_t w[4];
+    if constexpr (sizeof(E) == 2) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t lo = i0 + 2 * j < n ? static_cast<uint32_t>(g[i0 + 2 * j]) : 0xFF80u;
+        const uint32_t hi = i0 + 2 * j + 1 < n ? static_cast<uint32_t>(g[i0 + 2 * j + 1]) : 0xFF80u;
+        w[j] = lo | (hi << 16);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) w[j] = __float_as_uint(i0 + j < n ? static_cast<float>(g[i0 + j]) : -INFINITY);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  template <typename WFun>
+  __device__ __forceinline__ void weights(int k, const WFun& wfun, float (&w)[Elem<E>::kVec]) const {
+    float xt[Elem<E>::kVec], xd[Elem<E>::kVec];
+    Elem<E>::unpack(rt[k], xt);
+    Elem<E>::unpack(rd[k], xd);
+    wfun(xt, xd, w);
+  }
+};
+
+// The weight sum of a lane's 4 vectors (in vector order).
+template <typename E, typename WFun>
+__device__ __forceinline__ float piece_lane_sum(const PieceRows<E>& pr, const WFun& wfun) {
+  float s = 0.f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float w[Elem<E>::kVec];
+    pr.weights(k, wfun, w);
+    s += pair_sum(w);
+  }
+  return s;
+}
+
+// One warp, one value per lane in index order: the exclusive prefix of every
+// lane (fp64) and the first lane whose running sum passes tl, else the last
+// lane with a positive value (-1 if none).
+__device__ __forceinline__ int lane_locate(double v, double tl, double* before) {
+  const int lane = threadIdx.x & 31;
+  double incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  const unsigned hm = __ballot_sync(0xFFFFFFFFu, v > 0.0 && tl < incl);
+  const unsigned pm = __ballot_sync(0xFFFFFFFFu, v > 0.0);
+  const int L = hm ? __ffs(hm) - 1 : (pm ? 31 - __clz(pm) : -1);
+  *before = __shfl_sync(0xFFFFFFFFu, incl - v, L >= 0 ? L : 0);
+  return L;
+}
+
+// One warp: the element of a loaded piece whose running weight first exceeds
+// tl (relative to the piece start), falling back to the last element with
+// positive weight: a lane scan over the lanes' sums, then the found lane's 4
+// vectors element by element (fp32 from the lane's start: the lane's weight is
+// a small share of the row's).  Returns the element index relative to the
+// piece start (-1 if none), the weight before it and its weight.
+template <typename E, typename WFun>
+__device__ __forceinline__ ScanHit scan_piece(const PieceRows<E>& pr, const WFun& wfun, double tl) {
+  constexpr int kVec = Elem<E>::kVec;
+  const int lane = threadIdx.x & 31;
+  float w[4][kVec];
+  float ls = 0.f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    pr.weights(k, wfun, w[k]);
+    ls += pair_sum(w[k]);
+  }
+  double before = 0.0;
+  const int L = lane_locate(static_cast<double>(ls), tl, &before);
+  if (L < 0) return ScanHit{-1, NAN, 0.f};
+  int el = -1;
+  float edge = 0.f, we = 0.f;
+  if (lane == L) {
+    const float t = static_cast<float>(tl - before);
+    float acc = 0.f;
+    bool done = false;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+#pragma unroll
+      for (int e = 0; e < kVec; ++e) {
+        if (!done && w[k][e] > 0.f) {
+          el = k * kVec + e;  // the hit, or the last positive element so far
+          edge = acc;
+          we = w[k][e];
+          done = t < acc + w[k][e];
+        }
+        acc += w[k][e];
+      }
+    }
+  }
+  el = __shfl_sync(0xFFFFFFFFu, el, L);
+  edge = __shfl_sync(0xFFFFFFFFu, edge, L);
+  we = __shfl_sync(0xFFFFFFFFu, we, L);
+  if (el < 0) return ScanHit{-1, NAN, 0.f};
+  return ScanHit{4 * L * kVec + el, before + static_cast<double>(edge), we};
+}
+
+// One warp: a row's piece sums, copied into the warp's shared slice `v` (lane
+// L's consecutive share first summed by lane L), the lane sums and the row
+// total (fp64 over lanes), valid in every lane.
+struct RowPieces {
+  float* v;  // shared, np floats
+  int per;
+  float lane_sum;
+  double total;
+  __device__ __forceinline__ void load(const float* psum, int np, float* slice) {
+    const int lane = threadIdx.x & 31;
+    v = slice;
+    per = (np + 31) / 32;
+    for (int q = lane; q < np; q += 32) v[q] = __ldcg(psum + q);
+    __syncwarp();
+    lane_sum = 0.f;
+    for (int k = 0; k < per; ++k) {
+      const int q = lane * per + k;
+      if (q < np) lane_sum += v[q];
+    }
+    double t = static_cast<double>(lane_sum);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
+    total = t;
+  }
+};
+
+
+// The element of a row drawn at u * total of the row's piece sums.
+struct RowDraw {
+  int elem;     // element index in the row, -1 if none
+  double edge;  // weight before it (from the row start)
+  float w;      // its weight
+};
+
+// One warp: the lane whose run of pieces holds target = u * total, the piece
+// within that run, then that piece reloaded and scanned (wfun gives the
+// weights; drow may be null).
+template <typename E, typename WFun>
+__device__ __forceinline__ RowDraw warp_locate_row(const RowPieces& rp, double u, const E* trow, const E* drow,
+                                                   int V, bool aligned, const WFun& wfun) {
+  constexpr int kVec = Elem<E>::kVec;
+  const int lane = threadIdx.x & 31;
+  const int pelems = kPieceVecs * kVec;
+  const int np = (V + pelems - 1) / pelems;
+  const double target = u * rp.total;
+  double before = 0.0;
+  const int L = lane_locate(static_cast<double>(rp.lane_sum), target, &before);
+  int owner = -1;
+  float obefore = 0.f;
+  if (lane == L) {
+    const float t = static_cast<float>(target - before);
+    float acc = 0.f;
+    for (int k = 0; k < rp.per; ++k) {
+      const int q = L * rp.per + k;
+      const float w = q < np ? rp.v[q] : 0.f;
+      if (w > 0.f) {
+        owner = q;  // the hit, or the last positive piece so far
+        obefore = acc;
+        if (t < acc + w) break;
+      }
+      acc += w;
+    }
+  }
+  owner = __shfl_sync(0xFFFFFFFFu, owner, L >= 0 ? L : 0);
+  const double owner_before = before + static_cast<double>(__shfl_sync(0xFFFFFFFFu, obefore, L >= 0 ? L : 0));
+  RowDraw d{-1, NAN, 0.f};
+  if (L >= 0 && owner >= 0) {
+    const int olo = owner * pelems;
+    PieceRows<E> pr;
+    pr.load(trow + olo, drow ? drow + olo : nullptr, min(pelems, V - olo), aligned);
+    const ScanHit h = scan_piece(pr, wfun, target - owner_before);
+    if (h.elem >= 0) d = RowDraw{olo + h.elem, owner_before + h.edge, h.w};
+  }
+  return d;
+}
+
 }  // namespace ssdv

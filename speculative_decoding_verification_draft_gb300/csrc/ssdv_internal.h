@@ -10,16 +10,6 @@
 
 namespace ssdv {
 
-// How a unit's rows are split across the CTAs of its cluster.
-struct Geometry {
-  int V;            // vocabulary size
-  int slice;        // elements per CTA slice, a multiple of 8 (16 bytes for bf16 and fp32)
-  int csize;        // CTAs per cluster (1..16)
-  int row_smem;     // shared-memory bytes reserved per staged row slice
-  int stage_elems;  // elements per staged copy (one stage)
-  int bulk;         // 1: rows 16-byte aligned, staged with bulk async copies
-};
-
 // How verification splits each row: the streaming kernel runs one CTA per
 // (request, position, chunk); the sampling kernel one warp per piece (128
 // vectors) of each request's draw row (of every row in the debug mode).
@@ -59,16 +49,31 @@ struct VerifyArgs {
   ChunkGeometry geo;
 };
 
-struct SaguaroArgs {
-  const void* target;  // [B, g+1, V]
-  const void* draft;   // [B, g, V]
+// Saguaro pre-speculation (the residual and mix kernels; the streaming kernel
+// of verification supplies the per-chunk records).  Pointers are offset to
+// the segment of requests this launch covers; unit u = b * (g + 1) + j.
+struct SagArgs {
+  const void* target;       // [B, g+1, V]
+  const void* draft;        // [B, g, V]
   int B, g, k;
+  int req_base;             // request index of row 0 in the Philox counters
   float temperature;
   uint64_t seed;
+  int npw;                  // warps per unit (ceil(npiece / ppw))
   int32_t* bonus_topk;      // [B, g+1, k]
   int32_t* saguaro_tokens;  // [B, g+1]
   float* stats;             // [B, g+1, SSD_NSTAT_SAGUARO] or null
-  Geometry geo;
+  const float4* part;       // workspace [units, nchunk, 2]: the streaming kernel's records
+  float* psum2;             // workspace [units, npiece]: residual (or target) piece sums
+  float* psum3;             // workspace [units, npiece]: Saguaro-weight piece sums
+  float* cand_v;            // workspace [units, npw, 8]: every warp's top-8 weights
+  int32_t* cand_i;          // workspace [units, npw, 8]: and their indices
+  float4* rowstat;          // workspace [units]: target max, target sum, draft max, draft sum
+  double* rowsum;           // workspace [units]: S_j in weight units (NaN: the unit failed)
+  int32_t* ticket2;         // workspace [units]: residual-kernel warps arrived
+  int32_t* ticket3;         // workspace [units]: mix-kernel warps arrived
+  int32_t* status;          // workspace [1]: device error bits
+  ChunkGeometry geo;
 };
 
 // Workspace layout (byte offsets), shared by the launchers and the API: the
@@ -82,13 +87,20 @@ WorkspaceLayout workspace_layout(int B, int gmax);
 
 ssd_status choose_chunks(int V, int esize, bool aligned, ChunkGeometry* geo, int* smem_bytes);
 
-// Launch configuration for one call; returns SSD_OK or an error.
-ssd_status choose_geometry(int V, int esize, bool aligned, bool two_rows, Geometry* geo, int* smem_bytes);
-
 // Streaming statistics kernel followed by the decision / sampling kernel (both
 // with programmatic dependent launch; each waits for its predecessor).
 cudaError_t launch_verify(const VerifyArgs& a, int esize, int smem_bytes, cudaStream_t stream);
-cudaError_t launch_saguaro(const SaguaroArgs& a, int esize, int smem_bytes, cudaStream_t stream);
+// The streaming kernel alone (Saguaro's first kernel).
+cudaError_t launch_stream(const VerifyArgs& a, int esize, int smem_bytes, cudaStream_t stream);
+// Saguaro's residual and mix kernels (each waits for its predecessor).
+cudaError_t launch_saguaro(const SagArgs& a, int esize, cudaStream_t stream);
+
+// Saguaro workspace layout (byte offsets from the workspace start; status at 0).
+struct SagLayout {
+  size_t ticket2, ticket3, rowstat, rowsum, part, psum2, psum3, cand_v, cand_i, total;
+};
+constexpr int kSagMinPpw = 2;  // pieces per warp of the Saguaro kernels, at least
+SagLayout saguaro_layout(int B, int g, int V);
 
 cudaError_t launch_uniforms(uint64_t seed, int B, int W, float* out, cudaStream_t stream);
 

@@ -9,16 +9,21 @@
 // r_j, and one sample from p_saguaro proportional to
 // sqrt(p_D(v) * max(r_j(v), 1e-8)), p_D = p_j (q_gamma at j = gamma).
 //
-// One cluster per (request, j) unit, slices resident in shared memory: the
-// statistics pass reads HBM once; the residual pass (sum and top-k), the mix
-// pass (normaliser) and the inverse-CDF search run on-chip.
+// Three kernels per segment of requests, chained by programmatic dependent
+// launch (each waits for its predecessor before reading its results):
+//  1. the verification streaming kernel: per-chunk (max, sum) records of every
+//     target row and draft row -- one HBM read of every logit;
+//  2. residual_kernel: warps over 128-vector pieces of every unit's rows: the
+//     residual weights (target weights at j = gamma), the pieces' sums and a
+//     top-8 per warp; the last warp of a unit fixes S_j and merges the top-k;
+//  3. mix_kernel: warps over the same pieces: the Saguaro weights, their
+//     piece sums; the last warp of a unit draws the token (and, when S_j = 0,
+//     merges the top-k of q_j instead).
 #include "ssdv_device.cuh"
 
 namespace ssdv {
 
 namespace {
-
-constexpr int kTopK = SSD_MAX_TOPK;  // every unit tracks the top 8; the first k are written
 
 template <typename E>
 struct PassAW {  // residual (scaled by Z_t) or target weights
@@ -62,251 +67,336 @@ struct MixW {
   }
 };
 
+
+constexpr int kS = 128;  // threads of a residual / mix CTA
+constexpr int kSW = kS / 32;
+constexpr int kTopK = SSD_MAX_TOPK;  // every warp tracks the top 8; the first k are written
+
+// Row statistics of unit u from its chunk records (one warp; lanes < NC hold
+// a record each), valid in every lane: target and draft (max, sum).
+__device__ __forceinline__ void unit_stats(const SagArgs& a, size_t u, float c, MaxSum* t, MaxSum* d, int* err) {
+  const int lane = threadIdx.x & 31, NC = a.geo.nchunk;
+  MaxSum tt{-INFINITY, 0.f}, dd{-INFINITY, 0.f};
+  ArgMax am{-INFINITY, -1};
+  int e = 0;
+  if (lane < NC) {
+    const float4* rec = a.part + (u * NC + lane) * 2;
+    const float4 r0 = __ldcg(rec), r1 = __ldcg(rec + 1);
+    tt = MaxSum{r0.x, r0.y};
+    dd = MaxSum{r0.z, r0.w};
+    e = __float_as_int(r1.z);
+  }
+  butterfly_stats(tt, dd, am, e, c);
+  *t = tt;
+  *d = dd;
+  *err = e;
+}
+
+// One warp: the k best of n candidates (value, index), descending, the lower
+// index first among equal values; every lane gets the list.  Candidates are
+// distinct, so each round takes the best one ranking after the previous pick.
+__device__ __forceinline__ void merge_candidates(const float* cv, const int* ci, int n, int k, float* ov, int* oi) {
+  const int lane = threadIdx.x & 31;
+  float lv = INFINITY;
+  int li = -1;
+  for (int s = 0; s < k; ++s) {
+    float bv = -1.f;
+    int bi = 0x7FFFFFFF;
+    for (int q = lane; q < n; q += 32) {
+      const float v = cv[q];
+      const int i = ci[q];
+      if (i == 0x7FFFFFFF || !ranks_before(lv, li, v, i)) continue;  // taken already, or empty
+      if (ranks_before(v, i, bv, bi)) {
+        bv = v;
+        bi = i;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float v2 = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
+      const int i2 = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+      if (ranks_before(v2, i2, bv, bi)) {
+        bv = v2;
+        bi = i2;
+      }
+    }
+    ov[s] = bv;
+    oi[s] = bi;
+    lv = bv;
+    li = bi;
+  }
+}
+
+// This warp's pieces: weight sums into psum, top-8 into the unit's candidate
+// slots (when tk is wanted).  Returns true in the last warp of the unit to
+// arrive (every lane), after which the other warps' sums are visible.
+template <typename E, typename WFun, bool kTop>
+__device__ __forceinline__ bool unit_pieces(const SagArgs& a, size_t u, int wi, const E* trow, const E* drow,
+                                            const WFun& wfun, float* psum, int32_t* ticket) {
+  constexpr int kVec = Elem<E>::kVec;
+  const int lane = threadIdx.x & 31;
+  const int V = a.geo.V, NP = a.geo.npiece, ppw = a.geo.ppw;
+  const int pelems = kPieceVecs * kVec;
+  const int p0 = wi * ppw;
+  const int pn = min(ppw, NP - p0);
+  TopK<kTopK> tk;
+  tk.init();
+  for (int j = 0; j < pn; ++j) {
+    const int lo = (p0 + j) * pelems;
+    PieceRows<E> pr;
+    pr.load(trow + lo, drow ? drow + lo : nullptr, min(pelems, V - lo), a.geo.bulk != 0);
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float w[kVec];
+      pr.weights(k, wfun, w);
+      s += pair_sum(w);
+      if constexpr (kTop) {
+        const int base = lo + (4 * lane + k) * kVec;
+#pragma unroll
+        for (int e = 0; e < kVec; ++e)
+          if (base + e < V) tk.push(w[e], base + e);
+      }
+    }
+    s = warp_sum(s);
+    if (lane == 0) psum[u * NP + p0 + j] = s;
+  }
+  if constexpr (kTop) {
+    float mv[kTopK];
+    int mi[kTopK];
+    warp_merge_topk<kTopK>(tk, mv, mi);
+    if (lane < kTopK) {
+      float v = mv[0];
+      int i = mi[0];
+#pragma unroll
+      for (int r = 1; r < kTopK; ++r)
+        if (lane == r) {
+          v = mv[r];
+          i = mi[r];
+        }
+      a.cand_v[(u * a.npw + wi) * kTopK + lane] = v;
+      a.cand_i[(u * a.npw + wi) * kTopK + lane] = i;
+    }
+  }
+  int is_last = 0;
+  if (lane == 0) is_last = ticket_add(ticket + u) == a.npw - 1;
+  const bool last = __shfl_sync(0xFFFFFFFFu, is_last, 0) != 0;
+  if (last) __syncwarp();  // the arrival's acquire (lane 0) orders every lane's loads after it
+  return last;
+}
+
+// The last warp of a unit: its top-k from the warps' candidates (copied to
+// shared memory first) into bonus_topk, and the statistics of slots 0 and k-1
+// (weights over `total`).
+__device__ __forceinline__ void write_topk(const SagArgs& a, size_t u, double total, float* s_cv, int* s_ci,
+                                          float* st) {
+  const int lane = threadIdx.x & 31;
+  const int n = a.npw * kTopK;
+  for (int q = lane; q < n; q += 32) {
+    s_cv[q] = __ldcg(a.cand_v + u * n + q);
+    s_ci[q] = __ldcg(a.cand_i + u * n + q);
+  }
+  __syncwarp();
+  float ov[kTopK];
+  int oi[kTopK];
+  merge_candidates(s_cv, s_ci, n, a.k, ov, oi);
+  if (lane == 0) {
+    int32_t* out = a.bonus_topk + u * a.k;
+    for (int s = 0; s < a.k; ++s) out[s] = (oi[s] >= 0 && oi[s] < a.geo.V) ? oi[s] : -1;
+    if (st) {
+      st[5] = static_cast<float>(static_cast<double>(ov[0]) / total);
+      st[6] = static_cast<float>(static_cast<double>(ov[a.k - 1]) / total);
+    }
+  }
+}
+
 }  // namespace
 
+// ---------------------------------------------------------------------------
+// Kernel 2: residual sums and top-k.  Grid (warp groups, j, request).
+// ---------------------------------------------------------------------------
 template <typename E>
-__global__ void __launch_bounds__(kThreads) saguaro_kernel(const SaguaroArgs a) {
-  constexpr int kVec = Elem<E>::kVec;
-  extern __shared__ __align__(128) uint8_t dyn_smem[];
-  __shared__ __align__(8) uint64_t bars[kMaxStages];
-  __shared__ __align__(8) uint64_t xbar[kNumX];
-  __shared__ __align__(16) Inbox inbox;
-  __shared__ __align__(16) float cta_top_v[kTopK];
-  __shared__ __align__(16) int cta_top_i[kTopK];
-  __shared__ float red_f[5 * kWarps];
-  __shared__ int red_i[2 * kWarps];
-  __shared__ float wsum[kWarps];
-  __shared__ float wtop_v[kWarps][kTopK];
-  __shared__ int wtop_i[kWarps][kTopK];
-  __shared__ int sh_warp, sh_result, sh_owner, sh_err;
-  __shared__ double sh_base, sh_local, sh_total, sh_prefix, sh_edge;
-  __shared__ float sh_edge_w;
-  __shared__ float sh_mt, sh_zt, sh_md, sh_zd;
-
-  const Geometry& geo = a.geo;
-  const int V = geo.V;
-  const int C = geo.csize;
-  const int rank = static_cast<int>(cluster_rank());
-  const int unit = blockIdx.x / C;
-  const int W = a.g + 1;
-  const int b = unit / W;
-  const int j = unit % W;
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
-
+__global__ void __launch_bounds__(kS) residual_kernel(const SagArgs a) {
+  extern __shared__ __align__(16) uint8_t dyn_smem[];
+  __shared__ float4 sh_stats;
+  __shared__ int sh_err;
+  griddep_launch_dependents();  // the mix kernel may become resident (it waits for this grid)
+  const int W = a.g + 1, j = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wi = blockIdx.x * kSW + warp;
+  const size_t u = static_cast<size_t>(b) * W + j;
   const bool bonus = (j == a.g);
-  const size_t trow = (static_cast<size_t>(b) * W + j) * V;
-  const size_t drow = (static_cast<size_t>(b) * a.g + j) * V;
-  const int lo = rank * geo.slice;
-  const int n = max(0, min(geo.slice, V - lo));
-
-  Slice<E> sl;
-  sl.gt = static_cast<const E*>(a.target) + trow + lo;
-  sl.gd = bonus ? nullptr : static_cast<const E*>(a.draft) + drow + lo;
-  sl.st = reinterpret_cast<E*>(dyn_smem);
-  sl.sd = reinterpret_cast<E*>(dyn_smem + geo.row_smem);
-  sl.n = n;
-  sl.nvec = (n + kVec - 1) / kVec;
-  sl.nstage = (n + geo.stage_elems - 1) / geo.stage_elems;
-  sl.bulk = geo.bulk != 0;
-
-  if (tid == 0) inbox_init(xbar, C, rank == 0);
   const float c = kLog2e / a.temperature;
-  stage_issue(sl, bars, geo.stage_elems);
-  cluster_arrive_release();
-  const ThreadStats<E> ts = stats_pass(sl, bars, geo.stage_elems / kVec, c, true, false, lo);
-  const BlockStats bs = block_reduce_stats(ts, c, red_f, red_i);
-  cluster_wait_acquire();
-  const float u_sag = unit_draws(a.seed, b, j).saguaro;
-  const size_t out_idx = static_cast<size_t>(b) * W + j;
-  float* st = (a.stats && rank == 0) ? a.stats + out_idx * SSD_NSTAT_SAGUARO : nullptr;
+  griddep_wait();  // the streaming kernel's records are complete and visible
   if (warp == 0) {
-    push_stats(&inbox, xbar, C, rank, bs);
-    const BlockStats all = gather_stats(&inbox, xbar, C, c);
-    if (tid == 0) {
-      sh_mt = all.t.m;
-      sh_zt = all.t.s;
-      sh_md = all.d.m;
-      sh_zd = all.d.s;
-      sh_err = all.timeout;
-      if (st) {
-        st[0] = logf(all.t.s) - fmaf(all.t.m, c, -scaled_max(all.t.m, c)) * 0.6931471805599453f;
-        st[1] = bonus ? NAN : logf(all.d.s) - fmaf(all.d.m, c, -scaled_max(all.d.m, c)) * 0.6931471805599453f;
-        st[7] = NAN;
-      }
+    MaxSum t, d;
+    int err;
+    unit_stats(a, u, c, &t, &d, &err);
+    if (lane == 0) {
+      sh_stats = make_float4(t.m, t.s, d.m, d.s);
+      sh_err = err;
     }
   }
   __syncthreads();
+  if (wi >= a.npw) return;
+  const float4 s4 = sh_stats;
+  const int V = a.geo.V;
+  const E* trow = static_cast<const E*>(a.target) + u * V;
+  const E* drow = bonus ? nullptr : static_cast<const E*>(a.draft) + (static_cast<size_t>(b) * a.g + j) * V;
+  const PassAW<E> wf{c, scaled_max(s4.x, c), bonus ? 0.f : scaled_max(s4.z, c), bonus ? 0.f : s4.y / s4.w,
+                     bonus ? 1 : 0};
+  if (!unit_pieces<E, PassAW<E>, true>(a, u, wi, trow, drow, wf, a.psum2, a.ticket2)) return;
 
-  const float mct = scaled_max(sh_mt, c);
-  const float mcd = bonus ? 0.f : scaled_max(sh_md, c);
-  const float kr = bonus ? 0.f : sh_zt / sh_zd;
+  // The last warp: S_j, and the top-k unless the residual is empty (then the
+  // mix kernel takes the top-k of q_j).
+  RowPieces rp;
+  float* s_pieces = reinterpret_cast<float*>(dyn_smem) + warp * a.geo.npiece;
+  rp.load(a.psum2 + u * a.geo.npiece, a.geo.npiece, s_pieces);
+  const double S = rp.total;
+  float* st = a.stats ? a.stats + u * SSD_NSTAT_SAGUARO : nullptr;
+  const int err = sh_err;
+  if (lane == 0) {
+    a.rowstat[u] = s4;
+    a.rowsum[u] = err ? NAN : S;
+    a.ticket3[u] = 0;  // the mix kernel's counter starts at zero (read after this grid completes)
+    if (err) {
+      // a staging wait of the streaming kernel ran out: this unit's outputs are -1
+      atomicOr(a.status, 1 << SSD_ERR_TIMEOUT);
+      for (int s = 0; s < a.k; ++s) a.bonus_topk[u * a.k + s] = -1;
+      a.saguaro_tokens[u] = -1;
+    } else if (st) {
+      st[0] = logf(s4.y) - fmaf(s4.x, c, -scaled_max(s4.x, c)) * 0.6931471805599453f;
+      st[1] = bonus ? NAN : logf(s4.w) - fmaf(s4.z, c, -scaled_max(s4.z, c)) * 0.6931471805599453f;
+      st[2] = bonus ? 1.f : static_cast<float>(S / static_cast<double>(s4.y));
+    }
+  }
+  if (!err && (bonus || S > 0.0)) {
+    __syncwarp();
+    float* s_cv = reinterpret_cast<float*>(dyn_smem) + kSW * a.geo.npiece;
+    int* s_ci = reinterpret_cast<int*>(s_cv + a.npw * kTopK);
+    write_topk(a, u, S, s_cv, s_ci, st);
+  }
+}
 
-  // Pass A: residual weights (or q at the bonus position / on zero residual
-  // mass), their cluster sum, and this CTA's top-8.
-  int target_only = bonus ? 1 : 0;
-  int p = 0;
-  double sum_a = 0.0, resid_mass = 1.0;
-  for (;;) {
+// ---------------------------------------------------------------------------
+// Kernel 3: the Saguaro mix and its draw.  Grid as kernel 2.
+// ---------------------------------------------------------------------------
+template <typename E>
+__global__ void __launch_bounds__(kS) mix_kernel(const SagArgs a) {
+  extern __shared__ __align__(16) uint8_t dyn_smem[];
+  griddep_launch_dependents();  // the next kernel may become resident (it waits for this grid)
+  const int W = a.g + 1, j = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wi = blockIdx.x * kSW + warp;
+  if (wi >= a.npw) return;
+  const size_t u = static_cast<size_t>(b) * W + j;
+  const bool bonus = (j == a.g);
+  const float c = kLog2e / a.temperature;
+  griddep_wait();  // the residual kernel's sums are complete and visible
+  const float4 s4 = __ldcg(a.rowstat + u);
+  const double S = __ldcg(a.rowsum + u);
+  if (isnan(S)) return;  // the unit failed; the residual kernel wrote its -1 outputs
+  const bool target_only = bonus || !(S > 0.0);  // r = q_j: the bonus position or an empty residual
+  const double sum_a = (bonus || S > 0.0) ? S : static_cast<double>(s4.y);
+  const int V = a.geo.V;
+  const E* trow = static_cast<const E*>(a.target) + u * V;
+  const E* drow = bonus ? nullptr : static_cast<const E*>(a.draft) + (static_cast<size_t>(b) * a.g + j) * V;
+  const float mct = scaled_max(s4.x, c), mcd = bonus ? 0.f : scaled_max(s4.z, c);
+  const MixW<E> mw{c, mct, mcd, bonus ? 0.f : s4.y / s4.w, target_only ? 1 : 0, bonus ? 1 : 0,
+                   static_cast<float>(1.0 / sum_a), bonus ? 1.f / s4.y : 1.f / s4.w};
+  const bool fallback = !bonus && !(S > 0.0);  // empty residual: the top-k of q_j is taken here
+  const bool last = unit_pieces<E, MixW<E>, false>(a, u, wi, trow, drow, mw, a.psum3, a.ticket3);
+  if (!last) return;
+
+  // The last warp: Zs, the draw, and (empty residual) the top-k of q_j.
+  RowPieces rp;
+  float* s_pieces = reinterpret_cast<float*>(dyn_smem) + warp * a.geo.npiece;
+  rp.load(a.psum3 + u * a.geo.npiece, a.geo.npiece, s_pieces);
+  const float u_sag = unit_draws(a.seed, a.req_base + b, j).saguaro;
+  const RowDraw d = warp_locate_row<E>(rp, static_cast<double>(u_sag), trow, drow, V, a.geo.bulk != 0, mw);
+  float* st = a.stats ? a.stats + u * SSD_NSTAT_SAGUARO : nullptr;
+  if (lane == 0) {
+    const bool ok = d.elem >= 0 && rp.total > 0.0;
+    a.saguaro_tokens[u] = ok ? d.elem : -1;
+    if (!ok) atomicOr(a.status, 1 << SSD_ERR_TIMEOUT);
+    if (st && ok) {
+      st[3] = static_cast<float>(rp.total);
+      st[4] = static_cast<float>(static_cast<double>(d.w) / rp.total);
+      st[8] = static_cast<float>(static_cast<double>(u_sag) - d.edge / rp.total);
+      st[9] = static_cast<float>((d.edge + static_cast<double>(d.w)) / rp.total - static_cast<double>(u_sag));
+    }
+  }
+  if (fallback) {
+    // Empty residual: r_j = q_j, whose top-k is the top-k of the target
+    // logits.  This warp scans the row once (a rare corner case).
     TopK<kTopK> tk;
     tk.init();
-    const PassAW<E> wf{c, mct, mcd, kr, target_only};
-    const double cta = weighted_pass<E, kTopK>(sl, lo, wf, wsum, tk);
+    const int pelems = kPieceVecs * Elem<E>::kVec;
+    const PassAW<E> tw{c, mct, 0.f, 0.f, 1};
+    for (int q = 0; q < a.geo.npiece; ++q) {
+      const int lo = q * pelems;
+      PieceRows<E> pr;
+      pr.load(trow + lo, nullptr, min(pelems, V - lo), a.geo.bulk != 0);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        float w[Elem<E>::kVec];
+        pr.weights(k, tw, w);
+        const int base = lo + (4 * lane + k) * Elem<E>::kVec;
+#pragma unroll
+        for (int e = 0; e < Elem<E>::kVec; ++e)
+          if (base + e < V) tk.push(w[e], base + e);
+      }
+    }
     float mv[kTopK];
     int mi[kTopK];
     warp_merge_topk<kTopK>(tk, mv, mi);
     if (lane == 0) {
-#pragma unroll
-      for (int r = 0; r < kTopK; ++r) {
-        wtop_v[warp][r] = mv[r];
-        wtop_i[warp][r] = mi[r];
+      int32_t* out = a.bonus_topk + u * a.k;
+      for (int s = 0; s < a.k; ++s) out[s] = (mi[s] >= 0 && mi[s] < V) ? mi[s] : -1;
+      if (st) {
+        st[5] = static_cast<float>(static_cast<double>(mv[0]) / static_cast<double>(s4.y));
+        st[6] = static_cast<float>(static_cast<double>(mv[a.k - 1]) / static_cast<double>(s4.y));
       }
     }
-    __syncthreads();
-    if (warp == 0) {
-      if (tid == 0) {
-        int head[kWarps] = {0};
-        for (int r = 0; r < kTopK; ++r) {
-          int best = -1;
-          for (int w = 0; w < kWarps; ++w) {
-            if (head[w] >= kTopK) continue;
-            if (best < 0 || ranks_before(wtop_v[w][head[w]], wtop_i[w][head[w]], wtop_v[best][head[best]],
-                                         wtop_i[best][head[best]]))
-              best = w;
-          }
-          cta_top_v[r] = wtop_v[best][head[best]];
-          cta_top_i[r] = wtop_i[best][head[best]];
-          ++head[best];
-        }
-      }
-      push_sum(&inbox, xbar, C, rank, p, cta);
-      int owner, to = 0;
-      double local, prefix;
-      const double total = gather_sums(&inbox, xbar, C, p, 0.5, &owner, &local, &prefix, &to);
-      if (tid == 0) {
-        sh_total = total;
-        sh_err |= to;
-      }
-    }
-    __syncthreads();
-    if (p == 0 && !bonus) resid_mass = sh_total / static_cast<double>(sh_zt);
-    if (!(sh_total > 0.0) && !target_only) {
-      target_only = 1;
-      ++p;
-      continue;
-    }
-    sum_a = sh_total;
-    break;
   }
-
-  // Bonus prediction: every CTA sends its top-8 to rank 0, which merges them.
-  if (tid == 0) {
-    const uint32_t bar = dsmem_addr(&xbar[kXTop], 0);
-    const float4* v4 = reinterpret_cast<const float4*>(cta_top_v);
-    const float4* i4 = reinterpret_cast<const float4*>(cta_top_i);
-    st_async_v4(dsmem_addr(&inbox.top[rank][0], 0), v4[0], bar);
-    st_async_v4(dsmem_addr(&inbox.top[rank][1], 0), v4[1], bar);
-    st_async_v4(dsmem_addr(&inbox.top[rank][2], 0), i4[0], bar);
-    st_async_v4(dsmem_addr(&inbox.top[rank][3], 0), i4[1], bar);
-  }
-  if (rank == 0 && tid == 0) {
-    if (!xbar_wait_bounded(&xbar[kXTop])) sh_err = 1;
-    int head[kMaxCluster];
-    for (int r = 0; r < C; ++r) head[r] = 0;
-    int32_t* out = a.bonus_topk + out_idx * a.k;
-    for (int s = 0; s < a.k; ++s) {
-      int best = -1;
-      float bv = 0.f;
-      int bi = 0;
-      for (int r = 0; r < C; ++r) {
-        if (head[r] >= a.k) continue;
-        const float* tv = reinterpret_cast<const float*>(&inbox.top[r][0]);
-        const int* ti = reinterpret_cast<const int*>(&inbox.top[r][2]);
-        if (best < 0 || ranks_before(tv[head[r]], ti[head[r]], bv, bi)) {
-          best = r;
-          bv = tv[head[r]];
-          bi = ti[head[r]];
-        }
-      }
-      ++head[best];
-      out[s] = (bi >= 0 && bi < V && !sh_err) ? bi : -1;
-      if (st && s == 0) st[5] = static_cast<float>(bv / sum_a);
-      if (st && s == a.k - 1) st[6] = static_cast<float>(bv / sum_a);
-    }
-    if (st) st[2] = static_cast<float>(resid_mass);
-  }
-
-  // Saguaro mix pass and its inverse-CDF draw.
-  const MixW<E> mw{c, mct, mcd, kr, target_only, bonus ? 1 : 0, static_cast<float>(1.0 / sum_a),
-                   bonus ? 1.f / sh_zt : 1.f / sh_zd};
-  {
-    TopK<0> none;
-    const double cta = weighted_pass<E, 0>(sl, lo, mw, wsum, none);
-    if (warp == 0) {
-      push_sum(&inbox, xbar, C, rank, 2, cta);
-      int owner, to = 0;
-      double local, prefix;
-      const double total = gather_sums(&inbox, xbar, C, 2, static_cast<double>(u_sag), &owner, &local, &prefix, &to);
-      if (tid == 0) {
-        sh_total = total;
-        sh_owner = owner;
-        sh_local = local;
-        sh_prefix = prefix;
-        sh_err |= to;
-      }
-    }
-    __syncthreads();
-  }
-  if (sh_owner == rank) {
-    cdf_search(sl, lo, mw, wsum, sh_local, &sh_warp, &sh_base, &sh_result, &sh_edge, &sh_edge_w);
-    if (tid == 0) a.saguaro_tokens[out_idx] = sh_err ? -1 : sh_result;
-    if (a.stats && tid == 0 && sh_result >= lo) {
-      // p_saguaro of the drawn token (debug statistics only)
-      const int v = (sh_result - lo) / kVec, e = (sh_result - lo) % kVec;
-      float xt[kVec], xd[kVec], w[kVec];
-      load_vec(sl.st, v, xt);
-      if (sl.gd) load_vec(sl.sd, v, xd);
-      mw(xt, xd, w);
-      float* st0 = a.stats + out_idx * SSD_NSTAT_SAGUARO;
-      st0[3] = static_cast<float>(sh_total);
-      st0[4] = static_cast<float>(w[e] / sh_total);
-      st0[8] = static_cast<float>(static_cast<double>(u_sag) - (sh_prefix + sh_edge) / sh_total);
-      st0[9] = static_cast<float>((sh_prefix + sh_edge + static_cast<double>(sh_edge_w)) / sh_total -
-                                  static_cast<double>(u_sag));
-    }
-  } else if (sh_owner < 0 && rank == 0 && tid == 0) {
-    a.saguaro_tokens[out_idx] = -1;
-  }
-  if (sh_err) stage_drain(sl, bars);
 }
 
-template __global__ void saguaro_kernel<uint16_t>(const SaguaroArgs);
-template __global__ void saguaro_kernel<float>(const SaguaroArgs);
+template __global__ void residual_kernel<uint16_t>(const SagArgs);
+template __global__ void residual_kernel<float>(const SagArgs);
+template __global__ void mix_kernel<uint16_t>(const SagArgs);
+template __global__ void mix_kernel<float>(const SagArgs);
 
-cudaError_t launch_saguaro(const SaguaroArgs& a, int esize, int smem_bytes, cudaStream_t stream) {
-  const void* fn = esize == 2 ? reinterpret_cast<const void*>(&saguaro_kernel<uint16_t>)
-                              : reinterpret_cast<const void*>(&saguaro_kernel<float>);
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
-  if (e != cudaSuccess) return e;
-  if (a.geo.csize > 8) {
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+namespace {
+
+template <typename E>
+cudaError_t launch_saguaro_t(const SagArgs& a, cudaStream_t stream) {
+  const int smem = static_cast<int>(sizeof(float) * (kSW * a.geo.npiece) + 8 * a.npw * kTopK);
+  if (smem > 48 * 1024) {
+    cudaError_t e =
+        cudaFuncSetAttribute(reinterpret_cast<const void*>(&residual_kernel<E>), cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&mix_kernel<E>), cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
   }
-  const long long units = static_cast<long long>(a.B) * (a.g + 1);
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(units * a.geo.csize), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
+  cfg.gridDim = dim3((a.npw + kSW - 1) / kSW, a.g + 1, a.B);
+  cfg.blockDim = dim3(kS, 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = a.geo.csize;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
+  cfg.attrs = pdl;
   cfg.numAttrs = 1;
-  if (esize == 2) return cudaLaunchKernelEx(&cfg, saguaro_kernel<uint16_t>, a);
-  return cudaLaunchKernelEx(&cfg, saguaro_kernel<float>, a);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, residual_kernel<E>, a);
+  if (e != cudaSuccess) return e;
+  return cudaLaunchKernelEx(&cfg, mix_kernel<E>, a);
+}
+
+}  // namespace
+
+cudaError_t launch_saguaro(const SagArgs& a, int esize, cudaStream_t stream) {
+  return esize == 2 ? launch_saguaro_t<uint16_t>(a, stream) : launch_saguaro_t<float>(a, stream);
 }
 
 }  // namespace ssdv

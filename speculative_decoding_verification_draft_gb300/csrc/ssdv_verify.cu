@@ -40,11 +40,6 @@ namespace ssdv {
 
 namespace {
 
-__device__ __forceinline__ void griddep_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
 __device__ __forceinline__ bool temperature_ok(float T) { return T == 0.f || (T >= 1e-6f && T <= 3.0e38f); }
 
 // Residual weights scaled by Z_t: w = max(e_t - (Z_t/Z_d) e_d, 0) with
@@ -172,7 +167,8 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const VerifyArgs a) {
   sl.sd = reinterpret_cast<E*>(dyn_smem + geo.row_smem);
   // the draft token of this position: if it falls in this chunk, the record
   // carries its two logits for the accept test
-  const int x = (has_draft && tid == 0) ? a.draft_tokens[static_cast<size_t>(b) * a.gmax + i] : -1;
+  const int x =
+      (has_draft && tid == 0 && a.draft_tokens) ? a.draft_tokens[static_cast<size_t>(b) * a.gmax + i] : -1;
   const bool ok = stage_chunk(sl, &bar, &sh_ok);
   const uint4* vt = reinterpret_cast<const uint4*>(sl.st);
   const uint4* vd = reinterpret_cast<const uint4*>(sl.sd);
@@ -335,13 +331,6 @@ __device__ __forceinline__ void locate_target_chunk(const VerifyArgs& a, int uni
 
 }  // namespace
 
-// Arrival counter with acquire-release semantics: the releases of earlier
-// arrivals (their published sums) are visible to the last one.
-__device__ __forceinline__ int ticket_add(int32_t* p) {
-  int old;
-  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(p) : "memory");
-  return old;
-}
 
 // ---------------------------------------------------------------------------
 // Kernel 2: decisions and the draw, warp by warp.  A piece is 128 vectors
@@ -356,213 +345,27 @@ __device__ __forceinline__ int ticket_add(int32_t* p) {
 // ---------------------------------------------------------------------------
 constexpr int kT2 = 128;  // threads of a sampling CTA
 constexpr int kW2 = kT2 / 32;
-constexpr int kPieceVecs = 128;  // vectors per piece: 4 per lane
 
-// A piece's vectors as raw 16-byte words, lane L holding the 4 consecutive
-// vectors 4L .. 4L+3, target and, when gd is given, draft; elements past n
-// read as -inf (weight 0).  One round of loads.
-template <typename E>
-struct PieceRows {
-  uint4 rt[4], rd[4];
-  __device__ __forceinline__ void load(const E* gt, const E* gd, int n, bool aligned) {
-    constexpr int kVec = Elem<E>::kVec;
-    const int lane = threadIdx.x & 31;
-    const int nv = (n + kVec - 1) / kVec;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int v = 4 * lane + k;
-      rt[k] = rd[k] = Elem<E>::max_init();  // all -inf
-      if (v >= nv) continue;
-      if (aligned) {
-        rt[k] = __ldg(reinterpret_cast<const uint4*>(gt) + v);
-        if (gd) rd[k] = __ldg(reinterpret_cast<const uint4*>(gd) + v);
-      } else {
-        rt[k] = gather_vec(gt, v * kVec, n);
-        if (gd) rd[k] = gather_vec(gd, v * kVec, n);
-      }
-    }
-  }
-  // Elements [i0, i0 + kVec) of a row not aligned to 16 bytes, -inf past n.
-  static __device__ __forceinline__ uint4 gather_vec(const E* g, int i0, int n) {
-    uint32_t w[4];
-    if constexpr (sizeof(E) == 2) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t lo = i0 + 2 * j < n ? static_cast<uint32_t>(g[i0 + 2 * j]) : 0xFF80u;
-        const uint32_t hi = i0 + 2 * j + 1 < n ? static_cast<uint32_t>(g[i0 + 2 * j + 1]) : 0xFF80u;
-        w[j] = lo | (hi << 16);
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) w[j] = __float_as_uint(i0 + j < n ? static_cast<float>(g[i0 + j]) : -INFINITY);
-    }
-    return make_uint4(w[0], w[1], w[2], w[3]);
-  }
-  template <typename WFun>
-  __device__ __forceinline__ void weights(int k, const WFun& wfun, float (&w)[Elem<E>::kVec]) const {
-    float xt[Elem<E>::kVec], xd[Elem<E>::kVec];
-    Elem<E>::unpack(rt[k], xt);
-    Elem<E>::unpack(rd[k], xd);
-    wfun(xt, xd, w);
-  }
-};
-
-// The weight sum of a lane's 4 vectors (in vector order).
-template <typename E, typename WFun>
-__device__ __forceinline__ float piece_lane_sum(const PieceRows<E>& pr, const WFun& wfun) {
-  float s = 0.f;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    float w[Elem<E>::kVec];
-    pr.weights(k, wfun, w);
-    s += pair_sum(w);
-  }
-  return s;
-}
-
-// One warp, one value per lane in index order: the exclusive prefix of every
-// lane (fp64) and the first lane whose running sum passes tl, else the last
-// lane with a positive value (-1 if none).
-__device__ __forceinline__ int lane_locate(double v, double tl, double* before) {
-  const int lane = threadIdx.x & 31;
-  double incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const double t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (lane >= o) incl += t;
-  }
-  const unsigned hm = __ballot_sync(0xFFFFFFFFu, v > 0.0 && tl < incl);
-  const unsigned pm = __ballot_sync(0xFFFFFFFFu, v > 0.0);
-  const int L = hm ? __ffs(hm) - 1 : (pm ? 31 - __clz(pm) : -1);
-  *before = __shfl_sync(0xFFFFFFFFu, incl - v, L >= 0 ? L : 0);
-  return L;
-}
-
-// One warp: the element of a loaded piece whose running weight first exceeds
-// tl (relative to the piece start), falling back to the last element with
-// positive weight: a lane scan over the lanes' sums, then the found lane's 4
-// vectors element by element (fp32 from the lane's start: the lane's weight is
-// a small share of the row's).  Returns the element index relative to the
-// piece start (-1 if none), the weight before it and its weight.
-template <typename E, typename WFun>
-__device__ __forceinline__ ScanHit scan_piece(const PieceRows<E>& pr, const WFun& wfun, double tl) {
-  constexpr int kVec = Elem<E>::kVec;
-  const int lane = threadIdx.x & 31;
-  float w[4][kVec];
-  float ls = 0.f;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    pr.weights(k, wfun, w[k]);
-    ls += pair_sum(w[k]);
-  }
-  double before = 0.0;
-  const int L = lane_locate(static_cast<double>(ls), tl, &before);
-  if (L < 0) return ScanHit{-1, NAN, 0.f};
-  int el = -1;
-  float edge = 0.f, we = 0.f;
-  if (lane == L) {
-    const float t = static_cast<float>(tl - before);
-    float acc = 0.f;
-    bool done = false;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-#pragma unroll
-      for (int e = 0; e < kVec; ++e) {
-        if (!done && w[k][e] > 0.f) {
-          el = k * kVec + e;  // the hit, or the last positive element so far
-          edge = acc;
-          we = w[k][e];
-          done = t < acc + w[k][e];
-        }
-        acc += w[k][e];
-      }
-    }
-  }
-  el = __shfl_sync(0xFFFFFFFFu, el, L);
-  edge = __shfl_sync(0xFFFFFFFFu, edge, L);
-  we = __shfl_sync(0xFFFFFFFFu, we, L);
-  if (el < 0) return ScanHit{-1, NAN, 0.f};
-  return ScanHit{4 * L * kVec + el, before + static_cast<double>(edge), we};
-}
-
-// One warp: a row's piece sums, copied into the warp's shared slice `v` (lane
-// L's consecutive share first summed by lane L), the lane sums and the row
-// total (fp64 over lanes), valid in every lane.
-struct RowPieces {
-  float* v;  // shared, np floats
-  int per;
-  float lane_sum;
-  double total;
-  __device__ __forceinline__ void load(const float* psum, int np, float* slice) {
-    const int lane = threadIdx.x & 31;
-    v = slice;
-    per = (np + 31) / 32;
-    for (int q = lane; q < np; q += 32) v[q] = __ldcg(psum + q);
-    __syncwarp();
-    lane_sum = 0.f;
-    for (int k = 0; k < per; ++k) {
-      const int q = lane * per + k;
-      if (q < np) lane_sum += v[q];
-    }
-    double t = static_cast<double>(lane_sum);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
-    total = t;
-  }
-};
-
-// One warp: the draw at u * total from a row's piece sums: the lane whose
-// pieces hold it, the piece within that lane's run, then that piece reloaded
-// and scanned; writes request b's outputs (tok_x: its first n draft tokens)
-// and, with statistics, the CDF edges of the drawn token.
+// One warp: the draw at u * total from a row's piece sums (warp_locate_row);
+// writes request b's outputs (tok_x: its first n draft tokens) and, with
+// statistics, the CDF edges of the drawn token.
 template <typename E, typename WFun>
 __device__ __noinline__ void warp_draw_row(const VerifyArgs& a, int b, int n, size_t pi_idx, const RowPieces& rp,
                                            double ures, const E* trow, const E* drow, bool aligned, const WFun& wfun,
                                            const int* tok_x) {
-  constexpr int kVec = Elem<E>::kVec;
   const int lane = threadIdx.x & 31;
-  const int V = a.geo.V, pelems = kPieceVecs * kVec;
-  const double tot = rp.total;
-  const double target = ures * tot;
-  double before = 0.0;
-  const int L = lane_locate(static_cast<double>(rp.lane_sum), target, &before);
-  int owner = -1;
-  float obefore = 0.f;
-  if (lane == L) {
-    const float t = static_cast<float>(target - before);
-    float acc = 0.f;
-    for (int k = 0; k < rp.per; ++k) {
-      const int q = L * rp.per + k;
-      const float w = q < a.geo.npiece ? rp.v[q] : 0.f;
-      if (w > 0.f) {
-        owner = q;  // the hit, or the last positive piece so far
-        obefore = acc;
-        if (t < acc + w) break;
-      }
-      acc += w;
-    }
-  }
-  owner = __shfl_sync(0xFFFFFFFFu, owner, L >= 0 ? L : 0);
-  const double owner_before = before + static_cast<double>(__shfl_sync(0xFFFFFFFFu, obefore, L >= 0 ? L : 0));
-  ScanHit h{-1, NAN, 0.f};
-  const int olo = owner * pelems;
-  if (L >= 0 && owner >= 0) {
-    PieceRows<E> pr;
-    pr.load(trow + olo, drow ? drow + olo : nullptr, min(pelems, V - olo), aligned);
-    h = scan_piece(pr, wfun, target - owner_before);
-  }
+  const RowDraw d = warp_locate_row<E>(rp, ures, trow, drow, a.geo.V, aligned, wfun);
   if (lane == 0) {
-    if (h.elem < 0 || !(tot > 0.0)) {
+    if (d.elem < 0 || !(rp.total > 0.0)) {
       write_error(a, b);
       atomicOr(a.status, 1 << SSD_ERR_TIMEOUT);
     } else {
       if (a.stats) {
         float* st = a.stats + pi_idx * SSD_NSTAT_VERIFY;
-        const double e0 = owner_before + h.edge;
-        st[8] = static_cast<float>(ures - e0 / tot);
-        st[9] = static_cast<float>((e0 + static_cast<double>(h.w)) / tot - ures);
+        st[8] = static_cast<float>(ures - d.edge / rp.total);
+        st[9] = static_cast<float>((d.edge + static_cast<double>(d.w)) / rp.total - ures);
       }
-      write_outputs(a, b, n, olo + h.elem, tok_x);
+      write_outputs(a, b, n, d.elem, tok_x);
     }
   }
 }
@@ -824,7 +627,7 @@ cudaError_t ensure_smem(const void* fn, int smem_bytes, int* cached) {
 }
 
 template <typename E>
-cudaError_t launch_verify_t(const VerifyArgs& a, int smem_bytes, cudaStream_t stream) {
+cudaError_t launch_stream_t(const VerifyArgs& a, int smem_bytes, cudaStream_t stream) {
   static thread_local int dev_cached = -1, smem1 = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -835,7 +638,6 @@ cudaError_t launch_verify_t(const VerifyArgs& a, int smem_bytes, cudaStream_t st
   }
   e = ensure_smem(reinterpret_cast<const void*>(&stream_kernel<E>), smem_bytes, &smem1);
   if (e != cudaSuccess) return e;
-
   cudaLaunchAttribute pdl[1];
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
@@ -846,7 +648,12 @@ cudaError_t launch_verify_t(const VerifyArgs& a, int smem_bytes, cudaStream_t st
   c1.stream = stream;
   c1.attrs = pdl;
   c1.numAttrs = 1;
-  e = cudaLaunchKernelEx(&c1, stream_kernel<E>, a);
+  return cudaLaunchKernelEx(&c1, stream_kernel<E>, a);
+}
+
+template <typename E>
+cudaError_t launch_verify_t(const VerifyArgs& a, int smem_bytes, cudaStream_t stream) {
+  cudaError_t e = launch_stream_t<E>(a, smem_bytes, stream);
   if (e != cudaSuccess) return e;
   const int P = a.debug ? a.gmax + 1 : 1;  // position slots of the sampling grid
   cudaLaunchConfig_t cfg = {};
@@ -866,6 +673,10 @@ cudaError_t launch_verify_t(const VerifyArgs& a, int smem_bytes, cudaStream_t st
 
 cudaError_t launch_verify(const VerifyArgs& a, int esize, int smem_bytes, cudaStream_t stream) {
   return esize == 2 ? launch_verify_t<uint16_t>(a, smem_bytes, stream) : launch_verify_t<float>(a, smem_bytes, stream);
+}
+
+cudaError_t launch_stream(const VerifyArgs& a, int esize, int smem_bytes, cudaStream_t stream) {
+  return esize == 2 ? launch_stream_t<uint16_t>(a, smem_bytes, stream) : launch_stream_t<float>(a, smem_bytes, stream);
 }
 
 }  // namespace ssdv

@@ -50,9 +50,11 @@ def _declare(lib):
     lib.ssd_verify_ragged.argtypes = [P, P, I, P, I, I, I, P, P, U64, P, P, P, SZ, P]
     lib.ssd_verify_noalloc.argtypes = [P, P, I, P, I, I, I, F, U64, P, P, P]
     lib.ssd_verify_pipelined.argtypes = [P, P, I, P, I, I, I, F, U64, P, P, P, SZ, P]
-    lib.ssd_saguaro_prespec.argtypes = [P, P, I, I, I, I, I, F, U64, P, P, P]
+    lib.ssd_saguaro_prespec.argtypes = [P, P, I, I, I, I, I, F, U64, P, P, P, SZ, P]
+    lib.ssd_saguaro_workspace_bytes.argtypes = [I, I, I]
+    lib.ssd_saguaro_workspace_bytes.restype = SZ
     lib.ssd_debug_rowstats.argtypes = [P, P, I, P, I, I, I, F, U64, P, P, P, P, SZ, P]
-    lib.ssd_debug_saguaro_stats.argtypes = [P, P, I, I, I, I, I, F, U64, P, P, P, P]
+    lib.ssd_debug_saguaro_stats.argtypes = [P, P, I, I, I, I, I, F, U64, P, P, P, P, SZ, P]
     lib.ssd_read_status.argtypes = [P, SZ, P, P]
     lib.ssd_debug_uniforms.argtypes = [U64, I, I, P, P]
     lib.ssd_status_str.argtypes = [I]
@@ -139,6 +141,33 @@ def _workspace(B: int, gmax: int, device, given: Optional[torch.Tensor]):
     if ws is None or ws.numel() < need:
         ws = torch.zeros(max(need, 1 << 16), dtype=torch.uint8, device=device)
         _ws_cache[key] = ws
+    return ws
+
+
+_sag_ws_cache = {}
+
+
+def saguaro_workspace_bytes(B: int, gamma: int, V: int) -> int:
+    return int(lib().ssd_saguaro_workspace_bytes(B, gamma, V))
+
+
+def make_saguaro_workspace(B: int, gamma: int, V: int, device=None) -> torch.Tensor:
+    """A zeroed device workspace for Saguaro calls of up to B requests, gamma, V."""
+    n = saguaro_workspace_bytes(B, gamma, V)
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def _saguaro_workspace(B: int, g: int, V: int, device, given: Optional[torch.Tensor]):
+    # kept apart from the verification workspaces: a pipelined verification
+    # call may write its workspace while the previous kernel still runs
+    if given is not None:
+        return given
+    key = _ws_key(device)
+    need = saguaro_workspace_bytes(B, g, V)
+    ws = _sag_ws_cache.get(key)
+    if ws is None or ws.numel() < need:
+        ws = torch.zeros(max(need, 1 << 16), dtype=torch.uint8, device=device)
+        _sag_ws_cache[key] = ws
     return ws
 
 
@@ -245,7 +274,7 @@ def verify_ragged(target: torch.Tensor, draft: torch.Tensor, draft_tokens: torch
 
 def saguaro_prespec(target: torch.Tensor, draft: torch.Tensor, k: int, temperature: float, seed: int,
                     bonus_topk: Optional[torch.Tensor] = None, saguaro_tokens: Optional[torch.Tensor] = None,
-                    stream=None):
+                    workspace: Optional[torch.Tensor] = None, stream=None):
     """ssd_saguaro_prespec: returns (bonus_topk [B, g+1, k], saguaro_tokens [B, g+1])."""
     B, W, V = target.shape
     g = W - 1
@@ -255,10 +284,12 @@ def saguaro_prespec(target: torch.Tensor, draft: torch.Tensor, k: int, temperatu
     if saguaro_tokens is None:
         saguaro_tokens = torch.empty(B, W, dtype=torch.int32, device=dev)
     dptr = _dev(draft, "draft_logits", target.dtype) if g > 0 else None
+    ws = _saguaro_workspace(B, g, V, dev, workspace)
     _check(lib().ssd_saguaro_prespec(_dev(target, "target_logits"), dptr, _dtype_code(target), B, g, V, int(k),
                                      float(temperature), int(seed) & ((1 << 64) - 1),
                                      _dev(bonus_topk, "bonus_topk", torch.int32),
-                                     _dev(saguaro_tokens, "saguaro_tokens", torch.int32), _stream(stream)))
+                                     _dev(saguaro_tokens, "saguaro_tokens", torch.int32), _dev(ws, "workspace"),
+                                     ws.numel(), _stream(stream)))
     return bonus_topk, saguaro_tokens
 
 
@@ -280,7 +311,7 @@ def debug_rowstats(target, draft, draft_tokens, temperature, seed, workspace=Non
     return out_tokens, n_accepted, stats
 
 
-def debug_saguaro_stats(target, draft, k, temperature, seed, stream=None):
+def debug_saguaro_stats(target, draft, k, temperature, seed, workspace=None, stream=None):
     """ssd_debug_saguaro_stats: (bonus_topk, saguaro_tokens, stats [B, g+1, 10])."""
     B, W, V = target.shape
     g = W - 1
@@ -289,10 +320,12 @@ def debug_saguaro_stats(target, draft, k, temperature, seed, stream=None):
     saguaro_tokens = torch.empty(B, W, dtype=torch.int32, device=dev)
     stats = torch.empty(B, W, NSTAT_SAGUARO, dtype=torch.float32, device=dev)
     dptr = _dev(draft, "draft_logits", target.dtype) if g > 0 else None
+    ws = _saguaro_workspace(B, g, V, dev, workspace)
     _check(lib().ssd_debug_saguaro_stats(_dev(target, "target_logits"), dptr, _dtype_code(target), B, g, V,
                                          int(k), float(temperature), int(seed) & ((1 << 64) - 1),
                                          _dev(bonus_topk, "bonus_topk"), _dev(saguaro_tokens, "saguaro_tokens"),
-                                         _dev(stats, "stats"), _stream(stream)))
+                                         _dev(stats, "stats"), _dev(ws, "workspace"), ws.numel(),
+                                         _stream(stream)))
     return bonus_topk, saguaro_tokens, stats
 
 

@@ -147,13 +147,13 @@ def test_equal_distributions(ssdv):
 
 
 def test_saguaro_config_full_sampled(ssdv):
-    """B=256, gamma 6, V 152064 fp32, sigma 0.6, T 0.8, k 3 (config 4):
+    """B=256, gamma 6, V 152064 fp32, sigma 0.6, T 0.8, k 3 (the Saguaro workload):
     GPU over the whole batch, oracle on 12 sampled requests."""
     batch = wl.zipf_batch(256, 6, 152064, dtype=torch.float32, temperature=0.8, seed=3, sigma_range=(0.6, 0.6),
                           sample_tokens=False)
     topk, tok, st = run(ssdv, batch, 3, 0.8, 3, stats=True)
     subset = np.random.default_rng(1).choice(256, 12, replace=False)
-    assert_saguaro_parity(batch, 3, 0.8, 3, topk, tok, st, subset=subset, what="config 4")
+    assert_saguaro_parity(batch, 3, 0.8, 3, topk, tok, st, subset=subset, what="Saguaro workload")
     # product entry point agrees with the debug entry point
     topk2, tok2, _ = run(ssdv, batch, 3, 0.8, 3)
     assert np.array_equal(topk, topk2) and np.array_equal(tok, tok2)
@@ -163,3 +163,27 @@ def test_saguaro_config_full_sampled(ssdv):
     ref = o.saguaro_batch(tgt[subset], dft[subset], 3, 0.8, 3, stats=True, nthreads=16, req_ids=subset)
     rel = np.abs(st[subset, :, 3] / ref["stats"][:, :, 3] - 1)
     assert rel.max() < 1e-5, rel.max()
+
+
+def test_segments_and_workspace_reuse(ssdv, monkeypatch):
+    """Requests split into segments (each its own streaming, residual and mix
+    kernels) give the same outputs as one segment; a workspace reused by a
+    smaller shape (whose counters overlap the larger shape's sums) and then by
+    the larger shape again changes nothing."""
+    batch = wl.zipf_batch(24, 3, 5000, dtype=torch.bfloat16, temperature=0.8, seed=8, sigma_range=(0.6, 0.6),
+                          sample_tokens=False)
+    small = wl.zipf_batch(2, 1, 300, dtype=torch.float32, temperature=0.8, seed=9, sigma_range=(0.6, 0.6),
+                          sample_tokens=False)
+    b, s = batch.to("cuda"), small.to("cuda")
+    ws = ssdv.make_saguaro_workspace(24, 3, 5000)
+    topk_a, tok_a, st_a = ssdv.debug_saguaro_stats(b.target, b.draft, 4, 0.8, 5, workspace=ws)
+    topk_a, tok_a, st_a = topk_a.cpu().numpy(), tok_a.cpu().numpy(), st_a.cpu().numpy()
+    assert_saguaro_parity(batch, 4, 0.8, 5, topk_a, tok_a, st_a, what="one segment")
+    ssdv.saguaro_prespec(s.target, s.draft, 2, 0.8, 1, workspace=ws)
+    topk_s, tok_s, st_s = run(ssdv, small, 2, 0.8, 1, stats=True)
+    assert_saguaro_parity(small, 2, 0.8, 1, topk_s, tok_s, st_s, what="small shape")
+    monkeypatch.setenv("SSDV_SAG_SEGMENT", "5")
+    topk_b, tok_b = ssdv.saguaro_prespec(b.target, b.draft, 4, 0.8, 5, workspace=ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(topk_a, topk_b.cpu().numpy()) and np.array_equal(tok_a, tok_b.cpu().numpy())
+    assert ssdv.read_status(ws) == 0

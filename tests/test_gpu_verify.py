@@ -58,7 +58,7 @@ def test_toy_unbiasedness_on_gpu(ssdv):
 
 
 def test_gaussian_config(ssdv):
-    """B=1, gamma 5, V 32000 bf16, T 1 (config 2), over 24 seeds."""
+    """B=1, gamma 5, V 32000 bf16, T 1 (the single-request latency workload), over 24 seeds."""
     batch = wl.gaussian_batch(1, 5, 32000, seed=1)
     acc = []
     for seed in range(24):
@@ -183,7 +183,7 @@ def test_ragged_small(ssdv):
 
 
 def test_ragged_full_config_sampled(ssdv):
-    """B=512, gamma 1..8, V 128256 bf16 (config 5); oracle on 48 sampled requests."""
+    """B=512, gamma 1..8, V 128256 bf16 (the ragged batch workload); oracle on 48 sampled requests."""
     batch = wl.ragged_batch(512, 8, 128256, seed=4)
     b = batch.to("cuda")
     out, n = ssdv.verify_ragged(b.target, b.draft, b.draft_tokens, b.gamma, b.temperature, 4)
