@@ -141,6 +141,10 @@ __device__ __forceinline__ bool unit_pieces(const SagArgs& a, size_t u, int wi, 
   const int pn = min(ppw, NP - p0);
   TopK<kTopK> tk;
   tk.init();
+  // tau: the k-th largest of the lanes' best weights so far.  The warp holds
+  // k elements at or above it, so a smaller weight is not among the row's k
+  // largest and is not pushed (weights are >= 0; tau starts below them).
+  float tau = -1.f;
   for (int j = 0; j < pn; ++j) {
     const int lo = (p0 + j) * pelems;
     PieceRows<E> pr;
@@ -152,14 +156,30 @@ __device__ __forceinline__ bool unit_pieces(const SagArgs& a, size_t u, int wi, 
       pr.weights(k, wfun, w);
       s += pair_sum(w);
       if constexpr (kTop) {
-        const int base = lo + (4 * lane + k) * kVec;
+        float wm = w[0];
 #pragma unroll
-        for (int e = 0; e < kVec; ++e)
-          if (base + e < V) tk.push(w[e], base + e);
+        for (int e = 1; e < kVec; ++e) wm = fmaxf(wm, w[e]);
+        if (__any_sync(0xFFFFFFFFu, wm >= tau)) {
+          const int base = lo + (4 * lane + k) * kVec;
+#pragma unroll
+          for (int e = 0; e < kVec; ++e)
+            if (w[e] >= tau && base + e < V) tk.push(w[e], base + e);
+        }
       }
     }
     s = warp_sum(s);
     if (lane == 0) psum[u * NP + p0 + j] = s;
+    if constexpr (kTop) {
+      float x = tk.v[0];
+      for (int r = 0; r < a.k; ++r) {
+        float m = x;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        tau = m;
+        const unsigned hit = __ballot_sync(0xFFFFFFFFu, x == m);
+        if (lane == __ffs(hit) - 1) x = -2.f;
+      }
+    }
   }
   if constexpr (kTop) {
     float mv[kTopK];
@@ -176,7 +196,9 @@ __device__ __forceinline__ bool unit_pieces(const SagArgs& a, size_t u, int wi, 
         }
       a.cand_v[(u * a.npw + wi) * kTopK + lane] = v;
       a.cand_i[(u * a.npw + wi) * kTopK + lane] = i;
+      __threadfence();  // before lane 0's arrival below publishes them
     }
+    __syncwarp();
   }
   int is_last = 0;
   if (lane == 0) is_last = ticket_add(ticket + u) == a.npw - 1;

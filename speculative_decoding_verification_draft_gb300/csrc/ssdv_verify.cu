@@ -159,7 +159,6 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const VerifyArgs a) {
   Slice<E> sl;
   sl.n = min(geo.chunk, V - lo);
   sl.nvec = (sl.n + kVec - 1) / kVec;
-  sl.nstage = 1;
   sl.bulk = geo.bulk != 0;
   sl.gt = static_cast<const E*>(a.target) + (static_cast<size_t>(b) * W + i) * V + lo;
   sl.gd = has_draft ? static_cast<const E*>(a.draft) + (static_cast<size_t>(b) * a.gmax + i) * V + lo : nullptr;
@@ -299,34 +298,6 @@ __device__ void write_error(const VerifyArgs& a, int b) {
   int32_t* out = a.out_tokens + static_cast<size_t>(b) * W;
   for (int k = 0; k < W; ++k) out[k] = -1;
   a.n_accepted[b] = -1;
-}
-
-// Warp 0: the chunk weights of q at unit u (the records' sums moved to the
-// row maximum), their fp64 inclusive scan, and the chunk holding u*total.
-__device__ __forceinline__ void locate_target_chunk(const VerifyArgs& a, int unit, float M, float cc, double u,
-                                                    int* owner, double* local, double* prefix, double* total) {
-  const int lane = threadIdx.x & 31, NC = a.geo.nchunk;
-  double w = 0.0;
-  if (lane < NC) {
-    const float4 r = __ldcg(a.part + (static_cast<size_t>(unit) * NC + lane) * 2);
-    w = (r.x == -INFINITY) ? 0.0 : static_cast<double>(r.y * rescale(r.x, M, cc));
-  }
-  double incl = w;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const double t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (lane >= o) incl += t;
-  }
-  const double tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
-  const double target = u * tot;
-  const unsigned hit = __ballot_sync(0xFFFFFFFFu, lane < NC && w > 0.0 && target < incl);
-  const unsigned pos = __ballot_sync(0xFFFFFFFFu, lane < NC && w > 0.0);
-  const int r = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : -1);
-  const double pre = __shfl_sync(0xFFFFFFFFu, incl - w, r >= 0 ? r : 0);
-  *owner = r;
-  *prefix = r >= 0 ? pre : 0.0;
-  *local = target - *prefix;
-  *total = tot;
 }
 
 }  // namespace
