@@ -298,13 +298,23 @@ def secondary(ssdv, workloads, dev, stream):
     peak, _ = load_peaks()
     # Saguaro pre-speculation: B=256, gamma 6, V 152064 fp32, k 3
     sb = workloads.zipf_batch(256, 6, 152064, dtype=torch.float32, temperature=0.8, seed=3,
-                              sigma_range=(0.6, 0.6), device=dev, sample_tokens=False)
+                              sigma_range=(0.6, 0.6), device=dev)
     topk = torch.empty(256, 7, 3, dtype=torch.int32, device=dev)
     tok = torch.empty(256, 7, dtype=torch.int32, device=dev)
     ms = timeit(lambda: ssdv.saguaro_prespec(sb.target, sb.draft, 3, 0.8, 3, topk, tok, stream=stream), 10)
     by = sb.algorithmic_bytes()
     res["saguaro_B256_g6_V152064_f32"] = {"ms_per_round": ms, "rounds_per_s": 1e3 / ms, "bytes": by,
                                           "gbs": by / ms / 1e6, "frac_of_measured_hbm": by / ms / 1e6 / peak}
+    # the same round verified and pre-speculated: one fused call (with the
+    # cache check) against the two separate calls
+    ms_f = timeit(lambda: ssdv.verify_saguaro(sb.target, sb.draft, sb.draft_tokens, 3, 0.8, 3, stream=stream), 10)
+    out = torch.empty(256, 7, dtype=torch.int32, device=dev)
+    n = torch.empty(256, dtype=torch.int32, device=dev)
+    ws = ssdv.make_workspace(256, 6, dev)
+    ms_v = timeit(lambda: ssdv.verify(sb.target, sb.draft, sb.draft_tokens, 0.8, 3, out, n, ws, stream=stream), 10)
+    res["verify_saguaro_fused_B256_g6_V152064_f32"] = {
+        "ms_per_round": ms_f, "rounds_per_s": 1e3 / ms_f, "bytes": by, "gbs": by / ms_f / 1e6,
+        "frac_of_measured_hbm": by / ms_f / 1e6 / peak, "separate_calls_ms": ms + ms_v, "verify_alone_ms": ms_v}
     del sb
     torch.cuda.empty_cache()
     # ragged mixed batch: B=512, gamma 1..8, V 128256 bf16, half greedy

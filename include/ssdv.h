@@ -198,6 +198,35 @@ ssd_status ssd_saguaro_prespec(const void* target_logits, const void* draft_logi
  * sums and every warp's top-8 candidates. */
 size_t ssd_saguaro_workspace_bytes(int B, int gamma, int V);
 
+/* Verification and Saguaro pre-speculation of the same round in one call
+ * (SSD notes, section 4.1: the target verifies a round while the next one is
+ * pre-speculated from the same distributions).  Outputs exactly those of
+ * ssd_verify (out_tokens, n_accepted) and of ssd_saguaro_prespec (bonus_topk,
+ * saguaro_tokens) on the same arguments, with every logit row read from HBM
+ * once for both, plus the cache check of ssd_cache_check (hit, n_hits; either
+ * may be NULL).  temperature > 0 (Saguaro has no greedy form).
+ *   workspace >= ssd_saguaro_workspace_bytes(B, gamma, V) bytes, zeroed once.
+ * Constraints: those of ssd_verify and ssd_saguaro_prespec. */
+ssd_status ssd_verify_saguaro(const void* target_logits, const void* draft_logits, ssd_dtype dtype,
+                              const int32_t* draft_tokens, int B, int gamma, int V, int k,
+                              float temperature, uint64_t seed, int32_t* out_tokens,
+                              int32_t* n_accepted, int32_t* bonus_topk, int32_t* saguaro_tokens,
+                              int32_t* hit, int32_t* n_hits, void* workspace, size_t ws_bytes,
+                              void* stream);
+
+/* The Saguaro cache check (SSD notes, sections 3.3 and 4.1): a round hits the
+ * pre-speculated cache when its correction / bonus token is among the bonus
+ * tokens predicted for its acceptance length.
+ *   bonus_topk [B, gamma+1, k] (ssd_saguaro_prespec), out_tokens [B, gamma+1]
+ *   and n_accepted [B] (ssd_verify) of the same round;
+ *   hit [B] int32 (nullable): the slot s with bonus_topk[b, n_b, s] ==
+ *       out_tokens[b, n_b], else -1 (and -1 for a request with n_b = -1);
+ *   n_hits [1] int32 (nullable): the number of hits (set, not accumulated).
+ * At least one of hit / n_hits must be given.  One small kernel. */
+ssd_status ssd_cache_check(const int32_t* bonus_topk, const int32_t* out_tokens,
+                           const int32_t* n_accepted, int B, int gamma, int k, int32_t* hit,
+                           int32_t* n_hits, void* stream);
+
 /* Debug / parity: ssd_verify (same arguments and outputs) that also returns
  * the per-position quantities it computes, for every position whether or not
  * it is reached (the residual pass then runs at every position).

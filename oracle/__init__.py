@@ -56,6 +56,8 @@ def _declare(lib):
     lib.orc_softmax.restype = None
     lib.orc_argmax.argtypes = [P, c_int]
     lib.orc_argmax.restype = c_int
+    lib.orc_cache_check.argtypes = [P, P, P, c_int, c_int, c_int, P]
+    lib.orc_cache_check.restype = c_int
     lib.orc_choice.argtypes = [P, c_int, c_double, P]
     lib.orc_choice.restype = c_int
     lib.orc_topk.argtypes = [P, c_int, c_int, P, P]
@@ -238,6 +240,17 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle rejected the batch arguments")
         return dict(out_tokens=out, n_accepted=n, flag_pos=fp, flag_kind=fk, stats=st)
+
+    def cache_check(self, bonus_topk, out_tokens, n_accepted):
+        """(hit [B], number of hits) of one round's verify outcome against its
+        pre-speculated bonus tokens."""
+        topk = np.ascontiguousarray(bonus_topk, dtype=np.int32)
+        B, W, k = topk.shape
+        out = np.ascontiguousarray(out_tokens, dtype=np.int32).reshape(B, W)
+        n = np.ascontiguousarray(n_accepted, dtype=np.int32).reshape(B)
+        hit = np.empty(B, np.int32)
+        count = self.lib.orc_cache_check(_ptr(topk), _ptr(out), _ptr(n), B, W - 1, k, _ptr(hit))
+        return hit, count
 
     def saguaro_batch(self, target, draft, k: int, temperature: float, seed: int,
                       stats: bool = False, nthreads: int = 1, req_ids=None, band: float = FLAG_BAND):

@@ -749,4 +749,34 @@ int orc_saguaro_batch(const void* target, const void* draft, int dtype, int B, i
   return run_batch(jb);
 }
 
+/* ------------------------------------------------------------------------- */
+/* The Saguaro cache check ([SSD] §3.3 and §4.1: a round hits the cache of    */
+/* pre-speculated continuations when its correction / bonus token is among    */
+/* the bonus tokens predicted for its acceptance length n).  For request b:   */
+/*   hit[b] = the first slot s with bonus_topk[b, n_b, s] == out_tokens[b, n_b],*/
+/*            -1 if none or if n_b is -1 (an error).                          */
+/* Returns the number of hits.                                                */
+/* ------------------------------------------------------------------------- */
+int orc_cache_check(const int32_t* bonus_topk, const int32_t* out_tokens, const int32_t* n_accepted, int B,
+                    int g, int k, int32_t* hit) {
+  int count = 0;
+  for (int b = 0; b < B; ++b) {
+    const int n = n_accepted[b];
+    int h = -1;
+    if (n >= 0 && n <= g) {
+#if ORC_MUTANT == 11
+      const int row = n > 0 ? n - 1 : 0;
+#else
+      const int row = n;
+#endif
+      const int tok = out_tokens[(size_t)b * (g + 1) + n];
+      for (int s = 0; s < k && h < 0; ++s)
+        if (tok >= 0 && bonus_topk[((size_t)b * (g + 1) + row) * k + s] == tok) h = s;
+    }
+    hit[b] = h;
+    if (h >= 0) ++count;
+  }
+  return count;
+}
+
 int orc_mutant_id(void) { return ORC_MUTANT; }

@@ -351,13 +351,30 @@ ssd_status ssd_debug_rowstats(const void* target_logits, const void* draft_logit
                        temperature == 0.f, seed, out_tokens, n_accepted, workspace, ws_bytes, stats, stream);
 }
 
+// Verification outputs of a fused call (ssd_verify_saguaro); null members
+// mean a Saguaro-only call.
+struct FusedVerify {
+  const int32_t* draft_tokens = nullptr;
+  int32_t* out_tokens = nullptr;
+  int32_t* n_accepted = nullptr;
+  int32_t* hit = nullptr;
+  int32_t* n_hits = nullptr;
+};
+
 static ssd_status saguaro_common(const void* target, const void* draft, ssd_dtype dtype, int B, int g, int V, int k,
                                  float temperature, uint64_t seed, int32_t* bonus_topk, int32_t* tokens, float* stats,
-                                 void* workspace, size_t ws_bytes, void* stream) {
+                                 void* workspace, size_t ws_bytes, void* stream, const FusedVerify& fv = FusedVerify()) {
   const int es = esize_of(dtype);
+  const bool fused = fv.out_tokens != nullptr;
   if (es == 0) return fail(SSD_ERR_DTYPE, "unknown dtype %d", static_cast<int>(dtype));
   if (!target || !bonus_topk || !tokens || !workspace || (g > 0 && !draft))
     return fail(SSD_ERR_NULL, "a required pointer is NULL");
+  if (fused && (!fv.n_accepted || (g > 0 && !fv.draft_tokens)))
+    return fail(SSD_ERR_NULL, "n_accepted / draft_tokens is NULL");
+  if (fused && (!aligned_to(fv.out_tokens, 4) || !aligned_to(fv.n_accepted, 4) ||
+                (fv.draft_tokens && !aligned_to(fv.draft_tokens, 4)) || (fv.hit && !aligned_to(fv.hit, 4)) ||
+                (fv.n_hits && !aligned_to(fv.n_hits, 4))))
+    return fail(SSD_ERR_ALIGN, "a token / output pointer is not 4-byte aligned");
   if (B < 1 || g < 0 || g > SSD_MAX_GAMMA || V < 1 || V > SSD_MAX_V || k < 1 || k > SSD_MAX_TOPK || k > V)
     return fail(SSD_ERR_SHAPE, "bad shape B=%d gamma=%d V=%d k=%d", B, g, V, k);
   if (!(temperature >= 1e-6f) || !isfinite(temperature))
@@ -415,7 +432,19 @@ static ssd_status saguaro_common(const void* target, const void* draft, ssd_dtyp
     v.debug = 0;
     v.first = b0 == 0 ? 1 : 0;
     v.geo = geo;
-    cudaError_t e = launch_stream(v, es, smem, static_cast<cudaStream_t>(stream));
+    cudaError_t e;
+    if (fused) {
+      // the verification pair: its streaming records serve the Saguaro
+      // kernels too; its sampling kernel returns the counters it used to zero
+      v.draft_tokens = fv.draft_tokens ? fv.draft_tokens + static_cast<size_t>(b0) * g : nullptr;
+      v.out_tokens = fv.out_tokens + u0;
+      v.n_accepted = fv.n_accepted + b0;
+      v.psum = reinterpret_cast<float*>(ws + L.psum2) + u0 * geo.npiece;
+      v.geo.ppw = env_int("SSDV_PPW", 2) < 1 ? 1 : env_int("SSDV_PPW", 2);
+      e = launch_verify(v, es, smem, static_cast<cudaStream_t>(stream));
+    } else {
+      e = launch_stream(v, es, smem, static_cast<cudaStream_t>(stream));
+    }
     if (e != cudaSuccess) return cuda_fail(e, "saguaro streaming launch");
     SagArgs a;
     a.target = t;
@@ -444,6 +473,11 @@ static ssd_status saguaro_common(const void* target, const void* draft, ssd_dtyp
     e = launch_saguaro(a, es, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "saguaro launch");
   }
+  if (fused && (fv.hit || fv.n_hits)) {
+    const cudaError_t e = launch_cache_check(bonus_topk, fv.out_tokens, fv.n_accepted, B, W, k, fv.hit, fv.n_hits,
+                                             static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cache check launch");
+  }
   return SSD_OK;
 }
 
@@ -463,6 +497,39 @@ ssd_status ssd_debug_saguaro_stats(const void* target_logits, const void* draft_
   if (!stats) return fail(SSD_ERR_NULL, "stats is NULL");
   return saguaro_common(target_logits, draft_logits, dtype, B, gamma, V, k, temperature, seed, bonus_topk,
                         saguaro_tokens, stats, workspace, ws_bytes, stream);
+}
+
+ssd_status ssd_verify_saguaro(const void* target_logits, const void* draft_logits, ssd_dtype dtype,
+                              const int32_t* draft_tokens, int B, int gamma, int V, int k, float temperature,
+                              uint64_t seed, int32_t* out_tokens, int32_t* n_accepted, int32_t* bonus_topk,
+                              int32_t* saguaro_tokens, int32_t* hit, int32_t* n_hits, void* workspace,
+                              size_t ws_bytes, void* stream) {
+  g_last_error.clear();
+  if (!out_tokens) return fail(SSD_ERR_NULL, "out_tokens is NULL");
+  FusedVerify fv;
+  fv.draft_tokens = draft_tokens;
+  fv.out_tokens = out_tokens;
+  fv.n_accepted = n_accepted;
+  fv.hit = hit;
+  fv.n_hits = n_hits;
+  return saguaro_common(target_logits, draft_logits, dtype, B, gamma, V, k, temperature, seed, bonus_topk,
+                        saguaro_tokens, nullptr, workspace, ws_bytes, stream, fv);
+}
+
+ssd_status ssd_cache_check(const int32_t* bonus_topk, const int32_t* out_tokens, const int32_t* n_accepted, int B,
+                           int gamma, int k, int32_t* hit, int32_t* n_hits, void* stream) {
+  g_last_error.clear();
+  if (!bonus_topk || !out_tokens || !n_accepted || (!hit && !n_hits))
+    return fail(SSD_ERR_NULL, "a required pointer is NULL");
+  if (B < 1 || gamma < 0 || gamma > SSD_MAX_GAMMA || k < 1 || k > SSD_MAX_TOPK)
+    return fail(SSD_ERR_SHAPE, "bad shape B=%d gamma=%d k=%d", B, gamma, k);
+  if (!aligned_to(bonus_topk, 4) || !aligned_to(out_tokens, 4) || !aligned_to(n_accepted, 4) ||
+      (hit && !aligned_to(hit, 4)) || (n_hits && !aligned_to(n_hits, 4)))
+    return fail(SSD_ERR_ALIGN, "a pointer is not 4-byte aligned");
+  const cudaError_t e = launch_cache_check(bonus_topk, out_tokens, n_accepted, B, gamma + 1, k, hit, n_hits,
+                                           static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cache check launch");
+  return SSD_OK;
 }
 
 ssd_status ssd_debug_uniforms(uint64_t seed, int B, int W, float* out, void* stream) {

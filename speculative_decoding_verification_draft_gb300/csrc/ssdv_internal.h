@@ -95,6 +95,12 @@ cudaError_t launch_stream(const VerifyArgs& a, int esize, int smem_bytes, cudaSt
 // Saguaro's residual and mix kernels (each waits for its predecessor).
 cudaError_t launch_saguaro(const SagArgs& a, int esize, cudaStream_t stream);
 
+// The cache check: hit[b] = the slot of bonus_topk[b, n_b, :] holding
+// out_tokens[b, n_b] (-1 if none), n_hits[0] = the number of hits (either
+// output may be null).  One kernel, launched after its predecessor.
+cudaError_t launch_cache_check(const int32_t* bonus_topk, const int32_t* out_tokens, const int32_t* n_accepted, int B,
+                               int W, int k, int32_t* hit, int32_t* n_hits, cudaStream_t stream);
+
 // Saguaro workspace layout (byte offsets from the workspace start; status at 0).
 struct SagLayout {
   size_t ticket2, ticket3, rowstat, rowsum, part, psum2, psum3, cand_v, cand_i, total;

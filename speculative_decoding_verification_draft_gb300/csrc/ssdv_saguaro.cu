@@ -417,6 +417,57 @@ cudaError_t launch_saguaro_t(const SagArgs& a, cudaStream_t stream) {
 
 }  // namespace
 
+// ---------------------------------------------------------------------------
+// The cache check (SSD notes, sections 3.3 and 4.1): a round's outcome hits
+// the pre-speculated cache when its correction / bonus token is among the
+// predicted bonus tokens for its acceptance length.  One CTA over the batch.
+// ---------------------------------------------------------------------------
+constexpr int kCheckThreads = 1024;
+
+__global__ void __launch_bounds__(kCheckThreads) cache_check_kernel(const int32_t* bonus_topk,
+                                                                   const int32_t* out_tokens,
+                                                                   const int32_t* n_accepted, int B, int W, int k,
+                                                                   int32_t* hit, int32_t* n_hits) {
+  __shared__ int wsum[kCheckThreads / 32];
+  griddep_wait();  // the verification and Saguaro outputs are complete and visible
+  int count = 0;
+  for (int b = threadIdx.x; b < B; b += kCheckThreads) {
+    const int n = n_accepted[b];
+    int h = -1;
+    if (n >= 0 && n < W) {
+      const int tok = out_tokens[static_cast<size_t>(b) * W + n];
+      const int32_t* row = bonus_topk + (static_cast<size_t>(b) * W + n) * k;
+      for (int s = k - 1; s >= 0; --s)
+        if (tok >= 0 && row[s] == tok) h = s;
+    }
+    if (hit) hit[b] = h;
+    count += h >= 0 ? 1 : 0;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) count += __shfl_xor_sync(0xFFFFFFFFu, count, o);
+  if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = count;
+  __syncthreads();
+  if (threadIdx.x == 0 && n_hits) {
+    int t = 0;
+    for (int w = 0; w < kCheckThreads / 32; ++w) t += wsum[w];
+    n_hits[0] = t;
+  }
+}
+
+cudaError_t launch_cache_check(const int32_t* bonus_topk, const int32_t* out_tokens, const int32_t* n_accepted, int B,
+                               int W, int k, int32_t* hit, int32_t* n_hits, cudaStream_t stream) {
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1, 1, 1);
+  cfg.blockDim = dim3(kCheckThreads, 1, 1);
+  cfg.stream = stream;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, cache_check_kernel, bonus_topk, out_tokens, n_accepted, B, W, k, hit, n_hits);
+}
+
 cudaError_t launch_saguaro(const SagArgs& a, int esize, cudaStream_t stream) {
   return esize == 2 ? launch_saguaro_t<uint16_t>(a, stream) : launch_saguaro_t<float>(a, stream);
 }

@@ -55,6 +55,8 @@ def _declare(lib):
     lib.ssd_saguaro_workspace_bytes.restype = SZ
     lib.ssd_debug_rowstats.argtypes = [P, P, I, P, I, I, I, F, U64, P, P, P, P, SZ, P]
     lib.ssd_debug_saguaro_stats.argtypes = [P, P, I, I, I, I, I, F, U64, P, P, P, P, SZ, P]
+    lib.ssd_verify_saguaro.argtypes = [P, P, I, P, I, I, I, I, F, U64, P, P, P, P, P, P, P, SZ, P]
+    lib.ssd_cache_check.argtypes = [P, P, P, I, I, I, P, P, P]
     lib.ssd_read_status.argtypes = [P, SZ, P, P]
     lib.ssd_debug_uniforms.argtypes = [U64, I, I, P, P]
     lib.ssd_status_str.argtypes = [I]
@@ -63,6 +65,7 @@ def _declare(lib):
     lib.ssd_last_error.restype = ctypes.c_char_p
     for name in ("ssd_workspace_init", "ssd_verify", "ssd_verify_noalloc", "ssd_verify_pipelined",
                  "ssd_verify_ragged", "ssd_saguaro_prespec", "ssd_debug_rowstats", "ssd_debug_saguaro_stats", "ssd_read_status",
+                 "ssd_verify_saguaro", "ssd_cache_check",
                  "ssd_debug_uniforms"):
         getattr(lib, name).restype = I
     return lib
@@ -291,6 +294,44 @@ def saguaro_prespec(target: torch.Tensor, draft: torch.Tensor, k: int, temperatu
                                      _dev(saguaro_tokens, "saguaro_tokens", torch.int32), _dev(ws, "workspace"),
                                      ws.numel(), _stream(stream)))
     return bonus_topk, saguaro_tokens
+
+
+def verify_saguaro(target: torch.Tensor, draft: torch.Tensor, draft_tokens: torch.Tensor, k: int,
+                   temperature: float, seed: int, workspace: Optional[torch.Tensor] = None, check: bool = True,
+                   stream=None):
+    """ssd_verify_saguaro: one call for both; returns (out_tokens [B, g+1], n_accepted [B],
+    bonus_topk [B, g+1, k], saguaro_tokens [B, g+1], hit [B] or None, n_hits [1] or None)."""
+    B, W, V = target.shape
+    g = W - 1
+    dev = target.device
+    out_tokens = torch.empty(B, W, dtype=torch.int32, device=dev)
+    n_accepted = torch.empty(B, dtype=torch.int32, device=dev)
+    bonus_topk = torch.empty(B, W, k, dtype=torch.int32, device=dev)
+    saguaro_tokens = torch.empty(B, W, dtype=torch.int32, device=dev)
+    hit = torch.empty(B, dtype=torch.int32, device=dev) if check else None
+    n_hits = torch.empty(1, dtype=torch.int32, device=dev) if check else None
+    ws = _saguaro_workspace(B, g, V, dev, workspace)
+    dptr = _dev(draft, "draft_logits", target.dtype) if g > 0 else None
+    tptr = _dev(draft_tokens, "draft_tokens", torch.int32) if g > 0 else None
+    _check(lib().ssd_verify_saguaro(_dev(target, "target_logits"), dptr, _dtype_code(target), tptr, B, g, V, int(k),
+                                    float(temperature), int(seed) & ((1 << 64) - 1), _dev(out_tokens, "out_tokens"),
+                                    _dev(n_accepted, "n_accepted"), _dev(bonus_topk, "bonus_topk"),
+                                    _dev(saguaro_tokens, "saguaro_tokens"),
+                                    _dev(hit, "hit") if check else None, _dev(n_hits, "n_hits") if check else None,
+                                    _dev(ws, "workspace"), ws.numel(), _stream(stream)))
+    return out_tokens, n_accepted, bonus_topk, saguaro_tokens, hit, n_hits
+
+
+def cache_check(bonus_topk: torch.Tensor, out_tokens: torch.Tensor, n_accepted: torch.Tensor, stream=None):
+    """ssd_cache_check: (hit [B], n_hits [1])."""
+    B, W, k = bonus_topk.shape
+    dev = bonus_topk.device
+    hit = torch.empty(B, dtype=torch.int32, device=dev)
+    n_hits = torch.empty(1, dtype=torch.int32, device=dev)
+    _check(lib().ssd_cache_check(_dev(bonus_topk, "bonus_topk", torch.int32), _dev(out_tokens, "out_tokens", torch.int32),
+                                 _dev(n_accepted, "n_accepted", torch.int32), B, W - 1, k, _dev(hit, "hit"),
+                                 _dev(n_hits, "n_hits"), _stream(stream)))
+    return hit, n_hits
 
 
 def debug_rowstats(target, draft, draft_tokens, temperature, seed, workspace=None, stream=None):

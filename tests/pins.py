@@ -552,10 +552,51 @@ def pin_saguaro_equal_distributions(o):
     assert np.allclose([law.get(v, 0.0) for v in range(V)], softmax(z / T), atol=1e-9)
 
 
+def pin_cache_hit_rate(o):
+    """A round hits the Saguaro cache when its correction / bonus token is
+    among the top-k predicted for its acceptance length n.  Over the round's
+    uniforms (exact law by enumeration) the hit probability must equal the
+    closed form sum_n P(N = n) * (mass of r_n on its top-k), with
+    P(N = n) = a_0 ... a_{n-1} (1 - a_n), a_i = min(1, q_i(x_i) / p_i(x_i)),
+    r_n the normalised residual (q_gamma at n = gamma): the accept rule and
+    residual law of the verification section, composed with the cache rule."""
+    from scipy.special import softmax
+    rng = np.random.Generator(np.random.PCG64(21))
+    V, g, T, k = 6, 2, 0.9, 2
+    xt = rng.normal(0, 1.0, (g + 1, V))
+    xd = rng.normal(0, 1.0, (g, V))
+    tok = np.array([int(np.argmax(xd[0])), int(np.argsort(xd[1])[-2])], np.int32)
+    top = o.saguaro_request(xt, xd, T, k, np.full(g + 1, 0.5))["topk"]
+    law = request_law(o, xt, xd, T, tok)
+    p_hit = 0.0
+    for out, pr in law.items():  # out: x_0 .. x_{n-1}, the correction / bonus at n, then -1
+        n = len(emitted(out)) - 1
+        row = np.array([out], np.int32)
+        hit, count = o.cache_check(top[None], row, np.array([n], np.int32))
+        assert count == (1 if hit[0] >= 0 else 0)
+        if hit[0] >= 0:
+            assert top[n, hit[0]] == out[n]
+            p_hit += pr
+    q = softmax(xt / T, axis=1)
+    p = softmax(xd / T, axis=1)
+    a = [min(1.0, q[i, tok[i]] / p[i, tok[i]]) for i in range(g)]
+    closed = 0.0
+    for n in range(g + 1):
+        r = q[g] if n == g else np.maximum(q[n] - p[n], 0.0)
+        r = r / r.sum()
+        mass = r[np.argsort(-r, kind="stable")[:k]].sum()
+        pn = np.prod(a[:n]) * (1.0 - a[n] if n < g else 1.0)
+        closed += pn * mass
+    assert abs(p_hit - closed) < 1e-9, (p_hit, closed)
+    # an error outcome (n = -1) never hits
+    hit, count = o.cache_check(top[None], np.full((1, g + 1), -1, np.int32), np.array([-1], np.int32))
+    assert hit[0] == -1 and count == 0
+
+
 ALL_PINS = [
     pin_philox_vs_triton, pin_uniform_mapping, pin_uniform_statistics, pin_softmax, pin_argmax,
     pin_topk, pin_choice, pin_toy_closed_forms, pin_losslessness_toy_chain,
     pin_losslessness_random, pin_greedy, pin_low_temperature_limit, pin_expected_tokens,
     pin_toy_kl, pin_saguaro_toy_topk, pin_saguaro_bonus_position,
-    pin_saguaro_disjoint_supports, pin_saguaro_equal_distributions,
+    pin_saguaro_disjoint_supports, pin_saguaro_equal_distributions, pin_cache_hit_rate,
 ]

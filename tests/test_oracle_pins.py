@@ -85,3 +85,7 @@ def test_saguaro_disjoint_supports(orc):
 
 def test_saguaro_equal_distributions(orc):
     pins.pin_saguaro_equal_distributions(orc)
+
+
+def test_cache_hit_rate(orc):
+    pins.pin_cache_hit_rate(orc)
