@@ -305,6 +305,12 @@ def secondary(ssdv, workloads, dev, stream):
     by = sb.algorithmic_bytes()
     res["saguaro_B256_g6_V152064_f32"] = {"ms_per_round": ms, "rounds_per_s": 1e3 / ms, "bytes": by,
                                           "gbs": by / ms / 1e6, "frac_of_measured_hbm": by / ms / 1e6 / peak}
+    # the bonus top-k from the draft logits instead of the residual
+    ms_d = timeit(lambda: ssdv.saguaro_prespec(sb.target, sb.draft, 3, 0.8, 3, topk, tok, stream=stream,
+                                               source="draft"), 10)
+    res["saguaro_draft_topk_B256_g6_V152064_f32"] = {"ms_per_round": ms_d, "rounds_per_s": 1e3 / ms_d, "bytes": by,
+                                                     "gbs": by / ms_d / 1e6,
+                                                     "frac_of_measured_hbm": by / ms_d / 1e6 / peak}
     # the same round verified and pre-speculated: one fused call (with the
     # cache check) against the two separate calls
     ms_f = timeit(lambda: ssdv.verify_saguaro(sb.target, sb.draft, sb.draft_tokens, 3, 0.8, 3, stream=stream), 10)

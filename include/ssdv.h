@@ -66,6 +66,12 @@ typedef enum {
 
 typedef enum { SSD_BF16 = 0, SSD_F32 = 1 } ssd_dtype;
 
+/* Where Saguaro's predicted bonus tokens come from (SSD notes, section 3.1):
+ * the k largest entries of the residual r_j, or the draft's k most likely
+ * tokens (its k largest logits of row j; the target's at j = gamma, where
+ * there is no draft row). */
+typedef enum { SSD_TOPK_RESIDUAL = 0, SSD_TOPK_DRAFT = 1 } ssd_topk_source;
+
 #define SSD_MAX_GAMMA 31   /* largest gamma / gamma_max accepted                 */
 #define SSD_MAX_TOPK 8     /* largest k accepted by ssd_saguaro_prespec           */
 #define SSD_MAX_V (1 << 19)  /* fp32 units above ~440k need more than 16 CTAs */
@@ -178,7 +184,9 @@ ssd_status ssd_verify_ragged(const void* target_logits, const void* draft_logits
  *   r_j = (q_j - p_j)+ / sum (q_j - p_j)+  for j < gamma (q_j if that mass is
  *         zero), and r_gamma = q_gamma;
  *   bonus_topk[b, j, 0..k-1] = the k largest entries of r_j, descending, the
- *         lower index first among equal values;
+ *         lower index first among equal values (topk_source ==
+ *         SSD_TOPK_RESIDUAL), or the k largest draft logits of row j (target
+ *         logits at j = gamma), same order (SSD_TOPK_DRAFT);
  *   saguaro_tokens[b, j] = one sample from p_saguaro proportional to
  *         sqrt(p_D(v) * max(r_j(v), 1e-8)), p_D = p_j (q_gamma at j = gamma).
  *   target_logits [B, gamma+1, V], draft_logits [B, gamma, V];
@@ -188,7 +196,8 @@ ssd_status ssd_verify_ragged(const void* target_logits, const void* draft_logits
  *   errors as for verification (ssd_read_status).
  * Constraints: temperature > 0, 1 <= k <= SSD_MAX_TOPK, k <= V. */
 ssd_status ssd_saguaro_prespec(const void* target_logits, const void* draft_logits, ssd_dtype dtype,
-                               int B, int gamma, int V, int k, float temperature, uint64_t seed,
+                               int B, int gamma, int V, int k, ssd_topk_source topk_source,
+                               float temperature, uint64_t seed,
                                int32_t* bonus_topk, int32_t* saguaro_tokens, void* workspace,
                                size_t ws_bytes, void* stream);
 
@@ -209,7 +218,8 @@ size_t ssd_saguaro_workspace_bytes(int B, int gamma, int V);
  * Constraints: those of ssd_verify and ssd_saguaro_prespec. */
 ssd_status ssd_verify_saguaro(const void* target_logits, const void* draft_logits, ssd_dtype dtype,
                               const int32_t* draft_tokens, int B, int gamma, int V, int k,
-                              float temperature, uint64_t seed, int32_t* out_tokens,
+                              ssd_topk_source topk_source, float temperature, uint64_t seed,
+                              int32_t* out_tokens,
                               int32_t* n_accepted, int32_t* bonus_topk, int32_t* saguaro_tokens,
                               int32_t* hit, int32_t* n_hits, void* workspace, size_t ws_bytes,
                               void* stream);
@@ -249,11 +259,13 @@ ssd_status ssd_debug_rowstats(const void* target_logits, const void* draft_logit
  * stats [B, gamma+1, 10] float: 0 target log-sum, 1 draft log-sum (NaN at
  * j = gamma), 2 residual mass S_j (1 at j = gamma), 3 Zs = sum_v sqrt(p_D(v) *
  * max(r_j(v), 1e-8)), 4 p_saguaro(token), 5 r_j of top slot 0, 6 r_j of top
- * slot k-1, 7 NaN, 8, 9 the distances u - lo, hi - u of the Saguaro uniform to
- * the normalised CDF boundaries of the drawn token.
+ * slot k-1 (with SSD_TOPK_DRAFT: p_j of those slots, q_gamma at j = gamma),
+ * 7 NaN, 8, 9 the distances u - lo, hi - u of the Saguaro uniform to the
+ * normalised CDF boundaries of the drawn token.
  * Outputs and workspace as ssd_saguaro_prespec. */
 ssd_status ssd_debug_saguaro_stats(const void* target_logits, const void* draft_logits,
                                    ssd_dtype dtype, int B, int gamma, int V, int k,
+                                   ssd_topk_source topk_source,
                                    float temperature, uint64_t seed, int32_t* bonus_topk,
                                    int32_t* saguaro_tokens, float* stats, void* workspace,
                                    size_t ws_bytes, void* stream);

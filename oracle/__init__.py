@@ -64,12 +64,12 @@ def _declare(lib):
     lib.orc_topk.restype = None
     lib.orc_verify_request.argtypes = [c_int, c_int, P, P, c_double, P, P, P, c_double, P, P, P, P]
     lib.orc_verify_request.restype = c_int
-    lib.orc_saguaro_request.argtypes = [c_int, c_int, P, P, c_double, c_int, P, c_double, P, P, P, P, P]
+    lib.orc_saguaro_request.argtypes = [c_int, c_int, P, P, c_double, c_int, c_int, P, c_double, P, P, P, P, P]
     lib.orc_saguaro_request.restype = c_int
     lib.orc_verify_batch.argtypes = [P, P, c_int, P, c_int, c_int, c_int, P, P, c_float, c_u64,
                                      P, P, P, P, P, P, c_double, c_int]
     lib.orc_verify_batch.restype = c_int
-    lib.orc_saguaro_batch.argtypes = [P, P, c_int, c_int, c_int, c_int, c_int, c_float, c_u64,
+    lib.orc_saguaro_batch.argtypes = [P, P, c_int, c_int, c_int, c_int, c_int, c_int, c_float, c_u64,
                                       P, P, P, P, P, P, c_double, c_int]
     lib.orc_saguaro_position.argtypes = [c_int, P, P, c_double, P, P, P, P, P]
     lib.orc_saguaro_position.restype = None
@@ -92,6 +92,12 @@ def load(path: Optional[str] = None):
                 build()
             _lib = Oracle(_declare(ctypes.CDLL(LIBRARY)))
     return _lib
+
+
+def _src(source: str) -> int:
+    if source not in ("residual", "draft"):
+        raise ValueError(f"top-k source must be 'residual' or 'draft', got {source!r}")
+    return 0 if source == "residual" else 1
 
 
 def _ptr(a: Optional[np.ndarray]):
@@ -189,7 +195,10 @@ class Oracle:
                                         ctypes.byref(fk), _ptr(st))
         return dict(n=n, out=out, flag_pos=fp.value, flag_kind=fk.value, stats=st)
 
-    def saguaro_request(self, xt, xd, T, k, u_sag, stats: bool = False, band: float = FLAG_BAND):
+    def saguaro_request(self, xt, xd, T, k, u_sag, stats: bool = False, band: float = FLAG_BAND,
+                        source: str = "residual"):
+        """source: "residual" (top-k of r_j) or "draft" (top-k of the draft logits,
+        the target logits at j = gamma)."""
         xt = np.ascontiguousarray(xt, dtype=np.float64)
         g, V = xt.shape[0] - 1, xt.shape[1]
         xd = np.ascontiguousarray(xd, dtype=np.float64).reshape(g, V) if g > 0 else np.zeros((1, V))
@@ -199,7 +208,7 @@ class Oracle:
         kf = np.empty(g + 1, np.int32)
         tf = np.empty(g + 1, np.int32)
         st = np.empty((g + 1, NSTAT_SAGUARO), np.float64) if stats else None
-        self.lib.orc_saguaro_request(g, V, _ptr(xt), _ptr(xd), float(T), k, _ptr(u), float(band),
+        self.lib.orc_saguaro_request(g, V, _ptr(xt), _ptr(xd), float(T), k, _src(source), _ptr(u), float(band),
                                      _ptr(topk), _ptr(tok), _ptr(kf), _ptr(tf), _ptr(st))
         return dict(topk=topk, tokens=tok, topk_flag=kf, tok_flag=tf, stats=st)
 
@@ -253,7 +262,8 @@ class Oracle:
         return hit, count
 
     def saguaro_batch(self, target, draft, k: int, temperature: float, seed: int,
-                      stats: bool = False, nthreads: int = 1, req_ids=None, band: float = FLAG_BAND):
+                      stats: bool = False, nthreads: int = 1, req_ids=None, band: float = FLAG_BAND,
+                      source: str = "residual"):
         target, dt = _logit_array(target)
         draft, dd = _logit_array(draft)
         assert dt == dd
@@ -265,7 +275,7 @@ class Oracle:
         tf = np.empty((B, W), np.int32)
         st = np.empty((B, W, NSTAT_SAGUARO), np.float64) if stats else None
         rid = None if req_ids is None else np.ascontiguousarray(req_ids, dtype=np.int32).reshape(B)
-        rc = self.lib.orc_saguaro_batch(_ptr(target), _ptr(draft), dt, B, g, V, k,
+        rc = self.lib.orc_saguaro_batch(_ptr(target), _ptr(draft), dt, B, g, V, k, _src(source),
                                         float(temperature), seed, _ptr(topk), _ptr(tok), _ptr(kf),
                                         _ptr(tf), _ptr(st), _ptr(rid), float(band), nthreads)
         if rc != 0:

@@ -441,6 +441,11 @@ int orc_verify_request(int g, int V, const double* xt, const double* xd, double 
 /*   topk_j = the k largest entries of r_j;                                    */
 /*   s_j(v) = sqrt(p_D(v) * max(r_j(v), 1e-8)),  p_saguaro = s_j / sum s_j;    */
 /*   token_j = inverse-CDF draw from p_saguaro with u_sag[j].                  */
+/* src = 1 takes the bonus top-k from the draft logits instead ([SAG] §3.1    */
+/* `predict_bonus`: top-k of the draft logits, the draft's most likely        */
+/* tokens): the k largest draft logits of row j (j < g), the k largest target */
+/* logits at j = g (no draft row there); softmax is monotone, so these are    */
+/* the k most likely tokens of p_j (q_g); exact comparisons, never flagged.   */
 /* topk_flag[j]: bit t set when slot t is within the top-k ambiguity gap of a */
 /* neighbouring value; tok_flag[j]: 1 when the draw is within 1e-6 of a CDF   */
 /* boundary.  stats ((g+1) x 10): t_logsum, d_logsum, S, Zs = sum s,          */
@@ -454,7 +459,7 @@ static int topk_close(double a, double b) {
   return d <= ORC_TOPK_REL * m || d <= ORC_TOPK_ABS;
 }
 
-int orc_saguaro_request(int g, int V, const double* xt, const double* xd, double T, int k,
+int orc_saguaro_request(int g, int V, const double* xt, const double* xd, double T, int k, int src,
                         const double* u_sag, double band, int32_t* topk, int32_t* tokens,
                         int32_t* topk_flag, int32_t* tok_flag, double* stats) {
   if (stats) fill_nan(stats, (g + 1) * ORC_NSTAT_SAGUARO);
@@ -486,14 +491,26 @@ int orc_saguaro_request(int g, int V, const double* xt, const double* xd, double
       for (int v = 0; v < V; ++v) r[v] = q[v];
       pD = q;
     }
-    /* Bonus prediction: top-k of the residual (one more, to judge ambiguity). */
+    /* Bonus prediction: top-k of the residual (one more, to judge ambiguity),
+       or of the draft's (target's, at j = g) logits, then reported as
+       probabilities of that row. */
     int kk = k + 1 <= V ? k + 1 : V;
-    orc_topk(r, V, kk, idx, val);
     int flags = 0;
-    for (int t = 0; t < k; ++t) {
-      topk[j * k + t] = idx[t];
-      if (t + 1 < kk && topk_close(val[t], val[t + 1])) flags |= 1 << t;
-      if (t > 0 && topk_close(val[t - 1], val[t])) flags |= 1 << t;
+    if (src == 1) {
+#if ORC_MUTANT == 12
+      orc_topk(xt + (size_t)j * V, V, kk, idx, val);
+#else
+      orc_topk(j < g ? xd + (size_t)j * V : xt + (size_t)j * V, V, kk, idx, val);
+#endif
+      for (int t = 0; t < kk; ++t) val[t] = (j < g ? p : q)[idx[t]];
+      for (int t = 0; t < k; ++t) topk[j * k + t] = idx[t];
+    } else {
+      orc_topk(r, V, kk, idx, val);
+      for (int t = 0; t < k; ++t) {
+        topk[j * k + t] = idx[t];
+        if (t + 1 < kk && topk_close(val[t], val[t + 1])) flags |= 1 << t;
+        if (t > 0 && topk_close(val[t - 1], val[t])) flags |= 1 << t;
+      }
     }
     topk_flag[j] = flags;
     /* Saguaro sampling distribution (geometric mean of p_D and residual). */
@@ -597,6 +614,7 @@ typedef struct {
   float temp_scalar;
   uint64_t seed;
   int k;
+  int topk_src; /* saguaro: 0 residual, 1 draft logits */
   const int32_t* req_ids; /* nullable: request index used in the Philox counter */
   int32_t* out_a; /* verify: out_tokens     saguaro: bonus_topk    */
   int32_t* out_b; /* verify: n_accepted     saguaro: saguaro_tokens */
@@ -628,7 +646,7 @@ static void run_request(const orc_job* jb, int b, double* xt, double* xd) {
     for (int j = 0; j < g; ++j) orc_row_to_f64(jb->draft, jb->dtype, (size_t)b * gmax + j, V, xd + (size_t)j * V);
     double u[64];
     for (int j = 0; j <= g; ++j) u[j] = orc_uniform(jb->seed, rid, (uint32_t)j, 2u);
-    orc_saguaro_request(g, V, xt, xd, T, k, u, jb->band, jb->out_a + (size_t)b * W * k, jb->out_b + (size_t)b * W,
+    orc_saguaro_request(g, V, xt, xd, T, k, jb->topk_src, u, jb->band, jb->out_a + (size_t)b * W * k, jb->out_b + (size_t)b * W,
                         jb->flag_a + (size_t)b * W, jb->flag_b + (size_t)b * W,
                         jb->stats ? jb->stats + (size_t)b * W * ORC_NSTAT_SAGUARO : NULL);
     return;
@@ -721,7 +739,7 @@ int orc_verify_batch(const void* target, const void* draft, int dtype, const int
 
 /* Batched Saguaro pre-speculation.  bonus_topk [B, g+1, k], saguaro_tokens
  * [B, g+1], topk_flag / tok_flag [B, g+1], stats (nullable) [B, g+1, 10]. */
-int orc_saguaro_batch(const void* target, const void* draft, int dtype, int B, int g, int V, int k,
+int orc_saguaro_batch(const void* target, const void* draft, int dtype, int B, int g, int V, int k, int src,
                       float temperature, uint64_t seed, int32_t* bonus_topk, int32_t* saguaro_tokens,
                       int32_t* topk_flag, int32_t* tok_flag, double* stats, const int32_t* req_ids,
                       double band, int nthreads) {
@@ -739,6 +757,7 @@ int orc_saguaro_batch(const void* target, const void* draft, int dtype, int B, i
   jb.temp_scalar = temperature;
   jb.seed = seed;
   jb.k = k;
+  jb.topk_src = src;
   jb.out_a = bonus_topk;
   jb.out_b = saguaro_tokens;
   jb.flag_a = topk_flag;

@@ -362,7 +362,8 @@ struct FusedVerify {
 };
 
 static ssd_status saguaro_common(const void* target, const void* draft, ssd_dtype dtype, int B, int g, int V, int k,
-                                 float temperature, uint64_t seed, int32_t* bonus_topk, int32_t* tokens, float* stats,
+                                 ssd_topk_source src, float temperature, uint64_t seed, int32_t* bonus_topk,
+                                 int32_t* tokens, float* stats,
                                  void* workspace, size_t ws_bytes, void* stream, const FusedVerify& fv = FusedVerify()) {
   const int es = esize_of(dtype);
   const bool fused = fv.out_tokens != nullptr;
@@ -377,6 +378,8 @@ static ssd_status saguaro_common(const void* target, const void* draft, ssd_dtyp
     return fail(SSD_ERR_ALIGN, "a token / output pointer is not 4-byte aligned");
   if (B < 1 || g < 0 || g > SSD_MAX_GAMMA || V < 1 || V > SSD_MAX_V || k < 1 || k > SSD_MAX_TOPK || k > V)
     return fail(SSD_ERR_SHAPE, "bad shape B=%d gamma=%d V=%d k=%d", B, g, V, k);
+  if (src != SSD_TOPK_RESIDUAL && src != SSD_TOPK_DRAFT)
+    return fail(SSD_ERR_SHAPE, "unknown top-k source %d", static_cast<int>(src));
   if (!(temperature >= 1e-6f) || !isfinite(temperature))
     return fail(SSD_ERR_TEMPERATURE, "Saguaro needs a temperature in [1e-6, inf), got %g",
                 static_cast<double>(temperature));
@@ -452,6 +455,7 @@ static ssd_status saguaro_common(const void* target, const void* draft, ssd_dtyp
     a.B = nb;
     a.g = g;
     a.k = k;
+    a.topk_src = src == SSD_TOPK_DRAFT ? 1 : 0;
     a.req_base = b0;
     a.temperature = temperature;
     a.seed = seed;
@@ -482,26 +486,29 @@ static ssd_status saguaro_common(const void* target, const void* draft, ssd_dtyp
 }
 
 ssd_status ssd_saguaro_prespec(const void* target_logits, const void* draft_logits, ssd_dtype dtype, int B, int gamma,
-                               int V, int k, float temperature, uint64_t seed, int32_t* bonus_topk,
+                               int V, int k, ssd_topk_source topk_source, float temperature, uint64_t seed,
+                               int32_t* bonus_topk,
                                int32_t* saguaro_tokens, void* workspace, size_t ws_bytes, void* stream) {
   g_last_error.clear();
-  return saguaro_common(target_logits, draft_logits, dtype, B, gamma, V, k, temperature, seed, bonus_topk,
-                        saguaro_tokens, nullptr, workspace, ws_bytes, stream);
+  return saguaro_common(target_logits, draft_logits, dtype, B, gamma, V, k, topk_source, temperature, seed,
+                        bonus_topk, saguaro_tokens, nullptr, workspace, ws_bytes, stream);
 }
 
 ssd_status ssd_debug_saguaro_stats(const void* target_logits, const void* draft_logits, ssd_dtype dtype, int B,
-                                   int gamma, int V, int k, float temperature, uint64_t seed, int32_t* bonus_topk,
+                                   int gamma, int V, int k, ssd_topk_source topk_source, float temperature,
+                                   uint64_t seed, int32_t* bonus_topk,
                                    int32_t* saguaro_tokens, float* stats, void* workspace, size_t ws_bytes,
                                    void* stream) {
   g_last_error.clear();
   if (!stats) return fail(SSD_ERR_NULL, "stats is NULL");
-  return saguaro_common(target_logits, draft_logits, dtype, B, gamma, V, k, temperature, seed, bonus_topk,
-                        saguaro_tokens, stats, workspace, ws_bytes, stream);
+  return saguaro_common(target_logits, draft_logits, dtype, B, gamma, V, k, topk_source, temperature, seed,
+                        bonus_topk, saguaro_tokens, stats, workspace, ws_bytes, stream);
 }
 
 ssd_status ssd_verify_saguaro(const void* target_logits, const void* draft_logits, ssd_dtype dtype,
-                              const int32_t* draft_tokens, int B, int gamma, int V, int k, float temperature,
-                              uint64_t seed, int32_t* out_tokens, int32_t* n_accepted, int32_t* bonus_topk,
+                              const int32_t* draft_tokens, int B, int gamma, int V, int k,
+                              ssd_topk_source topk_source, float temperature, uint64_t seed, int32_t* out_tokens,
+                              int32_t* n_accepted, int32_t* bonus_topk,
                               int32_t* saguaro_tokens, int32_t* hit, int32_t* n_hits, void* workspace,
                               size_t ws_bytes, void* stream) {
   g_last_error.clear();
@@ -512,8 +519,8 @@ ssd_status ssd_verify_saguaro(const void* target_logits, const void* draft_logit
   fv.n_accepted = n_accepted;
   fv.hit = hit;
   fv.n_hits = n_hits;
-  return saguaro_common(target_logits, draft_logits, dtype, B, gamma, V, k, temperature, seed, bonus_topk,
-                        saguaro_tokens, nullptr, workspace, ws_bytes, stream, fv);
+  return saguaro_common(target_logits, draft_logits, dtype, B, gamma, V, k, topk_source, temperature, seed,
+                        bonus_topk, saguaro_tokens, nullptr, workspace, ws_bytes, stream, fv);
 }
 
 ssd_status ssd_cache_check(const int32_t* bonus_topk, const int32_t* out_tokens, const int32_t* n_accepted, int B,

@@ -320,30 +320,36 @@ __device__ __forceinline__ void butterfly_stats(MaxSum& t, MaxSum& d, ArgMax& a,
 // Top-K: a lane's K largest (weight, index) pairs, descending, and the merge
 // of a warp's lanes.
 // ---------------------------------------------------------------------------
-template <int K>
+// kNegInf: keys may be -inf (logits), so an empty slot is told apart by its
+// index; otherwise keys are finite and larger than the empty value -inf.
+template <int K, bool kNegInf = false>
 struct TopK {
+  static constexpr int kEmpty = 0x7FFFFFFF;  // index of an empty slot (ranks after everything)
   float v[K > 0 ? K : 1];
   int i[K > 0 ? K : 1];
   __device__ __forceinline__ void init() {
 #pragma unroll
     for (int s = 0; s < (K > 0 ? K : 1); ++s) {
-      v[s] = -1.f;
-      i[s] = 0x7FFFFFFF;
+      v[s] = -INFINITY;
+      i[s] = kEmpty;
     }
   }
-  // Insert (w, idx); indices arrive in increasing order per lane, so an equal
-  // weight never displaces an earlier (lower-index) entry.
+  // Whether (w, a later index) ranks before slot s: slot s is empty or w is
+  // larger.  Indices arrive in increasing order per lane, so an equal value
+  // never displaces an earlier (lower-index) entry.
+  __device__ __forceinline__ bool beats(float w, int s) const {
+    if constexpr (kNegInf) return i[s] == kEmpty || w > v[s];
+    return w > v[s];
+  }
   __device__ __forceinline__ void push(float w, int idx) {
     if constexpr (K > 0) {
-      if (!(w > v[K - 1])) return;
+      if (!beats(w, K - 1)) return;
 #pragma unroll
       for (int s = K - 1; s >= 0; --s) {
-        const float pv = (s > 0) ? v[s - 1] : INFINITY;
-        const int pi = (s > 0) ? i[s - 1] : 0;
-        if (w > pv) {
-          v[s] = pv;
-          i[s] = pi;
-        } else if (w > v[s]) {
+        if (s > 0 && beats(w, s - 1)) {
+          v[s] = v[s - 1];
+          i[s] = i[s - 1];
+        } else if (beats(w, s)) {
           v[s] = w;
           i[s] = idx;
         }
@@ -356,8 +362,8 @@ struct TopK {
       v[s] = v[s + 1];
       i[s] = i[s + 1];
     }
-    v[(K > 0 ? K : 1) - 1] = -1.f;
-    i[(K > 0 ? K : 1) - 1] = 0x7FFFFFFF;
+    v[(K > 0 ? K : 1) - 1] = -INFINITY;
+    i[(K > 0 ? K : 1) - 1] = kEmpty;
   }
 };
 
@@ -367,8 +373,8 @@ __device__ __forceinline__ bool ranks_before(float v1, int i1, float v2, int i2)
 
 // Merge the lanes' top-K lists of one warp; every lane returns the warp's
 // list in `out` (descending, lower index first among equals).
-template <int K>
-__device__ __forceinline__ void warp_merge_topk(TopK<K>& tk, float (&ov)[K], int (&oi)[K]) {
+template <int K, bool kNegInf>
+__device__ __forceinline__ void warp_merge_topk(TopK<K, kNegInf>& tk, float (&ov)[K], int (&oi)[K]) {
 #pragma unroll
   for (int r = 0; r < K; ++r) {
     float v = tk.v[0];
@@ -458,6 +464,11 @@ struct PieceRows {
       for (int j = 0; j < 4; ++j) w[j] = __float_as_uint(i0 + j < n ? static_cast<float>(g[i0 + j]) : -INFINITY);
     }
     return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  // The raw logits of vector k (target, draft).
+  __device__ __forceinline__ void raw(int k, float (&xt)[Elem<E>::kVec], float (&xd)[Elem<E>::kVec]) const {
+    Elem<E>::unpack(rt[k], xt);
+    Elem<E>::unpack(rd[k], xd);
   }
   template <typename WFun>
   __device__ __forceinline__ void weights(int k, const WFun& wfun, float (&w)[Elem<E>::kVec]) const {

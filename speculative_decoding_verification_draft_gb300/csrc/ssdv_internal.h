@@ -56,6 +56,7 @@ struct SagArgs {
   const void* target;       // [B, g+1, V]
   const void* draft;        // [B, g, V]
   int B, g, k;
+  int topk_src;             // 0: top-k of the residual; 1: of the draft logits (target logits at j = g)
   int req_base;             // request index of row 0 in the Philox counters
   float temperature;
   uint64_t seed;

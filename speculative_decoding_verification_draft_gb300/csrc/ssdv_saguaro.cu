@@ -94,13 +94,14 @@ __device__ __forceinline__ void unit_stats(const SagArgs& a, size_t u, float c, 
 
 // One warp: the k best of n candidates (value, index), descending, the lower
 // index first among equal values; every lane gets the list.  Candidates are
-// distinct, so each round takes the best one ranking after the previous pick.
+// distinct, so each round takes the best one ranking after the previous pick;
+// empty slots (index 0x7FFFFFFF) rank after everything.
 __device__ __forceinline__ void merge_candidates(const float* cv, const int* ci, int n, int k, float* ov, int* oi) {
   const int lane = threadIdx.x & 31;
   float lv = INFINITY;
   int li = -1;
   for (int s = 0; s < k; ++s) {
-    float bv = -1.f;
+    float bv = -INFINITY;
     int bi = 0x7FFFFFFF;
     for (int q = lane; q < n; q += 32) {
       const float v = cv[q];
@@ -127,24 +128,30 @@ __device__ __forceinline__ void merge_candidates(const float* cv, const int* ci,
   }
 }
 
-// This warp's pieces: weight sums into psum, top-8 into the unit's candidate
-// slots (when tk is wanted).  Returns true in the last warp of the unit to
-// arrive (every lane), after which the other warps' sums are visible.
-template <typename E, typename WFun, bool kTop>
+// Top-k keys of the residual kernel: the weights, or (draft source) the
+// draft logits -- the target logits at the bonus position.
+enum { kKeyNone = 0, kKeyWeight = 1, kKeyLogit = 2 };
+
+// This warp's pieces: weight sums into psum, top-8 (by kKey) into the unit's
+// candidate slots.  Returns true in the last warp of the unit to arrive
+// (every lane), after which the other warps' sums are visible.
+template <typename E, typename WFun, int kKey>
 __device__ __forceinline__ bool unit_pieces(const SagArgs& a, size_t u, int wi, const E* trow, const E* drow,
                                             const WFun& wfun, float* psum, int32_t* ticket) {
+  constexpr bool kTop = kKey != kKeyNone;
   constexpr int kVec = Elem<E>::kVec;
   const int lane = threadIdx.x & 31;
   const int V = a.geo.V, NP = a.geo.npiece, ppw = a.geo.ppw;
   const int pelems = kPieceVecs * kVec;
   const int p0 = wi * ppw;
   const int pn = min(ppw, NP - p0);
-  TopK<kTopK> tk;
+  TopK<kTopK, kKey == kKeyLogit> tk;
   tk.init();
-  // tau: the k-th largest of the lanes' best weights so far.  The warp holds
-  // k elements at or above it, so a smaller weight is not among the row's k
-  // largest and is not pushed (weights are >= 0; tau starts below them).
-  float tau = -1.f;
+  // tau: the k-th largest of the lanes' best keys so far.  The warp holds k
+  // elements at or above it, so a smaller key is not among the row's k
+  // largest and is not pushed.
+  const bool key_target = drow == nullptr;
+  float tau = -INFINITY;
   for (int j = 0; j < pn; ++j) {
     const int lo = (p0 + j) * pelems;
     PieceRows<E> pr;
@@ -156,14 +163,24 @@ __device__ __forceinline__ bool unit_pieces(const SagArgs& a, size_t u, int wi, 
       pr.weights(k, wfun, w);
       s += pair_sum(w);
       if constexpr (kTop) {
-        float wm = w[0];
+        float key[kVec];
+        if constexpr (kKey == kKeyLogit) {
+          float xt[kVec], xd[kVec];
+          pr.raw(k, xt, xd);
 #pragma unroll
-        for (int e = 1; e < kVec; ++e) wm = fmaxf(wm, w[e]);
-        if (__any_sync(0xFFFFFFFFu, wm >= tau)) {
-          const int base = lo + (4 * lane + k) * kVec;
+          for (int e = 0; e < kVec; ++e) key[e] = key_target ? xt[e] : xd[e];
+        } else {
+#pragma unroll
+          for (int e = 0; e < kVec; ++e) key[e] = w[e];
+        }
+        const int base = lo + (4 * lane + k) * kVec;
+        float km = key[0];  // elements past V are padding: weight 0, logit -inf
+#pragma unroll
+        for (int e = 1; e < kVec; ++e) km = fmaxf(km, key[e]);
+        if (__any_sync(0xFFFFFFFFu, km >= tau)) {
 #pragma unroll
           for (int e = 0; e < kVec; ++e)
-            if (w[e] >= tau && base + e < V) tk.push(w[e], base + e);
+            if (key[e] >= tau && base + e < V) tk.push(key[e], base + e);
         }
       }
     }
@@ -177,14 +194,14 @@ __device__ __forceinline__ bool unit_pieces(const SagArgs& a, size_t u, int wi, 
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
         tau = m;
         const unsigned hit = __ballot_sync(0xFFFFFFFFu, x == m);
-        if (lane == __ffs(hit) - 1) x = -2.f;
+        if (lane == __ffs(hit) - 1) x = -INFINITY;
       }
     }
   }
   if constexpr (kTop) {
     float mv[kTopK];
     int mi[kTopK];
-    warp_merge_topk<kTopK>(tk, mv, mi);
+    warp_merge_topk(tk, mv, mi);
     if (lane < kTopK) {
       float v = mv[0];
       int i = mi[0];
@@ -209,9 +226,10 @@ __device__ __forceinline__ bool unit_pieces(const SagArgs& a, size_t u, int wi, 
 
 // The last warp of a unit: its top-k from the warps' candidates (copied to
 // shared memory first) into bonus_topk, and the statistics of slots 0 and k-1
-// (weights over `total`).
+// as probabilities: weights over `total`, or (logit keys) exp2(x*c - mc) / z.
 __device__ __forceinline__ void write_topk(const SagArgs& a, size_t u, double total, float* s_cv, int* s_ci,
-                                          float* st) {
+                                          float* st, bool logit_keys = false, float c = 0.f, float mc = 0.f,
+                                          float z = 1.f) {
   const int lane = threadIdx.x & 31;
   const int n = a.npw * kTopK;
   for (int q = lane; q < n; q += 32) {
@@ -225,7 +243,10 @@ __device__ __forceinline__ void write_topk(const SagArgs& a, size_t u, double to
   if (lane == 0) {
     int32_t* out = a.bonus_topk + u * a.k;
     for (int s = 0; s < a.k; ++s) out[s] = (oi[s] >= 0 && oi[s] < a.geo.V) ? oi[s] : -1;
-    if (st) {
+    if (st && logit_keys) {
+      st[5] = fast_exp2(fmaf(ov[0], c, -mc)) / z;
+      st[6] = fast_exp2(fmaf(ov[a.k - 1], c, -mc)) / z;
+    } else if (st) {
       st[5] = static_cast<float>(static_cast<double>(ov[0]) / total);
       st[6] = static_cast<float>(static_cast<double>(ov[a.k - 1]) / total);
     }
@@ -237,7 +258,7 @@ __device__ __forceinline__ void write_topk(const SagArgs& a, size_t u, double to
 // ---------------------------------------------------------------------------
 // Kernel 2: residual sums and top-k.  Grid (warp groups, j, request).
 // ---------------------------------------------------------------------------
-template <typename E>
+template <typename E, int kKey>
 __global__ void __launch_bounds__(kS) residual_kernel(const SagArgs a) {
   extern __shared__ __align__(16) uint8_t dyn_smem[];
   __shared__ float4 sh_stats;
@@ -267,7 +288,7 @@ __global__ void __launch_bounds__(kS) residual_kernel(const SagArgs a) {
   const E* drow = bonus ? nullptr : static_cast<const E*>(a.draft) + (static_cast<size_t>(b) * a.g + j) * V;
   const PassAW<E> wf{c, scaled_max(s4.x, c), bonus ? 0.f : scaled_max(s4.z, c), bonus ? 0.f : s4.y / s4.w,
                      bonus ? 1 : 0};
-  if (!unit_pieces<E, PassAW<E>, true>(a, u, wi, trow, drow, wf, a.psum2, a.ticket2)) return;
+  if (!unit_pieces<E, PassAW<E>, kKey>(a, u, wi, trow, drow, wf, a.psum2, a.ticket2)) return;
 
   // The last warp: S_j, and the top-k unless the residual is empty (then the
   // mix kernel takes the top-k of q_j).
@@ -292,11 +313,14 @@ __global__ void __launch_bounds__(kS) residual_kernel(const SagArgs a) {
       st[2] = bonus ? 1.f : static_cast<float>(S / static_cast<double>(s4.y));
     }
   }
-  if (!err && (bonus || S > 0.0)) {
+  const bool logit_keys = kKey == kKeyLogit;
+  if (!err && (logit_keys || bonus || S > 0.0)) {
     __syncwarp();
     float* s_cv = reinterpret_cast<float*>(dyn_smem) + kSW * a.geo.npiece;
     int* s_ci = reinterpret_cast<int*>(s_cv + a.npw * kTopK);
-    write_topk(a, u, S, s_cv, s_ci, st);
+    // logit keys report p_j (q_gamma at the bonus position) of the slots
+    const float mc = bonus ? scaled_max(s4.x, c) : scaled_max(s4.z, c);
+    write_topk(a, u, S, s_cv, s_ci, st, logit_keys, c, mc, bonus ? s4.y : s4.w);
   }
 }
 
@@ -326,8 +350,10 @@ __global__ void __launch_bounds__(kS) mix_kernel(const SagArgs a) {
   const float mct = scaled_max(s4.x, c), mcd = bonus ? 0.f : scaled_max(s4.z, c);
   const MixW<E> mw{c, mct, mcd, bonus ? 0.f : s4.y / s4.w, target_only ? 1 : 0, bonus ? 1 : 0,
                    static_cast<float>(1.0 / sum_a), bonus ? 1.f / s4.y : 1.f / s4.w};
-  const bool fallback = !bonus && !(S > 0.0);  // empty residual: the top-k of q_j is taken here
-  const bool last = unit_pieces<E, MixW<E>, false>(a, u, wi, trow, drow, mw, a.psum3, a.ticket3);
+  // empty residual with the residual as the top-k source: the top-k of q_j
+  // is taken here
+  const bool fallback = a.topk_src == 0 && !bonus && !(S > 0.0);
+  const bool last = unit_pieces<E, MixW<E>, kKeyNone>(a, u, wi, trow, drow, mw, a.psum3, a.ticket3);
   if (!last) return;
 
   // The last warp: Zs, the draw, and (empty residual) the top-k of q_j.
@@ -383,8 +409,10 @@ __global__ void __launch_bounds__(kS) mix_kernel(const SagArgs a) {
   }
 }
 
-template __global__ void residual_kernel<uint16_t>(const SagArgs);
-template __global__ void residual_kernel<float>(const SagArgs);
+template __global__ void residual_kernel<uint16_t, kKeyWeight>(const SagArgs);
+template __global__ void residual_kernel<float, kKeyWeight>(const SagArgs);
+template __global__ void residual_kernel<uint16_t, kKeyLogit>(const SagArgs);
+template __global__ void residual_kernel<float, kKeyLogit>(const SagArgs);
 template __global__ void mix_kernel<uint16_t>(const SagArgs);
 template __global__ void mix_kernel<float>(const SagArgs);
 
@@ -393,11 +421,13 @@ namespace {
 template <typename E>
 cudaError_t launch_saguaro_t(const SagArgs& a, cudaStream_t stream) {
   const int smem = static_cast<int>(sizeof(float) * (kSW * a.geo.npiece) + 8 * a.npw * kTopK);
+  const void* resid = a.topk_src == 1 ? reinterpret_cast<const void*>(&residual_kernel<E, kKeyLogit>)
+                                      : reinterpret_cast<const void*>(&residual_kernel<E, kKeyWeight>);
   if (smem > 48 * 1024) {
-    cudaError_t e =
-        cudaFuncSetAttribute(reinterpret_cast<const void*>(&residual_kernel<E>), cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(resid, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&mix_kernel<E>), cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&mix_kernel<E>),
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
   }
   cudaLaunchAttribute pdl[1];
@@ -410,7 +440,8 @@ cudaError_t launch_saguaro_t(const SagArgs& a, cudaStream_t stream) {
   cfg.stream = stream;
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, residual_kernel<E>, a);
+  cudaError_t e = a.topk_src == 1 ? cudaLaunchKernelEx(&cfg, residual_kernel<E, kKeyLogit>, a)
+                                  : cudaLaunchKernelEx(&cfg, residual_kernel<E, kKeyWeight>, a);
   if (e != cudaSuccess) return e;
   return cudaLaunchKernelEx(&cfg, mix_kernel<E>, a);
 }

@@ -50,12 +50,12 @@ def _declare(lib):
     lib.ssd_verify_ragged.argtypes = [P, P, I, P, I, I, I, P, P, U64, P, P, P, SZ, P]
     lib.ssd_verify_noalloc.argtypes = [P, P, I, P, I, I, I, F, U64, P, P, P]
     lib.ssd_verify_pipelined.argtypes = [P, P, I, P, I, I, I, F, U64, P, P, P, SZ, P]
-    lib.ssd_saguaro_prespec.argtypes = [P, P, I, I, I, I, I, F, U64, P, P, P, SZ, P]
+    lib.ssd_saguaro_prespec.argtypes = [P, P, I, I, I, I, I, I, F, U64, P, P, P, SZ, P]
     lib.ssd_saguaro_workspace_bytes.argtypes = [I, I, I]
     lib.ssd_saguaro_workspace_bytes.restype = SZ
     lib.ssd_debug_rowstats.argtypes = [P, P, I, P, I, I, I, F, U64, P, P, P, P, SZ, P]
-    lib.ssd_debug_saguaro_stats.argtypes = [P, P, I, I, I, I, I, F, U64, P, P, P, P, SZ, P]
-    lib.ssd_verify_saguaro.argtypes = [P, P, I, P, I, I, I, I, F, U64, P, P, P, P, P, P, P, SZ, P]
+    lib.ssd_debug_saguaro_stats.argtypes = [P, P, I, I, I, I, I, I, F, U64, P, P, P, P, SZ, P]
+    lib.ssd_verify_saguaro.argtypes = [P, P, I, P, I, I, I, I, I, F, U64, P, P, P, P, P, P, P, SZ, P]
     lib.ssd_cache_check.argtypes = [P, P, P, I, I, I, P, P, P]
     lib.ssd_read_status.argtypes = [P, SZ, P, P]
     lib.ssd_debug_uniforms.argtypes = [U64, I, I, P, P]
@@ -106,6 +106,15 @@ def _dev(t: torch.Tensor, name: str, dtype=None) -> int:
     if dtype is not None and t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     return t.data_ptr()
+
+
+TOPK_SOURCES = {"residual": 0, "draft": 1}
+
+
+def _source(source: str) -> int:
+    if source not in TOPK_SOURCES:
+        raise ValueError(f"top-k source must be one of {sorted(TOPK_SOURCES)}, got {source!r}")
+    return TOPK_SOURCES[source]
 
 
 def _stream(stream) -> int:
@@ -277,8 +286,9 @@ def verify_ragged(target: torch.Tensor, draft: torch.Tensor, draft_tokens: torch
 
 def saguaro_prespec(target: torch.Tensor, draft: torch.Tensor, k: int, temperature: float, seed: int,
                     bonus_topk: Optional[torch.Tensor] = None, saguaro_tokens: Optional[torch.Tensor] = None,
-                    workspace: Optional[torch.Tensor] = None, stream=None):
-    """ssd_saguaro_prespec: returns (bonus_topk [B, g+1, k], saguaro_tokens [B, g+1])."""
+                    workspace: Optional[torch.Tensor] = None, stream=None, source: str = "residual"):
+    """ssd_saguaro_prespec: returns (bonus_topk [B, g+1, k], saguaro_tokens [B, g+1]).
+    source: "residual" (top-k of r_j) or "draft" (the draft's k largest logits)."""
     B, W, V = target.shape
     g = W - 1
     dev = target.device
@@ -289,7 +299,7 @@ def saguaro_prespec(target: torch.Tensor, draft: torch.Tensor, k: int, temperatu
     dptr = _dev(draft, "draft_logits", target.dtype) if g > 0 else None
     ws = _saguaro_workspace(B, g, V, dev, workspace)
     _check(lib().ssd_saguaro_prespec(_dev(target, "target_logits"), dptr, _dtype_code(target), B, g, V, int(k),
-                                     float(temperature), int(seed) & ((1 << 64) - 1),
+                                     _source(source), float(temperature), int(seed) & ((1 << 64) - 1),
                                      _dev(bonus_topk, "bonus_topk", torch.int32),
                                      _dev(saguaro_tokens, "saguaro_tokens", torch.int32), _dev(ws, "workspace"),
                                      ws.numel(), _stream(stream)))
@@ -298,7 +308,7 @@ def saguaro_prespec(target: torch.Tensor, draft: torch.Tensor, k: int, temperatu
 
 def verify_saguaro(target: torch.Tensor, draft: torch.Tensor, draft_tokens: torch.Tensor, k: int,
                    temperature: float, seed: int, workspace: Optional[torch.Tensor] = None, check: bool = True,
-                   stream=None):
+                   stream=None, source: str = "residual"):
     """ssd_verify_saguaro: one call for both; returns (out_tokens [B, g+1], n_accepted [B],
     bonus_topk [B, g+1, k], saguaro_tokens [B, g+1], hit [B] or None, n_hits [1] or None)."""
     B, W, V = target.shape
@@ -314,7 +324,7 @@ def verify_saguaro(target: torch.Tensor, draft: torch.Tensor, draft_tokens: torc
     dptr = _dev(draft, "draft_logits", target.dtype) if g > 0 else None
     tptr = _dev(draft_tokens, "draft_tokens", torch.int32) if g > 0 else None
     _check(lib().ssd_verify_saguaro(_dev(target, "target_logits"), dptr, _dtype_code(target), tptr, B, g, V, int(k),
-                                    float(temperature), int(seed) & ((1 << 64) - 1), _dev(out_tokens, "out_tokens"),
+                                    _source(source), float(temperature), int(seed) & ((1 << 64) - 1), _dev(out_tokens, "out_tokens"),
                                     _dev(n_accepted, "n_accepted"), _dev(bonus_topk, "bonus_topk"),
                                     _dev(saguaro_tokens, "saguaro_tokens"),
                                     _dev(hit, "hit") if check else None, _dev(n_hits, "n_hits") if check else None,
@@ -352,7 +362,7 @@ def debug_rowstats(target, draft, draft_tokens, temperature, seed, workspace=Non
     return out_tokens, n_accepted, stats
 
 
-def debug_saguaro_stats(target, draft, k, temperature, seed, workspace=None, stream=None):
+def debug_saguaro_stats(target, draft, k, temperature, seed, workspace=None, stream=None, source="residual"):
     """ssd_debug_saguaro_stats: (bonus_topk, saguaro_tokens, stats [B, g+1, 10])."""
     B, W, V = target.shape
     g = W - 1
@@ -363,7 +373,7 @@ def debug_saguaro_stats(target, draft, k, temperature, seed, workspace=None, str
     dptr = _dev(draft, "draft_logits", target.dtype) if g > 0 else None
     ws = _saguaro_workspace(B, g, V, dev, workspace)
     _check(lib().ssd_debug_saguaro_stats(_dev(target, "target_logits"), dptr, _dtype_code(target), B, g, V,
-                                         int(k), float(temperature), int(seed) & ((1 << 64) - 1),
+                                         int(k), _source(source), float(temperature), int(seed) & ((1 << 64) - 1),
                                          _dev(bonus_topk, "bonus_topk"), _dev(saguaro_tokens, "saguaro_tokens"),
                                          _dev(stats, "stats"), _dev(ws, "workspace"), ws.numel(),
                                          _stream(stream)))

@@ -593,10 +593,41 @@ def pin_cache_hit_rate(o):
     assert hit[0] == -1 and count == 0
 
 
+def pin_draft_topk(o):
+    """The bonus predictor of the SSD notes (section 3.1) takes the top-k of
+    the draft logits.  On the verification blog's toy tables (draft after
+    token 0: .55 .15 .10 .07 .06 .04 .03; after another token: .30 .20 .15
+    .12 .10 .08 .05) the draft top-3 is [0, 1, 2] in both rows and the
+    reported values are the printed probabilities.  On random logits with
+    planted ties it equals numpy's stable argsort of the negated logits (the
+    draft row for j < gamma, the target row at j = gamma), and the Saguaro
+    draw does not depend on where the top-k comes from."""
+    d0, d1, t0, t1 = toy_tables()
+    for p, q in [(d0, t0), (d1, t1)]:
+        xt = np.log(np.stack([q, q]))
+        xd = np.log(p)[None]
+        r = o.saguaro_request(xt, xd, 1.0, 3, [0.3, 0.3], stats=True, source="draft")
+        assert list(r["topk"][0]) == [0, 1, 2], r["topk"][0]
+        assert abs(r["stats"][0, 5] - p[0]) < 1e-12 and abs(r["stats"][0, 6] - p[2]) < 1e-12
+        assert list(r["topk"][1]) == list(np.argsort(-q, kind="stable")[:3])
+        assert r["topk_flag"][0] == 0
+    rng = np.random.Generator(np.random.PCG64(23))
+    V, g, k, T = 40, 3, 5, 0.7
+    xt = np.round(rng.normal(0, 1.0, (g + 1, V)), 1)
+    xd = np.round(rng.normal(0, 1.0, (g, V)), 1)
+    u = rng.random(g + 1)
+    r = o.saguaro_request(xt, xd, T, k, u, source="draft")
+    for j in range(g + 1):
+        row = xd[j] if j < g else xt[g]
+        assert list(r["topk"][j]) == list(np.argsort(-row, kind="stable")[:k]), j
+    r0 = o.saguaro_request(xt, xd, T, k, u, source="residual")
+    assert list(r["tokens"]) == list(r0["tokens"])
+
+
 ALL_PINS = [
     pin_philox_vs_triton, pin_uniform_mapping, pin_uniform_statistics, pin_softmax, pin_argmax,
     pin_topk, pin_choice, pin_toy_closed_forms, pin_losslessness_toy_chain,
     pin_losslessness_random, pin_greedy, pin_low_temperature_limit, pin_expected_tokens,
     pin_toy_kl, pin_saguaro_toy_topk, pin_saguaro_bonus_position,
-    pin_saguaro_disjoint_supports, pin_saguaro_equal_distributions, pin_cache_hit_rate,
+    pin_saguaro_disjoint_supports, pin_saguaro_equal_distributions, pin_cache_hit_rate, pin_draft_topk,
 ]

@@ -64,13 +64,15 @@ def test_host_validation_without_gpu(lib):
     assert L.ssd_verify(odd, p, 0, p, 1, 1, 8, 1.0, 0, p, p, p, 1 << 20, None) == 4
     assert L.ssd_verify(p, p, 0, p, 4, 2, 8, 1.0, 0, p, p, p, 8, None) == 9
     # Saguaro: k and temperature
-    assert L.ssd_saguaro_prespec(p, p, 0, 1, 1, 8, 9, 1.0, 0, p, p, p, 1 << 20, None) == 2
-    assert L.ssd_saguaro_prespec(p, p, 0, 1, 1, 8, 3, 0.0, 0, p, p, p, 1 << 20, None) == 6
-    assert L.ssd_saguaro_prespec(p, p, 0, 1, 1, 8, 3, 1.0, 0, p, p, None, 1 << 20, None) == 1
-    assert L.ssd_saguaro_prespec(p, p, 0, 4, 2, 8, 3, 1.0, 0, p, p, p, 8, None) == 9
+    assert L.ssd_saguaro_prespec(p, p, 0, 1, 1, 8, 9, 0, 1.0, 0, p, p, p, 1 << 20, None) == 2
+    assert L.ssd_saguaro_prespec(p, p, 0, 1, 1, 8, 3, 0, 0.0, 0, p, p, p, 1 << 20, None) == 6
+    assert L.ssd_saguaro_prespec(p, p, 0, 1, 1, 8, 3, 0, 1.0, 0, p, p, None, 1 << 20, None) == 1
+    assert L.ssd_saguaro_prespec(p, p, 0, 4, 2, 8, 3, 0, 1.0, 0, p, p, p, 8, None) == 9
+    assert L.ssd_saguaro_prespec(p, p, 0, 1, 1, 8, 3, 2, 1.0, 0, p, p, p, 1 << 20, None) == 2  # unknown source
     # fused call: greedy rejected; cache check: needs an output, k in range
-    assert L.ssd_verify_saguaro(p, p, 0, p, 1, 1, 8, 3, 0.0, 0, p, p, p, p, None, None, p, 1 << 20, None) == 6
-    assert L.ssd_verify_saguaro(p, p, 0, p, 1, 1, 8, 3, 1.0, 0, None, p, p, p, None, None, p, 1 << 20, None) == 1
+    assert L.ssd_verify_saguaro(p, p, 0, p, 1, 1, 8, 3, 0, 0.0, 0, p, p, p, p, None, None, p, 1 << 20, None) == 6
+    assert L.ssd_verify_saguaro(p, p, 0, p, 1, 1, 8, 3, 0, 1.0, 0, None, p, p, p, None, None, p, 1 << 20,
+                                None) == 1
     assert L.ssd_cache_check(p, p, p, 4, 2, 3, None, None, None) == 1
     assert L.ssd_cache_check(p, p, p, 4, 2, 9, p, None, None) == 2
     # Saguaro workspace: zero for a bad shape, grows with the vocabulary

@@ -19,20 +19,23 @@ def ssdv():
     return gc.cuda_lib()
 
 
-def separate_and_fused(ssdv, b, k, T, seed):
+def separate_and_fused(ssdv, b, k, T, seed, source="residual"):
     out_s, n_s = ssdv.verify(b.target, b.draft, b.draft_tokens, T, seed)
-    topk_s, tok_s = ssdv.saguaro_prespec(b.target, b.draft, k, T, seed)
-    out_f, n_f, topk_f, tok_f, hit, n_hits = ssdv.verify_saguaro(b.target, b.draft, b.draft_tokens, k, T, seed)
+    topk_s, tok_s = ssdv.saguaro_prespec(b.target, b.draft, k, T, seed, source=source)
+    out_f, n_f, topk_f, tok_f, hit, n_hits = ssdv.verify_saguaro(b.target, b.draft, b.draft_tokens, k, T, seed,
+                                                                 source=source)
     torch.cuda.synchronize()
     return [x.cpu().numpy() for x in (out_s, n_s, topk_s, tok_s, out_f, n_f, topk_f, tok_f, hit, n_hits)]
 
 
+@pytest.mark.parametrize("source", ["residual", "draft"])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("B,gamma,V,k", [(24, 4, 20000, 3), (5, 1, 4099, 8), (3, 0, 777, 2), (16, 6, 1000, 1)])
-def test_fused_equals_separate_calls(ssdv, dtype, B, gamma, V, k):
+def test_fused_equals_separate_calls(ssdv, dtype, B, gamma, V, k, source):
     batch = wl.zipf_batch(B, gamma, V, dtype=dtype, temperature=0.8, seed=V + B, sigma_range=(0.3, 1.2))
     b = batch.to("cuda")
-    out_s, n_s, topk_s, tok_s, out_f, n_f, topk_f, tok_f, hit, n_hits = separate_and_fused(ssdv, b, k, 0.8, 11)
+    out_s, n_s, topk_s, tok_s, out_f, n_f, topk_f, tok_f, hit, n_hits = separate_and_fused(ssdv, b, k, 0.8, 11,
+                                                                                           source)
     assert np.array_equal(out_s, out_f) and np.array_equal(n_s, n_f)
     assert np.array_equal(topk_s, topk_f) and np.array_equal(tok_s, tok_f)
     hit_o, count_o = gc.orc().cache_check(topk_f, out_f, n_f)

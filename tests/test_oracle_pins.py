@@ -89,3 +89,7 @@ def test_saguaro_equal_distributions(orc):
 
 def test_cache_hit_rate(orc):
     pins.pin_cache_hit_rate(orc)
+
+
+def test_draft_topk(orc):
+    pins.pin_draft_topk(orc)
