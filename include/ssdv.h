@@ -224,6 +224,24 @@ ssd_status ssd_verify_saguaro(const void* target_logits, const void* draft_logit
                               int32_t* hit, int32_t* n_hits, void* workspace, size_t ws_bytes,
                               void* stream);
 
+/* Verification of draft tokens sampled from the Saguaro distribution (SSD
+ * notes, sections 3.2 and 5.1: SSD is standard speculative decoding under
+ * Saguaro sampling).  Position i's draft token x_i was drawn from
+ *   p'_i(v) = sqrt(p_i(v) * max(r_i(v), 1e-8)) / sum_w sqrt(p_i(w) * max(r_i(w), 1e-8)),
+ *   r_i = (q_i - p_i)+ / sum (q_i - p_i)+  (q_i when that mass is zero),
+ * so p'_i takes p_i's place: accept iff u_i < min(1, q_i(x_i) / p'_i(x_i)),
+ * and the correction at the first rejection n comes from
+ * (q_n - p'_n)+ / sum (q_n - p'_n)+ (q_n if that mass is zero); the bonus from
+ * q_gamma.  Arguments and outputs as ssd_verify; temperature > 0.
+ *   workspace >= ssd_saguaro_workspace_bytes(B, gamma, V) bytes, zeroed once.
+ * Kernels: the streaming pass, the Saguaro residual and mix passes over the
+ * draft positions (no top-k, no draw), then the sampling kernel. */
+ssd_status ssd_verify_saguaro_draft(const void* target_logits, const void* draft_logits,
+                                    ssd_dtype dtype, const int32_t* draft_tokens, int B, int gamma,
+                                    int V, float temperature, uint64_t seed, int32_t* out_tokens,
+                                    int32_t* n_accepted, void* workspace, size_t ws_bytes,
+                                    void* stream);
+
 /* The Saguaro cache check (SSD notes, sections 3.3 and 4.1): a round hits the
  * pre-speculated cache when its correction / bonus token is among the bonus
  * tokens predicted for its acceptance length.

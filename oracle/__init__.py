@@ -62,12 +62,12 @@ def _declare(lib):
     lib.orc_choice.restype = c_int
     lib.orc_topk.argtypes = [P, c_int, c_int, P, P]
     lib.orc_topk.restype = None
-    lib.orc_verify_request.argtypes = [c_int, c_int, P, P, c_double, P, P, P, c_double, P, P, P, P]
+    lib.orc_verify_request.argtypes = [c_int, c_int, P, P, c_double, c_int, P, P, P, c_double, P, P, P, P]
     lib.orc_verify_request.restype = c_int
     lib.orc_saguaro_request.argtypes = [c_int, c_int, P, P, c_double, c_int, c_int, P, c_double, P, P, P, P, P]
     lib.orc_saguaro_request.restype = c_int
     lib.orc_verify_batch.argtypes = [P, P, c_int, P, c_int, c_int, c_int, P, P, c_float, c_u64,
-                                     P, P, P, P, P, P, c_double, c_int]
+                                     P, P, P, P, P, P, c_double, c_int, c_int]
     lib.orc_verify_batch.restype = c_int
     lib.orc_saguaro_batch.argtypes = [P, P, c_int, c_int, c_int, c_int, c_int, c_int, c_float, c_u64,
                                       P, P, P, P, P, P, c_double, c_int]
@@ -98,6 +98,12 @@ def _src(source: str) -> int:
     if source not in ("residual", "draft"):
         raise ValueError(f"top-k source must be 'residual' or 'draft', got {source!r}")
     return 0 if source == "residual" else 1
+
+
+def _dist(draft_dist: str) -> int:
+    if draft_dist not in ("draft", "saguaro"):
+        raise ValueError(f"draft distribution must be 'draft' or 'saguaro', got {draft_dist!r}")
+    return 0 if draft_dist == "draft" else 1
 
 
 def _ptr(a: Optional[np.ndarray]):
@@ -178,8 +184,11 @@ class Oracle:
         return r, ps
 
     # --- one request, explicit uniforms ----------------------------------
-    def verify_request(self, xt, xd, T, tok, u_acc, u_res, stats: bool = False, band: float = FLAG_BAND):
-        """xt: (g+1, V) fp64 target logits; xd: (g, V) draft logits; tok: (g,)."""
+    def verify_request(self, xt, xd, T, tok, u_acc, u_res, stats: bool = False, band: float = FLAG_BAND,
+                       draft_dist: str = "draft"):
+        """xt: (g+1, V) fp64 target logits; xd: (g, V) draft logits; tok: (g,).
+        draft_dist: "draft" (tokens sampled from p) or "saguaro" (from the
+        Saguaro distribution of each position, which then replaces p)."""
         xt = np.ascontiguousarray(xt, dtype=np.float64)
         g, V = xt.shape[0] - 1, xt.shape[1]
         xd = np.ascontiguousarray(xd, dtype=np.float64).reshape(g, V) if g > 0 else np.zeros((1, V))
@@ -190,7 +199,7 @@ class Oracle:
         out = np.empty(g + 1, np.int32)
         fp, fk = ctypes.c_int32(), ctypes.c_int32()
         st = np.empty((g + 1, NSTAT_VERIFY), np.float64) if stats else None
-        n = self.lib.orc_verify_request(g, V, _ptr(xt), _ptr(xd), float(T), _ptr(tok), _ptr(ua),
+        n = self.lib.orc_verify_request(g, V, _ptr(xt), _ptr(xd), float(T), _dist(draft_dist), _ptr(tok), _ptr(ua),
                                         _ptr(ur), float(band), _ptr(out), ctypes.byref(fp),
                                         ctypes.byref(fk), _ptr(st))
         return dict(n=n, out=out, flag_pos=fp.value, flag_kind=fk.value, stats=st)
@@ -215,7 +224,7 @@ class Oracle:
     # --- batches over typed logits, Philox uniforms ----------------------
     def verify_batch(self, target, draft, draft_tokens, temperature, seed: int,
                      gamma=None, stats: bool = False, nthreads: int = 1, req_ids=None,
-                     band: float = FLAG_BAND):
+                     band: float = FLAG_BAND, draft_dist: str = "draft"):
         """target [B, gmax+1, V], draft [B, gmax, V] (uint16 bf16 bits or float32).
 
         ``temperature``: a float, or a float32 array [B] (per request).
@@ -245,7 +254,8 @@ class Oracle:
         rid = None if req_ids is None else np.ascontiguousarray(req_ids, dtype=np.int32).reshape(B)
         rc = self.lib.orc_verify_batch(_ptr(target), _ptr(draft), dt, _ptr(tok), B, gmax, V,
                                        _ptr(gam), _ptr(temps), tscalar, seed, _ptr(out), _ptr(n),
-                                       _ptr(fp), _ptr(fk), _ptr(st), _ptr(rid), float(band), nthreads)
+                                       _ptr(fp), _ptr(fk), _ptr(st), _ptr(rid), float(band), nthreads,
+                                       _dist(draft_dist))
         if rc != 0:
             raise ValueError("oracle rejected the batch arguments")
         return dict(out_tokens=out, n_accepted=n, flag_pos=fp, flag_kind=fk, stats=st)

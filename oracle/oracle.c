@@ -289,11 +289,56 @@ typedef struct {
   double qx, px, a, S;
 } orc_position;
 
+/* The Saguaro sampling distribution of a position ([SAG] §3.2), written over
+ * p: p' = s / sum s with s = sqrt(p * max(r, 1e-8)), r = (q - p)+ / S (q when
+ * S <= 0).  r is scratch. */
+static void saguaro_draft_dist(int V, const double* q, double* p, double* r) {
+  double S = 0.0;
+  for (int v = 0; v < V; ++v) {
+    double d = q[v] - p[v];
+    r[v] = d > 0.0 ? d : 0.0;
+    S += r[v];
+  }
+  for (int v = 0; v < V; ++v) r[v] = S > 0.0 ? r[v] / S : q[v];
+  double Z = 0.0;
+  for (int v = 0; v < V; ++v) {
+    double rc = r[v] > ORC_SAGUARO_CLAMP ? r[v] : ORC_SAGUARO_CLAMP;
+    p[v] = sqrt(p[v] * rc);
+    Z += p[v];
+  }
+  for (int v = 0; v < V; ++v) p[v] /= Z;
+}
+
+/* sag = 1: the draft tokens were sampled from the Saguaro distribution p' of
+ * each position instead of p ([SAG] §5.1: SSD is standard SD under Saguaro
+ * sampling), so p' takes p's place in the accept test and the residual. */
 static orc_position position_quantities(int V, const double* ti, const double* di, double T, int x,
-                                        double* q, double* p, double* r) {
+                                        double* q, double* p, double* r, int sag) {
   orc_position P;
   orc_softmax(ti, V, T, q, &P.mt, &P.lst);
   orc_softmax(di, V, T, p, &P.md, &P.lsd);
+  if (sag) {
+    saguaro_draft_dist(V, q, p, r);
+    P.qx = q[x];
+    P.px = p[x];
+#if ORC_MUTANT == 13
+    { /* mutant: the accept test keeps the draft's p(x) */
+      double log_q = (ti[x] - P.mt) / T - P.lst;
+      double log_p = (di[x] - P.md) / T - P.lsd;
+      double ratio = exp(log_q - log_p);
+      P.a = ratio < 1.0 ? ratio : 1.0;
+    }
+#else
+    P.a = P.px > 0.0 ? (q[x] < P.px ? q[x] / P.px : 1.0) : 1.0;
+#endif
+    P.S = 0.0;
+    for (int v = 0; v < V; ++v) {
+      double d = q[v] - p[v];
+      r[v] = d > 0.0 ? d : 0.0;
+      P.S += r[v];
+    }
+    return P;
+  }
   P.qx = q[x];
   P.px = p[x];
   /* a = min(1, q(x) / p(x)).  The ratio is evaluated as exp(log q(x) -
@@ -324,7 +369,7 @@ static orc_position position_quantities(int V, const double* ti, const double* d
   return P;
 }
 
-int orc_verify_request(int g, int V, const double* xt, const double* xd, double T,
+int orc_verify_request(int g, int V, const double* xt, const double* xd, double T, int sag,
                        const int32_t* tok, const double* u_acc, const double* u_res, double band,
                        int32_t* out, int32_t* flag_pos, int32_t* flag_kind, double* stats) {
   for (int i = 0; i <= g; ++i) out[i] = -1;
@@ -363,7 +408,7 @@ int orc_verify_request(int g, int V, const double* xt, const double* xd, double 
 
   if (stats) { /* every position's quantities, whether or not it is reached */
     for (int i = 0; i < g; ++i) {
-      orc_position P = position_quantities(V, xt + (size_t)i * V, xd + (size_t)i * V, T, tok[i], q, p, r);
+      orc_position P = position_quantities(V, xt + (size_t)i * V, xd + (size_t)i * V, T, tok[i], q, p, r, sag);
       double* s = stats + i * ORC_NSTAT_VERIFY;
       s[0] = P.mt;
       s[1] = P.lst;
@@ -382,7 +427,7 @@ int orc_verify_request(int g, int V, const double* xt, const double* xd, double 
 
   int n = g;
   for (int i = 0; i < g; ++i) {
-    orc_position P = position_quantities(V, xt + (size_t)i * V, xd + (size_t)i * V, T, tok[i], q, p, r);
+    orc_position P = position_quantities(V, xt + (size_t)i * V, xd + (size_t)i * V, T, tok[i], q, p, r, sag);
     double u = u_acc[i];
     if (*flag_pos < 0 && fabs(u - P.a) < band) {
       *flag_pos = i;
@@ -615,6 +660,7 @@ typedef struct {
   uint64_t seed;
   int k;
   int topk_src; /* saguaro: 0 residual, 1 draft logits */
+  int sag;      /* verify: draft tokens sampled from the Saguaro distribution */
   const int32_t* req_ids; /* nullable: request index used in the Philox counter */
   int32_t* out_a; /* verify: out_tokens     saguaro: bonus_topk    */
   int32_t* out_b; /* verify: n_accepted     saguaro: saguaro_tokens */
@@ -667,7 +713,7 @@ static void run_request(const orc_job* jb, int b, double* xt, double* xd) {
     ur[i] = orc_uniform(jb->seed, rid, (uint32_t)i, 1u);
   }
   int32_t fp, fk;
-  int n = orc_verify_request(g, V, xt, xd, T, jb->draft_tokens + (size_t)b * gmax, ua, ur, jb->band, out, &fp, &fk,
+  int n = orc_verify_request(g, V, xt, xd, T, jb->sag, jb->draft_tokens + (size_t)b * gmax, ua, ur, jb->band, out, &fp, &fk,
                              jb->stats ? jb->stats + (size_t)b * W * ORC_NSTAT_VERIFY : NULL);
   if (n < 0) {
     for (int t = 0; t < W; ++t) out[t] = -1;
@@ -711,7 +757,7 @@ int orc_verify_batch(const void* target, const void* draft, int dtype, const int
                      int B, int gmax, int V, const int32_t* gamma, const float* temp,
                      float temp_scalar, uint64_t seed, int32_t* out_tokens, int32_t* n_accepted,
                      int32_t* flag_pos, int32_t* flag_kind, double* stats, const int32_t* req_ids,
-                     double band, int nthreads) {
+                     double band, int nthreads, int sag) {
   orc_job jb;
   memset(&jb, 0, sizeof jb);
   jb.req_ids = req_ids;
@@ -733,6 +779,7 @@ int orc_verify_batch(const void* target, const void* draft, int dtype, const int
   jb.flag_b = flag_kind;
   jb.stats = stats;
   jb.saguaro = 0;
+  jb.sag = sag;
   jb.nthreads = nthreads;
   return run_batch(jb);
 }

@@ -76,7 +76,8 @@ SagLayout saguaro_layout(int B, int g, int V) {
   L.ticket3 = round_up(L.ticket2 + 4 * units, 256);
   L.rowstat = round_up(L.ticket3 + 4 * units, 256);
   L.rowsum = L.rowstat + units * sizeof(float4);
-  L.part = round_up(L.rowsum + units * sizeof(double), 256);
+  L.zsum = L.rowsum + units * sizeof(double);
+  L.part = round_up(L.zsum + units * sizeof(float), 256);
   L.psum2 = L.part + units * kMaxChunks * 2 * sizeof(float4);
   L.psum3 = round_up(L.psum2 + units * np * sizeof(float), 256);
   L.cand_v = round_up(L.psum3 + units * np * sizeof(float), 256);
@@ -190,6 +191,8 @@ ssd_status verify_common(const void* target, const void* draft, ssd_dtype dtype,
   a.psum = reinterpret_cast<float*>(half + L.blocks);
   a.stats = stats;
   a.debug = stats ? 1 : 0;
+  a.sag_S = nullptr;
+  a.sag_Zs = nullptr;
   a.geo = geo;
   // Launch in segments of at most 65535 requests (the grid's third
   // dimension; SSDV_SEGMENT sets a smaller size).  Each segment keeps its
@@ -455,6 +458,7 @@ static ssd_status saguaro_common(const void* target, const void* draft, ssd_dtyp
     a.B = nb;
     a.g = g;
     a.k = k;
+    a.nj = W;
     a.topk_src = src == SSD_TOPK_DRAFT ? 1 : 0;
     a.req_base = b0;
     a.temperature = temperature;
@@ -470,6 +474,7 @@ static ssd_status saguaro_common(const void* target, const void* draft, ssd_dtyp
     a.cand_i = reinterpret_cast<int32_t*>(ws + L.cand_i) + u0 * npw * SSD_MAX_TOPK;
     a.rowstat = reinterpret_cast<float4*>(ws + L.rowstat) + u0;
     a.rowsum = reinterpret_cast<double*>(ws + L.rowsum) + u0;
+    a.zsum = nullptr;
     a.ticket2 = v.ticket;
     a.ticket3 = reinterpret_cast<int32_t*>(ws + L.ticket3) + u0;
     a.status = status;
@@ -521,6 +526,105 @@ ssd_status ssd_verify_saguaro(const void* target_logits, const void* draft_logit
   fv.n_hits = n_hits;
   return saguaro_common(target_logits, draft_logits, dtype, B, gamma, V, k, topk_source, temperature, seed,
                         bonus_topk, saguaro_tokens, nullptr, workspace, ws_bytes, stream, fv);
+}
+
+ssd_status ssd_verify_saguaro_draft(const void* target_logits, const void* draft_logits, ssd_dtype dtype,
+                                    const int32_t* draft_tokens, int B, int gamma, int V, float temperature,
+                                    uint64_t seed, int32_t* out_tokens, int32_t* n_accepted, void* workspace,
+                                    size_t ws_bytes, void* stream) {
+  g_last_error.clear();
+  const int es = esize_of(dtype);
+  const int g = gamma;
+  if (es == 0) return fail(SSD_ERR_DTYPE, "unknown dtype %d", static_cast<int>(dtype));
+  if (!target_logits || !out_tokens || !n_accepted || !workspace || (g > 0 && (!draft_logits || !draft_tokens)))
+    return fail(SSD_ERR_NULL, "a required pointer is NULL");
+  if (B < 1 || g < 0 || g > SSD_MAX_GAMMA || V < 1 || V > SSD_MAX_V)
+    return fail(SSD_ERR_SHAPE, "bad shape B=%d gamma=%d V=%d", B, g, V);
+  if (!(temperature >= 1e-6f) || !isfinite(temperature))
+    return fail(SSD_ERR_TEMPERATURE, "Saguaro sampling needs a temperature in [1e-6, inf), got %g",
+                static_cast<double>(temperature));
+  if (!aligned_to(target_logits, es) || (draft_logits && !aligned_to(draft_logits, es)) ||
+      !aligned_to(out_tokens, 4) || !aligned_to(n_accepted, 4) || (draft_tokens && !aligned_to(draft_tokens, 4)) ||
+      !aligned_to(workspace, 16))
+    return fail(SSD_ERR_ALIGN, "a pointer is not aligned to its element size (workspace: 16 bytes)");
+  const SagLayout L = saguaro_layout(B, g, V);
+  if (ws_bytes < L.total)
+    return fail(SSD_ERR_WORKSPACE, "workspace of %zu bytes < %zu required", ws_bytes, L.total);
+  const bool aligned = aligned_to(target_logits, 16) && (!draft_logits || aligned_to(draft_logits, 16)) &&
+                       ((static_cast<size_t>(V) * es) % 16 == 0);
+  ChunkGeometry geo;
+  int smem = 0;
+  ssd_status st = choose_chunks(V, es, aligned, &geo, &smem);
+  if (st != SSD_OK) return st;
+  const int W = g + 1;
+  if (static_cast<long long>(B) * W * geo.nchunk >= (1LL << 31)) return fail(SSD_ERR_SHAPE, "grid too large");
+  ChunkGeometry sgeo = geo;
+  sgeo.ppw = std::max(kSagMinPpw, env_int("SSDV_SAG_PPW", 8));
+  const int npw = (geo.npiece + sgeo.ppw - 1) / sgeo.ppw;
+  geo.ppw = std::max(1, env_int("SSDV_PPW", 2));
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* status = reinterpret_cast<int32_t*>(ws);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // Per segment of requests: the streaming kernel (records and the draft
+  // tokens' logits), the Saguaro residual and mix passes over positions
+  // 0..gamma-1 (residual masses S_i and normalisers Zs, no top-k, no draw),
+  // then the sampling kernel with p' in place of p.
+  int seg = env_int("SSDV_SAG_SEGMENT", 65535);
+  seg = std::max(1, std::min(seg, 65535));
+  for (int b0 = 0; b0 < B; b0 += seg) {
+    const int nb = B - b0 < seg ? B - b0 : seg;
+    const size_t u0 = static_cast<size_t>(b0) * W;
+    VerifyArgs v = {};
+    v.target = static_cast<const uint8_t*>(target_logits) + u0 * V * es;
+    v.draft = draft_logits ? static_cast<const uint8_t*>(draft_logits) + static_cast<size_t>(b0) * g * V * es
+                           : nullptr;
+    v.draft_tokens = draft_tokens ? draft_tokens + static_cast<size_t>(b0) * g : nullptr;
+    v.B = nb;
+    v.gmax = g;
+    v.req_base = b0;
+    v.temp_scalar = temperature;
+    v.seed = seed;
+    v.out_tokens = out_tokens + u0;
+    v.n_accepted = n_accepted + b0;
+    v.part = reinterpret_cast<float4*>(ws + L.part) + u0 * geo.nchunk * 2;
+    v.psum = reinterpret_cast<float*>(ws + L.psum2) + u0 * geo.npiece;
+    v.ticket = reinterpret_cast<int32_t*>(ws + L.ticket2) + u0;
+    v.status = status;
+    v.sag_S = reinterpret_cast<double*>(ws + L.rowsum) + u0;
+    v.sag_Zs = reinterpret_cast<float*>(ws + L.zsum) + u0;
+    v.first = b0 == 0 ? 1 : 0;
+    v.geo = geo;
+    cudaError_t e = launch_stream(v, es, smem, s);
+    if (e != cudaSuccess) return cuda_fail(e, "streaming launch");
+    if (g > 0) {
+      SagArgs a = {};
+      a.target = v.target;
+      a.draft = v.draft;
+      a.B = nb;
+      a.g = g;
+      a.k = 0;
+      a.nj = g;
+      a.req_base = b0;
+      a.temperature = temperature;
+      a.seed = seed;
+      a.npw = npw;
+      a.part = v.part;
+      a.psum2 = reinterpret_cast<float*>(ws + L.psum2) + u0 * geo.npiece;
+      a.psum3 = reinterpret_cast<float*>(ws + L.psum3) + u0 * geo.npiece;
+      a.rowstat = reinterpret_cast<float4*>(ws + L.rowstat) + u0;
+      a.rowsum = const_cast<double*>(v.sag_S);
+      a.zsum = const_cast<float*>(v.sag_Zs);
+      a.ticket2 = v.ticket;
+      a.ticket3 = reinterpret_cast<int32_t*>(ws + L.ticket3) + u0;
+      a.status = status;
+      a.geo = sgeo;
+      e = launch_saguaro(a, es, s);
+      if (e != cudaSuccess) return cuda_fail(e, "saguaro launch");
+    }
+    e = launch_sample(v, es, s);
+    if (e != cudaSuccess) return cuda_fail(e, "sampling launch");
+  }
+  return SSD_OK;
 }
 
 ssd_status ssd_cache_check(const int32_t* bonus_topk, const int32_t* out_tokens, const int32_t* n_accepted, int B,

@@ -43,6 +43,11 @@ struct VerifyArgs {
   int32_t* status;             // workspace [1]: device error bits
   float* stats;                // [B, gmax+1, SSD_NSTAT_VERIFY] or null (debug)
   int debug;                   // 1: decide and report every position (statistics)
+  const double* sag_S;         // [B, gmax+1] or null: residual masses S_i (weight units) of the Saguaro
+                               // passes; given, the draft tokens were sampled from the Saguaro
+                               // distribution p' of their position, which replaces p in the accept test
+                               // and the residual
+  const float* sag_Zs;         // [B, gmax+1]: the Saguaro normalisers sum_v sqrt(p max(r, 1e-8))
   int first;                   // 1: every streaming CTA waits for the previous kernel (the first
                                // segment of a call); 0: only the first CTA waits (a later segment, or
                                // a pipelined call)
@@ -55,14 +60,16 @@ struct VerifyArgs {
 struct SagArgs {
   const void* target;       // [B, g+1, V]
   const void* draft;        // [B, g, V]
-  int B, g, k;
+  int B, g, k;               // k = 0: no top-k
+  int nj;                   // positions j = 0 .. nj-1 of every request are processed (g + 1, or g)
   int topk_src;             // 0: top-k of the residual; 1: of the draft logits (target logits at j = g)
   int req_base;             // request index of row 0 in the Philox counters
   float temperature;
   uint64_t seed;
   int npw;                  // warps per unit (ceil(npiece / ppw))
   int32_t* bonus_topk;      // [B, g+1, k]
-  int32_t* saguaro_tokens;  // [B, g+1]
+  int32_t* saguaro_tokens;  // [B, g+1], or null: no draw (the normalisers Zs are still kept)
+  float* zsum;              // workspace [units] or null: Zs of every unit
   float* stats;             // [B, g+1, SSD_NSTAT_SAGUARO] or null
   const float4* part;       // workspace [units, nchunk, 2]: the streaming kernel's records
   float* psum2;             // workspace [units, npiece]: residual (or target) piece sums
@@ -91,6 +98,8 @@ ssd_status choose_chunks(int V, int esize, bool aligned, ChunkGeometry* geo, int
 // Streaming statistics kernel followed by the decision / sampling kernel (both
 // with programmatic dependent launch; each waits for its predecessor).
 cudaError_t launch_verify(const VerifyArgs& a, int esize, int smem_bytes, cudaStream_t stream);
+// The sampling kernel alone (after the Saguaro passes it reads).
+cudaError_t launch_sample(const VerifyArgs& a, int esize, cudaStream_t stream);
 // The streaming kernel alone (Saguaro's first kernel).
 cudaError_t launch_stream(const VerifyArgs& a, int esize, int smem_bytes, cudaStream_t stream);
 // Saguaro's residual and mix kernels (each waits for its predecessor).
@@ -104,7 +113,7 @@ cudaError_t launch_cache_check(const int32_t* bonus_topk, const int32_t* out_tok
 
 // Saguaro workspace layout (byte offsets from the workspace start; status at 0).
 struct SagLayout {
-  size_t ticket2, ticket3, rowstat, rowsum, part, psum2, psum3, cand_v, cand_i, total;
+  size_t ticket2, ticket3, rowstat, rowsum, zsum, part, psum2, psum3, cand_v, cand_i, total;
 };
 constexpr int kSagMinPpw = 2;  // pieces per warp of the Saguaro kernels, at least
 SagLayout saguaro_layout(int B, int g, int V);

@@ -302,11 +302,12 @@ __global__ void __launch_bounds__(kS) residual_kernel(const SagArgs a) {
     a.rowstat[u] = s4;
     a.rowsum[u] = err ? NAN : S;
     a.ticket3[u] = 0;  // the mix kernel's counter starts at zero (read after this grid completes)
+    a.ticket2[u] = 0;  // the last arrival: zero again for a later kernel of the call
     if (err) {
       // a staging wait of the streaming kernel ran out: this unit's outputs are -1
       atomicOr(a.status, 1 << SSD_ERR_TIMEOUT);
       for (int s = 0; s < a.k; ++s) a.bonus_topk[u * a.k + s] = -1;
-      a.saguaro_tokens[u] = -1;
+      if (a.saguaro_tokens) a.saguaro_tokens[u] = -1;
     } else if (st) {
       st[0] = logf(s4.y) - fmaf(s4.x, c, -scaled_max(s4.x, c)) * 0.6931471805599453f;
       st[1] = bonus ? NAN : logf(s4.w) - fmaf(s4.z, c, -scaled_max(s4.z, c)) * 0.6931471805599453f;
@@ -314,7 +315,7 @@ __global__ void __launch_bounds__(kS) residual_kernel(const SagArgs a) {
     }
   }
   const bool logit_keys = kKey == kKeyLogit;
-  if (!err && (logit_keys || bonus || S > 0.0)) {
+  if (kKey != kKeyNone && !err && (logit_keys || bonus || S > 0.0)) {
     __syncwarp();
     float* s_cv = reinterpret_cast<float*>(dyn_smem) + kSW * a.geo.npiece;
     int* s_ci = reinterpret_cast<int*>(s_cv + a.npw * kTopK);
@@ -352,7 +353,7 @@ __global__ void __launch_bounds__(kS) mix_kernel(const SagArgs a) {
                    static_cast<float>(1.0 / sum_a), bonus ? 1.f / s4.y : 1.f / s4.w};
   // empty residual with the residual as the top-k source: the top-k of q_j
   // is taken here
-  const bool fallback = a.topk_src == 0 && !bonus && !(S > 0.0);
+  const bool fallback = a.k > 0 && a.topk_src == 0 && !bonus && !(S > 0.0);
   const bool last = unit_pieces<E, MixW<E>, kKeyNone>(a, u, wi, trow, drow, mw, a.psum3, a.ticket3);
   if (!last) return;
 
@@ -360,6 +361,8 @@ __global__ void __launch_bounds__(kS) mix_kernel(const SagArgs a) {
   RowPieces rp;
   float* s_pieces = reinterpret_cast<float*>(dyn_smem) + warp * a.geo.npiece;
   rp.load(a.psum3 + u * a.geo.npiece, a.geo.npiece, s_pieces);
+  if (a.zsum && lane == 0) a.zsum[u] = static_cast<float>(rp.total);
+  if (!a.saguaro_tokens) return;  // the normaliser is all a later kernel needs
   const float u_sag = unit_draws(a.seed, a.req_base + b, j).saguaro;
   const RowDraw d = warp_locate_row<E>(rp, static_cast<double>(u_sag), trow, drow, V, a.geo.bulk != 0, mw);
   float* st = a.stats ? a.stats + u * SSD_NSTAT_SAGUARO : nullptr;
@@ -413,6 +416,8 @@ template __global__ void residual_kernel<uint16_t, kKeyWeight>(const SagArgs);
 template __global__ void residual_kernel<float, kKeyWeight>(const SagArgs);
 template __global__ void residual_kernel<uint16_t, kKeyLogit>(const SagArgs);
 template __global__ void residual_kernel<float, kKeyLogit>(const SagArgs);
+template __global__ void residual_kernel<uint16_t, kKeyNone>(const SagArgs);
+template __global__ void residual_kernel<float, kKeyNone>(const SagArgs);
 template __global__ void mix_kernel<uint16_t>(const SagArgs);
 template __global__ void mix_kernel<float>(const SagArgs);
 
@@ -421,8 +426,10 @@ namespace {
 template <typename E>
 cudaError_t launch_saguaro_t(const SagArgs& a, cudaStream_t stream) {
   const int smem = static_cast<int>(sizeof(float) * (kSW * a.geo.npiece) + 8 * a.npw * kTopK);
-  const void* resid = a.topk_src == 1 ? reinterpret_cast<const void*>(&residual_kernel<E, kKeyLogit>)
-                                      : reinterpret_cast<const void*>(&residual_kernel<E, kKeyWeight>);
+  const int key = a.k == 0 ? kKeyNone : (a.topk_src == 1 ? kKeyLogit : kKeyWeight);
+  const void* resid = key == kKeyLogit    ? reinterpret_cast<const void*>(&residual_kernel<E, kKeyLogit>)
+                      : key == kKeyWeight ? reinterpret_cast<const void*>(&residual_kernel<E, kKeyWeight>)
+                                          : reinterpret_cast<const void*>(&residual_kernel<E, kKeyNone>);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(resid, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess)
@@ -434,14 +441,15 @@ cudaError_t launch_saguaro_t(const SagArgs& a, cudaStream_t stream) {
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((a.npw + kSW - 1) / kSW, a.g + 1, a.B);
+  cfg.gridDim = dim3((a.npw + kSW - 1) / kSW, a.nj, a.B);
   cfg.blockDim = dim3(kS, 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cfg.stream = stream;
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
-  cudaError_t e = a.topk_src == 1 ? cudaLaunchKernelEx(&cfg, residual_kernel<E, kKeyLogit>, a)
-                                  : cudaLaunchKernelEx(&cfg, residual_kernel<E, kKeyWeight>, a);
+  cudaError_t e = key == kKeyLogit    ? cudaLaunchKernelEx(&cfg, residual_kernel<E, kKeyLogit>, a)
+                  : key == kKeyWeight ? cudaLaunchKernelEx(&cfg, residual_kernel<E, kKeyWeight>, a)
+                                      : cudaLaunchKernelEx(&cfg, residual_kernel<E, kKeyNone>, a);
   if (e != cudaSuccess) return e;
   return cudaLaunchKernelEx(&cfg, mix_kernel<E>, a);
 }

@@ -34,6 +34,8 @@
 // segment's CTAs saw the call's inputs complete, and may stream while the
 // previous segment's sampling kernel runs: the segments use disjoint
 // workspace rows.  A call never overlaps the work of the previous call.
+#include <type_traits>
+
 #include "ssdv_device.cuh"
 
 namespace ssdv {
@@ -60,6 +62,29 @@ struct ResidualW {
       f2_split(f2_fma(nk, ed, et), w0, w1);
       w[e] = fmaxf(w0, 0.f);
       w[e + 1] = fmaxf(w1, 0.f);
+    }
+  }
+};
+
+// Residual weights when the draft tokens came from the Saguaro distribution
+// p' = sqrt(p * max(r, 1e-8)) / Zs of their position (r = (q - p)+ / S, or q
+// when S = 0): w = max(q - p', 0) in probability units.
+template <typename E>
+struct SagDraftW {
+  float c, mct, mcd, kr;  // kr = Z_t / Z_d
+  float inv_zt, inv_zd;   // 1 / Z_t, 1 / Z_d
+  float inv_s;            // 1 / S in weight units (1 / Z_t when S = 0: r = q)
+  float inv_zs;           // 1 / Zs
+  int target_only;        // S = 0
+  __device__ __forceinline__ void operator()(const float (&xt)[Elem<E>::kVec], const float (&xd)[Elem<E>::kVec],
+                                             float (&w)[Elem<E>::kVec]) const {
+#pragma unroll
+    for (int e = 0; e < Elem<E>::kVec; ++e) {
+      const float et = fast_exp2(fmaf(xt[e], c, -mct));
+      const float ed = fast_exp2(fmaf(xd[e], c, -mcd));
+      const float wa = target_only ? et : fmaxf(fmaf(-kr, ed, et), 0.f);
+      const float ps = sqrtf(ed * inv_zd * fmaxf(wa * inv_s, 1e-8f)) * inv_zs;
+      w[e] = fmaxf(fmaf(et, inv_zt, -ps), 0.f);
     }
   }
 };
@@ -341,7 +366,7 @@ __device__ __noinline__ void warp_draw_row(const VerifyArgs& a, int b, int n, si
   }
 }
 
-template <typename E>
+template <typename E, bool kSag>
 __global__ void __launch_bounds__(kT2, 8) sample_kernel(const VerifyArgs a) {
   __shared__ UnitStat ust[SSD_MAX_GAMMA + 1];
   __shared__ int tok_x[SSD_MAX_GAMMA];
@@ -446,10 +471,26 @@ __global__ void __launch_bounds__(kT2, 8) sample_kernel(const VerifyArgs a) {
     const Draws dr = unit_draws(a.seed, a.req_base + b, min(lane, g));  // lane g: the bonus position
     bool acc = true;
     float ratio_acc = 1.f;
+    int sag_bad = 0;
     if (lane < g) {
       const UnitStat s = ust[lane];
       if (greedy) {
         acc = tok_x[lane] == s.ai;
+      } else if constexpr (kSag) {
+        // a = min(1, q(x)/p'(x)), p'(x) = sqrt(p(x) max(r(x), 1e-8)) / Zs
+        if (tok_d[lane] != -INFINITY) {
+          const size_t uu = static_cast<size_t>(b) * W + lane;
+          const double Sw = __ldcg(a.sag_S + uu);
+          const float zs = __ldcg(a.sag_Zs + uu);
+          const float et = fast_exp2(fmaf(tok_t[lane], cc, -scaled_max(s.tm, cc)));
+          const float ed = fast_exp2(fmaf(tok_d[lane], cc, -scaled_max(s.dm, cc)));
+          const float q = et / s.ts;
+          const float r = Sw > 0.0 ? static_cast<float>(fmaxf(fmaf(-(s.ts / s.ds), ed, et), 0.f) / Sw) : q;
+          const float ps = sqrtf(ed / s.ds * fmaxf(r, 1e-8f)) / zs;
+          if (ps > 0.f) ratio_acc = fminf(1.f, q / ps);
+          if (isnan(Sw) || !(zs > 0.f)) sag_bad = 1;  // the unit's Saguaro passes failed
+        }
+        acc = dr.accept < ratio_acc;
       } else {
         // a = min(1, q(x)/p(x)), the ratio as one exp2 of the exponent difference
         if (tok_d[lane] != -INFINITY) {
@@ -463,6 +504,9 @@ __global__ void __launch_bounds__(kT2, 8) sample_kernel(const VerifyArgs a) {
     const unsigned rej = __ballot_sync(0xFFFFFFFFu, lane < g && !acc);
     const int n = rej ? __ffs(rej) - 1 : g;
     if (lane == 0) sh_n = n;
+    if constexpr (kSag) {
+      if (__any_sync(0xFFFFFFFFu, sag_bad) && lane == 0) ust[0].err = 1;
+    }
     if (a.stats && c == 0 && lane == pi) {
       float* st = a.stats + (static_cast<size_t>(b) * W + pi) * SSD_NSTAT_VERIFY;
       const UnitStat s = ust[pi];
@@ -505,7 +549,20 @@ __global__ void __launch_bounds__(kT2, 8) sample_kernel(const VerifyArgs a) {
   const bool residual = pos < g;
   const UnitStat s = ust[pos];
   const float mct = scaled_max(s.tm, cc);
-  const ResidualW<E> rw{cc, mct, residual ? scaled_max(s.dm, cc) : 0.f, residual ? s.ts / s.ds : 0.f};
+  const float mcd = residual ? scaled_max(s.dm, cc) : 0.f;
+  const float kr = residual ? s.ts / s.ds : 0.f;
+  // the residual weights: (q - p)+ scaled by Z_t, or (q - p')+ under Saguaro sampling
+  using RW = std::conditional_t<kSag, SagDraftW<E>, ResidualW<E>>;
+  RW rw;
+  if constexpr (kSag) {
+    const size_t uu = static_cast<size_t>(b) * W + pos;
+    const double Sw = residual ? __ldcg(a.sag_S + uu) : 0.0;
+    const float zs = residual ? __ldcg(a.sag_Zs + uu) : 1.f;
+    rw = SagDraftW<E>{cc, mct, mcd, kr, 1.f / s.ts, 1.f / s.ds,
+                      Sw > 0.0 ? static_cast<float>(1.0 / Sw) : 1.f / s.ts, 1.f / zs, Sw > 0.0 ? 0 : 1};
+  } else {
+    rw = ResidualW<E>{cc, mct, mcd, kr};
+  }
   const TargetW<E> tw{cc, mct};
   const double ures = static_cast<double>(unit_draws(a.seed, a.req_base + b, pos).resample);
   const E* trow = static_cast<const E*>(a.target) + (static_cast<size_t>(b) * W + pos) * V;
@@ -566,8 +623,10 @@ __global__ void __launch_bounds__(kT2, 8) sample_kernel(const VerifyArgs a) {
 
 template __global__ void stream_kernel<uint16_t>(const VerifyArgs);
 template __global__ void stream_kernel<float>(const VerifyArgs);
-template __global__ void sample_kernel<uint16_t>(const VerifyArgs);
-template __global__ void sample_kernel<float>(const VerifyArgs);
+template __global__ void sample_kernel<uint16_t, false>(const VerifyArgs);
+template __global__ void sample_kernel<float, false>(const VerifyArgs);
+template __global__ void sample_kernel<uint16_t, true>(const VerifyArgs);
+template __global__ void sample_kernel<float, true>(const VerifyArgs);
 
 __global__ void uniforms_kernel(uint64_t seed, int B, int W, float* out) {
   const long long n = static_cast<long long>(B) * W;
@@ -623,9 +682,7 @@ cudaError_t launch_stream_t(const VerifyArgs& a, int smem_bytes, cudaStream_t st
 }
 
 template <typename E>
-cudaError_t launch_verify_t(const VerifyArgs& a, int smem_bytes, cudaStream_t stream) {
-  cudaError_t e = launch_stream_t<E>(a, smem_bytes, stream);
-  if (e != cudaSuccess) return e;
+cudaError_t launch_sample_t(const VerifyArgs& a, cudaStream_t stream) {
   const int P = a.debug ? a.gmax + 1 : 1;  // position slots of the sampling grid
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((a.geo.npiece + kW2 * a.geo.ppw - 1) / (kW2 * a.geo.ppw), P, a.B);
@@ -637,13 +694,25 @@ cudaError_t launch_verify_t(const VerifyArgs& a, int smem_bytes, cudaStream_t st
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, sample_kernel<E>, a);
+  return a.sag_S ? cudaLaunchKernelEx(&cfg, sample_kernel<E, true>, a)
+                 : cudaLaunchKernelEx(&cfg, sample_kernel<E, false>, a);
+}
+
+template <typename E>
+cudaError_t launch_verify_t(const VerifyArgs& a, int smem_bytes, cudaStream_t stream) {
+  cudaError_t e = launch_stream_t<E>(a, smem_bytes, stream);
+  if (e != cudaSuccess) return e;
+  return launch_sample_t<E>(a, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_verify(const VerifyArgs& a, int esize, int smem_bytes, cudaStream_t stream) {
   return esize == 2 ? launch_verify_t<uint16_t>(a, smem_bytes, stream) : launch_verify_t<float>(a, smem_bytes, stream);
+}
+
+cudaError_t launch_sample(const VerifyArgs& a, int esize, cudaStream_t stream) {
+  return esize == 2 ? launch_sample_t<uint16_t>(a, stream) : launch_sample_t<float>(a, stream);
 }
 
 cudaError_t launch_stream(const VerifyArgs& a, int esize, int smem_bytes, cudaStream_t stream) {

@@ -223,13 +223,13 @@ def step_law(f, lo=0.0, hi=1.0, tol=2.0**-44):
     return out
 
 
-def request_law(o, xt, xd, T, tok):
+def request_law(o, xt, xd, T, tok, **kw):
     """{emitted tuple: probability} of one request, over its uniforms."""
     g = len(tok)
     law = defaultdict(float)
 
     def run(ua, ur):
-        return o.verify_request(xt, xd, T, tok, ua, ur)
+        return o.verify_request(xt, xd, T, tok, ua, ur, **kw)
 
     def explore(i, ua, weight):
         ur = np.full(g + 1, 0.5)
@@ -624,10 +624,40 @@ def pin_draft_topk(o):
     assert list(r["tokens"]) == list(r0["tokens"])
 
 
+def pin_saguaro_draft_lossless(o):
+    """Draft tokens sampled from the Saguaro distribution p' of their position
+    (the SSD notes, section 3.2) and verified with p' in p's place: the first
+    emitted token follows q exactly, averaged over x_0 ~ p' (the verification
+    blog's acceptance theorem holds for any draft distribution; the SSD notes'
+    section 5.1 reads SSD as standard SD under Saguaro sampling).  The same
+    tokens verified against the plain p give a different law."""
+    from scipy.special import softmax
+    rng = np.random.Generator(np.random.PCG64(25))
+    V, T = 5, 0.9
+    for g in (1, 2):
+        xt = rng.normal(0, 1.0, (g + 1, V))
+        xd = rng.normal(0, 1.0, (g, V))
+        q0, p0 = softmax(xt[0] / T), softmax(xd[0] / T)
+        r = np.maximum(q0 - p0, 0.0)
+        r /= r.sum()
+        s = np.sqrt(p0 * np.maximum(r, 1e-8))
+        psag = s / s.sum()
+        marg, marg_plain = np.zeros(V), np.zeros(V)
+        for x0 in range(V):
+            tok = [x0] + [int(np.argmax(xd[i])) for i in range(1, g)]
+            for out, pr in request_law(o, xt, xd, T, tok, draft_dist="saguaro").items():
+                marg[out[0]] += psag[x0] * pr
+            for out, pr in request_law(o, xt, xd, T, tok).items():
+                marg_plain[out[0]] += psag[x0] * pr
+        assert np.allclose(marg, q0, atol=1e-9), (marg, q0)
+        assert np.abs(marg_plain - q0).max() > 1e-3
+
+
 ALL_PINS = [
     pin_philox_vs_triton, pin_uniform_mapping, pin_uniform_statistics, pin_softmax, pin_argmax,
     pin_topk, pin_choice, pin_toy_closed_forms, pin_losslessness_toy_chain,
     pin_losslessness_random, pin_greedy, pin_low_temperature_limit, pin_expected_tokens,
     pin_toy_kl, pin_saguaro_toy_topk, pin_saguaro_bonus_position,
     pin_saguaro_disjoint_supports, pin_saguaro_equal_distributions, pin_cache_hit_rate, pin_draft_topk,
+    pin_saguaro_draft_lossless,
 ]

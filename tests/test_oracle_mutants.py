@@ -19,7 +19,7 @@ BATTERY = [
     pins.pin_greedy, pins.pin_toy_closed_forms, pins.pin_saguaro_bonus_position,
     pins.pin_saguaro_disjoint_supports, pins.pin_saguaro_equal_distributions,
     pins.pin_low_temperature_limit, pins.pin_losslessness_random, pins.pin_losslessness_toy_chain,
-    pins.pin_cache_hit_rate, pins.pin_draft_topk, pins.pin_philox_vs_triton,
+    pins.pin_cache_hit_rate, pins.pin_draft_topk, pins.pin_saguaro_draft_lossless, pins.pin_philox_vs_triton,
 ]
 
 MUTANTS = {
@@ -35,6 +35,7 @@ MUTANTS = {
     10: "greedy argmax ties to the higher index",
     11: "cache check against the top-k of acceptance length n-1",
     12: "draft-logit top-k taken from the target row",
+    13: "Saguaro-draft verification with the draft's p(x) in the accept test",
 }
 
 

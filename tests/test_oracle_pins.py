@@ -93,3 +93,7 @@ def test_cache_hit_rate(orc):
 
 def test_draft_topk(orc):
     pins.pin_draft_topk(orc)
+
+
+def test_saguaro_draft_lossless(orc):
+    pins.pin_saguaro_draft_lossless(orc)
