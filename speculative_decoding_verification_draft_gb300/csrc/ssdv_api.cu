@@ -399,7 +399,7 @@ static ssd_status saguaro_common(const void* target, const void* draft, ssd_dtyp
   ssd_status st = choose_chunks(V, es, aligned, &geo, &smem);
   if (st != SSD_OK) return st;
   // Pieces per warp of the residual and mix kernels (SSDV_SAG_PPW overrides).
-  geo.ppw = std::max(kSagMinPpw, env_int("SSDV_SAG_PPW", 8));
+  geo.ppw = std::max(kSagMinPpw, env_int("SSDV_SAG_PPW", 16));
   const int npw = (geo.npiece + geo.ppw - 1) / geo.ppw;
   const int W = g + 1;
   if (static_cast<long long>(B) * W * geo.nchunk >= (1LL << 31)) return fail(SSD_ERR_SHAPE, "grid too large");
@@ -559,7 +559,7 @@ ssd_status ssd_verify_saguaro_draft(const void* target_logits, const void* draft
   const int W = g + 1;
   if (static_cast<long long>(B) * W * geo.nchunk >= (1LL << 31)) return fail(SSD_ERR_SHAPE, "grid too large");
   ChunkGeometry sgeo = geo;
-  sgeo.ppw = std::max(kSagMinPpw, env_int("SSDV_SAG_PPW", 8));
+  sgeo.ppw = std::max(kSagMinPpw, env_int("SSDV_SAG_PPW", 16));
   const int npw = (geo.npiece + sgeo.ppw - 1) / sgeo.ppw;
   geo.ppw = std::max(1, env_int("SSDV_PPW", 2));
   uint8_t* ws = static_cast<uint8_t*>(workspace);
