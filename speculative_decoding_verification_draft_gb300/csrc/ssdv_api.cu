@@ -220,7 +220,10 @@ ssd_status verify_common(const void* target, const void* draft, ssd_dtype dtype,
     s.ticket = a.ticket + u0;
     s.part = a.part + u0 * geo.nchunk * 2;
     s.psum = a.psum + u0 * NP;
-    const cudaError_t e = launch_verify(s, es, smem, static_cast<cudaStream_t>(stream));
+    // small vocabularies (no statistics wanted): one warp per request
+    const cudaError_t e = (V <= kSmallV && !stats && env_int("SSDV_SMALL_V", 1) != 0)
+                              ? launch_small_verify(s, es, static_cast<cudaStream_t>(stream))
+                              : launch_verify(s, es, smem, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "verify launch");
   }
   return SSD_OK;

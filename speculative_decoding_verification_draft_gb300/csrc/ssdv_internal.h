@@ -98,6 +98,10 @@ ssd_status choose_chunks(int V, int esize, bool aligned, ChunkGeometry* geo, int
 // Streaming statistics kernel followed by the decision / sampling kernel (both
 // with programmatic dependent launch; each waits for its predecessor).
 cudaError_t launch_verify(const VerifyArgs& a, int esize, int smem_bytes, cudaStream_t stream);
+// Small vocabularies: one warp per request, the whole verification in one
+// kernel (no workspace but the status word; no statistics).
+constexpr int kSmallV = 256;
+cudaError_t launch_small_verify(const VerifyArgs& a, int esize, cudaStream_t stream);
 // The sampling kernel alone (after the Saguaro passes it reads).
 cudaError_t launch_sample(const VerifyArgs& a, int esize, cudaStream_t stream);
 // The streaming kernel alone (Saguaro's first kernel).

@@ -621,6 +621,193 @@ __global__ void __launch_bounds__(kT2, 8) sample_kernel(const VerifyArgs a) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// Small vocabularies (V <= kSmallV): one warp verifies one request in
+// registers -- no records, no workspace, one launch.  Lane L holds elements
+// [L*E, L*E + E) of a row, E = ceil(V / 32) <= 8, so lane sums in lane order
+// are the row's running sums in index order.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kSmallE = kSmallV / 32;
+
+template <typename E>
+__device__ __forceinline__ void small_load(const E* row, int V, int lo, int ne, float (&x)[kSmallE]) {
+#pragma unroll
+  for (int k = 0; k < kSmallE; ++k) x[k] = (k < ne && lo + k < V) ? Elem<E>::to_float(row[lo + k]) : -INFINITY;
+}
+
+// Warp max and sum of exp2(x*c - fl(m*c)) of a row held as above.
+__device__ __forceinline__ MaxSum small_stats(const float (&x)[kSmallE], float c) {
+  float m = x[0];
+#pragma unroll
+  for (int k = 1; k < kSmallE; ++k) m = fmaxf(m, x[k]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  float s = 0.f;
+  if (m != -INFINITY) {
+    const float nm = -scaled_max(m, c);
+#pragma unroll
+    for (int k = 0; k < kSmallE; ++k) s += fast_exp2(fmaf(x[k], c, nm));
+  }
+  return MaxSum{m, warp_sum(s)};
+}
+
+// The element of a lane-blocked row (weights w) whose running weight first
+// exceeds u * sum (fp64 across lanes, fp32 within a lane), falling back to the
+// last element with positive weight; -1 if every weight is zero.
+__device__ __forceinline__ int small_draw(const float (&w)[kSmallE], int lo, double u) {
+  const int lane = threadIdx.x & 31;
+  float ls = 0.f;
+#pragma unroll
+  for (int k = 0; k < kSmallE; ++k) ls += w[k];
+  double tot = static_cast<double>(ls);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xFFFFFFFFu, tot, o);
+  if (!(tot > 0.0)) return -1;
+  double before = 0.0;
+  const int L = lane_locate(static_cast<double>(ls), u * tot, &before);
+  int el = -1;
+  if (lane == L) {
+    const float t = static_cast<float>(u * tot - before);
+    float acc = 0.f;
+    bool done = false;
+#pragma unroll
+    for (int k = 0; k < kSmallE; ++k) {
+      if (!done && w[k] > 0.f) {
+        el = lo + k;
+        done = t < acc + w[k];
+      }
+      acc += w[k];
+    }
+  }
+  return __shfl_sync(0xFFFFFFFFu, el, L >= 0 ? L : 0);
+}
+
+// Element k (a runtime index) of a lane's block.
+__device__ __forceinline__ float small_pick(const float (&x)[kSmallE], int k) {
+  float v = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < kSmallE; ++j)
+    if (j == k) v = x[j];
+  return v;
+}
+
+}  // namespace
+
+template <typename E>
+__global__ void __launch_bounds__(256) small_verify_kernel(const VerifyArgs a) {
+  __shared__ int tok_s[8][SSD_MAX_GAMMA];
+  griddep_wait();  // the previous kernel on the stream is complete (inputs and outputs)
+  griddep_launch_dependents();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.x * 8 + warp;
+  if (b >= a.B) return;
+  const int V = a.geo.V, W = a.gmax + 1;
+  const int g = a.gamma ? a.gamma[b] : a.gmax;
+  const float T = a.temps ? a.temps[b] : a.temp_scalar;
+  const bool bad_gamma = g > a.gmax, bad_temp = !temperature_ok(T);
+  if (g < 0 || bad_gamma || bad_temp) {  // padded or invalid request
+    if (lane == 0) {
+      write_error(a, b);
+      if (bad_gamma) atomicOr(a.status, 1 << SSD_ERR_GAMMA);
+      if (bad_temp && g >= 0) atomicOr(a.status, 1 << SSD_ERR_TEMPERATURE);
+    }
+    return;
+  }
+  int* tok_x = tok_s[warp];
+  bool bad = false;
+  if (lane < g) {
+    const int x = a.draft_tokens[static_cast<size_t>(b) * a.gmax + lane];
+    bad = x < 0 || x >= V;
+    tok_x[lane] = x;
+  }
+  if (__any_sync(0xFFFFFFFFu, bad)) {
+    if (lane == 0) {
+      write_error(a, b);
+      atomicOr(a.status, 1 << SSD_ERR_TOKEN_RANGE);
+    }
+    return;
+  }
+  __syncwarp();
+  const int ne = (V + 31) / 32;
+  const int lo = lane * ne;
+  const E* trows = static_cast<const E*>(a.target) + static_cast<size_t>(b) * W * V;
+  const E* drows = static_cast<const E*>(a.draft) + static_cast<size_t>(b) * a.gmax * V;
+  const uint32_t rid = static_cast<uint32_t>(a.req_base + b);
+  int n = g, last = -1;
+  float xt[kSmallE], xd[kSmallE], w[kSmallE];
+  if (T == 0.f) {
+    // greedy: accept while the draft token is the target argmax
+    for (int i = 0; i <= g; ++i) {
+      small_load(trows + static_cast<size_t>(i) * V, V, lo, ne, xt);
+      ArgMax am{-INFINITY, -1};
+#pragma unroll
+      for (int k = 0; k < kSmallE; ++k)
+        if (k < ne && lo + k < V && (am.i < 0 || xt[k] > am.v)) am = ArgMax{xt[k], lo + k};
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const ArgMax oa{__shfl_xor_sync(0xFFFFFFFFu, am.v, o), __shfl_xor_sync(0xFFFFFFFFu, am.i, o)};
+        am = better_arg(am, oa);
+      }
+      if (i == g || tok_x[i] != am.i) {
+        n = i;
+        last = am.i;
+        break;
+      }
+    }
+  } else {
+    const float c = kLog2e / T;
+    for (int i = 0; i < g; ++i) {
+      small_load(trows + static_cast<size_t>(i) * V, V, lo, ne, xt);
+      small_load(drows + static_cast<size_t>(i) * V, V, lo, ne, xd);
+      const MaxSum st = small_stats(xt, c), sd = small_stats(xd, c);
+      const int x = tok_x[i];
+      const float lx_t = __shfl_sync(0xFFFFFFFFu, small_pick(xt, x % ne), x / ne);
+      const float lx_d = __shfl_sync(0xFFFFFFFFu, small_pick(xd, x % ne), x / ne);
+      const float mct = scaled_max(st.m, c), mcd = scaled_max(sd.m, c);
+      float ratio = 1.f;  // a -inf draft logit: p(x) = 0, accepted
+      if (lx_d != -INFINITY)
+        ratio = fminf(1.f, fast_exp2(fmaf(lx_t, c, -mct) - fmaf(lx_d, c, -mcd)) * (sd.s / st.s));
+      const Draws dr = unit_draws(a.seed, rid, i);
+      if (dr.accept < ratio) continue;
+      // rejected at i: the correction from (q_i - p_i)+ (q_i if that is empty)
+      const float kr = st.s / sd.s;
+#pragma unroll
+      for (int k = 0; k < kSmallE; ++k)
+        w[k] = fmaxf(fmaf(-kr, fast_exp2(fmaf(xd[k], c, -mcd)), fast_exp2(fmaf(xt[k], c, -mct))), 0.f);
+      const double ures = static_cast<double>(dr.resample);
+      last = small_draw(w, lo, ures);
+      if (last < 0) {
+#pragma unroll
+        for (int k = 0; k < kSmallE; ++k) w[k] = fast_exp2(fmaf(xt[k], c, -mct));
+        last = small_draw(w, lo, ures);
+      }
+      n = i;
+      break;
+    }
+    if (n == g) {  // every draft token accepted: the bonus from q_g
+      small_load(trows + static_cast<size_t>(g) * V, V, lo, ne, xt);
+      const MaxSum st = small_stats(xt, c);
+      const float mct = scaled_max(st.m, c);
+#pragma unroll
+      for (int k = 0; k < kSmallE; ++k) w[k] = fast_exp2(fmaf(xt[k], c, -mct));
+      last = small_draw(w, lo, static_cast<double>(unit_draws(a.seed, rid, g).resample));
+    }
+  }
+  if (lane == 0) {
+    if (last < 0) {
+      write_error(a, b);
+      atomicOr(a.status, 1 << SSD_ERR_TIMEOUT);
+    } else {
+      write_outputs(a, b, n, last, tok_x);
+    }
+  }
+}
+
+template __global__ void small_verify_kernel<uint16_t>(const VerifyArgs);
+template __global__ void small_verify_kernel<float>(const VerifyArgs);
+
 template __global__ void stream_kernel<uint16_t>(const VerifyArgs);
 template __global__ void stream_kernel<float>(const VerifyArgs);
 template __global__ void sample_kernel<uint16_t, false>(const VerifyArgs);
@@ -709,6 +896,20 @@ cudaError_t launch_verify_t(const VerifyArgs& a, int smem_bytes, cudaStream_t st
 
 cudaError_t launch_verify(const VerifyArgs& a, int esize, int smem_bytes, cudaStream_t stream) {
   return esize == 2 ? launch_verify_t<uint16_t>(a, smem_bytes, stream) : launch_verify_t<float>(a, smem_bytes, stream);
+}
+
+cudaError_t launch_small_verify(const VerifyArgs& a, int esize, cudaStream_t stream) {
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((a.B + 7) / 8, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  return esize == 2 ? cudaLaunchKernelEx(&cfg, small_verify_kernel<uint16_t>, a)
+                    : cudaLaunchKernelEx(&cfg, small_verify_kernel<float>, a);
 }
 
 cudaError_t launch_sample(const VerifyArgs& a, int esize, cudaStream_t stream) {

@@ -299,3 +299,29 @@ def test_host_side_errors(ssdv):
     with pytest.raises(ssdv.SsdError) as e:
         ssdv.verify(b.target, None, b.draft_tokens, 0.8, 1)
     assert e.value.status == 1
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("V,gamma", [(7, 4), (100, 3), (256, 6), (33, 1), (1, 2), (257, 2)])
+def test_small_vocab_one_warp_path(ssdv, dtype, V, gamma, monkeypatch):
+    """V <= 256 runs one warp per request (no records, no workspace); both that
+    path and the general one match the oracle."""
+    batch = wl.zipf_batch(300, gamma, V, dtype=dtype, temperature=0.9, seed=7 * V + gamma, sigma_range=(0.2, 1.4))
+    ref = gc.verify_oracle(batch, 13)
+    out, n = run_verify(ssdv, batch, 13)
+    gc.assert_verify_parity(out, n, ref, V, f"one-warp V={V} g={gamma} {dtype}")
+    monkeypatch.setenv("SSDV_SMALL_V", "0")
+    out2, n2 = run_verify(ssdv, batch, 13)
+    gc.assert_verify_parity(out2, n2, ref, V, f"general V={V} g={gamma} {dtype}")
+
+
+def test_small_vocab_ragged_and_greedy(ssdv):
+    """The one-warp path with per-request gamma (padded requests) and
+    temperature (half greedy), NaN padding never read."""
+    batch = wl.ragged_batch(200, 6, 200, seed=9)
+    b = batch.to("cuda")
+    out, n = ssdv.verify_ragged(b.target, b.draft, b.draft_tokens, b.gamma, b.temperature, 21)
+    torch.cuda.synchronize()
+    ref = gc.verify_oracle(batch, 21)
+    gc.assert_verify_parity(out.cpu().numpy(), n.cpu().numpy(), ref, 200, "one-warp ragged")
+    assert ssdv.read_status() == 0
