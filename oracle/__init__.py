@@ -57,17 +57,19 @@ def _declare(lib):
     lib.orc_argmax.argtypes = [P, c_int]
     lib.orc_argmax.restype = c_int
     lib.orc_cache_check.argtypes = [P, P, P, c_int, c_int, c_int, P]
+    lib.orc_nucleus.argtypes = [P, P, c_int, c_double, c_double, P]
+    lib.orc_nucleus.restype = None
     lib.orc_cache_check.restype = c_int
     lib.orc_choice.argtypes = [P, c_int, c_double, P]
     lib.orc_choice.restype = c_int
     lib.orc_topk.argtypes = [P, c_int, c_int, P, P]
     lib.orc_topk.restype = None
-    lib.orc_verify_request.argtypes = [c_int, c_int, P, P, c_double, c_int, P, P, P, c_double, P, P, P, P]
+    lib.orc_verify_request.argtypes = [c_int, c_int, P, P, c_double, c_int, c_double, P, P, P, c_double, P, P, P, P]
     lib.orc_verify_request.restype = c_int
     lib.orc_saguaro_request.argtypes = [c_int, c_int, P, P, c_double, c_int, c_int, P, c_double, P, P, P, P, P]
     lib.orc_saguaro_request.restype = c_int
     lib.orc_verify_batch.argtypes = [P, P, c_int, P, c_int, c_int, c_int, P, P, c_float, c_u64,
-                                     P, P, P, P, P, P, c_double, c_int, c_int]
+                                     P, P, P, P, P, P, c_double, c_int, c_int, c_double]
     lib.orc_verify_batch.restype = c_int
     lib.orc_saguaro_batch.argtypes = [P, P, c_int, c_int, c_int, c_int, c_int, c_int, c_float, c_u64,
                                       P, P, P, P, P, P, c_double, c_int]
@@ -185,7 +187,7 @@ class Oracle:
 
     # --- one request, explicit uniforms ----------------------------------
     def verify_request(self, xt, xd, T, tok, u_acc, u_res, stats: bool = False, band: float = FLAG_BAND,
-                       draft_dist: str = "draft"):
+                       draft_dist: str = "draft", top_p: float = 1.0):
         """xt: (g+1, V) fp64 target logits; xd: (g, V) draft logits; tok: (g,).
         draft_dist: "draft" (tokens sampled from p) or "saguaro" (from the
         Saguaro distribution of each position, which then replaces p)."""
@@ -199,7 +201,8 @@ class Oracle:
         out = np.empty(g + 1, np.int32)
         fp, fk = ctypes.c_int32(), ctypes.c_int32()
         st = np.empty((g + 1, NSTAT_VERIFY), np.float64) if stats else None
-        n = self.lib.orc_verify_request(g, V, _ptr(xt), _ptr(xd), float(T), _dist(draft_dist), _ptr(tok), _ptr(ua),
+        n = self.lib.orc_verify_request(g, V, _ptr(xt), _ptr(xd), float(T), _dist(draft_dist), float(top_p),
+                                        _ptr(tok), _ptr(ua),
                                         _ptr(ur), float(band), _ptr(out), ctypes.byref(fp),
                                         ctypes.byref(fk), _ptr(st))
         return dict(n=n, out=out, flag_pos=fp.value, flag_kind=fk.value, stats=st)
@@ -224,7 +227,7 @@ class Oracle:
     # --- batches over typed logits, Philox uniforms ----------------------
     def verify_batch(self, target, draft, draft_tokens, temperature, seed: int,
                      gamma=None, stats: bool = False, nthreads: int = 1, req_ids=None,
-                     band: float = FLAG_BAND, draft_dist: str = "draft"):
+                     band: float = FLAG_BAND, draft_dist: str = "draft", top_p: float = 1.0):
         """target [B, gmax+1, V], draft [B, gmax, V] (uint16 bf16 bits or float32).
 
         ``temperature``: a float, or a float32 array [B] (per request).
@@ -255,10 +258,18 @@ class Oracle:
         rc = self.lib.orc_verify_batch(_ptr(target), _ptr(draft), dt, _ptr(tok), B, gmax, V,
                                        _ptr(gam), _ptr(temps), tscalar, seed, _ptr(out), _ptr(n),
                                        _ptr(fp), _ptr(fk), _ptr(st), _ptr(rid), float(band), nthreads,
-                                       _dist(draft_dist))
+                                       _dist(draft_dist), float(top_p))
         if rc != 0:
             raise ValueError("oracle rejected the batch arguments")
         return dict(out_tokens=out, n_accepted=n, flag_pos=fp, flag_kind=fk, stats=st)
+
+    def nucleus(self, x, prob, top_p: float, band: float = FLAG_BAND):
+        """(renormalised prob over the top-p nucleus of logits x, ambiguous?)."""
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        pr = np.array(prob, dtype=np.float64)
+        amb = ctypes.c_int(0)
+        self.lib.orc_nucleus(_ptr(x), _ptr(pr), x.size, float(top_p), float(band), ctypes.byref(amb))
+        return pr, bool(amb.value)
 
     def cache_check(self, bonus_topk, out_tokens, n_accepted):
         """(hit [B], number of hits) of one round's verify outcome against its

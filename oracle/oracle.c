@@ -170,6 +170,55 @@ void orc_softmax(const double* x, int V, double T, double* prob, double* out_max
   if (out_logsum) *out_logsum = log(sum);
 }
 
+/* Nucleus (top-p) truncation ([SD] §三 closing remark and §五.4: verification
+ * composes with temperature and top-p when both sides use the same
+ * parameters).  Kept: the tokens whose logit is at least th, the largest logit
+ * value with P{v : x_v >= th} >= top_p -- the most likely tokens, in order,
+ * until their mass reaches top_p, plus every token tied with the last one.
+ * prob (normalised) is renormalised over them in place.  top_p >= 1 keeps
+ * everything.  *ambig is set when the mass strictly above th or the kept mass
+ * lies within `band` of top_p (a decision within rounding of flipping). */
+typedef struct {
+  double x;
+  int i;
+} orc_xi;
+
+static int cmp_desc(const void* a, const void* b) {
+  const orc_xi* p = (const orc_xi*)a;
+  const orc_xi* q = (const orc_xi*)b;
+  if (p->x != q->x) return p->x > q->x ? -1 : 1;
+  return p->i - q->i;
+}
+
+void orc_nucleus(const double* x, double* prob, int V, double top_p, double band, int* ambig) {
+  if (!(top_p < 1.0)) return;
+  orc_xi* o = (orc_xi*)malloc(sizeof(orc_xi) * (size_t)V);
+  for (int v = 0; v < V; ++v) {
+    o[v].x = x[v];
+    o[v].i = v;
+  }
+  qsort(o, (size_t)V, sizeof(orc_xi), cmp_desc);
+  double cum = 0.0, th = -INFINITY;
+  for (int i = 0; i < V;) {
+    int j = i;
+    double group = 0.0;
+    while (j < V && o[j].x == o[i].x) group += prob[o[j++].i];
+    const double before = cum;
+    cum += group;
+    if (cum >= top_p) {
+      th = o[i].x;
+      if (top_p - before < band || cum - top_p < band) *ambig = 1;
+      break;
+    }
+    i = j;
+  }
+  free(o);
+  if (th == -INFINITY) return; /* rounding kept the mass below top_p: keep all */
+  double kept = 0.0;
+  for (int v = 0; v < V; ++v) kept += x[v] >= th ? prob[v] : 0.0;
+  for (int v = 0; v < V; ++v) prob[v] = x[v] >= th ? prob[v] / kept : 0.0;
+}
+
 /* Greedy target choice: the largest logit, lowest index among equals. */
 int orc_argmax(const double* x, int V) {
   int best = 0;
@@ -313,10 +362,28 @@ static void saguaro_draft_dist(int V, const double* q, double* p, double* r) {
  * each position instead of p ([SAG] §5.1: SSD is standard SD under Saguaro
  * sampling), so p' takes p's place in the accept test and the residual. */
 static orc_position position_quantities(int V, const double* ti, const double* di, double T, int x,
-                                        double* q, double* p, double* r, int sag) {
+                                        double* q, double* p, double* r, int sag, double top_p, double band,
+                                        int* ambig) {
   orc_position P;
   orc_softmax(ti, V, T, q, &P.mt, &P.lst);
   orc_softmax(di, V, T, p, &P.md, &P.lsd);
+  if (top_p < 1.0) {
+    /* both distributions truncated to their nuclei, then the usual steps */
+    orc_nucleus(ti, q, V, top_p, band, ambig);
+#if ORC_MUTANT != 14
+    orc_nucleus(di, p, V, top_p, band, ambig);
+#endif
+    P.qx = q[x];
+    P.px = p[x];
+    P.a = P.px > 0.0 ? (P.qx < P.px ? P.qx / P.px : 1.0) : 1.0;
+    P.S = 0.0;
+    for (int v = 0; v < V; ++v) {
+      double d = q[v] - p[v];
+      r[v] = d > 0.0 ? d : 0.0;
+      P.S += r[v];
+    }
+    return P;
+  }
   if (sag) {
     saguaro_draft_dist(V, q, p, r);
     P.qx = q[x];
@@ -369,7 +436,7 @@ static orc_position position_quantities(int V, const double* ti, const double* d
   return P;
 }
 
-int orc_verify_request(int g, int V, const double* xt, const double* xd, double T, int sag,
+int orc_verify_request(int g, int V, const double* xt, const double* xd, double T, int sag, double top_p,
                        const int32_t* tok, const double* u_acc, const double* u_res, double band,
                        int32_t* out, int32_t* flag_pos, int32_t* flag_kind, double* stats) {
   for (int i = 0; i <= g; ++i) out[i] = -1;
@@ -406,9 +473,11 @@ int orc_verify_request(int g, int V, const double* xt, const double* xd, double 
   double* p = (double*)malloc(sizeof(double) * (size_t)V);
   double* r = (double*)malloc(sizeof(double) * (size_t)V);
 
+  int ambig = 0; /* top-p: a nucleus decision within `band` of flipping */
   if (stats) { /* every position's quantities, whether or not it is reached */
     for (int i = 0; i < g; ++i) {
-      orc_position P = position_quantities(V, xt + (size_t)i * V, xd + (size_t)i * V, T, tok[i], q, p, r, sag);
+      orc_position P = position_quantities(V, xt + (size_t)i * V, xd + (size_t)i * V, T, tok[i], q, p, r, sag, top_p,
+                                         band, &ambig);
       double* s = stats + i * ORC_NSTAT_VERIFY;
       s[0] = P.mt;
       s[1] = P.lst;
@@ -423,12 +492,18 @@ int orc_verify_request(int g, int V, const double* xt, const double* xd, double 
     orc_softmax(xt + (size_t)g * V, V, T, q, &mt, &lst);
     stats[g * ORC_NSTAT_VERIFY + 0] = mt;
     stats[g * ORC_NSTAT_VERIFY + 1] = lst;
+    ambig = 0;
   }
 
   int n = g;
   for (int i = 0; i < g; ++i) {
-    orc_position P = position_quantities(V, xt + (size_t)i * V, xd + (size_t)i * V, T, tok[i], q, p, r, sag);
+    orc_position P = position_quantities(V, xt + (size_t)i * V, xd + (size_t)i * V, T, tok[i], q, p, r, sag, top_p,
+                                         band, &ambig);
     double u = u_acc[i];
+    if (*flag_pos < 0 && ambig) { /* this position's nuclei could come out differently */
+      *flag_pos = i;
+      *flag_kind = 0;
+    }
     if (*flag_pos < 0 && fabs(u - P.a) < band) {
       *flag_pos = i;
       *flag_kind = 0;
@@ -461,6 +536,12 @@ int orc_verify_request(int g, int V, const double* xt, const double* xd, double 
     int row = g;
 #endif
     orc_softmax(xt + (size_t)row * V, V, T, q, NULL, NULL);
+    ambig = 0;
+    orc_nucleus(xt + (size_t)row * V, q, V, top_p, band, &ambig);
+    if (*flag_pos < 0 && ambig) {
+      *flag_pos = g;
+      *flag_kind = 1;
+    }
     double dist, e_lo, e_hi;
     out[g] = orc_choice_edges(q, V, u_res[g], &dist, &e_lo, &e_hi);
     if (stats) {
@@ -661,6 +742,7 @@ typedef struct {
   int k;
   int topk_src; /* saguaro: 0 residual, 1 draft logits */
   int sag;      /* verify: draft tokens sampled from the Saguaro distribution */
+  double top_p; /* verify: nucleus truncation of both distributions (>= 1: none) */
   const int32_t* req_ids; /* nullable: request index used in the Philox counter */
   int32_t* out_a; /* verify: out_tokens     saguaro: bonus_topk    */
   int32_t* out_b; /* verify: n_accepted     saguaro: saguaro_tokens */
@@ -713,7 +795,7 @@ static void run_request(const orc_job* jb, int b, double* xt, double* xd) {
     ur[i] = orc_uniform(jb->seed, rid, (uint32_t)i, 1u);
   }
   int32_t fp, fk;
-  int n = orc_verify_request(g, V, xt, xd, T, jb->sag, jb->draft_tokens + (size_t)b * gmax, ua, ur, jb->band, out, &fp, &fk,
+  int n = orc_verify_request(g, V, xt, xd, T, jb->sag, jb->top_p, jb->draft_tokens + (size_t)b * gmax, ua, ur, jb->band, out, &fp, &fk,
                              jb->stats ? jb->stats + (size_t)b * W * ORC_NSTAT_VERIFY : NULL);
   if (n < 0) {
     for (int t = 0; t < W; ++t) out[t] = -1;
@@ -757,7 +839,7 @@ int orc_verify_batch(const void* target, const void* draft, int dtype, const int
                      int B, int gmax, int V, const int32_t* gamma, const float* temp,
                      float temp_scalar, uint64_t seed, int32_t* out_tokens, int32_t* n_accepted,
                      int32_t* flag_pos, int32_t* flag_kind, double* stats, const int32_t* req_ids,
-                     double band, int nthreads, int sag) {
+                     double band, int nthreads, int sag, double top_p) {
   orc_job jb;
   memset(&jb, 0, sizeof jb);
   jb.req_ids = req_ids;
@@ -780,6 +862,7 @@ int orc_verify_batch(const void* target, const void* draft, int dtype, const int
   jb.stats = stats;
   jb.saguaro = 0;
   jb.sag = sag;
+  jb.top_p = top_p;
   jb.nthreads = nthreads;
   return run_batch(jb);
 }

@@ -653,11 +653,56 @@ def pin_saguaro_draft_lossless(o):
         assert np.abs(marg_plain - q0).max() > 1e-3
 
 
+def pin_top_p(o):
+    """Top-p composed with verification (the verification blog's closing
+    remark and its section on matching sampling parameters: speculative
+    decoding stacks on temperature and top-p when both sides truncate the same
+    way).  On the printed toy tables at top_p = 0.75 the target after token 0
+    (.50 .18 .11 .08 ...) keeps {0, 1, 2} (mass .79) and the draft (.55 .15
+    .10 ...) keeps {0, 1, 2} (.80); at 0.8 the target keeps {0, 1, 2, 3}.  With
+    x_0 drawn from the truncated draft, the first emitted token follows the
+    truncated target exactly.  Tokens tied with the last one needed are kept;
+    top_p = 1 changes nothing."""
+    d0, d1, t0, t1 = toy_tables()
+    qP, amb = o.nucleus(np.log(t0), t0, 0.75)
+    assert not amb and np.allclose(qP, np.r_[t0[:3] / t0[:3].sum(), np.zeros(4)], atol=1e-12)
+    pP, amb = o.nucleus(np.log(d0), d0, 0.75)
+    assert not amb and np.allclose(pP, np.r_[d0[:3] / d0[:3].sum(), np.zeros(4)], atol=1e-12)
+    q8, _ = o.nucleus(np.log(t0), t0, 0.8)
+    assert np.count_nonzero(q8) == 4
+    # first emitted token of a round, x_0 ~ truncated draft: the truncated target
+    xt = np.log(np.stack([t0, t1]))
+    xd = np.log(d0)[None]
+    marg = np.zeros(7)
+    for x0 in range(7):
+        if pP[x0] == 0:
+            continue
+        for out, pr in request_law(o, xt, xd, 1.0, [x0], top_p=0.75).items():
+            marg[out[0]] += pP[x0] * pr
+    assert np.allclose(marg, qP, atol=1e-9), (marg, qP)
+    # ties at the boundary: logits 2, 1, 1, 1, 0 -- reaching 0.5 needs one of the
+    # three tied tokens, so all three are kept
+    x = np.array([2.0, 1.0, 1.0, 1.0, 0.0])
+    from scipy.special import softmax
+    pr = softmax(x)
+    kept, _ = o.nucleus(x, pr, 0.5)
+    assert list(np.nonzero(kept)[0]) == [0, 1, 2, 3]
+    # top_p = 1: the plain verification
+    rng = np.random.Generator(np.random.PCG64(27))
+    xt = rng.normal(0, 1.0, (3, 9))
+    xd = rng.normal(0, 1.0, (2, 9))
+    for seed in range(20):
+        u = np.random.default_rng(seed).random((2, 3))
+        a = o.verify_request(xt, xd, 0.8, [1, 4], u[0], u[1])
+        b = o.verify_request(xt, xd, 0.8, [1, 4], u[0], u[1], top_p=1.0)
+        assert list(a["out"]) == list(b["out"])
+
+
 ALL_PINS = [
     pin_philox_vs_triton, pin_uniform_mapping, pin_uniform_statistics, pin_softmax, pin_argmax,
     pin_topk, pin_choice, pin_toy_closed_forms, pin_losslessness_toy_chain,
     pin_losslessness_random, pin_greedy, pin_low_temperature_limit, pin_expected_tokens,
     pin_toy_kl, pin_saguaro_toy_topk, pin_saguaro_bonus_position,
     pin_saguaro_disjoint_supports, pin_saguaro_equal_distributions, pin_cache_hit_rate, pin_draft_topk,
-    pin_saguaro_draft_lossless,
+    pin_saguaro_draft_lossless, pin_top_p,
 ]

@@ -19,7 +19,8 @@ BATTERY = [
     pins.pin_greedy, pins.pin_toy_closed_forms, pins.pin_saguaro_bonus_position,
     pins.pin_saguaro_disjoint_supports, pins.pin_saguaro_equal_distributions,
     pins.pin_low_temperature_limit, pins.pin_losslessness_random, pins.pin_losslessness_toy_chain,
-    pins.pin_cache_hit_rate, pins.pin_draft_topk, pins.pin_saguaro_draft_lossless, pins.pin_philox_vs_triton,
+    pins.pin_cache_hit_rate, pins.pin_draft_topk, pins.pin_saguaro_draft_lossless, pins.pin_top_p,
+    pins.pin_philox_vs_triton,
 ]
 
 MUTANTS = {
@@ -36,6 +37,7 @@ MUTANTS = {
     11: "cache check against the top-k of acceptance length n-1",
     12: "draft-logit top-k taken from the target row",
     13: "Saguaro-draft verification with the draft's p(x) in the accept test",
+    14: "top-p truncating the target but not the draft",
 }
 
 

@@ -97,3 +97,7 @@ def test_draft_topk(orc):
 
 def test_saguaro_draft_lossless(orc):
     pins.pin_saguaro_draft_lossless(orc)
+
+
+def test_top_p(orc):
+    pins.pin_top_p(orc)
