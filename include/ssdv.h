@@ -114,6 +114,30 @@ ssd_status ssd_verify(const void* target_logits, const void* draft_logits, ssd_d
                       uint64_t seed, int32_t* out_tokens, int32_t* n_accepted, void* workspace,
                       size_t ws_bytes, void* stream);
 
+/* Verification with top-p (nucleus) truncation on both sides (the
+ * verification blog's closing remark and its section on matching sampling
+ * parameters: speculative decoding stacks on temperature and top-p when the
+ * target and the draft truncate the same way).  Every target row q_i and
+ * draft row p_i keeps the tokens whose logit is at least th, the largest logit
+ * value with P{x >= th} >= top_p (the most likely tokens until their mass
+ * reaches top_p, plus every token tied with the last one needed), and is
+ * renormalised; then ssd_verify's steps run on the truncated distributions: a
+ * draft token outside the target's nucleus is rejected, one outside the
+ * draft's is accepted, the correction comes from (q'_n - p'_n)+ and the bonus
+ * from q'_gamma.  temperature == 0 (greedy) or top_p == 1 is ssd_verify.
+ *   0 < top_p <= 1; B <= 65535.
+ *   workspace >= ssd_verify_top_p_workspace_bytes(B, gamma) bytes, zeroed once.
+ * Kernels: the streaming pass, then per radix level (2 for bf16, 3 for fp32)
+ * a histogram pass over the rows and a select pass, then the sampling kernel. */
+ssd_status ssd_verify_top_p(const void* target_logits, const void* draft_logits, ssd_dtype dtype,
+                            const int32_t* draft_tokens, int B, int gamma, int V, float temperature,
+                            float top_p, uint64_t seed, int32_t* out_tokens, int32_t* n_accepted,
+                            void* workspace, size_t ws_bytes, void* stream);
+
+/* Bytes of device workspace ssd_verify_top_p needs (a verification workspace
+ * plus the per-row select state and radix histograms). */
+size_t ssd_verify_top_p_workspace_bytes(int B, int gamma_max);
+
 /* Pipelined verification: ssd_verify for a chain of calls whose inputs are
  * already complete.  This entry point has no counterpart in the method's
  * description; it serves a caller that keeps several independent batches in

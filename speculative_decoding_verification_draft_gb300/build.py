@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIBRARY = os.path.join(PKG, "libssdv.so")
-SOURCES = ["ssdv_api.cu", "ssdv_verify.cu", "ssdv_saguaro.cu"]
+SOURCES = ["ssdv_api.cu", "ssdv_verify.cu", "ssdv_saguaro.cu", "ssdv_topp.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

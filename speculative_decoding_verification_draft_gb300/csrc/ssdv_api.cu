@@ -86,6 +86,26 @@ SagLayout saguaro_layout(int B, int g, int V) {
   return L;
 }
 
+// Top-p extension of the verification workspace: per row slot (B, gmax+1, 2)
+// the select state, the thresholds and kept masses, then every level's
+// histograms (fp32's 2048 + 2048 + 1024 bins, the most).
+struct TopPLayout {
+  size_t prefix, above, goal, th, z, hist, total;
+};
+constexpr int kTopPBins = 2048 + 2048 + 1024;
+static TopPLayout topp_layout(int B, int gmax) {
+  TopPLayout T;
+  const size_t slots = static_cast<size_t>(B) * static_cast<size_t>(gmax + 1) * 2;
+  T.prefix = round_up(workspace_layout(B, gmax).total, 256);
+  T.above = round_up(T.prefix + 4 * slots, 256);
+  T.goal = T.above + 8 * slots;
+  T.th = T.goal + 8 * slots;
+  T.z = T.th + 4 * slots;
+  T.hist = round_up(T.z + 4 * slots, 256);
+  T.total = T.hist + slots * kTopPBins * 8;
+  return T;
+}
+
 namespace {
 
 // Consecutive calls on one workspace use alternate halves, so a pipelined
@@ -140,7 +160,8 @@ namespace {
 ssd_status verify_common(const void* target, const void* draft, ssd_dtype dtype, const int32_t* draft_tokens, int B,
                          int gmax, int V, const int32_t* gamma, const float* temps, float temp_scalar,
                          bool all_greedy, uint64_t seed, int32_t* out_tokens, int32_t* n_accepted, void* workspace,
-                         size_t ws_bytes, float* stats, void* stream, bool pipelined = false) {
+                         size_t ws_bytes, float* stats, void* stream, bool pipelined = false, float top_p = 1.f) {
+  const bool use_topp = top_p < 1.f && !all_greedy;
   const int es = esize_of(dtype);
   if (es == 0) return fail(SSD_ERR_DTYPE, "unknown dtype %d", static_cast<int>(dtype));
   if (!target || !out_tokens || !n_accepted || !workspace) return fail(SSD_ERR_NULL, "a required pointer is NULL");
@@ -154,8 +175,10 @@ ssd_status verify_common(const void* target, const void* draft, ssd_dtype dtype,
       (stats && !aligned_to(stats, 4)) || (gamma && !aligned_to(gamma, 4)) || (temps && !aligned_to(temps, 4)))
     return fail(SSD_ERR_ALIGN, "a pointer is not aligned to its element size (workspace: 16 bytes)");
   const WorkspaceLayout L = workspace_layout(B, gmax);
-  if (ws_bytes < L.total)
-    return fail(SSD_ERR_WORKSPACE, "workspace of %zu bytes < %zu required", ws_bytes, L.total);
+  const size_t need = use_topp ? topp_layout(B, gmax).total : L.total;
+  if (ws_bytes < need) return fail(SSD_ERR_WORKSPACE, "workspace of %zu bytes < %zu required", ws_bytes, need);
+  if (use_topp && (B > 65535 || stats))
+    return fail(SSD_ERR_UNSUPPORTED, "top-p verification takes at most 65535 requests and no statistics");
   const bool aligned = aligned_to(target, 16) && (!draft || aligned_to(draft, 16)) &&
                        ((static_cast<size_t>(V) * es) % 16 == 0);
   ChunkGeometry geo;
@@ -193,7 +216,58 @@ ssd_status verify_common(const void* target, const void* draft, ssd_dtype dtype,
   a.debug = stats ? 1 : 0;
   a.sag_S = nullptr;
   a.sag_Zs = nullptr;
+  a.tp_th = nullptr;
+  a.tp_z = nullptr;
   a.geo = geo;
+  if (use_topp) {
+    // The streaming kernel, the radix-select levels of every row's nucleus
+    // threshold, then the sampling kernel on the truncated distributions.
+    const TopPLayout TL = topp_layout(B, gmax);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int levels = es == 2 ? 2 : 3;
+    const int shifts[3] = {es == 2 ? 24 : 21, es == 2 ? 16 : 10, 0};
+    const int bits[3] = {es == 2 ? 8 : 11, es == 2 ? 8 : 11, 10};
+    const size_t slots = static_cast<size_t>(B) * (gmax + 1) * 2;
+    size_t hist_bytes = 0;
+    for (int l = 0; l < levels; ++l) hist_bytes += slots * (static_cast<size_t>(8) << bits[l]);
+    cudaError_t e = cudaMemsetAsync(ws + TL.hist, 0, hist_bytes, st);
+    if (e != cudaSuccess) return cuda_fail(e, "top-p histogram memset");
+    a.first = 1;
+    a.tp_th = reinterpret_cast<float*>(ws + TL.th);
+    a.tp_z = reinterpret_cast<float*>(ws + TL.z);
+    e = launch_stream(a, es, smem, st);
+    if (e != cudaSuccess) return cuda_fail(e, "verify launch");
+    TopPArgs t = {};
+    t.target = target;
+    t.draft = draft;
+    t.B = B;
+    t.gmax = gmax;
+    t.gamma = gamma;
+    t.temps = temps;
+    t.temp_scalar = temp_scalar;
+    t.top_p = top_p;
+    t.part = a.part;
+    t.geo = geo;
+    t.nlevels = levels;
+    t.prefix = reinterpret_cast<uint32_t*>(ws + TL.prefix);
+    t.above = reinterpret_cast<unsigned long long*>(ws + TL.above);
+    t.goal = reinterpret_cast<unsigned long long*>(ws + TL.goal);
+    t.th = reinterpret_cast<float*>(ws + TL.th);
+    t.z = reinterpret_cast<float*>(ws + TL.z);
+    size_t off = TL.hist;
+    for (int l = 0; l < levels; ++l) {
+      t.level = l;
+      t.shift = shifts[l];
+      t.bits = bits[l];
+      t.hist = reinterpret_cast<unsigned long long*>(ws + off);
+      off += slots * (static_cast<size_t>(8) << bits[l]);
+      e = launch_topp_level(t, es, st);
+      if (e != cudaSuccess) return cuda_fail(e, "top-p launch");
+    }
+    e = launch_sample(a, es, st);
+    if (e != cudaSuccess) return cuda_fail(e, "verify launch");
+    return SSD_OK;
+  }
   // Launch in segments of at most 65535 requests (the grid's third
   // dimension; SSDV_SEGMENT sets a smaller size).  Each segment keeps its
   // requests' global indices for the Philox counters and its own rows of the
@@ -296,6 +370,25 @@ ssd_status ssd_verify(const void* target_logits, const void* draft_logits, ssd_d
     return fail(SSD_ERR_TEMPERATURE, "temperature %g is not 0 or in [1e-6, inf)", static_cast<double>(temperature));
   return verify_common(target_logits, draft_logits, dtype, draft_tokens, B, gamma, V, nullptr, nullptr, temperature,
                        temperature == 0.f, seed, out_tokens, n_accepted, workspace, ws_bytes, nullptr, stream);
+}
+
+size_t ssd_verify_top_p_workspace_bytes(int B, int gamma_max) {
+  if (B < 1 || gamma_max < 0) return 0;
+  return topp_layout(B, gamma_max).total;
+}
+
+ssd_status ssd_verify_top_p(const void* target_logits, const void* draft_logits, ssd_dtype dtype,
+                            const int32_t* draft_tokens, int B, int gamma, int V, float temperature, float top_p,
+                            uint64_t seed, int32_t* out_tokens, int32_t* n_accepted, void* workspace, size_t ws_bytes,
+                            void* stream) {
+  g_last_error.clear();
+  if (!temperature_valid(temperature))
+    return fail(SSD_ERR_TEMPERATURE, "temperature %g is not 0 or in [1e-6, inf)", static_cast<double>(temperature));
+  if (!(top_p > 0.f) || !(top_p <= 1.f))
+    return fail(SSD_ERR_SHAPE, "top_p %g is not in (0, 1]", static_cast<double>(top_p));
+  return verify_common(target_logits, draft_logits, dtype, draft_tokens, B, gamma, V, nullptr, nullptr, temperature,
+                       temperature == 0.f, seed, out_tokens, n_accepted, workspace, ws_bytes, nullptr, stream, false,
+                       top_p);
 }
 
 ssd_status ssd_verify_pipelined(const void* target_logits, const void* draft_logits, ssd_dtype dtype,

@@ -48,6 +48,10 @@ struct VerifyArgs {
                                // distribution p' of their position, which replaces p in the accept test
                                // and the residual
   const float* sag_Zs;         // [B, gmax+1]: the Saguaro normalisers sum_v sqrt(p max(r, 1e-8))
+  const float* tp_th;          // [B, gmax+1, 2] or null: top-p nucleus thresholds (logits) of each
+                               // target (slot 0) and draft (slot 1) row; given, both distributions are
+                               // truncated to their nuclei
+  const float* tp_z;           // [B, gmax+1, 2]: the nuclei's masses, in units of exp2(x c - fl(m c))
   int first;                   // 1: every streaming CTA waits for the previous kernel (the first
                                // segment of a call); 0: only the first CTA waits (a later segment, or
                                // a pipelined call)
@@ -83,6 +87,27 @@ struct SagArgs {
   int32_t* status;          // workspace [1]: device error bits
   ChunkGeometry geo;
 };
+
+// One level of the top-p radix select: digit = (key >> shift) & ((1 << bits) - 1).
+struct TopPArgs {
+  const void* target;   // [B, gmax+1, V]
+  const void* draft;    // [B, gmax, V]
+  int B, gmax;
+  const int32_t* gamma; // [B] or null
+  const float* temps;   // [B] or null (temp_scalar)
+  float temp_scalar;
+  float top_p;
+  const float4* part;   // the streaming kernel's records
+  ChunkGeometry geo;
+  int level, nlevels, shift, bits;
+  unsigned long long* hist;    // [B, gmax+1, 2, 1 << bits]: this level's histograms (zeroed by the caller)
+  uint32_t* prefix;            // [B, gmax+1, 2]: the key digits fixed so far
+  unsigned long long* above;   // [B, gmax+1, 2]: mass of keys above the prefix's range
+  unsigned long long* goal;    // [B, gmax+1, 2]: ceil(top_p * total mass)
+  float* th;                   // [B, gmax+1, 2]: the nucleus threshold (logit), after the last level
+  float* z;                    // [B, gmax+1, 2]: the nucleus mass, after the last level
+};
+cudaError_t launch_topp_level(const TopPArgs& a, int esize, cudaStream_t stream);
 
 // Workspace layout (byte offsets), shared by the launchers and the API: the
 // status word, then two halves used by alternate calls, each holding the

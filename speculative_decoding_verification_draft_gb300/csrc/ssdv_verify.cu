@@ -89,6 +89,35 @@ struct SagDraftW {
   }
 };
 
+// Top-p: the residual of the truncated distributions, scaled by the target's
+// kept mass: w = max(e_t [x_t >= th_t] - (Zt/Zd) e_d [x_d >= th_d], 0), with
+// Zt, Zd the kept masses (the nuclei: logits at or above the thresholds).
+template <typename E>
+struct TopPResidualW {
+  float c, mct, mcd, kr;  // kr = Zt / Zd of the kept masses
+  float th_t, th_d;       // nucleus thresholds (logits)
+  __device__ __forceinline__ void operator()(const float (&xt)[Elem<E>::kVec], const float (&xd)[Elem<E>::kVec],
+                                             float (&w)[Elem<E>::kVec]) const {
+#pragma unroll
+    for (int e = 0; e < Elem<E>::kVec; ++e) {
+      const float et = xt[e] >= th_t ? fast_exp2(fmaf(xt[e], c, -mct)) : 0.f;
+      const float ed = xd[e] >= th_d ? fast_exp2(fmaf(xd[e], c, -mcd)) : 0.f;
+      w[e] = fmaxf(fmaf(-kr, ed, et), 0.f);
+    }
+  }
+};
+
+// Top-p target weights: w = e_t on the nucleus, 0 elsewhere.
+template <typename E>
+struct TopPTargetW {
+  float c, mct, th_t;
+  __device__ __forceinline__ void operator()(const float (&xt)[Elem<E>::kVec], const float (&)[Elem<E>::kVec],
+                                             float (&w)[Elem<E>::kVec]) const {
+#pragma unroll
+    for (int e = 0; e < Elem<E>::kVec; ++e) w[e] = xt[e] >= th_t ? fast_exp2(fmaf(xt[e], c, -mct)) : 0.f;
+  }
+};
+
 // Target weights: w = e_t (proportional to q).
 template <typename E>
 struct TargetW {
@@ -366,8 +395,12 @@ __device__ __noinline__ void warp_draw_row(const VerifyArgs& a, int b, int n, si
   }
 }
 
-template <typename E, bool kSag>
+// Sampling modes: plain; draft tokens from the Saguaro distribution; top-p.
+enum { kModePlain = 0, kModeSag = 1, kModeTopP = 2 };
+
+template <typename E, int kMode>
 __global__ void __launch_bounds__(kT2, 8) sample_kernel(const VerifyArgs a) {
+  constexpr bool kSag = kMode == kModeSag, kTopP = kMode == kModeTopP;
   __shared__ UnitStat ust[SSD_MAX_GAMMA + 1];
   __shared__ int tok_x[SSD_MAX_GAMMA];
   __shared__ float tok_t[SSD_MAX_GAMMA], tok_d[SSD_MAX_GAMMA];
@@ -476,6 +509,17 @@ __global__ void __launch_bounds__(kT2, 8) sample_kernel(const VerifyArgs a) {
       const UnitStat s = ust[lane];
       if (greedy) {
         acc = tok_x[lane] == s.ai;
+      } else if constexpr (kTopP) {
+        // a = min(1, q'(x)/p'(x)) on the truncated distributions: q'(x) = 0
+        // outside the target's nucleus (rejected), p'(x) = 0 outside the
+        // draft's (accepted)
+        const size_t rt = (static_cast<size_t>(b) * W + lane) * 2;
+        const float tht = __ldcg(a.tp_th + rt), thd = __ldcg(a.tp_th + rt + 1);
+        const float zt = __ldcg(a.tp_z + rt), zd = __ldcg(a.tp_z + rt + 1);
+        const float q = tok_t[lane] >= tht ? fast_exp2(fmaf(tok_t[lane], cc, -scaled_max(s.tm, cc))) / zt : 0.f;
+        const float p = tok_d[lane] >= thd ? fast_exp2(fmaf(tok_d[lane], cc, -scaled_max(s.dm, cc))) / zd : 0.f;
+        if (p > 0.f) ratio_acc = fminf(1.f, q / p);
+        acc = dr.accept < ratio_acc;
       } else if constexpr (kSag) {
         // a = min(1, q(x)/p'(x)), p'(x) = sqrt(p(x) max(r(x), 1e-8)) / Zs
         if (tok_d[lane] != -INFINITY) {
@@ -551,19 +595,30 @@ __global__ void __launch_bounds__(kT2, 8) sample_kernel(const VerifyArgs a) {
   const float mct = scaled_max(s.tm, cc);
   const float mcd = residual ? scaled_max(s.dm, cc) : 0.f;
   const float kr = residual ? s.ts / s.ds : 0.f;
-  // the residual weights: (q - p)+ scaled by Z_t, or (q - p')+ under Saguaro sampling
-  using RW = std::conditional_t<kSag, SagDraftW<E>, ResidualW<E>>;
+  // the residual weights: (q - p)+ scaled by Z_t, (q - p')+ under Saguaro
+  // sampling, or the truncated residual under top-p
+  using RW = std::conditional_t<kSag, SagDraftW<E>, std::conditional_t<kTopP, TopPResidualW<E>, ResidualW<E>>>;
+  using TW = std::conditional_t<kTopP, TopPTargetW<E>, TargetW<E>>;
   RW rw;
+  TW tw;
+  if constexpr (kTopP) {
+    const size_t rt = (static_cast<size_t>(b) * W + pos) * 2;
+    const float tht = __ldcg(a.tp_th + rt), zt = __ldcg(a.tp_z + rt);
+    const float thd = residual ? __ldcg(a.tp_th + rt + 1) : 0.f, zd = residual ? __ldcg(a.tp_z + rt + 1) : 1.f;
+    rw = TopPResidualW<E>{cc, mct, mcd, zt / zd, tht, thd};
+    tw = TopPTargetW<E>{cc, mct, tht};
+  } else {
+    tw = TW{cc, mct};
+  }
   if constexpr (kSag) {
     const size_t uu = static_cast<size_t>(b) * W + pos;
     const double Sw = residual ? __ldcg(a.sag_S + uu) : 0.0;
     const float zs = residual ? __ldcg(a.sag_Zs + uu) : 1.f;
     rw = SagDraftW<E>{cc, mct, mcd, kr, 1.f / s.ts, 1.f / s.ds,
                       Sw > 0.0 ? static_cast<float>(1.0 / Sw) : 1.f / s.ts, 1.f / zs, Sw > 0.0 ? 0 : 1};
-  } else {
+  } else if constexpr (!kTopP) {
     rw = ResidualW<E>{cc, mct, mcd, kr};
   }
-  const TargetW<E> tw{cc, mct};
   const double ures = static_cast<double>(unit_draws(a.seed, a.req_base + b, pos).resample);
   const E* trow = static_cast<const E*>(a.target) + (static_cast<size_t>(b) * W + pos) * V;
   const E* drow = residual ? static_cast<const E*>(a.draft) + (static_cast<size_t>(b) * a.gmax + pos) * V : nullptr;
@@ -810,10 +865,12 @@ template __global__ void small_verify_kernel<float>(const VerifyArgs);
 
 template __global__ void stream_kernel<uint16_t>(const VerifyArgs);
 template __global__ void stream_kernel<float>(const VerifyArgs);
-template __global__ void sample_kernel<uint16_t, false>(const VerifyArgs);
-template __global__ void sample_kernel<float, false>(const VerifyArgs);
-template __global__ void sample_kernel<uint16_t, true>(const VerifyArgs);
-template __global__ void sample_kernel<float, true>(const VerifyArgs);
+template __global__ void sample_kernel<uint16_t, kModePlain>(const VerifyArgs);
+template __global__ void sample_kernel<float, kModePlain>(const VerifyArgs);
+template __global__ void sample_kernel<uint16_t, kModeSag>(const VerifyArgs);
+template __global__ void sample_kernel<float, kModeSag>(const VerifyArgs);
+template __global__ void sample_kernel<uint16_t, kModeTopP>(const VerifyArgs);
+template __global__ void sample_kernel<float, kModeTopP>(const VerifyArgs);
 
 __global__ void uniforms_kernel(uint64_t seed, int B, int W, float* out) {
   const long long n = static_cast<long long>(B) * W;
@@ -881,8 +938,9 @@ cudaError_t launch_sample_t(const VerifyArgs& a, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return a.sag_S ? cudaLaunchKernelEx(&cfg, sample_kernel<E, true>, a)
-                 : cudaLaunchKernelEx(&cfg, sample_kernel<E, false>, a);
+  return a.sag_S  ? cudaLaunchKernelEx(&cfg, sample_kernel<E, kModeSag>, a)
+         : a.tp_th ? cudaLaunchKernelEx(&cfg, sample_kernel<E, kModeTopP>, a)
+                   : cudaLaunchKernelEx(&cfg, sample_kernel<E, kModePlain>, a);
 }
 
 template <typename E>

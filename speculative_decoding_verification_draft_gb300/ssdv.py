@@ -58,6 +58,9 @@ def _declare(lib):
     lib.ssd_verify_saguaro.argtypes = [P, P, I, P, I, I, I, I, I, F, U64, P, P, P, P, P, P, P, SZ, P]
     lib.ssd_cache_check.argtypes = [P, P, P, I, I, I, P, P, P]
     lib.ssd_verify_saguaro_draft.argtypes = [P, P, I, P, I, I, I, F, U64, P, P, P, SZ, P]
+    lib.ssd_verify_top_p.argtypes = [P, P, I, P, I, I, I, F, F, U64, P, P, P, SZ, P]
+    lib.ssd_verify_top_p_workspace_bytes.argtypes = [I, I]
+    lib.ssd_verify_top_p_workspace_bytes.restype = SZ
     lib.ssd_read_status.argtypes = [P, SZ, P, P]
     lib.ssd_debug_uniforms.argtypes = [U64, I, I, P, P]
     lib.ssd_status_str.argtypes = [I]
@@ -66,7 +69,7 @@ def _declare(lib):
     lib.ssd_last_error.restype = ctypes.c_char_p
     for name in ("ssd_workspace_init", "ssd_verify", "ssd_verify_noalloc", "ssd_verify_pipelined",
                  "ssd_verify_ragged", "ssd_saguaro_prespec", "ssd_debug_rowstats", "ssd_debug_saguaro_stats", "ssd_read_status",
-                 "ssd_verify_saguaro", "ssd_cache_check", "ssd_verify_saguaro_draft",
+                 "ssd_verify_saguaro", "ssd_cache_check", "ssd_verify_saguaro_draft", "ssd_verify_top_p",
                  "ssd_debug_uniforms"):
         getattr(lib, name).restype = I
     return lib
@@ -331,6 +334,39 @@ def verify_saguaro(target: torch.Tensor, draft: torch.Tensor, draft_tokens: torc
                                     _dev(hit, "hit") if check else None, _dev(n_hits, "n_hits") if check else None,
                                     _dev(ws, "workspace"), ws.numel(), _stream(stream)))
     return out_tokens, n_accepted, bonus_topk, saguaro_tokens, hit, n_hits
+
+
+_topp_ws_cache = {}
+
+
+def verify_top_p(target: torch.Tensor, draft: Optional[torch.Tensor], draft_tokens: torch.Tensor, temperature: float,
+                 top_p: float, seed: int, out_tokens: Optional[torch.Tensor] = None,
+                 n_accepted: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None, stream=None):
+    """ssd_verify_top_p: both distributions truncated to their top-p nuclei.
+    Returns (out_tokens [B, g+1], n_accepted [B])."""
+    B, W, V = target.shape
+    g = W - 1
+    dev = target.device
+    if out_tokens is None:
+        out_tokens = torch.empty(B, W, dtype=torch.int32, device=dev)
+    if n_accepted is None:
+        n_accepted = torch.empty(B, dtype=torch.int32, device=dev)
+    ws = workspace
+    if ws is None:
+        key = _ws_key(dev)
+        need = int(lib().ssd_verify_top_p_workspace_bytes(B, g))
+        ws = _topp_ws_cache.get(key)
+        if ws is None or ws.numel() < need:
+            ws = torch.zeros(max(need, 1 << 16), dtype=torch.uint8, device=dev)
+            _topp_ws_cache[key] = ws
+    dptr = _dev(draft, "draft_logits", target.dtype) if draft is not None else None
+    tptr = _dev(draft_tokens, "draft_tokens", torch.int32) if g > 0 else None
+    _check(lib().ssd_verify_top_p(_dev(target, "target_logits"), dptr, _dtype_code(target), tptr, B, g, V,
+                                  float(temperature), float(top_p), int(seed) & ((1 << 64) - 1),
+                                  _dev(out_tokens, "out_tokens", torch.int32),
+                                  _dev(n_accepted, "n_accepted", torch.int32), _dev(ws, "workspace"), ws.numel(),
+                                  _stream(stream)))
+    return out_tokens, n_accepted
 
 
 def verify_saguaro_draft(target: torch.Tensor, draft: torch.Tensor, draft_tokens: torch.Tensor, temperature: float,

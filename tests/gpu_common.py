@@ -33,7 +33,7 @@ def orc():
 
 
 def verify_oracle(batch, seed, stats=False, req_ids=None, subset=None, nthreads=16, band=PAGES_BAND,
-                  draft_dist="draft"):
+                  draft_dist="draft", top_p=1.0):
     tgt, dft = batch.numpy_logits()
     tok = batch.draft_tokens.cpu().numpy()
     temps = batch.temperature
@@ -49,7 +49,7 @@ def verify_oracle(batch, seed, stats=False, req_ids=None, subset=None, nthreads=
             temps = temps[subset]
         req_ids = subset
     return orc().verify_batch(tgt, dft, tok, temps, seed, gamma=gam, stats=stats, nthreads=nthreads,
-                              req_ids=req_ids, band=band, draft_dist=draft_dist)
+                              req_ids=req_ids, band=band, draft_dist=draft_dist, top_p=top_p)
 
 
 def compare_verify(out_g, n_g, ref, V):

@@ -31,7 +31,8 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for want in ("ssd_verify", "ssd_verify_pipelined", "ssd_verify_noalloc", "ssd_verify_ragged",
                  "ssd_saguaro_prespec", "ssd_saguaro_workspace_bytes", "ssd_workspace_bytes",
-                 "ssd_verify_saguaro", "ssd_cache_check", "ssd_verify_saguaro_draft",
+                 "ssd_verify_saguaro", "ssd_cache_check", "ssd_verify_saguaro_draft", "ssd_verify_top_p",
+                 "ssd_verify_top_p_workspace_bytes",
                  "ssd_workspace_init", "ssd_debug_rowstats", "ssd_debug_saguaro_stats",
                  "ssd_debug_uniforms", "ssd_read_status", "ssd_status_str", "ssd_last_error"):
         assert want in names
@@ -74,6 +75,10 @@ def test_host_validation_without_gpu(lib):
     assert L.ssd_verify_saguaro(p, p, 0, p, 1, 1, 8, 3, 0, 1.0, 0, None, p, p, p, None, None, p, 1 << 20,
                                 None) == 1
     assert L.ssd_cache_check(p, p, p, 4, 2, 3, None, None, None) == 1
+    # top-p: top_p in (0, 1]; its workspace is larger than plain verification's
+    assert L.ssd_verify_top_p(p, p, 0, p, 1, 1, 8, 1.0, 0.0, 0, p, p, p, 1 << 20, None) == 2
+    assert L.ssd_verify_top_p(p, p, 0, p, 1, 1, 8, 1.0, 1.5, 0, p, p, p, 1 << 20, None) == 2
+    assert L.ssd_verify_top_p_workspace_bytes(8, 4) > L.ssd_workspace_bytes(8, 4)
     # verification under Saguaro sampling: greedy rejected, workspace sized by V
     assert L.ssd_verify_saguaro_draft(p, p, 0, p, 1, 1, 8, 0.0, 0, p, p, p, 1 << 20, None) == 6
     assert L.ssd_verify_saguaro_draft(p, p, 0, p, 4, 2, 8, 1.0, 0, p, p, p, 8, None) == 9
