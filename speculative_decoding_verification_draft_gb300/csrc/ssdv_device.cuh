@@ -20,6 +20,8 @@
 namespace ssdv {
 
 constexpr int kThreads = 256;
+// vectors of a chunk row per thread in the register form of the streaming kernel
+constexpr int kRegVecs = 8;
 constexpr int kWarps = kThreads / 32;
 constexpr uint32_t kWaitLimit = 1u << 24;  // bounded polls of an mbarrier
 constexpr float kLog2e = 1.4426950408889634f;
@@ -394,10 +396,53 @@ __device__ __forceinline__ void warp_merge_topk(TopK<K, kNegInf>& tk, float (&ov
   }
 }
 
+// ---------------------------------------------------------------------------
+// Float-float numbers: hi + lo with |lo| at most half an ulp of hi, about 48
+// significant bits.  Running sums across lanes and pieces use them: a chain of
+// dependent fp64 adds is slow on GB300's small fp64 units, and fp32 alone
+// would put a row's CDF edges too far from the exact ones.  The error-free
+// transformations are Knuth's TwoSum and the FMA form of Dekker's TwoProduct;
+// every operation is an explicit round-to-nearest intrinsic, so the compiler
+// neither contracts nor reorders them.
+// ---------------------------------------------------------------------------
+struct FF {
+  float hi, lo;
+};
+__device__ __forceinline__ FF ff_fast_two_sum(float a, float b) {  // |a| >= |b|
+  const float s = __fadd_rn(a, b);
+  return FF{s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+__device__ __forceinline__ FF ff_add(FF a, FF b) {
+  const float s = __fadd_rn(a.hi, b.hi);
+  const float bb = __fsub_rn(s, a.hi);
+  const float e = __fadd_rn(__fsub_rn(a.hi, __fsub_rn(s, bb)), __fsub_rn(b.hi, bb));
+  return ff_fast_two_sum(s, __fadd_rn(e, __fadd_rn(a.lo, b.lo)));
+}
+__device__ __forceinline__ FF ff_sub(FF a, FF b) { return ff_add(a, FF{-b.hi, -b.lo}); }
+// a * u for a float u
+__device__ __forceinline__ FF ff_mul(FF a, float u) {
+  const float p = __fmul_rn(a.hi, u);
+  const float e = __fmaf_rn(a.hi, u, -p);
+  return ff_fast_two_sum(p, __fmaf_rn(a.lo, u, e));
+}
+__device__ __forceinline__ bool ff_lt(FF a, FF b) { return a.hi < b.hi || (a.hi == b.hi && a.lo < b.lo); }
+__device__ __forceinline__ float ff_float(FF a) { return __fadd_rn(a.hi, a.lo); }
+__device__ __forceinline__ double ff_double(FF a) { return static_cast<double>(a.hi) + static_cast<double>(a.lo); }
+__device__ __forceinline__ FF ff_shfl_xor(FF a, int o) {
+  return FF{__shfl_xor_sync(0xFFFFFFFFu, a.hi, o), __shfl_xor_sync(0xFFFFFFFFu, a.lo, o)};
+}
+// sum of one float per lane, valid in every lane
+__device__ __forceinline__ FF ff_warp_sum(float v) {
+  FF t{v, 0.f};
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) t = ff_add(t, ff_shfl_xor(t, o));
+  return t;
+}
+
 struct ScanHit {
-  int elem;     // element index relative to the chunk start, -1 if none
-  double edge;  // weight before the element, relative to the scan start
-  float w;      // the element's weight
+  int elem;  // element index relative to the chunk start, -1 if none
+  FF edge;   // weight before the element, relative to the scan start
+  float w;   // the element's weight
 };
 
 // ---------------------------------------------------------------------------
@@ -493,20 +538,21 @@ __device__ __forceinline__ float piece_lane_sum(const PieceRows<E>& pr, const WF
 }
 
 // One warp, one value per lane in index order: the exclusive prefix of every
-// lane (fp64) and the first lane whose running sum passes tl, else the last
-// lane with a positive value (-1 if none).
-__device__ __forceinline__ int lane_locate(double v, double tl, double* before) {
+// lane (float-float) and the first lane whose running sum passes tl, else the
+// last lane with a positive value (-1 if none).
+__device__ __forceinline__ int lane_locate(float v, FF tl, FF* before) {
   const int lane = threadIdx.x & 31;
-  double incl = v;
+  FF incl{v, 0.f};
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const double t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (lane >= o) incl += t;
+    const FF t{__shfl_up_sync(0xFFFFFFFFu, incl.hi, o), __shfl_up_sync(0xFFFFFFFFu, incl.lo, o)};
+    if (lane >= o) incl = ff_add(incl, t);
   }
-  const unsigned hm = __ballot_sync(0xFFFFFFFFu, v > 0.0 && tl < incl);
-  const unsigned pm = __ballot_sync(0xFFFFFFFFu, v > 0.0);
+  const unsigned hm = __ballot_sync(0xFFFFFFFFu, v > 0.f && ff_lt(tl, incl));
+  const unsigned pm = __ballot_sync(0xFFFFFFFFu, v > 0.f);
   const int L = hm ? __ffs(hm) - 1 : (pm ? 31 - __clz(pm) : -1);
-  *before = __shfl_sync(0xFFFFFFFFu, incl - v, L >= 0 ? L : 0);
+  const FF ex = ff_sub(incl, FF{v, 0.f});
+  *before = FF{__shfl_sync(0xFFFFFFFFu, ex.hi, L >= 0 ? L : 0), __shfl_sync(0xFFFFFFFFu, ex.lo, L >= 0 ? L : 0)};
   return L;
 }
 
@@ -517,7 +563,7 @@ __device__ __forceinline__ int lane_locate(double v, double tl, double* before) 
 // a small share of the row's).  Returns the element index relative to the
 // piece start (-1 if none), the weight before it and its weight.
 template <typename E, typename WFun>
-__device__ __forceinline__ ScanHit scan_piece(const PieceRows<E>& pr, const WFun& wfun, double tl) {
+__device__ __forceinline__ ScanHit scan_piece(const PieceRows<E>& pr, const WFun& wfun, FF tl) {
   constexpr int kVec = Elem<E>::kVec;
   const int lane = threadIdx.x & 31;
   float w[4][kVec];
@@ -527,13 +573,13 @@ __device__ __forceinline__ ScanHit scan_piece(const PieceRows<E>& pr, const WFun
     pr.weights(k, wfun, w[k]);
     ls += pair_sum(w[k]);
   }
-  double before = 0.0;
-  const int L = lane_locate(static_cast<double>(ls), tl, &before);
-  if (L < 0) return ScanHit{-1, NAN, 0.f};
+  FF before;
+  const int L = lane_locate(ls, tl, &before);
+  if (L < 0) return ScanHit{-1, FF{NAN, 0.f}, 0.f};
   int el = -1;
   float edge = 0.f, we = 0.f;
   if (lane == L) {
-    const float t = static_cast<float>(tl - before);
+    const float t = ff_float(ff_sub(tl, before));
     float acc = 0.f;
     bool done = false;
 #pragma unroll
@@ -553,8 +599,8 @@ __device__ __forceinline__ ScanHit scan_piece(const PieceRows<E>& pr, const WFun
   el = __shfl_sync(0xFFFFFFFFu, el, L);
   edge = __shfl_sync(0xFFFFFFFFu, edge, L);
   we = __shfl_sync(0xFFFFFFFFu, we, L);
-  if (el < 0) return ScanHit{-1, NAN, 0.f};
-  return ScanHit{4 * L * kVec + el, before + static_cast<double>(edge), we};
+  if (el < 0) return ScanHit{-1, FF{NAN, 0.f}, 0.f};
+  return ScanHit{4 * L * kVec + el, ff_add(before, FF{edge, 0.f}), we};
 }
 
 // One warp: a row's piece sums, copied into the warp's shared slice `v` (lane
@@ -564,7 +610,8 @@ struct RowPieces {
   float* v;  // shared, np floats
   int per;
   float lane_sum;
-  double total;
+  FF tot;        // the row total
+  double total;  // the same, as one fp64 value
   __device__ __forceinline__ void load(const float* psum, int np, float* slice) {
     const int lane = threadIdx.x & 31;
     v = slice;
@@ -576,38 +623,36 @@ struct RowPieces {
       const int q = lane * per + k;
       if (q < np) lane_sum += v[q];
     }
-    double t = static_cast<double>(lane_sum);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
-    total = t;
+    tot = ff_warp_sum(lane_sum);
+    total = ff_double(tot);
   }
 };
 
 
 // The element of a row drawn at u * total of the row's piece sums.
 struct RowDraw {
-  int elem;     // element index in the row, -1 if none
-  double edge;  // weight before it (from the row start)
-  float w;      // its weight
+  int elem;  // element index in the row, -1 if none
+  FF edge;   // weight before it (from the row start)
+  float w;   // its weight
 };
 
 // One warp: the lane whose run of pieces holds target = u * total, the piece
 // within that run, then that piece reloaded and scanned (wfun gives the
 // weights; drow may be null).
 template <typename E, typename WFun>
-__device__ __forceinline__ RowDraw warp_locate_row(const RowPieces& rp, double u, const E* trow, const E* drow,
+__device__ __forceinline__ RowDraw warp_locate_row(const RowPieces& rp, float u, const E* trow, const E* drow,
                                                    int V, bool aligned, const WFun& wfun) {
   constexpr int kVec = Elem<E>::kVec;
   const int lane = threadIdx.x & 31;
   const int pelems = kPieceVecs * kVec;
   const int np = (V + pelems - 1) / pelems;
-  const double target = u * rp.total;
-  double before = 0.0;
-  const int L = lane_locate(static_cast<double>(rp.lane_sum), target, &before);
+  const FF target = ff_mul(rp.tot, u);
+  FF before;
+  const int L = lane_locate(rp.lane_sum, target, &before);
   int owner = -1;
   float obefore = 0.f;
   if (lane == L) {
-    const float t = static_cast<float>(target - before);
+    const float t = ff_float(ff_sub(target, before));
     float acc = 0.f;
     for (int k = 0; k < rp.per; ++k) {
       const int q = L * rp.per + k;
@@ -621,14 +666,14 @@ __device__ __forceinline__ RowDraw warp_locate_row(const RowPieces& rp, double u
     }
   }
   owner = __shfl_sync(0xFFFFFFFFu, owner, L >= 0 ? L : 0);
-  const double owner_before = before + static_cast<double>(__shfl_sync(0xFFFFFFFFu, obefore, L >= 0 ? L : 0));
-  RowDraw d{-1, NAN, 0.f};
+  const FF owner_before = ff_add(before, FF{__shfl_sync(0xFFFFFFFFu, obefore, L >= 0 ? L : 0), 0.f});
+  RowDraw d{-1, FF{NAN, 0.f}, 0.f};
   if (L >= 0 && owner >= 0) {
     const int olo = owner * pelems;
     PieceRows<E> pr;
     pr.load(trow + olo, drow ? drow + olo : nullptr, min(pelems, V - olo), aligned);
-    const ScanHit h = scan_piece(pr, wfun, target - owner_before);
-    if (h.elem >= 0) d = RowDraw{olo + h.elem, owner_before + h.edge, h.w};
+    const ScanHit h = scan_piece(pr, wfun, ff_sub(target, owner_before));
+    if (h.elem >= 0) d = RowDraw{olo + h.elem, ff_add(owner_before, h.edge), h.w};
   }
   return d;
 }

@@ -364,7 +364,7 @@ __global__ void __launch_bounds__(kS) mix_kernel(const SagArgs a) {
   if (a.zsum && lane == 0) a.zsum[u] = static_cast<float>(rp.total);
   if (!a.saguaro_tokens) return;  // the normaliser is all a later kernel needs
   const float u_sag = unit_draws(a.seed, a.req_base + b, j).saguaro;
-  const RowDraw d = warp_locate_row<E>(rp, static_cast<double>(u_sag), trow, drow, V, a.geo.bulk != 0, mw);
+  const RowDraw d = warp_locate_row<E>(rp, u_sag, trow, drow, V, a.geo.bulk != 0, mw);
   float* st = a.stats ? a.stats + u * SSD_NSTAT_SAGUARO : nullptr;
   if (lane == 0) {
     const bool ok = d.elem >= 0 && rp.total > 0.0;
@@ -373,8 +373,9 @@ __global__ void __launch_bounds__(kS) mix_kernel(const SagArgs a) {
     if (st && ok) {
       st[3] = static_cast<float>(rp.total);
       st[4] = static_cast<float>(static_cast<double>(d.w) / rp.total);
-      st[8] = static_cast<float>(static_cast<double>(u_sag) - d.edge / rp.total);
-      st[9] = static_cast<float>((d.edge + static_cast<double>(d.w)) / rp.total - static_cast<double>(u_sag));
+      const double edge = ff_double(d.edge);
+      st[8] = static_cast<float>(static_cast<double>(u_sag) - edge / rp.total);
+      st[9] = static_cast<float>((edge + static_cast<double>(d.w)) / rp.total - static_cast<double>(u_sag));
     }
   }
   if (fallback) {

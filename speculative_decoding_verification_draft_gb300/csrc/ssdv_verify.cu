@@ -34,6 +34,8 @@
 // segment's CTAs saw the call's inputs complete, and may stream while the
 // previous segment's sampling kernel runs: the segments use disjoint
 // workspace rows.  A call never overlaps the work of the previous call.
+#include <cstdlib>
+#include <cstring>
 #include <type_traits>
 
 #include "ssdv_device.cuh"
@@ -334,6 +336,188 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const VerifyArgs a) {
 }
 
 // ---------------------------------------------------------------------------
+// Kernel 1, register form (rows 16-byte aligned, at most kNV vectors of a
+// chunk row per thread).  Every thread issues the 16-byte loads of all its
+// target and draft vectors at once, so a CTA keeps its whole chunk in flight
+// with no staging buffer, no mbarrier and one block barrier.  A thread whose
+// k-th vector lies past the chunk re-reads the chunk's last vector instead:
+// harmless for the maxima, and left out of the sums.  Each warp takes the
+// maxima of its lanes' vectors, sums exp2(x*c - fl(m_w*c)) against its own
+// maxima m_w, and thread 0 folds the eight warps' (max, sum) pairs into the
+// chunk record (the same record as the staged form).
+// ---------------------------------------------------------------------------
+namespace {
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+template <typename E>
+__device__ __forceinline__ float ld_logit(const E* p) {
+  if constexpr (sizeof(E) == 2) {
+    unsigned short h;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(h) : "l"(p));
+    return Elem<E>::to_float(h);
+  } else {
+    float f;
+    asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(f) : "l"(p));
+    return f;
+  }
+}
+
+// Resident CTAs per SM the register form is built for (registers bound it).
+constexpr int reg_min_blocks(int nv) { return nv <= 4 ? 5 : nv <= 6 ? 4 : 3; }
+
+}  // namespace
+
+template <typename E, int kNV>
+__global__ void __launch_bounds__(kThreads, reg_min_blocks(kNV)) stream_reg_kernel(const VerifyArgs a) {
+  constexpr int kVec = Elem<E>::kVec;
+  __shared__ float red_f[4 * kWarps];
+  __shared__ int red_i[kWarps];
+  // ordering with the previous kernel: as in the staged form
+  if (a.first || (blockIdx.x | blockIdx.y | blockIdx.z) == 0) griddep_wait();
+  griddep_launch_dependents();
+
+  const ChunkGeometry& geo = a.geo;
+  const int V = geo.V, NC = geo.nchunk, W = a.gmax + 1;
+  const int c = blockIdx.x, b = blockIdx.y, i = W - 1 - static_cast<int>(blockIdx.z);
+  const int tid = threadIdx.x;
+  if (i == 0 && c == 0 && tid < W) a.ticket[b * W + tid] = 0;
+
+  const int g = a.gamma ? a.gamma[b] : a.gmax;
+  const float T = a.temps ? a.temps[b] : a.temp_scalar;
+  if (g < 0 || g > a.gmax || !temperature_ok(T) || i > g) return;  // padded rows are never read
+  const bool greedy = (T == 0.f);
+  const bool has_draft = !greedy && i < g;
+
+  const int lo = c * geo.chunk;
+  const int nvec = min(geo.chunk, V - lo) / kVec;  // aligned rows: whole vectors, at least one
+  const E* rt_e = static_cast<const E*>(a.target) + (static_cast<size_t>(b) * W + i) * V + lo;
+  const E* rd_e = has_draft ? static_cast<const E*>(a.draft) + (static_cast<size_t>(b) * a.gmax + i) * V + lo : nullptr;
+  const uint4* gt = reinterpret_cast<const uint4*>(rt_e);
+  const uint4* gd = reinterpret_cast<const uint4*>(rd_e);
+
+  uint4 vt[kNV], vd[kNV];
+#pragma unroll
+  for (int k = 0; k < kNV; ++k) vt[k] = ld_stream(gt + min(tid + k * kThreads, nvec - 1));
+  if (has_draft) {
+#pragma unroll
+    for (int k = 0; k < kNV; ++k) vd[k] = ld_stream(gd + min(tid + k * kThreads, nvec - 1));
+  } else {
+#pragma unroll
+    for (int k = 0; k < kNV; ++k) vd[k] = Elem<E>::max_init();
+  }
+  // the draft token's two logits, when it falls in this chunk
+  float xt_tok = 0.f, xd_tok = 0.f;
+  if (tid == 0 && has_draft && a.draft_tokens) {
+    const int x = a.draft_tokens[static_cast<size_t>(b) * a.gmax + i];
+    if (x >= lo && x < lo + nvec * kVec) {
+      xt_tok = ld_logit(rt_e + (x - lo));
+      xd_tok = ld_logit(rd_e + (x - lo));
+    }
+  }
+
+  const int warp = tid >> 5, lane = tid & 31;
+  float4* rec = a.part + ((static_cast<size_t>(b) * W + i) * NC + c) * 2;
+  if (greedy) {
+    // target argmax: each thread in index order (the first of equal values
+    // wins), then the warp butterfly and thread 0 over warps
+    ArgMax am{-INFINITY, -1};
+#pragma unroll
+    for (int k = 0; k < kNV; ++k) {
+      const int v = tid + k * kThreads;
+      if (v < nvec) {
+        float f[kVec];
+        Elem<E>::unpack(vt[k], f);
+#pragma unroll
+        for (int e = 0; e < kVec; ++e)
+          if (am.i < 0 || f[e] > am.v) am = ArgMax{f[e], lo + v * kVec + e};
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const ArgMax oa{__shfl_xor_sync(0xFFFFFFFFu, am.v, o), __shfl_xor_sync(0xFFFFFFFFu, am.i, o)};
+      am = better_arg(am, oa);
+    }
+    if (lane == 0) {
+      red_f[warp] = am.v;
+      red_i[warp] = am.i;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      ArgMax best{-INFINITY, -1};
+      for (int w = 0; w < kWarps; ++w) best = better_arg(best, ArgMax{red_f[w], red_i[w]});
+      rec[0] = make_float4(best.v, 0.f, -INFINITY, 0.f);
+      rec[1] = make_float4(best.v, __int_as_float(best.i), 0.f, 0.f);
+    }
+    return;
+  }
+
+  // the warp's maxima (packed per thread, then a butterfly)
+  uint4 pt = Elem<E>::max_init(), pd = Elem<E>::max_init();
+#pragma unroll
+  for (int k = 0; k < kNV; ++k) {
+    pt = Elem<E>::max_acc(pt, vt[k]);
+    pd = Elem<E>::max_acc(pd, vd[k]);
+  }
+  float mt = Elem<E>::max_final(pt), md = Elem<E>::max_final(pd);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, o));
+    md = fmaxf(md, __shfl_xor_sync(0xFFFFFFFFu, md, o));
+  }
+  // sums of exp2(x*c - fl(m_w*c)) against the warp's maxima
+  const float cc = kLog2e / T;
+  const F2 c2 = f2_make(cc, cc);
+  float st = 0.f, sd = 0.f;
+  if (mt != -INFINITY) {
+    const float nm = -scaled_max(mt, cc);
+    const F2 nm2 = f2_make(nm, nm);
+    F2 acc = f2_make(0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < kNV; ++k)
+      if (tid + k * kThreads < nvec) acc = f2_add(acc, Elem<E>::exp_sum(vt[k], c2, nm2));
+    float a0, a1;
+    f2_split(acc, a0, a1);
+    st = a0 + a1;
+  }
+  if (md != -INFINITY) {
+    const float nm = -scaled_max(md, cc);
+    const F2 nm2 = f2_make(nm, nm);
+    F2 acc = f2_make(0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < kNV; ++k)
+      if (tid + k * kThreads < nvec) acc = f2_add(acc, Elem<E>::exp_sum(vd[k], c2, nm2));
+    float a0, a1;
+    f2_split(acc, a0, a1);
+    sd = a0 + a1;
+  }
+  st = warp_sum(st);
+  sd = warp_sum(sd);
+  if (lane == 0) {
+    red_f[warp] = mt;
+    red_f[kWarps + warp] = st;
+    red_f[2 * kWarps + warp] = md;
+    red_f[3 * kWarps + warp] = sd;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    MaxSum t{-INFINITY, 0.f}, d{-INFINITY, 0.f};
+    for (int w = 0; w < kWarps; ++w) {
+      t = combine_ms(t, MaxSum{red_f[w], red_f[kWarps + w]}, cc);
+      d = combine_ms(d, MaxSum{red_f[2 * kWarps + w], red_f[3 * kWarps + w]}, cc);
+    }
+    rec[0] = make_float4(t.m, t.s, has_draft ? d.m : -INFINITY, d.s);
+    rec[1] = make_float4(xd_tok, 0.f, 0.f, xt_tok);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Kernel 2: decisions and the draw.
 // ---------------------------------------------------------------------------
 namespace {
@@ -376,7 +560,7 @@ constexpr int kW2 = kT2 / 32;
 // statistics, the CDF edges of the drawn token.
 template <typename E, typename WFun>
 __device__ __noinline__ void warp_draw_row(const VerifyArgs& a, int b, int n, size_t pi_idx, const RowPieces& rp,
-                                           double ures, const E* trow, const E* drow, bool aligned, const WFun& wfun,
+                                           float ures, const E* trow, const E* drow, bool aligned, const WFun& wfun,
                                            const int* tok_x) {
   const int lane = threadIdx.x & 31;
   const RowDraw d = warp_locate_row<E>(rp, ures, trow, drow, a.geo.V, aligned, wfun);
@@ -387,8 +571,9 @@ __device__ __noinline__ void warp_draw_row(const VerifyArgs& a, int b, int n, si
     } else {
       if (a.stats) {
         float* st = a.stats + pi_idx * SSD_NSTAT_VERIFY;
-        st[8] = static_cast<float>(ures - d.edge / rp.total);
-        st[9] = static_cast<float>((d.edge + static_cast<double>(d.w)) / rp.total - ures);
+        const double edge = ff_double(d.edge);
+        st[8] = static_cast<float>(static_cast<double>(ures) - edge / rp.total);
+        st[9] = static_cast<float>((edge + static_cast<double>(d.w)) / rp.total - static_cast<double>(ures));
       }
       write_outputs(a, b, n, d.elem, tok_x);
     }
@@ -405,6 +590,7 @@ __global__ void __launch_bounds__(kT2, 8) sample_kernel(const VerifyArgs a) {
   __shared__ int tok_x[SSD_MAX_GAMMA];
   __shared__ float tok_t[SSD_MAX_GAMMA], tok_d[SSD_MAX_GAMMA];
   __shared__ int sh_n, sh_bad;
+  __shared__ float sh_uacc[SSD_MAX_GAMMA + 1], sh_ures[SSD_MAX_GAMMA + 1];
   extern __shared__ float s_pieces[];  // [kW2][NP]: the last warp's copy of its row's piece sums
 
   constexpr int kVec = Elem<E>::kVec;
@@ -436,8 +622,13 @@ __global__ void __launch_bounds__(kT2, 8) sample_kernel(const VerifyArgs a) {
 
   // Inputs only (overlaps the streaming kernel's tail; the kernel that wrote
   // them completed before any streaming CTA let this grid launch): the draft
-  // tokens.
+  // tokens, and every position's accept and resample uniforms.
   if (warp == 0) {
+    if (lane <= g) {
+      const Draws d = unit_draws(a.seed, a.req_base + b, lane);
+      sh_uacc[lane] = d.accept;
+      sh_ures[lane] = d.resample;
+    }
     bool bad = false;
     if (lane < g) {
       const int x = a.draft_tokens[static_cast<size_t>(b) * a.gmax + lane];
@@ -501,7 +692,7 @@ __global__ void __launch_bounds__(kT2, 8) sample_kernel(const VerifyArgs a) {
 
   // Decisions: accept tests of positions 0..g-1 and the first rejection.
   if (warp == 0) {
-    const Draws dr = unit_draws(a.seed, a.req_base + b, min(lane, g));  // lane g: the bonus position
+    const float uacc = sh_uacc[min(lane, g)];
     bool acc = true;
     float ratio_acc = 1.f;
     int sag_bad = 0;
@@ -519,7 +710,7 @@ __global__ void __launch_bounds__(kT2, 8) sample_kernel(const VerifyArgs a) {
         const float q = tok_t[lane] >= tht ? fast_exp2(fmaf(tok_t[lane], cc, -scaled_max(s.tm, cc))) / zt : 0.f;
         const float p = tok_d[lane] >= thd ? fast_exp2(fmaf(tok_d[lane], cc, -scaled_max(s.dm, cc))) / zd : 0.f;
         if (p > 0.f) ratio_acc = fminf(1.f, q / p);
-        acc = dr.accept < ratio_acc;
+        acc = uacc < ratio_acc;
       } else if constexpr (kSag) {
         // a = min(1, q(x)/p'(x)), p'(x) = sqrt(p(x) max(r(x), 1e-8)) / Zs
         if (tok_d[lane] != -INFINITY) {
@@ -534,7 +725,7 @@ __global__ void __launch_bounds__(kT2, 8) sample_kernel(const VerifyArgs a) {
           if (ps > 0.f) ratio_acc = fminf(1.f, q / ps);
           if (isnan(Sw) || !(zs > 0.f)) sag_bad = 1;  // the unit's Saguaro passes failed
         }
-        acc = dr.accept < ratio_acc;
+        acc = uacc < ratio_acc;
       } else {
         // a = min(1, q(x)/p(x)), the ratio as one exp2 of the exponent difference
         if (tok_d[lane] != -INFINITY) {
@@ -542,7 +733,7 @@ __global__ void __launch_bounds__(kT2, 8) sample_kernel(const VerifyArgs a) {
           const float ld = fmaf(tok_d[lane], cc, -scaled_max(s.dm, cc));
           ratio_acc = fminf(1.f, fast_exp2(lt - ld) * (s.ds / s.ts));
         }
-        acc = dr.accept < ratio_acc;
+        acc = uacc < ratio_acc;
       }
     }
     const unsigned rej = __ballot_sync(0xFFFFFFFFu, lane < g && !acc);
@@ -619,7 +810,7 @@ __global__ void __launch_bounds__(kT2, 8) sample_kernel(const VerifyArgs a) {
   } else if constexpr (!kTopP) {
     rw = ResidualW<E>{cc, mct, mcd, kr};
   }
-  const double ures = static_cast<double>(unit_draws(a.seed, a.req_base + b, pos).resample);
+  const float ures = sh_ures[pos];
   const E* trow = static_cast<const E*>(a.target) + (static_cast<size_t>(b) * W + pos) * V;
   const E* drow = residual ? static_cast<const E*>(a.draft) + (static_cast<size_t>(b) * a.gmax + pos) * V : nullptr;
   const bool aligned = geo.bulk != 0;
@@ -709,22 +900,21 @@ __device__ __forceinline__ MaxSum small_stats(const float (&x)[kSmallE], float c
 }
 
 // The element of a lane-blocked row (weights w) whose running weight first
-// exceeds u * sum (fp64 across lanes, fp32 within a lane), falling back to the
-// last element with positive weight; -1 if every weight is zero.
-__device__ __forceinline__ int small_draw(const float (&w)[kSmallE], int lo, double u) {
+// exceeds u * sum (float-float across lanes, fp32 within a lane), falling back
+// to the last element with positive weight; -1 if every weight is zero.
+__device__ __forceinline__ int small_draw(const float (&w)[kSmallE], int lo, float u) {
   const int lane = threadIdx.x & 31;
   float ls = 0.f;
 #pragma unroll
   for (int k = 0; k < kSmallE; ++k) ls += w[k];
-  double tot = static_cast<double>(ls);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xFFFFFFFFu, tot, o);
-  if (!(tot > 0.0)) return -1;
-  double before = 0.0;
-  const int L = lane_locate(static_cast<double>(ls), u * tot, &before);
+  const FF tot = ff_warp_sum(ls);
+  if (!(tot.hi > 0.f)) return -1;
+  const FF target = ff_mul(tot, u);
+  FF before;
+  const int L = lane_locate(ls, target, &before);
   int el = -1;
   if (lane == L) {
-    const float t = static_cast<float>(u * tot - before);
+    const float t = ff_float(ff_sub(target, before));
     float acc = 0.f;
     bool done = false;
 #pragma unroll
@@ -831,7 +1021,7 @@ __global__ void __launch_bounds__(256) small_verify_kernel(const VerifyArgs a) {
 #pragma unroll
       for (int k = 0; k < kSmallE; ++k)
         w[k] = fmaxf(fmaf(-kr, fast_exp2(fmaf(xd[k], c, -mcd)), fast_exp2(fmaf(xt[k], c, -mct))), 0.f);
-      const double ures = static_cast<double>(dr.resample);
+      const float ures = dr.resample;
       last = small_draw(w, lo, ures);
       if (last < 0) {
 #pragma unroll
@@ -847,7 +1037,7 @@ __global__ void __launch_bounds__(256) small_verify_kernel(const VerifyArgs a) {
       const float mct = scaled_max(st.m, c);
 #pragma unroll
       for (int k = 0; k < kSmallE; ++k) w[k] = fast_exp2(fmaf(xt[k], c, -mct));
-      last = small_draw(w, lo, static_cast<double>(unit_draws(a.seed, rid, g).resample));
+      last = small_draw(w, lo, unit_draws(a.seed, rid, g).resample);
     }
   }
   if (lane == 0) {
@@ -865,6 +1055,12 @@ template __global__ void small_verify_kernel<float>(const VerifyArgs);
 
 template __global__ void stream_kernel<uint16_t>(const VerifyArgs);
 template __global__ void stream_kernel<float>(const VerifyArgs);
+template __global__ void stream_reg_kernel<uint16_t, 4>(const VerifyArgs);
+template __global__ void stream_reg_kernel<float, 4>(const VerifyArgs);
+template __global__ void stream_reg_kernel<uint16_t, 6>(const VerifyArgs);
+template __global__ void stream_reg_kernel<float, 6>(const VerifyArgs);
+template __global__ void stream_reg_kernel<uint16_t, 8>(const VerifyArgs);
+template __global__ void stream_reg_kernel<float, 8>(const VerifyArgs);
 template __global__ void sample_kernel<uint16_t, kModePlain>(const VerifyArgs);
 template __global__ void sample_kernel<float, kModePlain>(const VerifyArgs);
 template __global__ void sample_kernel<uint16_t, kModeSag>(const VerifyArgs);
@@ -892,6 +1088,16 @@ cudaError_t launch_uniforms(uint64_t seed, int B, int W, float* out, cudaStream_
 
 namespace {
 
+// The register form takes aligned rows whose chunks hold at most kRegVecs
+// vectors per thread (SSDV_STREAM=staged selects the staged form).
+bool use_register_stream(const ChunkGeometry& geo, int vec) {
+  static const bool staged = [] {
+    const char* s = getenv("SSDV_STREAM");
+    return s && strcmp(s, "staged") == 0;
+  }();
+  return !staged && geo.bulk && geo.chunk <= kRegVecs * kThreads * vec;
+}
+
 // cudaFuncSetAttribute once per (kernel, size) on the current device.
 cudaError_t ensure_smem(const void* fn, int smem_bytes, int* cached) {
   if (*cached == smem_bytes) return cudaSuccess;
@@ -910,18 +1116,25 @@ cudaError_t launch_stream_t(const VerifyArgs& a, int smem_bytes, cudaStream_t st
     smem1 = -1;
     dev_cached = dev;
   }
-  e = ensure_smem(reinterpret_cast<const void*>(&stream_kernel<E>), smem_bytes, &smem1);
-  if (e != cudaSuccess) return e;
   cudaLaunchAttribute pdl[1];
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t c1 = {};
   c1.gridDim = dim3(a.geo.nchunk, a.B, a.gmax + 1);
   c1.blockDim = dim3(kThreads, 1, 1);
-  c1.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
   c1.stream = stream;
   c1.attrs = pdl;
   c1.numAttrs = 1;
+  if (use_register_stream(a.geo, Elem<E>::kVec)) {
+    c1.dynamicSmemBytes = 0;
+    const int per = (a.geo.chunk / Elem<E>::kVec + kThreads - 1) / kThreads;  // vectors per thread
+    if (per <= 4) return cudaLaunchKernelEx(&c1, stream_reg_kernel<E, 4>, a);
+    if (per <= 6) return cudaLaunchKernelEx(&c1, stream_reg_kernel<E, 6>, a);
+    return cudaLaunchKernelEx(&c1, stream_reg_kernel<E, 8>, a);
+  }
+  e = ensure_smem(reinterpret_cast<const void*>(&stream_kernel<E>), smem_bytes, &smem1);
+  if (e != cudaSuccess) return e;
+  c1.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
   return cudaLaunchKernelEx(&c1, stream_kernel<E>, a);
 }
 
