@@ -329,6 +329,19 @@ def secondary(ssdv, workloads, dev, stream):
         "frac_of_measured_hbm": by / ms_f / 1e6 / peak, "separate_calls_ms": ms + ms_v, "verify_alone_ms": ms_v}
     del sb
     torch.cuda.empty_cache()
+    # top-p verification on the bench workload (B=64, gamma 4, V 128256 bf16,
+    # T 0.8), nucleus 0.9 on both sides
+    pb = workloads.zipf_batch(64, 4, 128256, dtype=torch.bfloat16, temperature=0.8, seed=2,
+                              sigma_range=(0.3, 1.2), device=dev)
+    out = torch.empty(64, 5, dtype=torch.int32, device=dev)
+    n = torch.empty(64, dtype=torch.int32, device=dev)
+    ms = timeit(lambda: ssdv.verify_top_p(pb.target, pb.draft, pb.draft_tokens, 0.8, 0.9, 2, out, n,
+                                          stream=stream), 50)
+    by = pb.algorithmic_bytes()
+    res["top_p_0.9_B64_g4_V128256_bf16"] = {"ms_per_round": ms, "rounds_per_s": 1e3 / ms, "bytes": by,
+                                            "gbs": by / ms / 1e6, "frac_of_measured_hbm": by / ms / 1e6 / peak}
+    del pb
+    torch.cuda.empty_cache()
     # ragged mixed batch: B=512, gamma 1..8, V 128256 bf16, half greedy
     rb = workloads.ragged_batch(512, 8, 128256, seed=4, device=dev)
     out = torch.empty(512, 9, dtype=torch.int32, device=dev)

@@ -356,19 +356,6 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
   return r;
 }
 
-template <typename E>
-__device__ __forceinline__ float ld_logit(const E* p) {
-  if constexpr (sizeof(E) == 2) {
-    unsigned short h;
-    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(h) : "l"(p));
-    return Elem<E>::to_float(h);
-  } else {
-    float f;
-    asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(f) : "l"(p));
-    return f;
-  }
-}
-
 // Resident CTAs per SM the register form is built for (registers bound it).
 constexpr int reg_min_blocks(int nv) { return nv <= 4 ? 5 : nv <= 6 ? 4 : 3; }
 
@@ -411,15 +398,6 @@ __global__ void __launch_bounds__(kThreads, reg_min_blocks(kNV)) stream_reg_kern
   } else {
 #pragma unroll
     for (int k = 0; k < kNV; ++k) vd[k] = Elem<E>::max_init();
-  }
-  // the draft token's two logits, when it falls in this chunk
-  float xt_tok = 0.f, xd_tok = 0.f;
-  if (tid == 0 && has_draft && a.draft_tokens) {
-    const int x = a.draft_tokens[static_cast<size_t>(b) * a.gmax + i];
-    if (x >= lo && x < lo + nvec * kVec) {
-      xt_tok = ld_logit(rt_e + (x - lo));
-      xd_tok = ld_logit(rd_e + (x - lo));
-    }
   }
 
   const int warp = tid >> 5, lane = tid & 31;
@@ -513,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, reg_min_blocks(kNV)) stream_reg_kern
       d = combine_ms(d, MaxSum{red_f[2 * kWarps + w], red_f[3 * kWarps + w]}, cc);
     }
     rec[0] = make_float4(t.m, t.s, has_draft ? d.m : -INFINITY, d.s);
-    rec[1] = make_float4(xd_tok, 0.f, 0.f, xt_tok);
+    rec[1] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 }
 
@@ -634,6 +612,10 @@ __global__ void __launch_bounds__(kT2, 8) sample_kernel(const VerifyArgs a) {
       const int x = a.draft_tokens[static_cast<size_t>(b) * a.gmax + lane];
       bad = x < 0 || x >= V;
       tok_x[lane] = x;
+      if (!bad && !greedy) {  // the two logits of the accept test
+        tok_t[lane] = Elem<E>::to_float(static_cast<const E*>(a.target)[(static_cast<size_t>(b) * W + lane) * V + x]);
+        tok_d[lane] = Elem<E>::to_float(static_cast<const E*>(a.draft)[(static_cast<size_t>(b) * a.gmax + lane) * V + x]);
+      }
     }
     const unsigned anybad = __ballot_sync(0xFFFFFFFFu, bad);
     if (lane == 0) sh_bad = anybad != 0;
@@ -649,15 +631,8 @@ __global__ void __launch_bounds__(kT2, 8) sample_kernel(const VerifyArgs a) {
   griddep_wait();  // the streaming kernel's records are complete and visible
 
   // Row statistics of every position of the request, combined from the chunk
-  // records (the same butterfly in every CTA: identical results), and the two
-  // logits of each accept test from the record of the token's chunk.
+  // records (the same butterfly in every CTA: identical results).
   const float cc = greedy ? 1.f : kLog2e / T;
-  if (!greedy && warp == 0 && lane < g) {
-    const int cx = tok_x[lane] / geo.chunk;
-    const float4 r1 = __ldcg(a.part + ((static_cast<size_t>(b) * W + lane) * NC + cx) * 2 + 1);
-    tok_d[lane] = r1.x;
-    tok_t[lane] = r1.w;
-  }
   // A warp combines positions warp, warp + kW2, ..., two at a time: both
   // positions' records are loaded (one round), then combined.
   for (int u0 = warp; u0 <= g; u0 += 2 * kW2) {
