@@ -88,16 +88,17 @@ SagLayout saguaro_layout(int B, int g, int V) {
 
 // Top-p extension of the verification workspace: per row slot (B, gmax+1, 2)
 // the select state, the thresholds and kept masses, then every level's
-// histograms (fp32's 2048 + 2048 + 1024 bins, the most).
+// histograms (fp32's 256 + 2048 + 2048 + 1024 bins, the most).
 struct TopPLayout {
-  size_t prefix, above, goal, th, z, hist, total;
+  size_t prefix, bstar, above, goal, th, z, hist, total;
 };
-constexpr int kTopPBins = 2048 + 2048 + 1024;
+constexpr int kTopPBins = 256 + 2048 + 2048 + 1024;
 static TopPLayout topp_layout(int B, int gmax) {
   TopPLayout T;
   const size_t slots = static_cast<size_t>(B) * static_cast<size_t>(gmax + 1) * 2;
   T.prefix = round_up(workspace_layout(B, gmax).total, 256);
-  T.above = round_up(T.prefix + 4 * slots, 256);
+  T.bstar = T.prefix + 4 * slots;
+  T.above = round_up(T.bstar + 4 * slots, 256);
   T.goal = T.above + 8 * slots;
   T.th = T.goal + 8 * slots;
   T.z = T.th + 4 * slots;
@@ -224,9 +225,10 @@ ssd_status verify_common(const void* target, const void* draft, ssd_dtype dtype,
     // threshold, then the sampling kernel on the truncated distributions.
     const TopPLayout TL = topp_layout(B, gmax);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const int levels = es == 2 ? 2 : 3;
-    const int shifts[3] = {es == 2 ? 24 : 21, es == 2 ? 16 : 10, 0};
-    const int bits[3] = {es == 2 ? 8 : 11, es == 2 ? 8 : 11, 10};
+    // level 0: 256 mass bins; then the key digits inside the chosen bin
+    const int levels = es == 2 ? 3 : 4;
+    const int shifts[4] = {0, es == 2 ? 24 : 21, es == 2 ? 16 : 10, 0};
+    const int bits[4] = {8, es == 2 ? 8 : 11, es == 2 ? 8 : 11, 10};
     const size_t slots = static_cast<size_t>(B) * (gmax + 1) * 2;
     size_t hist_bytes = 0;
     for (int l = 0; l < levels; ++l) hist_bytes += slots * (static_cast<size_t>(8) << bits[l]);
@@ -250,6 +252,7 @@ ssd_status verify_common(const void* target, const void* draft, ssd_dtype dtype,
     t.geo = geo;
     t.nlevels = levels;
     t.prefix = reinterpret_cast<uint32_t*>(ws + TL.prefix);
+    t.bstar = reinterpret_cast<uint32_t*>(ws + TL.bstar);
     t.above = reinterpret_cast<unsigned long long*>(ws + TL.above);
     t.goal = reinterpret_cast<unsigned long long*>(ws + TL.goal);
     t.th = reinterpret_cast<float*>(ws + TL.th);

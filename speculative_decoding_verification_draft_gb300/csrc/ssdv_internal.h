@@ -88,7 +88,9 @@ struct SagArgs {
   ChunkGeometry geo;
 };
 
-// One level of the top-p radix select: digit = (key >> shift) & ((1 << bits) - 1).
+// One level of the top-p select.  Level 0: digit = 255 - (mass bin of the
+// element); later levels: digit = (key >> shift) & ((1 << bits) - 1) of the
+// elements in the chosen bin.
 struct TopPArgs {
   const void* target;   // [B, gmax+1, V]
   const void* draft;    // [B, gmax, V]
@@ -101,6 +103,7 @@ struct TopPArgs {
   ChunkGeometry geo;
   int level, nlevels, shift, bits;
   unsigned long long* hist;    // [B, gmax+1, 2, 1 << bits]: this level's histograms (zeroed by the caller)
+  uint32_t* bstar;             // [B, gmax+1, 2]: the mass bin holding the threshold (level 0's result)
   uint32_t* prefix;            // [B, gmax+1, 2]: the key digits fixed so far
   unsigned long long* above;   // [B, gmax+1, 2]: mass of keys above the prefix's range
   unsigned long long* goal;    // [B, gmax+1, 2]: ceil(top_p * total mass)

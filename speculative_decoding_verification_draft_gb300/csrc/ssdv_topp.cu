@@ -7,14 +7,18 @@
 // top_p of the row's probability mass (tokens tied with the last one needed
 // are kept), renormalised.
 //
-// th is found per row by a radix select over a monotone 32-bit key of the
-// logit, from the high digits down (bf16: two 8-bit digits of the 16 bits that
-// matter; fp32: digits of 11, 11 and 10 bits).  Each level is a histogram pass
-// over the rows' chunks -- the mass exp2(x c - fl(m c)) of every element whose
-// key matches the digits fixed so far, in fixed point (2^-40 units) so that
-// the integer sums are exact and the same on every run whatever the order of
-// the atomics -- then a select pass (one warp per row) that fixes the next
-// digit: the largest one whose upper mass reaches ceil(top_p * total).
+// th is found per row by a select over levels, each a histogram pass over the
+// rows' chunks followed by a select pass (one warp per row).  Level 0 bins
+// every element by its mass relative to the row maximum, an eighth of an
+// octave per bin (bin = floor(8 (fl(m c) - x c)), the last bin holding the
+// tail), which spreads a row's elements over many bins; the select fixes the
+// bin b* in which the mass counted from the top reaches ceil(top_p * total).
+// The later levels resolve th inside b* by a radix select over a monotone
+// 32-bit key of the logit, high digits first (bf16: two 8-bit digits of the
+// 16 bits that matter; fp32: digits of 11, 11 and 10 bits), counting only the
+// elements of b*.  Masses exp2(x c - fl(m c)) are summed in fixed point (2^-40
+// units), so the integer sums are exact and the same on every run whatever
+// the order of the atomics.
 #include "ssdv_device.cuh"
 
 namespace ssdv {
@@ -35,6 +39,14 @@ __device__ __forceinline__ float key_logit(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
+// round(e * 2^40) for 0 <= e < 2, from two 32-bit conversions
+__device__ __forceinline__ unsigned long long mass_fixed(float e) {
+  const float f = e * 256.f;
+  const uint32_t hi = __float2uint_rz(f);
+  const float r = f - __uint2float_rz(hi);  // exact
+  return (static_cast<unsigned long long>(hi) << 32) + __float2uint_rn(r * 4294967296.f);
+}
+
 // Row slot rs = (b * W + i) * 2 + which (0 target, 1 draft): whether it is a
 // row of a sampled request that verification reads.
 __device__ __forceinline__ bool slot_active(const TopPArgs& a, int b, int i, int which, float* T_out) {
@@ -51,7 +63,11 @@ __device__ __forceinline__ bool slot_active(const TopPArgs& a, int b, int i, int
 // (i, which), request).
 template <typename E>
 __global__ void __launch_bounds__(kHistThreads) topp_hist_kernel(const TopPArgs a) {
-  extern __shared__ __align__(16) unsigned long long s_hist[];
+  // each bin's 64-bit mass as two 32-bit words (native shared atomics): the
+  // low word, and the high word with the carries out of the low one
+  // [copies][2][nb]: low words, high words; level 0 (every element counts)
+  // gives each warp a copy of its own, the later levels share one
+  extern __shared__ __align__(16) uint32_t s_hist[];
   __shared__ float sh_m;
   griddep_launch_dependents();
   const int W = a.gmax + 1, NC = a.geo.nchunk, V = a.geo.V;
@@ -59,7 +75,27 @@ __global__ void __launch_bounds__(kHistThreads) topp_hist_kernel(const TopPArgs 
   float T;
   if (!slot_active(a, b, i, which, &T)) return;
   const int nb = 1 << a.bits;
-  for (int d = threadIdx.x; d < nb; d += kHistThreads) s_hist[d] = 0ull;
+  const int copies = a.level == 0 ? kHistThreads / 32 : 1;
+  for (int d = threadIdx.x; d < 2 * nb * copies; d += kHistThreads) s_hist[d] = 0u;
+  uint32_t* my_hist = s_hist + (copies > 1 ? (threadIdx.x >> 5) * 2 * nb : 0);
+  // The chunk's logits are inputs, complete before the call's first kernel:
+  // their loads go out before the wait, all of a thread's at once.
+  constexpr int kVec = Elem<E>::kVec, kNV = 6;
+  const E* row = which ? static_cast<const E*>(a.draft) + (static_cast<size_t>(b) * a.gmax + i) * V
+                       : static_cast<const E*>(a.target) + (static_cast<size_t>(b) * W + i) * V;
+  const int lo = c * a.geo.chunk;
+  const int n = min(a.geo.chunk, V - lo);
+  const int nvec = n / kVec;  // aligned rows: whole vectors
+  const bool batched = a.geo.bulk && nvec <= kNV * kHistThreads;
+  uint4 r[kNV];
+  if (batched) {
+    const uint4* rv = reinterpret_cast<const uint4*>(row + lo);
+#pragma unroll
+    for (int k = 0; k < kNV; ++k) {
+      const int v = threadIdx.x + k * kHistThreads;
+      r[k] = v < nvec ? __ldg(rv + v) : Elem<E>::max_init();
+    }
+  }
   griddep_wait();  // the records (and the previous level's digits) are complete and visible
   const size_t rs = (static_cast<size_t>(b) * W + i) * 2 + which;
   if (threadIdx.x < 32) {
@@ -75,51 +111,111 @@ __global__ void __launch_bounds__(kHistThreads) topp_hist_kernel(const TopPArgs 
   }
   __syncthreads();
   const float cc = kLog2e / T;
-  const float nmc = -scaled_max(sh_m, cc);
-  const uint32_t prefix = a.level ? __ldcg(a.prefix + rs) : 0u;
-  const int hi_shift = a.shift + a.bits;  // bits above this level's digit: all decided
-  const E* row = which ? static_cast<const E*>(a.draft) + (static_cast<size_t>(b) * a.gmax + i) * V
-                       : static_cast<const E*>(a.target) + (static_cast<size_t>(b) * W + i) * V;
-  const int lo = c * a.geo.chunk;
-  const int n = min(a.geo.chunk, V - lo);
-  for (int e = threadIdx.x; e < n; e += kHistThreads) {
-    const float x = Elem<E>::to_float(row[lo + e]);
-    if (x == -INFINITY) continue;  // no mass
-    const uint32_t k = logit_key(x);
-    if (hi_shift < 32 && (k >> hi_shift) != prefix) continue;
-    const unsigned long long mass = __float2ull_rn(fast_exp2(fmaf(x, cc, nmc)) * kFix);
-    if (mass) atomicAdd(&s_hist[(k >> a.shift) & (nb - 1)], mass);
+  const float mc = scaled_max(sh_m, cc);
+  const bool bin_level = a.level == 0;
+  const uint32_t bstar = bin_level ? 0u : __ldcg(a.bstar + rs);
+  const uint32_t prefix = a.level >= 2 ? __ldcg(a.prefix + rs) : 0u;
+  const int hi_shift = a.shift + a.bits;  // key bits above this level's digit (levels >= 2: all decided)
+  // Levels >= 1: the logits whose bin can be b* lie in [xlo, xhi], the bin's
+  // edges d = b*/8 and (b*+1)/8 turned into logits and widened well past the
+  // rounding of d; everything outside is rejected by two compares, and the
+  // few candidates take the exact bin test.
+  float xlo = -INFINITY, xhi = INFINITY;
+  if (!bin_level) {
+    const float pad = (fabsf(mc / cc) + 1.f) * 1e-5f;
+    if (bstar > 0u) xhi = (mc - static_cast<float>(bstar) * 0.125f) / cc + pad;
+    if (bstar < 255u) xlo = (mc - static_cast<float>(bstar + 1u) * 0.125f) / cc - pad;
+  }
+  auto count = [&](float x) {
+    if (x == -INFINITY || x < xlo || x > xhi) return;  // no mass, or certainly another bin
+    const float d = __fmaf_rn(-x, cc, mc);  // fl(m c) - x c, one rounding
+    const int bin = min(255, max(0, __float2int_rd(d * 8.f)));
+    int digit;
+    if (bin_level) {
+      digit = 255 - bin;  // larger digit, larger mass
+    } else {
+      if (static_cast<uint32_t>(bin) != bstar) return;
+      const uint32_t k = logit_key(x);
+      if (a.level >= 2 && (k >> hi_shift) != prefix) return;
+      digit = static_cast<int>((k >> a.shift) & static_cast<uint32_t>(nb - 1));
+    }
+    const unsigned long long mass = mass_fixed(fast_exp2(-d));
+    const uint32_t lo32 = static_cast<uint32_t>(mass), hi32 = static_cast<uint32_t>(mass >> 32);
+    const uint32_t old = lo32 ? atomicAdd(&my_hist[digit], lo32) : 0u;
+    const uint32_t hi_add = hi32 + (old + lo32 < old ? 1u : 0u);  // the carry out of the low word
+    if (hi_add) atomicAdd(&my_hist[nb + digit], hi_add);
+  };
+  if (batched) {
+#pragma unroll
+    for (int k = 0; k < kNV; ++k) {
+      float f[kVec];
+      Elem<E>::unpack(r[k], f);
+#pragma unroll
+      for (int e = 0; e < kVec; ++e) count(f[e]);
+    }
+  } else if (a.geo.bulk) {
+    const uint4* rv = reinterpret_cast<const uint4*>(row + lo);
+    for (int v = threadIdx.x; v < nvec; v += kHistThreads) {
+      float f[kVec];
+      Elem<E>::unpack(__ldg(rv + v), f);
+#pragma unroll
+      for (int e = 0; e < kVec; ++e) count(f[e]);
+    }
+  } else {
+    for (int e = threadIdx.x; e < n; e += kHistThreads) count(Elem<E>::to_float(row[lo + e]));
   }
   __syncthreads();
   unsigned long long* h = a.hist + rs * nb;
-  for (int d = threadIdx.x; d < nb; d += kHistThreads)
-    if (s_hist[d]) atomicAdd(&h[d], s_hist[d]);
+  for (int d = threadIdx.x; d < nb; d += kHistThreads) {
+    unsigned long long m = 0ull;
+    for (int q = 0; q < copies; ++q)
+      m += (static_cast<unsigned long long>(s_hist[q * 2 * nb + nb + d]) << 32) + s_hist[q * 2 * nb + d];
+    if (m) atomicAdd(&h[d], m);
+  }
 }
 
-// Select of one level: one warp per row slot fixes the next digit.  At the
-// last level it writes the threshold logit and the kept mass.
+// Select of one level: one CTA per row slot fixes the next digit.  Thread t
+// holds bins [t * per, t * per + per), per = bins / 256; a block suffix scan
+// of the bin masses (the mass at or above each thread's first bin) finds the
+// last thread whose suffix, with the mass above the level's range, reaches the
+// goal, and that thread finds the digit among its bins.  At the last level it
+// writes the threshold logit and the kept mass.
 __global__ void __launch_bounds__(256) topp_select_kernel(const TopPArgs a) {
+  __shared__ unsigned long long s_w[8];
   griddep_launch_dependents();
   const int W = a.gmax + 1;
-  const int lane = threadIdx.x & 31;
-  const size_t rs = static_cast<size_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  const size_t nslots = static_cast<size_t>(a.B) * W * 2;
-  if (rs >= nslots) return;
+  const size_t rs = blockIdx.x;
   const int b = static_cast<int>(rs / (2 * W)), i = static_cast<int>((rs / 2) % W), which = static_cast<int>(rs & 1);
   float T;
-  if (!slot_active(a, b, i, which, &T)) return;
+  if (!slot_active(a, b, i, which, &T)) return;  // uniform over the CTA
   griddep_wait();  // the level's histograms are complete and visible
-  const int nb = 1 << a.bits, per = nb / 32;
-  const unsigned long long* h = a.hist + rs * nb;
-  // lane L holds bins [L * per, L * per + per)
-  unsigned long long ls = 0ull;
-  for (int k = 0; k < per; ++k) ls += __ldcg(h + lane * per + k);
-  unsigned long long above = a.level ? __ldcg(a.above + rs) : 0ull;
+  const int nb = 1 << a.bits, per = nb >> 8;  // 1, 4 or 8
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const unsigned long long* h = a.hist + rs * nb + static_cast<size_t>(t) * per;
+  unsigned long long v[8], ls = 0ull;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    v[k] = k < per ? __ldcg(h + k) : 0ull;
+    ls += v[k];
+  }
+  // suffix sums: within the warp, then the later warps' totals
+  unsigned long long suf = ls;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long x = __shfl_down_sync(0xFFFFFFFFu, suf, o);
+    if (lane + o < 32) suf += x;
+  }
+  if (lane == 0) s_w[warp] = suf;
+  __syncthreads();
+  unsigned long long tot = 0ull;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    tot += s_w[w];
+    if (w > warp) suf += s_w[w];
+  }
+  const unsigned long long above = a.level ? __ldcg(a.above + rs) : 0ull;
   unsigned long long goal;
   if (a.level == 0) {
-    unsigned long long tot = ls;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xFFFFFFFFu, tot, o);
     goal = static_cast<unsigned long long>(ceil(static_cast<double>(a.top_p) * static_cast<double>(tot)));
     // the product rounds in fp64 (tot may exceed 2^53): keep 1 <= goal <= tot
     goal = goal < tot ? goal : tot;
@@ -127,47 +223,45 @@ __global__ void __launch_bounds__(256) topp_select_kernel(const TopPArgs a) {
   } else {
     goal = __ldcg(a.goal + rs);
   }
-  // suffix sums over lanes: the mass of bins at or above lane L's first bin
-  unsigned long long suf = ls;
+  // the suffix does not grow with t, so the threads that reach the goal are
+  // 0 .. t*: their count locates t*
+  const int tstar = max(0, __syncthreads_count(above + suf >= goal) - 1);
+  if (t != tstar) return;
+  // within the thread, from its top bin down
+  unsigned long long cum = above + suf - ls;
+  int d = t * per;
+  unsigned long long dmass = v[0];
+  bool found = false;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const unsigned long long t = __shfl_down_sync(0xFFFFFFFFu, suf, o);
-    if (lane + o < 32) suf += t;
-  }
-  // the highest lane whose suffix (with the mass above the prefix range)
-  // reaches the target holds the digit
-  const unsigned hitm = __ballot_sync(0xFFFFFFFFu, above + suf >= goal);
-  const int L = hitm ? 31 - __clz(hitm) : 0;
-  const unsigned long long above_lane = above + __shfl_sync(0xFFFFFFFFu, suf - ls, L);
-  if (lane == L) {
-    // within the lane, from its top bin down
-    unsigned long long cum = above_lane;
-    int d = lane * per;
-    unsigned long long dmass = 0ull;
-    for (int k = per - 1; k >= 0; --k) {
-      const unsigned long long m = __ldcg(h + lane * per + k);
-      if (cum + m >= goal || k == 0) {
-        d = lane * per + k;
-        dmass = m;
-        break;
+  for (int k = 7; k >= 0; --k) {
+    if (k < per && !found) {
+      if (cum + v[k] >= goal || k == 0) {
+        d = t * per + k;
+        dmass = v[k];
+        found = true;
+      } else {
+        cum += v[k];
       }
-      cum += m;
     }
-    const uint32_t prefix = a.level ? __ldcg(a.prefix + rs) : 0u;
-    const uint32_t np = (prefix << a.bits) | static_cast<uint32_t>(d);
-    if (a.level + 1 < a.nlevels) {
-      a.prefix[rs] = np;
-      a.above[rs] = cum;
-      a.goal[rs] = goal;
-    } else {
-      // the key's undecided low bits (bf16: the 16 that a bf16 logit lacks)
-      // are those of the smallest logit with these digits, so th is that
-      // logit exactly
-      uint32_t k = np << a.shift;
-      if (a.shift && !(k & 0x80000000u)) k |= (1u << a.shift) - 1u;
-      a.th[rs] = key_logit(k);
-      a.z[rs] = static_cast<float>(static_cast<double>(cum + dmass) * (1.0 / 1099511627776.0));
-    }
+  }
+  const uint32_t prefix = a.level >= 2 ? __ldcg(a.prefix + rs) : 0u;
+  const uint32_t np = (prefix << a.bits) | static_cast<uint32_t>(d);
+  if (a.level == 0) {
+    a.bstar[rs] = 255u - static_cast<uint32_t>(d);
+    a.above[rs] = cum;
+    a.goal[rs] = goal;
+  } else if (a.level + 1 < a.nlevels) {
+    a.prefix[rs] = np;
+    a.above[rs] = cum;
+    a.goal[rs] = goal;
+  } else {
+    // the key's undecided low bits (bf16: the 16 that a bf16 logit lacks)
+    // are those of the smallest logit with these digits, so th is that
+    // logit exactly
+    uint32_t k = np << a.shift;
+    if (a.shift && !(k & 0x80000000u)) k |= (1u << a.shift) - 1u;
+    a.th[rs] = key_logit(k);
+    a.z[rs] = static_cast<float>(static_cast<double>(cum + dmass) * (1.0 / 1099511627776.0));
   }
 }
 
@@ -181,7 +275,8 @@ cudaError_t launch_topp_level(const TopPArgs& a, int esize, cudaStream_t stream)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.geo.nchunk, 2 * (a.gmax + 1), a.B);
   cfg.blockDim = dim3(kHistThreads, 1, 1);
-  cfg.dynamicSmemBytes = static_cast<size_t>(8) << a.bits;
+  // two 32-bit words per bin; level 0: one histogram per warp
+  cfg.dynamicSmemBytes = (static_cast<size_t>(8) << a.bits) * (a.level == 0 ? kHistThreads / 32 : 1);
   cfg.stream = stream;
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
@@ -189,7 +284,7 @@ cudaError_t launch_topp_level(const TopPArgs& a, int esize, cudaStream_t stream)
                              : cudaLaunchKernelEx(&cfg, topp_hist_kernel<float>, a);
   if (e != cudaSuccess) return e;
   const size_t nslots = static_cast<size_t>(a.B) * (a.gmax + 1) * 2;
-  cfg.gridDim = dim3(static_cast<unsigned>((nslots + 7) / 8), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(nslots), 1, 1);
   cfg.blockDim = dim3(256, 1, 1);
   cfg.dynamicSmemBytes = 0;
   return cudaLaunchKernelEx(&cfg, topp_select_kernel, a);
