@@ -491,7 +491,7 @@ def main():
         "hbm_gbs": alg / (step_ms * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "peak_kind": peak_kind,
-                     "kernel": "stream_kernel<bf16> + sample_kernel<bf16> (one call)",
+                     "kernel": "stream_reg_kernel<bf16, 6> + sample_kernel<bf16> (one call)",
                      "algorithmic_bytes_per_launch": alg, "us_per_call": step_ms * 1e3,
                      "calls": "ssd_verify_pipelined, back to back",
                      "plain_us_per_call": r["plain_ms"] * 1e3,
