@@ -9,21 +9,23 @@
 // the target argmax.
 //
 // Two kernels on the caller's stream:
-//  1. stream_kernel: one CTA per (request, position, vocabulary chunk) stages
-//     the target chunk (and the draft chunk of a sampled draft position) into
-//     shared memory with bulk async copies and reduces both in one pass to a
-//     32-byte record (max and sum of exponentials of each row, the target
-//     argmax of a greedy row, and the draft token's two logits when the token
-//     falls in the chunk).
-//     Every logit is read from HBM exactly once, by short-lived CTAs.
-//  2. sample_kernel: small CTAs, each covering four pieces (128 vectors
-//     each) of one request's draw row.  Every CTA combines the request's
-//     records, takes every accept decision and finds the first rejection n;
-//     then each warp loads its piece of row n (L2-resident: the streaming
-//     kernel reads the low positions last) in one round of loads -- target and
-//     draft for a residual draw, target for the bonus draw -- and publishes the
-//     piece's weight sum.  The last warp to arrive sums the pieces in order,
-//     finds the piece holding u * S, reloads that piece and scans it.
+//  1. The streaming kernel: one CTA per (request, position, vocabulary chunk)
+//     reduces the target chunk (and the draft chunk of a sampled draft
+//     position) to a 32-byte record: max and sum of exponentials of each row,
+//     or the target argmax of a greedy row.  Rows whose starts are 16-byte
+//     aligned take the register form (stream_reg_kernel: every thread's
+//     16-byte loads issued at once); other rows are staged into shared memory
+//     (stream_kernel).  Every logit is read from HBM exactly once, by
+//     short-lived CTAs.
+//  2. sample_kernel: small CTAs, each covering a few pieces (128 vectors
+//     each) of one request's draw row.  Before waiting for the records it
+//     reads the draft tokens, their two logits and the uniforms (inputs).
+//     Every CTA combines the request's records, takes every accept decision
+//     and finds the first rejection n; then each warp loads its pieces of row
+//     n (L2-resident: the streaming kernel reads the low positions last) --
+//     target and draft for a residual draw, target for the bonus draw -- and
+//     publishes their weight sums.  The last warp to arrive sums the pieces in
+//     order, finds the piece holding u * S, reloads that piece and scans it.
 //
 // A call runs as segments of requests, each a streaming + sampling pair, all
 // launched with programmatic dependent launch.  The first streaming kernel's
@@ -220,10 +222,6 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const VerifyArgs a) {
   sl.gd = has_draft ? static_cast<const E*>(a.draft) + (static_cast<size_t>(b) * a.gmax + i) * V + lo : nullptr;
   sl.st = reinterpret_cast<E*>(dyn_smem);
   sl.sd = reinterpret_cast<E*>(dyn_smem + geo.row_smem);
-  // the draft token of this position: if it falls in this chunk, the record
-  // carries its two logits for the accept test
-  const int x =
-      (has_draft && tid == 0 && a.draft_tokens) ? a.draft_tokens[static_cast<size_t>(b) * a.gmax + i] : -1;
   const bool ok = stage_chunk(sl, &bar, &sh_ok);
   const uint4* vt = reinterpret_cast<const uint4*>(sl.st);
   const uint4* vd = reinterpret_cast<const uint4*>(sl.sd);
@@ -326,12 +324,7 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const VerifyArgs a) {
       s1 += red_f[3 * kWarps + w];
     }
     rec[0] = make_float4(mt, s0, has_draft ? md : -INFINITY, s1);
-    float xt_tok = 0.f, xd_tok = 0.f;
-    if (x >= lo && x < lo + sl.n) {
-      xt_tok = Elem<E>::to_float(sl.st[x - lo]);
-      xd_tok = Elem<E>::to_float(sl.sd[x - lo]);
-    }
-    rec[1] = make_float4(xd_tok, 0.f, __int_as_float(ok ? 0 : 1), xt_tok);
+    rec[1] = make_float4(0.f, 0.f, __int_as_float(ok ? 0 : 1), 0.f);
   }
 }
 
