@@ -530,7 +530,7 @@ constexpr int kW2 = kT2 / 32;
 // writes request b's outputs (tok_x: its first n draft tokens) and, with
 // statistics, the CDF edges of the drawn token.
 template <typename E, typename WFun>
-__device__ __noinline__ void warp_draw_row(const VerifyArgs& a, int b, int n, size_t pi_idx, const RowPieces& rp,
+__device__ __forceinline__ void warp_draw_row(const VerifyArgs& a, int b, int n, size_t pi_idx, const RowPieces& rp,
                                            float ures, const E* trow, const E* drow, bool aligned, const WFun& wfun,
                                            const int* tok_x) {
   const int lane = threadIdx.x & 31;
