@@ -325,3 +325,29 @@ def test_small_vocab_ragged_and_greedy(ssdv):
     ref = gc.verify_oracle(batch, 21)
     gc.assert_verify_parity(out.cpu().numpy(), n.cpu().numpy(), ref, 200, "one-warp ragged")
     assert ssdv.read_status() == 0
+
+
+def test_graph_replay_matches_eager_calls(ssdv):
+    """Two plain calls on one workspace, captured in a CUDA graph and replayed,
+    give the outputs of the same calls made eagerly."""
+    b = wl.zipf_batch(8, 4, 20000, dtype=torch.bfloat16, temperature=0.8, seed=12, sigma_range=(0.3, 1.2)).to("cuda")
+    ws = ssdv.make_workspace(8, 4, "cuda")
+    outs = [(torch.empty(8, 5, dtype=torch.int32, device="cuda"), torch.empty(8, dtype=torch.int32, device="cuda"))
+            for _ in range(2)]
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        ssdv.verify(b.target, b.draft, b.draft_tokens, 0.8, 3, outs[0][0], outs[0][1], ws, stream=s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        for k, (out, n) in enumerate(outs):
+            ssdv.verify(b.target, b.draft, b.draft_tokens, 0.8, 3 + k, out, n, ws, stream=s)
+    for out, n in outs:
+        out.fill_(-7)
+        n.fill_(-7)
+    graph.replay()
+    torch.cuda.synchronize()
+    for k, (out, n) in enumerate(outs):
+        e_out, e_n = ssdv.verify(b.target, b.draft, b.draft_tokens, 0.8, 3 + k)
+        torch.cuda.synchronize()
+        assert torch.equal(out, e_out) and torch.equal(n, e_n)
