@@ -127,8 +127,10 @@ ssd_status ssd_verify(const void* target_logits, const void* draft_logits, ssd_d
  * from q'_gamma.  temperature == 0 (greedy) or top_p == 1 is ssd_verify.
  *   0 < top_p <= 1; B <= 65535.
  *   workspace >= ssd_verify_top_p_workspace_bytes(B, gamma) bytes, zeroed once.
- * Kernels: the streaming pass, then per radix level (2 for bf16, 3 for fp32)
- * a histogram pass over the rows and a select pass, then the sampling kernel. */
+ * Kernels: the streaming pass; then per level of the threshold select (3 for
+ * bf16, 4 for fp32: one of mass bins, then the logit key's digits inside the
+ * chosen bin) a histogram pass over the rows and a select pass; then the
+ * sampling kernel. */
 ssd_status ssd_verify_top_p(const void* target_logits, const void* draft_logits, ssd_dtype dtype,
                             const int32_t* draft_tokens, int B, int gamma, int V, float temperature,
                             float top_p, uint64_t seed, int32_t* out_tokens, int32_t* n_accepted,
