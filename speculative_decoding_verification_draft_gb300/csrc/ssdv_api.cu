@@ -188,11 +188,21 @@ ssd_status verify_common(const void* target, const void* draft, ssd_dtype dtype,
   if (st != SSD_OK) return st;
   const long long ctas = static_cast<long long>(B) * (gmax + 1) * geo.nchunk;
   if (ctas >= (1LL << 31)) return fail(SSD_ERR_SHAPE, "grid too large");
-  // Pieces per warp of the sampling kernel: two (one wave of small CTAs, the
-  // shortest chain) for a plain call; for a pipelined call enough that the
-  // sampling grid becomes resident while the streaming kernel still runs, so
-  // the next call's streaming kernel can launch early (SSDV_PPW overrides).
-  geo.ppw = env_int("SSDV_PPW", pipelined ? 4 : 2);
+  // Pieces per warp of the sampling kernel (SSDV_PPW overrides).  A plain
+  // call takes one piece per warp (one round of loads) when the sampling grid
+  // then still fits in one wave of 8 small CTAs per SM, else two.  A pipelined
+  // call takes four, so that the sampling grid becomes resident while the
+  // streaming kernel still runs and the next call's streaming kernel can
+  // launch early.
+  int ppw_default = pipelined ? 4 : 2;
+  if (!pipelined) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+        static_cast<long long>(B) * ((geo.npiece + 3) / 4) <= 8LL * sms)
+      ppw_default = 1;
+  }
+  geo.ppw = env_int("SSDV_PPW", ppw_default);
   if (geo.ppw < 1) geo.ppw = 1;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   VerifyArgs a;
