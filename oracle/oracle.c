@@ -617,7 +617,7 @@ int orc_saguaro_request(int g, int V, const double* xt, const double* xd, double
       for (int v = 0; v < V; ++v) r[v] = q[v];
       pD = q;
     }
-    /* Bonus prediction: top-k of the residual (one more, to judge ambiguity),
+    /* Bonus prediction: top-k of the residual (one more, to detect a near-tie at the k-th slot),
        or of the draft's (target's, at j = g) logits, then reported as
        probabilities of that row. */
     int kk = k + 1 <= V ? k + 1 : V;
