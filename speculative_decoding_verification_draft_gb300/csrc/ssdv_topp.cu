@@ -25,7 +25,6 @@ namespace ssdv {
 
 namespace {
 
-constexpr float kFix = 1099511627776.0f;  // 2^40
 constexpr int kHistThreads = 256;
 
 __device__ __forceinline__ bool temperature_ok_tp(float T) { return T == 0.f || (T >= 1e-6f && T <= 3.0e38f); }
@@ -59,119 +58,189 @@ __device__ __forceinline__ bool slot_active(const TopPArgs& a, int b, int i, int
 
 }  // namespace
 
-// Histogram of one level over one chunk of one row.  Grid (chunk, row slot
-// (i, which), request).
-template <typename E>
-__global__ void __launch_bounds__(kHistThreads) topp_hist_kernel(const TopPArgs a) {
-  // each bin's 64-bit mass as two 32-bit words (native shared atomics): the
-  // low word, and the high word with the carries out of the low one
-  // [copies][2][nb]: low words, high words; level 0 (every element counts)
-  // gives each warp a copy of its own, the later levels share one
-  extern __shared__ __align__(16) uint32_t s_hist[];
-  __shared__ float sh_m;
-  griddep_launch_dependents();
-  const int W = a.gmax + 1, NC = a.geo.nchunk, V = a.geo.V;
-  const int c = blockIdx.x, i = blockIdx.y >> 1, which = blockIdx.y & 1, b = blockIdx.z;
-  float T;
-  if (!slot_active(a, b, i, which, &T)) return;
-  const int nb = 1 << a.bits;
-  const int copies = a.level == 0 ? kHistThreads / 32 : 1;
-  for (int d = threadIdx.x; d < 2 * nb * copies; d += kHistThreads) s_hist[d] = 0u;
-  uint32_t* my_hist = s_hist + (copies > 1 ? (threadIdx.x >> 5) * 2 * nb : 0);
-  // The chunk's logits are inputs, complete before the call's first kernel:
-  // their loads go out before the wait, all of a thread's at once.
-  constexpr int kVec = Elem<E>::kVec, kNV = 6;
-  const E* row = which ? static_cast<const E*>(a.draft) + (static_cast<size_t>(b) * a.gmax + i) * V
-                       : static_cast<const E*>(a.target) + (static_cast<size_t>(b) * W + i) * V;
-  const int lo = c * a.geo.chunk;
-  const int n = min(a.geo.chunk, V - lo);
+namespace {
+
+// The row maximum from the row's chunk records (every lane of the calling
+// warp gets it): the largest chunk maximum.
+__device__ __forceinline__ float row_max_warp(const TopPArgs& a, int b, int i, int which) {
+  const int lane = threadIdx.x & 31, NC = a.geo.nchunk, W = a.gmax + 1;
+  float m = -INFINITY;
+  for (int q = lane; q < NC; q += 32) {
+    const float4 r0 = __ldcg(a.part + ((static_cast<size_t>(b) * W + i) * NC + q) * 2);
+    m = fmaxf(m, which ? r0.z : r0.x);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  return m;
+}
+
+constexpr int kNVH = 6;  // 16-byte vectors per thread loaded at once
+
+// One chunk of one row: its elements' logits handed to f, the aligned case
+// from loads issued (all of a thread's at once) before the wait for the
+// previous kernel, since the logits are inputs complete before the call.
+template <typename E, typename F>
+__device__ __forceinline__ void for_chunk(const TopPArgs& a, const E* row, int lo, int n, F&& f) {
+  constexpr int kVec = Elem<E>::kVec;
   const int nvec = n / kVec;  // aligned rows: whole vectors
-  const bool batched = a.geo.bulk && nvec <= kNV * kHistThreads;
-  uint4 r[kNV];
+  const bool batched = a.geo.bulk && nvec <= kNVH * kHistThreads;
+  uint4 r[kNVH];
   if (batched) {
     const uint4* rv = reinterpret_cast<const uint4*>(row + lo);
 #pragma unroll
-    for (int k = 0; k < kNV; ++k) {
+    for (int k = 0; k < kNVH; ++k) {
       const int v = threadIdx.x + k * kHistThreads;
       r[k] = v < nvec ? __ldg(rv + v) : Elem<E>::max_init();
     }
   }
   griddep_wait();  // the records (and the previous level's digits) are complete and visible
-  const size_t rs = (static_cast<size_t>(b) * W + i) * 2 + which;
-  if (threadIdx.x < 32) {
-    // the row maximum: the largest chunk maximum of the row's records
-    float m = -INFINITY;
-    for (int q = threadIdx.x; q < NC; q += 32) {
-      const float4 r0 = __ldcg(a.part + ((static_cast<size_t>(b) * W + i) * NC + q) * 2);
-      m = fmaxf(m, which ? r0.z : r0.x);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-    if (threadIdx.x == 0) sh_m = m;
-  }
-  __syncthreads();
-  const float cc = kLog2e / T;
-  const float mc = scaled_max(sh_m, cc);
-  const bool bin_level = a.level == 0;
-  const uint32_t bstar = bin_level ? 0u : __ldcg(a.bstar + rs);
-  const uint32_t prefix = a.level >= 2 ? __ldcg(a.prefix + rs) : 0u;
-  const int hi_shift = a.shift + a.bits;  // key bits above this level's digit (levels >= 2: all decided)
-  // Levels >= 1: the logits whose bin can be b* lie in [xlo, xhi], the bin's
-  // edges d = b*/8 and (b*+1)/8 turned into logits and widened well past the
-  // rounding of d; everything outside is rejected by two compares, and the
-  // few candidates take the exact bin test.
-  float xlo = -INFINITY, xhi = INFINITY;
-  if (!bin_level) {
-    const float pad = (fabsf(mc / cc) + 1.f) * 1e-5f;
-    if (bstar > 0u) xhi = (mc - static_cast<float>(bstar) * 0.125f) / cc + pad;
-    if (bstar < 255u) xlo = (mc - static_cast<float>(bstar + 1u) * 0.125f) / cc - pad;
-  }
-  auto count = [&](float x) {
-    if (x == -INFINITY || x < xlo || x > xhi) return;  // no mass, or certainly another bin
-    const float d = __fmaf_rn(-x, cc, mc);  // fl(m c) - x c, one rounding
-    const int bin = min(255, max(0, __float2int_rd(d * 8.f)));
-    int digit;
-    if (bin_level) {
-      digit = 255 - bin;  // larger digit, larger mass
-    } else {
-      if (static_cast<uint32_t>(bin) != bstar) return;
-      const uint32_t k = logit_key(x);
-      if (a.level >= 2 && (k >> hi_shift) != prefix) return;
-      digit = static_cast<int>((k >> a.shift) & static_cast<uint32_t>(nb - 1));
-    }
-    const unsigned long long mass = mass_fixed(fast_exp2(-d));
-    const uint32_t lo32 = static_cast<uint32_t>(mass), hi32 = static_cast<uint32_t>(mass >> 32);
-    const uint32_t old = lo32 ? atomicAdd(&my_hist[digit], lo32) : 0u;
-    const uint32_t hi_add = hi32 + (old + lo32 < old ? 1u : 0u);  // the carry out of the low word
-    if (hi_add) atomicAdd(&my_hist[nb + digit], hi_add);
-  };
+  f.begin();
   if (batched) {
 #pragma unroll
-    for (int k = 0; k < kNV; ++k) {
-      float f[kVec];
-      Elem<E>::unpack(r[k], f);
+    for (int k = 0; k < kNVH; ++k) {
+      float x[kVec];
+      Elem<E>::unpack(r[k], x);
 #pragma unroll
-      for (int e = 0; e < kVec; ++e) count(f[e]);
+      for (int e = 0; e < kVec; ++e) f(x[e]);
     }
   } else if (a.geo.bulk) {
     const uint4* rv = reinterpret_cast<const uint4*>(row + lo);
     for (int v = threadIdx.x; v < nvec; v += kHistThreads) {
-      float f[kVec];
-      Elem<E>::unpack(__ldg(rv + v), f);
+      float x[kVec];
+      Elem<E>::unpack(__ldg(rv + v), x);
 #pragma unroll
-      for (int e = 0; e < kVec; ++e) count(f[e]);
+      for (int e = 0; e < kVec; ++e) f(x[e]);
     }
   } else {
-    for (int e = threadIdx.x; e < n; e += kHistThreads) count(Elem<E>::to_float(row[lo + e]));
+    for (int e = threadIdx.x; e < n; e += kHistThreads) f(Elem<E>::to_float(row[lo + e]));
   }
+}
+
+template <typename E>
+__device__ __forceinline__ const E* slot_row(const TopPArgs& a, int b, int i, int which) {
+  const int W = a.gmax + 1, V = a.geo.V;
+  return which ? static_cast<const E*>(a.draft) + (static_cast<size_t>(b) * a.gmax + i) * V
+               : static_cast<const E*>(a.target) + (static_cast<size_t>(b) * W + i) * V;
+}
+
+// Level 0's counter: every element's mass into the warp's own copy of the
+// 256 mass bins (two 32-bit words a bin: the low word, and the high word that
+// takes the carries out of it).
+struct MassBins {
+  const TopPArgs* a;
+  int b, i, which;
+  uint32_t* hist;  // this warp's copy
+  float cc, mc;
+  __device__ __forceinline__ void begin() { mc = scaled_max(row_max_warp(*a, b, i, which), cc); }
+  __device__ __forceinline__ void operator()(float x) const {
+    if (x == -INFINITY) return;  // no mass
+    const float d = __fmaf_rn(-x, cc, mc);  // fl(m c) - x c, one rounding
+    const int bin = min(255, max(0, __float2int_rd(d * 8.f)));
+    const int digit = 255 - bin;  // larger digit, larger mass
+    const unsigned long long mass = mass_fixed(fast_exp2(-d));
+    const uint32_t lo32 = static_cast<uint32_t>(mass), hi32 = static_cast<uint32_t>(mass >> 32);
+    const uint32_t old = lo32 ? atomicAdd(&hist[digit], lo32) : 0u;
+    const uint32_t hi_add = hi32 + (old + lo32 < old ? 1u : 0u);  // the carry out of the low word
+    if (hi_add) atomicAdd(&hist[256 + digit], hi_add);
+  }
+};
+
+// Later levels' counter: the elements of the chosen mass bin b* whose key
+// carries the digits fixed so far add their mass to the global histogram of
+// this level's digit.  Almost every element is rejected by two compares
+// against b*'s logit interval, so the few masses go straight to global
+// memory: no shared histogram and no block barrier.
+struct DigitMasses {
+  const TopPArgs* a;
+  int b, i, which;
+  unsigned long long* hist;  // this row slot's global histogram
+  float cc, mc, xlo, xhi;
+  uint32_t bstar, prefix;
+  int hi_shift, nb;
+  __device__ __forceinline__ void begin() {
+    mc = scaled_max(row_max_warp(*a, b, i, which), cc);
+    // the logits whose bin can be b*: the bin's edges d = b*/8 and (b*+1)/8
+    // turned into logits and widened well past the rounding of d; the few
+    // candidates take the exact bin test
+    const float pad = (fabsf(mc / cc) + 1.f) * 1e-5f;
+    xlo = -INFINITY;
+    xhi = INFINITY;
+    if (bstar > 0u) xhi = (mc - static_cast<float>(bstar) * 0.125f) / cc + pad;
+    if (bstar < 255u) xlo = (mc - static_cast<float>(bstar + 1u) * 0.125f) / cc - pad;
+  }
+  __device__ __forceinline__ void operator()(float x) const {
+    if (x == -INFINITY || x < xlo || x > xhi) return;  // no mass, or certainly another bin
+    const float d = __fmaf_rn(-x, cc, mc);
+    const int bin = min(255, max(0, __float2int_rd(d * 8.f)));
+    if (static_cast<uint32_t>(bin) != bstar) return;
+    const uint32_t k = logit_key(x);
+    if (a->level >= 2 && (k >> hi_shift) != prefix) return;
+    const int digit = static_cast<int>((k >> a->shift) & static_cast<uint32_t>(nb - 1));
+    const unsigned long long mass = mass_fixed(fast_exp2(-d));
+    if (mass) atomicAdd(&hist[digit], mass);
+  }
+};
+
+}  // namespace
+
+// Level 0 over one chunk of one row.  Grid (chunk, row slot (i, which),
+// request).  Each warp bins into its own copy; the copies are summed into the
+// row's global histogram at the end.
+template <typename E>
+__global__ void __launch_bounds__(kHistThreads) topp_hist_kernel(const TopPArgs a) {
+  extern __shared__ __align__(16) uint32_t s_hist[];  // [warps][2][256]
+  griddep_launch_dependents();
+  const int c = blockIdx.x, i = blockIdx.y >> 1, which = blockIdx.y & 1, b = blockIdx.z;
+  float T;
+  if (!slot_active(a, b, i, which, &T)) return;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t* my_hist = s_hist + warp * 512;
+  for (int d = lane; d < 512; d += 32) my_hist[d] = 0u;
+  __syncwarp();
+  const int lo = c * a.geo.chunk;
+  MassBins f{&a, b, i, which, my_hist, kLog2e / T, 0.f};
+  for_chunk<E>(a, slot_row<E>(a, b, i, which), lo, min(a.geo.chunk, a.geo.V - lo), f);
   __syncthreads();
-  unsigned long long* h = a.hist + rs * nb;
-  for (int d = threadIdx.x; d < nb; d += kHistThreads) {
+  const size_t rs = (static_cast<size_t>(b) * (a.gmax + 1) + i) * 2 + which;
+  unsigned long long* h = a.hist + rs * 256;
+  for (int d = threadIdx.x; d < 256; d += kHistThreads) {
     unsigned long long m = 0ull;
-    for (int q = 0; q < copies; ++q)
-      m += (static_cast<unsigned long long>(s_hist[q * 2 * nb + nb + d]) << 32) + s_hist[q * 2 * nb + d];
+    for (int q = 0; q < kHistThreads / 32; ++q)
+      m += (static_cast<unsigned long long>(s_hist[q * 512 + 256 + d]) << 32) + s_hist[q * 512 + d];
     if (m) atomicAdd(&h[d], m);
   }
+}
+
+// Levels 1.. over one chunk of one row.  Grid as level 0.
+template <typename E>
+__global__ void __launch_bounds__(kHistThreads) topp_refine_kernel(const TopPArgs a) {
+  griddep_launch_dependents();
+  const int c = blockIdx.x, i = blockIdx.y >> 1, which = blockIdx.y & 1, b = blockIdx.z;
+  float T;
+  if (!slot_active(a, b, i, which, &T)) return;
+  const size_t rs = (static_cast<size_t>(b) * (a.gmax + 1) + i) * 2 + which;
+  const int lo = c * a.geo.chunk;
+  DigitMasses f;
+  f.a = &a;
+  f.b = b;
+  f.i = i;
+  f.which = which;
+  f.nb = 1 << a.bits;
+  f.hist = a.hist + rs * f.nb;
+  f.cc = kLog2e / T;
+  f.hi_shift = a.shift + a.bits;  // key bits above this level's digit (levels >= 2: all decided)
+  // b* and the prefix come from the previous selects: read after the wait
+  struct Late {
+    DigitMasses& g;
+    size_t rs;
+    __device__ __forceinline__ void begin() {
+      g.bstar = __ldcg(g.a->bstar + rs);
+      g.prefix = g.a->level >= 2 ? __ldcg(g.a->prefix + rs) : 0u;
+      g.begin();
+    }
+    __device__ __forceinline__ void operator()(float x) const { g(x); }
+  } late{f, rs};
+  for_chunk<E>(a, slot_row<E>(a, b, i, which), lo, min(a.geo.chunk, a.geo.V - lo), late);
 }
 
 // Select of one level: one CTA per row slot fixes the next digit.  Thread t
@@ -267,6 +336,8 @@ __global__ void __launch_bounds__(256) topp_select_kernel(const TopPArgs a) {
 
 template __global__ void topp_hist_kernel<uint16_t>(const TopPArgs);
 template __global__ void topp_hist_kernel<float>(const TopPArgs);
+template __global__ void topp_refine_kernel<uint16_t>(const TopPArgs);
+template __global__ void topp_refine_kernel<float>(const TopPArgs);
 
 cudaError_t launch_topp_level(const TopPArgs& a, int esize, cudaStream_t stream) {
   cudaLaunchAttribute pdl[1];
@@ -275,13 +346,18 @@ cudaError_t launch_topp_level(const TopPArgs& a, int esize, cudaStream_t stream)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.geo.nchunk, 2 * (a.gmax + 1), a.B);
   cfg.blockDim = dim3(kHistThreads, 1, 1);
-  // two 32-bit words per bin; level 0: one histogram per warp
-  cfg.dynamicSmemBytes = (static_cast<size_t>(8) << a.bits) * (a.level == 0 ? kHistThreads / 32 : 1);
+  // level 0: one histogram of 256 bins (two 32-bit words each) per warp
+  cfg.dynamicSmemBytes = a.level == 0 ? static_cast<size_t>(8 * 256) * (kHistThreads / 32) : 0;
   cfg.stream = stream;
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
-  cudaError_t e = esize == 2 ? cudaLaunchKernelEx(&cfg, topp_hist_kernel<uint16_t>, a)
-                             : cudaLaunchKernelEx(&cfg, topp_hist_kernel<float>, a);
+  cudaError_t e;
+  if (a.level == 0)
+    e = esize == 2 ? cudaLaunchKernelEx(&cfg, topp_hist_kernel<uint16_t>, a)
+                   : cudaLaunchKernelEx(&cfg, topp_hist_kernel<float>, a);
+  else
+    e = esize == 2 ? cudaLaunchKernelEx(&cfg, topp_refine_kernel<uint16_t>, a)
+                   : cudaLaunchKernelEx(&cfg, topp_refine_kernel<float>, a);
   if (e != cudaSuccess) return e;
   const size_t nslots = static_cast<size_t>(a.B) * (a.gmax + 1) * 2;
   cfg.gridDim = dim3(static_cast<unsigned>(nslots), 1, 1);
