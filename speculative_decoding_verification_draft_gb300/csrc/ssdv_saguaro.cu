@@ -70,6 +70,17 @@ struct MixW {
 
 constexpr int kS = 128;  // threads of a residual / mix CTA
 constexpr int kSW = kS / 32;
+// Resident CTAs per SM the residual and mix kernels are built for.  Both
+// passes wait on HBM with few warps per SM, so fp32 rows trade registers for
+// warps: 6 and 8 CTAs per SM (80 and 64 registers, against 90 and 80 left
+// free), measured 0.999 against 1.070 ms per Saguaro round at B=256, gamma 6,
+// V=152064.  bf16 rows measured slower that way and keep the allocation they
+// get unconstrained (the residual kernel without top-k: 72 registers, 7 CTAs
+// per SM; with top-k: up to 128, 4; the mix kernel: 80, 6).
+template <typename E, int kKey>
+constexpr int resid_min_blocks() { return sizeof(E) == 4 ? 6 : (kKey == 0 ? 7 : 4); }
+template <typename E>
+constexpr int mix_min_blocks() { return sizeof(E) == 4 ? 8 : 6; }
 constexpr int kTopK = SSD_MAX_TOPK;  // every warp tracks the top 8; the first k are written
 
 // Row statistics of unit u from its chunk records (one warp; lanes < NC hold
@@ -259,7 +270,7 @@ __device__ __forceinline__ void write_topk(const SagArgs& a, size_t u, double to
 // Kernel 2: residual sums and top-k.  Grid (warp groups, j, request).
 // ---------------------------------------------------------------------------
 template <typename E, int kKey>
-__global__ void __launch_bounds__(kS) residual_kernel(const SagArgs a) {
+__global__ void __launch_bounds__(kS, resid_min_blocks<E, kKey>()) residual_kernel(const SagArgs a) {
   extern __shared__ __align__(16) uint8_t dyn_smem[];
   __shared__ float4 sh_stats;
   __shared__ int sh_err;
@@ -329,7 +340,7 @@ __global__ void __launch_bounds__(kS) residual_kernel(const SagArgs a) {
 // Kernel 3: the Saguaro mix and its draw.  Grid as kernel 2.
 // ---------------------------------------------------------------------------
 template <typename E>
-__global__ void __launch_bounds__(kS) mix_kernel(const SagArgs a) {
+__global__ void __launch_bounds__(kS, mix_min_blocks<E>()) mix_kernel(const SagArgs a) {
   extern __shared__ __align__(16) uint8_t dyn_smem[];
   griddep_launch_dependents();  // the next kernel may become resident (it waits for this grid)
   const int W = a.g + 1, j = blockIdx.y, b = blockIdx.z;
