@@ -205,6 +205,21 @@ ssd_status ssd_verify_ragged(const void* target_logits, const void* draft_logits
                              int32_t* out_tokens, int32_t* n_accepted, void* workspace,
                              size_t ws_bytes, void* stream);
 
+/* Pipelined ragged verification: ssd_verify_ragged for a chain of calls whose
+ * inputs are already complete.  Like ssd_verify_pipelined, this entry point
+ * has no counterpart in the method's description.  Same arguments, outputs,
+ * numerics and random draws as ssd_verify_ragged; the difference is the one
+ * between ssd_verify_pipelined and ssd_verify.  The streaming kernel may read
+ * this call's logits while the previous call's sampling kernel still runs, so
+ * the caller guarantees that the inputs (logits, draft tokens, gamma and
+ * temperature arrays) were complete before the previous verification call on
+ * `stream` completed. */
+ssd_status ssd_verify_ragged_pipelined(const void* target_logits, const void* draft_logits, ssd_dtype dtype,
+                                       const int32_t* draft_tokens, int B, int gamma_max, int V,
+                                       const int32_t* gamma, const float* temperature, uint64_t seed,
+                                       int32_t* out_tokens, int32_t* n_accepted, void* workspace,
+                                       size_t ws_bytes, void* stream);
+
 /* Saguaro pre-speculation (SSD notes, sections 3.1 and 3.2).  For each request
  * b and each acceptance length j = 0..gamma:
  *   r_j = (q_j - p_j)+ / sum (q_j - p_j)+  for j < gamma (q_j if that mass is

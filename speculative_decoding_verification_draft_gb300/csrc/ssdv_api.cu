@@ -447,6 +447,17 @@ ssd_status ssd_verify_ragged(const void* target_logits, const void* draft_logits
                        false, seed, out_tokens, n_accepted, workspace, ws_bytes, nullptr, stream);
 }
 
+ssd_status ssd_verify_ragged_pipelined(const void* target_logits, const void* draft_logits, ssd_dtype dtype,
+                                       const int32_t* draft_tokens, int B, int gamma_max, int V,
+                                       const int32_t* gamma, const float* temperature, uint64_t seed,
+                                       int32_t* out_tokens, int32_t* n_accepted, void* workspace, size_t ws_bytes,
+                                       void* stream) {
+  g_last_error.clear();
+  if (!gamma || !temperature) return fail(SSD_ERR_NULL, "gamma / temperature arrays are NULL");
+  return verify_common(target_logits, draft_logits, dtype, draft_tokens, B, gamma_max, V, gamma, temperature, 0.f,
+                       false, seed, out_tokens, n_accepted, workspace, ws_bytes, nullptr, stream, true);
+}
+
 ssd_status ssd_debug_rowstats(const void* target_logits, const void* draft_logits, ssd_dtype dtype,
                               const int32_t* draft_tokens, int B, int gamma, int V, float temperature,
                               uint64_t seed, int32_t* out_tokens, int32_t* n_accepted, float* stats, void* workspace,

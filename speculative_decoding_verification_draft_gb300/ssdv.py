@@ -48,6 +48,7 @@ def _declare(lib):
     lib.ssd_workspace_init.argtypes = [P, SZ, P]
     lib.ssd_verify.argtypes = [P, P, I, P, I, I, I, F, U64, P, P, P, SZ, P]
     lib.ssd_verify_ragged.argtypes = [P, P, I, P, I, I, I, P, P, U64, P, P, P, SZ, P]
+    lib.ssd_verify_ragged_pipelined.argtypes = [P, P, I, P, I, I, I, P, P, U64, P, P, P, SZ, P]
     lib.ssd_verify_noalloc.argtypes = [P, P, I, P, I, I, I, F, U64, P, P, P]
     lib.ssd_verify_pipelined.argtypes = [P, P, I, P, I, I, I, F, U64, P, P, P, SZ, P]
     lib.ssd_saguaro_prespec.argtypes = [P, P, I, I, I, I, I, I, F, U64, P, P, P, SZ, P]
@@ -68,7 +69,8 @@ def _declare(lib):
     lib.ssd_last_error.argtypes = []
     lib.ssd_last_error.restype = ctypes.c_char_p
     for name in ("ssd_workspace_init", "ssd_verify", "ssd_verify_noalloc", "ssd_verify_pipelined",
-                 "ssd_verify_ragged", "ssd_saguaro_prespec", "ssd_debug_rowstats", "ssd_debug_saguaro_stats", "ssd_read_status",
+                 "ssd_verify_ragged", "ssd_verify_ragged_pipelined", "ssd_saguaro_prespec", "ssd_debug_rowstats",
+                 "ssd_debug_saguaro_stats", "ssd_read_status",
                  "ssd_verify_saguaro", "ssd_cache_check", "ssd_verify_saguaro_draft", "ssd_verify_top_p",
                  "ssd_debug_uniforms"):
         getattr(lib, name).restype = I
@@ -268,8 +270,11 @@ def verify_noalloc(target: torch.Tensor, draft: Optional[torch.Tensor], draft_to
 def verify_ragged(target: torch.Tensor, draft: torch.Tensor, draft_tokens: torch.Tensor,
                   gamma: torch.Tensor, temperature: torch.Tensor, seed: int,
                   out_tokens: Optional[torch.Tensor] = None, n_accepted: Optional[torch.Tensor] = None,
-                  workspace: Optional[torch.Tensor] = None, stream=None):
-    """ssd_verify_ragged: per-request gamma [B] int32 and temperature [B] float32."""
+                  workspace: Optional[torch.Tensor] = None, stream=None, pipelined: bool = False):
+    """ssd_verify_ragged: per-request gamma [B] int32 and temperature [B] float32.
+
+    pipelined=True calls ssd_verify_ragged_pipelined: the inputs must have been
+    complete before the previous verification call on the stream completed."""
     B, W, V = target.shape
     gmax = W - 1
     dev = target.device
@@ -278,13 +283,12 @@ def verify_ragged(target: torch.Tensor, draft: torch.Tensor, draft_tokens: torch
     if n_accepted is None:
         n_accepted = torch.empty(B, dtype=torch.int32, device=dev)
     ws = _workspace(B, gmax, dev, workspace)
-    _check(lib().ssd_verify_ragged(_dev(target, "target_logits"), _dev(draft, "draft_logits", target.dtype),
-                                   _dtype_code(target), _dev(draft_tokens, "draft_tokens", torch.int32), B, gmax,
-                                   V, _dev(gamma, "gamma", torch.int32), _dev(temperature, "temperature",
-                                                                              torch.float32),
-                                   int(seed) & ((1 << 64) - 1), _dev(out_tokens, "out_tokens", torch.int32),
-                                   _dev(n_accepted, "n_accepted", torch.int32), _dev(ws, "workspace"),
-                                   ws.numel(), _stream(stream)))
+    fn = lib().ssd_verify_ragged_pipelined if pipelined else lib().ssd_verify_ragged
+    _check(fn(_dev(target, "target_logits"), _dev(draft, "draft_logits", target.dtype), _dtype_code(target),
+              _dev(draft_tokens, "draft_tokens", torch.int32), B, gmax, V, _dev(gamma, "gamma", torch.int32),
+              _dev(temperature, "temperature", torch.float32), int(seed) & ((1 << 64) - 1),
+              _dev(out_tokens, "out_tokens", torch.int32), _dev(n_accepted, "n_accepted", torch.int32),
+              _dev(ws, "workspace"), ws.numel(), _stream(stream)))
     return out_tokens, n_accepted
 
 

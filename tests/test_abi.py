@@ -30,6 +30,7 @@ def lib():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for want in ("ssd_verify", "ssd_verify_pipelined", "ssd_verify_noalloc", "ssd_verify_ragged",
+                 "ssd_verify_ragged_pipelined",
                  "ssd_saguaro_prespec", "ssd_saguaro_workspace_bytes", "ssd_workspace_bytes",
                  "ssd_verify_saguaro", "ssd_cache_check", "ssd_verify_saguaro_draft", "ssd_verify_top_p",
                  "ssd_verify_top_p_workspace_bytes",

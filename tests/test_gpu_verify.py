@@ -272,6 +272,33 @@ def test_pipelined_chain_matches_plain_calls(ssdv):
     assert torch.equal(o, ref[1][0]) and torch.equal(n, ref[1][1])
 
 
+def test_ragged_pipelined_chain_matches_plain_calls(ssdv):
+    """Chained ssd_verify_ragged_pipelined calls on resident ragged batches
+    (padded rows NaN, half the requests greedy) give the outputs of the same
+    calls made one at a time with ssd_verify_ragged."""
+    cpu_sets = [wl.ragged_batch(24, 6, 30000, seed=80 + k) for k in range(3)]
+    sets = [b.to("cuda") for b in cpu_sets]
+    ws = ssdv.make_workspace(24, 6)
+    ref = []
+    for k, b in enumerate(sets):
+        o, n = ssdv.verify_ragged(b.target, b.draft, b.draft_tokens, b.gamma, b.temperature, 200 + k,
+                                  workspace=ws)
+        torch.cuda.synchronize()
+        ref.append((o.clone(), n.clone()))
+    outs = [(torch.full((24, 7), -9, dtype=torch.int32, device="cuda"),
+             torch.full((24,), -9, dtype=torch.int32, device="cuda")) for _ in range(9)]
+    for r in range(9):  # no synchronisation inside the chain; call 4 is a plain one
+        k = r % 3
+        b = sets[k]
+        ssdv.verify_ragged(b.target, b.draft, b.draft_tokens, b.gamma, b.temperature, 200 + k, outs[r][0],
+                           outs[r][1], workspace=ws, pipelined=(r != 4))
+    torch.cuda.synchronize()
+    for r in range(9):
+        assert torch.equal(outs[r][0], ref[r % 3][0]) and torch.equal(outs[r][1], ref[r % 3][1]), r
+    # and the plain calls match the oracle (the ragged parity the chain inherits)
+    gc.assert_verify_parity(ref[0][0], ref[0][1], gc.verify_oracle(cpu_sets[0], 200), 30000, "ragged B=24 g<=6")
+
+
 def test_workspace_shared_across_shapes(ssdv):
     """One workspace serves calls of different (B, gamma) in any order."""
     ws = ssdv.make_workspace(64, 8)
