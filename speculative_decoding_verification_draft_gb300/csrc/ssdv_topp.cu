@@ -7,8 +7,8 @@
 // top_p of the row's probability mass (tokens tied with the last one needed
 // are kept), renormalised.
 //
-// th is found per row by a select over levels, each a histogram pass over the
-// rows' chunks followed by a select pass (one warp per row).  Level 0 bins
+// th is found per row by a select over levels, each a counting pass over the
+// rows' chunks followed by a select pass (one CTA per row).  Level 0 bins
 // every element by its mass relative to the row maximum, an eighth of an
 // octave per bin (bin = floor(8 (fl(m c) - x c)), the last bin holding the
 // tail), which spreads a row's elements over many bins; the select fixes the
@@ -16,7 +16,8 @@
 // The later levels resolve th inside b* by a radix select over a monotone
 // 32-bit key of the logit, high digits first (bf16: two 8-bit digits of the
 // 16 bits that matter; fp32: digits of 11, 11 and 10 bits), counting only the
-// elements of b*.  Masses exp2(x c - fl(m c)) are summed in fixed point (2^-40
+// elements of b* (topp_refine_kernel: so few that their masses go straight to
+// global memory).  Masses exp2(x c - fl(m c)) are summed in fixed point (2^-40
 // units), so the integer sums are exact and the same on every run whatever
 // the order of the atomics.
 #include "ssdv_device.cuh"
