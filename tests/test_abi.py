@@ -84,6 +84,13 @@ def test_host_validation_without_gpu(lib):
     assert L.ssd_verify_saguaro_draft(p, p, 0, p, 1, 1, 8, 0.0, 0, p, p, p, 1 << 20, None) == 6
     assert L.ssd_verify_saguaro_draft(p, p, 0, p, 4, 2, 8, 1.0, 0, p, p, p, 8, None) == 9
     assert L.ssd_cache_check(p, p, p, 4, 2, 9, p, None, None) == 2
+    # ragged calls, plain and pipelined: the per-request arrays are required,
+    # then the shape and the workspace are checked as for ssd_verify
+    for fn in (L.ssd_verify_ragged, L.ssd_verify_ragged_pipelined):
+        assert fn(p, p, 0, p, 1, 1, 8, None, p, 0, p, p, p, 1 << 20, None) == 1
+        assert fn(p, p, 0, p, 1, 1, 8, p, None, 0, p, p, p, 1 << 20, None) == 1
+        assert fn(p, p, 0, p, 0, 1, 8, p, p, 0, p, p, p, 1 << 20, None) == 2
+        assert fn(p, p, 0, p, 4, 2, 8, p, p, 0, p, p, p, 8, None) == 9
     # Saguaro workspace: zero for a bad shape, grows with the vocabulary
     assert L.ssd_saguaro_workspace_bytes(0, 1, 8) == 0
     assert L.ssd_saguaro_workspace_bytes(4, 2, 1 << 17) > L.ssd_saguaro_workspace_bytes(4, 2, 1 << 10)
