@@ -27,6 +27,8 @@ namespace ssdv {
 namespace {
 
 constexpr int kHistThreads = 256;
+constexpr uint32_t kRowDone = 0xFFFFFFFFu;     // bstar of a row whose th is fixed before the last level
+constexpr uint32_t kDirectFlag = 0x80000000u;  // level 1's word for the select: keys counted directly
 
 __device__ __forceinline__ bool temperature_ok_tp(float T) { return T == 0.f || (T >= 1e-6f && T <= 3.0e38f); }
 
@@ -158,6 +160,8 @@ struct DigitMasses {
   float cc, mc, xlo, xhi;
   uint32_t bstar, prefix;
   int hi_shift, nb;
+  bool direct;      // level 1 of bf16 rows: the digit is the whole 16-bit key, less base16
+  uint32_t base16;
   __device__ __forceinline__ void begin() {
     mc = scaled_max(row_max_warp(*a, b, i, which), cc);
     // the logits whose bin can be b*: the bin's edges d = b*/8 and (b*+1)/8
@@ -168,6 +172,17 @@ struct DigitMasses {
     xhi = INFINITY;
     if (bstar > 0u) xhi = (mc - static_cast<float>(bstar) * 0.125f) / cc + pad;
     if (bstar < 255u) xlo = (mc - static_cast<float>(bstar + 1u) * 0.125f) / cc - pad;
+    // bf16 logits carry 16 key bits.  When b*'s interval spans at most nb of
+    // them, level 1 counts every key of b* in a bin of its own, and its
+    // select fixes th outright (the key is monotone in the logit, so every
+    // candidate's key lies in [key(xlo), key(xhi)]).
+    direct = false;
+    base16 = 0u;
+    if (a->level == 1 && a->nlevels == 3 && bstar > 0u && bstar < 255u) {
+      const uint32_t lo16 = logit_key(xlo) >> 16, hi16 = logit_key(xhi) >> 16;
+      direct = hi16 - lo16 < static_cast<uint32_t>(nb);
+      base16 = lo16;
+    }
   }
   __device__ __forceinline__ void operator()(float x) const {
     if (x == -INFINITY || x < xlo || x > xhi) return;  // no mass, or certainly another bin
@@ -176,7 +191,8 @@ struct DigitMasses {
     if (static_cast<uint32_t>(bin) != bstar) return;
     const uint32_t k = logit_key(x);
     if (a->level >= 2 && (k >> hi_shift) != prefix) return;
-    const int digit = static_cast<int>((k >> a->shift) & static_cast<uint32_t>(nb - 1));
+    const int digit = direct ? static_cast<int>((k >> 16) - base16)
+                             : static_cast<int>((k >> a->shift) & static_cast<uint32_t>(nb - 1));
     const unsigned long long mass = mass_fixed(fast_exp2(-d));
     if (mass) atomicAdd(&hist[digit], mass);
   }
@@ -220,6 +236,12 @@ __global__ void __launch_bounds__(kHistThreads) topp_refine_kernel(const TopPArg
   float T;
   if (!slot_active(a, b, i, which, &T)) return;
   const size_t rs = (static_cast<size_t>(b) * (a.gmax + 1) + i) * 2 + which;
+  if (a.level >= 2 && a.nlevels == 3) {
+    // bf16 rows whose level-1 select fixed th already are done: wait for it
+    // before loading anything, so that they cost no reads
+    griddep_wait();
+    if (__ldcg(a.bstar + rs) == kRowDone) return;
+  }
   const int lo = c * a.geo.chunk;
   DigitMasses f;
   f.a = &a;
@@ -238,6 +260,10 @@ __global__ void __launch_bounds__(kHistThreads) topp_refine_kernel(const TopPArg
       g.bstar = __ldcg(g.a->bstar + rs);
       g.prefix = g.a->level >= 2 ? __ldcg(g.a->prefix + rs) : 0u;
       g.begin();
+      // level 1 of bf16 rows: tell the select how this row was counted (every
+      // CTA of the row derives the same answer)
+      if (g.a->level == 1 && g.a->nlevels == 3 && blockIdx.x == 0 && threadIdx.x == 0)
+        g.a->prefix[rs] = g.direct ? (kDirectFlag | g.base16) : 0u;
     }
     __device__ __forceinline__ void operator()(float x) const { g(x); }
   } late{f, rs};
@@ -259,6 +285,7 @@ __global__ void __launch_bounds__(256) topp_select_kernel(const TopPArgs a) {
   float T;
   if (!slot_active(a, b, i, which, &T)) return;  // uniform over the CTA
   griddep_wait();  // the level's histograms are complete and visible
+  if (a.level >= 2 && __ldcg(a.bstar + rs) == kRowDone) return;  // th fixed at level 1 (uniform)
   const int nb = 1 << a.bits, per = nb >> 8;  // 1, 4 or 8
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const unsigned long long* h = a.hist + rs * nb + static_cast<size_t>(t) * per;
@@ -316,7 +343,16 @@ __global__ void __launch_bounds__(256) topp_select_kernel(const TopPArgs a) {
   }
   const uint32_t prefix = a.level >= 2 ? __ldcg(a.prefix + rs) : 0u;
   const uint32_t np = (prefix << a.bits) | static_cast<uint32_t>(d);
-  if (a.level == 0) {
+  const uint32_t word = a.level == 1 && a.nlevels == 3 ? __ldcg(a.prefix + rs) : 0u;
+  if (word & kDirectFlag) {
+    // bf16 row counted by whole keys: digit d is key16 - base16, so th is
+    // that key's logit (low bits as at the last level) and the row is done
+    uint32_t k = ((word & 0xFFFFu) + static_cast<uint32_t>(d)) << 16;
+    if (!(k & 0x80000000u)) k |= 0xFFFFu;
+    a.th[rs] = key_logit(k);
+    a.z[rs] = static_cast<float>(static_cast<double>(cum + dmass) * (1.0 / 1099511627776.0));
+    a.bstar[rs] = kRowDone;
+  } else if (a.level == 0) {
     a.bstar[rs] = 255u - static_cast<uint32_t>(d);
     a.above[rs] = cum;
     a.goal[rs] = goal;
