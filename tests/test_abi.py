@@ -96,3 +96,24 @@ def test_host_validation_without_gpu(lib):
     assert L.ssd_saguaro_workspace_bytes(4, 2, 1 << 17) > L.ssd_saguaro_workspace_bytes(4, 2, 1 << 10)
     for code in range(12):
         assert L.ssd_status_str(code).startswith(b"SSD_")
+
+
+def test_binding_has_no_host_fallback(monkeypatch):
+    """The Python binding only marshals device tensors into the C ABI: host
+    tensors are refused before any call, and a missing library is an error,
+    not a switch to some other implementation."""
+    import torch
+    from speculative_decoding_verification_draft_gb300 import ssdv
+    t = torch.zeros(2, 3, 16, dtype=torch.bfloat16)
+    d = torch.zeros(2, 2, 16, dtype=torch.bfloat16)
+    k = torch.zeros(2, 2, dtype=torch.int32)
+    ws = torch.zeros(1 << 16, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="CUDA device"):
+        ssdv.verify(t, d, k, 1.0, 0, workspace=ws)
+    with pytest.raises(ValueError, match="CUDA device"):
+        ssdv.verify_ragged(t, d, k, torch.full((2,), 2, dtype=torch.int32), torch.ones(2), 0, workspace=ws,
+                           pipelined=True)
+    monkeypatch.setattr(ssdv, "_lib", None)
+    monkeypatch.setattr(ssdv, "LIBRARY", os.path.join(ROOT, "no_such_dir", "libssdv.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        ssdv.lib()
