@@ -414,21 +414,31 @@ def secondary(ssdv, workloads, dev, stream):
 
 def cpu_baseline(batch_cpu, budget_s=12.0, max_s=30.0):
     """The fp64 oracle on the host cores: whole rounds of the same workload,
-    repeated until about budget_s of wall time (bounded by max_s)."""
+    repeated until about budget_s of wall time (bounded by max_s).  It also
+    counts the oracle's flagged draws (a uniform within the flag band of its
+    accept threshold or CDF edge; at most one a request, since the rest of a
+    flagged request is left out of the comparison) against all the draws of
+    those rounds."""
     import oracle
     orc = oracle.load()
     tgt, dft = batch_cpu.numpy_logits()
     tok = batch_cpu.draft_tokens.cpu().numpy()
+    gamma = tgt.shape[1] - 1
     cores = os.cpu_count() or 1
-    rounds, t_start = 0, time.perf_counter()
+    rounds, flagged, draws, t_start = 0, 0, 0, time.perf_counter()
     while True:
-        orc.verify_batch(tgt, dft, tok, TEMP, 99 + rounds, nthreads=cores)
+        r = orc.verify_batch(tgt, dft, tok, TEMP, 99 + rounds, nthreads=cores)
         rounds += 1
+        # a request draws one accept uniform per position tested (up to the
+        # first rejection) and one for the correction or bonus token
+        flagged += int((r["flag_pos"] >= 0).sum())
+        draws += int(np.minimum(r["n_accepted"] + 1, gamma).sum()) + len(r["n_accepted"])
         el = time.perf_counter() - t_start
         if el >= budget_s or el + el / rounds > max_s:
             break
     return {"value": rounds / el, "unit": "rounds/s", "cores": cores, "kind": "oracle",
-            "sample": f"{rounds} whole rounds (B=64, gamma 4, V 128256 bf16), fp64 C oracle, {cores} threads"}
+            "sample": f"{rounds} whole rounds (B=64, gamma 4, V 128256 bf16), fp64 C oracle, {cores} threads",
+            "flagged_draws": flagged, "draws": draws}
 
 
 def reference_arm(args):

@@ -43,3 +43,17 @@ def test_reference_arm_other_ranks_exit_without_work():
                   env_extra={"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"}, timeout=300)
     assert p.returncode == 0, p.stderr[-2000:]
     assert p.stdout.strip() == ""
+
+
+def test_cpu_baseline_counts_flagged_draws():
+    """The CPU-baseline leg (the oracle on the host cores) over one whole round
+    of the bench workload: its rate, and its flagged draws, which the method's
+    parity rule allows at up to 1e-4 of all draws."""
+    import bench
+    from speculative_decoding_verification_draft_gb300 import workloads
+    batch = workloads.zipf_batch(bench.B, bench.GAMMA, bench.V, temperature=bench.TEMP, seed=2)
+    cb = bench.cpu_baseline(batch, budget_s=0.0, max_s=60.0)
+    assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["cores"] >= 1
+    # one round: between 2 and gamma + 1 draws per request
+    assert 2 * bench.B <= cb["draws"] <= (bench.GAMMA + 1) * bench.B
+    assert 0 <= cb["flagged_draws"] <= cb["draws"] * 1e-4 + 1
