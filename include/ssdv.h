@@ -79,7 +79,8 @@ typedef enum { SSD_TOPK_RESIDUAL = 0, SSD_TOPK_DRAFT = 1 } ssd_topk_source;
 #define SSD_NSTAT_SAGUARO 10
 
 /* Bytes of device workspace ssd_verify / ssd_verify_pipelined /
- * ssd_verify_ragged / ssd_debug_rowstats need for a batch of B requests with
+ * ssd_verify_ragged / ssd_verify_ragged_pipelined / ssd_debug_rowstats need
+ * for a batch of B requests with
  * up to gamma_max draft tokens.  The workspace holds a status word and two
  * halves, used by alternate calls, of arrival counters (cleared by every call),
  * per-chunk row statistics and per-piece residual sums. */
