@@ -20,8 +20,9 @@
  *    last draft token); row i of the draft is the draft distribution that
  *    proposed draft token i.  dtype is SSD_BF16 or SSD_F32 for both.
  *  - Rows whose start is 16-byte aligned (base 16-byte aligned and V*size
- *    a multiple of 16) are staged into shared memory with bulk async copies;
- *    other rows take a plain-load path.  Both give the same results.
+ *    a multiple of 16) are read with 16-byte vector loads straight into
+ *    registers; other rows are copied into shared memory with plain loads.
+ *    Both give the same results.
  *  - Every real row must hold at least one finite logit; NaN and +inf logits
  *    are not valid input.  -inf logits are allowed (probability 0).
  *  - Temperature: softmax(x / T) on both target and draft.  T == 0 selects
@@ -61,7 +62,7 @@ typedef enum {
   SSD_ERR_UNSUPPORTED = 8, /* no launch configuration fits this device / shape   */
   SSD_ERR_WORKSPACE = 9,   /* workspace missing or smaller than required         */
   SSD_ERR_GAMMA = 10,      /* (device) a per-request gamma above gamma_max       */
-  SSD_ERR_TIMEOUT = 11     /* (device) a bounded wait for a bulk copy ran out    */
+  SSD_ERR_DRAW = 11        /* (device) a draw found no token of positive weight  */
 } ssd_status;
 
 typedef enum { SSD_BF16 = 0, SSD_F32 = 1 } ssd_dtype;
@@ -179,10 +180,12 @@ ssd_status ssd_verify_pipelined(const void* target_logits, const void* draft_log
  * B * (gamma + 1) <= 474 (B = 64 at gamma <= 6); a larger batch returns
  * SSD_ERR_WORKSPACE before anything is launched.
  *
- * The first call on each device (with that device current) looks up the
- * array's address with cudaGetSymbolAddress and zeroes the array with
- * cudaMemsetAsync on `stream`; make that first call before any stream capture
- * begins.  The kernels clear their own arrival counters on every call; the
+ * Every call looks up the current device's copy of the array with
+ * cudaGetSymbolAddress (a host-side query that allocates nothing).  The first
+ * call that sees a given address -- the first call on each device, and the
+ * first after a device reset, which reloads the library's device code and may
+ * move the array -- zeroes it with cudaMemsetAsync on `stream`; make that
+ * first call before any stream capture begins.  The kernels clear their own arrival counters on every call; the
  * status word is never read back on this path (a request with bad input still
  * gets n_accepted = -1 and out_tokens = -1).
  *

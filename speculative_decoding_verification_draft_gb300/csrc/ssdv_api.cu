@@ -8,9 +8,11 @@
 #include <string.h>
 
 #include <algorithm>
+#include <list>
 #include <mutex>
 #include <string>
 #include <unordered_map>
+#include <vector>
 
 #include "ssdv_device.cuh"
 #include "ssdv_internal.h"
@@ -111,13 +113,29 @@ namespace {
 
 // Consecutive calls on one workspace use alternate halves, so a pipelined
 // call's streaming kernel may run while the previous call's sampling kernel
-// reads the other half.  The parity is kept per workspace address on the host.
+// reads the other half.  The parity is kept on the host per workspace
+// address, for the kHalfSlots most recently used addresses (least recently
+// used first out): a workspace evicted from the table was last used at least
+// kHalfSlots calls on other workspaces ago, and starts again from half 0.
+constexpr size_t kHalfSlots = 4096;
 std::mutex g_half_mutex;
-std::unordered_map<const void*, unsigned long long> g_half;
+std::list<std::pair<const void*, unsigned long long>> g_half_lru;  // most recent first
+std::unordered_map<const void*, std::list<std::pair<const void*, unsigned long long>>::iterator> g_half;
 
 int next_half(const void* workspace) {
   std::lock_guard<std::mutex> lock(g_half_mutex);
-  return static_cast<int>(g_half[workspace]++ & 1ull);
+  auto it = g_half.find(workspace);
+  if (it == g_half.end()) {
+    if (g_half_lru.size() >= kHalfSlots) {
+      g_half.erase(g_half_lru.back().first);
+      g_half_lru.pop_back();
+    }
+    g_half_lru.emplace_front(workspace, 0ull);
+    it = g_half.emplace(workspace, g_half_lru.begin()).first;
+  } else if (it->second != g_half_lru.begin()) {
+    g_half_lru.splice(g_half_lru.begin(), g_half_lru, it->second);
+  }
+  return static_cast<int>(it->second->second++ & 1ull);
 }
 
 }  // namespace
@@ -148,7 +166,7 @@ ssd_status choose_chunks(int V, int esize, bool aligned, ChunkGeometry* geo, int
   geo->chunk = chunk;
   geo->nchunk = (V + chunk - 1) / chunk;
   geo->row_smem = row_smem;
-  geo->bulk = aligned ? 1 : 0;
+  geo->aligned = aligned ? 1 : 0;
   // pieces of the sampling kernel: 128 vectors of a row each
   geo->npiece = static_cast<int>((static_cast<long long>(V) + 128 * (16 / esize) - 1) / (128 * (16 / esize)));
   if (geo->npiece > kMaxPieces) return fail(SSD_ERR_UNSUPPORTED, "V=%d: more than %d pieces per row", V, kMaxPieces);
@@ -321,33 +339,32 @@ ssd_status verify_common(const void* target, const void* draft, ssd_dtype dtype,
 }  // namespace ssdv
 
 // Scratch of ssd_verify_noalloc: one fixed array per device, so that entry
-// point never allocates.  Its address is looked up once per device.
+// point never allocates.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[SSD_NOALLOC_SCRATCH_BYTES];
 
 namespace ssdv {
 namespace {
 
-constexpr int kNoallocMaxDevices = 64;
+// Device addresses of the array already zeroed.  Keyed by the address, not
+// the device ordinal: after a device reset the module is loaded again and the
+// array may sit elsewhere, and that new copy is zeroed before first use.
 std::mutex g_noalloc_mutex;
-void* g_noalloc_ptr[kNoallocMaxDevices] = {};
+std::vector<void*> g_noalloc_zeroed;
 
-// The current device's scratch address; on the first call for a device, look
-// it up (that device is current) and zero the array on `stream`.
+// The current device's scratch address, looked up on every call (a host-side
+// query that allocates nothing); an address seen for the first time is zeroed
+// on `stream`.
 ssd_status noalloc_scratch(cudaStream_t stream, void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  if (dev < 0 || dev >= kNoallocMaxDevices) return fail(SSD_ERR_UNSUPPORTED, "device ordinal %d >= 64", dev);
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the no-alloc scratch");
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  if (!g_noalloc_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the no-alloc scratch");
+  if (std::find(g_noalloc_zeroed.begin(), g_noalloc_zeroed.end(), p) == g_noalloc_zeroed.end()) {
     e = cudaMemsetAsync(p, 0, SSD_NOALLOC_SCRATCH_BYTES, stream);
     if (e != cudaSuccess) return cuda_fail(e, "no-alloc scratch memset");
-    g_noalloc_ptr[dev] = p;
+    g_noalloc_zeroed.push_back(p);
   }
-  *out = g_noalloc_ptr[dev];
+  *out = p;
   return SSD_OK;
 }
 
@@ -805,7 +822,7 @@ const char* ssd_status_str(ssd_status status) {
     case SSD_ERR_UNSUPPORTED: return "SSD_ERR_UNSUPPORTED: no launch configuration fits";
     case SSD_ERR_WORKSPACE: return "SSD_ERR_WORKSPACE: workspace missing or too small";
     case SSD_ERR_GAMMA: return "SSD_ERR_GAMMA: a per-request gamma above gamma_max";
-    case SSD_ERR_TIMEOUT: return "SSD_ERR_TIMEOUT: a bounded wait for a bulk copy ran out";
+    case SSD_ERR_DRAW: return "SSD_ERR_DRAW: a draw found no token of positive weight";
   }
   return "unknown ssd_status";
 }

@@ -1,14 +1,9 @@
-// ssdv_device.cuh -- device building blocks shared by the verification and
-// Saguaro kernels: inline-PTX wrappers (mbarrier, bulk async copy, cluster
-// barrier, distributed shared memory), the Philox4x32-10 generator, row
-// staging into shared memory, the fused softmax-statistics pass, the weighted
-// pass with per-warp partial sums, and the inverse-CDF search.
-//
-// Work decomposition: one thread-block cluster per (request, position) unit.
-// CTA `rank` of the cluster owns the contiguous vocabulary slice
-// [rank * slice, rank * slice + n) of the unit's rows and keeps it resident in
-// its shared memory, so every logit is read from HBM exactly once; the
-// second and later passes (residual, Saguaro mix, CDF search) run on-chip.
+// ssdv_device.cuh -- device building blocks shared by the verification,
+// Saguaro and top-p kernels: exp2 and packed fp32 pairs, the bf16 / fp32
+// element types, the Philox4x32-10 generator, softmax statistics and their
+// combine, warp top-k lists, float-float running sums, programmatic dependent
+// launch and arrival counters, and the piece loads and lane-scan searches of
+// the inverse-CDF draw.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -23,7 +18,6 @@ constexpr int kThreads = 256;
 // vectors of a chunk row per thread in the register form of the streaming kernel
 constexpr int kRegVecs = 8;
 constexpr int kWarps = kThreads / 32;
-constexpr uint32_t kWaitLimit = 1u << 24;  // bounded polls of an mbarrier
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------------------
@@ -151,62 +145,6 @@ __device__ __forceinline__ F2 Elem<float>::exp_sum(const uint4& v, F2 c2, F2 nmc
 }
 
 // ---------------------------------------------------------------------------
-// PTX wrappers
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void fence_mbar_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-
-// Bounded wait for phase `parity` of an mbarrier; false if the bound ran out.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-  for (uint32_t it = 0; it < kWaitLimit; ++it)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
-}
-
-__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-
-// Bulk asynchronous copy global -> this CTA's shared memory, completing on an
-// mbarrier.  dst, src 16-byte aligned; bytes a positive multiple of 16.
-__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
-                                              uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
-      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
-      : "memory");
-}
-
-// ---------------------------------------------------------------------------
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11).  Key = (seed lo, seed hi),
 // counter = (request, position, 0, 0).  Word d is the uniform of draw d.
 // ---------------------------------------------------------------------------
@@ -294,7 +232,6 @@ struct Slice {
   E* sd;        // shared draft slice (valid when gd)
   int n;        // elements in this CTA's slice (may be 0)
   int nvec;     // ceil(n / kVec)
-  bool bulk;
 };
 
 template <typename E>
@@ -304,8 +241,8 @@ __device__ __forceinline__ void load_vec(const E* base, int v, float (&f)[Elem<E
 }
 
 // Warp butterfly of per-lane row statistics (target and draft (max, sum), the
-// target argmax, an error flag); the result is valid in every lane.
-__device__ __forceinline__ void butterfly_stats(MaxSum& t, MaxSum& d, ArgMax& a, int& to, float c) {
+// target argmax); the result is valid in every lane.
+__device__ __forceinline__ void butterfly_stats(MaxSum& t, MaxSum& d, ArgMax& a, float c) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     MaxSum ot{__shfl_xor_sync(0xFFFFFFFFu, t.m, o), __shfl_xor_sync(0xFFFFFFFFu, t.s, o)};
@@ -314,7 +251,6 @@ __device__ __forceinline__ void butterfly_stats(MaxSum& t, MaxSum& d, ArgMax& a,
     t = combine_ms(t, ot, c);
     d = combine_ms(d, od, c);
     a = better_arg(a, oa);
-    to |= __shfl_xor_sync(0xFFFFFFFFu, to, o);
   }
 }
 

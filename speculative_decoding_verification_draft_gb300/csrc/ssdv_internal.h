@@ -17,8 +17,8 @@ struct ChunkGeometry {
   int V;         // vocabulary size
   int chunk;     // elements per chunk, a multiple of 8
   int nchunk;    // chunks per row, 1..kMaxChunks
-  int row_smem;  // shared-memory bytes per staged row chunk (a multiple of 128)
-  int bulk;      // 1: rows 16-byte aligned, staged with bulk async copies
+  int row_smem;  // shared-memory bytes per row chunk of the shared-memory form (a multiple of 128)
+  int aligned;   // 1: rows 16-byte aligned (read with 16-byte vector loads)
   int npiece;    // pieces (128 vectors) per row, at most kMaxPieces
   int ppw;       // pieces per warp of the sampling kernel
 };

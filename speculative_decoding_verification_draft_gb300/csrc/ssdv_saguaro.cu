@@ -85,22 +85,18 @@ constexpr int kTopK = SSD_MAX_TOPK;  // every warp tracks the top 8; the first k
 
 // Row statistics of unit u from its chunk records (one warp; lanes < NC hold
 // a record each), valid in every lane: target and draft (max, sum).
-__device__ __forceinline__ void unit_stats(const SagArgs& a, size_t u, float c, MaxSum* t, MaxSum* d, int* err) {
+__device__ __forceinline__ void unit_stats(const SagArgs& a, size_t u, float c, MaxSum* t, MaxSum* d) {
   const int lane = threadIdx.x & 31, NC = a.geo.nchunk;
   MaxSum tt{-INFINITY, 0.f}, dd{-INFINITY, 0.f};
   ArgMax am{-INFINITY, -1};
-  int e = 0;
   if (lane < NC) {
-    const float4* rec = a.part + (u * NC + lane) * 2;
-    const float4 r0 = __ldcg(rec), r1 = __ldcg(rec + 1);
+    const float4 r0 = __ldcg(a.part + (u * NC + lane) * 2);
     tt = MaxSum{r0.x, r0.y};
     dd = MaxSum{r0.z, r0.w};
-    e = __float_as_int(r1.z);
   }
-  butterfly_stats(tt, dd, am, e, c);
+  butterfly_stats(tt, dd, am, c);
   *t = tt;
   *d = dd;
-  *err = e;
 }
 
 // One warp: the k best of n candidates (value, index), descending, the lower
@@ -166,7 +162,7 @@ __device__ __forceinline__ bool unit_pieces(const SagArgs& a, size_t u, int wi, 
   for (int j = 0; j < pn; ++j) {
     const int lo = (p0 + j) * pelems;
     PieceRows<E> pr;
-    pr.load(trow + lo, drow ? drow + lo : nullptr, min(pelems, V - lo), a.geo.bulk != 0);
+    pr.load(trow + lo, drow ? drow + lo : nullptr, min(pelems, V - lo), a.geo.aligned != 0);
     float s = 0.f;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -273,7 +269,6 @@ template <typename E, int kKey>
 __global__ void __launch_bounds__(kS, resid_min_blocks<E, kKey>()) residual_kernel(const SagArgs a) {
   extern __shared__ __align__(16) uint8_t dyn_smem[];
   __shared__ float4 sh_stats;
-  __shared__ int sh_err;
   griddep_launch_dependents();  // the mix kernel may become resident (it waits for this grid)
   const int W = a.g + 1, j = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -284,12 +279,8 @@ __global__ void __launch_bounds__(kS, resid_min_blocks<E, kKey>()) residual_kern
   griddep_wait();  // the streaming kernel's records are complete and visible
   if (warp == 0) {
     MaxSum t, d;
-    int err;
-    unit_stats(a, u, c, &t, &d, &err);
-    if (lane == 0) {
-      sh_stats = make_float4(t.m, t.s, d.m, d.s);
-      sh_err = err;
-    }
+    unit_stats(a, u, c, &t, &d);
+    if (lane == 0) sh_stats = make_float4(t.m, t.s, d.m, d.s);
   }
   __syncthreads();
   if (wi >= a.npw) return;
@@ -308,25 +299,19 @@ __global__ void __launch_bounds__(kS, resid_min_blocks<E, kKey>()) residual_kern
   rp.load(a.psum2 + u * a.geo.npiece, a.geo.npiece, s_pieces);
   const double S = rp.total;
   float* st = a.stats ? a.stats + u * SSD_NSTAT_SAGUARO : nullptr;
-  const int err = sh_err;
   if (lane == 0) {
     a.rowstat[u] = s4;
-    a.rowsum[u] = err ? NAN : S;
+    a.rowsum[u] = S;
     a.ticket3[u] = 0;  // the mix kernel's counter starts at zero (read after this grid completes)
     a.ticket2[u] = 0;  // the last arrival: zero again for a later kernel of the call
-    if (err) {
-      // a staging wait of the streaming kernel ran out: this unit's outputs are -1
-      atomicOr(a.status, 1 << SSD_ERR_TIMEOUT);
-      for (int s = 0; s < a.k; ++s) a.bonus_topk[u * a.k + s] = -1;
-      if (a.saguaro_tokens) a.saguaro_tokens[u] = -1;
-    } else if (st) {
+    if (st) {
       st[0] = logf(s4.y) - fmaf(s4.x, c, -scaled_max(s4.x, c)) * 0.6931471805599453f;
       st[1] = bonus ? NAN : logf(s4.w) - fmaf(s4.z, c, -scaled_max(s4.z, c)) * 0.6931471805599453f;
       st[2] = bonus ? 1.f : static_cast<float>(S / static_cast<double>(s4.y));
     }
   }
   const bool logit_keys = kKey == kKeyLogit;
-  if (kKey != kKeyNone && !err && (logit_keys || bonus || S > 0.0)) {
+  if (kKey != kKeyNone && (logit_keys || bonus || S > 0.0)) {
     __syncwarp();
     float* s_cv = reinterpret_cast<float*>(dyn_smem) + kSW * a.geo.npiece;
     int* s_ci = reinterpret_cast<int*>(s_cv + a.npw * kTopK);
@@ -375,12 +360,12 @@ __global__ void __launch_bounds__(kS, mix_min_blocks<E>()) mix_kernel(const SagA
   if (a.zsum && lane == 0) a.zsum[u] = static_cast<float>(rp.total);
   if (!a.saguaro_tokens) return;  // the normaliser is all a later kernel needs
   const float u_sag = unit_draws(a.seed, a.req_base + b, j).saguaro;
-  const RowDraw d = warp_locate_row<E>(rp, u_sag, trow, drow, V, a.geo.bulk != 0, mw);
+  const RowDraw d = warp_locate_row<E>(rp, u_sag, trow, drow, V, a.geo.aligned != 0, mw);
   float* st = a.stats ? a.stats + u * SSD_NSTAT_SAGUARO : nullptr;
   if (lane == 0) {
     const bool ok = d.elem >= 0 && rp.total > 0.0;
     a.saguaro_tokens[u] = ok ? d.elem : -1;
-    if (!ok) atomicOr(a.status, 1 << SSD_ERR_TIMEOUT);
+    if (!ok) atomicOr(a.status, 1 << SSD_ERR_DRAW);
     if (st && ok) {
       st[3] = static_cast<float>(rp.total);
       st[4] = static_cast<float>(static_cast<double>(d.w) / rp.total);
@@ -399,7 +384,7 @@ __global__ void __launch_bounds__(kS, mix_min_blocks<E>()) mix_kernel(const SagA
     for (int q = 0; q < a.geo.npiece; ++q) {
       const int lo = q * pelems;
       PieceRows<E> pr;
-      pr.load(trow + lo, nullptr, min(pelems, V - lo), a.geo.bulk != 0);
+      pr.load(trow + lo, nullptr, min(pelems, V - lo), a.geo.aligned != 0);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         float w[Elem<E>::kVec];

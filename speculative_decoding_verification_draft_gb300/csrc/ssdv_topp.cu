@@ -86,7 +86,7 @@ template <typename E, typename F>
 __device__ __forceinline__ void for_chunk(const TopPArgs& a, const E* row, int lo, int n, F&& f) {
   constexpr int kVec = Elem<E>::kVec;
   const int nvec = n / kVec;  // aligned rows: whole vectors
-  const bool batched = a.geo.bulk && nvec <= kNVH * kHistThreads;
+  const bool batched = a.geo.aligned && nvec <= kNVH * kHistThreads;
   uint4 r[kNVH];
   if (batched) {
     const uint4* rv = reinterpret_cast<const uint4*>(row + lo);
@@ -106,7 +106,7 @@ __device__ __forceinline__ void for_chunk(const TopPArgs& a, const E* row, int l
 #pragma unroll
       for (int e = 0; e < kVec; ++e) f(x[e]);
     }
-  } else if (a.geo.bulk) {
+  } else if (a.geo.aligned) {
     const uint4* rv = reinterpret_cast<const uint4*>(row + lo);
     for (int v = threadIdx.x; v < nvec; v += kHistThreads) {
       float x[kVec];

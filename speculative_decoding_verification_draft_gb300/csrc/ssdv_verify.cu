@@ -133,30 +133,11 @@ struct TargetW {
   }
 };
 
-// Stage one chunk (target and optionally draft) into shared memory: bulk
-// copies completing on `bar` (fresh phase 0), or plain loads padded with -inf
-// to a whole vector when the rows are not 16-byte aligned.  Returns false when
-// the bounded wait ran out.
-// One thread issues the copies and waits on the barrier while the others
-// park at __syncthreads (which costs no issue slots); the copies' data is
-// visible to every thread after the barrier.
+// Copy one chunk (target and optionally draft) of a row that is not 16-byte
+// aligned into shared memory with plain loads, padded with -inf to a whole
+// vector; visible to every thread after the block barrier.
 template <typename E>
-__device__ __forceinline__ bool stage_chunk(const Slice<E>& sl, uint64_t* bar, int* sh_ok) {
-  if (sl.bulk) {
-    if (threadIdx.x == 0) {
-      mbar_init(bar, 1);
-      fence_mbar_init();
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      const uint32_t bytes = static_cast<uint32_t>(sl.n) * sizeof(E);
-      mbar_arrive_expect_tx(bar, sl.gd ? 2 * bytes : bytes);
-      const uint64_t pol = l2_policy_evict_normal();
-      bulk_copy_g2s(sl.st, sl.gt, bytes, bar, pol);
-      if (sl.gd) bulk_copy_g2s(sl.sd, sl.gd, bytes, bar, pol);
-      *sh_ok = mbar_wait_bounded(bar, 0) ? 1 : 0;
-    }
-    __syncthreads();
-    return *sh_ok != 0;
-  }
+__device__ __forceinline__ void stage_chunk(const Slice<E>& sl) {
   constexpr int kVec = Elem<E>::kVec;
   const int padded = sl.nvec * kVec;
   for (int e = threadIdx.x; e < padded; e += kThreads) {
@@ -164,13 +145,12 @@ __device__ __forceinline__ bool stage_chunk(const Slice<E>& sl, uint64_t* bar, i
     if (sl.gd) sl.sd[e] = e < sl.n ? sl.gd[e] : Elem<E>::neg_inf();
   }
   __syncthreads();
-  return true;
 }
 
 // One unit's combined row statistics (sampling kernel).
 struct UnitStat {
   float tm, ts, dm, ds, av;
-  int ai, err;
+  int ai;
 };
 
 }  // namespace
@@ -182,10 +162,8 @@ template <typename E>
 __global__ void __launch_bounds__(kThreads) stream_kernel(const VerifyArgs a) {
   constexpr int kVec = Elem<E>::kVec;
   extern __shared__ __align__(128) uint8_t dyn_smem[];
-  __shared__ __align__(8) uint64_t bar;
   __shared__ float red_f[5 * kWarps];
   __shared__ int red_i[2 * kWarps];
-  __shared__ int sh_ok;
   // The first segment of a call waits for the previous kernel on the stream
   // before it reads or writes anything.  A later segment reads logits that
   // were complete before the first segment's CTAs passed that wait (its
@@ -217,12 +195,11 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const VerifyArgs a) {
   Slice<E> sl;
   sl.n = min(geo.chunk, V - lo);
   sl.nvec = (sl.n + kVec - 1) / kVec;
-  sl.bulk = geo.bulk != 0;
   sl.gt = static_cast<const E*>(a.target) + (static_cast<size_t>(b) * W + i) * V + lo;
   sl.gd = has_draft ? static_cast<const E*>(a.draft) + (static_cast<size_t>(b) * a.gmax + i) * V + lo : nullptr;
   sl.st = reinterpret_cast<E*>(dyn_smem);
   sl.sd = reinterpret_cast<E*>(dyn_smem + geo.row_smem);
-  const bool ok = stage_chunk(sl, &bar, &sh_ok);
+  stage_chunk(sl);
   const uint4* vt = reinterpret_cast<const uint4*>(sl.st);
   const uint4* vd = reinterpret_cast<const uint4*>(sl.sd);
 
@@ -257,7 +234,7 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const VerifyArgs a) {
       ArgMax best{-INFINITY, -1};
       for (int w = 0; w < kWarps; ++w) best = better_arg(best, ArgMax{red_f[w], red_i[w]});
       rec[0] = make_float4(best.v, 0.f, -INFINITY, 0.f);
-      rec[1] = make_float4(best.v, __int_as_float(best.i), __int_as_float(ok ? 0 : 1), 0.f);
+      rec[1] = make_float4(best.v, __int_as_float(best.i), 0.f, 0.f);
     }
     return;
   }
@@ -324,7 +301,7 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const VerifyArgs a) {
       s1 += red_f[3 * kWarps + w];
     }
     rec[0] = make_float4(mt, s0, has_draft ? md : -INFINITY, s1);
-    rec[1] = make_float4(0.f, 0.f, __int_as_float(ok ? 0 : 1), 0.f);
+    rec[1] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 }
 
@@ -337,7 +314,7 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const VerifyArgs a) {
 // harmless for the maxima, and left out of the sums.  Each warp takes the
 // maxima of its lanes' vectors, sums exp2(x*c - fl(m_w*c)) against its own
 // maxima m_w, and thread 0 folds the eight warps' (max, sum) pairs into the
-// chunk record (the same record as the staged form).
+// chunk record (the same record as the shared-memory form).
 // ---------------------------------------------------------------------------
 namespace {
 
@@ -359,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, reg_min_blocks(kNV)) stream_reg_kern
   constexpr int kVec = Elem<E>::kVec;
   __shared__ float red_f[4 * kWarps];
   __shared__ int red_i[kWarps];
-  // ordering with the previous kernel: as in the staged form
+  // ordering with the previous kernel: as in the shared-memory form
   if (a.first || (blockIdx.x | blockIdx.y | blockIdx.z) == 0) griddep_wait();
   griddep_launch_dependents();
 
@@ -538,7 +515,7 @@ __device__ __forceinline__ void warp_draw_row(const VerifyArgs& a, int b, int n,
   if (lane == 0) {
     if (d.elem < 0 || !(rp.total > 0.0)) {
       write_error(a, b);
-      atomicOr(a.status, 1 << SSD_ERR_TIMEOUT);
+      atomicOr(a.status, 1 << SSD_ERR_DRAW);
     } else {
       if (a.stats) {
         float* st = a.stats + pi_idx * SSD_NSTAT_VERIFY;
@@ -560,7 +537,7 @@ __global__ void __launch_bounds__(kT2, 8) sample_kernel(const VerifyArgs a) {
   __shared__ UnitStat ust[SSD_MAX_GAMMA + 1];
   __shared__ int tok_x[SSD_MAX_GAMMA];
   __shared__ float tok_t[SSD_MAX_GAMMA], tok_d[SSD_MAX_GAMMA];
-  __shared__ int sh_n, sh_bad;
+  __shared__ int sh_n, sh_bad, sh_sag_bad;
   __shared__ float sh_uacc[SSD_MAX_GAMMA + 1], sh_ures[SSD_MAX_GAMMA + 1];
   extern __shared__ float s_pieces[];  // [kW2][NP]: the last warp's copy of its row's piece sums
 
@@ -645,15 +622,13 @@ __global__ void __launch_bounds__(kT2, 8) sample_kernel(const VerifyArgs a) {
       if (u > g) break;
       MaxSum t{-INFINITY, 0.f}, d{-INFINITY, 0.f};
       ArgMax am{-INFINITY, -1};
-      int err = 0;
       if (lane < NC) {
         t = MaxSum{r0[j].x, r0[j].y};
         d = MaxSum{r0[j].z, r0[j].w};
         if (greedy) am = ArgMax{r1[j].x, __float_as_int(r1[j].y)};
-        err = __float_as_int(r1[j].z);
       }
-      butterfly_stats(t, d, am, err, cc);
-      if (lane == 0) ust[u] = UnitStat{t.m, t.s, d.m, d.s, am.v, am.i, err};
+      butterfly_stats(t, d, am, cc);
+      if (lane == 0) ust[u] = UnitStat{t.m, t.s, d.m, d.s, am.v, am.i};
     }
   }
   __syncthreads();
@@ -691,7 +666,7 @@ __global__ void __launch_bounds__(kT2, 8) sample_kernel(const VerifyArgs a) {
           const float r = Sw > 0.0 ? static_cast<float>(fmaxf(fmaf(-(s.ts / s.ds), ed, et), 0.f) / Sw) : q;
           const float ps = sqrtf(ed / s.ds * fmaxf(r, 1e-8f)) / zs;
           if (ps > 0.f) ratio_acc = fminf(1.f, q / ps);
-          if (isnan(Sw) || !(zs > 0.f)) sag_bad = 1;  // the unit's Saguaro passes failed
+          if (!(zs > 0.f)) sag_bad = 1;  // no Saguaro weight: nothing to verify against
         }
         acc = uacc < ratio_acc;
       } else {
@@ -708,7 +683,8 @@ __global__ void __launch_bounds__(kT2, 8) sample_kernel(const VerifyArgs a) {
     const int n = rej ? __ffs(rej) - 1 : g;
     if (lane == 0) sh_n = n;
     if constexpr (kSag) {
-      if (__any_sync(0xFFFFFFFFu, sag_bad) && lane == 0) ust[0].err = 1;
+      const int any_bad = __any_sync(0xFFFFFFFFu, sag_bad);
+      if (lane == 0) sh_sag_bad = any_bad;
     }
     if (a.stats && c == 0 && lane == pi) {
       float* st = a.stats + (static_cast<size_t>(b) * W + pi) * SSD_NSTAT_VERIFY;
@@ -731,13 +707,12 @@ __global__ void __launch_bounds__(kT2, 8) sample_kernel(const VerifyArgs a) {
   }
   __syncthreads();
   const int n = sh_n;
-  int err_any = 0;
-  for (int u = 0; u <= g; ++u) err_any |= ust[u].err;
+  const bool err_any = kSag && sh_sag_bad;
   if (greedy || err_any) {
     if (pi == 0 && c == 0 && tid == 0) {
       if (err_any) {
         write_error(a, b);
-        atomicOr(a.status, 1 << SSD_ERR_TIMEOUT);
+        atomicOr(a.status, 1 << SSD_ERR_DRAW);
       } else {
         write_outputs(a, b, n, ust[n].ai, tok_x);
       }
@@ -781,7 +756,7 @@ __global__ void __launch_bounds__(kT2, 8) sample_kernel(const VerifyArgs a) {
   const float ures = sh_ures[pos];
   const E* trow = static_cast<const E*>(a.target) + (static_cast<size_t>(b) * W + pos) * V;
   const E* drow = residual ? static_cast<const E*>(a.draft) + (static_cast<size_t>(b) * a.gmax + pos) * V : nullptr;
-  const bool aligned = geo.bulk != 0;
+  const bool aligned = geo.aligned != 0;
   const size_t pi_idx = static_cast<size_t>(b) * W + pi;
   float* psum = a.psum + pi_idx * NP;
 
@@ -1011,7 +986,7 @@ __global__ void __launch_bounds__(256) small_verify_kernel(const VerifyArgs a) {
   if (lane == 0) {
     if (last < 0) {
       write_error(a, b);
-      atomicOr(a.status, 1 << SSD_ERR_TIMEOUT);
+      atomicOr(a.status, 1 << SSD_ERR_DRAW);
     } else {
       write_outputs(a, b, n, last, tok_x);
     }
@@ -1057,13 +1032,9 @@ cudaError_t launch_uniforms(uint64_t seed, int B, int W, float* out, cudaStream_
 namespace {
 
 // The register form takes aligned rows whose chunks hold at most kRegVecs
-// vectors per thread (SSDV_STREAM=staged selects the staged form).
+// vectors per thread.
 bool use_register_stream(const ChunkGeometry& geo, int vec) {
-  static const bool staged = [] {
-    const char* s = getenv("SSDV_STREAM");
-    return s && strcmp(s, "staged") == 0;
-  }();
-  return !staged && geo.bulk && geo.chunk <= kRegVecs * kThreads * vec;
+  return geo.aligned && geo.chunk <= kRegVecs * kThreads * vec;
 }
 
 // cudaFuncSetAttribute once per (kernel, size) on the current device.

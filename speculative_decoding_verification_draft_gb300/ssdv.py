@@ -27,7 +27,7 @@ MAX_TOPK = 8
 STATUS_NAMES = {
     0: "SSD_OK", 1: "SSD_ERR_NULL", 2: "SSD_ERR_SHAPE", 3: "SSD_ERR_DTYPE", 4: "SSD_ERR_ALIGN",
     5: "SSD_ERR_TOKEN_RANGE", 6: "SSD_ERR_TEMPERATURE", 7: "SSD_ERR_CUDA", 8: "SSD_ERR_UNSUPPORTED",
-    9: "SSD_ERR_WORKSPACE", 10: "SSD_ERR_GAMMA", 11: "SSD_ERR_TIMEOUT",
+    9: "SSD_ERR_WORKSPACE", 10: "SSD_ERR_GAMMA", 11: "SSD_ERR_DRAW",
 }
 
 
