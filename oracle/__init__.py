@@ -76,6 +76,9 @@ def _declare(lib):
     lib.orc_saguaro_position.argtypes = [c_int, P, P, c_double, P, P, P, P, P]
     lib.orc_saguaro_position.restype = None
     lib.orc_saguaro_batch.restype = c_int
+    lib.orc_draw_row.argtypes = [c_int, c_int, P, P, c_double, c_int, c_double, P, c_int, c_int, c_double,
+                                 P, P, P]
+    lib.orc_draw_row.restype = c_int
     lib.orc_mutant_id.argtypes = []
     lib.orc_mutant_id.restype = c_int
     return lib
@@ -206,6 +209,23 @@ class Oracle:
                                         _ptr(ur), float(band), _ptr(out), ctypes.byref(fp),
                                         ctypes.byref(fk), _ptr(st))
         return dict(n=n, out=out, flag_pos=fp.value, flag_kind=fk.value, stats=st)
+
+    def draw_row(self, xt, xd, T, tok, row: int, token: int, band: float = FLAG_BAND, draft_dist: str = "draft",
+                 top_p: float = 1.0):
+        """(lo, hi, flag_mass) of the draw row `row` of one request (its residual,
+        or q_gamma at row == gamma): token's normalised CDF interval [lo, hi) and
+        the measure of the uniforms whose draw from this row is flagged."""
+        xt = np.ascontiguousarray(xt, dtype=np.float64)
+        g, V = xt.shape[0] - 1, xt.shape[1]
+        xd = np.ascontiguousarray(xd, dtype=np.float64).reshape(g, V) if g > 0 else np.zeros((1, V))
+        tok = np.ascontiguousarray(tok, dtype=np.int32).reshape(g) if g > 0 else np.zeros(1, np.int32)
+        lo, hi, fm = ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
+        rc = self.lib.orc_draw_row(g, V, _ptr(xt), _ptr(xd), float(T), _dist(draft_dist), float(top_p), _ptr(tok),
+                                   int(row), int(token), float(band), ctypes.byref(lo), ctypes.byref(hi),
+                                   ctypes.byref(fm))
+        if rc != 0:
+            raise ValueError("draw_row: greedy request, or row / token out of range")
+        return lo.value, hi.value, fm.value
 
     def saguaro_request(self, xt, xd, T, k, u_sag, stats: bool = False, band: float = FLAG_BAND,
                         source: str = "residual"):

@@ -349,6 +349,11 @@ static void saguaro_draft_dist(int V, const double* q, double* p, double* r) {
     S += r[v];
   }
   for (int v = 0; v < V; ++v) r[v] = S > 0.0 ? r[v] / S : q[v];
+#if ORC_MUTANT == 15
+  if (S > 0.0)
+    for (int v = 0; v < V; ++v) /* mutant: clamp the unnormalised residual, then normalise */
+      r[v] = (r[v] * S > ORC_SAGUARO_CLAMP ? r[v] * S : ORC_SAGUARO_CLAMP) / S;
+#endif
   double Z = 0.0;
   for (int v = 0; v < V; ++v) {
     double rc = r[v] > ORC_SAGUARO_CLAMP ? r[v] : ORC_SAGUARO_CLAMP;
@@ -560,6 +565,65 @@ int orc_verify_request(int g, int V, const double* xt, const double* xd, double 
 }
 
 /* ------------------------------------------------------------------------- */
+/* The draw row of one request, for checking a draw that another             */
+/* implementation made differently ([SD] §3: the correction comes from the   */
+/* residual of the rejected position, the bonus from the target row after   */
+/* the last draft token).  Row `row` < g: the residual (q - p)+ of that      */
+/* position (q when its mass S <= 0), under the same readings as             */
+/* orc_verify_request (Saguaro sampling, top-p); row == g: q_g.              */
+/*                                                                            */
+/* *lo, *hi: the normalised CDF interval [C_{t-1}/S, C_t/S) of token t, the  */
+/* running sums taken in index order as in orc_choice_edges.                 */
+/* *flag_mass: the measure of the uniforms whose draw from this row is       */
+/* flagged -- a uniform in token k's interval is flagged when it lies within */
+/* `band` of either end, which has measure min(w_k, 2 band) for the          */
+/* normalised weight w_k -- summed over k; 1 when a residual row's mass S is */
+/* below `band` (every draw there is flagged).                               */
+/* Returns 0, or -1 for a greedy request (T == 0), a bad row or token.       */
+/* ------------------------------------------------------------------------- */
+int orc_draw_row(int g, int V, const double* xt, const double* xd, double T, int sag, double top_p,
+                 const int32_t* tok, int row, int t, double band, double* lo, double* hi, double* flag_mass) {
+  if (!(T > 0.0) || row < 0 || row > g || t < 0 || t >= V) return -1;
+  double* q = (double*)malloc(sizeof(double) * (size_t)V);
+  double* p = (double*)malloc(sizeof(double) * (size_t)V);
+  double* r = (double*)malloc(sizeof(double) * (size_t)V);
+  int ambig = 0;
+  double S = 1.0;
+  const double* w;
+  if (row < g) {
+    int x = tok[row] >= 0 && tok[row] < V ? tok[row] : 0;
+    orc_position P = position_quantities(V, xt + (size_t)row * V, xd + (size_t)row * V, T, x, q, p, r, sag, top_p,
+                                         band, &ambig);
+    S = P.S;
+    if (!(P.S > 0.0))
+      for (int v = 0; v < V; ++v) r[v] = q[v];
+    w = r;
+  } else {
+    orc_softmax(xt + (size_t)g * V, V, T, q, NULL, NULL);
+    orc_nucleus(xt + (size_t)g * V, q, V, top_p, band, &ambig);
+    w = q;
+  }
+  double total = 0.0;
+  for (int v = 0; v < V; ++v) total += w[v];
+  double acc = 0.0, mass = 0.0;
+  for (int v = 0; v < V; ++v) {
+    double before = acc;
+    acc += w[v];
+    if (v == t) {
+      *lo = before / total;
+      *hi = acc / total;
+    }
+    double wk = w[v] / total;
+    mass += wk < 2.0 * band ? wk : 2.0 * band;
+  }
+  *flag_mass = (row < g && S < band) ? 1.0 : mass;
+  free(q);
+  free(p);
+  free(r);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------- */
 /* Saguaro pre-speculation for one request ([SAG] §3.1, §3.2, with the        */
 /* residual of [SD] §3).  For each acceptance length j = 0..g:                */
 /*   r_j = (q_j - p_j)+ / S_j   (j < g; r_j = q_j when S_j <= 0),              */
@@ -609,6 +673,10 @@ int orc_saguaro_request(int g, int V, const double* xt, const double* xd, double
       }
       if (S > 0.0) {
         for (int v = 0; v < V; ++v) r[v] /= S;
+#if ORC_MUTANT == 15
+        for (int v = 0; v < V; ++v) /* mutant: clamp the unnormalised residual, then normalise */
+          r[v] = (r[v] * S > ORC_SAGUARO_CLAMP ? r[v] * S : ORC_SAGUARO_CLAMP) / S;
+#endif
       } else {
         for (int v = 0; v < V; ++v) r[v] = q[v];
       }
@@ -700,6 +768,10 @@ void orc_saguaro_position(int V, const double* xt, const double* xd, double T, d
     }
     if (S > 0.0) {
       for (int v = 0; v < V; ++v) r[v] /= S;
+#if ORC_MUTANT == 15
+      for (int v = 0; v < V; ++v) /* mutant: clamp the unnormalised residual, then normalise */
+        r[v] = (r[v] * S > ORC_SAGUARO_CLAMP ? r[v] * S : ORC_SAGUARO_CLAMP) / S;
+#endif
     } else {
       for (int v = 0; v < V; ++v) r[v] = q[v];
     }

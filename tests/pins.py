@@ -637,11 +637,10 @@ def pin_saguaro_draft_lossless(o):
     for g in (1, 2):
         xt = rng.normal(0, 1.0, (g + 1, V))
         xd = rng.normal(0, 1.0, (g, V))
-        q0, p0 = softmax(xt[0] / T), softmax(xd[0] / T)
-        r = np.maximum(q0 - p0, 0.0)
-        r /= r.sum()
-        s = np.sqrt(p0 * np.maximum(r, 1e-8))
-        psag = s / s.sum()
+        q0 = softmax(xt[0] / T)
+        # the Saguaro distribution of position 0, as the oracle's Saguaro step
+        # defines it (its clamp order is pinned by pin_saguaro_clamp_order)
+        _, psag = o.saguaro_position(xt[0], xd[0], T)
         marg, marg_plain = np.zeros(V), np.zeros(V)
         for x0 in range(V):
             tok = [x0] + [int(np.argmax(xd[i])) for i in range(1, g)]
@@ -698,11 +697,90 @@ def pin_top_p(o):
         assert list(a["out"]) == list(b["out"])
 
 
+def pin_saguaro_clamp_order(o):
+    """The SSD notes (section 3.2) clamp the residual once it is a probability
+    vector -- r = (q - p)+ / S, then max(r, 1e-8) -- and renormalise the mix.
+    A row whose residual has one positive entry makes the order visible: with
+    a uniform draft p = 1/V and q moving mass S from every other token onto
+    token 0, r = (1, 0, ..., 0) whatever S is, so by hand
+      p_saguaro(0) = sqrt(1/V) / (sqrt(1/V) + (V - 1) sqrt(1e-8 / V))
+                   = 1 / (1 + (V - 1) 1e-4),
+    Zs = sqrt(1/V) (1 + (V - 1) 1e-4), and every other token gets 1e-4 of
+    token 0's probability -- the same for every S.  Clamping before the
+    normalisation (max((q - p)+, 1e-8) / S) would give 1 / (1 + (V - 1) 1e-4 /
+    sqrt(S)) instead."""
+    V = 1001
+    want0 = 1.0 / (1.0 + (V - 1) * 1e-4)
+    want_zs = np.sqrt(1.0 / V) * (1.0 + (V - 1) * 1e-4)
+    for S in (0.5, 0.2):
+        q = np.full(V, 1.0 / V - S / (V - 1))
+        q[0] = 1.0 / V + S
+        xt = np.log(np.stack([q, q]))
+        xd = np.zeros((1, V))
+        r, ps, _, _, mass = o.saguaro_position(xt[0], xd[0], 1.0, full=True)
+        assert abs(mass - S) < 1e-12, mass
+        assert r[0] == 1.0 and np.all(r[1:] == 0.0)
+        assert abs(ps[0] / want0 - 1) < 1e-12, (S, ps[0], want0)
+        assert np.allclose(ps[1:], 1e-4 * ps[0], rtol=1e-12, atol=0)
+        res = o.saguaro_request(xt, xd, 1.0, 1, [0.5, 0.5], stats=True)
+        assert res["tokens"][0] == 0
+        assert abs(res["stats"][0, 3] / want_zs - 1) < 1e-12 and abs(res["stats"][0, 4] / want0 - 1) < 1e-12
+        # the law's first step: token 0 owns [0, p_saguaro(0))
+        assert o.saguaro_request(xt, xd, 1.0, 1, [want0 - 1e-9, 0.5])["tokens"][0] == 0
+        assert o.saguaro_request(xt, xd, 1.0, 1, [want0 + 1e-9, 0.5])["tokens"][0] == 1
+
+
+def pin_draw_row(o):
+    """A token's CDF interval in a request's draw row, and the row's flag mass.
+    Closed forms: a uniform row of V tokens gives token t the interval
+    [t/V, (t+1)/V) and flag mass V * min(1/V, 2 band); a residual row of mass
+    below the band flags every draw (mass 1).  Against the pinned decision
+    function: the token the oracle draws for a uniform u owns an interval
+    holding u, the intervals tile [0, 1), and the share of uniforms the
+    oracle flags matches the mass (binomial, 5 sigma)."""
+    z = np.zeros((2, 50))
+    for V, band, fm_want in [(50, 1e-3, 50 * 2e-3), (1000, 1e-3, 1.0)]:
+        xt = np.zeros((2, V))
+        xd = np.zeros((1, V))
+        for t in (0, 7, V - 1):
+            lo, hi, fm = o.draw_row(xt, xd, 1.0, [0], 1, t, band=band)
+            assert abs(lo - t / V) < 1e-14 and abs(hi - (t + 1) / V) < 1e-14
+            assert abs(fm - fm_want) < 1e-12, (V, fm)
+    rng = np.random.Generator(np.random.PCG64(31))
+    xd = rng.normal(0, 1.0, (1, 60))
+    xt = np.stack([xd[0] + 1e-10 * rng.normal(size=60), xd[0]])
+    assert o.draw_row(xt, xd, 1.0, [3], 0, 5)[2] == 1.0
+    V, g = 40, 2
+    xt = rng.normal(0, 1.2, (g + 1, V))
+    xd = rng.normal(0, 1.2, (g, V))
+    p0 = np.exp(xd[0] - xd[0].max())
+    q0 = np.exp(xt[0] - xt[0].max())
+    tok = [int(np.argmax(p0 / p0.sum() - q0 / q0.sum())), 3]  # q(x) < p(x): rejected at u = 1 - 2^-24
+    for u in np.concatenate([rng.random(40), [0.0, 1 - 2**-24]]):
+        out = o.verify_request(xt, xd, 1.0, tok, [1 - 2**-24, 0.5], [u, 0.5, 0.5])["out"]
+        lo, hi, _ = o.draw_row(xt, xd, 1.0, tok, 0, int(out[0]))
+        assert lo <= u < hi, (u, lo, hi)
+        out = o.verify_request(xt, xd, 1.0, tok, [0.0, 0.0], [0.5, 0.5, u])["out"]
+        lo, hi, _ = o.draw_row(xt, xd, 1.0, tok, g, int(out[g]))
+        assert lo <= u < hi, (u, lo, hi)
+    edges = [o.draw_row(xt, xd, 1.0, tok, 0, t)[:2] for t in range(V)]
+    assert edges[0][0] == 0.0 and abs(edges[-1][1] - 1.0) < 1e-12
+    assert all(edges[t][1] == edges[t + 1][0] for t in range(V - 1))
+    band = 4e-3
+    fm = o.draw_row(xt, xd, 1.0, tok, 0, 0, band=band)[2]
+    n, flagged = 4000, 0
+    for u in rng.random(n):
+        r = o.verify_request(xt, xd, 1.0, tok, [1 - 2**-24, 0.5], [u, 0.5, 0.5], band=band)
+        flagged += r["flag_pos"] == 0 and r["flag_kind"] == 1
+    sd = np.sqrt(n * fm * (1 - fm))
+    assert abs(flagged - n * fm) <= 5 * sd + 1, (flagged, n * fm)
+
+
 ALL_PINS = [
     pin_philox_vs_triton, pin_uniform_mapping, pin_uniform_statistics, pin_softmax, pin_argmax,
     pin_topk, pin_choice, pin_toy_closed_forms, pin_losslessness_toy_chain,
     pin_losslessness_random, pin_greedy, pin_low_temperature_limit, pin_expected_tokens,
     pin_toy_kl, pin_saguaro_toy_topk, pin_saguaro_bonus_position,
     pin_saguaro_disjoint_supports, pin_saguaro_equal_distributions, pin_cache_hit_rate, pin_draft_topk,
-    pin_saguaro_draft_lossless, pin_top_p,
+    pin_saguaro_draft_lossless, pin_top_p, pin_saguaro_clamp_order, pin_draw_row,
 ]

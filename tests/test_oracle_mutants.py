@@ -17,7 +17,7 @@ import pins
 BATTERY = [
     pins.pin_softmax, pins.pin_argmax, pins.pin_topk, pins.pin_choice, pins.pin_uniform_mapping,
     pins.pin_greedy, pins.pin_toy_closed_forms, pins.pin_saguaro_bonus_position,
-    pins.pin_saguaro_disjoint_supports, pins.pin_saguaro_equal_distributions,
+    pins.pin_saguaro_disjoint_supports, pins.pin_saguaro_equal_distributions, pins.pin_saguaro_clamp_order,
     pins.pin_low_temperature_limit, pins.pin_losslessness_random, pins.pin_losslessness_toy_chain,
     pins.pin_cache_hit_rate, pins.pin_draft_topk, pins.pin_saguaro_draft_lossless, pins.pin_top_p,
     pins.pin_philox_vs_triton,
@@ -38,6 +38,7 @@ MUTANTS = {
     12: "draft-logit top-k taken from the target row",
     13: "Saguaro-draft verification with the draft's p(x) in the accept test",
     14: "top-p truncating the target but not the draft",
+    15: "Saguaro clamp applied to the residual before it is normalised",
 }
 
 

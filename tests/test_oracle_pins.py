@@ -101,3 +101,11 @@ def test_saguaro_draft_lossless(orc):
 
 def test_top_p(orc):
     pins.pin_top_p(orc)
+
+
+def test_saguaro_clamp_order(orc):
+    pins.pin_saguaro_clamp_order(orc)
+
+
+def test_draw_row(orc):
+    pins.pin_draw_row(orc)
