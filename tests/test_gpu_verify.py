@@ -81,6 +81,26 @@ def test_zipf_config_full(ssdv, zipf64):
         gc.assert_verify_parity(out, n, ref, 128256, f"zipf seed {seed}")
 
 
+def test_flag_rate_matches_band(ssdv, zipf64):
+    """Sixteen seeds of the bench workload, every request checked (flagged
+    ones draw by draw), and the number of flagged requests against the rate
+    the 1e-6 band implies at this vocabulary: each correction / bonus draw is
+    flagged with the flag mass of its row (a few per cent here -- the band
+    covers the whole interval of every token below 2e-6 of mass -- so the
+    method's 1e-4 budget is out of reach at V = 128256 and is reported, not
+    asserted), each accept draw with probability 2e-6 at most."""
+    flagged, pred, var, draws = 0, 0.0, 0.0, 0
+    for seed in range(40, 56):
+        out, n = run_verify(ssdv, zipf64, seed)
+        ref = gc.verify_oracle(zipf64, seed)
+        f, d = gc.assert_verify_parity(out, n, ref, 128256, f"zipf seed {seed}")
+        p, sd = gc.flag_rate_prediction(ref)
+        flagged, pred, var, draws = flagged + f, pred + p, var + sd * sd, draws + d
+    print(f"\nflagged requests {flagged} of {16 * 64} ({flagged / draws:.2e} of {draws} draws); "
+          f"predicted from the band {pred:.1f} +- {np.sqrt(var):.1f}")
+    assert abs(flagged - pred) <= 5 * np.sqrt(var) + 2
+
+
 def test_zipf_rowstats(ssdv, zipf64):
     """Softmax log-sums, q(x), p(x), residual mass and accept probability."""
     b = zipf64.to("cuda")
@@ -196,6 +216,17 @@ def test_ragged_full_config_sampled(ssdv):
     assert np.all((n >= 0) & (n <= gam))
     for r in range(512):
         assert np.all(out[r, : n[r] + 1] >= 0) and np.all(out[r, n[r] + 1:] == -1)
+
+
+def test_ragged_full_config_all_requests(ssdv):
+    """B=512, gamma 1..8, V 128256 bf16, half greedy (the ragged batch
+    workload): every request against the oracle, on two seeds."""
+    batch = wl.ragged_batch(512, 8, 128256, seed=4)
+    b = batch.to("cuda")
+    for seed in (4, 5):
+        out, n = ssdv.verify_ragged(b.target, b.draft, b.draft_tokens, b.gamma, b.temperature, seed)
+        ref = gc.verify_oracle(batch, seed)
+        gc.assert_verify_parity(out, n, ref, 128256, f"ragged workload, all 512 requests, seed {seed}")
 
 
 def test_padded_and_bad_requests(ssdv):
