@@ -263,37 +263,29 @@ __device__ __forceinline__ void write_topk(const SagArgs& a, size_t u, double to
 }  // namespace
 
 // ---------------------------------------------------------------------------
-// Kernel 2: residual sums and top-k.  Grid (warp groups, j, request).
+// The residual pass of one unit, warp by warp: residual weights (target
+// weights at j = gamma), their piece sums and the warps' top-8 candidates;
+// the last warp of the unit fixes S_j, writes the row statistics and merges
+// the top-k.  s4 = the unit's row statistics (target max, sum, draft max,
+// sum).  Returns true in (every lane of) that last warp.
 // ---------------------------------------------------------------------------
 template <typename E, int kKey>
-__global__ void __launch_bounds__(kS, resid_min_blocks<E, kKey>()) residual_kernel(const SagArgs a) {
-  extern __shared__ __align__(16) uint8_t dyn_smem[];
-  __shared__ float4 sh_stats;
-  griddep_launch_dependents();  // the mix kernel may become resident (it waits for this grid)
-  const int W = a.g + 1, j = blockIdx.y, b = blockIdx.z;
+__device__ __forceinline__ bool residual_unit(const SagArgs& a, int b, int j, int wi, uint8_t* dyn_smem,
+                                              float4 s4) {
+  const int W = a.g + 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int wi = blockIdx.x * kSW + warp;
   const size_t u = static_cast<size_t>(b) * W + j;
   const bool bonus = (j == a.g);
   const float c = kLog2e / a.temperature;
-  griddep_wait();  // the streaming kernel's records are complete and visible
-  if (warp == 0) {
-    MaxSum t, d;
-    unit_stats(a, u, c, &t, &d);
-    if (lane == 0) sh_stats = make_float4(t.m, t.s, d.m, d.s);
-  }
-  __syncthreads();
-  if (wi >= a.npw) return;
-  const float4 s4 = sh_stats;
   const int V = a.geo.V;
   const E* trow = static_cast<const E*>(a.target) + u * V;
   const E* drow = bonus ? nullptr : static_cast<const E*>(a.draft) + (static_cast<size_t>(b) * a.g + j) * V;
   const PassAW<E> wf{c, scaled_max(s4.x, c), bonus ? 0.f : scaled_max(s4.z, c), bonus ? 0.f : s4.y / s4.w,
                      bonus ? 1 : 0};
-  if (!unit_pieces<E, PassAW<E>, kKey>(a, u, wi, trow, drow, wf, a.psum2, a.ticket2)) return;
+  if (!unit_pieces<E, PassAW<E>, kKey>(a, u, wi, trow, drow, wf, a.psum2, a.ticket2)) return false;
 
   // The last warp: S_j, and the top-k unless the residual is empty (then the
-  // mix kernel takes the top-k of q_j).
+  // mix pass takes the top-k of q_j).
   RowPieces rp;
   float* s_pieces = reinterpret_cast<float*>(dyn_smem) + warp * a.geo.npiece;
   rp.load(a.psum2 + u * a.geo.npiece, a.geo.npiece, s_pieces);
@@ -319,26 +311,25 @@ __global__ void __launch_bounds__(kS, resid_min_blocks<E, kKey>()) residual_kern
     const float mc = bonus ? scaled_max(s4.x, c) : scaled_max(s4.z, c);
     write_topk(a, u, S, s_cv, s_ci, st, logit_keys, c, mc, bonus ? s4.y : s4.w);
   }
+  return true;
 }
 
 // ---------------------------------------------------------------------------
-// Kernel 3: the Saguaro mix and its draw.  Grid as kernel 2.
+// The mix pass of one unit, warp by warp: the Saguaro weights
+// sqrt(p_D max(r, 1e-8)) and their piece sums; the last warp of the unit
+// keeps Zs, draws the token (and, when S_j = 0, merges the top-k of q_j).
+// Reads the residual pass's row statistics and S_j of the unit.  Returns true
+// in (every lane of) that last warp.
 // ---------------------------------------------------------------------------
 template <typename E>
-__global__ void __launch_bounds__(kS, mix_min_blocks<E>()) mix_kernel(const SagArgs a) {
-  extern __shared__ __align__(16) uint8_t dyn_smem[];
-  griddep_launch_dependents();  // the next kernel may become resident (it waits for this grid)
-  const int W = a.g + 1, j = blockIdx.y, b = blockIdx.z;
+__device__ __forceinline__ bool mix_unit(const SagArgs& a, int b, int j, int wi, uint8_t* dyn_smem) {
+  const int W = a.g + 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int wi = blockIdx.x * kSW + warp;
-  if (wi >= a.npw) return;
   const size_t u = static_cast<size_t>(b) * W + j;
   const bool bonus = (j == a.g);
   const float c = kLog2e / a.temperature;
-  griddep_wait();  // the residual kernel's sums are complete and visible
   const float4 s4 = __ldcg(a.rowstat + u);
   const double S = __ldcg(a.rowsum + u);
-  if (isnan(S)) return;  // the unit failed; the residual kernel wrote its -1 outputs
   const bool target_only = bonus || !(S > 0.0);  // r = q_j: the bonus position or an empty residual
   const double sum_a = (bonus || S > 0.0) ? S : static_cast<double>(s4.y);
   const int V = a.geo.V;
@@ -350,15 +341,14 @@ __global__ void __launch_bounds__(kS, mix_min_blocks<E>()) mix_kernel(const SagA
   // empty residual with the residual as the top-k source: the top-k of q_j
   // is taken here
   const bool fallback = a.k > 0 && a.topk_src == 0 && !bonus && !(S > 0.0);
-  const bool last = unit_pieces<E, MixW<E>, kKeyNone>(a, u, wi, trow, drow, mw, a.psum3, a.ticket3);
-  if (!last) return;
+  if (!unit_pieces<E, MixW<E>, kKeyNone>(a, u, wi, trow, drow, mw, a.psum3, a.ticket3)) return false;
 
   // The last warp: Zs, the draw, and (empty residual) the top-k of q_j.
   RowPieces rp;
   float* s_pieces = reinterpret_cast<float*>(dyn_smem) + warp * a.geo.npiece;
   rp.load(a.psum3 + u * a.geo.npiece, a.geo.npiece, s_pieces);
   if (a.zsum && lane == 0) a.zsum[u] = static_cast<float>(rp.total);
-  if (!a.saguaro_tokens) return;  // the normaliser is all a later kernel needs
+  if (!a.saguaro_tokens) return true;  // the normaliser is all a later kernel needs
   const float u_sag = unit_draws(a.seed, a.req_base + b, j).saguaro;
   const RowDraw d = warp_locate_row<E>(rp, u_sag, trow, drow, V, a.geo.aligned != 0, mw);
   float* st = a.stats ? a.stats + u * SSD_NSTAT_SAGUARO : nullptr;
@@ -407,6 +397,49 @@ __global__ void __launch_bounds__(kS, mix_min_blocks<E>()) mix_kernel(const SagA
       }
     }
   }
+  return true;
+}
+
+// The row statistics of unit u into sh (warp 0), visible to the CTA after the
+// barrier.
+__device__ __forceinline__ void cta_unit_stats(const SagArgs& a, size_t u, float4* sh) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == 0) {
+    MaxSum t, d;
+    unit_stats(a, u, kLog2e / a.temperature, &t, &d);
+    if (lane == 0) *sh = make_float4(t.m, t.s, d.m, d.s);
+  }
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// Kernel 2: residual sums and top-k.  Grid (warp groups, j, request).
+// ---------------------------------------------------------------------------
+template <typename E, int kKey>
+__global__ void __launch_bounds__(kS, resid_min_blocks<E, kKey>()) residual_kernel(const SagArgs a) {
+  extern __shared__ __align__(16) uint8_t dyn_smem[];
+  __shared__ float4 sh_stats;
+  griddep_launch_dependents();  // the mix kernel may become resident (it waits for this grid)
+  const int W = a.g + 1, j = blockIdx.y, b = blockIdx.z;
+  const int wi = blockIdx.x * kSW + (threadIdx.x >> 5);
+  griddep_wait();  // the streaming kernel's records are complete and visible
+  cta_unit_stats(a, static_cast<size_t>(b) * W + j, &sh_stats);
+  if (wi >= a.npw) return;
+  residual_unit<E, kKey>(a, b, j, wi, dyn_smem, sh_stats);
+}
+
+// ---------------------------------------------------------------------------
+// Kernel 3: the Saguaro mix and its draw.  Grid as kernel 2.
+// ---------------------------------------------------------------------------
+template <typename E>
+__global__ void __launch_bounds__(kS, mix_min_blocks<E>()) mix_kernel(const SagArgs a) {
+  extern __shared__ __align__(16) uint8_t dyn_smem[];
+  griddep_launch_dependents();  // the next kernel may become resident (it waits for this grid)
+  const int j = blockIdx.y, b = blockIdx.z;
+  const int wi = blockIdx.x * kSW + (threadIdx.x >> 5);
+  if (wi >= a.npw) return;
+  griddep_wait();  // the residual kernel's sums are complete and visible
+  mix_unit<E>(a, b, j, wi, dyn_smem);
 }
 
 template __global__ void residual_kernel<uint16_t, kKeyWeight>(const SagArgs);
