@@ -276,7 +276,6 @@ ssd_status verify_common(const void* target, const void* draft, ssd_dtype dtype,
     t.temps = temps;
     t.temp_scalar = temp_scalar;
     t.top_p = top_p;
-    t.alu = env_int("SSDV_TOPP_ALU", 0);
     t.part = a.part;
     t.geo = geo;
     t.nlevels = levels;

@@ -102,7 +102,6 @@ struct TopPArgs {
   const float4* part;   // the streaming kernel's records
   ChunkGeometry geo;
   int level, nlevels, shift, bits;
-  int alu;                     // 1: bins and fixed-point masses computed without XU conversions
   unsigned long long* hist;    // [B, gmax+1, 2, 1 << bits]: this level's histograms (zeroed by the caller)
   uint32_t* bstar;             // [B, gmax+1, 2]: the mass bin holding the threshold (level 0's result)
   uint32_t* prefix;            // [B, gmax+1, 2]: the key digits fixed so far

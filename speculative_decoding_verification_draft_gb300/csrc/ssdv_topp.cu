@@ -49,26 +49,6 @@ __device__ __forceinline__ unsigned long long mass_fixed(float e) {
   return (static_cast<unsigned long long>(hi) << 32) + __float2uint_rn(r * 4294967296.f);
 }
 
-// The same fixed-point mass without the XU pipe: e * 2^40 is exact in fp32
-// (a power-of-two scaling), and its integer part is read off the float's
-// exponent and mantissa with integer shifts (truncation, not rounding: every
-// level and the select use this one function).
-__device__ __forceinline__ unsigned long long mass_fixed_alu(float e) {
-  const uint32_t bits = __float_as_uint(e * 1099511627776.f);
-  const int ex = static_cast<int>(bits >> 23) - 127;  // f in [2^ex, 2^(ex+1))
-  const uint32_t mant = (bits & 0x7FFFFFu) | 0x800000u;
-  if (ex < 0) return 0ull;
-  return ex >= 23 ? static_cast<unsigned long long>(mant) << (ex - 23) : static_cast<unsigned long long>(mant >> (23 - ex));
-}
-
-// floor(8 d) clamped to [0, 255] with one round-down add on the FMA pipe:
-// for 0 <= v < 2^23, v + 2^23 rounded down is 2^23 + floor(v), whose low
-// mantissa bits are floor(v).
-__device__ __forceinline__ int mass_bin_alu(float d) {
-  const float v = fminf(fmaxf(d * 8.f, 0.f), 255.5f);
-  return static_cast<int>(__float_as_uint(__fadd_rd(v, 8388608.f)) - 0x4B000000u);
-}
-
 // Row slot rs = (b * W + i) * 2 + which (0 target, 1 draft): whether it is a
 // row of a sampled request that verification reads.
 __device__ __forceinline__ bool slot_active(const TopPArgs& a, int b, int i, int which, float* T_out) {
@@ -158,9 +138,9 @@ struct MassBins {
   __device__ __forceinline__ void operator()(float x) const {
     if (x == -INFINITY) return;  // no mass
     const float d = __fmaf_rn(-x, cc, mc);  // fl(m c) - x c, one rounding
-    const int bin = a->alu ? mass_bin_alu(d) : min(255, max(0, __float2int_rd(d * 8.f)));
+    const int bin = min(255, max(0, __float2int_rd(d * 8.f)));
     const int digit = 255 - bin;  // larger digit, larger mass
-    const unsigned long long mass = a->alu ? mass_fixed_alu(fast_exp2(-d)) : mass_fixed(fast_exp2(-d));
+    const unsigned long long mass = mass_fixed(fast_exp2(-d));
     const uint32_t lo32 = static_cast<uint32_t>(mass), hi32 = static_cast<uint32_t>(mass >> 32);
     const uint32_t old = lo32 ? atomicAdd(&hist[digit], lo32) : 0u;
     const uint32_t hi_add = hi32 + (old + lo32 < old ? 1u : 0u);  // the carry out of the low word
@@ -207,13 +187,13 @@ struct DigitMasses {
   __device__ __forceinline__ void operator()(float x) const {
     if (x == -INFINITY || x < xlo || x > xhi) return;  // no mass, or certainly another bin
     const float d = __fmaf_rn(-x, cc, mc);
-    const int bin = a->alu ? mass_bin_alu(d) : min(255, max(0, __float2int_rd(d * 8.f)));
+    const int bin = min(255, max(0, __float2int_rd(d * 8.f)));
     if (static_cast<uint32_t>(bin) != bstar) return;
     const uint32_t k = logit_key(x);
     if (a->level >= 2 && (k >> hi_shift) != prefix) return;
     const int digit = direct ? static_cast<int>((k >> 16) - base16)
                              : static_cast<int>((k >> a->shift) & static_cast<uint32_t>(nb - 1));
-    const unsigned long long mass = a->alu ? mass_fixed_alu(fast_exp2(-d)) : mass_fixed(fast_exp2(-d));
+    const unsigned long long mass = mass_fixed(fast_exp2(-d));
     if (mass) atomicAdd(&hist[digit], mass);
   }
 };
