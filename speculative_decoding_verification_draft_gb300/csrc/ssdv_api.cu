@@ -247,6 +247,7 @@ ssd_status verify_common(const void* target, const void* draft, ssd_dtype dtype,
   a.sag_Zs = nullptr;
   a.tp_th = nullptr;
   a.tp_z = nullptr;
+  a.pieces_ready = 0;
   a.geo = geo;
   if (use_topp) {
     // The streaming kernel, the radix-select levels of every row's nucleus
@@ -575,20 +576,22 @@ static ssd_status saguaro_common(const void* target, const void* draft, ssd_dtyp
     v.debug = 0;
     v.first = b0 == 0 ? 1 : 0;
     v.geo = geo;
-    cudaError_t e;
+    // The streaming kernel: one read of every row, whose records serve
+    // verification and Saguaro alike.
+    cudaError_t e = launch_stream(v, es, smem, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "saguaro streaming launch");
     if (fused) {
-      // the verification pair: its streaming records serve the Saguaro
-      // kernels too; its sampling kernel returns the counters it used to zero
+      // Verification draws after the residual pass, from its piece sums: for
+      // every acceptance length j they are the sums, in the same order and
+      // arithmetic, of the very weights the verification's draw at n = j
+      // uses ((q_j - p_j)+ scaled by Z_t, or q_gamma at the bonus), so the
+      // draw rows are not read again.
       v.draft_tokens = fv.draft_tokens ? fv.draft_tokens + static_cast<size_t>(b0) * g : nullptr;
       v.out_tokens = fv.out_tokens + u0;
       v.n_accepted = fv.n_accepted + b0;
       v.psum = reinterpret_cast<float*>(ws + L.psum2) + u0 * geo.npiece;
-      v.geo.ppw = env_int("SSDV_PPW", 2) < 1 ? 1 : env_int("SSDV_PPW", 2);
-      e = launch_verify(v, es, smem, static_cast<cudaStream_t>(stream));
-    } else {
-      e = launch_stream(v, es, smem, static_cast<cudaStream_t>(stream));
+      v.pieces_ready = 1;
     }
-    if (e != cudaSuccess) return cuda_fail(e, "saguaro streaming launch");
     SagArgs a;
     a.target = t;
     a.draft = d;
@@ -616,7 +619,13 @@ static ssd_status saguaro_common(const void* target, const void* draft, ssd_dtyp
     a.ticket3 = reinterpret_cast<int32_t*>(ws + L.ticket3) + u0;
     a.status = status;
     a.geo = geo;
-    e = launch_saguaro(a, es, static_cast<cudaStream_t>(stream));
+    if (fused) {
+      e = launch_saguaro(a, es, static_cast<cudaStream_t>(stream), kSagResidual);
+      if (e == cudaSuccess) e = launch_sample(v, es, static_cast<cudaStream_t>(stream));
+      if (e == cudaSuccess) e = launch_saguaro(a, es, static_cast<cudaStream_t>(stream), kSagMix);
+    } else {
+      e = launch_saguaro(a, es, static_cast<cudaStream_t>(stream));
+    }
     if (e != cudaSuccess) return cuda_fail(e, "saguaro launch");
   }
   if (fused && (fv.hit || fv.n_hits)) {

@@ -52,6 +52,9 @@ struct VerifyArgs {
                                // target (slot 0) and draft (slot 1) row; given, both distributions are
                                // truncated to their nuclei
   const float* tp_z;           // [B, gmax+1, 2]: the nuclei's masses, in units of exp2(x c - fl(m c))
+  int pieces_ready;            // 1: psum already holds the piece sums of every position's draw row,
+                               // [B, gmax+1, npiece] (the Saguaro residual pass's): one CTA per request
+                               // takes the decision and draws, with no pass over the rows
   int first;                   // 1: every streaming CTA waits for the previous kernel (the first
                                // segment of a call); 0: only the first CTA waits (a later segment, or
                                // a pipelined call)
@@ -135,7 +138,9 @@ cudaError_t launch_sample(const VerifyArgs& a, int esize, cudaStream_t stream);
 // The streaming kernel alone (Saguaro's first kernel).
 cudaError_t launch_stream(const VerifyArgs& a, int esize, int smem_bytes, cudaStream_t stream);
 // Saguaro's residual and mix kernels (each waits for its predecessor).
-cudaError_t launch_saguaro(const SagArgs& a, int esize, cudaStream_t stream);
+// passes: 1 the residual kernel, 2 the mix kernel, 3 both.
+constexpr int kSagResidual = 1, kSagMix = 2;
+cudaError_t launch_saguaro(const SagArgs& a, int esize, cudaStream_t stream, int passes = kSagResidual | kSagMix);
 
 // The cache check: hit[b] = the slot of bonus_topk[b, n_b, :] holding
 // out_tokens[b, n_b] (-1 if none), n_hits[0] = the number of hits (either

@@ -454,7 +454,7 @@ template __global__ void mix_kernel<float>(const SagArgs);
 namespace {
 
 template <typename E>
-cudaError_t launch_saguaro_t(const SagArgs& a, cudaStream_t stream) {
+cudaError_t launch_saguaro_t(const SagArgs& a, cudaStream_t stream, int passes) {
   const int smem = static_cast<int>(sizeof(float) * (kSW * a.geo.npiece) + 8 * a.npw * kTopK);
   const int key = a.k == 0 ? kKeyNone : (a.topk_src == 1 ? kKeyLogit : kKeyWeight);
   const void* resid = key == kKeyLogit    ? reinterpret_cast<const void*>(&residual_kernel<E, kKeyLogit>)
@@ -477,11 +477,13 @@ cudaError_t launch_saguaro_t(const SagArgs& a, cudaStream_t stream) {
   cfg.stream = stream;
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
-  cudaError_t e = key == kKeyLogit    ? cudaLaunchKernelEx(&cfg, residual_kernel<E, kKeyLogit>, a)
-                  : key == kKeyWeight ? cudaLaunchKernelEx(&cfg, residual_kernel<E, kKeyWeight>, a)
-                                      : cudaLaunchKernelEx(&cfg, residual_kernel<E, kKeyNone>, a);
-  if (e != cudaSuccess) return e;
-  return cudaLaunchKernelEx(&cfg, mix_kernel<E>, a);
+  if (passes & kSagResidual) {
+    const cudaError_t e = key == kKeyLogit    ? cudaLaunchKernelEx(&cfg, residual_kernel<E, kKeyLogit>, a)
+                          : key == kKeyWeight ? cudaLaunchKernelEx(&cfg, residual_kernel<E, kKeyWeight>, a)
+                                              : cudaLaunchKernelEx(&cfg, residual_kernel<E, kKeyNone>, a);
+    if (e != cudaSuccess) return e;
+  }
+  return (passes & kSagMix) ? cudaLaunchKernelEx(&cfg, mix_kernel<E>, a) : cudaSuccess;
 }
 
 }  // namespace
@@ -537,8 +539,8 @@ cudaError_t launch_cache_check(const int32_t* bonus_topk, const int32_t* out_tok
   return cudaLaunchKernelEx(&cfg, cache_check_kernel, bonus_topk, out_tokens, n_accepted, B, W, k, hit, n_hits);
 }
 
-cudaError_t launch_saguaro(const SagArgs& a, int esize, cudaStream_t stream) {
-  return esize == 2 ? launch_saguaro_t<uint16_t>(a, stream) : launch_saguaro_t<float>(a, stream);
+cudaError_t launch_saguaro(const SagArgs& a, int esize, cudaStream_t stream, int passes) {
+  return esize == 2 ? launch_saguaro_t<uint16_t>(a, stream, passes) : launch_saguaro_t<float>(a, stream, passes);
 }
 
 }  // namespace ssdv

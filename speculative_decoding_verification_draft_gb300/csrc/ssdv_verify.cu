@@ -761,13 +761,20 @@ __global__ void __launch_bounds__(kT2, 8) sample_kernel(const VerifyArgs a) {
   float* psum = a.psum + pi_idx * NP;
 
   // This warp's pieces (geo.ppw of them, one after the other): their weight
-  // sums, then one arrival for all of them.
+  // sums, then one arrival for all of them.  With the pieces ready (the
+  // Saguaro residual pass summed every position's draw row the same way),
+  // warp 0 of the request's one CTA draws from row n's sums directly.
   const int ppw = geo.ppw;
   const int p0 = (c * kW2 + warp) * ppw;
-  if (p0 >= NP) return;
+  if (a.pieces_ready) {
+    if (warp != 0) return;
+    psum = a.psum + (static_cast<size_t>(b) * W + pos) * NP;
+  } else if (p0 >= NP) {
+    return;
+  }
   const int pn = min(ppw, NP - p0);
-  bool last;
-  {
+  bool last = a.pieces_ready != 0;
+  if (!a.pieces_ready) {
     for (int j = 0; j < pn; ++j) {
       const int lo = (p0 + j) * pelems;
       PieceRows<E> pr;
@@ -784,7 +791,7 @@ __global__ void __launch_bounds__(kT2, 8) sample_kernel(const VerifyArgs a) {
 
   // The last warp: the piece sums in order, the piece holding u * S, then
   // that piece reloaded and scanned.
-  if (lane == 0) a.ticket[pi_idx] = 0;  // the last arrival of this call: reset for the next
+  if (lane == 0 && !a.pieces_ready) a.ticket[pi_idx] = 0;  // the last arrival of this call: reset for the next
   RowPieces rp;
   rp.load(psum, NP, s_pieces + warp * NP);
   if (a.stats && residual && lane == 0)
@@ -1081,7 +1088,8 @@ template <typename E>
 cudaError_t launch_sample_t(const VerifyArgs& a, cudaStream_t stream) {
   const int P = a.debug ? a.gmax + 1 : 1;  // position slots of the sampling grid
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((a.geo.npiece + kW2 * a.geo.ppw - 1) / (kW2 * a.geo.ppw), P, a.B);
+  cfg.gridDim = a.pieces_ready ? dim3(1, 1, a.B)
+                               : dim3((a.geo.npiece + kW2 * a.geo.ppw - 1) / (kW2 * a.geo.ppw), P, a.B);
   cfg.blockDim = dim3(kT2, 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(kW2) * a.geo.npiece * sizeof(float);
   cfg.stream = stream;
