@@ -77,8 +77,10 @@ constexpr int kSW = kS / 32;
 // V=152064.  bf16 rows measured slower that way and keep the allocation they
 // get unconstrained (the residual kernel without top-k: 72 registers, 7 CTAs
 // per SM; with top-k: up to 128, 4; the mix kernel: 80, 6).
-template <typename E, int kKey>
-constexpr int resid_min_blocks() { return sizeof(E) == 4 ? 6 : (kKey == 0 ? 7 : 4); }
+// kK: the per-lane top-k list (4 when k <= 4, else 8): the shorter list frees
+// registers for a seventh fp32 CTA per SM.
+template <typename E, int kKey, int kK = 8>
+constexpr int resid_min_blocks() { return sizeof(E) == 4 ? (kK <= 4 ? 7 : 6) : (kKey == 0 ? 7 : 4); }
 template <typename E>
 constexpr int mix_min_blocks() { return sizeof(E) == 4 ? 8 : 6; }
 constexpr int kTopK = SSD_MAX_TOPK;  // every warp tracks the top 8; the first k are written
@@ -142,7 +144,7 @@ enum { kKeyNone = 0, kKeyWeight = 1, kKeyLogit = 2 };
 // This warp's pieces: weight sums into psum, top-8 (by kKey) into the unit's
 // candidate slots.  Returns true in the last warp of the unit to arrive
 // (every lane), after which the other warps' sums are visible.
-template <typename E, typename WFun, int kKey>
+template <typename E, typename WFun, int kKey, int kK = kTopK>
 __device__ __forceinline__ bool unit_pieces(const SagArgs& a, size_t u, int wi, const E* trow, const E* drow,
                                             const WFun& wfun, float* psum, int32_t* ticket) {
   constexpr bool kTop = kKey != kKeyNone;
@@ -152,7 +154,7 @@ __device__ __forceinline__ bool unit_pieces(const SagArgs& a, size_t u, int wi, 
   const int pelems = kPieceVecs * kVec;
   const int p0 = wi * ppw;
   const int pn = min(ppw, NP - p0);
-  TopK<kTopK, kKey == kKeyLogit> tk;
+  TopK<kK, kKey == kKeyLogit> tk;
   tk.init();
   // tau: the k-th largest of the lanes' best keys so far.  The warp holds k
   // elements at or above it, so a smaller key is not among the row's k
@@ -206,14 +208,14 @@ __device__ __forceinline__ bool unit_pieces(const SagArgs& a, size_t u, int wi, 
     }
   }
   if constexpr (kTop) {
-    float mv[kTopK];
-    int mi[kTopK];
+    float mv[kK];
+    int mi[kK];
     warp_merge_topk(tk, mv, mi);
-    if (lane < kTopK) {
-      float v = mv[0];
-      int i = mi[0];
+    if (lane < kTopK) {  // the warp's kTopK candidate slots; past kK they stay empty
+      float v = -INFINITY;
+      int i = 0x7FFFFFFF;
 #pragma unroll
-      for (int r = 1; r < kTopK; ++r)
+      for (int r = 0; r < kK; ++r)
         if (lane == r) {
           v = mv[r];
           i = mi[r];
@@ -269,7 +271,7 @@ __device__ __forceinline__ void write_topk(const SagArgs& a, size_t u, double to
 // the top-k.  s4 = the unit's row statistics (target max, sum, draft max,
 // sum).  Returns true in (every lane of) that last warp.
 // ---------------------------------------------------------------------------
-template <typename E, int kKey>
+template <typename E, int kKey, int kK = kTopK>
 __device__ __forceinline__ bool residual_unit(const SagArgs& a, int b, int j, int wi, uint8_t* dyn_smem,
                                               float4 s4) {
   const int W = a.g + 1;
@@ -282,7 +284,7 @@ __device__ __forceinline__ bool residual_unit(const SagArgs& a, int b, int j, in
   const E* drow = bonus ? nullptr : static_cast<const E*>(a.draft) + (static_cast<size_t>(b) * a.g + j) * V;
   const PassAW<E> wf{c, scaled_max(s4.x, c), bonus ? 0.f : scaled_max(s4.z, c), bonus ? 0.f : s4.y / s4.w,
                      bonus ? 1 : 0};
-  if (!unit_pieces<E, PassAW<E>, kKey>(a, u, wi, trow, drow, wf, a.psum2, a.ticket2)) return false;
+  if (!unit_pieces<E, PassAW<E>, kKey, kK>(a, u, wi, trow, drow, wf, a.psum2, a.ticket2)) return false;
 
   // The last warp: S_j, and the top-k unless the residual is empty (then the
   // mix pass takes the top-k of q_j).
@@ -415,8 +417,8 @@ __device__ __forceinline__ void cta_unit_stats(const SagArgs& a, size_t u, float
 // ---------------------------------------------------------------------------
 // Kernel 2: residual sums and top-k.  Grid (warp groups, j, request).
 // ---------------------------------------------------------------------------
-template <typename E, int kKey>
-__global__ void __launch_bounds__(kS, resid_min_blocks<E, kKey>()) residual_kernel(const SagArgs a) {
+template <typename E, int kKey, int kK>
+__global__ void __launch_bounds__(kS, resid_min_blocks<E, kKey, kK>()) residual_kernel(const SagArgs a) {
   extern __shared__ __align__(16) uint8_t dyn_smem[];
   __shared__ float4 sh_stats;
   griddep_launch_dependents();  // the mix kernel may become resident (it waits for this grid)
@@ -425,7 +427,7 @@ __global__ void __launch_bounds__(kS, resid_min_blocks<E, kKey>()) residual_kern
   griddep_wait();  // the streaming kernel's records are complete and visible
   cta_unit_stats(a, static_cast<size_t>(b) * W + j, &sh_stats);
   if (wi >= a.npw) return;
-  residual_unit<E, kKey>(a, b, j, wi, dyn_smem, sh_stats);
+  residual_unit<E, kKey, kK>(a, b, j, wi, dyn_smem, sh_stats);
 }
 
 // ---------------------------------------------------------------------------
@@ -442,12 +444,16 @@ __global__ void __launch_bounds__(kS, mix_min_blocks<E>()) mix_kernel(const SagA
   mix_unit<E>(a, b, j, wi, dyn_smem);
 }
 
-template __global__ void residual_kernel<uint16_t, kKeyWeight>(const SagArgs);
-template __global__ void residual_kernel<float, kKeyWeight>(const SagArgs);
-template __global__ void residual_kernel<uint16_t, kKeyLogit>(const SagArgs);
-template __global__ void residual_kernel<float, kKeyLogit>(const SagArgs);
-template __global__ void residual_kernel<uint16_t, kKeyNone>(const SagArgs);
-template __global__ void residual_kernel<float, kKeyNone>(const SagArgs);
+template __global__ void residual_kernel<uint16_t, kKeyWeight, 8>(const SagArgs);
+template __global__ void residual_kernel<float, kKeyWeight, 8>(const SagArgs);
+template __global__ void residual_kernel<uint16_t, kKeyLogit, 8>(const SagArgs);
+template __global__ void residual_kernel<float, kKeyLogit, 8>(const SagArgs);
+template __global__ void residual_kernel<uint16_t, kKeyWeight, 4>(const SagArgs);
+template __global__ void residual_kernel<float, kKeyWeight, 4>(const SagArgs);
+template __global__ void residual_kernel<uint16_t, kKeyLogit, 4>(const SagArgs);
+template __global__ void residual_kernel<float, kKeyLogit, 4>(const SagArgs);
+template __global__ void residual_kernel<uint16_t, kKeyNone, 8>(const SagArgs);
+template __global__ void residual_kernel<float, kKeyNone, 8>(const SagArgs);
 template __global__ void mix_kernel<uint16_t>(const SagArgs);
 template __global__ void mix_kernel<float>(const SagArgs);
 
@@ -457,9 +463,13 @@ template <typename E>
 cudaError_t launch_saguaro_t(const SagArgs& a, cudaStream_t stream, int passes) {
   const int smem = static_cast<int>(sizeof(float) * (kSW * a.geo.npiece) + 8 * a.npw * kTopK);
   const int key = a.k == 0 ? kKeyNone : (a.topk_src == 1 ? kKeyLogit : kKeyWeight);
-  const void* resid = key == kKeyLogit    ? reinterpret_cast<const void*>(&residual_kernel<E, kKeyLogit>)
-                      : key == kKeyWeight ? reinterpret_cast<const void*>(&residual_kernel<E, kKeyWeight>)
-                                          : reinterpret_cast<const void*>(&residual_kernel<E, kKeyNone>);
+  const bool short_list = a.k <= 4;  // per-lane top-4 lists: 72 registers, 7 fp32 CTAs per SM
+  const void* resid =
+      key == kKeyLogit    ? (short_list ? reinterpret_cast<const void*>(&residual_kernel<E, kKeyLogit, 4>)
+                                        : reinterpret_cast<const void*>(&residual_kernel<E, kKeyLogit, 8>))
+      : key == kKeyWeight ? (short_list ? reinterpret_cast<const void*>(&residual_kernel<E, kKeyWeight, 4>)
+                                        : reinterpret_cast<const void*>(&residual_kernel<E, kKeyWeight, 8>))
+                          : reinterpret_cast<const void*>(&residual_kernel<E, kKeyNone, 8>);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(resid, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess)
@@ -478,9 +488,15 @@ cudaError_t launch_saguaro_t(const SagArgs& a, cudaStream_t stream, int passes) 
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
   if (passes & kSagResidual) {
-    const cudaError_t e = key == kKeyLogit    ? cudaLaunchKernelEx(&cfg, residual_kernel<E, kKeyLogit>, a)
-                          : key == kKeyWeight ? cudaLaunchKernelEx(&cfg, residual_kernel<E, kKeyWeight>, a)
-                                              : cudaLaunchKernelEx(&cfg, residual_kernel<E, kKeyNone>, a);
+    cudaError_t e;
+    if (key == kKeyLogit)
+      e = short_list ? cudaLaunchKernelEx(&cfg, residual_kernel<E, kKeyLogit, 4>, a)
+                     : cudaLaunchKernelEx(&cfg, residual_kernel<E, kKeyLogit, 8>, a);
+    else if (key == kKeyWeight)
+      e = short_list ? cudaLaunchKernelEx(&cfg, residual_kernel<E, kKeyWeight, 4>, a)
+                     : cudaLaunchKernelEx(&cfg, residual_kernel<E, kKeyWeight, 8>, a);
+    else
+      e = cudaLaunchKernelEx(&cfg, residual_kernel<E, kKeyNone, 8>, a);
     if (e != cudaSuccess) return e;
   }
   return (passes & kSagMix) ? cudaLaunchKernelEx(&cfg, mix_kernel<E>, a) : cudaSuccess;
