@@ -60,6 +60,11 @@ def test_host_validation_without_gpu(lib):
     # shape checks run before any device query
     p = ctypes.c_void_p(16)
     assert L.ssd_verify(p, p, 0, p, 0, 1, 8, 1.0, 0, p, p, p, 1 << 20, None) == 2
+    # one past each declared maximum: gamma 32 (SSD_MAX_GAMMA 31), V 2^19 + 1 (SSD_MAX_V)
+    assert L.ssd_verify(p, p, 0, p, 1, 32, 8, 1.0, 0, p, p, p, 1 << 20, None) == 2
+    assert L.ssd_verify(p, p, 0, p, 1, 1, (1 << 19) + 1, 1.0, 0, p, p, p, 1 << 20, None) == 2
+    assert L.ssd_saguaro_prespec(p, p, 0, 1, 32, 8, 3, 0, 1.0, 0, p, p, p, 1 << 20, None) == 2
+    assert L.ssd_saguaro_prespec(p, p, 0, 1, 1, (1 << 19) + 1, 3, 0, 1.0, 0, p, p, p, 1 << 20, None) == 2
     assert L.ssd_verify(p, p, 0, p, 1, 33, 8, 1.0, 0, p, p, p, 1 << 20, None) == 2
     # misaligned bf16 pointer, small workspace
     odd = ctypes.c_void_p(17)
