@@ -15,10 +15,15 @@
 //     target row and draft row -- one HBM read of every logit;
 //  2. residual_kernel: warps over 128-vector pieces of every unit's rows: the
 //     residual weights (target weights at j = gamma), the pieces' sums and a
-//     top-8 per warp; the last warp of a unit fixes S_j and merges the top-k;
+//     top-4 (k <= 4) or top-8 per lane, merged per warp; the last warp of a
+//     unit fixes S_j and merges the top-k;
 //  3. mix_kernel: warps over the same pieces: the Saguaro weights, their
 //     piece sums; the last warp of a unit draws the token (and, when S_j = 0,
 //     merges the top-k of q_j instead).
+// A round that also verifies (the fused call) runs the verification's
+// sampling kernel between 2 and 3: the residual kernel's piece sums of unit
+// (b, j) are, in the same order and arithmetic, the sums of the weights the
+// verification draws from when n = j, so the draw needs no pass over the rows.
 #include "ssdv_device.cuh"
 
 namespace ssdv {

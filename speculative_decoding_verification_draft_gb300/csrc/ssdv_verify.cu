@@ -36,8 +36,6 @@
 // segment's CTAs saw the call's inputs complete, and may stream while the
 // previous segment's sampling kernel runs: the segments use disjoint
 // workspace rows.  A call never overlaps the work of the previous call.
-#include <cstdlib>
-#include <cstring>
 #include <type_traits>
 
 #include "ssdv_device.cuh"
