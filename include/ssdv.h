@@ -176,9 +176,10 @@ ssd_status ssd_verify_pipelined(const void* target_logits, const void* draft_log
  * kernels run); the scratch is a fixed file-scope device array of
  * SSD_NOALLOC_SCRATCH_BYTES bytes inside the library, and the call allocates
  * no device memory.  The batch must fit it:
- * ssd_workspace_bytes(B, gamma) <= SSD_NOALLOC_SCRATCH_BYTES, i.e.
- * B * (gamma + 1) <= 474 (B = 64 at gamma <= 6); a larger batch returns
- * SSD_ERR_WORKSPACE before anything is launched.
+ * ssd_workspace_bytes(B, gamma) <= SSD_NOALLOC_SCRATCH_BYTES, which holds
+ * whenever B * (gamma + 1) <= 1600 (B = 64 at gamma <= 24, B = 256 at
+ * gamma <= 5); a larger batch returns SSD_ERR_WORKSPACE before anything is
+ * launched.
  *
  * Every call looks up the current device's copy of the array with
  * cudaGetSymbolAddress (a host-side query that allocates nothing).  The first

@@ -61,9 +61,8 @@ WorkspaceLayout workspace_layout(int B, int gmax) {
   L.half0 = 256;
   L.ticket = 0;  // offsets within a half
   L.part = round_up(L.ticket + 4 * units, 256);
-  L.csum = L.part + units * kMaxChunks * 2 * sizeof(float4);
-  L.blocks = L.csum + units * kMaxChunks * sizeof(double);
-  L.half_bytes = round_up(L.blocks + units * kMaxChunks * 128 * sizeof(float), 256);
+  L.blocks = L.part + units * kMaxChunks * 2 * sizeof(float4);
+  L.half_bytes = round_up(L.blocks + units * kMaxPieces * sizeof(float), 256);
   L.total = L.half0 + 2 * L.half_bytes;
   return L;
 }
@@ -248,6 +247,9 @@ ssd_status verify_common(const void* target, const void* draft, ssd_dtype dtype,
   a.tp_th = nullptr;
   a.tp_z = nullptr;
   a.pieces_ready = 0;
+  // streaming order: request-major for pipelined calls of one gamma, where it
+  // measured faster; position-major for plain and ragged calls
+  a.req_major = (pipelined && !gamma) ? 1 : 0;
   a.geo = geo;
   if (use_topp) {
     // The streaming kernel, the radix-select levels of every row's nucleus
@@ -445,7 +447,7 @@ ssd_status ssd_verify_noalloc(const void* target_logits, const void* draft_logit
   if (need > SSD_NOALLOC_SCRATCH_BYTES)
     return fail(SSD_ERR_WORKSPACE,
                 "B=%d gamma=%d needs %zu bytes of scratch, above the fixed %u-byte array of ssd_verify_noalloc "
-                "(B*(gamma+1) <= 474); call ssd_verify with a workspace instead",
+                "(B*(gamma+1) <= 1600 always fits); call ssd_verify with a workspace instead",
                 B, gamma, need, SSD_NOALLOC_SCRATCH_BYTES);
   void* scratch = nullptr;
   const ssd_status st = noalloc_scratch(static_cast<cudaStream_t>(stream), &scratch);
@@ -575,6 +577,7 @@ static ssd_status saguaro_common(const void* target, const void* draft, ssd_dtyp
     v.stats = nullptr;
     v.debug = 0;
     v.first = b0 == 0 ? 1 : 0;
+    v.req_major = 1;  // request-major streaming: measured faster for the Saguaro passes
     v.geo = geo;
     // The streaming kernel: one read of every row, whose records serve
     // verification and Saguaro alike.
@@ -739,6 +742,7 @@ ssd_status ssd_verify_saguaro_draft(const void* target_logits, const void* draft
     v.sag_S = reinterpret_cast<double*>(ws + L.rowsum) + u0;
     v.sag_Zs = reinterpret_cast<float*>(ws + L.zsum) + u0;
     v.first = b0 == 0 ? 1 : 0;
+    v.req_major = 1;  // request-major streaming: measured faster for the Saguaro passes
     v.geo = geo;
     cudaError_t e = launch_stream(v, es, smem, s);
     if (e != cudaSuccess) return cuda_fail(e, "streaming launch");

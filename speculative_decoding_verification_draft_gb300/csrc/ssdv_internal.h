@@ -58,6 +58,8 @@ struct VerifyArgs {
   int first;                   // 1: every streaming CTA waits for the previous kernel (the first
                                // segment of a call); 0: only the first CTA waits (a later segment, or
                                // a pipelined call)
+  int req_major;               // streaming grid order: 1 request by request (chunk, position, request);
+                               // 0 position-major (chunk, request, position)
   ChunkGeometry geo;
 };
 
@@ -120,7 +122,7 @@ cudaError_t launch_topp_level(const TopPArgs& a, int esize, cudaStream_t stream)
 // arrival counters (cleared by every call), chunk records and piece sums of
 // the call's shape (ticket .. blocks are offsets within a half).
 struct WorkspaceLayout {
-  size_t status, half0, half_bytes, ticket, part, csum, blocks, total;
+  size_t status, half0, half_bytes, ticket, part, blocks, total;
 };
 WorkspaceLayout workspace_layout(int B, int gmax);
 

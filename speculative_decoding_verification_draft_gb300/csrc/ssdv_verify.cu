@@ -173,11 +173,17 @@ __global__ void __launch_bounds__(kThreads) stream_kernel(const VerifyArgs a) {
 
   const ChunkGeometry& geo = a.geo;
   const int V = geo.V, NC = geo.nchunk, W = a.gmax + 1;
-  // Dispatch order: chunk, then request, then position from the last to the
-  // first, so the rows of the low positions -- where the first rejection, and
-  // with it the sampling kernel's residual pass, usually falls -- are read
-  // last and are still in L2 when the sampling kernel needs them.
-  const int c = blockIdx.x, b = blockIdx.y, i = W - 1 - static_cast<int>(blockIdx.z);
+  // Dispatch order, positions from the last to the first.  Position-major
+  // (chunk, request, position): the rows of the low positions -- where the
+  // first rejection, and with it the sampling kernel's residual pass, usually
+  // falls -- are read last and are still in L2 when the sampling kernel needs
+  // them.  Request-major (chunk, position, request): one request's rows after
+  // another.  Measured at B=64, gamma 4, V=128256 bf16: 29.06 against 29.46
+  // us per pipelined call, 42.02 against 41.84 us per plain call; the Saguaro
+  // round 0.940 against 0.945 ms; a ragged round 0.241 against 0.238 ms.
+  const int c = blockIdx.x;
+  const int b = a.req_major ? blockIdx.z : blockIdx.y;
+  const int i = W - 1 - static_cast<int>(a.req_major ? blockIdx.y : blockIdx.z);
   const int tid = threadIdx.x;
   // The first CTA of each request clears the request's arrival counters for
   // the sampling kernel (which reads them only after this grid completes).
@@ -340,7 +346,9 @@ __global__ void __launch_bounds__(kThreads, reg_min_blocks(kNV)) stream_reg_kern
 
   const ChunkGeometry& geo = a.geo;
   const int V = geo.V, NC = geo.nchunk, W = a.gmax + 1;
-  const int c = blockIdx.x, b = blockIdx.y, i = W - 1 - static_cast<int>(blockIdx.z);
+  const int c = blockIdx.x;  // dispatch order as in the shared-memory form
+  const int b = a.req_major ? blockIdx.z : blockIdx.y;
+  const int i = W - 1 - static_cast<int>(a.req_major ? blockIdx.y : blockIdx.z);
   const int tid = threadIdx.x;
   if (i == 0 && c == 0 && tid < W) a.ticket[b * W + tid] = 0;
 
@@ -1064,7 +1072,7 @@ cudaError_t launch_stream_t(const VerifyArgs& a, int smem_bytes, cudaStream_t st
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t c1 = {};
-  c1.gridDim = dim3(a.geo.nchunk, a.B, a.gmax + 1);
+  c1.gridDim = a.req_major ? dim3(a.geo.nchunk, a.gmax + 1, a.B) : dim3(a.geo.nchunk, a.B, a.gmax + 1);
   c1.blockDim = dim3(kThreads, 1, 1);
   c1.stream = stream;
   c1.attrs = pdl;

@@ -15,7 +15,7 @@ from speculative_decoding_verification_draft_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
 
-SCRATCH_UNITS = 474  # B * (gamma + 1) that fit the 16 MiB scratch
+SCRATCH_UNITS = 1600  # B * (gamma + 1) that always fit the 16 MiB scratch
 
 
 def _outputs(batch):
@@ -64,21 +64,22 @@ def test_noalloc_matches_workspace_path_small_and_greedy(dtype):
 
 def test_noalloc_at_the_scratch_limit():
     ssdv = cuda_lib()
-    B, g = 79, 5  # 474 units: the limit
-    assert ssdv.workspace_bytes(B, g) <= 16 << 20
+    B, g = 272, 5  # 1632 units: the largest batch at gamma 5
+    assert ssdv.workspace_bytes(B, g) <= 16 << 20 < ssdv.workspace_bytes(B + 1, g)
+    assert ssdv.workspace_bytes(SCRATCH_UNITS // 32, 31) <= 16 << 20
     a = wl.zipf_batch(B, g, 3001, seed=21).to("cuda")
     b = wl.zipf_batch(B, g, 3001, seed=22).to("cuda")
-    _assert_same(_two_in_a_row(ssdv, [a, b], [8, 9]), "B=79 gamma=5")
+    _assert_same(_two_in_a_row(ssdv, [a, b], [8, 9]), "B=272 gamma=5")
 
 
 def test_noalloc_rejects_batches_beyond_the_scratch():
     ssdv = cuda_lib()
-    B, g = 64, 15  # 1024 units > 474
+    B, g = 64, 31  # 2048 units > 1600
     assert ssdv.workspace_bytes(B, g) > 16 << 20
     batch = wl.zipf_batch(B, g, 64, seed=31).to("cuda")
     o, n = _outputs(batch)
     with pytest.raises(ssdv.SsdError) as err:
         ssdv.verify_noalloc(batch.target, batch.draft, batch.draft_tokens, batch.temperature, 1, o, n)
-    assert err.value.status == 9 and "474" in str(err.value)
+    assert err.value.status == 9 and str(SCRATCH_UNITS) in str(err.value)
     torch.cuda.synchronize()
     assert (o == -9).all() and (n == -9).all(), "a rejected call must launch nothing"
