@@ -280,7 +280,7 @@ template <typename E, int kKey, int kK = kTopK>
 __device__ __forceinline__ bool residual_unit(const SagArgs& a, int b, int j, int wi, uint8_t* dyn_smem,
                                               float4 s4) {
   const int W = a.g + 1;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31;
   const size_t u = static_cast<size_t>(b) * W + j;
   const bool bonus = (j == a.g);
   const float c = kLog2e / a.temperature;
@@ -294,7 +294,8 @@ __device__ __forceinline__ bool residual_unit(const SagArgs& a, int b, int j, in
   // The last warp: S_j, and the top-k unless the residual is empty (then the
   // mix pass takes the top-k of q_j).
   RowPieces rp;
-  float* s_pieces = reinterpret_cast<float*>(dyn_smem) + warp * a.geo.npiece;
+  // one copy per CTA: a CTA's warps all cover unit u, whose last warp is unique
+  float* s_pieces = reinterpret_cast<float*>(dyn_smem);
   rp.load(a.psum2 + u * a.geo.npiece, a.geo.npiece, s_pieces);
   const double S = rp.total;
   float* st = a.stats ? a.stats + u * SSD_NSTAT_SAGUARO : nullptr;
@@ -312,7 +313,7 @@ __device__ __forceinline__ bool residual_unit(const SagArgs& a, int b, int j, in
   const bool logit_keys = kKey == kKeyLogit;
   if (kKey != kKeyNone && (logit_keys || bonus || S > 0.0)) {
     __syncwarp();
-    float* s_cv = reinterpret_cast<float*>(dyn_smem) + kSW * a.geo.npiece;
+    float* s_cv = reinterpret_cast<float*>(dyn_smem) + a.geo.npiece;
     int* s_ci = reinterpret_cast<int*>(s_cv + a.npw * kTopK);
     // logit keys report p_j (q_gamma at the bonus position) of the slots
     const float mc = bonus ? scaled_max(s4.x, c) : scaled_max(s4.z, c);
@@ -331,7 +332,7 @@ __device__ __forceinline__ bool residual_unit(const SagArgs& a, int b, int j, in
 template <typename E>
 __device__ __forceinline__ bool mix_unit(const SagArgs& a, int b, int j, int wi, uint8_t* dyn_smem) {
   const int W = a.g + 1;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31;
   const size_t u = static_cast<size_t>(b) * W + j;
   const bool bonus = (j == a.g);
   const float c = kLog2e / a.temperature;
@@ -352,7 +353,7 @@ __device__ __forceinline__ bool mix_unit(const SagArgs& a, int b, int j, int wi,
 
   // The last warp: Zs, the draw, and (empty residual) the top-k of q_j.
   RowPieces rp;
-  float* s_pieces = reinterpret_cast<float*>(dyn_smem) + warp * a.geo.npiece;
+  float* s_pieces = reinterpret_cast<float*>(dyn_smem);  // one copy per CTA, as in the residual pass
   rp.load(a.psum3 + u * a.geo.npiece, a.geo.npiece, s_pieces);
   if (a.zsum && lane == 0) a.zsum[u] = static_cast<float>(rp.total);
   if (!a.saguaro_tokens) return true;  // the normaliser is all a later kernel needs
@@ -466,7 +467,7 @@ namespace {
 
 template <typename E>
 cudaError_t launch_saguaro_t(const SagArgs& a, cudaStream_t stream, int passes) {
-  const int smem = static_cast<int>(sizeof(float) * (kSW * a.geo.npiece) + 8 * a.npw * kTopK);
+  const int smem = static_cast<int>(sizeof(float) * a.geo.npiece + 8 * a.npw * kTopK);
   const int key = a.k == 0 ? kKeyNone : (a.topk_src == 1 ? kKeyLogit : kKeyWeight);
   const bool short_list = a.k <= 4;  // per-lane top-4 lists: 72 registers, 7 fp32 CTAs per SM
   const void* resid =

@@ -545,7 +545,11 @@ __global__ void __launch_bounds__(kT2, 8) sample_kernel(const VerifyArgs a) {
   __shared__ float tok_t[SSD_MAX_GAMMA], tok_d[SSD_MAX_GAMMA];
   __shared__ int sh_n, sh_bad, sh_sag_bad;
   __shared__ float sh_uacc[SSD_MAX_GAMMA + 1], sh_ures[SSD_MAX_GAMMA + 1];
-  extern __shared__ float s_pieces[];  // [kW2][NP]: the last warp's copy of its row's piece sums
+  // [NP]: the last warp's copy of its row's piece sums.  A CTA's warps all
+  // cover one draw row, and only one warp of the grid arrives last on a row,
+  // so one copy per CTA suffices (less shared memory leaves more of the
+  // unified L1/shared array to L1).
+  extern __shared__ float s_pieces[];
 
   constexpr int kVec = Elem<E>::kVec;
   const ChunkGeometry& geo = a.geo;
@@ -799,7 +803,7 @@ __global__ void __launch_bounds__(kT2, 8) sample_kernel(const VerifyArgs a) {
   // that piece reloaded and scanned.
   if (lane == 0 && !a.pieces_ready) a.ticket[pi_idx] = 0;  // the last arrival of this call: reset for the next
   RowPieces rp;
-  rp.load(psum, NP, s_pieces + warp * NP);
+  rp.load(psum, NP, s_pieces);
   if (a.stats && residual && lane == 0)
     a.stats[pi_idx * SSD_NSTAT_VERIFY + 6] = static_cast<float>(rp.total / static_cast<double>(s.ts));
   if (pos != n) return;
@@ -817,7 +821,7 @@ __global__ void __launch_bounds__(kT2, 8) sample_kernel(const VerifyArgs a) {
         if (lane == 0) psum[q] = ps;
       }
       __syncwarp();
-      rp.load(psum, NP, s_pieces + warp * NP);
+      rp.load(psum, NP, s_pieces);
     }
     warp_draw_row<E>(a, b, n, pi_idx, rp, ures, trow, nullptr, aligned, tw, tok_x);
   }
@@ -1097,7 +1101,7 @@ cudaError_t launch_sample_t(const VerifyArgs& a, cudaStream_t stream) {
   cfg.gridDim = a.pieces_ready ? dim3(1, 1, a.B)
                                : dim3((a.geo.npiece + kW2 * a.geo.ppw - 1) / (kW2 * a.geo.ppw), P, a.B);
   cfg.blockDim = dim3(kT2, 1, 1);
-  cfg.dynamicSmemBytes = static_cast<size_t>(kW2) * a.geo.npiece * sizeof(float);
+  cfg.dynamicSmemBytes = static_cast<size_t>(a.geo.npiece) * sizeof(float);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
