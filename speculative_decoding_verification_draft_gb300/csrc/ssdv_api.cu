@@ -42,6 +42,8 @@ bool aligned_to(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int esize_of(ssd_dtype dt) { return dt == SSD_BF16 ? 2 : (dt == SSD_F32 ? 4 : 0); }
 
+constexpr int kMaxChunkElems = SSD_MAX_V / kMaxChunks;  // 16384
+
 bool temperature_valid(float T) { return T == 0.f || (T >= 1e-6f && isfinite(T)); }
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -157,6 +159,9 @@ ssd_status choose_chunks(int V, int esize, bool aligned, ChunkGeometry* geo, int
   long long nc = (row_bytes + want - 1) / want;
   if (nc < 1) nc = 1;
   if (nc > kMaxChunks) nc = kMaxChunks;
+  // at most kMaxChunkElems elements a chunk (top-p's level 0 counts a chunk's
+  // masses in 32-bit words sized for that); V <= 2^19 keeps nc <= kMaxChunks
+  if (nc < (V + kMaxChunkElems - 1) / kMaxChunkElems) nc = (V + kMaxChunkElems - 1) / kMaxChunkElems;
   const int chunk = static_cast<int>(round_up((static_cast<size_t>(V) + nc - 1) / nc, 8));
   const int row_smem = static_cast<int>(round_up(static_cast<size_t>(chunk) * esize, 128));
   if (2 * row_smem > max_smem)

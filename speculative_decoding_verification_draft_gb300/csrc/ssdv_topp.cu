@@ -127,8 +127,11 @@ __device__ __forceinline__ const E* slot_row(const TopPArgs& a, int b, int i, in
 }
 
 // Level 0's counter: every element's mass into the warp's own copy of the
-// 256 mass bins (two 32-bit words a bin: the low word, and the high word that
-// takes the carries out of it).
+// 256 mass bins, as two 32-bit words a bin: the low 20 bits of the 2^-40
+// fixed-point mass, and the bits above them.  A mass is at most 2^40 (e <= 1),
+// so each word takes less than 2^20 per element, and a warp sees at most
+// 2048 elements of a chunk (chunks hold at most 16384): neither word can
+// overflow, and no atomic needs its old value.
 struct MassBins {
   const TopPArgs* a;
   int b, i, which;
@@ -141,10 +144,9 @@ struct MassBins {
     const int bin = min(255, max(0, __float2int_rd(d * 8.f)));
     const int digit = 255 - bin;  // larger digit, larger mass
     const unsigned long long mass = mass_fixed(fast_exp2(-d));
-    const uint32_t lo32 = static_cast<uint32_t>(mass), hi32 = static_cast<uint32_t>(mass >> 32);
-    const uint32_t old = lo32 ? atomicAdd(&hist[digit], lo32) : 0u;
-    const uint32_t hi_add = hi32 + (old + lo32 < old ? 1u : 0u);  // the carry out of the low word
-    if (hi_add) atomicAdd(&hist[256 + digit], hi_add);
+    const uint32_t lo20 = static_cast<uint32_t>(mass) & 0xFFFFFu, hi20 = static_cast<uint32_t>(mass >> 20);
+    if (lo20) atomicAdd(&hist[digit], lo20);
+    if (hi20) atomicAdd(&hist[256 + digit], hi20);
   }
 };
 
@@ -223,7 +225,7 @@ __global__ void __launch_bounds__(kHistThreads) topp_hist_kernel(const TopPArgs 
   for (int d = threadIdx.x; d < 256; d += kHistThreads) {
     unsigned long long m = 0ull;
     for (int q = 0; q < kHistThreads / 32; ++q)
-      m += (static_cast<unsigned long long>(s_hist[q * 512 + 256 + d]) << 32) + s_hist[q * 512 + d];
+      m += (static_cast<unsigned long long>(s_hist[q * 512 + 256 + d]) << 20) + s_hist[q * 512 + d];
     if (m) atomicAdd(&h[d], m);
   }
 }
