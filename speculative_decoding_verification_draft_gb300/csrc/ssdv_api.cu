@@ -93,7 +93,7 @@ SagLayout saguaro_layout(int B, int g, int V) {
 // the select state, the thresholds and kept masses, then every level's
 // histograms (fp32's 256 + 2048 + 2048 + 1024 bins, the most).
 struct TopPLayout {
-  size_t prefix, bstar, above, goal, th, z, hist, total;
+  size_t prefix, bstar, above, goal, th, z, todo, todo_count, hist, total;
 };
 constexpr int kTopPBins = 256 + 2048 + 2048 + 1024;
 static TopPLayout topp_layout(int B, int gmax) {
@@ -105,7 +105,9 @@ static TopPLayout topp_layout(int B, int gmax) {
   T.goal = T.above + 8 * slots;
   T.th = T.goal + 8 * slots;
   T.z = T.th + 4 * slots;
-  T.hist = round_up(T.z + 4 * slots, 256);
+  T.todo = round_up(T.z + 4 * slots, 256);
+  T.todo_count = round_up(T.todo + 4 * slots, 256);  // zeroed with the histograms
+  T.hist = T.todo_count + 256;
   T.total = T.hist + slots * kTopPBins * 8;
   return T;
 }
@@ -268,7 +270,7 @@ ssd_status verify_common(const void* target, const void* draft, ssd_dtype dtype,
     const size_t slots = static_cast<size_t>(B) * (gmax + 1) * 2;
     size_t hist_bytes = 0;
     for (int l = 0; l < levels; ++l) hist_bytes += slots * (static_cast<size_t>(8) << bits[l]);
-    cudaError_t e = cudaMemsetAsync(ws + TL.hist, 0, hist_bytes, st);
+    cudaError_t e = cudaMemsetAsync(ws + TL.todo_count, 0, (TL.hist - TL.todo_count) + hist_bytes, st);
     if (e != cudaSuccess) return cuda_fail(e, "top-p histogram memset");
     a.first = 1;
     a.tp_th = reinterpret_cast<float*>(ws + TL.th);
@@ -293,6 +295,8 @@ ssd_status verify_common(const void* target, const void* draft, ssd_dtype dtype,
     t.goal = reinterpret_cast<unsigned long long*>(ws + TL.goal);
     t.th = reinterpret_cast<float*>(ws + TL.th);
     t.z = reinterpret_cast<float*>(ws + TL.z);
+    t.todo = reinterpret_cast<uint32_t*>(ws + TL.todo);
+    t.todo_count = reinterpret_cast<uint32_t*>(ws + TL.todo_count);
     size_t off = TL.hist;
     for (int l = 0; l < levels; ++l) {
       t.level = l;

@@ -114,6 +114,8 @@ struct TopPArgs {
   unsigned long long* goal;    // [B, gmax+1, 2]: ceil(top_p * total mass)
   float* th;                   // [B, gmax+1, 2]: the nucleus threshold (logit), after the last level
   float* z;                    // [B, gmax+1, 2]: the nucleus mass, after the last level
+  uint32_t* todo;              // [B, gmax+1, 2]: row slots that level 1 left open (bf16 rows)
+  uint32_t* todo_count;        // [1]: their number (zeroed by the caller)
 };
 cudaError_t launch_topp_level(const TopPArgs& a, int esize, cudaStream_t stream);
 

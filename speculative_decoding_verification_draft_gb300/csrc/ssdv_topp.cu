@@ -20,6 +20,8 @@
 // global memory).  Masses exp2(x c - fl(m c)) are summed in fixed point (2^-40
 // units), so the integer sums are exact and the same on every run whatever
 // the order of the atomics.
+#include <algorithm>
+
 #include "ssdv_device.cuh"
 
 namespace ssdv {
@@ -230,20 +232,10 @@ __global__ void __launch_bounds__(kHistThreads) topp_hist_kernel(const TopPArgs 
   }
 }
 
-// Levels 1.. over one chunk of one row.  Grid as level 0.
+// One chunk c of row slot (b, i, which) at levels 1.. (the CTA's threads).
 template <typename E>
-__global__ void __launch_bounds__(kHistThreads) topp_refine_kernel(const TopPArgs a) {
-  griddep_launch_dependents();
-  const int c = blockIdx.x, i = blockIdx.y >> 1, which = blockIdx.y & 1, b = blockIdx.z;
-  float T;
-  if (!slot_active(a, b, i, which, &T)) return;
+__device__ __forceinline__ void refine_chunk(const TopPArgs& a, int c, int b, int i, int which, float T) {
   const size_t rs = (static_cast<size_t>(b) * (a.gmax + 1) + i) * 2 + which;
-  if (a.level >= 2 && a.nlevels == 3) {
-    // bf16 rows whose level-1 select fixed th already are done: wait for it
-    // before loading anything, so that they cost no reads
-    griddep_wait();
-    if (__ldcg(a.bstar + rs) == kRowDone) return;
-  }
   const int lo = c * a.geo.chunk;
   DigitMasses f;
   f.a = &a;
@@ -258,18 +250,47 @@ __global__ void __launch_bounds__(kHistThreads) topp_refine_kernel(const TopPArg
   struct Late {
     DigitMasses& g;
     size_t rs;
+    int c;
     __device__ __forceinline__ void begin() {
       g.bstar = __ldcg(g.a->bstar + rs);
       g.prefix = g.a->level >= 2 ? __ldcg(g.a->prefix + rs) : 0u;
       g.begin();
       // level 1 of bf16 rows: tell the select how this row was counted (every
       // CTA of the row derives the same answer)
-      if (g.a->level == 1 && g.a->nlevels == 3 && blockIdx.x == 0 && threadIdx.x == 0)
+      if (g.a->level == 1 && g.a->nlevels == 3 && c == 0 && threadIdx.x == 0)
         g.a->prefix[rs] = g.direct ? (kDirectFlag | g.base16) : 0u;
     }
     __device__ __forceinline__ void operator()(float x) const { g(x); }
-  } late{f, rs};
+  } late{f, rs, c};
   for_chunk<E>(a, slot_row<E>(a, b, i, which), lo, min(a.geo.chunk, a.geo.V - lo), late);
+}
+
+// Levels 1.. over one chunk of one row.  Grid as level 0.
+template <typename E>
+__global__ void __launch_bounds__(kHistThreads) topp_refine_kernel(const TopPArgs a) {
+  griddep_launch_dependents();
+  const int c = blockIdx.x, i = blockIdx.y >> 1, which = blockIdx.y & 1, b = blockIdx.z;
+  float T;
+  if (!slot_active(a, b, i, which, &T)) return;
+  refine_chunk<E>(a, c, b, i, which, T);
+}
+
+// Level 2 of bf16 rows: only the row slots that level 1 left open (a few per
+// cent at top_p 0.9), as (slot, chunk) items over a grid of one wave, so that
+// the rows level 1 finished cost no CTAs.
+template <typename E>
+__global__ void __launch_bounds__(kHistThreads) topp_refine_open_kernel(const TopPArgs a) {
+  griddep_launch_dependents();
+  griddep_wait();  // level 1's select has listed the open rows
+  const int NC = a.geo.nchunk, W = a.gmax + 1;
+  const int items = static_cast<int>(__ldcg(a.todo_count)) * NC;
+  for (int it = blockIdx.x; it < items; it += gridDim.x) {
+    const int rs = static_cast<int>(__ldcg(a.todo + it / NC));
+    const int which = rs & 1, i = (rs >> 1) % W, b = (rs >> 1) / W;
+    float T;
+    if (!slot_active(a, b, i, which, &T)) continue;  // listed rows are active; uniform over the CTA
+    refine_chunk<E>(a, it % NC, b, i, which, T);
+  }
 }
 
 // Select of one level: one CTA per row slot fixes the next digit.  Thread t
@@ -362,6 +383,8 @@ __global__ void __launch_bounds__(256) topp_select_kernel(const TopPArgs a) {
     a.prefix[rs] = np;
     a.above[rs] = cum;
     a.goal[rs] = goal;
+    // bf16 rows still open after level 1: level 2 counts only these
+    if (a.level == 1 && a.nlevels == 3) a.todo[atomicAdd(a.todo_count, 1u)] = static_cast<uint32_t>(rs);
   } else {
     // the key's undecided low bits (bf16: the 16 that a bf16 logit lacks)
     // are those of the smallest logit with these digits, so th is that
@@ -377,6 +400,7 @@ template __global__ void topp_hist_kernel<uint16_t>(const TopPArgs);
 template __global__ void topp_hist_kernel<float>(const TopPArgs);
 template __global__ void topp_refine_kernel<uint16_t>(const TopPArgs);
 template __global__ void topp_refine_kernel<float>(const TopPArgs);
+template __global__ void topp_refine_open_kernel<uint16_t>(const TopPArgs);
 
 cudaError_t launch_topp_level(const TopPArgs& a, int esize, cudaStream_t stream) {
   cudaLaunchAttribute pdl[1];
@@ -391,12 +415,23 @@ cudaError_t launch_topp_level(const TopPArgs& a, int esize, cudaStream_t stream)
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
   cudaError_t e;
-  if (a.level == 0)
+  if (a.level == 0) {
     e = esize == 2 ? cudaLaunchKernelEx(&cfg, topp_hist_kernel<uint16_t>, a)
                    : cudaLaunchKernelEx(&cfg, topp_hist_kernel<float>, a);
-  else
+  } else if (a.level == 2 && a.nlevels == 3 && esize == 2) {
+    // one wave over the rows level 1 left open
+    int dev = 0, sms = 0, per_sm = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topp_refine_open_kernel<uint16_t>, kHistThreads, 0);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(static_cast<unsigned>(std::max(1, sms * std::max(1, per_sm))), 1, 1);
+    e = cudaLaunchKernelEx(&cfg, topp_refine_open_kernel<uint16_t>, a);
+  } else {
     e = esize == 2 ? cudaLaunchKernelEx(&cfg, topp_refine_kernel<uint16_t>, a)
                    : cudaLaunchKernelEx(&cfg, topp_refine_kernel<float>, a);
+  }
   if (e != cudaSuccess) return e;
   const size_t nslots = static_cast<size_t>(a.B) * (a.gmax + 1) * 2;
   cfg.gridDim = dim3(static_cast<unsigned>(nslots), 1, 1);
