@@ -293,62 +293,11 @@ __global__ void __launch_bounds__(kHistThreads) topp_refine_open_kernel(const To
   }
 }
 
-// Select of one level: one CTA per row slot fixes the next digit.  Thread t
-// holds bins [t * per, t * per + per), per = bins / 256; a block suffix scan
-// of the bin masses (the mass at or above each thread's first bin) finds the
-// last thread whose suffix, with the mass above the level's range, reaches the
-// goal, and that thread finds the digit among its bins.  At the last level it
-// writes the threshold logit and the kept mass.
-__global__ void __launch_bounds__(256) topp_select_kernel(const TopPArgs a) {
-  __shared__ unsigned long long s_w[8];
-  griddep_launch_dependents();
-  const int W = a.gmax + 1;
-  const size_t rs = blockIdx.x;
-  const int b = static_cast<int>(rs / (2 * W)), i = static_cast<int>((rs / 2) % W), which = static_cast<int>(rs & 1);
-  float T;
-  if (!slot_active(a, b, i, which, &T)) return;  // uniform over the CTA
-  griddep_wait();  // the level's histograms are complete and visible
-  if (a.level >= 2 && __ldcg(a.bstar + rs) == kRowDone) return;  // th fixed at level 1 (uniform)
-  const int nb = 1 << a.bits, per = nb >> 8;  // 1, 4 or 8
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const unsigned long long* h = a.hist + rs * nb + static_cast<size_t>(t) * per;
-  unsigned long long v[8], ls = 0ull;
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    v[k] = k < per ? __ldcg(h + k) : 0ull;
-    ls += v[k];
-  }
-  // suffix sums: within the warp, then the later warps' totals
-  unsigned long long suf = ls;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const unsigned long long x = __shfl_down_sync(0xFFFFFFFFu, suf, o);
-    if (lane + o < 32) suf += x;
-  }
-  if (lane == 0) s_w[warp] = suf;
-  __syncthreads();
-  unsigned long long tot = 0ull;
-#pragma unroll
-  for (int w = 0; w < 8; ++w) {
-    tot += s_w[w];
-    if (w > warp) suf += s_w[w];
-  }
-  const unsigned long long above = a.level ? __ldcg(a.above + rs) : 0ull;
-  unsigned long long goal;
-  if (a.level == 0) {
-    goal = static_cast<unsigned long long>(ceil(static_cast<double>(a.top_p) * static_cast<double>(tot)));
-    // the product rounds in fp64 (tot may exceed 2^53): keep 1 <= goal <= tot
-    goal = goal < tot ? goal : tot;
-    if (goal == 0ull) goal = 1ull;
-  } else {
-    goal = __ldcg(a.goal + rs);
-  }
-  // the suffix does not grow with t, so the threads that reach the goal are
-  // 0 .. t*: their count locates t*
-  const int tstar = max(0, __syncthreads_count(above + suf >= goal) - 1);
-  if (t != tstar) return;
-  // within the thread, from its top bin down
-  unsigned long long cum = above + suf - ls;
+// Thread t* of a select: the digit among its bins (cum = the mass above its
+// top bin), then the level's outputs.
+__device__ __forceinline__ void select_write(const TopPArgs& a, size_t rs, const unsigned long long (&v)[8],
+                                             int per, unsigned long long cum, unsigned long long goal) {
+  const int t = threadIdx.x;
   int d = t * per;
   unsigned long long dmass = v[0];
   bool found = false;
@@ -396,6 +345,79 @@ __global__ void __launch_bounds__(256) topp_select_kernel(const TopPArgs a) {
   }
 }
 
+// The select of row slot rs, by every thread of the CTA (s_w: 8 words of
+// shared memory, free again when it returns).  Thread t holds bins
+// [t * per, t * per + per), per = bins / 256; a block suffix scan of the bin
+// masses (the mass at or above each thread's first bin) finds the last thread
+// whose suffix, with the mass above the level's range, reaches the goal, and
+// that thread finds the digit among its bins.  At the last level it writes the
+// threshold logit and the kept mass.
+__device__ __forceinline__ void select_slot(const TopPArgs& a, size_t rs, unsigned long long* s_w) {
+  const int nb = 1 << a.bits, per = nb >> 8;  // 1, 4 or 8
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const unsigned long long* h = a.hist + rs * nb + static_cast<size_t>(t) * per;
+  unsigned long long v[8], ls = 0ull;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    v[k] = k < per ? __ldcg(h + k) : 0ull;
+    ls += v[k];
+  }
+  // suffix sums: within the warp, then the later warps' totals
+  unsigned long long suf = ls;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long x = __shfl_down_sync(0xFFFFFFFFu, suf, o);
+    if (lane + o < 32) suf += x;
+  }
+  if (lane == 0) s_w[warp] = suf;
+  __syncthreads();
+  unsigned long long tot = 0ull;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    tot += s_w[w];
+    if (w > warp) suf += s_w[w];
+  }
+  const unsigned long long above = a.level ? __ldcg(a.above + rs) : 0ull;
+  unsigned long long goal;
+  if (a.level == 0) {
+    goal = static_cast<unsigned long long>(ceil(static_cast<double>(a.top_p) * static_cast<double>(tot)));
+    // the product rounds in fp64 (tot may exceed 2^53): keep 1 <= goal <= tot
+    goal = goal < tot ? goal : tot;
+    if (goal == 0ull) goal = 1ull;
+  } else {
+    goal = __ldcg(a.goal + rs);
+  }
+  // the suffix does not grow with t, so the threads that reach the goal are
+  // 0 .. t*: their count locates t*
+  const int tstar = max(0, __syncthreads_count(above + suf >= goal) - 1);
+  if (t == tstar) select_write(a, rs, v, per, above + suf - ls, goal);
+  __syncthreads();  // s_w is read by every thread before a later row reuses it
+}
+
+// Select of one level: one CTA per row slot fixes the next digit.
+__global__ void __launch_bounds__(256) topp_select_kernel(const TopPArgs a) {
+  __shared__ unsigned long long s_w[8];
+  griddep_launch_dependents();
+  const int W = a.gmax + 1;
+  const size_t rs = blockIdx.x;
+  const int b = static_cast<int>(rs / (2 * W)), i = static_cast<int>((rs / 2) % W), which = static_cast<int>(rs & 1);
+  float T;
+  if (!slot_active(a, b, i, which, &T)) return;  // uniform over the CTA
+  griddep_wait();  // the level's histograms are complete and visible
+  if (a.level >= 2 && __ldcg(a.bstar + rs) == kRowDone) return;  // th fixed at level 1 (uniform)
+  select_slot(a, rs, s_w);
+}
+
+// Select of level 2 of bf16 rows: one wave of CTAs over the rows level 1
+// left open.
+__global__ void __launch_bounds__(256) topp_select_open_kernel(const TopPArgs a) {
+  __shared__ unsigned long long s_w[8];
+  griddep_launch_dependents();
+  griddep_wait();  // the level's histograms and the open rows' list are complete and visible
+  const int n = static_cast<int>(__ldcg(a.todo_count));
+  for (int r = blockIdx.x; r < n; r += gridDim.x) select_slot(a, __ldcg(a.todo + r), s_w);
+}
+
 template __global__ void topp_hist_kernel<uint16_t>(const TopPArgs);
 template __global__ void topp_hist_kernel<float>(const TopPArgs);
 template __global__ void topp_refine_kernel<uint16_t>(const TopPArgs);
@@ -433,10 +455,20 @@ cudaError_t launch_topp_level(const TopPArgs& a, int esize, cudaStream_t stream)
                    : cudaLaunchKernelEx(&cfg, topp_refine_kernel<float>, a);
   }
   if (e != cudaSuccess) return e;
-  const size_t nslots = static_cast<size_t>(a.B) * (a.gmax + 1) * 2;
-  cfg.gridDim = dim3(static_cast<unsigned>(nslots), 1, 1);
   cfg.blockDim = dim3(256, 1, 1);
   cfg.dynamicSmemBytes = 0;
+  if (a.level == 2 && a.nlevels == 3 && esize == 2) {
+    // one wave over the rows level 1 left open
+    int dev = 0, sms = 0, per_sm = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topp_select_open_kernel, 256, 0);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(static_cast<unsigned>(std::max(1, sms * std::max(1, per_sm))), 1, 1);
+    return cudaLaunchKernelEx(&cfg, topp_select_open_kernel, a);
+  }
+  const size_t nslots = static_cast<size_t>(a.B) * (a.gmax + 1) * 2;
+  cfg.gridDim = dim3(static_cast<unsigned>(nslots), 1, 1);
   return cudaLaunchKernelEx(&cfg, topp_select_kernel, a);
 }
 
