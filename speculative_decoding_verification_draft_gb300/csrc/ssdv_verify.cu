@@ -68,6 +68,13 @@ struct ResidualW {
   }
 };
 
+// sqrt.approx, as the Saguaro mix pass computes the weights that Zs sums.
+__device__ __forceinline__ float sqrt_fast(float x) {
+  float y;
+  asm("sqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Residual weights when the draft tokens came from the Saguaro distribution
 // p' = sqrt(p * max(r, 1e-8)) / Zs of their position (r = (q - p)+ / S, or q
 // when S = 0): w = max(q - p', 0) in probability units.
@@ -85,7 +92,7 @@ struct SagDraftW {
       const float et = fast_exp2(fmaf(xt[e], c, -mct));
       const float ed = fast_exp2(fmaf(xd[e], c, -mcd));
       const float wa = target_only ? et : fmaxf(fmaf(-kr, ed, et), 0.f);
-      const float ps = sqrtf(ed * inv_zd * fmaxf(wa * inv_s, 1e-8f)) * inv_zs;
+      const float ps = sqrt_fast(ed * inv_zd * fmaxf(wa * inv_s, 1e-8f)) * inv_zs;
       w[e] = fmaxf(fmaf(et, inv_zt, -ps), 0.f);
     }
   }
@@ -674,7 +681,7 @@ __global__ void __launch_bounds__(kT2, 8) sample_kernel(const VerifyArgs a) {
           const float ed = fast_exp2(fmaf(tok_d[lane], cc, -scaled_max(s.dm, cc)));
           const float q = et / s.ts;
           const float r = Sw > 0.0 ? static_cast<float>(fmaxf(fmaf(-(s.ts / s.ds), ed, et), 0.f) / Sw) : q;
-          const float ps = sqrtf(ed / s.ds * fmaxf(r, 1e-8f)) / zs;
+          const float ps = sqrt_fast(ed / s.ds * fmaxf(r, 1e-8f)) / zs;
           if (ps > 0.f) ratio_acc = fminf(1.f, q / ps);
           if (!(zs > 0.f)) sag_bad = 1;  // no Saguaro weight: nothing to verify against
         }
