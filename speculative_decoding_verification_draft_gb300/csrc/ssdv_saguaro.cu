@@ -208,7 +208,10 @@ __device__ __forceinline__ bool unit_pieces(const SagArgs& a, size_t u, int wi, 
     }
     s = warp_sum(s);
     if (lane == 0) psum[u * NP + p0 + j] = s;
-    if constexpr (kTop) {
+    // tau after the first piece, then after every fourth: an older tau is
+    // still a lower bound on the warp's k-th key, so it only lets a few more
+    // elements be pushed
+    if (kTop && (j == 0 || (j & 3) == 3)) {
       float x = tk.v[0];
       for (int r = 0; r < a.k; ++r) {
         float m = x;
