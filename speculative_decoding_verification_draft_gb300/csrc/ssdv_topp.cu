@@ -188,8 +188,13 @@ struct DigitMasses {
       base16 = lo16;
     }
   }
+  // Whether x can lie in b*: not -inf (no mass) and inside b*'s logit interval.
+  __device__ __forceinline__ bool candidate(float x) const { return x != -INFINITY && x >= xlo && x <= xhi; }
   __device__ __forceinline__ void operator()(float x) const {
-    if (x == -INFINITY || x < xlo || x > xhi) return;  // no mass, or certainly another bin
+    if (candidate(x)) process(x);
+  }
+  // A candidate: the exact bin test, then its mass into its digit's bin.
+  __device__ __forceinline__ void process(float x) const {
     const float d = __fmaf_rn(-x, cc, mc);
     const int bin = min(255, max(0, __float2int_rd(d * 8.f)));
     if (static_cast<uint32_t>(bin) != bstar) return;
@@ -262,7 +267,44 @@ __device__ __forceinline__ void refine_chunk(const TopPArgs& a, int c, int b, in
     }
     __device__ __forceinline__ void operator()(float x) const { g(x); }
   } late{f, rs, c};
-  for_chunk<E>(a, slot_row<E>(a, b, i, which), lo, min(a.geo.chunk, a.geo.V - lo), late);
+  const E* row = slot_row<E>(a, b, i, which);
+  const int n = min(a.geo.chunk, a.geo.V - lo);
+  constexpr int kVec = Elem<E>::kVec;
+  const int nvec = n / kVec;  // aligned rows: whole vectors
+  // bf16 rows keep the per-element test (the mask measured 0.5 % slower there)
+  if (sizeof(E) == 2 || !(a.geo.aligned && nvec <= kNVH * kHistThreads)) {
+    for_chunk<E>(a, row, lo, n, late);
+    return;
+  }
+  // fp32 rows: almost every element fails the candidate test, so the test
+  // runs branch-free over the thread's elements into a bit mask, and the few
+  // candidates are read again (from L1) and processed one by one: 397.5 to
+  // 367.5 us per fp32 top-p round at B=64, gamma 4, V=128256, top_p 0.9.
+  static_assert(kNVH * kVec <= 64, "one bit per element of a thread");
+  const uint4* rv = reinterpret_cast<const uint4*>(row + lo);
+  uint4 r[kNVH];
+#pragma unroll
+  for (int k = 0; k < kNVH; ++k) {
+    const int v = threadIdx.x + k * kHistThreads;
+    r[k] = v < nvec ? __ldg(rv + v) : Elem<E>::max_init();
+  }
+  griddep_wait();  // the records and the previous levels' digits are complete and visible
+  late.begin();
+  unsigned long long mask = 0ull;
+#pragma unroll
+  for (int k = 0; k < kNVH; ++k) {
+    float x[kVec];
+    Elem<E>::unpack(r[k], x);
+#pragma unroll
+    for (int e = 0; e < kVec; ++e)
+      if (f.candidate(x[e])) mask |= 1ull << (k * kVec + e);
+  }
+  while (mask) {
+    const int bit = __ffsll(static_cast<long long>(mask)) - 1;
+    mask &= mask - 1ull;
+    const int v = threadIdx.x + (bit / kVec) * kHistThreads;
+    f.process(Elem<E>::to_float(row[lo + v * kVec + bit % kVec]));
+  }
 }
 
 // Levels 1.. over one chunk of one row.  Grid as level 0.
