@@ -106,7 +106,7 @@ __device__ __forceinline__ void for_chunk(const TopPArgs& a, const E* row, int l
       float x[kVec];
       Elem<E>::unpack(r[k], x);
 #pragma unroll
-      for (int e = 0; e < kVec; ++e) f(x[e]);
+      for (int e = 0; e < kVec; e += 2) f.pair(x[e], x[e + 1]);
     }
   } else if (a.geo.aligned) {
     const uint4* rv = reinterpret_cast<const uint4*>(row + lo);
@@ -149,6 +149,30 @@ struct MassBins {
     const uint32_t lo20 = static_cast<uint32_t>(mass) & 0xFFFFFu, hi20 = static_cast<uint32_t>(mass >> 20);
     if (lo20) atomicAdd(&hist[digit], lo20);
     if (hi20) atomicAdd(&hist[256 + digit], hi20);
+  }
+  // Two elements at once: the same roundings element by element, with the
+  // floating-point steps as f32x2 pairs (the multiplications are exact
+  // power-of-two scalings).  A -inf element gets d = +inf, the last bin and
+  // mass 0, so it adds nothing.
+  __device__ __forceinline__ void pair(float x0, float x1) const {
+    float d0, d1, s0, s1;
+    f2_split(f2_fma(f2_make(x0, x1), f2_make(-cc, -cc), f2_make(mc, mc)), d0, d1);  // fl(m c) - x c
+    f2_split(f2_fma(f2_make(d0, d1), f2_make(8.f, 8.f), f2_make(0.f, 0.f)), s0, s1);
+    const int g0 = 255 - min(255, max(0, __float2int_rd(s0)));
+    const int g1 = 255 - min(255, max(0, __float2int_rd(s1)));
+    float f0, f1, r0, r1, t0, t1;
+    f2_split(f2_fma(f2_make(fast_exp2(-d0), fast_exp2(-d1)), f2_make(256.f, 256.f), f2_make(0.f, 0.f)), f0, f1);
+    const uint32_t h0 = __float2uint_rz(f0), h1 = __float2uint_rz(f1);
+    f2_split(f2_add(f2_make(f0, f1), f2_make(-__uint2float_rz(h0), -__uint2float_rz(h1))), r0, r1);  // exact
+    f2_split(f2_fma(f2_make(r0, r1), f2_make(4294967296.f, 4294967296.f), f2_make(0.f, 0.f)), t0, t1);
+    const unsigned long long m0 = (static_cast<unsigned long long>(h0) << 32) + __float2uint_rn(t0);
+    const unsigned long long m1 = (static_cast<unsigned long long>(h1) << 32) + __float2uint_rn(t1);
+    const uint32_t lo0 = static_cast<uint32_t>(m0) & 0xFFFFFu, hi0 = static_cast<uint32_t>(m0 >> 20);
+    const uint32_t lo1 = static_cast<uint32_t>(m1) & 0xFFFFFu, hi1 = static_cast<uint32_t>(m1 >> 20);
+    if (lo0) atomicAdd(&hist[g0], lo0);
+    if (hi0) atomicAdd(&hist[256 + g0], hi0);
+    if (lo1) atomicAdd(&hist[g1], lo1);
+    if (hi1) atomicAdd(&hist[256 + g1], hi1);
   }
 };
 
@@ -193,6 +217,10 @@ struct DigitMasses {
   __device__ __forceinline__ void operator()(float x) const {
     if (candidate(x)) process(x);
   }
+  __device__ __forceinline__ void pair(float x0, float x1) const {
+    (*this)(x0);
+    (*this)(x1);
+  }
   // A candidate: the exact bin test, then its mass into its digit's bin.
   __device__ __forceinline__ void process(float x) const {
     const float d = __fmaf_rn(-x, cc, mc);
@@ -213,7 +241,7 @@ struct DigitMasses {
 // request).  Each warp bins into its own copy; the copies are summed into the
 // row's global histogram at the end.
 template <typename E>
-__global__ void __launch_bounds__(kHistThreads) topp_hist_kernel(const TopPArgs a) {
+__global__ void __launch_bounds__(kHistThreads, 5) topp_hist_kernel(const TopPArgs a) {
   extern __shared__ __align__(16) uint32_t s_hist[];  // [warps][2][256]
   griddep_launch_dependents();
   const int c = blockIdx.x, i = blockIdx.y >> 1, which = blockIdx.y & 1, b = blockIdx.z;
@@ -266,6 +294,7 @@ __device__ __forceinline__ void refine_chunk(const TopPArgs& a, int c, int b, in
         g.a->prefix[rs] = g.direct ? (kDirectFlag | g.base16) : 0u;
     }
     __device__ __forceinline__ void operator()(float x) const { g(x); }
+    __device__ __forceinline__ void pair(float x0, float x1) const { g.pair(x0, x1); }
   } late{f, rs, c};
   const E* row = slot_row<E>(a, b, i, which);
   const int n = min(a.geo.chunk, a.geo.V - lo);
