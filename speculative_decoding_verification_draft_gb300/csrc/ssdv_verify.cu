@@ -22,8 +22,9 @@
 //     reads the draft tokens, their two logits and the uniforms (inputs).
 //     Every CTA combines the request's records, takes every accept decision
 //     and finds the first rejection n; then each warp loads its pieces of row
-//     n (L2-resident: the streaming kernel reads the low positions last) --
-//     target and draft for a residual draw, target for the bonus draw -- and
+//     n (partly from L2: in plain calls the streaming kernel reads the low
+//     positions last) -- target and draft for a residual draw, target for the
+//     bonus draw -- and
 //     publishes their weight sums.  The last warp to arrive sums the pieces in
 //     order, finds the piece holding u * S, reloads that piece and scans it.
 //
@@ -35,7 +36,9 @@
 // own wait, so a later segment's streaming kernel launches after the first
 // segment's CTAs saw the call's inputs complete, and may stream while the
 // previous segment's sampling kernel runs: the segments use disjoint
-// workspace rows.  A call never overlaps the work of the previous call.
+// workspace rows.  A plain call never overlaps the work of the previous call;
+// a pipelined call's streaming kernel runs beside the previous call's sampling
+// kernel (only its first CTA waits), on the other workspace half.
 #include <type_traits>
 
 #include "ssdv_device.cuh"
