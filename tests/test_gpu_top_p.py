@@ -78,6 +78,16 @@ def test_config3_workload_all_requests(ssdv):
     gc.assert_verify_parity(out, n, ref, 128256, what="top-p, B=64 g=4 V=128256, all requests")
 
 
+def test_open_rows_at_full_size(ssdv):
+    """top_p 0.5 at the bench shape leaves about 30 % of the bf16 rows open
+    after level 1, so level 2's one-wave kernels walk several (row, chunk)
+    items per CTA: every request against the oracle."""
+    batch = wl.zipf_batch(64, 4, 128256, dtype=torch.bfloat16, temperature=0.8, seed=3, sigma_range=(0.3, 1.2))
+    out, n = run(ssdv, batch, 0.8, 0.5, 11)
+    ref = gc.verify_oracle(batch, 11, top_p=0.5)
+    gc.assert_verify_parity(out, n, ref, 128256, what="top-p 0.5, B=64 g=4 V=128256, all requests")
+
+
 def test_top_p_one_and_greedy_are_plain_verification(ssdv):
     """top_p = 1 keeps every token, and greedy rows ignore top_p: both give
     ssd_verify's outputs exactly."""
