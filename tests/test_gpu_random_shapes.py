@@ -5,8 +5,8 @@ vocabularies from 2 to 200000 (bf16 rows of odd length take the
 shared-memory form), temperatures including greedy, and one of plain
 verification (with the pipelined call, which must give the same outputs),
 ragged verification (plain and pipelined), top-p, Saguaro pre-speculation
-(either top-k source) and the fused call (which must equal the separate
-calls).  Each case is held to the parity rule of the other GPU tests."""
+(either top-k source), the fused call (which must equal the separate calls)
+and verification of draft tokens drawn from the Saguaro distribution.  Each case is held to the parity rule of the other GPU tests."""
 import random
 
 import pytest
@@ -34,7 +34,7 @@ def _cases():
         g = rng.choice([0, 1, 2, 3, 4, 5, 6, 8, 12, 16, 31])
         B = rng.randint(1, max(1, min(96, BUDGET // ((g + 1) * V))))
         T = rng.choice([0.0, 0.6, 0.8, 1.0, 1.3])
-        kind = rng.choice(["verify", "ragged", "top_p", "saguaro", "fused"])
+        kind = rng.choice(["verify", "ragged", "top_p", "saguaro", "fused", "saguaro_draft"])
         extra = dict(top_p=rng.choice([0.3, 0.5, 0.7, 0.9, 0.95, 0.99]), k=rng.randint(1, 8),
                      source=rng.choice(["residual", "draft"]))
         out.append((kind, dt, B, g, V, T, rng.randint(0, 10**9), extra))
@@ -74,6 +74,13 @@ def test_random_shape(ssdv, case):
         torch.cuda.synchronize()
         assert torch.equal(o1, o2) and torch.equal(n1, n2), f"{what}: pipelined ragged call differs"
         gc.assert_verify_parity(o1, n1, gc.verify_oracle(b, seed), V, what)
+    elif kind == "saguaro_draft":
+        Ts = T if T > 0 else 0.8
+        b = wl.zipf_batch(B, g, V, dtype=dt, temperature=Ts, seed=data_seed, sigma_range=(0.3, 1.2))
+        db = b.to("cuda")
+        o1, n1 = ssdv.verify_saguaro_draft(db.target, db.draft, db.draft_tokens, Ts, seed)
+        torch.cuda.synchronize()
+        gc.assert_verify_parity(o1, n1, gc.verify_oracle(b, seed, draft_dist="saguaro"), V, what)
     elif kind == "top_p":
         Tt = T if T > 0 else 0.8
         b = wl.zipf_batch(B, g, V, dtype=dt, temperature=Tt, seed=data_seed, sigma_range=(0.3, 1.2))
