@@ -39,6 +39,23 @@
  *    gamma above gamma_max, a bad per-request temperature) make that request's
  *    outputs -1 and set a bit in the workspace status word (see
  *    ssd_read_status); the other requests are unaffected.
+ *
+ * Tuning overrides (environment variables, read on every call; none changes
+ * the outputs, only how the work is split)
+ * ---------------------------------------------------------------------------
+ *  - SSDV_CHUNK_BYTES: bytes of a row per streaming CTA (default 24576; a
+ *    chunk holds at most 16384 elements and a row at most 32 chunks).
+ *  - SSDV_PPW: pieces (128 vectors) of the draw row per warp of the
+ *    verification sampling kernel (default 2 for plain calls, 1 when that
+ *    grid fits one wave, 4 for pipelined calls).
+ *  - SSDV_SEGMENT: requests per launch segment of verification (default and
+ *    maximum 65535, the grid's third dimension).
+ *  - SSDV_SMALL_V: 0 turns off the one-warp-per-request kernel that
+ *    vocabularies up to 256 take (default 1).
+ *  - SSDV_SAG_PPW: pieces per warp of the Saguaro residual and mix kernels
+ *    (default 16, at least 2).
+ *  - SSDV_SAG_SEGMENT: requests per launch segment of the Saguaro calls
+ *    (default and maximum 65535).
  */
 #ifndef SSDV_H
 #define SSDV_H
