@@ -40,8 +40,11 @@
  *    outputs -1 and set a bit in the workspace status word (see
  *    ssd_read_status); the other requests are unaffected.
  *
- * Tuning overrides (environment variables, read on every call; none changes
- * the outputs, only how the work is split)
+ * Tuning overrides (environment variables, read on every call).  They split
+ * the work differently.  SSDV_PPW, SSDV_SEGMENT, SSDV_SAG_PPW and
+ * SSDV_SAG_SEGMENT leave every sum in the same order and the outputs
+ * unchanged; SSDV_CHUNK_BYTES and SSDV_SMALL_V change the order of the row
+ * sums, so a draw within rounding of a threshold may come out the other way.
  * ---------------------------------------------------------------------------
  *  - SSDV_CHUNK_BYTES: bytes of a row per streaming CTA (default 24576; a
  *    chunk holds at most 16384 elements and a row at most 32 chunks).
