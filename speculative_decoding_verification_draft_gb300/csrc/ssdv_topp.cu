@@ -129,11 +129,14 @@ __device__ __forceinline__ const E* slot_row(const TopPArgs& a, int b, int i, in
 }
 
 // Level 0's counter: every element's mass into the warp's own copy of the
-// 256 mass bins, as two 32-bit words a bin: the low 20 bits of the 2^-40
-// fixed-point mass, and the bits above them.  A mass is at most 2^40 (e <= 1),
-// so each word takes less than 2^20 per element, and a warp sees at most
-// 2048 elements of a chunk (chunks hold at most 16384): neither word can
-// overflow, and no atomic needs its old value.
+// 256 mass bins, as two 32-bit words a bin.  The 2^-40 fixed-point mass
+// round(e 2^40) is split as hi 2^20 + lo with hi = floor(e 2^20) and
+// lo = round((e 2^20 - hi) 2^20), both straight from 32-bit conversions (e
+// 2^20 and its fraction are exact in fp32, so only the last step rounds, as
+// round(e 2^40) does).  Each word takes at most 2^20 per element (e <= 1),
+// and a warp sees at most 2048 elements of a chunk (chunks hold at most
+// 16384): neither word can overflow, and no atomic needs its old value.  The
+// bin's mass is (sum of hi) 2^20 + (sum of lo).
 struct MassBins {
   const TopPArgs* a;
   int b, i, which;
@@ -145,8 +148,9 @@ struct MassBins {
     const float d = __fmaf_rn(-x, cc, mc);  // fl(m c) - x c, one rounding
     const int bin = min(255, max(0, __float2int_rd(d * 8.f)));
     const int digit = 255 - bin;  // larger digit, larger mass
-    const unsigned long long mass = mass_fixed(fast_exp2(-d));
-    const uint32_t lo20 = static_cast<uint32_t>(mass) & 0xFFFFFu, hi20 = static_cast<uint32_t>(mass >> 20);
+    const float f = fast_exp2(-d) * 1048576.f;  // e 2^20, exact
+    const uint32_t hi20 = __float2uint_rz(f);
+    const uint32_t lo20 = __float2uint_rn((f - __uint2float_rz(hi20)) * 1048576.f);  // only the conversion rounds
     if (lo20) atomicAdd(&hist[digit], lo20);
     if (hi20) atomicAdd(&hist[256 + digit], hi20);
   }
@@ -161,14 +165,12 @@ struct MassBins {
     const int g0 = 255 - min(255, max(0, __float2int_rd(s0)));
     const int g1 = 255 - min(255, max(0, __float2int_rd(s1)));
     float f0, f1, r0, r1, t0, t1;
-    f2_split(f2_fma(f2_make(fast_exp2(-d0), fast_exp2(-d1)), f2_make(256.f, 256.f), f2_make(0.f, 0.f)), f0, f1);
-    const uint32_t h0 = __float2uint_rz(f0), h1 = __float2uint_rz(f1);
-    f2_split(f2_add(f2_make(f0, f1), f2_make(-__uint2float_rz(h0), -__uint2float_rz(h1))), r0, r1);  // exact
-    f2_split(f2_fma(f2_make(r0, r1), f2_make(4294967296.f, 4294967296.f), f2_make(0.f, 0.f)), t0, t1);
-    const unsigned long long m0 = (static_cast<unsigned long long>(h0) << 32) + __float2uint_rn(t0);
-    const unsigned long long m1 = (static_cast<unsigned long long>(h1) << 32) + __float2uint_rn(t1);
-    const uint32_t lo0 = static_cast<uint32_t>(m0) & 0xFFFFFu, hi0 = static_cast<uint32_t>(m0 >> 20);
-    const uint32_t lo1 = static_cast<uint32_t>(m1) & 0xFFFFFu, hi1 = static_cast<uint32_t>(m1 >> 20);
+    f2_split(f2_fma(f2_make(fast_exp2(-d0), fast_exp2(-d1)), f2_make(1048576.f, 1048576.f), f2_make(0.f, 0.f)), f0,
+             f1);  // e 2^20
+    const uint32_t hi0 = __float2uint_rz(f0), hi1 = __float2uint_rz(f1);
+    f2_split(f2_add(f2_make(f0, f1), f2_make(-__uint2float_rz(hi0), -__uint2float_rz(hi1))), r0, r1);  // exact
+    f2_split(f2_fma(f2_make(r0, r1), f2_make(1048576.f, 1048576.f), f2_make(0.f, 0.f)), t0, t1);
+    const uint32_t lo0 = __float2uint_rn(t0), lo1 = __float2uint_rn(t1);
     if (lo0) atomicAdd(&hist[g0], lo0);
     if (hi0) atomicAdd(&hist[256 + g0], hi0);
     if (lo1) atomicAdd(&hist[g1], lo1);
